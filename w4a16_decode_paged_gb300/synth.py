@@ -1,0 +1,120 @@
+"""Seeded synthetic inputs for the decode path (shared by tests, bench and smoke).
+
+This module only draws random numbers in the shapes and distributions of the
+workloads; it holds none of the method's arithmetic (no unpacking, no
+dequantisation, no norms, no attention).  Both the CUDA path and the CPU
+oracle receive the arrays it returns.
+
+Distributions (the pages give none; these follow the workload descriptions):
+  * packed int4 weights: uniform random uint32 words (every nibble, hence
+    every code in [-8, 7], equally likely), layout [N][K/8];
+  * group scales: fp16, uniform in [0.005, 0.02], layout [N][K/128];
+  * activations, embeddings, KV pages: fp16 N(0, 1);
+  * RMSNorm gammas: fp16 1 + 0.1 N(0, 1);
+  * q/k/v biases: fp16 N(0, 0.1) (omitted for the tiny layer);
+  * lm_head: fp16 N(0, 0.02);
+  * block tables: distinct pages drawn at random from the pool, entries past
+    a sequence's last page set to -1 (never read).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+PAGE = 16
+GROUP = 128
+
+# Workload shapes.  Names say what they are.
+TINY_LAYER = dict(name="tiny-layer-h896-ctx37", hidden=896, n_q_heads=7, n_kv_heads=1, head_dim=128,
+                  inter=2432, n_layers=1, vocab=0, eps=1e-6, theta=1e6, batch=1, context=37,
+                  pool_pages=8, bias=False, seed=1000)
+QWEN_LAYER = dict(name="qwen2.5-7b-layer-b1-ctx512", hidden=3584, n_q_heads=28, n_kv_heads=4,
+                  head_dim=128, inter=18944, n_layers=1, vocab=0, eps=1e-6, theta=1e6, batch=1,
+                  context=512, pool_pages=4096, bias=True, seed=1001)
+QWEN_MODEL = dict(name="qwen2.5-7b-28L-b1-ctx512", hidden=3584, n_q_heads=28, n_kv_heads=4,
+                  head_dim=128, inter=18944, n_layers=28, vocab=152064, eps=1e-6, theta=1e6, batch=1,
+                  context=512, gen_tokens=128, bias=True, seed=1002)
+QWEN_BATCHED = dict(name="qwen2.5-7b-28L-b32-ctxU1..4096", hidden=3584, n_q_heads=28, n_kv_heads=4,
+                    head_dim=128, inter=18944, n_layers=28, vocab=152064, eps=1e-6, theta=1e6, batch=32,
+                    max_context=4096, forced_lens=(15, 16, 17), pool_pages=16384, bias=True, seed=1003)
+QWEN_LONG = dict(name="qwen2.5-7b-layer-b4-ctx32768", hidden=3584, n_q_heads=28, n_kv_heads=4,
+                 head_dim=128, inter=18944, n_layers=1, vocab=0, eps=1e-6, theta=1e6, batch=4,
+                 context=32768, pool_pages=16384, partition_tokens=512, bias=True, seed=1004)
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def int4_weight(r: np.random.Generator, N: int, K: int):
+    """(qweight uint32 [N][K/8], scales fp16 [N][K/128])."""
+    assert K % GROUP == 0
+    qw = r.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    s = r.uniform(0.005, 0.02, size=(N, K // GROUP)).astype(np.float16)
+    return qw, s
+
+
+def normal_fp16(r: np.random.Generator, shape, std: float = 1.0, mean: float = 0.0):
+    return (r.standard_normal(shape, dtype=np.float32) * np.float32(std) + np.float32(mean)).astype(np.float16)
+
+
+def gamma(r: np.random.Generator, H: int):
+    return normal_fp16(r, (H,), std=0.1, mean=1.0)
+
+
+def layer_weights(r: np.random.Generator, cfg: dict) -> dict:
+    H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
+    w = {"ln1": gamma(r, H), "ln2": gamma(r, H)}
+    for name, N, K in (("q", Hq * D, H), ("k", Hkv * D, H), ("v", Hkv * D, H), ("o", H, Hq * D),
+                       ("g", I, H), ("u", I, H), ("d", H, I)):
+        w["w" + name], w["s" + name] = int4_weight(r, N, K)
+    if cfg.get("bias", False):
+        w["bq"] = normal_fp16(r, (Hq * D,), 0.1)
+        w["bk"] = normal_fp16(r, (Hkv * D,), 0.1)
+        w["bv"] = normal_fp16(r, (Hkv * D,), 0.1)
+    else:
+        w["bq"] = w["bk"] = w["bv"] = None
+    return w
+
+
+def kv_pool(r: np.random.Generator, pages: int, Hkv: int, D: int):
+    """fp16 N(0,1) pool, layout [pages][Hkv][16][D]."""
+    return normal_fp16(r, (pages, Hkv, PAGE, D))
+
+
+def block_table(r: np.random.Generator, lens, pool_pages: int, max_blocks: int | None = None):
+    """Disjoint random pages for each sequence; -1 past each sequence's need."""
+    lens = [int(x) for x in lens]
+    need = [(L + PAGE - 1) // PAGE for L in lens]
+    if max_blocks is None:
+        max_blocks = max(1, max(need))
+    assert sum(need) <= pool_pages
+    perm = r.permutation(pool_pages).astype(np.int32)
+    bt = np.full((len(lens), max_blocks), -1, np.int32)
+    o = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    return bt
+
+
+def batched_lens(r: np.random.Generator, B: int, max_context: int, forced=(15, 16, 17)):
+    lens = r.integers(1, max_context + 1, size=B).astype(np.int32)
+    for i, L in enumerate(forced):
+        lens[i] = L
+    return lens
+
+
+def layer_case(cfg: dict, lens=None, seed: int | None = None) -> dict:
+    """One decoder layer's weights, input, pools and paging state."""
+    r = rng(cfg["seed"] if seed is None else seed)
+    B = cfg["batch"]
+    w = layer_weights(r, cfg)
+    x = normal_fp16(r, (B, cfg["hidden"]))
+    if lens is None:
+        lens = np.full(B, cfg["context"], np.int32)
+    lens = np.asarray(lens, np.int32)
+    pool_pages = cfg["pool_pages"]
+    k_pool = kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"])
+    v_pool = kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"])
+    bt = block_table(r, lens, pool_pages)
+    return dict(weights=w, x=x, k_pool=k_pool, v_pool=v_pool, block_table=bt, context_lens=lens)
