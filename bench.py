@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Decode benchmark: Qwen2.5-7B-shaped W4A16 model, batch 1, context 512.
+
+One step = one greedy decode token through the whole path (embedding, 28
+decoder layers of RMSNorm / q|k|v W4A16 GEMV / RoPE + paged KV append / paged
+GQA attention with split-K combine / o GEMV / gate|up GEMV + SiLU-mul / down
+GEMV, final RMSNorm, fp16 lm_head, argmax), replayed from a CUDA graph.
+Inputs are seeded synthetic random-init weights of the model's shapes, with
+the prompt's 512 tokens of KV already in the paged cache.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (bounded sample, same metric and unit).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Qwen2.5-7B-shape W4A16 decode tok/s @b=1,ctx512; kernel HBM GB/s vs peak"
+UNIT = "tok/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--layers", type=int, default=28, help="decoder layers (28 = the workload)")
+    ap.add_argument("--context", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-timing", action="store_true")
+    ap.add_argument("--seed", type=int, default=1002)
+    return ap.parse_args()
+
+
+def model_cfg(layers):
+    from w4a16_decode_paged_gb300 import synth
+    return dict(synth.QWEN_MODEL, n_layers=layers)
+
+
+def make_inputs(cfg, seed, max_ctx, pool_pages=256):
+    """numpy weights, pools and paging state for the whole model."""
+    from w4a16_decode_paged_gb300 import synth
+    r = synth.rng(seed)
+    layers = [synth.layer_weights(r, cfg) for _ in range(cfg["n_layers"])]
+    kps = [synth.kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"]) for _ in range(cfg["n_layers"])]
+    vps = [synth.kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"]) for _ in range(cfg["n_layers"])]
+    embed = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]))
+    fnorm = synth.gamma(r, cfg["hidden"])
+    lm = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]), std=0.02)
+    bt = synth.block_table(r, [max_ctx], pool_pages)
+    tok = r.integers(0, cfg["vocab"], size=1).astype(np.int32)
+    return dict(layers=layers, kps=kps, vps=vps, embed=embed, fnorm=fnorm, lm=lm, bt=bt, tok=tok,
+                pool_pages=pool_pages)
+
+
+# ---------------------------------------------------------------------------- bytes (roofline)
+
+def gemv_bytes(N, K, M=1, bias=False, residual=False):
+    b = N * K // 2 + N * (K // 128) * 2 + M * K * 2 + M * N * 2
+    if bias:
+        b += N * 2
+    if residual:
+        b += M * N * 2
+    return b
+
+
+def layer_bytes(cfg, ctx):
+    H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
+    nqkv = (Hq + 2 * Hkv) * D
+    g = gemv_bytes(nqkv, H, bias=True) + gemv_bytes(H, Hq * D, residual=True) + \
+        (gemv_bytes(2 * I, H) - 2 * I * 2 + I * 2) + gemv_bytes(H, I, residual=True)
+    att = 2 * Hkv * ctx * D * 2 + 4 * math.ceil(ctx / 16) + 2 * Hq * D * 2
+    return g, att
+
+
+def step_bytes(cfg, ctx):
+    g, att = layer_bytes(cfg, ctx)
+    lm = cfg["vocab"] * cfg["hidden"] * 2
+    return cfg["n_layers"] * (g + att) + lm + cfg["hidden"] * 2
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.gpu_id is not None:
+                cmd += ["-i", str(self.gpu_id)]
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            v = d.get("hbm_gbs")
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v:
+                return float(v), "measured (MEASURED_PEAKS.json hbm_gbs)"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json on this box)"
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None when that summary was taken on different kernel source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(kernel)
+        if not d:
+            return None
+        src = os.path.join(ROOT, d["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return d["dram_bytes_per_launch"] if h == d["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_token_time(cfg, inp, ctx, budget_s=15.0):
+    """Seconds the CPU oracle needs for one decode token, from a bounded
+    sample: as many whole layers as fit in ~budget_s (>= 1), scaled to the
+    model's layer count, plus the full fp16 lm_head + argmax."""
+    import oracle as orc
+    orc.build()
+    nthreads = orc.num_threads()
+    bt = inp["bt"][:, :]
+    lens = np.array([ctx + 1], np.int32)
+    x = inp["embed"][inp["tok"][0]][None, :].copy()
+    t_layers, n_done = 0.0, 0
+    for l in range(cfg["n_layers"]):
+        kp, vp = inp["kps"][l].copy(), inp["vps"][l].copy()
+        t0 = time.perf_counter()
+        x = orc.decoder_layer(cfg, inp["layers"][l], x, kp, vp, bt, lens)
+        t_layers += time.perf_counter() - t0
+        n_done += 1
+        if t_layers > budget_s * 0.7:
+            break
+    t0 = time.perf_counter()
+    xn = orc.rmsnorm(x, inp["fnorm"], cfg["eps"])
+    logits = orc.fp16_gemv(xn[0], inp["lm"])
+    orc.argmax(logits)
+    t_lm = time.perf_counter() - t0
+    per_token = t_layers / n_done * cfg["n_layers"] + t_lm
+    sample = (f"{n_done} of {cfg['n_layers']} decoder layers timed (x{cfg['n_layers'] / n_done:.2f}) "
+              f"+ full lm_head GEMV and argmax, b=1, context {ctx + 1}")
+    return per_token, nthreads, sample, t_layers + t_lm
+
+
+def run_reference(args):
+    """CPU oracle arm: each step is one decoder layer (cycling over the 28)
+    plus 1/28 of the lm_head rows, i.e. 1/28 of a token's work."""
+    import oracle as orc
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    orc.build()
+    cfg = model_cfg(args.layers)
+    inp = make_inputs(cfg, args.seed, args.context + 16)
+    L = cfg["n_layers"]
+    lens = np.array([args.context + 1], np.int32)
+    x = inp["embed"][inp["tok"][0]][None, :].copy()
+    rows = math.ceil(cfg["vocab"] / L)
+
+    def one(i):
+        nonlocal x
+        l = i % L
+        kp, vp = inp["kps"][l].copy(), inp["vps"][l].copy()
+        x = orc.decoder_layer(cfg, inp["layers"][l], x, kp, vp, inp["bt"], lens)
+        lo = (i % L) * rows
+        orc.fp16_gemv(orc.rmsnorm(x, inp["fnorm"], cfg["eps"])[0], inp["lm"][lo:lo + rows])
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    tokens = args.steps / L
+    value = tokens / dt
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded random-init weights, N(0,1) KV)",
+           "config": {"workload": f"qwen2.5-7b-{L}L-b1-ctx{args.context} greedy decode", "batch": 1,
+                      "context": args.context, "layers": L},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                            "sample": f"each step = 1 of {L} decoder layers + 1/{L} of the lm_head rows "
+                                      f"(= 1/{L} token), {args.steps} steps"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+# ---------------------------------------------------------------------------- native arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from w4a16_decode_paged_gb300 import api, build
+    build.build()
+
+    cfg = model_cfg(args.layers)
+    K, W = args.steps, args.warmup
+    max_ctx = args.context + K + W + 16
+    t_gen = time.perf_counter()
+    inp = make_inputs(cfg, args.seed + rank, max_ctx)
+    t_gen = time.perf_counter() - t_gen
+
+    tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int32) if a.dtype == np.uint32 else a)).to(dev)
+    dls = [api.device_layer(w, kp, vp, device=dev) for w, kp, vp in zip(inp["layers"], inp["kps"], inp["vps"])]
+    embed, fnorm, lm = tdev(inp["embed"]), tdev(inp["fnorm"]), tdev(inp["lm"])
+    model = api.Model(cfg, dls, embed=embed, final_norm=fnorm, lm_head=lm, max_batch=1, max_context=max_ctx,
+                      num_pages=inp["pool_pages"])
+    bt = tdev(inp["bt"])
+    tok = tdev(inp["tok"])
+    lens = torch.tensor([args.context], dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    kernels_per_step = model.kernel_count(1)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        # ---- device-resident timing: K graph replays --------------------
+        lens.fill_(args.context)
+        for _ in range(W):
+            model.decode_step(tok, tok, bt, lens, use_graph=True)
+        stream.synchronize()
+        assert model.check_errors(stream) == 0
+        lens.fill_(args.context)
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_uuid(torch, dev)) as clk:
+            e0.record(stream)
+            for _ in range(K):
+                model.decode_step(tok, tok, bt, lens, use_graph=True)
+            e1.record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        assert int(lens.item()) == args.context + K
+        assert model.check_errors(stream) == 0
+
+        # ---- end to end through the C ABI with host buffers --------------
+        h_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        h_in.copy_(torch.from_numpy(inp["tok"]))
+        lens.fill_(args.context)
+        for _ in range(2):
+            tok.copy_(h_in, non_blocking=True)
+            model.decode_step(tok, tok, bt, lens, use_graph=True)
+            h_out.copy_(tok, non_blocking=True)
+            stream.synchronize()
+        lens.fill_(args.context)
+        stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            tok.copy_(h_in, non_blocking=True)
+            model.decode_step(tok, tok, bt, lens, use_graph=True)
+            h_out.copy_(tok, non_blocking=True)
+            stream.synchronize()
+            h_in.copy_(h_out)
+        e2e_s = time.perf_counter() - t0
+        barrier()
+
+        # ---- dominant kernel: gate|up W4A16 GEMV + SiLU-mul, live ---------
+        kern = None
+        if not args.no_kernel_timing:
+            kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream)
+
+    # max over ranks
+    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_s = float(t[0]), float(t[1])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = measured_peak()
+    value = world * K / (ms / 1e3)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+           "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "int4 weights x fp16 activations, fp32 accumulate",
+           "data": "synthetic (seeded random-init weights of the model's shapes; N(0,1) KV prefill)",
+           "config": {"workload": f"qwen2.5-7b-{cfg['n_layers']}L-b1-ctx{args.context} greedy decode (CUDA graph)",
+                      "batch": 1, "context": args.context, "layers": cfg["n_layers"],
+                      "l2": f"inputs larger than L2: {step_bytes(cfg, args.context) / 1e9:.2f} GB read per step",
+                      "parallelism": f"replicas x{world}"},
+           "gpu_launches": kernels_per_step * K,
+           "e2e": {"value": world * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+           "clocks": clk.summary()}
+    sb = step_bytes(cfg, args.context + K // 2)
+    out["step_roofline"] = {"bytes_per_step": sb, "achieved_gbs": sb / (ms / K / 1e3) / 1e9, "peak_gbs": peak,
+                            "frac": sb / (ms / K / 1e3) / 1e9 / peak, "roofline_ms": sb / (peak * 1e9) * 1e3}
+    if kern is not None:
+        out["roofline"] = {"bound": "hbm", "kernel": "w4a16_gemv_silu_mul (gate|up, 3584->2x18944)",
+                           "achieved": kern["gateup"]["gbs"], "peak": peak, "unit": "GB/s",
+                           "frac": kern["gateup"]["gbs"] / peak, "peak_source": peak_src,
+                           "traffic": traffic_record("gemv_gateup")}
+        out["kernels"] = kern
+    if not args.no_cpu_baseline:
+        per_tok, cores, sample, spent = oracle_token_time(cfg, inp, args.context)
+        out["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": sample, "seconds_spent": round(spent, 2)}
+    out["setup_s"] = {"generate_inputs": round(t_gen, 1)}
+    print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_gemv_kernels(torch, api, cfg, dls, dev, stream, reps=3):
+    """Average device time per launch of each GEMV kind as used in the step,
+    over all layers' weights (rotating, so nothing stays in L2), captured
+    in a CUDA graph and timed with CUDA events on the launching stream."""
+    H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
+    x = torch.randn((1, H), device=dev).half()
+    xi = torch.randn((1, I), device=dev).half()
+    xa = torch.randn((1, Hq * D), device=dev).half()
+    y_i = torch.empty((1, I), dtype=torch.float16, device=dev)
+    y_h = torch.empty((1, H), dtype=torch.float16, device=dev)
+    y_q = torch.empty((1, Hq * D), dtype=torch.float16, device=dev)
+    kinds = {
+        "gateup": (lambda w: api.w4a16_gemv_silu_mul(x, w["ln2"], 1e-6, w["wg"], w["sg"], w["wu"], w["su"], out=y_i),
+                   gemv_bytes(2 * I, H) - 2 * I * 2 + I * 2),
+        "down": (lambda w: api.w4a16_gemv(xi, w["wd"], w["sd"], residual=x, out=y_h), gemv_bytes(H, I, residual=True)),
+        "q": (lambda w: api.w4a16_gemv_rmsnorm(x, w["ln1"], 1e-6, w["wq"], w["sq"], bias=w["bq"], out=y_q),
+              gemv_bytes(Hq * D, H, bias=True)),
+        "o": (lambda w: api.w4a16_gemv(xa, w["wo"], w["so"], residual=x, out=y_h),
+              gemv_bytes(H, Hq * D, residual=True)),
+    }
+    res = {}
+    for name, (fn, nbytes) in kinds.items():
+        for w in dls[:2]:
+            fn(w)  # eager warm-up outside capture
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for w in dls:
+                fn(w)
+        g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        per = e0.elapsed_time(e1) / (reps * len(dls)) / 1e3
+        res[name] = {"us_per_launch": per * 1e6, "bytes_per_launch": nbytes, "gbs": nbytes / per / 1e9,
+                     "launches_timed": reps * len(dls)}
+        del g
+    return res
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,291 @@
+/*
+ * w4a16.h -- C ABI of the sm_103a W4A16 + paged-GQA single-token decode library.
+ *
+ * The operations follow the "annotated-llm-runtime" decode path as described on
+ *   [RU] aikraft.ru, "How to build your own LLM runtime from scratch",
+ *        section "Архитектурные решения и оптимизации" (28 layers, hidden 3584,
+ *        28 heads with 7:1 GQA, symmetric group-wise INT4 weights with group 128,
+ *        RMSNorm and lm_head in FP16, 16-token KV pages whose per-head slice is
+ *        4 KiB), and
+ *   [EN] explore.n1n.ai, "Building a Custom LLM Inference Runtime on H100",
+ *        sections "2. The KV Cache and PagedAttention", "3. CUDA Graph Capture",
+ *        "Bug 1: The KV Cache Indexing 'Off-By-One'", "Bug 2: Tensor Core
+ *        Alignment", "Bug 3: CUDA Graph Stream Synchronization" and
+ *        "Implementation Guide: Step-by-Step" (static pre-allocation).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - fp16 tensors are passed as `uint16_t*` holding IEEE binary16 bit patterns.
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, and must be
+ *    128-byte aligned ([EN] "Bug 2": the runtime enforces 128-byte alignment);
+ *    a misaligned pointer returns W4A16_ERR_ALIGNMENT.  Row pitches of the
+ *    packed tensors follow from the shapes (no padding).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work: none allocates, synchronises or copies through the host, so
+ *    all of them may be recorded into a CUDA graph ([EN] "Bug 3").
+ *  - Return value: W4A16_OK or an error code; w4a16_last_error() gives the
+ *    message of the last failure on the calling thread.  Shape and pointer
+ *    checks happen on the host before anything is enqueued.  Conditions only
+ *    the device can see (a block-table entry outside the pool, a token id
+ *    outside the vocabulary) are reported through an optional device
+ *    `err_flag` word: the offending access is skipped, bit 0 of *err_flag is
+ *    set, and nothing traps.
+ *
+ * Storage formats
+ * ---------------
+ *  - Packed INT4 weight of an [N][K] matrix: uint32 qweight[N][K/8]; element k
+ *    of row n is nibble (k % 8) of word k/8, lowest nibble first, stored
+ *    offset-binary u = q + 8 so q = u - 8 is in [-8, 7].  Scales: fp16
+ *    scales[N][K/128], one per 128 consecutive k.  Dequantised weight =
+ *    q * scale (symmetric, no zero point).  K must be a multiple of 128.
+ *  - Paged KV pool (one K pool and one V pool per layer): fp16
+ *    [num_pages][Hkv][16][D]; the (page, kv head) slice is 16*D*2 bytes
+ *    (4 KiB at D = 128).  block_table is int32 [B][max_blocks]; token t of
+ *    sequence b lives in page block_table[b][t / 16], slot t % 16.  Entries
+ *    past a sequence's last page are never read.
+ *  - context_lens (int32 [B], device) counts tokens AFTER the current token is
+ *    appended: the new token sits at position context_lens[b] - 1, and
+ *    attention covers positions [0, context_lens[b]).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+typedef struct CUstream_st* w4a16_stream_t; /* same type as cudaStream_t */
+
+enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad flag */
+  W4A16_ERR_ALIGNMENT = 2,   /* a pointer is not 128-byte aligned */
+  W4A16_ERR_SHAPE = 3,       /* K % 128 != 0, D != 128, Hq % Hkv != 0, ... */
+  W4A16_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  W4A16_ERR_CAPTURE = 5,     /* call not allowed while the stream is capturing */
+  W4A16_ERR_DEVICE_BOUNDS = 6, /* device reported an out-of-range index */
+  W4A16_ERR_TIMEOUT = 7      /* a bounded device wait gave up */
+};
+
+/* Message of the last failed call on this thread ("" if none). */
+W4A16_API const char* w4a16_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+W4A16_API int w4a16_version(void);
+
+/* ------------------------------------------------------------------------
+ * w4a16_gemv -- y = x . dequant(W)^T (+ bias) (+ residual), fp32 accumulate.
+ * [RU] "Архитектурные решения и оптимизации": q/k/v/o and gate/up/down are
+ * symmetric group-wise INT4 (group 128) with FP16 activations.
+ *   x        fp16 [M][K]              input activations
+ *   qweight  uint32 [N][K/8]          packed INT4 weight (format above)
+ *   scales   fp16 [N][K/128]          group scales
+ *   bias     fp16 [N] or NULL
+ *   residual fp16 [M][N] or NULL      added before the single fp16 rounding
+ *   y        fp16 [M][N]              output (must not alias x)
+ * Shapes: 1 <= M, K % 128 == 0, N >= 1.  The CUDA-core path handles M <= 4
+ * with M*K <= 49152; larger M uses the tensor-core (tcgen05) path when built,
+ * else returns W4A16_ERR_SHAPE.
+ * ------------------------------------------------------------------------ */
+W4A16_API int w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qweight, const uint16_t* scales,
+               int N, const uint16_t* bias, const uint16_t* residual, uint16_t* y,
+               w4a16_stream_t stream);
+
+/* w4a16_gemv with the RMSNorm of x fused in front (the input norm of the
+ * q/k/v projection): y = dequant(W) . (x / sqrt(mean(x^2) + eps) * gamma)
+ * (+ bias).  The normalised x is rounded to fp16 before the product.
+ *   gamma fp16 [K]. */
+W4A16_API int w4a16_gemv_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                       const uint32_t* qweight, const uint16_t* scales, int N,
+                       const uint16_t* bias, uint16_t* y, w4a16_stream_t stream);
+
+/* Gated MLP front half: y = silu(G . xn) * (U . xn), xn = RMSNorm(x) if gamma
+ * is non-NULL else x.  G and U are packed INT4 [N][K/8] with scales
+ * [N][K/128]; y fp16 [M][N].  silu(g) = g / (1 + exp(-g)). */
+W4A16_API int w4a16_gemv_silu_mul(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K,
+                        const uint32_t* qweight_gate, const uint16_t* scales_gate,
+                        const uint32_t* qweight_up, const uint16_t* scales_up, int N, uint16_t* y,
+                        w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * rmsnorm -- y[m] = x[m] / sqrt(mean_k x[m][k]^2 + eps) * gamma, fp32 math,
+ * one fp16 rounding.  [RU]: RMSNorm kept in FP16.  x, y fp16 [M][H];
+ * gamma fp16 [H].  y may alias x.
+ * ------------------------------------------------------------------------ */
+W4A16_API int rmsnorm(const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H, float eps,
+            w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kv_append_rope -- rotate q and k by RoPE at position p = context_lens[b]-1
+ * and append k, v to the paged pools ([EN] "2. The KV Cache and
+ * PagedAttention", "Bug 1"; RoPE itself is not on the pages: rotate-half
+ * pairs (i, i + D/2), inverse frequency theta^(-2i/D) rounded to fp32,
+ * angle = fp32 product p * inv_freq).
+ *   q        fp16 [B][Hq][D], rotated in place
+ *   k, v     fp16 [B][Hkv][D]; k is rotated on its way into the pool
+ *   row_stride  elements between sequence b and b+1 in q, k and v
+ *               (0 = packed, i.e. Hq*D for q and Hkv*D for k and v; a
+ *               non-zero value applies to all three, e.g. the row pitch
+ *               of a fused q|k|v buffer)
+ *   k_pool, v_pool fp16 [num_pages][Hkv][16][D]; exactly one slot per
+ *               (b, kv head) is written, nothing else changes
+ *   err_flag int32 device word or NULL: bit 0 set if a block-table entry
+ *            is outside [0, num_pages) (that sequence is skipped).
+ * D must be 128 and Hq % Hkv == 0.
+ * ------------------------------------------------------------------------ */
+W4A16_API int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v, int row_stride, uint16_t* k_pool,
+                   uint16_t* v_pool, int num_pages, const int32_t* block_table, int max_blocks,
+                   const int32_t* context_lens, int B, int Hq, int Hkv, int D, float theta,
+                   int32_t* err_flag, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode -- out[b][h] = sum_t softmax_t(q[b][h] . k_t * sm_scale) v_t
+ * over t < context_lens[b], k_t/v_t gathered through the block table, query
+ * head h reading kv head h / (Hq/Hkv) ([RU] 7:1 GQA; [EN] "2. The KV Cache
+ * and PagedAttention").  Tokens are split into partitions of
+ * partition_tokens (a multiple of 16); each partition's (max, sum, weighted
+ * V) partials go to `workspace` and are merged with the online-softmax
+ * combine by the last partition to finish (no extra launch).
+ *   q   fp16 [B][Hq][D] with row pitch q_stride elements (0 = Hq*D)
+ *   out fp16 [B][Hq][D] (packed)
+ *   max_context   upper bound on every context_lens[b] (sizes the grid)
+ *   workspace     device scratch of paged_gqa_decode_workspace_size() bytes;
+ *                 its counter words must be zero before the first use and
+ *                 every call leaves them zero again (w4a16_workspace_clear
+ *                 zeroes it once).  Calls that run concurrently on the GPU
+ *                 need separate workspaces.
+ *   err_flag      as for kv_append_rope (bad pages are skipped).
+ * D must be 128, Hq % Hkv == 0, Hq/Hkv <= 8.  context_lens[b] == 0 yields
+ * zeros.
+ * ------------------------------------------------------------------------ */
+W4A16_API int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t* k_pool,
+                     const uint16_t* v_pool, int num_pages, const int32_t* block_table,
+                     int max_blocks, const int32_t* context_lens, int max_context, int B, int Hq,
+                     int Hkv, int D, float sm_scale, int partition_tokens, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
+                     w4a16_stream_t stream);
+
+/* Bytes of workspace paged_gqa_decode needs for these sizes. */
+W4A16_API size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max_context,
+                                       int partition_tokens, int D);
+
+/* Partition size the library picks when partition_tokens == 0 is passed to
+ * paged_gqa_decode (a multiple of 16; depends on the SM count). */
+W4A16_API int paged_gqa_decode_default_partition(int B, int Hkv, int max_context);
+
+/* Zero a workspace once before first use (enqueued on `stream`). */
+W4A16_API int w4a16_workspace_clear(void* workspace, size_t bytes, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Embedding row gather: x[b] = embed[tokens[b]], embed fp16 [vocab][H].
+ * Not on the pages (plain decoder front end).  A token outside [0, vocab)
+ * sets bit 0 of err_flag and yields a zero row.
+ * ------------------------------------------------------------------------ */
+W4A16_API int embedding_gather(const uint16_t* embed, int vocab, int H, const int32_t* tokens, int B,
+                     uint16_t* x, int32_t* err_flag, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * lm_head_argmax -- logits = W . x (FP16 weight [vocab][H], fp32 accumulate)
+ * and token = argmax (lowest index on ties), per sequence.  [RU]: lm_head
+ * kept in FP16; the argmax is the greedy decode rule.
+ *   x          fp16 [B][H]
+ *   logits     fp16 [B][vocab] or NULL
+ *   tokens_out int32 [B]
+ *   workspace  lm_head_argmax_workspace_size() bytes; counter words zero
+ *              before first use, left zero by every call.
+ * ------------------------------------------------------------------------ */
+W4A16_API int lm_head_argmax(const uint16_t* x, int B, int H, const uint16_t* lm_head, int vocab,
+                   uint16_t* logits, int32_t* tokens_out, void* workspace, size_t workspace_bytes,
+                   w4a16_stream_t stream);
+W4A16_API size_t lm_head_argmax_workspace_size(int B, int vocab);
+
+/* ------------------------------------------------------------------------
+ * Whole model (Qwen2-shaped decoder).  [EN] "Implementation Guide": static
+ * pre-allocation and a CUDA-graph-captured decode step; [RU] "Ключевые
+ * метрики производительности": the graph-captured steady-state decode.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int hidden, n_q_heads, n_kv_heads, head_dim, inter, n_layers, vocab;
+  float eps, theta;
+  int num_pages;        /* pages in each layer's K (and V) pool */
+  int partition_tokens; /* split-K partition for attention; 0 = library choice */
+} w4a16_model_config;
+
+typedef struct {
+  const uint16_t *ln1, *ln2;                          /* fp16 [hidden] */
+  const uint32_t *wq, *wk, *wv, *wo, *wg, *wu, *wd;   /* packed INT4 */
+  const uint16_t *sq, *sk, *sv, *so, *sg, *su, *sd;   /* fp16 group scales */
+  const uint16_t *bq, *bk, *bv;                       /* fp16 biases or NULL */
+  uint16_t *k_pool, *v_pool;                          /* this layer's pools */
+} w4a16_layer_weights;
+
+typedef struct {
+  const uint16_t* embed;      /* fp16 [vocab][hidden] */
+  const uint16_t* final_norm; /* fp16 [hidden] */
+  const uint16_t* lm_head;    /* fp16 [vocab][hidden] */
+  const w4a16_layer_weights* layers; /* HOST array [n_layers], copied */
+} w4a16_model_weights;
+
+typedef struct w4a16_model w4a16_model;
+
+/* Builds the model handle.  The only call that allocates: one device arena
+ * for activations and workspaces sized for max_batch sequences of up to
+ * max_context tokens.  Weight and pool pointers are borrowed (caller keeps
+ * them alive). */
+W4A16_API int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
+                       int max_context, w4a16_model** out);
+W4A16_API void w4a16_model_destroy(w4a16_model* m);
+
+/* Device word the model's kernels report out-of-range indices into. */
+W4A16_API int32_t* w4a16_model_err_flag(w4a16_model* m);
+
+/* Synchronise `stream`, read and clear the model's device error word:
+ * returns W4A16_ERR_DEVICE_BOUNDS if a kernel skipped an out-of-range page or
+ * token, W4A16_ERR_TIMEOUT if a bounded wait gave up, else W4A16_OK.  This
+ * call blocks and copies to the host, so it must not be used while the
+ * stream is capturing. */
+W4A16_API int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream);
+
+/* One decoder layer on hidden states x fp16 [B][hidden] (in place), with
+ * context_lens already counting the appended token. */
+W4A16_API int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table,
+                      int max_blocks, const int32_t* context_lens, int B, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * decode_step -- one greedy decode step for B sequences:
+ *   context_lens[b] += 1 (on the device; the new token goes to position
+ *   context_lens[b] - 1), x = embed[tokens_in], n_layers decoder layers
+ *   (RMSNorm -> q/k/v GEMV + bias -> RoPE + KV append -> paged GQA
+ *   attention -> o GEMV + residual -> RMSNorm -> gate/up GEMV + SiLU-mul ->
+ *   down GEMV + residual), final RMSNorm, lm_head, argmax -> tokens_out.
+ *   tokens_in, tokens_out  int32 [B] device (may be the same buffer)
+ *   block_table            int32 [B][max_blocks]; pages for the new
+ *                          position must already be assigned
+ *   logits                 fp16 [B][vocab] or NULL
+ *   use_graph              1: capture the step into a CUDA graph on first
+ *                          use for this argument set and replay it after;
+ *                          0: launch the kernels directly.
+ * Every pointer must stay the same across replays of one graph (the graph
+ * is keyed on them); the data they point to may change between calls.
+ * ------------------------------------------------------------------------ */
+W4A16_API int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tokens_out,
+                const int32_t* block_table, int max_blocks, int32_t* context_lens, int B,
+                uint16_t* logits, int use_graph, w4a16_stream_t stream);
+
+/* Number of kernels one decode_step launches for B sequences (graph or not). */
+W4A16_API int decode_step_kernel_count(w4a16_model* m, int B);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

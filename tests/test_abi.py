@@ -1,0 +1,118 @@
+"""The C-ABI library loads and exports every symbol include/*.h declares, and
+its host-side argument checks reject bad calls before touching the GPU.
+CPU only: no call here reaches a kernel launch."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_decode_paged_gb300 import build
+    build.build()
+    from w4a16_decode_paged_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        for m in re.finditer(r"W4A16_API\s+[\w\s\*]+?\b(\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_five_path_calls():
+    names = _declared_symbols()
+    for n in ("w4a16_gemv", "paged_gqa_decode", "kv_append_rope", "rmsnorm", "decode_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_the_header(lib):
+    from w4a16_decode_paged_gb300 import _lib
+    assert _declared_symbols() <= set(_lib.SIGNATURES)
+
+
+def test_version(lib):
+    assert lib.w4a16_version() == 100
+
+
+ALIGNED = 1 << 20          # fake device addresses: never dereferenced
+MISALIGNED = (1 << 20) + 64
+
+
+def test_gemv_rejects_bad_shapes_and_alignment(lib):
+    from w4a16_decode_paged_gb300 import _lib
+    rc = lib.w4a16_gemv(ALIGNED, 1, 100, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 3 and b"multiple of 128" in lib.w4a16_last_error()
+    rc = lib.w4a16_gemv(MISALIGNED, 1, 128, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 2 and b"x must be 128-byte aligned" in lib.w4a16_last_error()
+    rc = lib.w4a16_gemv(ALIGNED, 1, 128, ALIGNED, MISALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 2
+    rc = lib.w4a16_gemv(None, 1, 128, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 1
+    rc = lib.w4a16_gemv(ALIGNED, 0, 128, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 1
+    rc = lib.w4a16_gemv(ALIGNED, 64, 4096, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
+    assert rc == 3  # outside the CUDA-core path (M*K too large)
+    with pytest.raises(_lib.W4A16Error):
+        _lib.check(rc)
+
+
+def test_attention_rejects_bad_shapes(lib):
+    args = lambda D=128, Hq=28, Hkv=4, part=512, ws=None, wsb=0, maxctx=512: (
+        ALIGNED, 0, ALIGNED, ALIGNED, 64, ALIGNED, 32, ALIGNED, maxctx, 1, Hq, Hkv, D, 0.088, part, ws, wsb,
+        ALIGNED, None, None)
+    assert lib.paged_gqa_decode(*args(D=64)) == 3
+    assert lib.paged_gqa_decode(*args(Hq=30, Hkv=4)) == 3
+    assert lib.paged_gqa_decode(*args(Hq=36, Hkv=4)) == 3          # 9 heads per kv head
+    assert lib.paged_gqa_decode(*args(part=100)) == 3
+    assert lib.paged_gqa_decode(*args(maxctx=1024)) == 3           # beyond max_blocks * 16
+    assert lib.paged_gqa_decode(*args(part=64)) == 1               # needs a workspace
+    need = lib.paged_gqa_decode_workspace_size(1, 28, 4, 512, 64, 128)
+    assert need >= 28 * 8 * 128 * 4
+    assert lib.paged_gqa_decode(*args(part=64, ws=MISALIGNED, wsb=need)) == 2
+
+
+def test_append_rejects_bad_shapes(lib):
+    base = [ALIGNED, ALIGNED, ALIGNED, 0, ALIGNED, ALIGNED, 64, ALIGNED, 4, ALIGNED, 1, 28, 4, 128, 1e6, None, None]
+    a = list(base); a[13] = 64
+    assert lib.kv_append_rope(*a) == 3
+    a = list(base); a[11] = 27
+    assert lib.kv_append_rope(*a) == 3
+    a = list(base); a[14] = 0.0
+    assert lib.kv_append_rope(*a) == 1
+    a = list(base); a[4] = MISALIGNED
+    assert lib.kv_append_rope(*a) == 2
+
+
+def test_rmsnorm_lm_head_reject(lib):
+    assert lib.rmsnorm(ALIGNED, ALIGNED, ALIGNED, 1, 12, 1e-6, None) == 3
+    assert lib.rmsnorm(ALIGNED, ALIGNED, MISALIGNED, 1, 16, 1e-6, None) == 2
+    ws = lib.lm_head_argmax_workspace_size(1, 1000)
+    assert lib.lm_head_argmax(ALIGNED, 5, 896, ALIGNED, 1000, None, ALIGNED, ALIGNED, ws, None) == 3
+    assert lib.lm_head_argmax(ALIGNED, 1, 896, ALIGNED, 1000, None, ALIGNED, ALIGNED, 8, None) == 1
+
+
+def test_model_create_rejects_bad_config(lib):
+    from w4a16_decode_paged_gb300 import _lib
+    c = _lib.ModelConfig(896, 7, 1, 64, 2432, 1, 0, 1e-6, 1e6, 8, 0)
+    w = _lib.ModelWeights(None, None, None, None)
+    h = ctypes.c_void_p()
+    assert lib.w4a16_model_create(ctypes.byref(c), ctypes.byref(w), 1, 64, ctypes.byref(h)) == 3
+    c = _lib.ModelConfig(896, 7, 1, 128, 2432, 1, 0, 1e-6, 1e6, 8, 0)
+    assert lib.w4a16_model_create(ctypes.byref(c), ctypes.byref(w), 1, 64, ctypes.byref(h)) == 1
+    assert not h.value

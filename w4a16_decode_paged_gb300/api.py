@@ -1,0 +1,244 @@
+"""Torch-tensor front end of the C ABI (same names as include/w4a16.h).
+
+Each function checks dtypes/devices, allocates outputs with torch when the
+caller gives none, and calls the library on torch's current CUDA stream.
+Nothing here computes any part of the decode path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from ._lib import LayerWeights, ModelConfig, ModelWeights, check, load
+
+__all__ = ["w4a16_gemv", "w4a16_gemv_rmsnorm", "w4a16_gemv_silu_mul", "rmsnorm", "kv_append_rope",
+           "paged_gqa_decode", "paged_gqa_decode_workspace_size", "paged_gqa_decode_default_partition",
+           "workspace_clear", "embedding_gather", "lm_head_argmax", "Model", "stream_handle"]
+
+
+def stream_handle(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, dtypes, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_H = (torch.float16,)
+_W = (torch.int32, torch.uint32)
+_I = (torch.int32,)
+
+
+def w4a16_gemv(x, qweight, scales, bias=None, residual=None, out=None, stream=None):
+    _need(x, _H, "x"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
+    M, K = x.shape
+    N = qweight.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check(load().w4a16_gemv(_p(x), M, K, _p(qweight), _p(scales), N, _p(bias), _p(residual), _p(out),
+                            stream_handle(stream)))
+    return out
+
+
+def w4a16_gemv_rmsnorm(x, gamma, eps, qweight, scales, bias=None, out=None, stream=None):
+    _need(x, _H, "x"); _need(gamma, _H, "gamma"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
+    M, K = x.shape
+    N = qweight.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check(load().w4a16_gemv_rmsnorm(_p(x), _p(gamma), float(eps), M, K, _p(qweight), _p(scales), N, _p(bias),
+                                    _p(out), stream_handle(stream)))
+    return out
+
+
+def w4a16_gemv_silu_mul(x, gamma, eps, qweight_gate, scales_gate, qweight_up, scales_up, out=None, stream=None):
+    _need(x, _H, "x")
+    M, K = x.shape
+    N = qweight_gate.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check(load().w4a16_gemv_silu_mul(_p(x), _p(gamma), float(eps), M, K, _p(qweight_gate), _p(scales_gate),
+                                     _p(qweight_up), _p(scales_up), N, _p(out), stream_handle(stream)))
+    return out
+
+
+def rmsnorm(x, gamma, eps, out=None, stream=None):
+    _need(x, _H, "x"); _need(gamma, _H, "gamma")
+    M, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    check(load().rmsnorm(_p(x), _p(gamma), _p(out), M, H, float(eps), stream_handle(stream)))
+    return out
+
+
+def kv_append_rope(q, k, v, k_pool, v_pool, block_table, context_lens, theta, row_stride=0, err_flag=None,
+                   n_q_heads=None, n_kv_heads=None, stream=None):
+    """q [B][Hq][D] (rotated in place), k/v [B][Hkv][D]; pools [pages][Hkv][16][D]."""
+    _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
+    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
+    pages, Hkv, _, D = k_pool.shape
+    B = block_table.shape[0]
+    Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
+    if n_kv_heads is not None:
+        Hkv = n_kv_heads
+    check(load().kv_append_rope(_p(q), _p(k), _p(v), int(row_stride), _p(k_pool), _p(v_pool), pages,
+                                _p(block_table), block_table.shape[1], _p(context_lens), B, Hq, Hkv, D,
+                                float(theta), _p(err_flag), stream_handle(stream)))
+    return q
+
+
+def paged_gqa_decode_workspace_size(B, Hq, Hkv, max_context, partition_tokens=0, D=128):
+    return int(load().paged_gqa_decode_workspace_size(B, Hq, Hkv, max_context, partition_tokens, D))
+
+
+def paged_gqa_decode_default_partition(B, Hkv, max_context):
+    return int(load().paged_gqa_decode_default_partition(B, Hkv, max_context))
+
+
+def workspace_clear(ws, stream=None):
+    check(load().w4a16_workspace_clear(_p(ws), ws.numel() * ws.element_size(), stream_handle(stream)))
+
+
+def paged_gqa_decode(q, k_pool, v_pool, block_table, context_lens, max_context, sm_scale=None, partition_tokens=0,
+                     workspace=None, out=None, err_flag=None, q_stride=0, n_q_heads=None, stream=None):
+    """q [B][Hq][D] (or rows of pitch q_stride); returns out [B][Hq][D]."""
+    _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
+    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
+    pages, Hkv, _, D = k_pool.shape
+    B = block_table.shape[0]
+    Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    lib = load()
+    if workspace is None:
+        nbytes = lib.paged_gqa_decode_workspace_size(B, Hq, Hkv, max_context, partition_tokens, D)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=k_pool.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=k_pool.device)
+    check(lib.paged_gqa_decode(_p(q), int(q_stride), _p(k_pool), _p(v_pool), pages, _p(block_table),
+                               block_table.shape[1], _p(context_lens), int(max_context), B, Hq, Hkv, D,
+                               float(sm_scale), int(partition_tokens), _p(workspace),
+                               workspace.numel() * workspace.element_size(), _p(out), _p(err_flag),
+                               stream_handle(stream)))
+    return out
+
+
+def embedding_gather(embed, tokens, out=None, err_flag=None, stream=None):
+    vocab, H = embed.shape
+    B = tokens.numel()
+    if out is None:
+        out = torch.empty((B, H), dtype=torch.float16, device=embed.device)
+    check(load().embedding_gather(_p(embed), vocab, H, _p(tokens), B, _p(out), _p(err_flag),
+                                  stream_handle(stream)))
+    return out
+
+
+def lm_head_argmax(x, lm_head, logits=None, tokens_out=None, workspace=None, want_logits=False, stream=None):
+    B, H = x.shape
+    vocab = lm_head.shape[0]
+    lib = load()
+    if workspace is None:
+        workspace = torch.zeros(lib.lm_head_argmax_workspace_size(B, vocab), dtype=torch.uint8, device=x.device)
+    if tokens_out is None:
+        tokens_out = torch.empty(B, dtype=torch.int32, device=x.device)
+    if logits is None and want_logits:
+        logits = torch.empty((B, vocab), dtype=torch.float16, device=x.device)
+    check(lib.lm_head_argmax(_p(x), B, H, _p(lm_head), vocab, _p(logits), _p(tokens_out), _p(workspace),
+                             workspace.numel(), stream_handle(stream)))
+    return tokens_out, logits
+
+
+class Model:
+    """Handle over w4a16_model_*: weights and pools stay owned by the caller
+    (torch tensors kept alive here), the library owns its activation arena."""
+
+    LAYER_KEYS = ("ln1", "ln2", "wq", "wk", "wv", "wo", "wg", "wu", "wd", "sq", "sk", "sv", "so", "sg", "su",
+                  "sd", "bq", "bk", "bv", "k_pool", "v_pool")
+
+    def __init__(self, cfg: dict, layers: list, embed=None, final_norm=None, lm_head=None, max_batch=1,
+                 max_context=4096, num_pages=None, partition_tokens=0):
+        self._lib = load()
+        self.cfg = dict(cfg)
+        self._keep = [embed, final_norm, lm_head]
+        c = ModelConfig(cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"],
+                        len(layers), cfg.get("vocab", 0) if lm_head is not None else 0, float(cfg["eps"]),
+                        float(cfg["theta"]), int(num_pages if num_pages is not None else
+                                                 layers[0]["k_pool"].shape[0]), int(partition_tokens))
+        arr = (LayerWeights * max(1, len(layers)))()
+        for i, lw in enumerate(layers):
+            for key in self.LAYER_KEYS:
+                t = lw.get(key)
+                self._keep.append(t)
+                setattr(arr[i], key, None if t is None else t.data_ptr())
+        self._layers_arr = arr
+        w = ModelWeights(_p(embed), _p(final_norm), _p(lm_head),
+                         ctypes.cast(arr, ctypes.POINTER(LayerWeights)))
+        h = ctypes.c_void_p()
+        check(self._lib.w4a16_model_create(ctypes.byref(c), ctypes.byref(w), int(max_batch), int(max_context),
+                                           ctypes.byref(h)))
+        self._h = h
+        self.max_batch, self.max_context = max_batch, max_context
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.w4a16_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def err_flag_ptr(self) -> int:
+        return int(self._lib.w4a16_model_err_flag(self._h) or 0)
+
+    def check_errors(self, stream=None) -> int:
+        """Status code of the device error word (blocks; clears the word)."""
+        return int(self._lib.w4a16_model_check_errors(self._h, stream_handle(stream)))
+
+    def layer(self, i, x, block_table, context_lens, stream=None):
+        check(self._lib.w4a16_model_layer(self._h, int(i), _p(x), _p(block_table), block_table.shape[1],
+                                          _p(context_lens), x.shape[0], stream_handle(stream)))
+        return x
+
+    def decode_step(self, tokens_in, tokens_out, block_table, context_lens, logits=None, use_graph=True,
+                    stream=None):
+        check(self._lib.decode_step(self._h, _p(tokens_in), _p(tokens_out), _p(block_table), block_table.shape[1],
+                                    _p(context_lens), tokens_in.numel(), _p(logits), int(bool(use_graph)),
+                                    stream_handle(stream)))
+        return tokens_out
+
+    def kernel_count(self, B=1) -> int:
+        return int(self._lib.decode_step_kernel_count(self._h, int(B)))
+
+
+def device_layer(w: dict, k_pool, v_pool, device="cuda") -> dict:
+    """Move one layer's numpy weights (as drawn by ``synth``) and its pools to
+    the device as torch tensors (uint32 words travel as int32)."""
+    import numpy as np
+
+    out = {}
+    for key, a in w.items():
+        if a is None:
+            out[key] = None
+            continue
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint32:
+            a = a.view(np.int32)
+        out[key] = torch.from_numpy(a).to(device)
+    for key, a in (("k_pool", k_pool), ("v_pool", v_pool)):
+        out[key] = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return out

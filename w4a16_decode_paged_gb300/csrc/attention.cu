@@ -1,0 +1,561 @@
+// attention.cu -- paged GQA decode attention with a fused split-K combine,
+// and RoPE + KV append.
+//
+// Paging follows "Building a Custom LLM Inference Runtime on H100"
+// (explore.n1n.ai), "2. The KV Cache and PagedAttention" and "Bug 1: The KV
+// Cache Indexing 'Off-By-One'": token t of sequence b is slot t % 16 of page
+// block_table[b][t / 16].  The pool layout [page][kv_head][16][128] fp16 makes
+// each (page, kv head) slice one contiguous 4 KiB run, the unit the aikraft.ru
+// article ("Архитектурные решения и оптимизации") aligns to cache lines; here
+// it is the unit of one 1-D bulk (TMA) copy into shared memory.
+//
+// One CTA handles (sequence b, kv head, partition p) for all G = Hq/Hkv query
+// heads that share the kv head (7:1 GQA in the article).  Its four warps take
+// the partition's pages round-robin; each warp owns a private ring of
+// ATT_STAGES (K, V) page slots filled by 1-D bulk copies on an mbarrier, so
+// no warp waits on another inside the page loop.  Per page a warp computes
+// the 16 x G scores with packed fp32 FMAs (each K element is converted once
+// and used for all G heads), an fp32 online softmax (exp2 with the scale
+// folded into q), and the P.V update.  The warps' states are merged in shared
+// memory; with several partitions the merged (max, sum, weighted V) partials
+// go to the workspace and the last CTA of the (b, kv head) group to finish
+// (an atomic ticket, no spin) merges them and writes the output.
+#include <cmath>
+#include <cstdio>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4 {
+
+constexpr int ATT_D = 128;
+constexpr int ATT_PAGE = 16;
+constexpr int ATT_NW = 4;          // warps per CTA
+constexpr int ATT_STAGES = 2;      // page slots per warp
+constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice
+constexpr uint32_t ATT_SLICE_BYTES = ATT_SLICE * 2;  // 4096
+constexpr size_t ATT_RING_BYTES = (size_t)ATT_NW * ATT_STAGES * 2 * ATT_SLICE_BYTES;
+constexpr size_t ATT_SMEM = ATT_RING_BYTES + ATT_NW * ATT_STAGES * 8 + ATT_NW * 8 * 16 * 4 + ATT_NW * 8 * 4;
+constexpr unsigned long long ATT_TIMEOUT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase (returns false on timeout).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > ATT_TIMEOUT_NS) return false;
+  }
+}
+
+__device__ __forceinline__ float2 h2f2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+template <int G>
+__global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  __half* ring = reinterpret_cast<__half*>(smraw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + ATT_RING_BYTES);
+  float* sbuf = reinterpret_cast<float*>(bars + ATT_NW * ATT_STAGES);  // [NW][8][16]
+  float* corr = sbuf + ATT_NW * 8 * 16;                               // [NW][8]
+  __shared__ int s_last;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.z, kvh = blockIdx.y, p = blockIdx.x;
+
+  pdl_launch_dependents();
+  if (threadIdx.x < ATT_NW * ATT_STAGES) mbar_init(&bars[threadIdx.x], 1);
+  fence_mbar_init();
+  __syncthreads();
+  pdl_wait();  // q, the pools and the lengths may come from earlier kernels
+
+  const int L = a.context_lens[b];
+  const int t_begin = p * a.part_tokens;
+  const int t_end = min(L, t_begin + a.part_tokens);
+  const int npages = t_end > t_begin ? (t_end - t_begin + ATT_PAGE - 1) / ATT_PAGE : 0;
+  const int pg0 = t_begin / ATT_PAGE;
+  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
+  bool timed_out = false;
+
+  // this warp's pages: i = warp, warp + NW, ...
+  const int my_pages = npages > warp ? (npages - warp + ATT_NW - 1) / ATT_NW : 0;
+  uint64_t* mybar = bars + warp * ATT_STAGES;
+  __half* myring = ring + (size_t)warp * ATT_STAGES * 2 * ATT_SLICE;
+
+  auto page_id = [&](int li) -> int {  // li: index into this warp's page list
+    const int gi = pg0 + warp + li * ATT_NW;
+    const int pg = (gi < a.max_blocks) ? bt[gi] : -1;
+    return (pg >= 0 && pg < a.num_pages) ? pg : -1;
+  };
+  auto issue = [&](int li) {  // lane 0 only
+    const int pg = page_id(li);
+    uint64_t* bar = &mybar[li % ATT_STAGES];
+    __half* dst = myring + (size_t)(li % ATT_STAGES) * 2 * ATT_SLICE;
+    if (pg >= 0) {
+      const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
+      mbar_arrive_expect_tx(bar, 2 * ATT_SLICE_BYTES);
+      bulk_g2s(dst, a.k_pool + off, ATT_SLICE_BYTES, bar);
+      bulk_g2s(dst + ATT_SLICE, a.v_pool + off, ATT_SLICE_BYTES, bar);
+    } else {
+      mbar_arrive(bar);  // nothing to copy; complete the phase
+      if (a.err_flag) atomicOr(a.err_flag, 1);
+    }
+  };
+  if (lane == 0) {
+    for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) issue(li);
+  }
+
+  // q for this lane's dims: lane = (tq, ds); dims [16 ds, 16 ds + 16)
+  const int tq = lane >> 3, ds = lane & 7;
+  float2 qr[G][8];
+  {
+    const __half* qb = a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint4* src = reinterpret_cast<const uint4*>(qb + h * ATT_D + 16 * ds);
+      uint4 u0 = src[0], u1 = src[1];
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float2 f = h2f2(w[j]);
+        qr[h][j] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+      }
+    }
+  }
+  float m_run = -INFINITY, l_run = 0.f;  // lane h < G holds head h's state
+  float2 o[G][2];                       // dims [4 lane, 4 lane + 4)
+#pragma unroll
+  for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
+  float* ws = sbuf + warp * 8 * 16;
+  float* wcorr = corr + warp * 8;
+
+  int consumed = 0;
+  for (int li = 0; li < my_pages; ++li) {
+    const int stage = li % ATT_STAGES;
+    const uint32_t parity = (li / ATT_STAGES) & 1;
+    if (!wait_phase(&mybar[stage], parity)) {
+      timed_out = true;
+      break;
+    }
+    consumed = li + 1;
+    const __half* Ks = myring + (size_t)stage * 2 * ATT_SLICE;
+    const __half* Vs = Ks + ATT_SLICE;
+    const int gi = warp + li * ATT_NW;  // page index within the partition
+    const int tok0 = (pg0 + gi) * ATT_PAGE;
+    const bool page_ok = page_id(li) >= 0;
+    const int nv = page_ok ? min(ATT_PAGE, t_end - tok0) : 0;
+
+    // ---- scores: 4 rounds of 4 tokens; lane (tq, ds) -------------------
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = tq + 4 * r;
+      const uint4* krow = reinterpret_cast<const uint4*>(Ks + t * ATT_D + 16 * ds);
+      // bank-conflict-free order: upper half of the lanes reads its second 16 B first
+      const int first = (ds >> 2) & 1;
+      uint4 ka = krow[first], kb = krow[first ^ 1];
+      uint4 k0 = first ? kb : ka, k1 = first ? ka : kb;
+      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+      float2 kf[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) kf[j] = h2f2(kw[j]);
+      float v[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) v[h] = 0.f;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc = ffma2(qr[h][j], kf[j], acc);
+        v[h] = acc.x + acc.y;
+      }
+      // transpose-reduce over the 8 ds lanes: lane ds ends with head ds's sum
+      float v4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool up = ds & 4;
+        float send = up ? v[j] : v[j + 4];
+        float keep = up ? v[j + 4] : v[j];
+        v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      float v2[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const bool up = ds & 2;
+        float send = up ? v4[j] : v4[j + 2];
+        float keep = up ? v4[j + 2] : v4[j];
+        v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      {
+        const bool up = ds & 1;
+        float send = up ? v2[0] : v2[1];
+        float keep = up ? v2[1] : v2[0];
+        float tot = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        if (ds < G) ws[ds * 16 + t] = tot;
+      }
+    }
+    __syncwarp();
+
+    // ---- online softmax: lane h < G owns head h -----------------------
+    if (lane < G) {
+      float s[16];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        s[t] = (t < nv) ? ws[lane * 16 + t] : -INFINITY;
+        mx = fmaxf(mx, s[t]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float c = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+      float sum = 0.f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float pv = (s[t] == -INFINITY) ? 0.f : exp2f(s[t] - m_new);
+        ws[lane * 16 + t] = pv;
+        sum += pv;
+      }
+      l_run = l_run * c + sum;
+      m_run = m_new;
+      wcorr[lane] = c;
+    }
+    __syncwarp();
+
+    // ---- P.V: lane owns dims [4 lane, 4 lane + 4) ---------------------
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float c = wcorr[h];
+      o[h][0] = make_float2(o[h][0].x * c, o[h][0].y * c);
+      o[h][1] = make_float2(o[h][1].x * c, o[h][1].y * c);
+    }
+    for (int t = 0; t < nv; ++t) {
+      const uint2 vv = *reinterpret_cast<const uint2*>(Vs + t * ATT_D + 4 * lane);
+      const float2 v0 = h2f2(vv.x), v1 = h2f2(vv.y);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pv = ws[h * 16 + t];
+        const float2 p2 = make_float2(pv, pv);
+        o[h][0] = ffma2(p2, v0, o[h][0]);
+        o[h][1] = ffma2(p2, v1, o[h][1]);
+      }
+    }
+    __syncwarp();
+    // refill this stage with the page ATT_STAGES ahead
+    if (lane == 0 && li + ATT_STAGES < my_pages) {
+      fence_proxy_async_smem();
+      issue(li + ATT_STAGES);
+    }
+  }
+  // Every issued copy has been consumed unless a wait timed out; in that case
+  // flag it and wait (bounded) for the copies still in flight before the
+  // ring memory is reused.
+  if (timed_out && lane == 0) {
+    if (a.err_flag) atomicOr(a.err_flag, 2);
+    for (int x = consumed; x < my_pages && x < consumed + ATT_STAGES; ++x)
+      (void)wait_phase(&mybar[x % ATT_STAGES], (x / ATT_STAGES) & 1);
+  }
+  __syncthreads();  // all warps done with their rings
+
+  // ---- merge the warps' states in shared memory (ring reused) ------------
+  float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
+  float* mml = mo + ATT_NW * 8 * ATT_D;                 // [NW][8][2]
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float* dst = mo + (warp * 8 + h) * ATT_D + 4 * lane;
+    dst[0] = o[h][0].x;
+    dst[1] = o[h][0].y;
+    dst[2] = o[h][1].x;
+    dst[3] = o[h][1].y;
+  }
+  if (lane < G) {
+    mml[(warp * 8 + lane) * 2 + 0] = m_run;
+    mml[(warp * 8 + lane) * 2 + 1] = l_run;
+  }
+  __syncthreads();
+
+  const int d = threadIdx.x;  // 128 threads = 128 dims
+  const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
+  if (a.P == 1) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = -INFINITY;
+      for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+      float acc = 0.f, den = 0.f;
+      if (M != -INFINITY) {
+        for (int w = 0; w < ATT_NW; ++w) {
+          const float mw = mml[(w * 8 + h) * 2];
+          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+          acc += mo[(w * 8 + h) * ATT_D + d] * f;
+          den += mml[(w * 8 + h) * 2 + 1] * f;
+        }
+      }
+      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+    }
+    return;
+  }
+
+  // several partitions: write this partition's partial, then the ticket
+  if (t_begin < L) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = -INFINITY;
+      for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+      float acc = 0.f, den = 0.f;
+      if (M != -INFINITY) {
+        for (int w = 0; w < ATT_NW; ++w) {
+          const float mw = mml[(w * 8 + h) * 2];
+          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+          acc += mo[(w * 8 + h) * ATT_D + d] * f;
+          den += mml[(w * 8 + h) * 2 + 1] * f;
+        }
+      }
+      const size_t slot = (qh0 + h) * a.P + p;
+      a.ws_o[slot * ATT_D + d] = acc;
+      if (d == 0) {
+        a.ws_ml[slot * 2 + 0] = M;
+        a.ws_ml[slot * 2 + 1] = den;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int ticket = atomicAdd(&a.counters[(size_t)b * a.Hkv + kvh], 1u);
+    s_last = (ticket == (unsigned int)(a.P - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int Pv = L > 0 ? min(a.P, (L + a.part_tokens - 1) / a.part_tokens) : 0;
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    const size_t base = (qh0 + h) * a.P;
+    float M = -INFINITY;
+    for (int j = 0; j < Pv; ++j) M = fmaxf(M, __ldcg(&a.ws_ml[(base + j) * 2]));
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (int j = 0; j < Pv; ++j) {
+        const float mj = __ldcg(&a.ws_ml[(base + j) * 2]);
+        const float f = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+        acc += __ldcg(&a.ws_o[(base + j) * ATT_D + d]) * f;
+        den += __ldcg(&a.ws_ml[(base + j) * 2 + 1]) * f;
+      }
+    }
+    a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+  }
+  if (threadIdx.x == 0) a.counters[(size_t)b * a.Hkv + kvh] = 0u;  // ready for the next call
+}
+
+size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P) {
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  return up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4) + up((size_t)B * Hkv * 4);
+}
+
+template <int G>
+static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
+  static bool configured = false;
+  auto kern = paged_attn_kernel<G>;
+  if (!configured) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
+    configured = true;
+  }
+  dim3 grid(a.P, a.Hkv, a.B);
+  cudaError_t e = launch_pdl(kern, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+int launch_paged_attention(const AttnArgs& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_attn_g<1>(a, s);
+    case 2: return launch_attn_g<2>(a, s);
+    case 4: return launch_attn_g<4>(a, s);
+    case 7: return launch_attn_g<7>(a, s);
+    case 8: return launch_attn_g<8>(a, s);
+    default:
+      return set_error(W4A16_ERR_SHAPE, "paged attention: Hq/Hkv=%d not built (1, 2, 4, 7, 8)", a.Hq / a.Hkv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RoPE + KV append: one CTA per sequence.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rope_append_kernel(const __grid_constant__ RopeArgs a) {
+  const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int pos = a.context_lens[b] - 1;
+  if (pos < 0) return;
+  const int blk = pos / ATT_PAGE, slot = pos % ATT_PAGE;
+  const int page = (blk < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + blk] : -1;
+  const bool ok = page >= 0 && page < a.num_pages;
+  if (!ok && threadIdx.x == 0 && a.err_flag) atomicOr(a.err_flag, 1);
+  const float fpos = (float)pos;
+  const int nrot = (a.Hq + a.Hkv) * (ATT_D / 2);
+  for (int idx = threadIdx.x; idx < nrot; idx += blockDim.x) {
+    const int head = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
+    const float ang = __fmul_rn(fpos, a.inv_freq[i]);  // the fp32 product, no contraction
+    float sn, cs;
+    sincosf(ang, &sn, &cs);
+    if (head < a.Hq) {
+      __half* x = a.q + (size_t)b * a.stride_q + (size_t)head * ATT_D;
+      const float x0 = __half2float(x[i]), x1 = __half2float(x[i + ATT_D / 2]);
+      x[i] = __float2half_rn(x0 * cs - x1 * sn);
+      x[i + ATT_D / 2] = __float2half_rn(x1 * cs + x0 * sn);
+    } else if (ok) {
+      const int kh = head - a.Hq;
+      const __half* x = a.k + (size_t)b * a.stride_kv + (size_t)kh * ATT_D;
+      const float x0 = __half2float(x[i]), x1 = __half2float(x[i + ATT_D / 2]);
+      __half* dst = a.k_pool + (((size_t)page * a.Hkv + kh) * ATT_PAGE + slot) * ATT_D;
+      dst[i] = __float2half_rn(x0 * cs - x1 * sn);
+      dst[i + ATT_D / 2] = __float2half_rn(x1 * cs + x0 * sn);
+    }
+  }
+  if (ok) {
+    for (int idx = threadIdx.x; idx < a.Hkv * ATT_D; idx += blockDim.x) {
+      const int kh = idx / ATT_D, dd = idx % ATT_D;
+      a.v_pool[(((size_t)page * a.Hkv + kh) * ATT_PAGE + slot) * ATT_D + dd] =
+          a.v[(size_t)b * a.stride_kv + (size_t)kh * ATT_D + dd];
+    }
+  }
+}
+
+void rope_inv_freq_table(float theta, int D, float* out) {
+  for (int i = 0; i < D / 2; ++i) out[i] = (float)std::pow((double)theta, -2.0 * (double)i / (double)D);
+}
+
+int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
+  cudaError_t e = launch_pdl(rope_append_kernel, dim3(a.B), dim3(256), 0, s, a);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "rope/append launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+int default_partition(int B, int Hkv, int max_context) {
+  const int want = std::max(1, (2 * num_sms()) / std::max(1, B * Hkv));
+  int pt = (max_context + want - 1) / want;
+  pt = (pt + 63) / 64 * 64;
+  if (pt < 64) pt = 64;
+  if (pt > 512) pt = 512;
+  return pt;
+}
+
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" int paged_gqa_decode_default_partition(int B, int Hkv, int max_context) {
+  if (B < 1 || Hkv < 1 || max_context < 1) return 64;
+  return default_partition(B, Hkv, max_context);
+}
+
+extern "C" size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max_context, int partition_tokens,
+                                                  int D) {
+  (void)D;
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_context < 1) return 0;
+  if (partition_tokens <= 0) partition_tokens = default_partition(B, Hkv, max_context);
+  const int P = (max_context + partition_tokens - 1) / partition_tokens;
+  return attention_workspace_bytes(B, Hq, Hkv, P);
+}
+
+extern "C" int w4a16_workspace_clear(void* workspace, size_t bytes, w4a16_stream_t stream) {
+  W4_CHECK_ARG(workspace || bytes == 0, "workspace_clear: null workspace");
+  if (bytes == 0) return W4A16_OK;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "workspace_clear: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+extern "C" int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t* k_pool, const uint16_t* v_pool,
+                                int num_pages, const int32_t* block_table, int max_blocks,
+                                const int32_t* context_lens, int max_context, int B, int Hq, int Hkv, int D,
+                                float sm_scale, int partition_tokens, void* workspace, size_t workspace_bytes,
+                                uint16_t* out, int32_t* err_flag, w4a16_stream_t stream) {
+  W4_CHECK_ARG(q && k_pool && v_pool && block_table && context_lens && out,
+               "paged_gqa_decode: null tensor pointer");
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1 && max_context >= 1,
+               "paged_gqa_decode: sizes must be positive");
+  W4_CHECK_SHAPE(D == ATT_D, "paged_gqa_decode: D=%d, only 128 is built", D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0 && Hq / Hkv <= 8, "paged_gqa_decode: Hq=%d Hkv=%d", Hq, Hkv);
+  W4_CHECK_SHAPE(max_context <= max_blocks * ATT_PAGE, "paged_gqa_decode: max_context %d > max_blocks*16",
+                 max_context);
+  if (partition_tokens <= 0) partition_tokens = default_partition(B, Hkv, max_context);
+  W4_CHECK_SHAPE(partition_tokens % ATT_PAGE == 0, "paged_gqa_decode: partition_tokens %% 16 != 0");
+  if (q_stride == 0) q_stride = Hq * D;
+  W4_CHECK_ARG(q_stride >= Hq * D, "paged_gqa_decode: q_stride too small");
+  W4_CHECK_ALIGN(q, 128, "q");
+  W4_CHECK_ALIGN(k_pool, 128, "k_pool");
+  W4_CHECK_ALIGN(v_pool, 128, "v_pool");
+  W4_CHECK_ALIGN(out, 128, "out");
+  W4_CHECK_ARG((q_stride * 2) % 16 == 0, "paged_gqa_decode: q_stride*2 must be a multiple of 16 bytes");
+  const int P = (max_context + partition_tokens - 1) / partition_tokens;
+  AttnArgs a = {};
+  if (P > 1) {
+    const size_t need = attention_workspace_bytes(B, Hq, Hkv, P);
+    W4_CHECK_ARG(workspace != nullptr && workspace_bytes >= need,
+                 "paged_gqa_decode: workspace of %zu bytes needed", need);
+    W4_CHECK_ALIGN(workspace, 128, "workspace");
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    char* w = static_cast<char*>(workspace);
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
+    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+  }
+  a.q = reinterpret_cast<const __half*>(q);
+  a.k_pool = reinterpret_cast<const __half*>(k_pool);
+  a.v_pool = reinterpret_cast<const __half*>(v_pool);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  a.err_flag = err_flag;
+  a.q_stride = q_stride;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.P = P;
+  a.part_tokens = partition_tokens;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  return launch_paged_attention(a, (cudaStream_t)stream);
+}
+
+extern "C" int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v, int row_stride, uint16_t* k_pool,
+                              uint16_t* v_pool, int num_pages, const int32_t* block_table, int max_blocks,
+                              const int32_t* context_lens, int B, int Hq, int Hkv, int D, float theta,
+                              int32_t* err_flag, w4a16_stream_t stream) {
+  W4_CHECK_ARG(q && k && v && k_pool && v_pool && block_table && context_lens, "kv_append_rope: null pointer");
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1, "kv_append_rope: sizes");
+  W4_CHECK_SHAPE(D == ATT_D, "kv_append_rope: D=%d, only 128 is built", D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0, "kv_append_rope: Hq %% Hkv != 0");
+  W4_CHECK_ARG(theta > 0.f, "kv_append_rope: theta must be positive");
+  W4_CHECK_ARG(row_stride >= 0, "kv_append_rope: negative row_stride");
+  W4_CHECK_ALIGN(q, 128, "q");
+  W4_CHECK_ALIGN(k, 128, "k");
+  W4_CHECK_ALIGN(v, 128, "v");
+  W4_CHECK_ALIGN(k_pool, 128, "k_pool");
+  W4_CHECK_ALIGN(v_pool, 128, "v_pool");
+  RopeArgs a = {};
+  a.q = reinterpret_cast<__half*>(q);
+  a.k = reinterpret_cast<__half*>(const_cast<uint16_t*>(k));
+  a.v = reinterpret_cast<const __half*>(v);
+  a.k_pool = reinterpret_cast<__half*>(k_pool);
+  a.v_pool = reinterpret_cast<__half*>(v_pool);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.err_flag = err_flag;
+  a.stride_q = row_stride ? row_stride : Hq * D;
+  a.stride_kv = row_stride ? row_stride : Hkv * D;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  rope_inv_freq_table(theta, D, a.inv_freq);
+  return launch_rope_append(a, (cudaStream_t)stream);
+}

@@ -1,0 +1,183 @@
+// common.cuh -- shared device/host helpers for the sm_103a decode kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "w4a16.h"
+
+namespace w4 {
+
+// ---------------------------------------------------------------------------
+// Host-side status plumbing.  Every entry point returns a status code and
+// leaves a thread-local message for w4a16_last_error().
+// ---------------------------------------------------------------------------
+int set_error(int code, const char* fmt, ...);
+int check_launch(const char* what);
+bool aligned(const void* p, size_t a);
+int num_sms();
+int device_index();
+
+#define W4_CHECK_ARG(cond, ...)                                   \
+  do {                                                            \
+    if (!(cond)) return ::w4::set_error(W4A16_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+#define W4_CHECK_SHAPE(cond, ...)                                 \
+  do {                                                            \
+    if (!(cond)) return ::w4::set_error(W4A16_ERR_SHAPE, __VA_ARGS__); \
+  } while (0)
+#define W4_CHECK_ALIGN(p, a, name)                                \
+  do {                                                            \
+    if ((p) != nullptr && !::w4::aligned((p), (a)))               \
+      return ::w4::set_error(W4A16_ERR_ALIGNMENT, "%s must be %d-byte aligned", name, (int)(a)); \
+  } while (0)
+
+// Launch with programmatic dependent launch (PDL) enabled, so the next
+// kernel in the stream may start its prologue while this one drains.
+template <typename Kern, typename... Args>
+inline cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers (inline PTX for sm_100+ features).
+// ---------------------------------------------------------------------------
+
+// PDL: let dependents launch / wait for the grids this one depends on.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 128-bit streaming load that bypasses L1 (weights are read exactly once).
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// (a & b) | c in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// acc += lo(a)*lo(b) + hi(a)*hi(b) with fp16 operands and fp32 accumulation
+// (mixed-precision FMA, exact products).  Two chained FMAs into one sum.
+__device__ __forceinline__ void fma2_f16_f32(float& acc, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\t"
+      "mov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+      "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+}
+
+// Two independent accumulators: acc0 += lo*lo, acc1 += hi*hi.
+__device__ __forceinline__ void fma2_f16_f32_split(float& acc0, float& acc1, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+      "fma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(a), "r"(b));
+}
+
+// Packed fp32 FMA (two lanes per instruction): d = a*b + c elementwise.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk copy (TMA) helpers.  All waits are bounded: a wait
+// that runs out sets *timed_out and returns false instead of spinning.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~max_iters polls (each try_wait itself
+// suspends for a hardware-defined interval).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t max_iters) {
+  for (uint32_t i = 0; i < max_iters; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
+// 1-D bulk async copy global -> shared, completion signalled on `bar`.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace w4

@@ -1,0 +1,85 @@
+// kernels.h -- internal launch interfaces shared by the C-ABI files and the
+// model runtime (not part of the public ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4 {
+
+// One weight matrix (or a row range of the logical output) of a GEMV.
+struct GemvSeg {
+  const uint32_t* qw;   // packed int4 [rows][K/8]
+  const __half* s;      // scales [rows][K/128]
+  const __half* bias;   // [rows] or null
+  int rows;
+};
+
+struct GemvArgs {
+  const __half* x;         // [M][K]
+  const __half* gamma;     // optional fused RMSNorm weight [K]
+  const __half* residual;  // optional [M][N]
+  __half* y;               // [M][N]
+  GemvSeg seg[3];          // rows of seg 0, then seg 1, ... (SiLU mode: gate, up)
+  int nseg;
+  int M, K, N;
+  float eps;
+};
+
+int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s);
+int gemv_cuda_core_supported(int M, int K);
+
+// Paged attention (+ fused split-K combine).
+struct AttnArgs {
+  const __half* q;          // [B][Hq][D] with row pitch q_stride
+  const __half* k_pool;     // [pages][Hkv][16][D]
+  const __half* v_pool;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  __half* out;              // [B][Hq][D]
+  float* ws_o;              // [B][Hq][P][D]
+  float* ws_ml;             // [B][Hq][P][2]
+  unsigned int* counters;   // [B][Hkv]
+  int32_t* err_flag;
+  int q_stride, num_pages, max_blocks, B, Hq, Hkv, P, part_tokens;
+  float scale_log2;         // sm_scale * log2(e)
+};
+int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
+size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P);
+
+// RoPE + KV append.
+struct RopeArgs {
+  __half* q;                // [B][Hq][D] pitch stride
+  __half* k;                // [B][Hkv][D] pitch stride (rotated in place too)
+  const __half* v;
+  __half* k_pool;
+  __half* v_pool;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  int32_t* err_flag;
+  int stride_q, stride_kv, num_pages, max_blocks, B, Hq, Hkv;
+  float inv_freq[64];       // fp32 inverse frequencies, D = 128
+};
+int launch_rope_append(const RopeArgs& a, cudaStream_t s);
+void rope_inv_freq_table(float theta, int D, float* out);
+
+int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s);
+int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
+                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s);
+
+struct LmHeadArgs {
+  const __half* x;      // [B][H]
+  const __half* w;      // [vocab][H]
+  __half* logits;       // [B][vocab] or null
+  int32_t* tokens_out;  // [B]
+  unsigned long long* partial;  // [B][blocks] packed (key, index)
+  unsigned int* counters;       // [B]
+  int B, H, vocab;
+  const __half* gamma;  // optional fused final RMSNorm
+  float eps;
+};
+int launch_lm_head_argmax(const LmHeadArgs& a, cudaStream_t s);
+size_t lm_head_workspace_bytes(int B, int vocab);
+
+}  // namespace w4

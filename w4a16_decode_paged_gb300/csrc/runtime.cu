@@ -1,0 +1,349 @@
+// runtime.cu -- the whole-model decode step: static arena, layer sequence,
+// CUDA-graph capture and replay.
+//
+// "Building a Custom LLM Inference Runtime on H100" (explore.n1n.ai) names
+// the pieces: pre-allocate the KV cache and activation buffers so nothing
+// calls cudaMalloc while decoding ("Implementation Guide", step 2), capture
+// the kernel sequence into a CUDA graph to remove per-launch CPU overhead
+// ("3. CUDA Graph Capture"), and keep every asynchronous operation ordered
+// inside the capture ("Bug 3").  The aikraft.ru article ("Ключевые метрики
+// производительности") reports the graph-captured decode as the steady state.
+//
+// One decode step = embedding (+ device-side context_lens advance), then per
+// layer: [RMSNorm + q|k|v GEMV + bias] -> [RoPE + KV append] -> [paged GQA
+// attention + split-K combine] -> [o GEMV + residual] -> [RMSNorm + gate|up
+// GEMV + SiLU-mul] -> [down GEMV + residual], then [final RMSNorm + lm_head +
+// argmax].  Every kernel is launched with programmatic dependent launch, so
+// a GEMV streams its first weights while its predecessor finishes.
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4 {
+int default_partition(int B, int Hkv, int max_context);
+}
+
+using namespace w4;
+
+struct GraphKey {
+  int B, max_blocks;
+  const void *tin, *tout, *bt, *lens, *logits;
+  bool operator<(const GraphKey& o) const {
+    return std::tie(B, max_blocks, tin, tout, bt, lens, logits) <
+           std::tie(o.B, o.max_blocks, o.tin, o.tout, o.bt, o.lens, o.logits);
+  }
+};
+
+struct w4a16_model {
+  w4a16_model_config cfg;
+  std::vector<w4a16_layer_weights> layers;
+  const __half *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  int max_batch = 0, max_context = 0, part_tokens = 0, P = 0;
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  __half *x = nullptr, *qkv = nullptr, *att = nullptr, *h = nullptr, *mlp = nullptr;
+  void* attn_ws = nullptr;
+  size_t attn_ws_bytes = 0;
+  void* lm_ws = nullptr;
+  size_t lm_ws_bytes = 0;
+  int32_t* err_flag = nullptr;
+  float inv_freq[64];
+  cudaStream_t cap_stream = nullptr;
+  std::mutex mu;
+  std::map<GraphKey, cudaGraphExec_t> graphs;
+};
+
+static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
+                                  int max_context, w4a16_model** out) {
+  W4_CHECK_ARG(cfg && w && out, "model_create: null argument");
+  *out = nullptr;
+  const w4a16_model_config& c = *cfg;
+  W4_CHECK_ARG(c.hidden > 0 && c.n_q_heads > 0 && c.n_kv_heads > 0 && c.inter > 0 && c.n_layers >= 0,
+               "model_create: bad sizes");
+  W4_CHECK_SHAPE(c.head_dim == 128, "model_create: head_dim must be 128");
+  W4_CHECK_SHAPE(c.hidden % 128 == 0 && c.inter % 128 == 0 && (c.n_q_heads * c.head_dim) % 128 == 0,
+                 "model_create: hidden, inter and Hq*D must be multiples of 128");
+  W4_CHECK_SHAPE(c.n_q_heads % c.n_kv_heads == 0, "model_create: Hq %% Hkv != 0");
+  W4_CHECK_ARG(max_batch >= 1 && max_context >= 1 && c.num_pages >= 1, "model_create: bad limits");
+  W4_CHECK_ARG(c.n_layers == 0 || w->layers != nullptr, "model_create: null layer array");
+  W4_CHECK_SHAPE(c.partition_tokens % 16 == 0 && c.partition_tokens >= 0, "model_create: partition_tokens");
+  const int maxK = std::max(std::max(c.hidden, c.inter), c.n_q_heads * c.head_dim);
+  W4_CHECK_SHAPE(gemv_cuda_core_supported(max_batch, maxK),
+                 "model_create: max_batch=%d with K=%d is outside the built GEMV paths", max_batch, maxK);
+
+  w4a16_model* m = new w4a16_model();
+  m->cfg = c;
+  m->layers.assign(w->layers, w->layers + c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const w4a16_layer_weights& L = m->layers[l];
+    if (!(L.ln1 && L.ln2 && L.wq && L.wk && L.wv && L.wo && L.wg && L.wu && L.wd && L.sq && L.sk && L.sv && L.so &&
+          L.sg && L.su && L.sd && L.k_pool && L.v_pool)) {
+      delete m;
+      return set_error(W4A16_ERR_INVALID_ARG, "model_create: layer %d has a null weight", l);
+    }
+  }
+  m->embed = reinterpret_cast<const __half*>(w->embed);
+  m->final_norm = reinterpret_cast<const __half*>(w->final_norm);
+  m->lm_head = reinterpret_cast<const __half*>(w->lm_head);
+  m->max_batch = max_batch;
+  m->max_context = max_context;
+  m->part_tokens = c.partition_tokens > 0 ? c.partition_tokens : default_partition(max_batch, c.n_kv_heads, max_context);
+  m->P = (max_context + m->part_tokens - 1) / m->part_tokens;
+  rope_inv_freq_table(c.theta, c.head_dim, m->inv_freq);
+
+  const int D = c.head_dim;
+  const size_t nqkv = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * D;
+  size_t off = 0;
+  const size_t o_x = off; off += up256((size_t)max_batch * c.hidden * 2);
+  const size_t o_qkv = off; off += up256((size_t)max_batch * nqkv * 2);
+  const size_t o_att = off; off += up256((size_t)max_batch * c.n_q_heads * D * 2);
+  const size_t o_h = off; off += up256((size_t)max_batch * c.hidden * 2);
+  const size_t o_mlp = off; off += up256((size_t)max_batch * c.inter * 2);
+  m->attn_ws_bytes = attention_workspace_bytes(max_batch, c.n_q_heads, c.n_kv_heads, m->P);
+  const size_t o_aws = off; off += up256(m->attn_ws_bytes);
+  m->lm_ws_bytes = lm_head_workspace_bytes(max_batch, c.vocab);
+  const size_t o_lws = off; off += up256(m->lm_ws_bytes);
+  const size_t o_err = off; off += 256;
+  m->arena_bytes = off;
+  cudaError_t e = cudaMalloc(&m->arena, off);
+  if (e != cudaSuccess) {
+    delete m;
+    return set_error(W4A16_ERR_CUDA, "model_create: arena of %zu bytes: %s", off, cudaGetErrorString(e));
+  }
+  cudaMemset(m->arena, 0, off);
+  m->x = reinterpret_cast<__half*>(m->arena + o_x);
+  m->qkv = reinterpret_cast<__half*>(m->arena + o_qkv);
+  m->att = reinterpret_cast<__half*>(m->arena + o_att);
+  m->h = reinterpret_cast<__half*>(m->arena + o_h);
+  m->mlp = reinterpret_cast<__half*>(m->arena + o_mlp);
+  m->attn_ws = m->arena + o_aws;
+  m->lm_ws = m->arena + o_lws;
+  m->err_flag = reinterpret_cast<int32_t*>(m->arena + o_err);
+  e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(m->arena);
+    delete m;
+    return set_error(W4A16_ERR_CUDA, "model_create: %s", cudaGetErrorString(e));
+  }
+  *out = m;
+  return W4A16_OK;
+}
+
+extern "C" void w4a16_model_destroy(w4a16_model* m) {
+  if (!m) return;
+  for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  if (m->arena) cudaFree(m->arena);
+  delete m;
+}
+
+extern "C" int32_t* w4a16_model_err_flag(w4a16_model* m) { return m ? m->err_flag : nullptr; }
+
+extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
+  W4_CHECK_ARG(m, "model_check_errors: null model");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cst) == cudaSuccess && cst != cudaStreamCaptureStatusNone)
+    return set_error(W4A16_ERR_CAPTURE, "model_check_errors: stream is capturing");
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, m->err_flag, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->err_flag, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "model_check_errors: %s", cudaGetErrorString(e));
+  if (host & 2) return set_error(W4A16_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", host);
+  if (host & 1) return set_error(W4A16_ERR_DEVICE_BOUNDS, "a kernel skipped an out-of-range index (flag 0x%x)", host);
+  return W4A16_OK;
+}
+
+static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int max_blocks, const int32_t* lens, int B,
+                     cudaStream_t s) {
+  const w4a16_model_config& c = m->cfg;
+  const w4a16_layer_weights& L = m->layers[l];
+  const int D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, H = c.hidden, I = c.inter;
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  auto hp = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
+  int rc;
+
+  GemvArgs g = {};
+  g.x = x;
+  g.gamma = hp(L.ln1);
+  g.eps = c.eps;
+  g.y = m->qkv;
+  g.seg[0] = {L.wq, hp(L.sq), hp(L.bq), Hq * D};
+  g.seg[1] = {L.wk, hp(L.sk), hp(L.bk), Hkv * D};
+  g.seg[2] = {L.wv, hp(L.sv), hp(L.bv), Hkv * D};
+  g.nseg = 3;
+  g.M = B;
+  g.K = H;
+  g.N = nqkv;
+  if ((rc = launch_gemv(g, false, s))) return rc;
+
+  RopeArgs r = {};
+  r.q = m->qkv;
+  r.k = m->qkv + Hq * D;
+  r.v = m->qkv + (Hq + Hkv) * D;
+  r.k_pool = reinterpret_cast<__half*>(L.k_pool);
+  r.v_pool = reinterpret_cast<__half*>(L.v_pool);
+  r.block_table = bt;
+  r.context_lens = lens;
+  r.err_flag = m->err_flag;
+  r.stride_q = r.stride_kv = nqkv;
+  r.num_pages = c.num_pages;
+  r.max_blocks = max_blocks;
+  r.B = B;
+  r.Hq = Hq;
+  r.Hkv = Hkv;
+  std::memcpy(r.inv_freq, m->inv_freq, sizeof(r.inv_freq));
+  if ((rc = launch_rope_append(r, s))) return rc;
+
+  AttnArgs a = {};
+  a.q = m->qkv;
+  a.q_stride = nqkv;
+  a.k_pool = reinterpret_cast<const __half*>(L.k_pool);
+  a.v_pool = reinterpret_cast<const __half*>(L.v_pool);
+  a.block_table = bt;
+  a.context_lens = lens;
+  a.out = m->att;
+  char* ws = static_cast<char*>(m->attn_ws);
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(ws + up256((size_t)m->max_batch * Hq * m->P * D * 4));
+  a.counters = reinterpret_cast<unsigned int*>(ws + up256((size_t)m->max_batch * Hq * m->P * D * 4) +
+                                               up256((size_t)m->max_batch * Hq * m->P * 2 * 4));
+  a.err_flag = m->err_flag;
+  a.num_pages = c.num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.P = m->P;
+  a.part_tokens = m->part_tokens;
+  a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+  if ((rc = launch_paged_attention(a, s))) return rc;
+
+  GemvArgs o = {};
+  o.x = m->att;
+  o.residual = x;
+  o.y = m->h;
+  o.seg[0] = {L.wo, hp(L.so), nullptr, H};
+  o.nseg = 1;
+  o.M = B;
+  o.K = Hq * D;
+  o.N = H;
+  if ((rc = launch_gemv(o, false, s))) return rc;
+
+  GemvArgs gu = {};
+  gu.x = m->h;
+  gu.gamma = hp(L.ln2);
+  gu.eps = c.eps;
+  gu.y = m->mlp;
+  gu.seg[0] = {L.wg, hp(L.sg), nullptr, I};
+  gu.seg[1] = {L.wu, hp(L.su), nullptr, I};
+  gu.nseg = 2;
+  gu.M = B;
+  gu.K = H;
+  gu.N = I;
+  if ((rc = launch_gemv(gu, true, s))) return rc;
+
+  GemvArgs dn = {};
+  dn.x = m->mlp;
+  dn.residual = m->h;
+  dn.y = x;
+  dn.seg[0] = {L.wd, hp(L.sd), nullptr, H};
+  dn.nseg = 1;
+  dn.M = B;
+  dn.K = I;
+  dn.N = H;
+  return launch_gemv(dn, false, s);
+}
+
+extern "C" int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table, int max_blocks,
+                                 const int32_t* context_lens, int B, w4a16_stream_t stream) {
+  W4_CHECK_ARG(m && x && block_table && context_lens, "model_layer: null argument");
+  W4_CHECK_ARG(layer >= 0 && layer < m->cfg.n_layers, "model_layer: layer %d out of range", layer);
+  W4_CHECK_ARG(B >= 1 && B <= m->max_batch && max_blocks >= 1, "model_layer: B=%d (max %d)", B, m->max_batch);
+  W4_CHECK_ALIGN(x, 128, "x");
+  return run_layer(m, layer, reinterpret_cast<__half*>(x), block_table, max_blocks, context_lens, B,
+                   (cudaStream_t)stream);
+}
+
+static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const int32_t* bt, int max_blocks,
+                        int32_t* lens, int B, uint16_t* logits, cudaStream_t s) {
+  const w4a16_model_config& c = m->cfg;
+  int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, s);
+  if (rc) return rc;
+  for (int l = 0; l < c.n_layers; ++l)
+    if ((rc = run_layer(m, l, m->x, bt, max_blocks, lens, B, s))) return rc;
+  LmHeadArgs a = {};
+  a.x = m->x;
+  a.w = m->lm_head;
+  a.gamma = m->final_norm;
+  a.eps = c.eps;
+  a.logits = reinterpret_cast<__half*>(logits);
+  a.tokens_out = tout;
+  a.partial = reinterpret_cast<unsigned long long*>(m->lm_ws);
+  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(m->lm_ws) + (size_t)4 * 4096 * 8);
+  a.B = B;
+  a.H = c.hidden;
+  a.vocab = c.vocab;
+  return launch_lm_head_argmax(a, s);
+}
+
+extern "C" int decode_step_kernel_count(w4a16_model* m, int B) {
+  (void)B;
+  return m ? 2 + 6 * m->cfg.n_layers : 0;
+}
+
+extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tokens_out, const int32_t* block_table,
+                           int max_blocks, int32_t* context_lens, int B, uint16_t* logits, int use_graph,
+                           w4a16_stream_t stream) {
+  W4_CHECK_ARG(m && tokens_in && tokens_out && block_table && context_lens, "decode_step: null argument");
+  W4_CHECK_ARG(m->embed && m->final_norm && m->lm_head && m->cfg.vocab > 0, "decode_step: model has no lm_head");
+  W4_CHECK_ARG(B >= 1 && B <= m->max_batch && max_blocks >= 1, "decode_step: B=%d (max %d)", B, m->max_batch);
+  W4_CHECK_SHAPE(B <= 4, "decode_step: B=%d > 4 needs the batched lm_head", B);
+  W4_CHECK_ALIGN(logits, 128, "logits");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!use_graph) return enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, s);
+
+  cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+  if (s != nullptr && cudaStreamIsCapturing(s, &cst) == cudaSuccess && cst == cudaStreamCaptureStatusActive) {
+    // The caller is capturing already: record the kernels into their graph.
+    return enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, s);
+  }
+  GraphKey key{B, max_blocks, tokens_in, tokens_out, block_table, context_lens, logits};
+  cudaGraphExec_t exec = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(m->mu);
+    auto it = m->graphs.find(key);
+    if (it != m->graphs.end()) exec = it->second;
+  }
+  if (!exec) {
+    // Capture on the model's private stream (the legacy default stream cannot
+    // capture); nothing but kernel launches is recorded.
+    cudaError_t e = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) return set_error(W4A16_ERR_CAPTURE, "decode_step: begin capture: %s", cudaGetErrorString(e));
+    int rc = enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, m->cap_stream);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(m->cap_stream, &graph);
+    if (rc != W4A16_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) return set_error(W4A16_ERR_CAPTURE, "decode_step: end capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "decode_step: instantiate: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lk(m->mu);
+    m->graphs[key] = exec;
+  }
+  cudaError_t e = cudaGraphLaunch(exec, s);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "decode_step: graph launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
