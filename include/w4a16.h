@@ -255,6 +255,11 @@ W4A16_API int32_t* w4a16_model_err_flag(w4a16_model* m);
  * stream is capturing. */
 W4A16_API int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream);
 
+/* Copy the final hidden states (before the final RMSNorm) that the last
+ * decode_step left in the model's arena into dst fp16 [B][hidden]
+ * (enqueued on `stream`; capture-safe). */
+W4A16_API int w4a16_model_hidden(w4a16_model* m, uint16_t* dst, int B, w4a16_stream_t stream);
+
 /* One decoder layer on hidden states x fp16 [B][hidden] (in place), with
  * context_lens already counting the appended token. */
 W4A16_API int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table,

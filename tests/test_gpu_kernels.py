@@ -129,10 +129,10 @@ def test_kv_append_rope_placement_bit_exact(api, Hq, Hkv, fused):
         kd = rd[:, Hq * D:(Hq + Hkv) * D]
         vd = rd[:, (Hq + Hkv) * D:]
         from w4a16_decode_paged_gb300._lib import check, load
+        btd, ld = to_dev(bt, torch), to_dev(lens, torch)  # kept alive until the launch is enqueued
         check(load().kv_append_rope(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), row.shape[1], kpd.data_ptr(),
-                                    vpd.data_ptr(), pages, to_dev(bt, torch).data_ptr(), bt.shape[1],
-                                    to_dev(lens, torch).data_ptr(), B, Hq, Hkv, D, theta, None,
-                                    torch.cuda.current_stream().cuda_stream))
+                                    vpd.data_ptr(), pages, btd.data_ptr(), bt.shape[1], ld.data_ptr(), B, Hq,
+                                    Hkv, D, theta, None, torch.cuda.current_stream().cuda_stream))
         torch.cuda.synchronize()
         q_got = to_host(rd)[:, :Hq * D].reshape(B, Hq, D)
     else:

@@ -205,6 +205,13 @@ class Model:
     def err_flag_ptr(self) -> int:
         return int(self._lib.w4a16_model_err_flag(self._h) or 0)
 
+    def hidden(self, B=1, out=None, stream=None):
+        """Final hidden states (pre final-norm) of the last decode step."""
+        if out is None:
+            out = torch.empty((B, self.cfg["hidden"]), dtype=torch.float16, device="cuda")
+        check(self._lib.w4a16_model_hidden(self._h, _p(out), int(B), stream_handle(stream)))
+        return out
+
     def check_errors(self, stream=None) -> int:
         """Status code of the device error word (blocks; clears the word)."""
         return int(self._lib.w4a16_model_check_errors(self._h, stream_handle(stream)))

@@ -14,11 +14,13 @@
 //   (w      & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u1, 1024 + 16 u5}
 //   (w >> 8 & 0x000F000F) | 0x64006400 = half2{1024 + u2, 1024 + u6}
 //   (w >> 8 & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u3, 1024 + 16 u7}
-// The activations are staged once per CTA in shared memory in the matching
-// order, with the odd-nibble ones pre-divided by 16 (exact), so that
-//   sum_i h_i * x'_i = sum_i q_i x_i + C,   C = 1032 sum_even x + 72 sum_odd x
-// and C (one fp32 per 32 weights, shared by every row) is subtracted once.
-// That leaves one shift, four LOP3 and eight FMAs per 8 weights.
+// One HSUB2 each turns these into exact codes: minus 1032 gives q for the
+// even nibbles, minus 1152 gives 16 q for the odd ones.  The activations are
+// staged once per CTA in shared memory in the matching order, with the
+// odd-nibble ones pre-divided by 16 (exact), so every product (16 q)(x / 16)
+// is exact in fp32.  That is one shift, four LOP3, four HSUB2 and eight FMAs
+// per 8 weights.  (Folding the 1032 offset into the sum instead would save
+// the HSUB2s but costs about eight bits of the fp32 sum when |x| is large.)
 //
 // Work split: LPR lanes cooperate on one weight row (LPR = 16 when K/32 is a
 // multiple of 16, else 8 or 4); a warp covers 32/LPR rows at a time; each
@@ -43,13 +45,14 @@ template <int LPR, int MT, bool SILU>
 __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int RPW = 32 / LPR;               // row slots per warp
   constexpr int RPT = SILU ? RPW / 2 : RPW;   // output rows per warp task
-  constexpr uint32_t MAGIC = 0x64006400u;
+  constexpr uint32_t MAGIC = 0x64006400u;     // half2{1024, 1024}
+  constexpr uint32_t EVEN_OFF = 0x64086408u;  // half2{1032, 1032}
+  constexpr uint32_t ODD_OFF = 0x64806480u;   // half2{1152, 1152}
   extern __shared__ uint4 smem[];
   const int K = a.K, M = a.M;
   const int NCH = K >> 5;      // 32-weight chunks per row
   const int NIT = NCH / LPR;   // chunks per lane per row
-  uint4* xs = smem;                                                // [MT][4][NCH]
-  float* cs = reinterpret_cast<float*>(smem + (size_t)MT * 4 * NCH); // [MT][NCH]
+  uint4* xs = smem;  // [MT][4][NCH]
   __shared__ float red[GEMV_WPB][MT];
   __shared__ float rscale[MT];
 
@@ -138,7 +141,6 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
   for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
     const int m = idx / NCH, j = idx - m * NCH;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
-    float csum = 0.f;
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       uint4 raw = src[wi];
@@ -151,19 +153,13 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
       }
-      __half b1 = __hmul(h[1], sixteenth), b5 = __hmul(h[5], sixteenth);
-      __half b3 = __hmul(h[3], sixteenth), b7 = __hmul(h[7], sixteenth);
       uint4 o;
       o.x = pack_h2(h[0], h[4]);
-      o.y = pack_h2(b1, b5);
+      o.y = pack_h2(__hmul(h[1], sixteenth), __hmul(h[5], sixteenth));
       o.z = pack_h2(h[2], h[6]);
-      o.w = pack_h2(b3, b7);
+      o.w = pack_h2(__hmul(h[3], sixteenth), __hmul(h[7], sixteenth));
       xs[(size_t)(m * 4 + wi) * NCH + j] = o;
-      float ev = __half2float(h[0]) + __half2float(h[4]) + __half2float(h[2]) + __half2float(h[6]);
-      float od = __half2float(b1) + __half2float(b5) + __half2float(b3) + __half2float(b7);
-      csum += 1032.0f * ev + 72.0f * 16.0f * od;
     }
-    cs[(size_t)m * NCH + j] = csum;
   }
   __syncthreads();
 
@@ -204,16 +200,16 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               if (m < M) {
-                float p0 = -cs[(size_t)m * NCH + j], p1 = 0.f;
+                float p0 = 0.f, p1 = 0.f;
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
                   const uint32_t w = wv[wi];
                   const uint32_t w8 = w >> 8;
                   const uint4 xv = xs[(size_t)(m * 4 + wi) * NCH + j];
-                  fma2_f16_f32_split(p0, p1, and_or(w, 0x000F000Fu, MAGIC), xv.x);
-                  fma2_f16_f32_split(p0, p1, and_or(w, 0x00F000F0u, MAGIC), xv.y);
-                  fma2_f16_f32_split(p0, p1, and_or(w8, 0x000F000Fu, MAGIC), xv.z);
-                  fma2_f16_f32_split(p0, p1, and_or(w8, 0x00F000F0u, MAGIC), xv.w);
+                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w, 0x000F000Fu, MAGIC), EVEN_OFF), xv.x);
+                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w, 0x00F000F0u, MAGIC), ODD_OFF), xv.y);
+                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w8, 0x000F000Fu, MAGIC), EVEN_OFF), xv.z);
+                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w8, 0x00F000F0u, MAGIC), ODD_OFF), xv.w);
                 }
                 acc[m] = fmaf(p0 + p1, s, acc[m]);
               }
@@ -234,9 +230,11 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
       for (int m = 0; m < MT; ++m) {
         const float other = __shfl_xor_sync(0xffffffffu, acc[m], 16);
         if (m < M && valid && lr == 0 && slot < RPT) {
-          const float g = acc[m];
+          // gate and up are rounded to fp16 like two separate GEMV outputs
+          const float g = __half2float(__float2half_rn(acc[m]));
+          const float u = __half2float(__float2half_rn(other));
           const float silu = g / (1.0f + expf(-g));
-          a.y[(size_t)m * a.N + out_row] = __float2half_rn(silu * other);
+          a.y[(size_t)m * a.N + out_row] = __float2half_rn(silu * u);
         }
       }
     } else if (valid && lr == 0) {
@@ -275,7 +273,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 template <int LPR, int MT, bool SILU>
 static int launch_one(const GemvArgs& a, cudaStream_t s) {
   auto kern = gemv_w4a16_kernel<LPR, MT, SILU>;
-  const size_t smem = (size_t)MT * a.K * 2 + (size_t)MT * (a.K / 32) * 4;
+  const size_t smem = (size_t)MT * a.K * 2;
   static int configured = 0;
   static int blocks_per_sm = 0;
   if (!configured) {

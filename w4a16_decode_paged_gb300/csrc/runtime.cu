@@ -147,6 +147,15 @@ extern "C" void w4a16_model_destroy(w4a16_model* m) {
 
 extern "C" int32_t* w4a16_model_err_flag(w4a16_model* m) { return m ? m->err_flag : nullptr; }
 
+extern "C" int w4a16_model_hidden(w4a16_model* m, uint16_t* dst, int B, w4a16_stream_t stream) {
+  W4_CHECK_ARG(m && dst, "model_hidden: null argument");
+  W4_CHECK_ARG(B >= 1 && B <= m->max_batch, "model_hidden: B=%d", B);
+  cudaError_t e = cudaMemcpyAsync(dst, m->x, (size_t)B * m->cfg.hidden * 2, cudaMemcpyDeviceToDevice,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "model_hidden: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
 extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
   W4_CHECK_ARG(m, "model_check_errors: null model");
   cudaStream_t s = (cudaStream_t)stream;

@@ -6,8 +6,13 @@ dequantisation, no norms, no attention).  Both the CUDA path and the CPU
 oracle receive the arrays it returns.
 
 Distributions (the pages give none; these follow the workload descriptions):
-  * packed int4 weights: uniform random uint32 words (every nibble, hence
-    every code in [-8, 7], equally likely), layout [N][K/8];
+  * packed int4 weights, layout [N][K/8], one of two code distributions:
+      - "full": uniform random uint32 words, so every nibble, hence every
+        code in [-8, 7], is equally likely (the single-layer workloads);
+      - "symmetric": codes uniform on [-7, 7], what a symmetric quantiser
+        with scale amax/7 emits (the multi-layer model workloads: the
+        [-8, 7] codes have mean -1/2, which adds the same offset to every
+        GEMV output and overflows fp16 after a few random layers);
   * group scales: fp16, uniform in [0.005, 0.02], layout [N][K/128];
   * activations, embeddings, KV pages: fp16 N(0, 1);
   * RMSNorm gammas: fp16 1 + 0.1 N(0, 1);
@@ -32,10 +37,11 @@ QWEN_LAYER = dict(name="qwen2.5-7b-layer-b1-ctx512", hidden=3584, n_q_heads=28, 
                   context=512, pool_pages=4096, bias=True, seed=1001)
 QWEN_MODEL = dict(name="qwen2.5-7b-28L-b1-ctx512", hidden=3584, n_q_heads=28, n_kv_heads=4,
                   head_dim=128, inter=18944, n_layers=28, vocab=152064, eps=1e-6, theta=1e6, batch=1,
-                  context=512, gen_tokens=128, bias=True, seed=1002)
+                  context=512, gen_tokens=128, bias=True, codes="symmetric", seed=1002)
 QWEN_BATCHED = dict(name="qwen2.5-7b-28L-b32-ctxU1..4096", hidden=3584, n_q_heads=28, n_kv_heads=4,
                     head_dim=128, inter=18944, n_layers=28, vocab=152064, eps=1e-6, theta=1e6, batch=32,
-                    max_context=4096, forced_lens=(15, 16, 17), pool_pages=16384, bias=True, seed=1003)
+                    max_context=4096, forced_lens=(15, 16, 17), pool_pages=16384, bias=True, codes="symmetric",
+                    seed=1003)
 QWEN_LONG = dict(name="qwen2.5-7b-layer-b4-ctx32768", hidden=3584, n_q_heads=28, n_kv_heads=4,
                  head_dim=128, inter=18944, n_layers=1, vocab=0, eps=1e-6, theta=1e6, batch=4,
                  context=32768, pool_pages=16384, partition_tokens=512, bias=True, seed=1004)
@@ -45,10 +51,20 @@ def rng(seed: int) -> np.random.Generator:
     return np.random.default_rng(seed)
 
 
-def int4_weight(r: np.random.Generator, N: int, K: int):
+# The 225 byte values whose two nibbles are both non-zero (no code -8).
+_BYTES_NO_ZERO_NIBBLE = np.array([b for b in range(256) if (b & 0xF) and (b >> 4)], dtype=np.uint8)
+
+
+def int4_weight(r: np.random.Generator, N: int, K: int, codes: str = "full"):
     """(qweight uint32 [N][K/8], scales fp16 [N][K/128])."""
     assert K % GROUP == 0
-    qw = r.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    if codes == "full":
+        qw = r.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    elif codes == "symmetric":
+        idx = r.integers(0, len(_BYTES_NO_ZERO_NIBBLE), size=(N, K // 2), dtype=np.uint8)
+        qw = np.ascontiguousarray(_BYTES_NO_ZERO_NIBBLE[idx]).view("<u4").reshape(N, K // 8)
+    else:
+        raise ValueError(codes)
     s = r.uniform(0.005, 0.02, size=(N, K // GROUP)).astype(np.float16)
     return qw, s
 
@@ -64,9 +80,10 @@ def gamma(r: np.random.Generator, H: int):
 def layer_weights(r: np.random.Generator, cfg: dict) -> dict:
     H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
     w = {"ln1": gamma(r, H), "ln2": gamma(r, H)}
+    codes = cfg.get("codes", "full")
     for name, N, K in (("q", Hq * D, H), ("k", Hkv * D, H), ("v", Hkv * D, H), ("o", H, Hq * D),
                        ("g", I, H), ("u", I, H), ("d", H, I)):
-        w["w" + name], w["s" + name] = int4_weight(r, N, K)
+        w["w" + name], w["s" + name] = int4_weight(r, N, K, codes)
     if cfg.get("bias", False):
         w["bq"] = normal_fp16(r, (Hq * D,), 0.1)
         w["bk"] = normal_fp16(r, (Hkv * D,), 0.1)
