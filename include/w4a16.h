@@ -182,6 +182,33 @@ W4A16_API size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max
  * paged_gqa_decode (a multiple of 16; depends on the SM count). */
 W4A16_API int paged_gqa_decode_default_partition(int B, int Hkv, int max_context);
 
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode_noalloc -- the same attention as paged_gqa_decode, for
+ * callers that cannot allocate device memory: a plugin handed only input
+ * and output pointers by a host framework that owns the device's memory
+ * pool, or code running while allocation is forbidden (inside a global-mode
+ * stream capture, where cudaMalloc is illegal).  Nothing is allocated: the
+ * split-K partials and ticket counters live in one static device array of
+ * W4A16_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds
+ * until the process exits.  The pages describe no such call; it has no
+ * counterpart there.
+ *   Arguments as for paged_gqa_decode, minus the workspace.
+ *   Sizes whose partials need more than W4A16_NOALLOC_SCRATCH_BYTES return
+ *   W4A16_ERR_SHAPE (need = paged_gqa_decode_workspace_size()).
+ *   The first call on each device looks the array's device address up (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call zeroes the counters it uses on `stream` before launching.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other threads) race and must be serialised by the caller.
+ * ------------------------------------------------------------------------ */
+#define W4A16_NOALLOC_SCRATCH_BYTES (4u << 20)
+W4A16_API int paged_gqa_decode_noalloc(const uint16_t* q, int q_stride, const uint16_t* k_pool,
+                                       const uint16_t* v_pool, int num_pages,
+                                       const int32_t* block_table, int max_blocks,
+                                       const int32_t* context_lens, int max_context, int B, int Hq,
+                                       int Hkv, int D, float sm_scale, int partition_tokens,
+                                       uint16_t* out, int32_t* err_flag, w4a16_stream_t stream);
+
 /* Zero a workspace once before first use (enqueued on `stream`). */
 W4A16_API int w4a16_workspace_clear(void* workspace, size_t bytes, w4a16_stream_t stream);
 

@@ -22,6 +22,7 @@
 // (an atomic ticket, no spin) merges them and writes the output.
 #include <cmath>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -558,4 +559,93 @@ extern "C" int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v,
   a.Hkv = Hkv;
   rope_inv_freq_table(theta, D, a.inv_freq);
   return launch_rope_append(a, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the split-K scratch is a static device array.
+// In host code `g_noalloc_scratch` names a host-side stand-in, not device
+// memory, so its device address is looked up once per device and passed to
+// the kernel like any workspace pointer.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[W4A16_NOALLOC_SCRATCH_BYTES];
+
+static int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "paged_gqa_decode_noalloc: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return set_error(W4A16_ERR_INVALID_ARG, "paged_gqa_decode_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return set_error(W4A16_ERR_CUDA, "paged_gqa_decode_noalloc: scratch address lookup: %s", cudaGetErrorString(e));
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return W4A16_OK;
+}
+
+extern "C" int paged_gqa_decode_noalloc(const uint16_t* q, int q_stride, const uint16_t* k_pool,
+                                        const uint16_t* v_pool, int num_pages, const int32_t* block_table,
+                                        int max_blocks, const int32_t* context_lens, int max_context, int B, int Hq,
+                                        int Hkv, int D, float sm_scale, int partition_tokens, uint16_t* out,
+                                        int32_t* err_flag, w4a16_stream_t stream) {
+  W4_CHECK_ARG(q && k_pool && v_pool && block_table && context_lens && out,
+               "paged_gqa_decode_noalloc: null tensor pointer");
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1 && max_context >= 1,
+               "paged_gqa_decode_noalloc: sizes must be positive");
+  W4_CHECK_SHAPE(D == ATT_D, "paged_gqa_decode_noalloc: D=%d, only 128 is built", D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0 && Hq / Hkv <= 8, "paged_gqa_decode_noalloc: Hq=%d Hkv=%d", Hq, Hkv);
+  W4_CHECK_SHAPE(max_context <= max_blocks * ATT_PAGE, "paged_gqa_decode_noalloc: max_context %d > max_blocks*16",
+                 max_context);
+  if (partition_tokens <= 0) partition_tokens = default_partition(B, Hkv, max_context);
+  W4_CHECK_SHAPE(partition_tokens % ATT_PAGE == 0, "paged_gqa_decode_noalloc: partition_tokens %% 16 != 0");
+  if (q_stride == 0) q_stride = Hq * D;
+  W4_CHECK_ARG(q_stride >= Hq * D, "paged_gqa_decode_noalloc: q_stride too small");
+  W4_CHECK_ALIGN(q, 128, "q");
+  W4_CHECK_ALIGN(k_pool, 128, "k_pool");
+  W4_CHECK_ALIGN(v_pool, 128, "v_pool");
+  W4_CHECK_ALIGN(out, 128, "out");
+  W4_CHECK_ARG((q_stride * 2) % 16 == 0, "paged_gqa_decode_noalloc: q_stride*2 must be a multiple of 16 bytes");
+  const int P = (max_context + partition_tokens - 1) / partition_tokens;
+  AttnArgs a = {};
+  if (P > 1) {
+    const size_t need = attention_workspace_bytes(B, Hq, Hkv, P);
+    if (need > W4A16_NOALLOC_SCRATCH_BYTES)
+      return set_error(W4A16_ERR_SHAPE,
+                       "paged_gqa_decode_noalloc: these sizes need %zu bytes of scratch; the static array holds %u",
+                       need, (unsigned)W4A16_NOALLOC_SCRATCH_BYTES);
+    void* base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc) return rc;
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    char* w = static_cast<char*>(base);
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
+    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+    // the array keeps the previous call's contents: the tickets must start at zero
+    cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)B * Hkv * sizeof(unsigned int), (cudaStream_t)stream);
+    if (e != cudaSuccess)
+      return set_error(W4A16_ERR_CUDA, "paged_gqa_decode_noalloc: clearing counters: %s", cudaGetErrorString(e));
+  }
+  a.q = reinterpret_cast<const __half*>(q);
+  a.k_pool = reinterpret_cast<const __half*>(k_pool);
+  a.v_pool = reinterpret_cast<const __half*>(v_pool);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  a.err_flag = err_flag;
+  a.q_stride = q_stride;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.P = P;
+  a.part_tokens = partition_tokens;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  return launch_paged_attention(a, (cudaStream_t)stream);
 }
