@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--seed", type=int, default=1002)
+    ap.add_argument("--kernel", default=None,
+                    choices=["gateup", "down", "qkv", "o", "attention", "lm_head"],
+                    help="time one kernel of the workload alone (per-launch JSON line)")
+    ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
     return ap.parse_args()
 
 
@@ -270,10 +274,101 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------- native arm
 
+def run_kernel(args):
+    """One kernel of the Qwen-shaped layer, launched K times from a CUDA graph
+    (weights rotated over enough copies to exceed L2), timed with events."""
+    import torch
+    from w4a16_decode_paged_gb300 import api, build, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    cfg = dict(synth.QWEN_LAYER, codes="symmetric")
+    H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
+    B, L = args.batch, args.context
+    r = synth.rng(args.seed)
+    tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int32) if a.dtype == np.uint32 else a)).to(dev)
+    name = args.kernel
+    if name == "attention":
+        lens = np.full(B, L, np.int32)
+        pages = B * ((L + 15) // 16) + 8
+        kp = torch.randn((pages, Hkv, 16, D), device=dev).half()
+        vp = torch.randn((pages, Hkv, 16, D), device=dev).half()
+        bt = tdev(synth.block_table(r, lens, pages))
+        ld = tdev(lens)
+        q = torch.randn((B, Hq, D), device=dev).half()
+        out = torch.empty_like(q)
+        part = api.paged_gqa_decode_default_partition(B, Hkv, L) if args.context < 8192 else 512
+        ws = torch.zeros(api.paged_gqa_decode_workspace_size(B, Hq, Hkv, L, part), dtype=torch.uint8, device=dev)
+        nbytes = B * (2 * Hkv * L * D * 2 + 4 * ((L + 15) // 16) + 2 * Hq * D * 2)
+        copies = 1
+        fns = [lambda: api.paged_gqa_decode(q, kp, vp, bt, ld, max_context=L, partition_tokens=part, workspace=ws,
+                                            out=out)]
+        extra = {"partition_tokens": part, "context": L, "batch": B}
+    elif name == "lm_head":
+        lm = torch.randn((cfg.get("vocab", 152064) or 152064, H), device=dev).half() * 0.02
+        x = torch.randn((B, H), device=dev).half()
+        ws = torch.zeros(api.load().lm_head_argmax_workspace_size(B, lm.shape[0]), dtype=torch.uint8, device=dev)
+        toks = torch.empty(B, dtype=torch.int32, device=dev)
+        nbytes = lm.numel() * 2 + B * H * 2 + B * 4
+        copies = 1
+        fns = [lambda: api.lm_head_argmax(x, lm, tokens_out=toks, workspace=ws)]
+        extra = {"vocab": lm.shape[0], "batch": B}
+    else:
+        shapes = {"gateup": (I, H), "down": (H, I), "qkv": ((Hq + 2 * Hkv) * D, H), "o": (H, Hq * D)}
+        N, K = shapes[name]
+        one = (2 * N if name == "gateup" else N) * (K // 2 + K // 128 * 2)
+        copies = max(1, math.ceil(3 * 128e6 / one))
+        x = torch.randn((B, K), device=dev).half()
+        g = torch.ones(K, device=dev).half()
+        res = torch.randn((B, N), device=dev).half()
+        y = torch.empty((B, N), dtype=torch.float16, device=dev)
+        fns = []
+        for _ in range(copies):
+            qw, sc = synth.int4_weight(r, N, K, "symmetric")
+            qw, sc = tdev(qw), tdev(sc)
+            if name == "gateup":
+                qu, su = synth.int4_weight(r, N, K, "symmetric")
+                qu, su = tdev(qu), tdev(su)
+                fns.append(lambda qw=qw, sc=sc, qu=qu, su=su: api.w4a16_gemv_silu_mul(x, g, 1e-6, qw, sc, qu, su, out=y))
+            elif name == "qkv":
+                fns.append(lambda qw=qw, sc=sc: api.w4a16_gemv_rmsnorm(x, g, 1e-6, qw, sc, out=y))
+            else:
+                fns.append(lambda qw=qw, sc=sc: api.w4a16_gemv(x, qw, sc, residual=res, out=y))
+        nbytes = one + B * K * 2 + B * N * 2 + (B * N * 2 if name in ("down", "o") else 0)
+        extra = {"N": N, "K": K, "batch": B, "weight_copies": copies}
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for f in fns:
+            f()
+        stream.synchronize()
+        g_ = torch.cuda.CUDAGraph()
+        per_graph = max(len(fns), 8)
+        with torch.cuda.graph(g_, stream=stream, capture_error_mode="relaxed"):
+            for i in range(per_graph):
+                fns[i % len(fns)]()
+        for _ in range(args.warmup):
+            g_.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g_.replay()
+        e1.record(stream)
+        stream.synchronize()
+    per = e0.elapsed_time(e1) / 1e3 / (args.steps * per_graph)
+    peak, src = measured_peak()
+    out = {"kernel": name, "us_per_launch": per * 1e6, "bytes_per_launch": nbytes, "gbs": nbytes / per / 1e9,
+           "frac_of_peak": nbytes / per / 1e9 / peak, "peak_gbs": peak, "peak_source": src,
+           "launches_timed": args.steps * per_graph, **extra}
+    print(json.dumps(out))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel:
+        return run_kernel(args)
 
     import torch
     import torch.distributed as dist

@@ -174,6 +174,25 @@ W4A16_API int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t* 
                      size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
                      w4a16_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode_rope_append -- kv_append_rope followed by
+ * paged_gqa_decode, as one kernel (the form the decode step runs).
+ *   qkv  fp16 rows of pitch qkv_stride: q [Hq][D] | k_new [Hkv][D] |
+ *        v_new [Hkv][D] per sequence (the q|k|v GEMV output); read only --
+ *        the rotated q is used in place, not written back.
+ *   theta  RoPE base; the new token's position is context_lens[b] - 1.
+ * k_new (rotated) and v_new are written to their slot in the pools, as
+ * kv_append_rope does; the other arguments are as for paged_gqa_decode.
+ * ------------------------------------------------------------------------ */
+W4A16_API int paged_gqa_decode_rope_append(const uint16_t* qkv, int qkv_stride, uint16_t* k_pool,
+                                           uint16_t* v_pool, int num_pages,
+                                           const int32_t* block_table, int max_blocks,
+                                           const int32_t* context_lens, int max_context, int B,
+                                           int Hq, int Hkv, int D, float theta, float sm_scale,
+                                           int partition_tokens, void* workspace,
+                                           size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
+                                           w4a16_stream_t stream);
+
 /* Bytes of workspace paged_gqa_decode needs for these sizes. */
 W4A16_API size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max_context,
                                        int partition_tokens, int D);

@@ -24,7 +24,8 @@ def api():
 # ----------------------------------------------------------------------------- GEMV
 
 GEMV_SHAPES = [(128, 1), (256, 37), (896, 128), (896, 1152), (896, 2432), (2432, 896), (1024, 64),
-               (3584, 130), (3584, 512), (3584, 4608), (3584, 18944), (18944, 3584)]
+               (3584, 130), (3584, 131), (3584, 2), (3584, 6), (3584, 512), (3584, 4608), (3584, 18944),
+               (18944, 3584), (18944, 14)]
 
 
 @pytest.mark.parametrize("K,N", GEMV_SHAPES)
@@ -60,7 +61,7 @@ def test_w4a16_gemv_rmsnorm_matches_oracle(api, K, N, M):
 
 
 @pytest.mark.parametrize("K,N,M,norm", [(896, 2432, 1, True), (3584, 18944, 1, True), (3584, 18944, 2, False),
-                                        (256, 40, 4, True)])
+                                        (256, 40, 4, True), (3584, 10, 1, True), (3584, 7, 3, False)])
 def test_w4a16_gemv_silu_mul_matches_oracle(api, K, N, M, norm):
     r = np.random.default_rng(K * 3 + N + M)
     qg, sg = synth.int4_weight(r, N, K)
@@ -315,3 +316,40 @@ def test_lm_head_argmax_ties_take_lowest_index(api):
     toks, _ = api.lm_head_argmax(to_dev(x, torch), to_dev(W, torch))
     torch.cuda.synchronize()
     assert int(to_host(toks)[0]) == 1234
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(7, 1), (28, 4)])
+@pytest.mark.parametrize("part", [16, 64, 0])
+def test_fused_rope_append_attention_matches_oracle(api, Hq, Hkv, part):
+    r = np.random.default_rng(Hq * 7 + part)
+    D, theta = 128, 1e6
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, 37, 513], np.int32)  # after the append
+    B = len(lens)
+    pages = int(sum((L + 15) // 16 for L in lens)) + 6
+    kp = synth.kv_pool(r, pages, Hkv, D)
+    vp = synth.kv_pool(r, pages, Hkv, D)
+    bt = synth.block_table(r, lens, pages)
+    qkv = synth.normal_fp16(r, (B, (Hq + 2 * Hkv) * D), std=2.0)
+    q = qkv[:, :Hq * D].reshape(B, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(B, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(B, Hkv, D)
+    q_rot = np.stack([orc.rope(q[b], int(lens[b]) - 1, theta) for b in range(B)])
+    k_rot = np.stack([orc.rope(k[b], int(lens[b]) - 1, theta) for b in range(B)])
+    kp_ref, vp_ref = kp.copy(), vp.copy()
+    orc.kv_append(k_rot, v, kp_ref, vp_ref, bt, lens)
+    ref = orc.paged_attention(q_rot, kp_ref, vp_ref, bt, lens, 1 / math.sqrt(D))
+    kpd, vpd = to_dev(kp, torch), to_dev(vp, torch)
+    qkvd = to_dev(qkv, torch)
+    out = api.paged_gqa_decode_rope_append(qkvd, kpd, vpd, to_dev(bt, torch), to_dev(lens, torch),
+                                           max_context=int(lens.max()), theta=theta, n_q_heads=Hq,
+                                           partition_tokens=part)
+    torch.cuda.synchronize()
+    assert_close(to_host(out), ref, what=f"fused attention Hq={Hq} part={part}")
+    kg, vg = to_host(kpd), to_host(vpd)
+    assert np.array_equal(vg, vp_ref)                 # v placement and values bit-exact
+    mask = np.zeros(kp.shape[:3], bool)
+    for b in range(B):
+        mask[bt[b, (lens[b] - 1) // 16], :, (lens[b] - 1) % 16] = True
+    assert np.array_equal(kg[~mask], kp[~mask])        # nothing else moved
+    assert_close(kg[mask], kp_ref[mask], what="appended k")
+    assert np.array_equal(to_host(qkvd), qkv)         # q|k|v rows are read only

@@ -56,6 +56,8 @@ SIGNATURES = {
     "rmsnorm": (I32, [P, P, P, I32, I32, F32, P]),
     "kv_append_rope": (I32, [P, P, P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, F32, P, P]),
     "paged_gqa_decode": (I32, [P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, SZ, P, P, P]),
+    "paged_gqa_decode_rope_append": (I32, [P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, F32, I32, P,
+                                           SZ, P, P, P]),
     "paged_gqa_decode_noalloc": (I32, [P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, P]),
     "paged_gqa_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
     "paged_gqa_decode_default_partition": (I32, [I32, I32, I32]),

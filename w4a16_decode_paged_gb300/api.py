@@ -14,7 +14,7 @@ import torch
 from ._lib import LayerWeights, ModelConfig, ModelWeights, check, load
 
 __all__ = ["w4a16_gemv", "w4a16_gemv_rmsnorm", "w4a16_gemv_silu_mul", "rmsnorm", "kv_append_rope",
-           "paged_gqa_decode", "paged_gqa_decode_workspace_size", "paged_gqa_decode_default_partition",
+           "paged_gqa_decode", "paged_gqa_decode_rope_append", "paged_gqa_decode_workspace_size", "paged_gqa_decode_default_partition",
            "workspace_clear", "embedding_gather", "lm_head_argmax", "Model", "stream_handle"]
 
 
@@ -132,6 +132,32 @@ def paged_gqa_decode(q, k_pool, v_pool, block_table, context_lens, max_context, 
                                float(sm_scale), int(partition_tokens), _p(workspace),
                                workspace.numel() * workspace.element_size(), _p(out), _p(err_flag),
                                stream_handle(stream)))
+    return out
+
+
+def paged_gqa_decode_rope_append(qkv, k_pool, v_pool, block_table, context_lens, max_context, theta, n_q_heads,
+                                 sm_scale=None, partition_tokens=0, workspace=None, out=None, err_flag=None,
+                                 stream=None):
+    """qkv rows [B][(Hq + 2 Hkv) D] (q | k_new | v_new); appends and attends."""
+    _need(qkv, _H, "qkv"); _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
+    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
+    pages, Hkv, _, D = k_pool.shape
+    B = block_table.shape[0]
+    Hq = n_q_heads
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    lib = load()
+    if workspace is None:
+        nbytes = lib.paged_gqa_decode_workspace_size(B, Hq, Hkv, max_context, partition_tokens, D)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=k_pool.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=k_pool.device)
+    check(lib.paged_gqa_decode_rope_append(_p(qkv), qkv.shape[-1] if qkv.dim() == 2 else 0, _p(k_pool), _p(v_pool),
+                                           pages, _p(block_table), block_table.shape[1], _p(context_lens),
+                                           int(max_context), B, Hq, Hkv, D, float(theta), float(sm_scale),
+                                           int(partition_tokens), _p(workspace),
+                                           workspace.numel() * workspace.element_size(), _p(out), _p(err_flag),
+                                           stream_handle(stream)))
     return out
 
 

@@ -60,25 +60,32 @@ __device__ __forceinline__ float2 h2f2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
-template <int G>
+template <int G, bool FUSE>
 __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smraw[];
   __half* ring = reinterpret_cast<__half*>(smraw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + ATT_RING_BYTES);
   float* sbuf = reinterpret_cast<float*>(bars + ATT_NW * ATT_STAGES);  // [NW][8][16]
   float* corr = sbuf + ATT_NW * 8 * 16;                               // [NW][8]
+  __shared__ float s_q[G][ATT_D];      // this group's q (rotated in the fused variant)
+  __shared__ __half s_knew[ATT_D];     // fused: rotated new k and new v
+  __shared__ __half s_vnew[ATT_D];
   __shared__ int s_last;
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, kvh = blockIdx.y, p = blockIdx.x;
 
-  pdl_launch_dependents();
-  if (threadIdx.x < ATT_NW * ATT_STAGES) mbar_init(&bars[threadIdx.x], 1);
+  if (tid < ATT_NW * ATT_STAGES) mbar_init(&bars[tid], 1);
   fence_mbar_init();
   __syncthreads();
-  pdl_wait();  // q, the pools and the lengths may come from earlier kernels
+  // The fused variant writes the only KV slot that changes in this step
+  // itself, and the lengths were written at the start of the step, so it
+  // may fetch pages before its predecessor (the q|k|v GEMV) finishes.  The
+  // plain variant may be preceded by a kernel that appended to the pools.
+  if (!FUSE) pdl_wait_then_trigger();
 
-  const int L = a.context_lens[b];
+  const int L = __ldcg(&a.context_lens[b]);
   const int t_begin = p * a.part_tokens;
   const int t_end = min(L, t_begin + a.part_tokens);
   const int npages = t_end > t_begin ? (t_end - t_begin + ATT_PAGE - 1) / ATT_PAGE : 0;
@@ -93,7 +100,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
 
   auto page_id = [&](int li) -> int {  // li: index into this warp's page list
     const int gi = pg0 + warp + li * ATT_NW;
-    const int pg = (gi < a.max_blocks) ? bt[gi] : -1;
+    const int pg = (gi < a.max_blocks) ? __ldcg(&bt[gi]) : -1;
     return (pg >= 0 && pg < a.num_pages) ? pg : -1;
   };
   auto issue = [&](int li) {  // lane 0 only
@@ -113,24 +120,61 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   if (lane == 0) {
     for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) issue(li);
   }
+  if (FUSE) pdl_wait_then_trigger();
+
+  // ---- q (and, fused, RoPE of q and the new k; append of k and v) ----------
+  const __half* qb = a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D;
+  const int pos = L - 1;
+  if (FUSE) {
+    const __half* kn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + kvh) * ATT_D;
+    const __half* vn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + a.Hkv + kvh) * ATT_D;
+    const float fpos = (float)(pos > 0 ? pos : 0);
+    for (int idx = tid; idx < (G + 1) * (ATT_D / 2); idx += blockDim.x) {
+      const int h = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
+      const float ang = __fmul_rn(fpos, a.inv_freq[i]);  // the fp32 product, no contraction
+      float sn, cs;
+      sincosf(ang, &sn, &cs);
+      const __half* src = h < G ? qb + h * ATT_D : kn;
+      const float x0 = __half2float(src[i]), x1 = __half2float(src[i + ATT_D / 2]);
+      const __half r0 = __float2half_rn(x0 * cs - x1 * sn);
+      const __half r1 = __float2half_rn(x1 * cs + x0 * sn);
+      if (h < G) {
+        s_q[h][i] = __half2float(r0);
+        s_q[h][i + ATT_D / 2] = __half2float(r1);
+      } else {
+        s_knew[i] = r0;
+        s_knew[i + ATT_D / 2] = r1;
+      }
+    }
+    for (int d = tid; d < ATT_D; d += blockDim.x) s_vnew[d] = vn[d];
+    __syncthreads();
+    if (pos >= t_begin && pos < t_end) {  // this partition holds the new token: append it
+      const int blk = pos / ATT_PAGE;
+      const int pg = (blk < a.max_blocks) ? __ldcg(&bt[blk]) : -1;
+      if (pg >= 0 && pg < a.num_pages) {
+        const size_t off = (((size_t)pg * a.Hkv + kvh) * ATT_PAGE + pos % ATT_PAGE) * ATT_D;
+        for (int d = tid; d < ATT_D; d += blockDim.x) {
+          a.k_pool[off + d] = s_knew[d];
+          a.v_pool[off + d] = s_vnew[d];
+        }
+      } else if (tid == 0 && a.err_flag) {
+        atomicOr(a.err_flag, 1);
+      }
+    }
+  } else {
+    for (int idx = tid; idx < G * ATT_D; idx += blockDim.x)
+      s_q[idx / ATT_D][idx % ATT_D] = __half2float(qb[(idx / ATT_D) * ATT_D + idx % ATT_D]);
+    __syncthreads();
+  }
 
   // q for this lane's dims: lane = (tq, ds); dims [16 ds, 16 ds + 16)
   const int tq = lane >> 3, ds = lane & 7;
   float2 qr[G][8];
-  {
-    const __half* qb = a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint4* src = reinterpret_cast<const uint4*>(qb + h * ATT_D + 16 * ds);
-      uint4 u0 = src[0], u1 = src[1];
-      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float2 f = h2f2(w[j]);
-        qr[h][j] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
-      }
-    }
-  }
+    for (int j = 0; j < 8; ++j)
+      qr[h][j] = make_float2(s_q[h][16 * ds + 2 * j] * a.scale_log2, s_q[h][16 * ds + 2 * j + 1] * a.scale_log2);
   float m_run = -INFINITY, l_run = 0.f;  // lane h < G holds head h's state
   float2 o[G][2];                       // dims [4 lane, 4 lane + 4)
 #pragma unroll
@@ -147,12 +191,19 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       break;
     }
     consumed = li + 1;
-    const __half* Ks = myring + (size_t)stage * 2 * ATT_SLICE;
-    const __half* Vs = Ks + ATT_SLICE;
+    __half* Ks = myring + (size_t)stage * 2 * ATT_SLICE;
+    __half* Vs = Ks + ATT_SLICE;
     const int gi = warp + li * ATT_NW;  // page index within the partition
     const int tok0 = (pg0 + gi) * ATT_PAGE;
     const bool page_ok = page_id(li) >= 0;
     const int nv = page_ok ? min(ATT_PAGE, t_end - tok0) : 0;
+    if (FUSE && page_ok && pos >= tok0 && pos < tok0 + ATT_PAGE) {
+      // the page was fetched before the append: patch the new token's row
+      const int slot = pos - tok0;
+      *reinterpret_cast<uint2*>(Ks + slot * ATT_D + 4 * lane) = *reinterpret_cast<const uint2*>(s_knew + 4 * lane);
+      *reinterpret_cast<uint2*>(Vs + slot * ATT_D + 4 * lane) = *reinterpret_cast<const uint2*>(s_vnew + 4 * lane);
+      __syncwarp();
+    }
 
     // ---- scores: 4 rounds of 4 tokens; lane (tq, ds) -------------------
 #pragma unroll
@@ -206,19 +257,19 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
 
     // ---- online softmax: lane h < G owns head h -----------------------
     if (lane < G) {
-      float s[16];
+      float sv[16];
       float mx = -INFINITY;
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        s[t] = (t < nv) ? ws[lane * 16 + t] : -INFINITY;
-        mx = fmaxf(mx, s[t]);
+        sv[t] = (t < nv) ? ws[lane * 16 + t] : -INFINITY;
+        mx = fmaxf(mx, sv[t]);
       }
       const float m_new = fmaxf(m_run, mx);
       const float c = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
       float sum = 0.f;
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        const float pv = (s[t] == -INFINITY) ? 0.f : exp2f(s[t] - m_new);
+        const float pv = (sv[t] == -INFINITY) ? 0.f : exp2f(sv[t] - m_new);
         ws[lane * 16 + t] = pv;
         sum += pv;
       }
@@ -280,7 +331,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
   __syncthreads();
 
-  const int d = threadIdx.x;  // 128 threads = 128 dims
+  const int d = tid;  // 128 threads = 128 dims
   const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
   if (a.P == 1) {
 #pragma unroll
@@ -326,31 +377,57 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     const unsigned int ticket = atomicAdd(&a.counters[(size_t)b * a.Hkv + kvh], 1u);
     s_last = (ticket == (unsigned int)(a.P - 1));
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // Combine, in parallel: (1) all (max, sum) pairs into shared memory,
+  // (2) one thread per head turns them into weights, (3) each thread (one
+  // output dim) sums the weighted partial outputs with independent loads.
   const int Pv = L > 0 ? min(a.P, (L + a.part_tokens - 1) / a.part_tokens) : 0;
+  float* cw = reinterpret_cast<float*>(smraw);  // [G][Pv] maxima, then weights
+  float* cl = cw + G * Pv;                      // [G][Pv] sums
+  for (int idx = tid; idx < G * Pv; idx += blockDim.x) {
+    const int h = idx / Pv, j = idx - h * Pv;
+    const size_t slot = (qh0 + h) * a.P + j;
+    cw[idx] = __ldcg(&a.ws_ml[slot * 2]);
+    cl[idx] = __ldcg(&a.ws_ml[slot * 2 + 1]);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float* mw = cw + tid * Pv;
+    float* lw = cl + tid * Pv;
+    float M = -INFINITY;
+    for (int j = 0; j < Pv; ++j) M = fmaxf(M, mw[j]);
+    float den = 0.f;
+    for (int j = 0; j < Pv; ++j) {
+      const float f = (M == -INFINITY || mw[j] == -INFINITY) ? 0.f : exp2f(mw[j] - M);
+      mw[j] = f;
+      den += lw[j] * f;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int j = 0; j < Pv; ++j) mw[j] *= inv;
+  }
+  __syncthreads();
 #pragma unroll 1
   for (int h = 0; h < G; ++h) {
-    const size_t base = (qh0 + h) * a.P;
-    float M = -INFINITY;
-    for (int j = 0; j < Pv; ++j) M = fmaxf(M, __ldcg(&a.ws_ml[(base + j) * 2]));
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int j = 0; j < Pv; ++j) {
-        const float mj = __ldcg(&a.ws_ml[(base + j) * 2]);
-        const float f = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-        acc += __ldcg(&a.ws_o[(base + j) * ATT_D + d]) * f;
-        den += __ldcg(&a.ws_ml[(base + j) * 2 + 1]) * f;
-      }
+    const float* wts = cw + h * Pv;
+    const float* src = a.ws_o + ((qh0 + h) * a.P) * ATT_D + d;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int j = 0;
+    for (; j + 4 <= Pv; j += 4) {
+      acc0 += wts[j] * __ldcg(src + (size_t)j * ATT_D);
+      acc1 += wts[j + 1] * __ldcg(src + (size_t)(j + 1) * ATT_D);
+      acc2 += wts[j + 2] * __ldcg(src + (size_t)(j + 2) * ATT_D);
+      acc3 += wts[j + 3] * __ldcg(src + (size_t)(j + 3) * ATT_D);
     }
-    a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+    for (; j < Pv; ++j) acc0 += wts[j] * __ldcg(src + (size_t)j * ATT_D);
+    a.out[(qh0 + h) * ATT_D + d] = __float2half_rn((acc0 + acc1) + (acc2 + acc3));
   }
-  if (threadIdx.x == 0) a.counters[(size_t)b * a.Hkv + kvh] = 0u;  // ready for the next call
+  if (tid == 0) a.counters[(size_t)b * a.Hkv + kvh] = 0u;  // ready for the next call
 }
 
 size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P) {
@@ -361,18 +438,23 @@ size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P) {
 template <int G>
 static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
   static bool configured = false;
-  auto kern = paged_attn_kernel<G>;
+  auto k0 = paged_attn_kernel<G, false>;
+  auto k1 = paged_attn_kernel<G, true>;
   if (!configured) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
+    cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
     configured = true;
   }
   dim3 grid(a.P, a.Hkv, a.B);
-  cudaError_t e = launch_pdl(kern, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a);
+  cudaError_t e = a.fuse_rope_append ? launch_pdl(k1, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a)
+                                     : launch_pdl(k0, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
 
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s) {
+  if (a.P > ATT_MAX_PARTITIONS)
+    return set_error(W4A16_ERR_SHAPE, "paged attention: %d partitions > %d", a.P, ATT_MAX_PARTITIONS);
   switch (a.Hq / a.Hkv) {
     case 1: return launch_attn_g<1>(a, s);
     case 2: return launch_attn_g<2>(a, s);
@@ -508,8 +590,8 @@ extern "C" int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t*
     a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
   }
   a.q = reinterpret_cast<const __half*>(q);
-  a.k_pool = reinterpret_cast<const __half*>(k_pool);
-  a.v_pool = reinterpret_cast<const __half*>(v_pool);
+  a.k_pool = reinterpret_cast<__half*>(const_cast<uint16_t*>(k_pool));
+  a.v_pool = reinterpret_cast<__half*>(const_cast<uint16_t*>(v_pool));
   a.block_table = block_table;
   a.context_lens = context_lens;
   a.out = reinterpret_cast<__half*>(out);
@@ -523,6 +605,63 @@ extern "C" int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t*
   a.P = P;
   a.part_tokens = partition_tokens;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
+  return launch_paged_attention(a, (cudaStream_t)stream);
+}
+
+extern "C" int paged_gqa_decode_rope_append(const uint16_t* qkv, int qkv_stride, uint16_t* k_pool, uint16_t* v_pool,
+                                            int num_pages, const int32_t* block_table, int max_blocks,
+                                            const int32_t* context_lens, int max_context, int B, int Hq, int Hkv,
+                                            int D, float theta, float sm_scale, int partition_tokens,
+                                            void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
+                                            w4a16_stream_t stream) {
+  W4_CHECK_ARG(qkv && k_pool && v_pool && block_table && context_lens && out,
+               "paged_gqa_decode_rope_append: null tensor pointer");
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1 && max_context >= 1,
+               "paged_gqa_decode_rope_append: sizes must be positive");
+  W4_CHECK_SHAPE(D == ATT_D, "paged_gqa_decode_rope_append: D=%d, only 128 is built", D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0 && Hq / Hkv <= 8, "paged_gqa_decode_rope_append: Hq=%d Hkv=%d", Hq, Hkv);
+  W4_CHECK_SHAPE(max_context <= max_blocks * ATT_PAGE, "paged_gqa_decode_rope_append: max_context > max_blocks*16");
+  W4_CHECK_ARG(theta > 0.f, "paged_gqa_decode_rope_append: theta must be positive");
+  if (partition_tokens <= 0) partition_tokens = default_partition(B, Hkv, max_context);
+  W4_CHECK_SHAPE(partition_tokens % ATT_PAGE == 0, "paged_gqa_decode_rope_append: partition_tokens %% 16 != 0");
+  if (qkv_stride == 0) qkv_stride = (Hq + 2 * Hkv) * D;
+  W4_CHECK_ARG(qkv_stride >= (Hq + 2 * Hkv) * D && (qkv_stride * 2) % 16 == 0,
+               "paged_gqa_decode_rope_append: bad qkv_stride");
+  W4_CHECK_ALIGN(qkv, 128, "qkv");
+  W4_CHECK_ALIGN(k_pool, 128, "k_pool");
+  W4_CHECK_ALIGN(v_pool, 128, "v_pool");
+  W4_CHECK_ALIGN(out, 128, "out");
+  const int P = (max_context + partition_tokens - 1) / partition_tokens;
+  AttnArgs a = {};
+  if (P > 1) {
+    const size_t need = attention_workspace_bytes(B, Hq, Hkv, P);
+    W4_CHECK_ARG(workspace != nullptr && workspace_bytes >= need,
+                 "paged_gqa_decode_rope_append: workspace of %zu bytes needed", need);
+    W4_CHECK_ALIGN(workspace, 128, "workspace");
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    char* w = static_cast<char*>(workspace);
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
+    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+  }
+  a.q = reinterpret_cast<const __half*>(qkv);
+  a.k_pool = reinterpret_cast<__half*>(k_pool);
+  a.v_pool = reinterpret_cast<__half*>(v_pool);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  a.err_flag = err_flag;
+  a.q_stride = qkv_stride;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.P = P;
+  a.part_tokens = partition_tokens;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.fuse_rope_append = 1;
+  rope_inv_freq_table(theta, D, a.inv_freq);
   return launch_paged_attention(a, (cudaStream_t)stream);
 }
 
@@ -632,8 +771,8 @@ extern "C" int paged_gqa_decode_noalloc(const uint16_t* q, int q_stride, const u
       return set_error(W4A16_ERR_CUDA, "paged_gqa_decode_noalloc: clearing counters: %s", cudaGetErrorString(e));
   }
   a.q = reinterpret_cast<const __half*>(q);
-  a.k_pool = reinterpret_cast<const __half*>(k_pool);
-  a.v_pool = reinterpret_cast<const __half*>(v_pool);
+  a.k_pool = reinterpret_cast<__half*>(const_cast<uint16_t*>(k_pool));
+  a.v_pool = reinterpret_cast<__half*>(const_cast<uint16_t*>(v_pool));
   a.block_table = block_table;
   a.context_lens = context_lens;
   a.out = reinterpret_cast<__half*>(out);

@@ -56,10 +56,23 @@ inline cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, c
 // ---------------------------------------------------------------------------
 
 // PDL: let dependents launch / wait for the grids this one depends on.
+//
+// Ordering rule kept by every kernel in this library: a kernel triggers its
+// dependents (launch_dependents) only after its own griddepcontrol.wait has
+// returned.  So when a kernel starts, its predecessor has passed its wait,
+// which means every grid before the predecessor has completed.  Before its
+// own wait a kernel may therefore read (through L2) anything written only by
+// grids older than its predecessor -- weights, the block table, the context
+// lengths written at the start of the step, KV pages of earlier positions --
+// but nothing its predecessor writes, and it writes nothing.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_then_trigger() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
 
 // 128-bit streaming load that bypasses L1 (weights are read exactly once).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
@@ -75,6 +88,18 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// Per-thread async copy of 16 bytes global -> shared (bypasses L1).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // (a & b) | c in one LOP3.

@@ -18,8 +18,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __half* __restrict__
                                                       __half* y, int H, float eps) {
   __shared__ float red[8];
   __shared__ float rs;
-  pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_then_trigger();
   const int m = blockIdx.x;
   const __half* xr = x + (size_t)m * H;
   float ss = 0.f;
@@ -65,8 +64,7 @@ int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H
 __global__ void __launch_bounds__(256) embedding_kernel(const __half* __restrict__ embed, int vocab, int H,
                                                         const int32_t* tokens, __half* x, int32_t* err_flag,
                                                         int32_t* lens) {
-  pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_then_trigger();
   const int b = blockIdx.x;
   const int tok = tokens[b];
   const bool ok = tok >= 0 && tok < vocab;
@@ -109,8 +107,7 @@ __global__ void __launch_bounds__(LM_WPB * 32) lm_head_kernel(const __grid_const
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int H = a.H, NC = H / 8;
-  pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_then_trigger();
 
   // stage x (RMS-normalised when gamma is given)
   for (int b = 0; b < a.B; ++b) {

@@ -9,18 +9,22 @@
 // and the products run as mixed-precision fp16 x fp16 -> fp32 FMAs, so every
 // product is exact and every sum is fp32.
 //
-// Dequant trick, per packed word w (nibbles u0..u7, u = q + 8):
-//   (w      & 0x000F000F) | 0x64006400 = half2{1024 + u0, 1024 + u4}
-//   (w      & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u1, 1024 + 16 u5}
-//   (w >> 8 & 0x000F000F) | 0x64006400 = half2{1024 + u2, 1024 + u6}
-//   (w >> 8 & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u3, 1024 + 16 u7}
-// One HSUB2 each turns these into exact codes: minus 1032 gives q for the
-// even nibbles, minus 1152 gives 16 q for the odd ones.  The activations are
-// staged once per CTA in shared memory in the matching order, with the
-// odd-nibble ones pre-divided by 16 (exact), so every product (16 q)(x / 16)
-// is exact in fp32.  That is one shift, four LOP3, four HSUB2 and eight FMAs
-// per 8 weights.  (Folding the 1032 offset into the sum instead would save
-// the HSUB2s but costs about eight bits of the fp32 sum when |x| is large.)
+// Dequant trick, per packed word w (nibbles u0..u7, u = q + 8).  Each pair of
+// nibbles (i, i + 4) is moved into the top four mantissa bits of the two
+// halves of a half2 and OR-ed with the exponent of 1.0:
+//   ((w << 6) & 0x03C003C0) | 0x3C003C00 = half2{1 + u0/16, 1 + u4/16}
+//   ((w << 2) & 0x03C003C0) | 0x3C003C00 = half2{1 + u1/16, 1 + u5/16}
+//   ((w >> 2) & 0x03C003C0) | 0x3C003C00 = half2{1 + u2/16, 1 + u6/16}
+//   ((w >> 6) & 0x03C003C0) | 0x3C003C00 = half2{1 + u3/16, 1 + u7/16}
+// The activations are staged once per CTA in shared memory in the matching
+// order, and mixed-precision fp16 x fp16 -> fp32 FMAs (exact products) give
+// S = sum_i (1 + u_i/16) x_i over a 32-weight chunk, so that
+//   sum_i q_i x_i = 16 S - 24 sum_i x_i,
+// with 24 sum x (one fp32 per chunk, shared by every row) staged beside x.
+// Because the implicit leading 1 is only ~16/15 of the code's range, the
+// subtraction costs about two bits of the fp32 sum (the 1024 + u magic would
+// cost about ten).  That is four shifts, four LOP3 and eight FMAs per 8
+// weights, with no fp16-pipe work.
 //
 // Work split: LPR lanes cooperate on one weight row (LPR = 16 when K/32 is a
 // multiple of 16, else 8 or 4); a warp covers 32/LPR rows at a time; each
@@ -41,18 +45,89 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
+// Stage x (optionally RMS-normalised, rounded to fp16) in shared memory in
+// nibble order: for 32-weight chunk j and word w of the chunk, one uint4 holds
+// {x0, x4}, {x1/16, x5/16}, {x2, x6}, {x3/16, x7/16} of k = 32 j + 8 w + i.
+// Layout [MT][4][K/32] uint4, so consecutive chunks are consecutive 16 bytes.
+template <int MT>
+__device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, float* cs, float (*red)[MT],
+                                                  float* rscale) {
+  const int K = a.K, M = a.M, NCH = K >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (a.gamma != nullptr) {
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+      for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+        uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + k);
+        const __half* h = reinterpret_cast<const __half*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float v = __half2float(h[i]);
+          ss = fmaf(v, v, ss);
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) red[warp][0] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w][0];
+        rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);
+      }
+      __syncthreads();
+    }
+  }
+  for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
+    const int m = idx / NCH, j = idx - m * NCH;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
+    float csum = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint4 raw = src[wi];
+      __half h[8];
+      *reinterpret_cast<uint4*>(h) = raw;
+      if (a.gamma != nullptr) {
+        uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + 32 * j + 8 * wi);
+        const __half* g = reinterpret_cast<const __half*>(&graw);
+        const float r = rscale[m];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
+      }
+      uint4 o;
+      o.x = pack_h2(h[0], h[4]);
+      o.y = pack_h2(h[1], h[5]);
+      o.z = pack_h2(h[2], h[6]);
+      o.w = pack_h2(h[3], h[7]);
+      xs[(size_t)(m * 4 + wi) * NCH + j] = o;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) csum += __half2float(h[i]);
+    }
+    cs[(size_t)m * NCH + j] = 24.0f * csum;
+  }
+  __syncthreads();
+}
+
+constexpr uint32_t NIB_MASK = 0x03C003C0u;  // top four mantissa bits of both halves
+constexpr uint32_t ONE_H2 = 0x3C003C00u;    // half2{1, 1}
+
+// S += sum over the 8 nibbles of word w of (1 + u/16) * x, x in staged order.
+__device__ __forceinline__ void word_dot(float& p0, float& p1, uint32_t w, const uint4 xv) {
+  fma2_f16_f32_split(p0, p1, and_or(w << 6, NIB_MASK, ONE_H2), xv.x);
+  fma2_f16_f32_split(p0, p1, and_or(w << 2, NIB_MASK, ONE_H2), xv.y);
+  fma2_f16_f32_split(p0, p1, and_or(w >> 2, NIB_MASK, ONE_H2), xv.z);
+  fma2_f16_f32_split(p0, p1, and_or(w >> 6, NIB_MASK, ONE_H2), xv.w);
+}
+
 template <int LPR, int MT, bool SILU>
 __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int RPW = 32 / LPR;               // row slots per warp
   constexpr int RPT = SILU ? RPW / 2 : RPW;   // output rows per warp task
-  constexpr uint32_t MAGIC = 0x64006400u;     // half2{1024, 1024}
-  constexpr uint32_t EVEN_OFF = 0x64086408u;  // half2{1032, 1032}
-  constexpr uint32_t ODD_OFF = 0x64806480u;   // half2{1152, 1152}
   extern __shared__ uint4 smem[];
   const int K = a.K, M = a.M;
   const int NCH = K >> 5;      // 32-weight chunks per row
   const int NIT = NCH / LPR;   // chunks per lane per row
-  uint4* xs = smem;  // [MT][4][NCH]
+  uint4* xs = smem;                                                   // [MT][4][NCH]
+  float* cs = reinterpret_cast<float*>(smem + (size_t)MT * 4 * NCH);  // [MT][NCH]
   __shared__ float red[GEMV_WPB][MT];
   __shared__ float rscale[MT];
 
@@ -61,9 +136,8 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
   const int ntask = (a.N + RPT - 1) / RPT;
   const int nwarps = gridDim.x * GEMV_WPB;
 
-  // Weights do not depend on the previous kernel: let the next kernel start
-  // early and issue this warp's first batch of weight loads before waiting.
-  pdl_launch_dependents();
+  // Weights do not depend on the previous kernel: issue this warp's first
+  // batch of weight loads before waiting for it.
 
   int task = blockIdx.x * GEMV_WPB + warp;
   uint4 wb[GEMV_U];
@@ -111,57 +185,9 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
     }
   }
 
-  pdl_wait();  // x (and residual) come from the previous kernel
+  pdl_wait_then_trigger();  // x (and residual) come from the previous kernel
 
-  // ---- stage x' (permuted, odd nibbles pre-scaled by 1/16) and C ----------
-  if (a.gamma != nullptr) {
-    for (int m = 0; m < M; ++m) {
-      float ss = 0.f;
-      for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
-        uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + k);
-        const __half* h = reinterpret_cast<const __half*>(&raw);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float v = __half2float(h[i]);
-          ss = fmaf(v, v, ss);
-        }
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) red[warp][0] = ss;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float t = 0.f;
-        for (int w = 0; w < GEMV_WPB; ++w) t += red[w][0];
-        rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);
-      }
-      __syncthreads();
-    }
-  }
-  const __half sixteenth = __float2half(0.0625f);
-  for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
-    const int m = idx / NCH, j = idx - m * NCH;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
-#pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-      uint4 raw = src[wi];
-      __half h[8];
-      *reinterpret_cast<uint4*>(h) = raw;
-      if (a.gamma != nullptr) {
-        uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + 32 * j + 8 * wi);
-        const __half* g = reinterpret_cast<const __half*>(&graw);
-        const float r = rscale[m];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
-      }
-      uint4 o;
-      o.x = pack_h2(h[0], h[4]);
-      o.y = pack_h2(__hmul(h[1], sixteenth), __hmul(h[5], sixteenth));
-      o.z = pack_h2(h[2], h[6]);
-      o.w = pack_h2(__hmul(h[3], sixteenth), __hmul(h[7], sixteenth));
-      xs[(size_t)(m * 4 + wi) * NCH + j] = o;
-    }
-  }
-  __syncthreads();
+  stage_activations<MT>(a, xs, cs, red, rscale);
 
   // ---- main loop over this warp's tasks -----------------------------------
   for (; task < ntask; task += nwarps) {
@@ -202,16 +228,8 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
               if (m < M) {
                 float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                  const uint32_t w = wv[wi];
-                  const uint32_t w8 = w >> 8;
-                  const uint4 xv = xs[(size_t)(m * 4 + wi) * NCH + j];
-                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w, 0x000F000Fu, MAGIC), EVEN_OFF), xv.x);
-                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w, 0x00F000F0u, MAGIC), ODD_OFF), xv.y);
-                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w8, 0x000F000Fu, MAGIC), EVEN_OFF), xv.z);
-                  fma2_f16_f32_split(p0, p1, hsub2(and_or(w8, 0x00F000F0u, MAGIC), ODD_OFF), xv.w);
-                }
-                acc[m] = fmaf(p0 + p1, s, acc[m]);
+                for (int wi = 0; wi < 4; ++wi) word_dot(p0, p1, wv[wi], xs[(size_t)(m * 4 + wi) * NCH + j]);
+                acc[m] = fmaf(fmaf(16.0f, p0 + p1, -cs[(size_t)m * NCH + j]), s, acc[m]);
               }
             }
           }
@@ -267,13 +285,244 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Fast path for K a multiple of 512 known at compile time (the model's
+// K = 3584 and 18944).  16 lanes per weight row.  Each lane streams the
+// 16-byte chunks it will use into its own slots of a shared-memory ring with
+// cp.async (a lane only ever reads what it copied, so no barrier is needed),
+// one batch of GEMV_RU chunks ahead of the batch it computes; bytes in
+// flight therefore cost shared memory, not registers.  Task shapes:
+//   KS = 1: each half-warp owns R rows (non-SiLU task = 2R rows; SiLU task =
+//           R output rows, half-warp 0 on the gate rows, 1 on the up rows);
+//   KS = 2: both half-warps work on the same R rows and split K (long K).
+// All strides are compile-time immediates.
+// ---------------------------------------------------------------------------
+constexpr int GEMV_RU = 8;  // chunks per lane per batch (R rows x U chunks)
+
+template <int NCH, int R, int KS, int MT, bool SILU>
+__global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
+  constexpr int LPR = 16, RU = GEMV_RU, U = RU / R;
+  constexpr int K = NCH * 32;
+  constexpr int NIT = NCH / LPR;                 // chunks per lane when one half-warp covers K
+  constexpr int NIT_L = (NIT + KS - 1) / KS;     // this lane's share (upper bound)
+  constexpr int NB = (NIT_L + U - 1) / U;        // batches per task
+  constexpr int WROW = K / 8;
+  constexpr int SROW = K / 128;
+  constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
+  constexpr int NT = GEMV_WPB * 32;
+  static_assert(RU % R == 0, "R must divide GEMV_RU");
+  static_assert(!(SILU && KS == 2), "SiLU pairs gate and up across half-warps");
+  extern __shared__ uint4 smem[];
+  uint4* xs = smem;                                          // [MT][4][NCH]
+  uint4* ring = smem + MT * 4 * NCH;                         // [2][RU][NT]
+  float* cs = reinterpret_cast<float*>(ring + 2 * RU * NT);  // [MT][NCH]
+  __shared__ float red[GEMV_WPB][MT];
+  __shared__ float rscale[MT];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int hw = lane >> 4, lr = lane & 15;
+  const int M = a.M;
+  const int ntask = (a.N + RPT - 1) / RPT;
+  const int nwarps = gridDim.x * GEMV_WPB;
+
+  // first output row of this lane's rows for task t, and the weight-row base
+  auto rows_of = [&](int t, int& out0, const uint32_t*& q, const __half*& sp, const __half*& bp) {
+    if (SILU) {
+      out0 = t * RPT;
+      const int r = max(min(out0, a.N - R), 0);
+      q = a.seg[hw].qw + (size_t)r * WROW;
+      sp = a.seg[hw].s + (size_t)r * SROW;
+      bp = nullptr;
+    } else {
+      out0 = KS == 2 ? t * RPT : t * RPT + hw * R;
+      int r = max(min(out0, a.N - R), 0);
+      int si = 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
+      q = a.seg[si].qw + (size_t)r * WROW;
+      sp = a.seg[si].s + (size_t)r * SROW;
+      bp = a.seg[si].bias ? a.seg[si].bias + r : nullptr;
+    }
+  };
+  auto chunk_it = [&](int i) { return KS == 2 ? 2 * i + hw : i; };
+
+  // issue cursor (one batch ahead of the compute cursor)
+  int i_task = blockIdx.x * GEMV_WPB + warp, i_b = 0, i_out0;
+  const uint32_t* i_q;
+  const __half *i_s, *i_bias;
+  if (i_task < ntask) rows_of(i_task, i_out0, i_q, i_s, i_bias);
+  __half sc[2][RU];
+  auto issue = [&](const int slot) {
+    if (i_task < ntask) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int it = chunk_it(i_b * U + u);
+        if (it < NIT) {
+          const int j = lr + LPR * it;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            cp_async16(&ring[(slot * RU + r * U + u) * NT + tid], i_q + r * WROW + 4 * j);
+            sc[slot][r * U + u] = i_s[r * SROW + (j >> 2)];
+          }
+        }
+      }
+      if (++i_b == NB) {
+        i_b = 0;
+        i_task += nwarps;
+        if (i_task < ntask) rows_of(i_task, i_out0, i_q, i_s, i_bias);
+      }
+    }
+    cp_async_commit();
+  };
+
+  issue(0);  // weights do not depend on the previous kernel
+  pdl_wait_then_trigger();
+  stage_activations<MT>(a, xs, cs, red, rscale);
+
+  // compute cursor
+  int c_task = blockIdx.x * GEMV_WPB + warp, c_b = 0, c_out0 = 0;
+  const uint32_t* c_q;
+  const __half *c_s, *c_bias = nullptr;
+  if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
+  float acc[R][MT];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+
+  auto compute = [&](const int slot) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = chunk_it(c_b * U + u);
+      if (it < NIT) {
+        const int j = lr + LPR * it;
+        uint4 wv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) wv[r] = ring[(slot * RU + r * U + u) * NT + tid];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < M) {
+            const uint4* xc = xs + (size_t)(m * 4) * NCH + j;
+            float p[R][2];
+#pragma unroll
+            for (int r = 0; r < R; ++r) p[r][0] = p[r][1] = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              const uint4 xv = xc[wi * NCH];
+#pragma unroll
+              for (int r = 0; r < R; ++r) word_dot(p[r][0], p[r][1], (&wv[r].x)[wi], xv);
+            }
+            const float c = cs[(size_t)m * NCH + j];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+              acc[r][m] = fmaf(fmaf(16.0f, p[r][0] + p[r][1], -c), __half2float(sc[slot][r * U + u]), acc[r][m]);
+          }
+        }
+      }
+    }
+    if (++c_b < NB) return;
+    // task complete: reduce over the half-warp (and across half-warps for KS = 2), write
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int o = (KS == 2 ? 16 : 8); o > 0; o >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], o);
+      }
+    if (SILU) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const float other = __shfl_xor_sync(0xffffffffu, acc[r][m], 16);
+          const int row = c_out0 + r;
+          if (m < M && hw == 0 && lr == 0 && row < a.N) {
+            const float g = __half2float(__float2half_rn(acc[r][m]));
+            const float uu = __half2float(__float2half_rn(other));
+            a.y[(size_t)m * a.N + row] = __float2half_rn(g / (1.0f + expf(-g)) * uu);
+          }
+        }
+    } else if (lr == 0 && (KS == 1 || hw == 0)) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = c_out0 + r;
+        if (row < a.N) {
+          const float bv = c_bias ? __half2float(c_bias[r]) : 0.f;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+              float v = acc[r][m] + bv;
+              if (a.residual) v += __half2float(a.residual[(size_t)m * a.N + row]);
+              a.y[(size_t)m * a.N + row] = __float2half_rn(v);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+    c_b = 0;
+    c_task += nwarps;
+    if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
+  };
+
+  while (c_task < ntask) {
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
+      issue(slot ^ 1);
+      cp_async_wait<1>();  // this lane's batch in `slot` has landed
+      compute(slot);
+      if (c_task >= ntask) break;
+    }
+  }
+  cp_async_wait<0>();
+}
+
+template <int NCH, int R, int KS, int MT, bool SILU>
+static int launch_fast(const GemvArgs& a, cudaStream_t s) {
+  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU>;
+  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * GEMV_RU * GEMV_WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    configured = true;
+  }
+  int bps = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, GEMV_WPB * 32, smem) != cudaSuccess || bps < 1)
+    bps = 1;
+  constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
+  const int ntask = (a.N + RPT - 1) / RPT;
+  int blocks = std::min((ntask + GEMV_WPB - 1) / GEMV_WPB, bps * num_sms());
+  blocks = std::max(blocks, 1);
+  cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(GEMV_WPB * 32), smem, s, a);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+template <int MT, bool SILU>
+static int dispatch_fast(const GemvArgs& a, cudaStream_t s, bool* used) {
+  *used = true;
+  if (SILU) {
+    if (a.K == 3584) return launch_fast<112, 2, 1, MT, true>(a, s);
+  } else {
+    if (a.K == 3584) return launch_fast<112, 1, 1, MT, false>(a, s);
+    if (a.K == 18944) return launch_fast<592, 1, 2, MT, false>(a, s);
+  }
+  *used = false;
+  return W4A16_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 template <int LPR, int MT, bool SILU>
 static int launch_one(const GemvArgs& a, cudaStream_t s) {
   auto kern = gemv_w4a16_kernel<LPR, MT, SILU>;
-  const size_t smem = (size_t)MT * a.K * 2;
+  const size_t smem = (size_t)MT * a.K * 2 + (size_t)MT * (a.K / 32) * 4;
   static int configured = 0;
   static int blocks_per_sm = 0;
   if (!configured) {
@@ -307,6 +556,21 @@ int gemv_cuda_core_supported(int M, int K) { return M >= 1 && M <= 4 && (long)M 
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s) {
   if (!gemv_cuda_core_supported(a.M, a.K))
     return set_error(W4A16_ERR_SHAPE, "gemv: M=%d K=%d outside the CUDA-core path (M<=4, M*K<=49152)", a.M, a.K);
+  // the fast path moves two rows per half-warp: every segment (and N) even
+  bool even_rows = a.N >= 2 && a.N % 2 == 0;
+  for (int i = 0; i < a.nseg; ++i) even_rows = even_rows && (a.seg[i].rows % 2 == 0);
+  if (even_rows) {
+    bool used = false;
+    int rc = W4A16_OK;
+    if (silu) {
+      rc = a.M == 1 ? dispatch_fast<1, true>(a, s, &used)
+                    : (a.M == 2 ? dispatch_fast<2, true>(a, s, &used) : dispatch_fast<4, true>(a, s, &used));
+    } else {
+      rc = a.M == 1 ? dispatch_fast<1, false>(a, s, &used)
+                    : (a.M == 2 ? dispatch_fast<2, false>(a, s, &used) : dispatch_fast<4, false>(a, s, &used));
+    }
+    if (used) return rc;
+  }
   if (silu) {
     if (a.M == 1) return dispatch_lpr<1, true>(a, s);
     if (a.M == 2) return dispatch_lpr<2, true>(a, s);

@@ -30,11 +30,11 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s);
 int gemv_cuda_core_supported(int M, int K);
 
-// Paged attention (+ fused split-K combine).
+// Paged attention (+ fused split-K combine, optionally fused RoPE + append).
 struct AttnArgs {
-  const __half* q;          // [B][Hq][D] with row pitch q_stride
-  const __half* k_pool;     // [pages][Hkv][16][D]
-  const __half* v_pool;
+  const __half* q;          // [B][Hq][D] with row pitch q_stride (fused: q | k_new | v_new rows)
+  __half* k_pool;           // [pages][Hkv][16][D] (written only by the fused variant)
+  __half* v_pool;
   const int32_t* block_table;
   const int32_t* context_lens;
   __half* out;              // [B][Hq][D]
@@ -44,8 +44,11 @@ struct AttnArgs {
   int32_t* err_flag;
   int q_stride, num_pages, max_blocks, B, Hq, Hkv, P, part_tokens;
   float scale_log2;         // sm_scale * log2(e)
+  int fuse_rope_append;     // 1: rotate q and k_new at len-1, append k_new/v_new, then attend
+  float inv_freq[64];       // RoPE inverse frequencies (fused variant)
 };
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
+constexpr int ATT_MAX_PARTITIONS = 1024;
 size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P);
 
 // RoPE + KV append.

@@ -10,11 +10,12 @@
 // производительности") reports the graph-captured decode as the steady state.
 //
 // One decode step = embedding (+ device-side context_lens advance), then per
-// layer: [RMSNorm + q|k|v GEMV + bias] -> [RoPE + KV append] -> [paged GQA
+// layer: [RMSNorm + q|k|v GEMV + bias] -> [RoPE + KV append + paged GQA
 // attention + split-K combine] -> [o GEMV + residual] -> [RMSNorm + gate|up
 // GEMV + SiLU-mul] -> [down GEMV + residual], then [final RMSNorm + lm_head +
 // argmax].  Every kernel is launched with programmatic dependent launch, so
-// a GEMV streams its first weights while its predecessor finishes.
+// a GEMV streams its first weights, and the attention its KV pages, while
+// the predecessor finishes.
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -195,29 +196,13 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   g.N = nqkv;
   if ((rc = launch_gemv(g, false, s))) return rc;
 
-  RopeArgs r = {};
-  r.q = m->qkv;
-  r.k = m->qkv + Hq * D;
-  r.v = m->qkv + (Hq + Hkv) * D;
-  r.k_pool = reinterpret_cast<__half*>(L.k_pool);
-  r.v_pool = reinterpret_cast<__half*>(L.v_pool);
-  r.block_table = bt;
-  r.context_lens = lens;
-  r.err_flag = m->err_flag;
-  r.stride_q = r.stride_kv = nqkv;
-  r.num_pages = c.num_pages;
-  r.max_blocks = max_blocks;
-  r.B = B;
-  r.Hq = Hq;
-  r.Hkv = Hkv;
-  std::memcpy(r.inv_freq, m->inv_freq, sizeof(r.inv_freq));
-  if ((rc = launch_rope_append(r, s))) return rc;
-
+  // RoPE of q and the new k, the KV append and the paged attention are one
+  // kernel: it prefetches this partition's pages while the q|k|v GEMV runs.
   AttnArgs a = {};
   a.q = m->qkv;
   a.q_stride = nqkv;
-  a.k_pool = reinterpret_cast<const __half*>(L.k_pool);
-  a.v_pool = reinterpret_cast<const __half*>(L.v_pool);
+  a.k_pool = reinterpret_cast<__half*>(L.k_pool);
+  a.v_pool = reinterpret_cast<__half*>(L.v_pool);
   a.block_table = bt;
   a.context_lens = lens;
   a.out = m->att;
@@ -235,6 +220,8 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   a.P = m->P;
   a.part_tokens = m->part_tokens;
   a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+  a.fuse_rope_append = 1;
+  std::memcpy(a.inv_freq, m->inv_freq, sizeof(a.inv_freq));
   if ((rc = launch_paged_attention(a, s))) return rc;
 
   GemvArgs o = {};
@@ -307,7 +294,7 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
 
 extern "C" int decode_step_kernel_count(w4a16_model* m, int B) {
   (void)B;
-  return m ? 2 + 6 * m->cfg.n_layers : 0;
+  return m ? 2 + 5 * m->cfg.n_layers : 0;
 }
 
 extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tokens_out, const int32_t* block_table,
