@@ -82,11 +82,12 @@ def lib_path() -> str:
 
 
 def load() -> ctypes.CDLL:
-    """Load the built library; raises if it has not been built."""
+    """Load the built library; raises if it has not been built.  Setting
+    W4A16_TRACE=1 loads the kernel-timeline build instead."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            path = _build.TRACE_LIB if os.environ.get("W4A16_TRACE") == "1" else _build.LIB
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"CUDA library {path} is missing: build it with "
@@ -96,6 +97,11 @@ def load() -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
+            if hasattr(lib, "w4a16_trace_start"):
+                lib.w4a16_trace_start.restype = I32
+                lib.w4a16_trace_start.argtypes = [P, ctypes.c_uint]
+                lib.w4a16_trace_count.restype = ctypes.c_uint
+                lib.w4a16_trace_count.argtypes = []
             _lib = lib
     return _lib
 

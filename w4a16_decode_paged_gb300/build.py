@@ -49,16 +49,28 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+TRACE_BUILD = os.path.join(HERE, "_build_trace")
+TRACE_LIB = os.path.join(TRACE_BUILD, "libw4a16_gb300_trace.so")
+
+
+def build_trace(force: bool = False) -> str:
+    """Kernel-timeline build (-DW4A16_TRACE): a separate library that adds
+    w4a16_trace_start / w4a16_trace_count; the product library is untouched."""
+    return build(force=force, extra_flags=["-DW4A16_TRACE", "-rdc=true"], out=TRACE_LIB)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str = None) -> str:
+    lib = out or LIB
+    bdir = os.path.dirname(lib)
+    if not force and os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(bdir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +81,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
+    tmp = lib + f".tmp{os.getpid()}"
+    rdc = ["-rdc=true"] if "-rdc=true" in flags else []
+    cmd = [cc, *ARCH, *rdc, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

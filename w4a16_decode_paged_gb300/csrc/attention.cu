@@ -29,9 +29,16 @@
 
 namespace w4 {
 
+#ifdef W4A16_TRACE
+__device__ TraceRec* g_trace_buf = nullptr;
+__device__ unsigned int g_trace_cap = 0;
+__device__ unsigned int g_trace_n = 0;
+#endif
+
 constexpr int ATT_D = 128;
 constexpr int ATT_PAGE = 16;
-constexpr int ATT_NW = 4;          // warps per CTA
+constexpr int ATT_NW = 8;          // warps per CTA
+constexpr int ATT_MAX_CLUSTER = 8; // partitions merged through distributed shared memory
 constexpr int ATT_STAGES = 2;      // page slots per warp
 constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice
 constexpr uint32_t ATT_SLICE_BYTES = ATT_SLICE * 2;  // 4096
@@ -67,14 +74,15 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + ATT_RING_BYTES);
   float* sbuf = reinterpret_cast<float*>(bars + ATT_NW * ATT_STAGES);  // [NW][8][16]
   float* corr = sbuf + ATT_NW * 8 * 16;                               // [NW][8]
-  __shared__ float s_q[G][ATT_D];      // this group's q (rotated in the fused variant)
-  __shared__ __half s_knew[ATT_D];     // fused: rotated new k and new v
-  __shared__ __half s_vnew[ATT_D];
+  __shared__ __align__(16) float s_q[G][ATT_D];   // this group's q (rotated in the fused variant)
+  __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
+  __shared__ __align__(16) __half s_vnew[ATT_D];
   __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, kvh = blockIdx.y, p = blockIdx.x;
+  W4_TRACE_SCOPE(a.tag);
 
   if (tid < ATT_NW * ATT_STAGES) mbar_init(&bars[tid], 1);
   fence_mbar_init();
@@ -83,7 +91,10 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   // itself, and the lengths were written at the start of the step, so it
   // may fetch pages before its predecessor (the q|k|v GEMV) finishes.  The
   // plain variant may be preceded by a kernel that appended to the pools.
-  if (!FUSE) pdl_wait_then_trigger();
+  if (!FUSE) {
+    pdl_wait_then_trigger();
+    W4_TRACE_WAITED();
+  }
 
   const int L = __ldcg(&a.context_lens[b]);
   const int t_begin = p * a.part_tokens;
@@ -98,13 +109,16 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   uint64_t* mybar = bars + warp * ATT_STAGES;
   __half* myring = ring + (size_t)warp * ATT_STAGES * 2 * ATT_SLICE;
 
-  auto page_id = [&](int li) -> int {  // li: index into this warp's page list
+  auto page_load = [&](int li) -> int {  // li: index into this warp's page list
     const int gi = pg0 + warp + li * ATT_NW;
     const int pg = (gi < a.max_blocks) ? __ldcg(&bt[gi]) : -1;
     return (pg >= 0 && pg < a.num_pages) ? pg : -1;
   };
-  auto issue = [&](int li) {  // lane 0 only
-    const int pg = page_id(li);
+  // Each lane loads one of this warp's page ids up front (one L2 round trip
+  // for all of them); page_of() broadcasts it.  Must be called warp-wide.
+  const int pg_lane = lane < my_pages ? page_load(lane) : -1;
+  auto page_of = [&](int li) -> int { return li < 32 ? __shfl_sync(0xffffffffu, pg_lane, li) : page_load(li); };
+  auto issue = [&](int li, int pg) {  // lane 0 only
     uint64_t* bar = &mybar[li % ATT_STAGES];
     __half* dst = myring + (size_t)(li % ATT_STAGES) * 2 * ATT_SLICE;
     if (pg >= 0) {
@@ -117,25 +131,39 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       if (a.err_flag) atomicOr(a.err_flag, 1);
     }
   };
-  if (lane == 0) {
-    for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) issue(li);
+  for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) {
+    const int pg = page_of(li);
+    if (lane == 0) issue(li, pg);
   }
-  if (FUSE) pdl_wait_then_trigger();
+  if (FUSE) {
+    pdl_wait_then_trigger();
+    W4_TRACE_WAITED();
+  }
 
   // ---- q (and, fused, RoPE of q and the new k; append of k and v) ----------
   const __half* qb = a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D;
   const int pos = L - 1;
   if (FUSE) {
+    // raw q | k_new | v_new of this group into shared memory (16-byte loads),
+    // and the 64 (cos, sin) pairs of this position, each computed once
+    __shared__ __align__(16) __half s_raw[(G + 2) * ATT_D];
+    __shared__ float s_cos[ATT_D / 2], s_sin[ATT_D / 2];
     const __half* kn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + kvh) * ATT_D;
     const __half* vn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + a.Hkv + kvh) * ATT_D;
-    const float fpos = (float)(pos > 0 ? pos : 0);
+    for (int c = tid; c < (G + 2) * (ATT_D / 8); c += blockDim.x) {
+      const int h = c / (ATT_D / 8), w = c % (ATT_D / 8);
+      const __half* src = h < G ? qb + h * ATT_D : (h == G ? kn : vn);
+      reinterpret_cast<uint4*>(s_raw)[c] = reinterpret_cast<const uint4*>(src)[w];
+    }
+    if (tid < ATT_D / 2) {
+      const float ang = __fmul_rn((float)(pos > 0 ? pos : 0), a.inv_freq[tid]);  // the fp32 product
+      sincosf(ang, &s_sin[tid], &s_cos[tid]);
+    }
+    __syncthreads();
     for (int idx = tid; idx < (G + 1) * (ATT_D / 2); idx += blockDim.x) {
       const int h = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
-      const float ang = __fmul_rn(fpos, a.inv_freq[i]);  // the fp32 product, no contraction
-      float sn, cs;
-      sincosf(ang, &sn, &cs);
-      const __half* src = h < G ? qb + h * ATT_D : kn;
-      const float x0 = __half2float(src[i]), x1 = __half2float(src[i + ATT_D / 2]);
+      const float cs = s_cos[i], sn = s_sin[i];
+      const float x0 = __half2float(s_raw[h * ATT_D + i]), x1 = __half2float(s_raw[h * ATT_D + i + ATT_D / 2]);
       const __half r0 = __float2half_rn(x0 * cs - x1 * sn);
       const __half r1 = __float2half_rn(x1 * cs + x0 * sn);
       if (h < G) {
@@ -146,7 +174,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
         s_knew[i + ATT_D / 2] = r1;
       }
     }
-    for (int d = tid; d < ATT_D; d += blockDim.x) s_vnew[d] = vn[d];
+    for (int d = tid; d < ATT_D; d += blockDim.x) s_vnew[d] = s_raw[(G + 1) * ATT_D + d];
     __syncthreads();
     if (pos >= t_begin && pos < t_end) {  // this partition holds the new token: append it
       const int blk = pos / ATT_PAGE;
@@ -167,6 +195,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     __syncthreads();
   }
 
+  W4_TRACE_MARK(0);
   // q for this lane's dims: lane = (tq, ds); dims [16 ds, 16 ds + 16)
   const int tq = lane >> 3, ds = lane & 7;
   float2 qr[G][8];
@@ -195,7 +224,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     __half* Vs = Ks + ATT_SLICE;
     const int gi = warp + li * ATT_NW;  // page index within the partition
     const int tok0 = (pg0 + gi) * ATT_PAGE;
-    const bool page_ok = page_id(li) >= 0;
+    const bool page_ok = page_of(li) >= 0;
     const int nv = page_ok ? min(ATT_PAGE, t_end - tok0) : 0;
     if (FUSE && page_ok && pos >= tok0 && pos < tok0 + ATT_PAGE) {
       // the page was fetched before the append: patch the new token's row
@@ -299,9 +328,12 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     }
     __syncwarp();
     // refill this stage with the page ATT_STAGES ahead
-    if (lane == 0 && li + ATT_STAGES < my_pages) {
-      fence_proxy_async_smem();
-      issue(li + ATT_STAGES);
+    if (li + ATT_STAGES < my_pages) {
+      const int pg = page_of(li + ATT_STAGES);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(li + ATT_STAGES, pg);
+      }
     }
   }
   // Every issued copy has been consumed unless a wait timed out; in that case
@@ -313,6 +345,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       (void)wait_phase(&mybar[x % ATT_STAGES], (x / ATT_STAGES) & 1);
   }
   __syncthreads();  // all warps done with their rings
+  W4_TRACE_MARK(1);
 
   // ---- merge the warps' states in shared memory (ring reused) ------------
   float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
@@ -331,48 +364,90 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
   __syncthreads();
 
-  const int d = tid;  // 128 threads = 128 dims
+  const int d = tid & (ATT_D - 1);  // dim of this thread; two threads per dim split the heads
+  const int hpar = tid / ATT_D;     // 0 or 1
   const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
-  if (a.P == 1) {
+  // this CTA's (partition's) merged state: cp_o[h][d] = sum e^(m - M) o,
+  // cp_ml[h] = (M, sum e^(m - M) l)
+  float* cp_o = mml + ATT_NW * 8 * 2;  // [G][128]
+  float* cp_ml = cp_o + G * ATT_D;     // [G][2]
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < G; ++h) {
+    if ((h & 1) != hpar) continue;
+    float M = -INFINITY;
+    for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < ATT_NW; ++w) {
+        const float mw = mml[(w * 8 + h) * 2];
+        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        acc += mo[(w * 8 + h) * ATT_D + d] * f;
+        den += mml[(w * 8 + h) * 2 + 1] * f;
+      }
+    }
+    if (a.P == 1) {
+      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+    } else {
+      cp_o[h * ATT_D + d] = acc;
+      if (d == 0) {
+        cp_ml[h * 2] = M;
+        cp_ml[h * 2 + 1] = den;
+      }
+    }
+  }
+  if (a.P == 1) return;
+  W4_TRACE_MARK(2);
+
+  if (a.use_cluster) {
+    // All partitions of this (sequence, kv head) form one thread-block
+    // cluster: merge them through distributed shared memory.  CTA rank r
+    // produces the heads h with h % P == r.
+    cluster_sync();
+    const int P = a.P;
+    const unsigned int rank = cluster_ctarank();
+    for (int h = (int)rank + hpar * P; h < G; h += 2 * P) {
+      // all remote values first (independent loads), then the merge
+      float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
+#pragma unroll
+      for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
+        if (j < P) {
+          mj[j] = ld_dsmem(&cp_ml[h * 2], j);
+          lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
+          oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
+        }
+      }
       float M = -INFINITY;
-      for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+#pragma unroll
+      for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
+        if (j < P) M = fmaxf(M, mj[j]);
       float acc = 0.f, den = 0.f;
       if (M != -INFINITY) {
-        for (int w = 0; w < ATT_NW; ++w) {
-          const float mw = mml[(w * 8 + h) * 2];
-          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-          acc += mo[(w * 8 + h) * ATT_D + d] * f;
-          den += mml[(w * 8 + h) * 2 + 1] * f;
+#pragma unroll
+        for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
+          if (j < P) {
+            const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+            acc += oj[j] * f;
+            den += lj[j] * f;
+          }
         }
       }
       a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
     }
+    cluster_sync();  // keep every CTA's shared memory alive until all reads are done
     return;
   }
 
-  // several partitions: write this partition's partial, then the ticket
+  // several partitions without a cluster: this partition's partial goes to
+  // the workspace, then the ticket
+  __syncthreads();
   if (t_begin < L) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
-      for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
-      float acc = 0.f, den = 0.f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < ATT_NW; ++w) {
-          const float mw = mml[(w * 8 + h) * 2];
-          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-          acc += mo[(w * 8 + h) * ATT_D + d] * f;
-          den += mml[(w * 8 + h) * 2 + 1] * f;
-        }
-      }
-      const size_t slot = (qh0 + h) * a.P + p;
-      a.ws_o[slot * ATT_D + d] = acc;
-      if (d == 0) {
-        a.ws_ml[slot * 2 + 0] = M;
-        a.ws_ml[slot * 2 + 1] = den;
-      }
+    for (int idx = tid; idx < G * ATT_D; idx += blockDim.x) {
+      const int h = idx / ATT_D, dd = idx % ATT_D;
+      a.ws_o[((qh0 + h) * a.P + p) * ATT_D + dd] = cp_o[idx];
+    }
+    if (tid < G) {
+      a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 0] = cp_ml[tid * 2];
+      a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 1] = cp_ml[tid * 2 + 1];
     }
   }
   __threadfence();
@@ -413,7 +488,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
   __syncthreads();
 #pragma unroll 1
-  for (int h = 0; h < G; ++h) {
+  for (int h = hpar; h < G; h += 2) {
     const float* wts = cw + h * Pv;
     const float* src = a.ws_o + ((qh0 + h) * a.P) * ATT_D + d;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
@@ -446,15 +521,32 @@ static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
     configured = true;
   }
   dim3 grid(a.P, a.Hkv, a.B);
-  cudaError_t e = a.fuse_rope_append ? launch_pdl(k1, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a)
-                                     : launch_pdl(k0, grid, dim3(ATT_NW * 32), ATT_SMEM, s, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(ATT_NW * 32);
+  cfg.dynamicSmemBytes = ATT_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.use_cluster ? a.P : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = a.fuse_rope_append ? cudaLaunchKernelEx(&cfg, k1, a) : cudaLaunchKernelEx(&cfg, k0, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
 
-int launch_paged_attention(const AttnArgs& a, cudaStream_t s) {
-  if (a.P > ATT_MAX_PARTITIONS)
-    return set_error(W4A16_ERR_SHAPE, "paged attention: %d partitions > %d", a.P, ATT_MAX_PARTITIONS);
+int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
+  if (a_in.P > ATT_MAX_PARTITIONS)
+    return set_error(W4A16_ERR_SHAPE, "paged attention: %d partitions > %d", a_in.P, ATT_MAX_PARTITIONS);
+  AttnArgs a = a_in;
+  // up to 8 partitions (a portable cluster) merge through distributed shared
+  // memory; more go through the workspace and a last-CTA ticket
+  a.use_cluster = (a.P > 1 && a.P <= ATT_MAX_CLUSTER) ? 1 : 0;
   switch (a.Hq / a.Hkv) {
     case 1: return launch_attn_g<1>(a, s);
     case 2: return launch_attn_g<2>(a, s);
@@ -519,13 +611,15 @@ int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
   return W4A16_OK;
 }
 
+// Partition size: up to 1024 tokens, 128-token partitions (one page per warp,
+// every page fetched before the CTA's dependency wait) merged within one
+// cluster; longer contexts use 512-token partitions.
 int default_partition(int B, int Hkv, int max_context) {
-  const int want = std::max(1, (2 * num_sms()) / std::max(1, B * Hkv));
-  int pt = (max_context + want - 1) / want;
-  pt = (pt + 63) / 64 * 64;
-  if (pt < 64) pt = 64;
-  if (pt > 512) pt = 512;
-  return pt;
+  (void)B;
+  (void)Hkv;
+  if (max_context <= ATT_MAX_CLUSTER * 128) return 128;  // one page per warp, one cluster
+  if (max_context <= ATT_MAX_CLUSTER * 512) return 512;
+  return 512;
 }
 
 }  // namespace w4

@@ -202,6 +202,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Thread-block cluster helpers (distributed shared memory).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ unsigned int cluster_ctarank() {
+  unsigned int r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Load a float from the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_dsmem(const float* p, int rank) {
+  // Not volatile: the loads are ordered after the cluster barrier (which is
+  // volatile with a memory clobber) and may overlap one another.
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
+
 // 1-D bulk async copy global -> shared, completion signalled on `bar`.
 // src, dst 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -211,5 +231,56 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// Optional kernel timeline (builds with -DW4A16_TRACE only).  Thread 0 of
+// every CTA records the global timer at entry, when griddepcontrol.wait
+// returns, and at exit, with the launch's tag (its index in the step).
+// ---------------------------------------------------------------------------
+struct TraceRec {
+  unsigned long long t_entry, t_wait, t_exit, mark[3];
+  unsigned int tag, cta, smid, pad;
+};
+static_assert(sizeof(TraceRec) == 64, "trace record layout is part of the trace API");
+#ifdef W4A16_TRACE
+extern __device__ TraceRec* g_trace_buf;
+extern __device__ unsigned int g_trace_cap;
+extern __device__ unsigned int g_trace_n;
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+struct TraceScope {
+  unsigned long long t0, tw, m[3];
+  unsigned int tag;
+  __device__ TraceScope(unsigned int tg) : t0(trace_now()), tw(0), m{0, 0, 0}, tag(tg) {}
+  __device__ void waited() { tw = trace_now(); }
+  __device__ void mark(int k) { m[k] = trace_now(); }
+  __device__ ~TraceScope() {
+    if (threadIdx.x == 0 && g_trace_buf != nullptr) {
+      const unsigned int i = atomicAdd(&g_trace_n, 1u);
+      if (i < g_trace_cap) {
+        unsigned int sm;
+        asm volatile("mov.u32 %0, %smid;" : "=r"(sm));
+        g_trace_buf[i] = TraceRec{t0, tw, trace_now(), {m[0], m[1], m[2]}, tag, (unsigned int)blockIdx.x, sm, 0u};
+      }
+    }
+  }
+};
+#define W4_TRACE_SCOPE(tag) ::w4::TraceScope w4_trace_scope_(tag)
+#define W4_TRACE_WAITED() w4_trace_scope_.waited()
+#define W4_TRACE_MARK(k) w4_trace_scope_.mark(k)
+#else
+#define W4_TRACE_SCOPE(tag) \
+  do {                     \
+  } while (0)
+#define W4_TRACE_WAITED() \
+  do {                    \
+  } while (0)
+#define W4_TRACE_MARK(k) \
+  do {                   \
+  } while (0)
+#endif
 
 }  // namespace w4

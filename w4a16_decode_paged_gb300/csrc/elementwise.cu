@@ -63,8 +63,10 @@ int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) embedding_kernel(const __half* __restrict__ embed, int vocab, int H,
                                                         const int32_t* tokens, __half* x, int32_t* err_flag,
-                                                        int32_t* lens) {
+                                                        int32_t* lens, int tag) {
+  W4_TRACE_SCOPE(tag);
   pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
   const int b = blockIdx.x;
   const int tok = tokens[b];
   const bool ok = tok >= 0 && tok < vocab;
@@ -76,9 +78,9 @@ __global__ void __launch_bounds__(256) embedding_kernel(const __half* __restrict
 }
 
 int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
-                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s) {
-  cudaError_t e =
-      launch_pdl(embedding_kernel, dim3(B), dim3(256), 0, s, embed, vocab, H, tokens, x, err_flag, lens_to_advance);
+                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s, int tag) {
+  cudaError_t e = launch_pdl(embedding_kernel, dim3(B), dim3(256), 0, s, embed, vocab, H, tokens, x, err_flag,
+                             lens_to_advance, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "embedding launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -107,7 +109,9 @@ __global__ void __launch_bounds__(LM_WPB * 32) lm_head_kernel(const __grid_const
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int H = a.H, NC = H / 8;
+  W4_TRACE_SCOPE(a.tag);
   pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
 
   // stage x (RMS-normalised when gamma is given)
   for (int b = 0; b < a.B; ++b) {

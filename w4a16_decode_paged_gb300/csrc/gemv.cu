@@ -54,7 +54,10 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
                                                   float* rscale) {
   const int K = a.K, M = a.M, NCH = K >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarp = blockDim.x >> 5;
   if (a.gamma != nullptr) {
+    // one pass: partial sums of squares per warp, one barrier, every thread
+    // then adds the warps' partials itself
     for (int m = 0; m < M; ++m) {
       float ss = 0.f;
       for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
@@ -67,14 +70,13 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
         }
       }
       ss = warp_sum(ss);
-      if (lane == 0) red[warp][0] = ss;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float t = 0.f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w][0];
-        rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);
-      }
-      __syncthreads();
+      if (lane == 0) red[warp][m] = ss;
+    }
+    __syncthreads();
+    for (int m = 0; m < M; ++m) {
+      float t = 0.f;
+      for (int w = 0; w < nwarp; ++w) t += red[w][m];
+      rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);  // per-thread copy
     }
   }
   for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
@@ -111,11 +113,24 @@ constexpr uint32_t NIB_MASK = 0x03C003C0u;  // top four mantissa bits of both ha
 constexpr uint32_t ONE_H2 = 0x3C003C00u;    // half2{1, 1}
 
 // S += sum over the 8 nibbles of word w of (1 + u/16) * x, x in staged order.
+// The shifts are written as integer multiplies (w << k == w * 2^k, and
+// w >> k == high word of w * 2^(32-k)) so they issue on the FMA pipe and
+// leave the half-rate ALU pipe to the four LOP3s.
+__device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t mul) {
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(mul));
+  return d;
+}
+__device__ __forceinline__ uint32_t shr_fma(uint32_t w, uint32_t mul) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(mul));
+  return d;
+}
 __device__ __forceinline__ void word_dot(float& p0, float& p1, uint32_t w, const uint4 xv) {
-  fma2_f16_f32_split(p0, p1, and_or(w << 6, NIB_MASK, ONE_H2), xv.x);
-  fma2_f16_f32_split(p0, p1, and_or(w << 2, NIB_MASK, ONE_H2), xv.y);
-  fma2_f16_f32_split(p0, p1, and_or(w >> 2, NIB_MASK, ONE_H2), xv.z);
-  fma2_f16_f32_split(p0, p1, and_or(w >> 6, NIB_MASK, ONE_H2), xv.w);
+  fma2_f16_f32_split(p0, p1, and_or(shl_fma(w, 64u), NIB_MASK, ONE_H2), xv.x);          // w << 6
+  fma2_f16_f32_split(p0, p1, and_or(shl_fma(w, 4u), NIB_MASK, ONE_H2), xv.y);           // w << 2
+  fma2_f16_f32_split(p0, p1, and_or(shr_fma(w, 1u << 30), NIB_MASK, ONE_H2), xv.z);     // w >> 2
+  fma2_f16_f32_split(p0, p1, and_or(shr_fma(w, 1u << 26), NIB_MASK, ONE_H2), xv.w);     // w >> 6
 }
 
 template <int LPR, int MT, bool SILU>
@@ -135,6 +150,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
   const int slot = lane / LPR, lr = lane % LPR;
   const int ntask = (a.N + RPT - 1) / RPT;
   const int nwarps = gridDim.x * GEMV_WPB;
+  W4_TRACE_SCOPE(a.tag);
 
   // Weights do not depend on the previous kernel: issue this warp's first
   // batch of weight loads before waiting for it.
@@ -186,6 +202,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
   }
 
   pdl_wait_then_trigger();  // x (and residual) come from the previous kernel
+  W4_TRACE_WAITED();
 
   stage_activations<MT>(a, xs, cs, red, rscale);
 
@@ -298,11 +315,12 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 //   KS = 2: both half-warps work on the same R rows and split K (long K).
 // All strides are compile-time immediates.
 // ---------------------------------------------------------------------------
-constexpr int GEMV_RU = 8;  // chunks per lane per batch (R rows x U chunks)
-
-template <int NCH, int R, int KS, int MT, bool SILU>
-__global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
-  constexpr int LPR = 16, RU = GEMV_RU, U = RU / R;
+// RU: chunks per lane per batch (R rows x U chunks).  K = 3584 uses 8 so a
+// whole row (7 chunks per lane) is in flight before the dependency wait;
+// the long-K down projection uses 4 to fit more CTAs per SM.
+template <int NCH, int R, int KS, int MT, bool SILU, int RU>
+__global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
+  constexpr int LPR = 16, U = RU / R;
   constexpr int K = NCH * 32;
   constexpr int NIT = NCH / LPR;                 // chunks per lane when one half-warp covers K
   constexpr int NIT_L = (NIT + KS - 1) / KS;     // this lane's share (upper bound)
@@ -311,7 +329,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_co
   constexpr int SROW = K / 128;
   constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
   constexpr int NT = GEMV_WPB * 32;
-  static_assert(RU % R == 0, "R must divide GEMV_RU");
+  static_assert(RU % R == 0, "R must divide RU");
   static_assert(!(SILU && KS == 2), "SiLU pairs gate and up across half-warps");
   extern __shared__ uint4 smem[];
   uint4* xs = smem;                                          // [MT][4][NCH]
@@ -325,6 +343,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_co
   const int M = a.M;
   const int ntask = (a.N + RPT - 1) / RPT;
   const int nwarps = gridDim.x * GEMV_WPB;
+  W4_TRACE_SCOPE(a.tag);
 
   // first output row of this lane's rows for task t, and the weight-row base
   auto rows_of = [&](int t, int& out0, const uint32_t*& q, const __half*& sp, const __half*& bp) {
@@ -379,6 +398,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_co
 
   issue(0);  // weights do not depend on the previous kernel
   pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
   stage_activations<MT>(a, xs, cs, red, rscale);
 
   // compute cursor
@@ -482,10 +502,10 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_fast(const __grid_co
   cp_async_wait<0>();
 }
 
-template <int NCH, int R, int KS, int MT, bool SILU>
+template <int NCH, int R, int KS, int MT, bool SILU, int RU>
 static int launch_fast(const GemvArgs& a, cudaStream_t s) {
-  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU>;
-  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * GEMV_RU * GEMV_WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
+  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU>;
+  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * RU * GEMV_WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -507,10 +527,10 @@ template <int MT, bool SILU>
 static int dispatch_fast(const GemvArgs& a, cudaStream_t s, bool* used) {
   *used = true;
   if (SILU) {
-    if (a.K == 3584) return launch_fast<112, 2, 1, MT, true>(a, s);
+    if (a.K == 3584) return launch_fast<112, 2, 1, MT, true, 8>(a, s);
   } else {
-    if (a.K == 3584) return launch_fast<112, 1, 1, MT, false>(a, s);
-    if (a.K == 18944) return launch_fast<592, 1, 2, MT, false>(a, s);
+    if (a.K == 3584) return launch_fast<112, 1, 1, MT, false, 8>(a, s);
+    if (a.K == 18944) return launch_fast<592, 1, 2, MT, false, 4>(a, s);
   }
   *used = false;
   return W4A16_OK;

@@ -25,6 +25,7 @@ struct GemvArgs {
   int nseg;
   int M, K, N;
   float eps;
+  int tag;                 // launch index (kernel timeline builds only)
 };
 
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s);
@@ -45,7 +46,9 @@ struct AttnArgs {
   int q_stride, num_pages, max_blocks, B, Hq, Hkv, P, part_tokens;
   float scale_log2;         // sm_scale * log2(e)
   int fuse_rope_append;     // 1: rotate q and k_new at len-1, append k_new/v_new, then attend
+  int use_cluster;          // set by the launcher: partitions merged in a thread-block cluster
   float inv_freq[64];       // RoPE inverse frequencies (fused variant)
+  int tag;                  // launch index (kernel timeline builds only)
 };
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
 constexpr int ATT_MAX_PARTITIONS = 1024;
@@ -69,7 +72,7 @@ void rope_inv_freq_table(float theta, int D, float* out);
 
 int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s);
 int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
-                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s);
+                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s, int tag = 0);
 
 struct LmHeadArgs {
   const __half* x;      // [B][H]
@@ -81,6 +84,7 @@ struct LmHeadArgs {
   int B, H, vocab;
   const __half* gamma;  // optional fused final RMSNorm
   float eps;
+  int tag;              // launch index (kernel timeline builds only)
 };
 int launch_lm_head_argmax(const LmHeadArgs& a, cudaStream_t s);
 size_t lm_head_workspace_bytes(int B, int vocab);

@@ -174,7 +174,7 @@ extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
 }
 
 static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int max_blocks, const int32_t* lens, int B,
-                     cudaStream_t s) {
+                     cudaStream_t s, int tag0 = 0) {
   const w4a16_model_config& c = m->cfg;
   const w4a16_layer_weights& L = m->layers[l];
   const int D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, H = c.hidden, I = c.inter;
@@ -194,6 +194,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   g.M = B;
   g.K = H;
   g.N = nqkv;
+  g.tag = tag0;
   if ((rc = launch_gemv(g, false, s))) return rc;
 
   // RoPE of q and the new k, the KV append and the paged attention are one
@@ -222,6 +223,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
   a.fuse_rope_append = 1;
   std::memcpy(a.inv_freq, m->inv_freq, sizeof(a.inv_freq));
+  a.tag = tag0 + 1;
   if ((rc = launch_paged_attention(a, s))) return rc;
 
   GemvArgs o = {};
@@ -233,6 +235,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   o.M = B;
   o.K = Hq * D;
   o.N = H;
+  o.tag = tag0 + 2;
   if ((rc = launch_gemv(o, false, s))) return rc;
 
   GemvArgs gu = {};
@@ -246,6 +249,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   gu.M = B;
   gu.K = H;
   gu.N = I;
+  gu.tag = tag0 + 3;
   if ((rc = launch_gemv(gu, true, s))) return rc;
 
   GemvArgs dn = {};
@@ -257,6 +261,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   dn.M = B;
   dn.K = I;
   dn.N = H;
+  dn.tag = tag0 + 4;
   return launch_gemv(dn, false, s);
 }
 
@@ -273,10 +278,10 @@ extern "C" int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const i
 static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const int32_t* bt, int max_blocks,
                         int32_t* lens, int B, uint16_t* logits, cudaStream_t s) {
   const w4a16_model_config& c = m->cfg;
-  int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, s);
+  int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, s, 0);
   if (rc) return rc;
   for (int l = 0; l < c.n_layers; ++l)
-    if ((rc = run_layer(m, l, m->x, bt, max_blocks, lens, B, s))) return rc;
+    if ((rc = run_layer(m, l, m->x, bt, max_blocks, lens, B, s, 1 + 5 * l))) return rc;
   LmHeadArgs a = {};
   a.x = m->x;
   a.w = m->lm_head;
@@ -289,6 +294,7 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
   a.B = B;
   a.H = c.hidden;
   a.vocab = c.vocab;
+  a.tag = 1 + 5 * c.n_layers;
   return launch_lm_head_argmax(a, s);
 }
 
@@ -343,3 +349,28 @@ extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* to
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "decode_step: graph launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
+
+#ifdef W4A16_TRACE
+namespace w4 {
+extern __device__ TraceRec* g_trace_buf;
+extern __device__ unsigned int g_trace_cap;
+extern __device__ unsigned int g_trace_n;
+}
+// Kernel timeline (trace builds only): start recording into a device buffer
+// of `cap` records of 32 bytes; w4a16_trace_count returns how many were
+// written (synchronises the device).
+extern "C" W4A16_API int w4a16_trace_start(void* dev_buf, unsigned int cap) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyToSymbol(w4::g_trace_buf, &dev_buf, sizeof(void*));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(w4::g_trace_cap, &cap, sizeof(cap));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(w4::g_trace_n, &zero, sizeof(zero));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e == cudaSuccess ? W4A16_OK : set_error(W4A16_ERR_CUDA, "trace_start: %s", cudaGetErrorString(e));
+}
+extern "C" W4A16_API unsigned int w4a16_trace_count(void) {
+  unsigned int n = 0;
+  cudaDeviceSynchronize();
+  cudaMemcpyFromSymbol(&n, w4::g_trace_n, sizeof(n));
+  return n;
+}
+#endif
