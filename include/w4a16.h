@@ -92,13 +92,44 @@ W4A16_API int w4a16_version(void);
  *   bias     fp16 [N] or NULL
  *   residual fp16 [M][N] or NULL      added before the single fp16 rounding
  *   y        fp16 [M][N]              output (must not alias x)
- * Shapes: 1 <= M, K % 128 == 0, N >= 1.  The CUDA-core path handles M <= 4
- * with M*K <= 49152; larger M uses the tensor-core (tcgen05) path when built,
- * else returns W4A16_ERR_SHAPE.
+ * Shapes: 1 <= M <= 32, K % 128 == 0, N >= 1.  M <= 4 with M*K <= 49152
+ * runs on the CUDA cores; larger M on the tensor cores (see w4a16_gemm).
  * ------------------------------------------------------------------------ */
 W4A16_API int w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qweight, const uint16_t* scales,
                int N, const uint16_t* bias, const uint16_t* residual, uint16_t* y,
                w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * w4a16_gemm -- the same product for a decode batch (1 <= M <= 32) on the
+ * tensor cores (tcgen05 MMAs, fp32 accumulation in tensor memory).  The
+ * MMAs take the exact integer codes q; each 128-wide scale group is summed
+ * in tensor memory and multiplied by its fp32 scale on the way out, so the
+ * only roundings are fp32 accumulation and the final fp16 store.
+ * Projections with few 128-row tiles split K across CTAs when a workspace of
+ * w4a16_gemm_workspace_size() bytes is given (zeroed once before first use;
+ * every call leaves its counters zero); with workspace == NULL they run
+ * without the split.  Calls sharing a workspace must not overlap on the GPU.
+ * w4a16_gemv routes 5 <= M <= 32 here (without the split).
+ * ------------------------------------------------------------------------ */
+W4A16_API int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweight,
+                         const uint16_t* scales, int N, const uint16_t* bias,
+                         const uint16_t* residual, uint16_t* y, void* workspace,
+                         size_t workspace_bytes, w4a16_stream_t stream);
+/* Gated MLP front half for a batch: y = silu(G . x) * (U . x), gate and up
+ * rounded to fp16 before the SiLU. */
+W4A16_API int w4a16_gemm_silu_mul(const uint16_t* x, int M, int K, const uint32_t* qweight_gate,
+                                  const uint16_t* scales_gate, const uint32_t* qweight_up,
+                                  const uint16_t* scales_up, int N, uint16_t* y, void* workspace,
+                                  size_t workspace_bytes, w4a16_stream_t stream);
+W4A16_API size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu);
+
+/* Batched FP16 lm_head on the tensor cores: logits fp32 [B][vocab] = x . W^T,
+ * B <= 32, H % 128 == 0; and the row-wise argmax (lowest index on ties) with
+ * an optional fp16 copy of the logits. */
+W4A16_API int lm_head_logits_batched(const uint16_t* x, int B, int H, const uint16_t* lm_head,
+                                     int vocab, float* logits, w4a16_stream_t stream);
+W4A16_API int argmax_rows(const float* logits, int B, int vocab, int32_t* tokens_out,
+                          uint16_t* logits16, w4a16_stream_t stream);
 
 /* w4a16_gemv with the RMSNorm of x fused in front (the input norm of the
  * q/k/v projection): y = dequant(W) . (x / sqrt(mean(x^2) + eps) * gamma)

@@ -1,0 +1,99 @@
+"""Tensor-core (tcgen05) batched-decode GEMM, batched lm_head and argmax vs the
+CPU oracle.  GPU only (marked gpu)."""
+import numpy as np
+import pytest
+
+import oracle as orc
+from gpu_util import assert_close, to_dev, to_host
+from w4a16_decode_paged_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from w4a16_decode_paged_gb300 import api as _api
+    from w4a16_decode_paged_gb300 import build
+    build.build()
+    return _api
+
+
+@pytest.mark.parametrize("K,N", [(128, 128), (256, 200), (3584, 512), (3584, 4608), (18944, 3584), (896, 130)])
+@pytest.mark.parametrize("M", [1, 5, 17, 32])
+@pytest.mark.parametrize("split", [False, True])
+def test_w4a16_gemm_matches_oracle(api, K, N, M, split):
+    r = np.random.default_rng(K * 13 + N + M * 101 + split)
+    qw, s = synth.int4_weight(r, N, K)
+    x = synth.normal_fp16(r, (M, K))
+    bias = synth.normal_fp16(r, (N,), 0.1) if M % 2 else None
+    res = synth.normal_fp16(r, (M, N)) if split else None
+    ref = orc.w4a16_gemv(x, qw, s, bias=bias, residual=res)
+    y = api.w4a16_gemm(to_dev(x, torch), to_dev(qw, torch), to_dev(s, torch),
+                       bias=None if bias is None else to_dev(bias, torch),
+                       residual=None if res is None else to_dev(res, torch), split=split)
+    torch.cuda.synchronize()
+    assert_close(to_host(y), ref, what=f"gemm K={K} N={N} M={M} split={split}")
+
+
+def test_w4a16_gemm_repeat_calls_leave_counters_zero(api):
+    r = np.random.default_rng(3)
+    qw, s = synth.int4_weight(r, 3584, 18944)
+    x = to_dev(synth.normal_fp16(r, (32, 18944)), torch)
+    qd, sd = to_dev(qw, torch), to_dev(s, torch)
+    ws = torch.zeros(api.load().w4a16_gemm_workspace_size(32, 18944, 3584, 0), dtype=torch.uint8, device="cuda")
+    y1 = api.w4a16_gemm(x, qd, sd, workspace=ws)
+    y2 = api.w4a16_gemm(x, qd, sd, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("K,N,M", [(896, 2432, 32), (3584, 18944, 32), (3584, 256, 9)])
+def test_w4a16_gemm_silu_mul_matches_oracle(api, K, N, M):
+    r = np.random.default_rng(K + N + M)
+    qg, sg = synth.int4_weight(r, N, K)
+    qu, su = synth.int4_weight(r, N, K)
+    x = synth.normal_fp16(r, (M, K))
+    ref = orc.silu_mul(orc.w4a16_gemv(x, qg, sg), orc.w4a16_gemv(x, qu, su))
+    y = api.w4a16_gemm_silu_mul(to_dev(x, torch), to_dev(qg, torch), to_dev(sg, torch), to_dev(qu, torch),
+                                to_dev(su, torch))
+    torch.cuda.synchronize()
+    assert_close(to_host(y), ref, what="gemm silu")
+
+
+def test_w4a16_gemv_routes_batches_to_tensor_cores(api):
+    r = np.random.default_rng(8)
+    qw, s = synth.int4_weight(r, 512, 3584)
+    x = synth.normal_fp16(r, (8, 3584))
+    y = api.w4a16_gemv(to_dev(x, torch), to_dev(qw, torch), to_dev(s, torch))
+    torch.cuda.synchronize()
+    assert_close(to_host(y), orc.w4a16_gemv(x, qw, s), what="gemv M=8")
+
+
+@pytest.mark.parametrize("B,H,V", [(32, 3584, 152064), (5, 896, 1000)])
+def test_batched_lm_head_and_argmax(api, B, H, V):
+    r = np.random.default_rng(B * V)
+    W = synth.normal_fp16(r, (V, H), std=0.02)
+    x = synth.normal_fp16(r, (B, H))
+    lg = api.lm_head_logits_batched(to_dev(x, torch), to_dev(W, torch))
+    l16 = torch.empty((B, V), dtype=torch.float16, device="cuda")
+    toks = api.argmax_rows(lg, logits16=l16)
+    torch.cuda.synchronize()
+    lg, toks = to_host(lg), to_host(toks)
+    for b in range(0, B, max(1, B // 4)):
+        ref = orc.fp16_gemv(x[b], W)
+        assert_close(lg[b], ref, atol=1e-3, rtol=1e-4, what="lm_head fp32 logits")
+        srt = np.sort(ref)
+        if srt[-1] - srt[-2] > 1e-3:
+            assert toks[b] == orc.argmax(ref)
+    assert np.array_equal(to_host(l16), lg.astype(np.float16))
+
+
+def test_argmax_rows_ties_lowest_index(api):
+    lg = torch.zeros((2, 5000), dtype=torch.float32, device="cuda")
+    lg[0, 4000] = 3.0
+    lg[0, 17] = 3.0
+    lg[1, :] = -1.0
+    toks = api.argmax_rows(lg)
+    torch.cuda.synchronize()
+    assert to_host(toks).tolist() == [17, 0]

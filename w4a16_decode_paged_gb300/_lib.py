@@ -51,6 +51,11 @@ SIGNATURES = {
     "w4a16_last_error": (ctypes.c_char_p, []),
     "w4a16_version": (I32, []),
     "w4a16_gemv": (I32, [P, I32, I32, P, P, I32, P, P, P, P]),
+    "w4a16_gemm": (I32, [P, I32, I32, P, P, I32, P, P, P, P, SZ, P]),
+    "w4a16_gemm_silu_mul": (I32, [P, I32, I32, P, P, P, P, I32, P, P, SZ, P]),
+    "w4a16_gemm_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "lm_head_logits_batched": (I32, [P, I32, I32, P, I32, P, P]),
+    "argmax_rows": (I32, [P, I32, I32, P, P, P]),
     "w4a16_gemv_rmsnorm": (I32, [P, P, F32, I32, I32, P, P, I32, P, P, P]),
     "w4a16_gemv_silu_mul": (I32, [P, P, F32, I32, I32, P, P, P, P, I32, P, P]),
     "rmsnorm": (I32, [P, P, P, I32, I32, F32, P]),

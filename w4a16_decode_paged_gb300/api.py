@@ -13,7 +13,7 @@ import torch
 
 from ._lib import LayerWeights, ModelConfig, ModelWeights, check, load
 
-__all__ = ["w4a16_gemv", "w4a16_gemv_rmsnorm", "w4a16_gemv_silu_mul", "rmsnorm", "kv_append_rope",
+__all__ = ["w4a16_gemv", "w4a16_gemm", "w4a16_gemm_silu_mul", "lm_head_logits_batched", "argmax_rows", "w4a16_gemv_rmsnorm", "w4a16_gemv_silu_mul", "rmsnorm", "kv_append_rope",
            "paged_gqa_decode", "paged_gqa_decode_rope_append", "paged_gqa_decode_workspace_size", "paged_gqa_decode_default_partition",
            "workspace_clear", "embedding_gather", "lm_head_argmax", "Model", "stream_handle"]
 
@@ -50,6 +50,56 @@ def w4a16_gemv(x, qweight, scales, bias=None, residual=None, out=None, stream=No
     check(load().w4a16_gemv(_p(x), M, K, _p(qweight), _p(scales), N, _p(bias), _p(residual), _p(out),
                             stream_handle(stream)))
     return out
+
+
+def w4a16_gemm(x, qweight, scales, bias=None, residual=None, out=None, workspace=None, split=True, stream=None):
+    """Tensor-core path for a decode batch (M <= 32)."""
+    _need(x, _H, "x"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
+    M, K = x.shape
+    N = qweight.shape[0]
+    lib = load()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None and split:
+        workspace = torch.zeros(max(256, lib.w4a16_gemm_workspace_size(M, K, N, 0)), dtype=torch.uint8,
+                                device=x.device)
+    check(lib.w4a16_gemm(_p(x), M, K, _p(qweight), _p(scales), N, _p(bias), _p(residual), _p(out), _p(workspace),
+                         0 if workspace is None else workspace.numel(), stream_handle(stream)))
+    return out
+
+
+def w4a16_gemm_silu_mul(x, qweight_gate, scales_gate, qweight_up, scales_up, out=None, workspace=None, split=True,
+                        stream=None):
+    _need(x, _H, "x")
+    M, K = x.shape
+    N = qweight_gate.shape[0]
+    lib = load()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None and split:
+        workspace = torch.zeros(max(256, lib.w4a16_gemm_workspace_size(M, K, N, 1)), dtype=torch.uint8,
+                                device=x.device)
+    check(lib.w4a16_gemm_silu_mul(_p(x), M, K, _p(qweight_gate), _p(scales_gate), _p(qweight_up), _p(scales_up), N,
+                                  _p(out), _p(workspace), 0 if workspace is None else workspace.numel(),
+                                  stream_handle(stream)))
+    return out
+
+
+def lm_head_logits_batched(x, lm_head, out=None, stream=None):
+    B, H = x.shape
+    V = lm_head.shape[0]
+    if out is None:
+        out = torch.empty((B, V), dtype=torch.float32, device=x.device)
+    check(load().lm_head_logits_batched(_p(x), B, H, _p(lm_head), V, _p(out), stream_handle(stream)))
+    return out
+
+
+def argmax_rows(logits32, tokens_out=None, logits16=None, stream=None):
+    B, V = logits32.shape
+    if tokens_out is None:
+        tokens_out = torch.empty(B, dtype=torch.int32, device=logits32.device)
+    check(load().argmax_rows(_p(logits32), B, V, _p(tokens_out), _p(logits16), stream_handle(stream)))
+    return tokens_out
 
 
 def w4a16_gemv_rmsnorm(x, gamma, eps, qweight, scales, bias=None, out=None, stream=None):

@@ -574,8 +574,26 @@ static int dispatch_lpr(const GemvArgs& a, cudaStream_t s) {
 int gemv_cuda_core_supported(int M, int K) { return M >= 1 && M <= 4 && (long)M * K <= 49152; }
 
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s) {
-  if (!gemv_cuda_core_supported(a.M, a.K))
-    return set_error(W4A16_ERR_SHAPE, "gemv: M=%d K=%d outside the CUDA-core path (M<=4, M*K<=49152)", a.M, a.K);
+  if (!gemv_cuda_core_supported(a.M, a.K)) {
+    // a real batch: the tensor-core GEMM (no RMSNorm prologue there)
+    if (a.M <= 32 && a.gamma == nullptr) {
+      TcArgs t = {};
+      t.x = a.x;
+      t.residual = a.residual;
+      t.y = a.y;
+      for (int i = 0; i < 3; ++i) t.seg[i] = a.seg[i];
+      t.nseg = a.nseg;
+      t.M = a.M;
+      t.K = a.K;
+      t.N = a.N;
+      t.ldy = a.N;
+      t.ksplit = 1;
+      t.tag = a.tag;
+      return launch_gemm_tc(t, true, silu, s);
+    }
+    return set_error(W4A16_ERR_SHAPE, "gemv: M=%d K=%d outside the built paths (M<=32; fused RMSNorm only for M<=4)",
+                     a.M, a.K);
+  }
   // the fast path moves two rows per half-warp: every segment (and N) even
   bool even_rows = a.N >= 2 && a.N % 2 == 0;
   for (int i = 0; i < a.nseg; ++i) even_rows = even_rows && (a.seg[i].rows % 2 == 0);

@@ -31,6 +31,26 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s);
 int gemv_cuda_core_supported(int M, int K);
 
+// Tensor-core (tcgen05) GEMM for decode batches of up to 32 sequences.
+struct TcArgs {
+  const __half* x;         // [M][K] activations
+  const __half* residual;  // [M][ldy] or null
+  __half* y;               // [M][ldy] fp16 output (unless y32)
+  float* y32;              // [M][ldy] fp32 output or null (dense lm_head logits)
+  GemvSeg seg[3];          // int4 weights (SiLU: gate, up)
+  int nseg;
+  const __half* w16;       // dense fp16 weights [N][K] (lm_head)
+  float* ws;               // split-K partial tiles
+  unsigned int* counters;  // split-K tickets, one per 128-row tile (zero before first use)
+  int32_t* err_flag;
+  int M, K, N, ldy, ksplit, tag;
+};
+int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
+size_t tc_workspace_bytes(int N, int ksplit, bool silu);
+int tc_default_ksplit(int N, int K);
+int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
+                       int tag);
+
 // Paged attention (+ fused split-K combine, optionally fused RoPE + append).
 struct AttnArgs {
   const __half* q;          // [B][Hq][D] with row pitch q_stride (fused: q | k_new | v_new rows)
