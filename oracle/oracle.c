@@ -105,7 +105,13 @@ uint16_t orc_double_to_half(double d) {
   return sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)m - 1024);
 }
 
-static inline double h2d(uint16_t h) { return orc_half_to_double(h); }
+/* Every binary16 value decoded once by orc_half_to_double (65536 entries,
+ * filled when the library loads); h2d is a lookup into it. */
+static double g_h2d[65536];
+__attribute__((constructor)) static void orc_fill_h2d(void) {
+  for (uint32_t h = 0; h < 65536u; ++h) g_h2d[h] = orc_half_to_double((uint16_t)h);
+}
+static inline double h2d(uint16_t h) { return g_h2d[h]; }
 static inline uint16_t d2h(double d) { return orc_double_to_half(d); }
 
 void orc_half_to_double_array(const uint16_t* h, int64_t n, double* out) {
@@ -201,13 +207,14 @@ void orc_w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qw, const u
                     int N, const uint16_t* bias, const uint16_t* residual, uint16_t* y) {
   int G = K / ORC_GROUP;
   for (int m = 0; m < M; ++m) {
+    const uint16_t* xm = x + (int64_t)m * K;
 #pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n) {
       double acc = 0.0;
       for (int k = 0; k < K; ++k) {
         int code = orc_unpack_code(qw[(int64_t)n * (K / 8) + k / 8], k % 8);
         double wv = (double)code * h2d(scales[(int64_t)n * G + k / ORC_GROUP]);
-        acc += h2d(x[(int64_t)m * K + k]) * wv;
+        acc += h2d(xm[k]) * wv;
       }
       if (bias) acc += h2d(bias[n]);
       if (residual) acc += h2d(residual[(int64_t)m * N + n]);
