@@ -47,6 +47,9 @@ def parse():
                     choices=["gateup", "down", "qkv", "o", "attention", "lm_head"],
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
+    ap.add_argument("--workload", default="b1", choices=["b1", "b32"],
+                    help="b1: 28-layer b=1 ctx-512 decode; b32: 28-layer batched decode, 32 sequences of "
+                         "U[1,4096] tokens in a 16384-page pool")
     return ap.parse_args()
 
 
@@ -55,20 +58,26 @@ def model_cfg(layers):
     return dict(synth.QWEN_MODEL, n_layers=layers)
 
 
-def make_inputs(cfg, seed, max_ctx, pool_pages=256):
-    """numpy weights, pools and paging state for the whole model."""
+def make_inputs(cfg, seed, lens, gen_tokens, pool_pages):
+    """numpy weights, pools and paging state for the whole model: B = len(lens)
+    sequences with lens[b] tokens already cached and pages assigned for
+    gen_tokens more."""
     from w4a16_decode_paged_gb300 import synth
-    r = synth.rng(seed)
-    layers = [synth.layer_weights(r, cfg) for _ in range(cfg["n_layers"])]
-    kps = [synth.kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"]) for _ in range(cfg["n_layers"])]
-    vps = [synth.kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"]) for _ in range(cfg["n_layers"])]
-    embed = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]))
-    fnorm = synth.gamma(r, cfg["hidden"])
-    lm = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]), std=0.02)
-    bt = synth.block_table(r, [max_ctx], pool_pages)
-    tok = r.integers(0, cfg["vocab"], size=1).astype(np.int32)
-    return dict(layers=layers, kps=kps, vps=vps, embed=embed, fnorm=fnorm, lm=lm, bt=bt, tok=tok,
-                pool_pages=pool_pages)
+    return synth.model_case(cfg, lens=lens, gen_tokens=gen_tokens, pool_pages=pool_pages, seed=seed)
+
+
+def workload(args):
+    """(cfg, cached lengths per sequence, pool pages, label) of the timed workload."""
+    from w4a16_decode_paged_gb300 import synth
+    if args.workload == "b32":
+        cfg = dict(synth.QWEN_BATCHED, n_layers=args.layers)
+        post = synth.batched_lens(synth.rng(cfg["seed"]), cfg["batch"], cfg["max_context"], cfg["forced_lens"])
+        label = (f"qwen2.5-7b-{cfg['n_layers']}L-b32-ctxU[1,4096] (15/16/17 forced) batched greedy decode "
+                 f"(CUDA graph, tcgen05 projections)")
+        return cfg, post - 1, cfg["pool_pages"], label
+    cfg = model_cfg(args.layers)
+    label = f"qwen2.5-7b-{cfg['n_layers']}L-b1-ctx{args.context} greedy decode (CUDA graph)"
+    return cfg, np.array([args.context], np.int32), 256, label
 
 
 # ---------------------------------------------------------------------------- bytes (roofline)
@@ -82,19 +91,24 @@ def gemv_bytes(N, K, M=1, bias=False, residual=False):
     return b
 
 
-def layer_bytes(cfg, ctx):
+def layer_bytes(cfg, lens):
+    """(projection bytes, attention bytes) of one layer for sequences whose
+    attention covers lens[b] tokens."""
+    lens = np.atleast_1d(np.asarray(lens, np.int64))
+    B = len(lens)
     H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
     nqkv = (Hq + 2 * Hkv) * D
-    g = gemv_bytes(nqkv, H, bias=True) + gemv_bytes(H, Hq * D, residual=True) + \
-        (gemv_bytes(2 * I, H) - 2 * I * 2 + I * 2) + gemv_bytes(H, I, residual=True)
-    att = 2 * Hkv * ctx * D * 2 + 4 * math.ceil(ctx / 16) + 2 * Hq * D * 2
+    g = gemv_bytes(nqkv, H, B, bias=True) + gemv_bytes(H, Hq * D, B, residual=True) + \
+        (gemv_bytes(2 * I, H, B) - B * I * 2) + gemv_bytes(H, I, B, residual=True)
+    att = int(sum(2 * Hkv * int(L) * D * 2 + 4 * math.ceil(int(L) / 16) for L in lens)) + B * 2 * Hq * D * 2
     return g, att
 
 
-def step_bytes(cfg, ctx):
-    g, att = layer_bytes(cfg, ctx)
+def step_bytes(cfg, lens):
+    lens = np.atleast_1d(lens)
+    g, att = layer_bytes(cfg, lens)
     lm = cfg["vocab"] * cfg["hidden"] * 2
-    return cfg["n_layers"] * (g + att) + lm + cfg["hidden"] * 2
+    return cfg["n_layers"] * (g + att) + lm + len(lens) * cfg["hidden"] * 2
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -197,58 +211,65 @@ def traffic_record(kernel):
 
 # ---------------------------------------------------------------------------- oracle timing
 
-def oracle_token_time(cfg, inp, ctx, budget_s=15.0):
-    """Seconds the CPU oracle needs for one decode token, from a bounded
-    sample: as many whole layers as fit in ~budget_s (>= 1), scaled to the
-    model's layer count, plus the full fp16 lm_head + argmax."""
+def oracle_token_time(cfg, inp, budget_s=15.0):
+    """Seconds the CPU oracle needs for one decode step of the workload's
+    batch, from a bounded sample: as many whole layers (all sequences) as
+    fit in ~budget_s (>= 1), scaled to the model's layer count, plus the
+    lm_head rows of one sequence scaled to the batch, and the argmax."""
     import oracle as orc
+    from w4a16_decode_paged_gb300 import synth
     orc.build()
     nthreads = orc.num_threads()
-    bt = inp["bt"][:, :]
-    lens = np.array([ctx + 1], np.int32)
-    x = inp["embed"][inp["tok"][0]][None, :].copy()
+    lens = inp["lens"] + 1
+    B = len(lens)
+    x = inp["embed"][inp["tok"]].copy()
     t_layers, n_done = 0.0, 0
     for l in range(cfg["n_layers"]):
-        kp, vp = inp["kps"][l].copy(), inp["vps"][l].copy()
+        kp, vp = synth.host_pool(inp, l, "k"), synth.host_pool(inp, l, "v")
         t0 = time.perf_counter()
-        x = orc.decoder_layer(cfg, inp["layers"][l], x, kp, vp, bt, lens)
+        x = orc.decoder_layer(cfg, inp["layers"][l], x, kp, vp, inp["bt"], lens)
         t_layers += time.perf_counter() - t0
         n_done += 1
         if t_layers > budget_s * 0.7:
             break
     t0 = time.perf_counter()
-    xn = orc.rmsnorm(x, inp["fnorm"], cfg["eps"])
+    xn = orc.rmsnorm(x[:1], inp["fnorm"], cfg["eps"])
     logits = orc.fp16_gemv(xn[0], inp["lm"])
     orc.argmax(logits)
-    t_lm = time.perf_counter() - t0
-    per_token = t_layers / n_done * cfg["n_layers"] + t_lm
-    sample = (f"{n_done} of {cfg['n_layers']} decoder layers timed (x{cfg['n_layers'] / n_done:.2f}) "
-              f"+ full lm_head GEMV and argmax, b=1, context {ctx + 1}")
-    return per_token, nthreads, sample, t_layers + t_lm
+    t_lm = (time.perf_counter() - t0) * B
+    per_step = t_layers / n_done * cfg["n_layers"] + t_lm
+    sample = (f"{n_done} of {cfg['n_layers']} decoder layers timed at batch {B} (x{cfg['n_layers'] / n_done:.2f}) "
+              f"+ lm_head GEMV and argmax of one sequence (x{B}); contexts {int(lens.min())}..{int(lens.max())}")
+    return per_step, nthreads, sample, t_layers + t_lm / B
 
 
 def run_reference(args):
     """CPU oracle arm: each step is one decoder layer (cycling over the 28)
-    plus 1/28 of the lm_head rows, i.e. 1/28 of a token's work."""
+    plus 1/28 of the lm_head rows, for every sequence of the workload, i.e.
+    1/28 of a decode step."""
     import oracle as orc
+    from w4a16_decode_paged_gb300 import synth
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     orc.build()
-    cfg = model_cfg(args.layers)
-    inp = make_inputs(cfg, args.seed, args.context + 16)
+    cfg, lens0, pool_pages, label = workload(args)
+    inp = make_inputs(cfg, args.seed if args.workload == "b1" else cfg["seed"], lens0, 16, pool_pages)
     L = cfg["n_layers"]
-    lens = np.array([args.context + 1], np.int32)
-    x = inp["embed"][inp["tok"][0]][None, :].copy()
+    lens = inp["lens"] + 1
+    B = len(lens)
+    x = inp["embed"][inp["tok"]].copy()
     rows = math.ceil(cfg["vocab"] / L)
 
     def one(i):
         nonlocal x
         l = i % L
-        kp, vp = inp["kps"][l].copy(), inp["vps"][l].copy()
+        kp, vp = synth.host_pool(inp, l, "k"), synth.host_pool(inp, l, "v")
         x = orc.decoder_layer(cfg, inp["layers"][l], x, kp, vp, inp["bt"], lens)
         lo = (i % L) * rows
-        orc.fp16_gemv(orc.rmsnorm(x, inp["fnorm"], cfg["eps"])[0], inp["lm"][lo:lo + rows])
+        xn = orc.rmsnorm(x, inp["fnorm"], cfg["eps"])
+        for b in range(B):
+            orc.fp16_gemv(xn[b], inp["lm"][lo:lo + rows])
 
     for i in range(args.warmup):
         one(i)
@@ -256,17 +277,16 @@ def run_reference(args):
     for i in range(args.steps):
         one(i)
     dt = time.perf_counter() - t0
-    tokens = args.steps / L
+    tokens = B * args.steps / L
     value = tokens / dt
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded random-init weights, N(0,1) KV)",
-           "config": {"workload": f"qwen2.5-7b-{L}L-b1-ctx{args.context} greedy decode", "batch": 1,
-                      "context": args.context, "layers": L},
+           "config": {"workload": label, "batch": B, "context": int(lens.max()), "layers": L},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                             "sample": f"each step = 1 of {L} decoder layers + 1/{L} of the lm_head rows "
-                                      f"(= 1/{L} token), {args.steps} steps"},
+                                      f"(= 1/{L} decode step of {B} sequence(s)), {args.steps} steps"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
     return 0
@@ -385,23 +405,28 @@ def main():
     from w4a16_decode_paged_gb300 import api, build
     build.build()
 
-    cfg = model_cfg(args.layers)
+    cfg, lens0, pool_pages, label = workload(args)
+    B = len(lens0)
     K, W = args.steps, args.warmup
-    max_ctx = args.context + K + W + 16
+    gen = K + W + 16
+    max_ctx = int(lens0.max()) + gen
+    seed = (args.seed if args.workload == "b1" else cfg["seed"]) + rank
     t_gen = time.perf_counter()
-    inp = make_inputs(cfg, args.seed + rank, max_ctx)
+    inp = make_inputs(cfg, seed, lens0, gen, pool_pages)
     t_gen = time.perf_counter() - t_gen
 
     tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int32) if a.dtype == np.uint32 else a)).to(dev)
-    dls = [api.device_layer(w, kp, vp, device=dev) for w, kp, vp in zip(inp["layers"], inp["kps"], inp["vps"])]
+    dls = [api.device_layer(w, api.device_pool(inp, l, "k", dev), api.device_pool(inp, l, "v", dev), device=dev)
+           for l, w in enumerate(inp["layers"])]
     embed, fnorm, lm = tdev(inp["embed"]), tdev(inp["fnorm"]), tdev(inp["lm"])
-    model = api.Model(cfg, dls, embed=embed, final_norm=fnorm, lm_head=lm, max_batch=1, max_context=max_ctx,
+    model = api.Model(cfg, dls, embed=embed, final_norm=fnorm, lm_head=lm, max_batch=B, max_context=max_ctx,
                       num_pages=inp["pool_pages"])
     bt = tdev(inp["bt"])
     tok = tdev(inp["tok"])
-    lens = torch.tensor([args.context], dtype=torch.int32, device=dev)
+    lens_init = tdev(inp["lens"])
+    lens = lens_init.clone()
     stream = torch.cuda.Stream(device=dev)
-    kernels_per_step = model.kernel_count(1)
+    kernels_per_step = model.kernel_count(B)
 
     def barrier():
         if world > 1:
@@ -409,12 +434,12 @@ def main():
 
     with torch.cuda.stream(stream):
         # ---- device-resident timing: K graph replays --------------------
-        lens.fill_(args.context)
+        lens.copy_(lens_init)
         for _ in range(W):
             model.decode_step(tok, tok, bt, lens, use_graph=True)
         stream.synchronize()
         assert model.check_errors(stream) == 0
-        lens.fill_(args.context)
+        lens.copy_(lens_init)
         stream.synchronize()
         barrier()
         torch.cuda.synchronize()
@@ -428,20 +453,20 @@ def main():
         torch.cuda.synchronize()
         barrier()
         ms = e0.elapsed_time(e1)
-        assert int(lens.item()) == args.context + K
+        assert torch.equal(lens, lens_init + K)
         assert model.check_errors(stream) == 0
 
         # ---- end to end through the C ABI with host buffers --------------
-        h_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
-        h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        h_in = torch.empty(B, dtype=torch.int32, pin_memory=True)
+        h_out = torch.empty(B, dtype=torch.int32, pin_memory=True)
         h_in.copy_(torch.from_numpy(inp["tok"]))
-        lens.fill_(args.context)
+        lens.copy_(lens_init)
         for _ in range(2):
             tok.copy_(h_in, non_blocking=True)
             model.decode_step(tok, tok, bt, lens, use_graph=True)
             h_out.copy_(tok, non_blocking=True)
             stream.synchronize()
-        lens.fill_(args.context)
+        lens.copy_(lens_init)
         stream.synchronize()
         barrier()
         t0 = time.perf_counter()
@@ -454,10 +479,10 @@ def main():
         e2e_s = time.perf_counter() - t0
         barrier()
 
-        # ---- dominant kernel: gate|up W4A16 GEMV + SiLU-mul, live ---------
+        # ---- dominant projection kernel: gate|up + SiLU-mul, live ---------
         kern = None
         if not args.no_kernel_timing:
-            kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream)
+            kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream, B)
 
     # max over ranks
     t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
@@ -470,30 +495,35 @@ def main():
         return 0
 
     peak, peak_src = measured_peak()
-    value = world * K / (ms / 1e3)
+    value = world * B * K / (ms / 1e3)
+    mid_lens = inp["lens"] + 1 + K // 2
+    sb = step_bytes(cfg, mid_lens)
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "int4 weights x fp16 activations, fp32 accumulate",
            "data": "synthetic (seeded random-init weights of the model's shapes; N(0,1) KV prefill)",
-           "config": {"workload": f"qwen2.5-7b-{cfg['n_layers']}L-b1-ctx{args.context} greedy decode (CUDA graph)",
-                      "batch": 1, "context": args.context, "layers": cfg["n_layers"],
-                      "l2": f"inputs larger than L2: {step_bytes(cfg, args.context) / 1e9:.2f} GB read per step",
+           "config": {"workload": label, "batch": B,
+                      "context": args.context if B == 1 else f"{int(inp['lens'].min()) + 1}..{int(inp['lens'].max()) + 1}",
+                      "layers": cfg["n_layers"],
+                      "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB read per step",
                       "parallelism": f"replicas x{world}"},
            "gpu_launches": kernels_per_step * K,
-           "e2e": {"value": world * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+           "e2e": {"value": world * B * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4 * B,
+                   "d2h_bytes_per_step": 4 * B},
            "clocks": clk.summary()}
-    sb = step_bytes(cfg, args.context + K // 2)
     out["step_roofline"] = {"bytes_per_step": sb, "achieved_gbs": sb / (ms / K / 1e3) / 1e9, "peak_gbs": peak,
                             "frac": sb / (ms / K / 1e3) / 1e9 / peak, "roofline_ms": sb / (peak * 1e9) * 1e3}
     if kern is not None:
-        out["roofline"] = {"bound": "hbm", "kernel": "w4a16_gemv_silu_mul (gate|up, 3584->2x18944)",
+        kname = ("w4a16_gemv_silu_mul (gate|up, 3584->2x18944)" if B <= 4 else
+                 f"w4a16_gemm_silu_mul (tcgen05, M={B}, gate|up, 3584->2x18944)")
+        out["roofline"] = {"bound": "hbm", "kernel": kname,
                            "achieved": kern["gateup"]["gbs"], "peak": peak, "unit": "GB/s",
                            "frac": kern["gateup"]["gbs"] / peak, "peak_source": peak_src,
-                           "traffic": traffic_record("gemv_gateup")}
+                           "traffic": traffic_record("gemv_gateup" if B <= 4 else "gemm_tc_gateup_b32")}
         out["kernels"] = kern
     if not args.no_cpu_baseline:
-        per_tok, cores, sample, spent = oracle_token_time(cfg, inp, args.context)
-        out["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": UNIT, "cores": cores, "kind": "oracle",
+        per_step, cores, sample, spent = oracle_token_time(cfg, inp)
+        out["cpu_baseline"] = {"value": B / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": sample, "seconds_spent": round(spent, 2)}
     out["setup_s"] = {"generate_inputs": round(t_gen, 1)}
     print(json.dumps(out))
@@ -502,26 +532,46 @@ def main():
     return 0
 
 
-def time_gemv_kernels(torch, api, cfg, dls, dev, stream, reps=3):
-    """Average device time per launch of each GEMV kind as used in the step,
-    over all layers' weights (rotating, so nothing stays in L2), captured
-    in a CUDA graph and timed with CUDA events on the launching stream."""
+def time_gemv_kernels(torch, api, cfg, dls, dev, stream, B=1, reps=3):
+    """Average device time per launch of each projection kind as used in the
+    step at batch B (CUDA-core GEMVs for B <= 4, tensor-core GEMMs with split
+    K above), over all layers' weights (rotating, so nothing stays in L2),
+    captured in a CUDA graph and timed with CUDA events on the launching
+    stream."""
     H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
-    x = torch.randn((1, H), device=dev).half()
-    xi = torch.randn((1, I), device=dev).half()
-    xa = torch.randn((1, Hq * D), device=dev).half()
-    y_i = torch.empty((1, I), dtype=torch.float16, device=dev)
-    y_h = torch.empty((1, H), dtype=torch.float16, device=dev)
-    y_q = torch.empty((1, Hq * D), dtype=torch.float16, device=dev)
-    kinds = {
-        "gateup": (lambda w: api.w4a16_gemv_silu_mul(x, w["ln2"], 1e-6, w["wg"], w["sg"], w["wu"], w["su"], out=y_i),
-                   gemv_bytes(2 * I, H) - 2 * I * 2 + I * 2),
-        "down": (lambda w: api.w4a16_gemv(xi, w["wd"], w["sd"], residual=x, out=y_h), gemv_bytes(H, I, residual=True)),
-        "q": (lambda w: api.w4a16_gemv_rmsnorm(x, w["ln1"], 1e-6, w["wq"], w["sq"], bias=w["bq"], out=y_q),
-              gemv_bytes(Hq * D, H, bias=True)),
-        "o": (lambda w: api.w4a16_gemv(xa, w["wo"], w["so"], residual=x, out=y_h),
-              gemv_bytes(H, Hq * D, residual=True)),
-    }
+    x = torch.randn((B, H), device=dev).half()
+    xi = torch.randn((B, I), device=dev).half()
+    xa = torch.randn((B, Hq * D), device=dev).half()
+    y_i = torch.empty((B, I), dtype=torch.float16, device=dev)
+    y_h = torch.empty((B, H), dtype=torch.float16, device=dev)
+    y_q = torch.empty((B, Hq * D), dtype=torch.float16, device=dev)
+    if B <= 4:
+        kinds = {
+            "gateup": (lambda w: api.w4a16_gemv_silu_mul(x, w["ln2"], 1e-6, w["wg"], w["sg"], w["wu"], w["su"],
+                                                         out=y_i),
+                       gemv_bytes(2 * I, H, B) - B * I * 2),
+            "down": (lambda w: api.w4a16_gemv(xi, w["wd"], w["sd"], residual=x, out=y_h),
+                     gemv_bytes(H, I, B, residual=True)),
+            "q": (lambda w: api.w4a16_gemv_rmsnorm(x, w["ln1"], 1e-6, w["wq"], w["sq"], bias=w["bq"], out=y_q),
+                  gemv_bytes(Hq * D, H, B, bias=True)),
+            "o": (lambda w: api.w4a16_gemv(xa, w["wo"], w["so"], residual=x, out=y_h),
+                  gemv_bytes(H, Hq * D, B, residual=True)),
+        }
+    else:
+        ws = torch.zeros(max(api.load().w4a16_gemm_workspace_size(B, K_, N_, s_) for N_, K_, s_ in
+                             ((I, H, 1), (H, I, 0), (Hq * D, H, 0), (H, Hq * D, 0))),
+                         dtype=torch.uint8, device=dev)
+        kinds = {
+            "gateup": (lambda w: api.w4a16_gemm_silu_mul(x, w["wg"], w["sg"], w["wu"], w["su"], out=y_i,
+                                                         workspace=ws),
+                       gemv_bytes(2 * I, H, B) - B * I * 2),
+            "down": (lambda w: api.w4a16_gemm(xi, w["wd"], w["sd"], residual=x, out=y_h, workspace=ws),
+                     gemv_bytes(H, I, B, residual=True)),
+            "q": (lambda w: api.w4a16_gemm(x, w["wq"], w["sq"], bias=w["bq"], out=y_q, workspace=ws),
+                  gemv_bytes(Hq * D, H, B, bias=True)),
+            "o": (lambda w: api.w4a16_gemm(xa, w["wo"], w["so"], residual=x, out=y_h, workspace=ws),
+                  gemv_bytes(H, Hq * D, B, residual=True)),
+        }
     res = {}
     for name, (fn, nbytes) in kinds.items():
         for w in dls[:2]:

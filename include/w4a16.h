@@ -107,8 +107,10 @@ W4A16_API int w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qweigh
  * only roundings are fp32 accumulation and the final fp16 store.
  * Projections with few 128-row tiles split K across CTAs when a workspace of
  * w4a16_gemm_workspace_size() bytes is given (zeroed once before first use;
- * every call leaves its counters zero); with workspace == NULL they run
- * without the split.  Calls sharing a workspace must not overlap on the GPU.
+ * every call leaves its counters zero; the counters occupy the first 8 KiB
+ * whatever the shape, so one workspace serves calls of different shapes in
+ * turn); with workspace == NULL they run without the split.  Calls sharing
+ * a workspace must not overlap on the GPU.
  * w4a16_gemv routes 5 <= M <= 32 here (without the split).
  * ------------------------------------------------------------------------ */
 W4A16_API int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweight,
@@ -192,8 +194,11 @@ W4A16_API int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v, 
  *   workspace     device scratch of paged_gqa_decode_workspace_size() bytes;
  *                 its counter words must be zero before the first use and
  *                 every call leaves them zero again (w4a16_workspace_clear
- *                 zeroes it once).  Calls that run concurrently on the GPU
- *                 need separate workspaces.
+ *                 zeroes it once).  The counters sit in the first 16 KiB
+ *                 whatever the sizes, so one workspace serves calls of
+ *                 different shapes in turn (B*Hkv <= 4096 when split);
+ *                 calls that run concurrently on the GPU need separate
+ *                 workspaces.
  *   err_flag      as for kv_append_rope (bad pages are skipped).
  * D must be 128, Hq % Hkv == 0, Hq/Hkv <= 8.  context_lens[b] == 0 yields
  * zeros.
@@ -315,8 +320,8 @@ typedef struct {
 typedef struct w4a16_model w4a16_model;
 
 /* Builds the model handle.  The only call that allocates: one device arena
- * for activations and workspaces sized for max_batch sequences of up to
- * max_context tokens.  Weight and pool pointers are borrowed (caller keeps
+ * for activations and workspaces sized for max_batch (1..32) sequences of up
+ * to max_context tokens.  Weight and pool pointers are borrowed (caller keeps
  * them alive). */
 W4A16_API int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
                        int max_context, w4a16_model** out);
@@ -337,6 +342,23 @@ W4A16_API int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream);
  * (enqueued on `stream`; capture-safe). */
 W4A16_API int w4a16_model_hidden(w4a16_model* m, uint16_t* dst, int B, w4a16_stream_t stream);
 
+/* Copy one of the activation buffers the last layer (or decode step) left
+ * in the model's arena into dst fp16 [B][width] (enqueued on `stream`):
+ *   W4A16_ACT_HIDDEN  the step's hidden state x            width hidden
+ *   W4A16_ACT_QKV     q | k | v projections (+bias)        width (Hq+2Hkv)*D
+ *   W4A16_ACT_ATTN    attention output, before o           width Hq*D
+ *   W4A16_ACT_RESID   x + o projection (post-attention)    width hidden
+ *   W4A16_ACT_MLP     silu(gate) * up                      width inter
+ * For checking each kernel of a layer on its own inputs. */
+enum {
+  W4A16_ACT_HIDDEN = 0,
+  W4A16_ACT_QKV = 1,
+  W4A16_ACT_ATTN = 2,
+  W4A16_ACT_RESID = 3,
+  W4A16_ACT_MLP = 4
+};
+W4A16_API int w4a16_model_activation(w4a16_model* m, int which, uint16_t* dst, int B, w4a16_stream_t stream);
+
 /* One decoder layer on hidden states x fp16 [B][hidden] (in place), with
  * context_lens already counting the appended token. */
 W4A16_API int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table,
@@ -349,6 +371,10 @@ W4A16_API int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const in
  *   (RMSNorm -> q/k/v GEMV + bias -> RoPE + KV append -> paged GQA
  *   attention -> o GEMV + residual -> RMSNorm -> gate/up GEMV + SiLU-mul ->
  *   down GEMV + residual), final RMSNorm, lm_head, argmax -> tokens_out.
+ *   B <= 4 runs the CUDA-core GEMVs with the RMSNorms fused in front and
+ *   the lm_head GEMV with a fused argmax; 4 < B <= max_batch runs each
+ *   RMSNorm on its own, the projections and the lm_head as tensor-core
+ *   GEMMs (fp32 logits in the model's arena) and a row-wise argmax.
  *   tokens_in, tokens_out  int32 [B] device (may be the same buffer)
  *   block_table            int32 [B][max_blocks]; pages for the new
  *                          position must already be assigned

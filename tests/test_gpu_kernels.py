@@ -239,6 +239,32 @@ def test_paged_gqa_decode_repeat_calls_and_zero_length(api):
     assert_close(got[1:], ref, what="attention repeat")
 
 
+def test_paged_gqa_decode_one_workspace_for_different_shapes(api):
+    """Calls of different batch sizes and partition counts in turn on one
+    workspace (the tickets sit at a fixed place whatever the shape)."""
+    r = np.random.default_rng(13)
+    D, Hq, Hkv = 128, 28, 4
+    shapes = [(2, 5000, 16), (9, 1200, 16), (4, 3000, 32)]   # (B, max length, partition tokens)
+    cases, need = [], 0
+    for B, Lmax, part in shapes:
+        lens = r.integers(1, Lmax + 1, size=B).astype(np.int32)
+        lens[0] = Lmax
+        pages = int(sum((L + 15) // 16 for L in lens)) + 3
+        kp, vp = synth.kv_pool(r, pages, Hkv, D), synth.kv_pool(r, pages, Hkv, D)
+        bt = synth.block_table(r, lens, pages)
+        q = synth.normal_fp16(r, (B, Hq, D))
+        ref = orc.paged_attention(q, kp, vp, bt, lens, 1 / math.sqrt(D))
+        cases.append(([to_dev(a, torch) for a in (q, kp, vp, bt, lens)], Lmax, part, ref))
+        need = max(need, api.paged_gqa_decode_workspace_size(B, Hq, Hkv, Lmax, part))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        outs = [api.paged_gqa_decode(*args, max_context=Lmax, partition_tokens=part, workspace=ws)
+                for args, Lmax, part, _ in cases]
+        torch.cuda.synchronize()
+        for o, (_, Lmax, part, ref) in zip(outs, cases):
+            assert_close(to_host(o), ref, what=f"shared workspace pass {rep} part={part}")
+
+
 def test_paged_gqa_decode_strided_q_matches_packed(api):
     r = np.random.default_rng(12)
     D, Hq, Hkv = 128, 28, 4

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle as orc
-from gpu_util import assert_close, assert_close_composite, to_dev, to_host
+from gpu_util import assert_close, layer_parity, to_dev, to_host
 from w4a16_decode_paged_gb300 import synth
 
 torch = pytest.importorskip("torch")
@@ -20,31 +20,7 @@ def api():
 
 
 def _layer_parity(api, cfg, lens=None, seed=None):
-    case = synth.layer_case(cfg, lens=lens, seed=seed)
-    w = case["weights"]
-    dl = api.device_layer(w, case["k_pool"], case["v_pool"])
-    model = api.Model(cfg, [dl], max_batch=cfg["batch"], max_context=int(case["context_lens"].max()) + 16,
-                      num_pages=case["k_pool"].shape[0])
-    x = to_dev(case["x"], torch)
-    bt = to_dev(case["block_table"], torch)
-    ld = to_dev(case["context_lens"], torch)
-    model.layer(0, x, bt, ld)
-    torch.cuda.synchronize()
-    kp, vp = case["k_pool"].copy(), case["v_pool"].copy()
-    ref = orc.decoder_layer(cfg, w, case["x"], kp, vp, case["block_table"], case["context_lens"])
-    assert_close_composite(to_host(x), ref, what=cfg["name"])
-    # pools: only the appended slots changed (placement bit-exact); the
-    # appended k, v come from the q|k|v GEMV, so their values match within
-    # the fp16 tolerance
-    for name, ref_pool in (("k_pool", kp), ("v_pool", vp)):
-        got = to_host(dl[name])
-        diff = np.any(got != case[name], axis=-1)
-        for pg, h, sl in np.argwhere(diff):
-            assert any(int(case["block_table"][b, (L - 1) // 16]) == pg and (L - 1) % 16 == sl
-                       for b, L in enumerate(case["context_lens"])), (name, pg, h, sl)
-        assert_close(got, ref_pool, what=name)
-    assert model.check_errors() == 0
-    model.close()
+    layer_parity(api, torch, orc, synth, cfg, lens=lens, seed=seed)
 
 
 def test_tiny_layer_matches_oracle(api):

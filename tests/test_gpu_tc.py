@@ -48,6 +48,36 @@ def test_w4a16_gemm_repeat_calls_leave_counters_zero(api):
     assert torch.equal(y1, y2)
 
 
+def test_one_workspace_serves_projections_of_different_shapes(api):
+    """The decoder layer's four projections in turn on one split-K workspace
+    (its tickets sit at a fixed place whatever the shape), twice over."""
+    r = np.random.default_rng(11)
+    M = 32
+    shapes = [(3584, 4608, False), (3584, 3584, False), (3584, 18944, True), (18944, 3584, False)]
+    lib = api.load()
+    ws = torch.zeros(max(lib.w4a16_gemm_workspace_size(M, K, N, int(silu)) for K, N, silu in shapes),
+                     dtype=torch.uint8, device="cuda")
+    cases = []
+    for K, N, silu in shapes:
+        x = synth.normal_fp16(r, (M, K))
+        w = [synth.int4_weight(r, N, K) for _ in range(2 if silu else 1)]
+        if silu:
+            ref = orc.silu_mul(orc.w4a16_gemv(x, *w[0]), orc.w4a16_gemv(x, *w[1]))
+        else:
+            ref = orc.w4a16_gemv(x, *w[0])
+        cases.append((to_dev(x, torch), [(to_dev(q, torch), to_dev(s_, torch)) for q, s_ in w], silu, ref))
+    for rep in range(2):
+        outs = []
+        for x, w, silu, ref in cases:
+            if silu:
+                outs.append(api.w4a16_gemm_silu_mul(x, w[0][0], w[0][1], w[1][0], w[1][1], workspace=ws))
+            else:
+                outs.append(api.w4a16_gemm(x, w[0][0], w[0][1], workspace=ws))
+        torch.cuda.synchronize()
+        for y, (_, _, _, ref) in zip(outs, cases):
+            assert_close(to_host(y), ref, what=f"shared workspace pass {rep}")
+
+
 @pytest.mark.parametrize("K,N,M", [(896, 2432, 32), (3584, 18944, 32), (3584, 256, 9)])
 def test_w4a16_gemm_silu_mul_matches_oracle(api, K, N, M):
     r = np.random.default_rng(K + N + M)

@@ -76,6 +76,7 @@ SIGNATURES = {
     "w4a16_model_err_flag": (P, [P]),
     "w4a16_model_check_errors": (I32, [P, P]),
     "w4a16_model_hidden": (I32, [P, P, I32, P]),
+    "w4a16_model_activation": (I32, [P, I32, P, I32, P]),
     "w4a16_model_layer": (I32, [P, I32, P, P, I32, P, I32, P]),
     "decode_step": (I32, [P, P, P, P, I32, P, I32, P, I32, P]),
     "decode_step_kernel_count": (I32, [P, I32]),

@@ -288,6 +288,20 @@ class Model:
         check(self._lib.w4a16_model_hidden(self._h, _p(out), int(B), stream_handle(stream)))
         return out
 
+    ACTIVATIONS = {"hidden": (0, "hidden"), "qkv": (1, None), "attn": (2, None), "resid": (3, "hidden"),
+                   "mlp": (4, "inter")}
+
+    def activation(self, name, B=1, stream=None):
+        """Copy of an arena activation buffer left by the last layer or step:
+        hidden, qkv, attn, resid (x + o) or mlp (silu(gate) * up)."""
+        which, key = self.ACTIVATIONS[name]
+        c = self.cfg
+        width = {"qkv": (c["n_q_heads"] + 2 * c["n_kv_heads"]) * c["head_dim"],
+                 "attn": c["n_q_heads"] * c["head_dim"]}.get(name) or c[key]
+        out = torch.empty((B, width), dtype=torch.float16, device="cuda")
+        check(self._lib.w4a16_model_activation(self._h, which, _p(out), int(B), stream_handle(stream)))
+        return out
+
     def check_errors(self, stream=None) -> int:
         """Status code of the device error word (blocks; clears the word)."""
         return int(self._lib.w4a16_model_check_errors(self._h, stream_handle(stream)))
@@ -306,6 +320,17 @@ class Model:
 
     def kernel_count(self, B=1) -> int:
         return int(self._lib.decode_step_kernel_count(self._h, int(B)))
+
+
+def device_pool(case: dict, layer: int, which: str, device="cuda"):
+    """One layer's K or V pool of a ``synth.model_case`` on the device: zeros,
+    with the pages the block tables name filled in."""
+    cfg = case["cfg"]
+    p = torch.zeros((case["pool_pages"], cfg["n_kv_heads"], 16, cfg["head_dim"]), dtype=torch.float16,
+                    device=device)
+    idx = torch.from_numpy(case["used_pages"]).to(device)
+    p[idx] = torch.from_numpy(case[which + "_used"][layer]).to(device)
+    return p
 
 
 def device_layer(w: dict, k_pool, v_pool, device="cuda") -> dict:

@@ -506,8 +506,17 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
 }
 
 size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P) {
+  (void)Hkv;
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  return up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4) + up((size_t)B * Hkv * 4);
+  return ATT_TICKET_BYTES + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4);
+}
+
+void attention_workspace_layout(AttnArgs& a, void* ws, int B, int Hq, int P) {
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  char* w = static_cast<char*>(ws);
+  a.counters = reinterpret_cast<unsigned int*>(w);
+  a.ws_o = reinterpret_cast<float*>(w + ATT_TICKET_BYTES);
+  a.ws_ml = reinterpret_cast<float*>(w + ATT_TICKET_BYTES + up((size_t)B * Hq * P * ATT_D * 4));
 }
 
 template <int G>
@@ -543,6 +552,9 @@ static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
 int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
   if (a_in.P > ATT_MAX_PARTITIONS)
     return set_error(W4A16_ERR_SHAPE, "paged attention: %d partitions > %d", a_in.P, ATT_MAX_PARTITIONS);
+  if (a_in.P > 1 && (size_t)a_in.B * a_in.Hkv * 4 > ATT_TICKET_BYTES)
+    return set_error(W4A16_ERR_SHAPE, "paged attention: B*Hkv=%d split-K tickets > %zu", a_in.B * a_in.Hkv,
+                     ATT_TICKET_BYTES / 4);
   AttnArgs a = a_in;
   // up to 8 partitions (a portable cluster) merge through distributed shared
   // memory; more go through the workspace and a last-CTA ticket
@@ -677,11 +689,7 @@ extern "C" int paged_gqa_decode(const uint16_t* q, int q_stride, const uint16_t*
     W4_CHECK_ARG(workspace != nullptr && workspace_bytes >= need,
                  "paged_gqa_decode: workspace of %zu bytes needed", need);
     W4_CHECK_ALIGN(workspace, 128, "workspace");
-    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    char* w = static_cast<char*>(workspace);
-    a.ws_o = reinterpret_cast<float*>(w);
-    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
-    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+    attention_workspace_layout(a, workspace, B, Hq, P);
   }
   a.q = reinterpret_cast<const __half*>(q);
   a.k_pool = reinterpret_cast<__half*>(const_cast<uint16_t*>(k_pool));
@@ -732,11 +740,7 @@ extern "C" int paged_gqa_decode_rope_append(const uint16_t* qkv, int qkv_stride,
     W4_CHECK_ARG(workspace != nullptr && workspace_bytes >= need,
                  "paged_gqa_decode_rope_append: workspace of %zu bytes needed", need);
     W4_CHECK_ALIGN(workspace, 128, "workspace");
-    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    char* w = static_cast<char*>(workspace);
-    a.ws_o = reinterpret_cast<float*>(w);
-    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
-    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+    attention_workspace_layout(a, workspace, B, Hq, P);
   }
   a.q = reinterpret_cast<const __half*>(qkv);
   a.k_pool = reinterpret_cast<__half*>(k_pool);
@@ -854,11 +858,7 @@ extern "C" int paged_gqa_decode_noalloc(const uint16_t* q, int q_stride, const u
     void* base = nullptr;
     int rc = noalloc_scratch(&base);
     if (rc) return rc;
-    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    char* w = static_cast<char*>(base);
-    a.ws_o = reinterpret_cast<float*>(w);
-    a.ws_ml = reinterpret_cast<float*>(w + up((size_t)B * Hq * P * ATT_D * 4));
-    a.counters = reinterpret_cast<unsigned int*>(w + up((size_t)B * Hq * P * ATT_D * 4) + up((size_t)B * Hq * P * 2 * 4));
+    attention_workspace_layout(a, base, B, Hq, P);
     // the array keeps the previous call's contents: the tickets must start at zero
     cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)B * Hkv * sizeof(unsigned int), (cudaStream_t)stream);
     if (e != cudaSuccess)

@@ -15,10 +15,12 @@ namespace w4 {
 // RMSNorm: one CTA per row.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma,
-                                                      __half* y, int H, float eps) {
+                                                      __half* y, int H, float eps, int tag) {
   __shared__ float red[8];
   __shared__ float rs;
+  W4_TRACE_SCOPE(tag);
   pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
   const int m = blockIdx.x;
   const __half* xr = x + (size_t)m * H;
   float ss = 0.f;
@@ -52,8 +54,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __half* __restrict__
   }
 }
 
-int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s) {
-  cudaError_t e = launch_pdl(rmsnorm_kernel, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
+int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s,
+                   int tag) {
+  cudaError_t e = launch_pdl(rmsnorm_kernel, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "rmsnorm launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }

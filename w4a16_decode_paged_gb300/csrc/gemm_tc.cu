@@ -431,13 +431,19 @@ size_t tc_workspace_bytes(int N, int ksplit, bool silu) {
   const int ntiles = (N + TC_M - 1) / TC_M;
   const size_t na = silu ? 2 : 1;
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  return up((size_t)ntiles * ksplit * na * TC_N * TC_M * 4) + up((size_t)ntiles * 4);
+  return TC_TICKET_BYTES + up((size_t)ntiles * ksplit * na * TC_N * TC_M * 4);
+}
+
+void tc_workspace_layout(TcArgs& a, void* ws) {
+  a.counters = static_cast<unsigned int*>(ws);
+  a.ws = reinterpret_cast<float*>(static_cast<char*>(ws) + TC_TICKET_BYTES);
 }
 
 int tc_default_ksplit(int N, int K) {
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nst = K / TC_K;
   int ks = 1;
+  if ((size_t)ntiles * 4 > TC_TICKET_BYTES) return 1;  // more tiles than tickets: no split
   while (ntiles * ks * 2 <= num_sms() * 2 && nst / (ks * 2) >= 8) ks *= 2;
   return ks;
 }
@@ -544,13 +550,8 @@ static int tc_common_checks(const uint16_t* x, int M, int K, int N, const uint16
   return W4A16_OK;
 }
 
-static void tc_ws(TcArgs& a, void* ws, int N, bool silu) {
-  if (a.ksplit <= 1) return;
-  const int ntiles = (N + 127) / 128;
-  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  a.ws = static_cast<float*>(ws);
-  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) +
-                                               up((size_t)ntiles * a.ksplit * (silu ? 2 : 1) * 32 * 128 * 4));
+static void tc_ws(TcArgs& a, void* ws) {
+  if (a.ksplit > 1) tc_workspace_layout(a, ws);
 }
 
 extern "C" int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweight, const uint16_t* scales, int N,
@@ -575,7 +576,7 @@ extern "C" int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweig
   a.N = N;
   a.ldy = N;
   a.ksplit = ks;
-  tc_ws(a, workspace, N, false);
+  tc_ws(a, workspace);
   return launch_gemm_tc(a, true, false, (cudaStream_t)stream);
 }
 
@@ -602,7 +603,7 @@ extern "C" int w4a16_gemm_silu_mul(const uint16_t* x, int M, int K, const uint32
   a.N = N;
   a.ldy = N;
   a.ksplit = ks;
-  tc_ws(a, workspace, N, true);
+  tc_ws(a, workspace);
   return launch_gemm_tc(a, true, true, (cudaStream_t)stream);
 }
 

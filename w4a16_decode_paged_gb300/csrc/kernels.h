@@ -46,8 +46,16 @@ struct TcArgs {
   int M, K, N, ldy, ksplit, tag;
 };
 int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
+
+// Split-K workspaces (tensor-core GEMM and attention) start with a fixed
+// block of tickets, zero between calls, followed by the partial results.
+// The tickets' place does not depend on the call's shape, so one zeroed
+// workspace can serve calls of different shapes in turn.
+constexpr size_t TC_TICKET_BYTES = 8192;    // one ticket per 128-row tile: up to 2048 tiles
+constexpr size_t ATT_TICKET_BYTES = 16384;  // one ticket per (sequence, kv head): up to 4096
 size_t tc_workspace_bytes(int N, int ksplit, bool silu);
 int tc_default_ksplit(int N, int K);
+void tc_workspace_layout(TcArgs& a, void* ws);  // sets a.counters / a.ws (a.ksplit > 1)
 int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
                        int tag);
 
@@ -73,6 +81,7 @@ struct AttnArgs {
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
 constexpr int ATT_MAX_PARTITIONS = 1024;
 size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P);
+void attention_workspace_layout(AttnArgs& a, void* ws, int B, int Hq, int P);  // sets ws_o, ws_ml, counters
 
 // RoPE + KV append.
 struct RopeArgs {
@@ -90,7 +99,8 @@ struct RopeArgs {
 int launch_rope_append(const RopeArgs& a, cudaStream_t s);
 void rope_inv_freq_table(float theta, int D, float* out);
 
-int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s);
+int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s,
+                   int tag = 0);
 int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
                      int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s, int tag = 0);
 

@@ -16,6 +16,11 @@
 // argmax].  Every kernel is launched with programmatic dependent launch, so
 // a GEMV streams its first weights, and the attention its KV pages, while
 // the predecessor finishes.
+//
+// A decode batch of more than 4 sequences is a dense contraction: each
+// projection becomes [RMSNorm] + a tensor-core GEMM (exact int4 codes into
+// tcgen05 MMAs, K split across CTAs), and the lm_head a tensor-core GEMM to
+// fp32 logits followed by a row-wise argmax.
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -52,6 +57,10 @@ struct w4a16_model {
   size_t attn_ws_bytes = 0;
   void* lm_ws = nullptr;
   size_t lm_ws_bytes = 0;
+  __half* xn = nullptr;      // normalised activations of the batched path [max_batch][max K]
+  float* logits32 = nullptr; // batched lm_head logits [max_batch][vocab] (max_batch > 4)
+  void* tc_ws = nullptr;     // split-K partial tiles + tickets of the tensor-core GEMMs
+  size_t tc_ws_bytes = 0;
   int32_t* err_flag = nullptr;
   float inv_freq[64];
   cudaStream_t cap_stream = nullptr;
@@ -60,6 +69,13 @@ struct w4a16_model {
 };
 
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Largest batch whose projections all take the CUDA-core GEMV with the
+// RMSNorm fused in front, and whose lm_head takes the fused GEMV + argmax.
+static constexpr int GEMV_MAX_BATCH = 4;
+static bool batched_path(const w4a16_model* m, int B) {
+  return B > GEMV_MAX_BATCH || !gemv_cuda_core_supported(B, m->cfg.hidden);
+}
 
 extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
                                   int max_context, w4a16_model** out) {
@@ -76,8 +92,7 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   W4_CHECK_ARG(c.n_layers == 0 || w->layers != nullptr, "model_create: null layer array");
   W4_CHECK_SHAPE(c.partition_tokens % 16 == 0 && c.partition_tokens >= 0, "model_create: partition_tokens");
   const int maxK = std::max(std::max(c.hidden, c.inter), c.n_q_heads * c.head_dim);
-  W4_CHECK_SHAPE(gemv_cuda_core_supported(max_batch, maxK),
-                 "model_create: max_batch=%d with K=%d is outside the built GEMV paths", max_batch, maxK);
+  W4_CHECK_SHAPE(max_batch <= 32, "model_create: max_batch=%d > 32 (one tensor-core tile of sequences)", max_batch);
 
   w4a16_model* m = new w4a16_model();
   m->cfg = c;
@@ -111,6 +126,18 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   const size_t o_aws = off; off += up256(m->attn_ws_bytes);
   m->lm_ws_bytes = lm_head_workspace_bytes(max_batch, c.vocab);
   const size_t o_lws = off; off += up256(m->lm_ws_bytes);
+  const size_t o_xn = off; off += up256((size_t)max_batch * maxK * 2);
+  const size_t o_l32 = off; off += max_batch > GEMV_MAX_BATCH ? up256((size_t)max_batch * c.vocab * 4) : 0;
+  {
+    auto need = [&](int N, int K, bool silu) {
+      m->tc_ws_bytes = std::max(m->tc_ws_bytes, tc_workspace_bytes(N, tc_default_ksplit(N, K), silu));
+    };
+    need((int)nqkv, c.hidden, false);
+    need(c.hidden, c.n_q_heads * D, false);
+    need(c.inter, c.hidden, true);
+    need(c.hidden, c.inter, false);
+  }
+  const size_t o_tws = off; off += up256(m->tc_ws_bytes);
   const size_t o_err = off; off += 256;
   m->arena_bytes = off;
   cudaError_t e = cudaMalloc(&m->arena, off);
@@ -126,6 +153,9 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   m->mlp = reinterpret_cast<__half*>(m->arena + o_mlp);
   m->attn_ws = m->arena + o_aws;
   m->lm_ws = m->arena + o_lws;
+  m->xn = reinterpret_cast<__half*>(m->arena + o_xn);
+  m->logits32 = max_batch > GEMV_MAX_BATCH ? reinterpret_cast<float*>(m->arena + o_l32) : nullptr;
+  m->tc_ws = m->arena + o_tws;
   m->err_flag = reinterpret_cast<int32_t*>(m->arena + o_err);
   e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -157,6 +187,25 @@ extern "C" int w4a16_model_hidden(w4a16_model* m, uint16_t* dst, int B, w4a16_st
   return W4A16_OK;
 }
 
+extern "C" int w4a16_model_activation(w4a16_model* m, int which, uint16_t* dst, int B, w4a16_stream_t stream) {
+  W4_CHECK_ARG(m && dst, "model_activation: null argument");
+  W4_CHECK_ARG(B >= 1 && B <= m->max_batch, "model_activation: B=%d", B);
+  const w4a16_model_config& c = m->cfg;
+  const __half* src = nullptr;
+  size_t width = 0;
+  switch (which) {
+    case W4A16_ACT_HIDDEN: src = m->x; width = c.hidden; break;
+    case W4A16_ACT_QKV: src = m->qkv; width = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim; break;
+    case W4A16_ACT_ATTN: src = m->att; width = (size_t)c.n_q_heads * c.head_dim; break;
+    case W4A16_ACT_RESID: src = m->h; width = c.hidden; break;
+    case W4A16_ACT_MLP: src = m->mlp; width = c.inter; break;
+    default: return set_error(W4A16_ERR_INVALID_ARG, "model_activation: unknown buffer %d", which);
+  }
+  cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)B * width * 2, cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "model_activation: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
 extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
   W4_CHECK_ARG(m, "model_check_errors: null model");
   cudaStream_t s = (cudaStream_t)stream;
@@ -171,6 +220,38 @@ extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
   if (host & 2) return set_error(W4A16_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", host);
   if (host & 1) return set_error(W4A16_ERR_DEVICE_BOUNDS, "a kernel skipped an out-of-range index (flag 0x%x)", host);
   return W4A16_OK;
+}
+
+// One projection.  Small batches take the CUDA-core GEMV (RMSNorm fused in
+// front); otherwise the RMSNorm (if any) runs on its own into m->xn and the
+// tensor-core GEMM follows with K split across CTAs.  Returns the number of
+// tags used through *tag.
+static int project(w4a16_model* m, GemvArgs g, bool silu, cudaStream_t s, int* tag) {
+  if (gemv_cuda_core_supported(g.M, g.K) && !(g.gamma && batched_path(m, g.M))) {
+    g.tag = (*tag)++;
+    return launch_gemv(g, silu, s);
+  }
+  int rc;
+  if (g.gamma) {
+    if ((rc = launch_rmsnorm(g.x, g.gamma, m->xn, g.M, g.K, g.eps, s, (*tag)++))) return rc;
+    g.x = m->xn;
+  }
+  TcArgs t = {};
+  t.x = g.x;
+  t.residual = g.residual;
+  t.y = g.y;
+  for (int i = 0; i < 3; ++i) t.seg[i] = g.seg[i];
+  t.nseg = g.nseg;
+  t.err_flag = m->err_flag;
+  t.M = g.M;
+  t.K = g.K;
+  t.N = g.N;
+  t.ldy = g.N;
+  t.ksplit = tc_default_ksplit(g.N, g.K);
+  if (tc_workspace_bytes(g.N, t.ksplit, silu) > m->tc_ws_bytes) t.ksplit = 1;
+  if (t.ksplit > 1) tc_workspace_layout(t, m->tc_ws);
+  t.tag = (*tag)++;
+  return launch_gemm_tc(t, true, silu, s);
 }
 
 static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int max_blocks, const int32_t* lens, int B,
@@ -194,8 +275,8 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   g.M = B;
   g.K = H;
   g.N = nqkv;
-  g.tag = tag0;
-  if ((rc = launch_gemv(g, false, s))) return rc;
+  int tag = tag0;
+  if ((rc = project(m, g, false, s, &tag))) return rc;
 
   // RoPE of q and the new k, the KV append and the paged attention are one
   // kernel: it prefetches this partition's pages while the q|k|v GEMV runs.
@@ -207,11 +288,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   a.block_table = bt;
   a.context_lens = lens;
   a.out = m->att;
-  char* ws = static_cast<char*>(m->attn_ws);
-  a.ws_o = reinterpret_cast<float*>(ws);
-  a.ws_ml = reinterpret_cast<float*>(ws + up256((size_t)m->max_batch * Hq * m->P * D * 4));
-  a.counters = reinterpret_cast<unsigned int*>(ws + up256((size_t)m->max_batch * Hq * m->P * D * 4) +
-                                               up256((size_t)m->max_batch * Hq * m->P * 2 * 4));
+  attention_workspace_layout(a, m->attn_ws, m->max_batch, Hq, m->P);
   a.err_flag = m->err_flag;
   a.num_pages = c.num_pages;
   a.max_blocks = max_blocks;
@@ -223,7 +300,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
   a.fuse_rope_append = 1;
   std::memcpy(a.inv_freq, m->inv_freq, sizeof(a.inv_freq));
-  a.tag = tag0 + 1;
+  a.tag = tag++;
   if ((rc = launch_paged_attention(a, s))) return rc;
 
   GemvArgs o = {};
@@ -235,8 +312,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   o.M = B;
   o.K = Hq * D;
   o.N = H;
-  o.tag = tag0 + 2;
-  if ((rc = launch_gemv(o, false, s))) return rc;
+  if ((rc = project(m, o, false, s, &tag))) return rc;
 
   GemvArgs gu = {};
   gu.x = m->h;
@@ -249,8 +325,7 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   gu.M = B;
   gu.K = H;
   gu.N = I;
-  gu.tag = tag0 + 3;
-  if ((rc = launch_gemv(gu, true, s))) return rc;
+  if ((rc = project(m, gu, true, s, &tag))) return rc;
 
   GemvArgs dn = {};
   dn.x = m->mlp;
@@ -261,9 +336,11 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   dn.M = B;
   dn.K = I;
   dn.N = H;
-  dn.tag = tag0 + 4;
-  return launch_gemv(dn, false, s);
+  return project(m, dn, false, s, &tag);
 }
+
+// kernels one layer launches at batch B
+static int layer_kernel_count(const w4a16_model* m, int B) { return batched_path(m, B) ? 7 : 5; }
 
 extern "C" int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table, int max_blocks,
                                  const int32_t* context_lens, int B, w4a16_stream_t stream) {
@@ -280,8 +357,27 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
   const w4a16_model_config& c = m->cfg;
   int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, s, 0);
   if (rc) return rc;
+  const int per_layer = layer_kernel_count(m, B);
   for (int l = 0; l < c.n_layers; ++l)
-    if ((rc = run_layer(m, l, m->x, bt, max_blocks, lens, B, s, 1 + 5 * l))) return rc;
+    if ((rc = run_layer(m, l, m->x, bt, max_blocks, lens, B, s, 1 + per_layer * l))) return rc;
+  const int tag = 1 + per_layer * c.n_layers;
+  if (batched_path(m, B)) {
+    // final RMSNorm, lm_head on the tensor cores (fp32 logits), argmax
+    if ((rc = launch_rmsnorm(m->x, m->final_norm, m->xn, B, c.hidden, c.eps, s, tag))) return rc;
+    TcArgs t = {};
+    t.x = m->xn;
+    t.y32 = m->logits32;
+    t.w16 = m->lm_head;
+    t.err_flag = m->err_flag;
+    t.M = B;
+    t.K = c.hidden;
+    t.N = c.vocab;
+    t.ldy = c.vocab;
+    t.ksplit = 1;
+    t.tag = tag + 1;
+    if ((rc = launch_gemm_tc(t, false, false, s))) return rc;
+    return launch_argmax_rows(m->logits32, B, c.vocab, tout, reinterpret_cast<__half*>(logits), s, tag + 2);
+  }
   LmHeadArgs a = {};
   a.x = m->x;
   a.w = m->lm_head;
@@ -294,13 +390,13 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
   a.B = B;
   a.H = c.hidden;
   a.vocab = c.vocab;
-  a.tag = 1 + 5 * c.n_layers;
+  a.tag = tag;
   return launch_lm_head_argmax(a, s);
 }
 
 extern "C" int decode_step_kernel_count(w4a16_model* m, int B) {
-  (void)B;
-  return m ? 2 + 5 * m->cfg.n_layers : 0;
+  if (!m) return 0;
+  return 1 + layer_kernel_count(m, B) * m->cfg.n_layers + (batched_path(m, B) ? 3 : 1);
 }
 
 extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tokens_out, const int32_t* block_table,
@@ -309,7 +405,6 @@ extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* to
   W4_CHECK_ARG(m && tokens_in && tokens_out && block_table && context_lens, "decode_step: null argument");
   W4_CHECK_ARG(m->embed && m->final_norm && m->lm_head && m->cfg.vocab > 0, "decode_step: model has no lm_head");
   W4_CHECK_ARG(B >= 1 && B <= m->max_batch && max_blocks >= 1, "decode_step: B=%d (max %d)", B, m->max_batch);
-  W4_CHECK_SHAPE(B <= 4, "decode_step: B=%d > 4 needs the batched lm_head", B);
   W4_CHECK_ALIGN(logits, 128, "logits");
   cudaStream_t s = (cudaStream_t)stream;
   if (!use_graph) return enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, s);

@@ -135,3 +135,38 @@ def layer_case(cfg: dict, lens=None, seed: int | None = None) -> dict:
     v_pool = kv_pool(r, pool_pages, cfg["n_kv_heads"], cfg["head_dim"])
     bt = block_table(r, lens, pool_pages)
     return dict(weights=w, x=x, k_pool=k_pool, v_pool=v_pool, block_table=bt, context_lens=lens)
+
+
+def model_case(cfg: dict, lens, gen_tokens: int = 0, pool_pages: int | None = None, seed: int | None = None) -> dict:
+    """Whole-model inputs for B = len(lens) sequences.
+
+    lens[b] tokens of KV are already cached for sequence b (0 is allowed);
+    each block table also covers gen_tokens further positions, so the pages
+    of the tokens still to be decoded are assigned up front.  Only the pages
+    some table names carry data (N(0,1), drawn per layer into k_used / v_used,
+    rows in the order of used_pages); the rest of each pool is zero and is
+    never read.  host_pool() expands one layer's pool to its full
+    [pool_pages][Hkv][16][D] layout."""
+    r = rng(cfg["seed"] if seed is None else seed)
+    L, H, Hkv, D, V = cfg["n_layers"], cfg["hidden"], cfg["n_kv_heads"], cfg["head_dim"], cfg["vocab"]
+    layers = [layer_weights(r, cfg) for _ in range(L)]
+    lens = np.asarray(lens, np.int32)
+    pool_pages = int(pool_pages or cfg.get("pool_pages", 256))
+    bt = block_table(r, lens + gen_tokens, pool_pages)
+    used = np.unique(bt[bt >= 0]).astype(np.int64)
+    k_used = [normal_fp16(r, (len(used), Hkv, PAGE, D)) for _ in range(L)]
+    v_used = [normal_fp16(r, (len(used), Hkv, PAGE, D)) for _ in range(L)]
+    embed = normal_fp16(r, (V, H))
+    fnorm = gamma(r, H)
+    lm = normal_fp16(r, (V, H), std=0.02)
+    tok = r.integers(0, V, size=len(lens)).astype(np.int32)
+    return dict(cfg=cfg, layers=layers, k_used=k_used, v_used=v_used, used_pages=used, pool_pages=pool_pages,
+                bt=bt, lens=lens, tok=tok, embed=embed, fnorm=fnorm, lm=lm)
+
+
+def host_pool(case: dict, layer: int, which: str) -> np.ndarray:
+    """Layer `layer`'s K (which="k") or V ("v") pool as one numpy array."""
+    cfg = case["cfg"]
+    p = np.zeros((case["pool_pages"], cfg["n_kv_heads"], PAGE, cfg["head_dim"]), np.float16)
+    p[case["used_pages"]] = case[which + "_used"][layer]
+    return p
