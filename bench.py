@@ -342,10 +342,22 @@ def run_kernel(args):
         res = torch.randn((B, N), device=dev).half()
         y = torch.empty((B, N), dtype=torch.float16, device=dev)
         fns = []
+        tc = B > 4   # decode batches above 4 take the tensor-core GEMM (RMSNorm not fused)
+        if tc:
+            ws = torch.zeros(api.load().w4a16_gemm_workspace_size(B, K, N, int(name == "gateup")),
+                             dtype=torch.uint8, device=dev)
         for _ in range(copies):
             qw, sc = synth.int4_weight(r, N, K, "symmetric")
             qw, sc = tdev(qw), tdev(sc)
-            if name == "gateup":
+            if tc and name == "gateup":
+                qu, su = synth.int4_weight(r, N, K, "symmetric")
+                qu, su = tdev(qu), tdev(su)
+                fns.append(lambda qw=qw, sc=sc, qu=qu, su=su: api.w4a16_gemm_silu_mul(x, qw, sc, qu, su, out=y,
+                                                                                      workspace=ws))
+            elif tc:
+                fns.append(lambda qw=qw, sc=sc: api.w4a16_gemm(x, qw, sc, residual=res if name in ("down", "o")
+                                                               else None, out=y, workspace=ws))
+            elif name == "gateup":
                 qu, su = synth.int4_weight(r, N, K, "symmetric")
                 qu, su = tdev(qu), tdev(su)
                 fns.append(lambda qw=qw, sc=sc, qu=qu, su=su: api.w4a16_gemv_silu_mul(x, g, 1e-6, qw, sc, qu, su, out=y))

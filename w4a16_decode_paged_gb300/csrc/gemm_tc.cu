@@ -9,20 +9,27 @@
 // 128-row weight tile, its B operand the (up to) 32 activation rows, so
 // D[n][m] (128 lanes x 32 columns, fp32) lives in tensor memory.
 //
-// Per 64-wide K stage, 128 threads dequantise their weight row (int4 codes
-// times the fp16 group scale, rounded to fp16) straight into the canonical
-// no-swizzle K-major shared-memory layout -- core matrices of 8 rows x 16
-// bytes; K-adjacent core matrices 128 B apart, 8-row groups 256 B apart --
-// and stage the activations the same way; one thread then issues four
-// kind::f16 MMAs (K = 16 each) and commits them to the stage's mbarrier.
-// Two stage buffers let the dequant of stage s+1 overlap the MMAs of s.
-// Within each 8-wide k group both operands use the order 0,4,1,5,2,6,3,7,
-// which is the order the two-nibbles-per-LOP3 unpack produces.
+// The weights are streamed once, so the kernel is a bandwidth pipe: a ring of
+// TC_S stages (64 k each) in shared memory, filled TC_AHEAD stages ahead with
+// cp.async (packed int4 rows and the activation tile, the latter directly in
+// the canonical no-swizzle K-major layout the MMA reads: core matrices of 8
+// rows x 16 bytes, K-adjacent core matrices 128 B apart, 8-row groups 256 B
+// apart).  Per stage each of 256 threads turns 32 codes of its weight row
+// into exact fp16 integers (q in [-8, 7]) in a double-buffered A tile, and
+// one thread issues four kind::f16 MMAs (K = 16) per weight matrix.
 //
-// Small-N projections split K across CTAs: each split writes its fp32 tile
-// to the workspace and the last split of a tile (atomic ticket) sums them
-// and runs the epilogue.  Dense fp16 weights (the batched lm_head) skip the
-// dequant and use the natural k order.
+// Precision: the MMAs see exact codes and exact fp16 activations (products
+// exact, fp32 sums).  Each 128-wide scale group accumulates into its own
+// tensor-memory buffer (two alternate); the threads read a group's sums
+// with tcgen05.ld two stages after its last MMAs were issued (while the
+// tensor core works on the next group) and add them times the row's fp32
+// scale, so the only roundings are fp32 sums and the final fp16 store.
+//
+// Small-N projections split K across CTAs (split length chosen so the work
+// items fill whole waves of CTAs): each split parks its fp32 tile in the
+// workspace and the last split of a tile (atomic ticket) sums them and runs
+// the epilogue.  Dense fp16 weights (the batched lm_head) are copied into the
+// ring in the canonical layout and used by the MMA as they are.
 #include <algorithm>
 #include <cstdio>
 
@@ -34,10 +41,20 @@ namespace w4 {
 constexpr int TC_M = 128;      // weight rows per tile (MMA M)
 constexpr int TC_N = 32;       // batch columns (MMA N)
 constexpr int TC_K = 64;       // K per stage
-constexpr int TC_THREADS = 128;
-constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB per matrix per stage
-constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB per stage
+constexpr int TC_THREADS = 256;
+constexpr int TC_S = 8;        // ring stages
+constexpr int TC_AHEAD = 6;    // stages loaded ahead of the one computed
+constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
+constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB activation tile per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
+
+template <bool INT4, bool SILU>
+struct TcShape {
+  static constexpr int NA = SILU ? 2 : 1;                                   // weight matrices per tile
+  static constexpr uint32_t A_RAW = INT4 ? NA * TC_M * 32 : TC_A_BYTES;     // A bytes per ring slot
+  static constexpr uint32_t SLOT = A_RAW + TC_B_BYTES;
+  static constexpr size_t SMEM = (size_t)TC_S * SLOT + (INT4 ? (size_t)2 * NA * TC_A_BYTES : 0) + 1024;
+};
 
 __device__ __forceinline__ unsigned long long tc_now() {
   unsigned long long t;
@@ -53,6 +70,13 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
       if (mbar_try_wait(bar, parity)) return true;
     if (tc_now() - t0 > TC_TIMEOUT_NS) return false;
   }
+}
+
+// 16-byte cp.async that writes zeros when `valid` is false (src not read).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
 }
 
 // Shared-memory matrix descriptor: no swizzle, K-major, LBO = 128 B between
@@ -83,59 +107,53 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 
-// 8 codes of one packed word -> exact fp16 codes q in the order 0,4,1,5,2,6,3,7.
+// The 8 codes of one packed word (nibble i = element i, offset binary
+// u = q + 8) as exact fp16 integers q0..q7 in k order.  A nibble placed in
+// the low mantissa bits of 1024 gives 1024 + u; one placed four bits higher
+// gives 1024 + 16 u, scaled back by 1/16 -- both exact in fp16.
 __device__ __forceinline__ uint4 codes_word(uint32_t w) {
   constexpr uint32_t MAGIC = 0x64006400u;      // half2{1024, 1024}
   constexpr uint32_t OFF = 0x64086408u;        // half2{1032, 1032}
   constexpr uint32_t SIXTEENTH = 0x2C002C00u;  // half2{1/16, 1/16}
   constexpr uint32_t M72 = 0xD480D480u;        // half2{-72, -72}
   const uint32_t w8 = w >> 8;
+  const uint32_t q04 = hsub2(and_or(w, 0x000F000Fu, MAGIC), OFF);
+  const uint32_t q15 = hfma2_u32(and_or(w, 0x00F000F0u, MAGIC), SIXTEENTH, M72);
+  const uint32_t q26 = hsub2(and_or(w8, 0x000F000Fu, MAGIC), OFF);
+  const uint32_t q37 = hfma2_u32(and_or(w8, 0x00F000F0u, MAGIC), SIXTEENTH, M72);
   uint4 o;
-  o.x = hsub2(and_or(w, 0x000F000Fu, MAGIC), OFF);                 // q0, q4
-  o.y = hfma2_u32(and_or(w, 0x00F000F0u, MAGIC), SIXTEENTH, M72);  // q1, q5
-  o.z = hsub2(and_or(w8, 0x000F000Fu, MAGIC), OFF);                // q2, q6
-  o.w = hfma2_u32(and_or(w8, 0x00F000F0u, MAGIC), SIXTEENTH, M72); // q3, q7
-  return o;
-}
-
-// fp16 x0..x7 -> order 0,4,1,5,2,6,3,7
-__device__ __forceinline__ uint4 permute_k8(uint4 v) {
-  uint4 o;
-  o.x = prmt(v.x, v.z, 0x5410);
-  o.y = prmt(v.x, v.z, 0x7632);
-  o.z = prmt(v.y, v.w, 0x5410);
-  o.w = prmt(v.y, v.w, 0x7632);
+  o.x = prmt(q04, q15, 0x5410);  // q0 q1
+  o.y = prmt(q26, q37, 0x5410);  // q2 q3
+  o.z = prmt(q04, q15, 0x7632);  // q4 q5
+  o.w = prmt(q26, q37, 0x7632);  // q6 q7
   return o;
 }
 
 template <bool INT4, bool SILU>
-__global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
-  constexpr int NA = SILU ? 2 : 1;  // weight matrices per tile (gate and up)
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* sA = smem;                               // [2][NA][TC_A_BYTES]
-  unsigned char* sB = smem + 2 * NA * TC_A_BYTES;         // [2][TC_B_BYTES]
-  __shared__ __align__(8) uint64_t bars[2];   // stage buffers free again
-  __shared__ __align__(8) uint64_t gbars[2];  // a group's MMAs complete (per tensor-memory buffer)
+__global__ void __launch_bounds__(TC_THREADS, SILU || !INT4 ? 1 : 2) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
+  using SH = TcShape<INT4, SILU>;
+  constexpr int NA = SH::NA;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
+  unsigned char* afp = smem + TC_S * SH::SLOT;   // [2][NA][TC_A_BYTES] exact codes (INT4)
+  __shared__ __align__(8) uint64_t bars[2];   // a stage's MMAs done: its A buffer and ring slot are free
+  __shared__ __align__(8) uint64_t gbars[2];  // a group's MMAs done (per tensor-memory buffer)
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last;
-  __shared__ int s_ok;
+  __shared__ volatile int s_fail;
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int warp = tid >> 5;
+  const int row_l = tid & (TC_M - 1);  // this thread's weight row within a tile
+  const int half = tid >> 7;           // k chunks 4h..4h+3 of a stage; batch columns 16h..16h+15
   const int K = a.K, M = a.M, N = a.N;
-  const int nst = K / TC_K;                               // stages over the whole K
-  const int per_split = ((nst + a.ksplit - 1) / a.ksplit + 1) & ~1;  // even: splits start on a group
+  const int nst = K / TC_K, ps = a.per_split, ks = a.ksplit;
   const int ntiles = (N + TC_M - 1) / TC_M;
-  const int nwork = ntiles * a.ksplit;
+  const int nwork = ntiles * ks;
   W4_TRACE_SCOPE(a.tag);
 
-  // tensor memory: NA accumulators of TC_N fp32 columns, allocated with a
-  // factor-2 margin (power of two, >= 32 columns)
+  // tensor memory: two group buffers of NA accumulators of TC_N fp32 columns
   constexpr uint32_t TMEM_COLS = 2 * NA * TC_N;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -148,173 +166,290 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     mbar_init(&bars[1], 1);
     mbar_init(&gbars[0], 1);
     mbar_init(&gbars[1], 1);
+    s_fail = 0;
     fence_mbar_init();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
-  pdl_wait_then_trigger();
-  W4_TRACE_WAITED();
 
-  bool ok = true;
-  uint32_t it = 0;  // stages processed by this CTA (selects buffer and mbarrier phase)
-  uint32_t gc = 0;  // 128-wide groups processed by this CTA (selects tensor-memory buffer)
-  uint32_t issued = 0;  // stages whose MMAs were issued (drained before tensor memory is freed)
-  for (int work = blockIdx.x; work < nwork && ok; work += gridDim.x) {
-    const int tile = work / a.ksplit, split = work % a.ksplit;
-    const int n0 = tile * TC_M;
-    const int s_begin = split * per_split, s_end = min(nst, s_begin + per_split);
-    // this thread's weight row (A operand row tid)
-    const int row = n0 + tid;
-    const bool row_ok = row < N;
-    const uint32_t* qrow[NA];
-    const __half* srow[NA];
-    const __half* wrow16 = nullptr;
-#pragma unroll
-    for (int g = 0; g < NA; ++g) {
-      qrow[g] = nullptr;
-      srow[g] = nullptr;
-    }
-    if (row_ok) {
-      if (INT4) {
-        if (SILU) {
-#pragma unroll
-          for (int g = 0; g < NA; ++g) {
-            qrow[g] = a.seg[g].qw + (size_t)row * (K / 8);
-            srow[g] = a.seg[g].s + (size_t)row * (K / 128);
-          }
-        } else {
-          int r = row, si = 0;
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-          qrow[0] = a.seg[si].qw + (size_t)r * (K / 8);
-          srow[0] = a.seg[si].s + (size_t)r * (K / 128);
-        }
-      } else {
-        wrow16 = a.w16 + (size_t)row * K;
-      }
-    }
-
-    // Per 128-wide group the MMAs accumulate exact codes x activations into
-    // one of two tensor-memory buffers; the threads read a group's sums one
-    // group later (while the tensor core works on the next group) and add
-    // them, times the row's fp32 scale, to registers.
-    float acc[NA][TC_N];
-#pragma unroll
-    for (int g = 0; g < NA; ++g)
-#pragma unroll
-      for (int j = 0; j < TC_N; ++j) acc[g][j] = 0.f;
-    float sc_prev[NA];
-#pragma unroll
-    for (int g = 0; g < NA; ++g) sc_prev[g] = 0.f;
-    auto read_group = [&](uint32_t grp, const float (&scale)[NA]) -> bool {
-      // grp: this CTA's running group index; wait for its MMAs, then read
-      if (tid == 0) s_ok = tc_wait(&gbars[grp & 1], (grp >> 1) & 1) ? 1 : 0;
-      __syncthreads();
-      if (!s_ok) return false;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll
-      for (int g = 0; g < NA; ++g) {
-        uint32_t r[32];
-        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (grp & 1) * (NA * TC_N) + (uint32_t)(g * TC_N);
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-            "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int j = 0; j < TC_N; ++j) acc[g][j] = fmaf(__uint_as_float(r[j]), scale[g], acc[g][j]);
-      }
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      return true;
-    };
-    // the row's scales live in the epilogue's lane mapping: thread (warp, lane) owns row n0 + 32 warp + lane
-    const int erow = n0 + warp * 32 + lane;
-    const __half* esrow[NA];
-#pragma unroll
-    for (int g = 0; g < NA; ++g) esrow[g] = nullptr;
-    if (INT4 && erow < N) {
+  // ---- loader cursor: (work item, stage) of the next stage to load ----------
+  int l_work = blockIdx.x, l_st = 0, l_end = 0;
+  const uint32_t* l_q[NA];
+  const __half* l_s[NA];
+  const __half* l_w = nullptr;
+  bool l_ok = false;  // this thread's row exists
+  auto l_item = [&]() {
+    if (l_work >= nwork) return;
+    const int tile = l_work / ks, split = l_work % ks;
+    l_st = split * ps;
+    l_end = min(nst, l_st + ps);
+    const int row = tile * TC_M + row_l;
+    l_ok = row < N;
+    const int rr = l_ok ? row : 0;
+    if (INT4) {
       if (SILU) {
 #pragma unroll
-        for (int g = 0; g < NA; ++g) esrow[g] = a.seg[g].s + (size_t)erow * (K / 128);
+        for (int g = 0; g < NA; ++g) {
+          l_q[g] = a.seg[g].qw + (size_t)rr * (K / 8);
+          l_s[g] = a.seg[g].s + (size_t)rr * (K / 128);
+        }
       } else {
-        int r = erow, si = 0;
+        int r = rr, si = 0;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
           if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-        esrow[0] = a.seg[si].s + (size_t)r * (K / 128);
+        l_q[0] = a.seg[si].qw + (size_t)r * (K / 8);
+        l_s[0] = a.seg[si].s + (size_t)r * (K / 128);
+      }
+    } else {
+      l_w = a.w16 + (size_t)rr * K;
+    }
+  };
+  auto l_next = [&]() {
+    if (l_work >= nwork) return;
+    if (++l_st >= l_end) {
+      l_work += gridDim.x;
+      l_item();
+    }
+  };
+  // weights of the loader's stage into ring slot `slot`
+  auto load_a = [&](int slot) {
+    if (l_work >= nwork) return;
+    unsigned char* sa = ring + slot * SH::SLOT;
+    const int k0 = l_st * TC_K;
+    if (INT4) {
+#pragma unroll
+      for (int g = 0; g < NA; ++g)
+        cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + half * 16, l_q[g] + k0 / 8 + 4 * half, l_ok);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int w = 4 * half + i;
+        cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), l_w + k0 + 8 * w, l_ok);
       }
     }
+  };
+  // activation tile of stage `st` into ring slot `slot` (canonical layout)
+  auto load_b = [&](int slot, int st) {
+    unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
+    const int m = tid >> 3, w = tid & 7;
+    const bool ok = m < M;
+    cp_async16_zfill(sb + tc_off(m, w, TC_N * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
+  };
 
-    for (int st = s_begin; st < s_end; ++st, ++it) {
-      const int buf = it & 1;
-      const int k0 = st * TC_K;
-      const bool group_first = (st & 1) == 0, group_last = (st & 1) == 1;
-      // the MMAs that last read this buffer (two stages ago) must be done;
-      // thread 0 waits and the outcome is shared, so every thread decides alike
-      if (it >= 2) {
-        if (tid == 0) s_ok = tc_wait(&bars[buf], ((it - 2) >> 1) & 1) ? 1 : 0;
-        __syncthreads();
-        if (!s_ok) {
-          ok = false;
-          break;
-        }
-      }
-      unsigned char* A = sA + buf * NA * TC_A_BYTES;
-      unsigned char* Bt = sB + buf * TC_B_BYTES;
-      // ---- A: this thread's row, 64 k (exact codes, no scale)
+  // scales: the row's scale of a group is loaded (plain load, into a
+  // register) when the loader issues the group's first stage, parked in a
+  // shared ring four stages later, and used when the group's sums are read
+  // (the second stage of the next group, or the end of the work item)
+  __shared__ __half s_scale[4][NA][TC_M];
+  __half pend[2][NA];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int g = 0; g < NA; ++g) pend[i][g] = __float2half(0.f);
+
+  // prologue: weights (independent of the previous kernel) before the
+  // dependency wait, activations after it; one commit group per stage
+  l_item();
+  int pro_work[TC_AHEAD], pro_st[TC_AHEAD];
+#pragma unroll
+  for (int i = 0; i < TC_AHEAD; ++i) {
+    pro_work[i] = l_work;
+    pro_st[i] = l_st;
+    load_a(i);
+    if (INT4 && half == 0 && l_work < nwork && (l_st & 1) == 0) {
 #pragma unroll
       for (int g = 0; g < NA; ++g) {
-        unsigned char* Ag = A + g * TC_A_BYTES;
-        if (INT4) {
-          uint4 q0 = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u), q1 = q0;  // code 0
-          if (row_ok) {
-            q0 = ldg_stream(qrow[g] + k0 / 8);
-            q1 = ldg_stream(qrow[g] + k0 / 8 + 4);
-          }
-          const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const __half v = l_ok ? l_s[g][l_st >> 1] : __float2half(0.f);
+        if (i == 0) s_scale[0][g][row_l] = v;
+        if (i == 2) pend[0][g] = v;
+        if (i == 4) pend[1][g] = v;
+      }
+    }
+    l_next();
+  }
+  pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
 #pragma unroll
-          for (int w = 0; w < 8; ++w) *reinterpret_cast<uint4*>(Ag + tc_off(tid, w, TC_M * 32)) = codes_word(wv[w]);
-        } else {
+  for (int i = 0; i < TC_AHEAD; ++i) {
+    if (pro_work[i] < nwork) load_b(i, pro_st[i]);
+    cp_async_commit();
+  }
+
+  // ---- compute ---------------------------------------------------------------
+  float acc[NA][16];
 #pragma unroll
-          for (int w = 0; w < 8; ++w)
-            *reinterpret_cast<uint4*>(Ag + tc_off(tid, w, TC_M * 32)) =
-                row_ok ? ldg_stream(wrow16 + k0 + 8 * w) : make_uint4(0, 0, 0, 0);
+  for (int g = 0; g < NA; ++g)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+
+  // add tensor-memory group buffer `grp` (this thread's row, 16 columns) times the scales
+  auto tm_read = [&](uint32_t grp, int sslot) {
+    // tcgen05.ld is warp-collective: the warp goes on only if every lane saw the barrier
+    if (!__all_sync(0xffffffffu, tc_wait(&gbars[grp & 1], (grp >> 1) & 1))) {
+      s_fail = 1;
+      return;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+    for (int g = 0; g < NA; ++g) {
+      uint32_t r[16];
+      const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * TC_N) +
+                             (uint32_t)(g * TC_N + half * 16);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          : "r"(taddr));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const float sc = INT4 ? __half2float(s_scale[sslot][g][row_l]) : 1.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[g][j] = fmaf(__uint_as_float(r[j]), sc, acc[g][j]);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  };
+
+  // per-item epilogue: split-K partials and ticket, then the outputs
+  auto epilogue = [&](int work) {
+    const int tile = work / ks, split = work % ks;
+    const int row = tile * TC_M + row_l;
+    bool finish = true;
+    if (ks > 1) {
+      float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * TC_N * TC_M);
+#pragma unroll
+      for (int g = 0; g < NA; ++g)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) wsp[(g * TC_N + half * 16 + j) * TC_M + row_l] = acc[g][j];
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
+      __syncthreads();
+      finish = s_last;
+      if (finish) {
+        __threadfence();
+#pragma unroll
+        for (int g = 0; g < NA; ++g)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+        for (int sp = 0; sp < ks; ++sp) {
+          const float* wp = a.ws + ((size_t)tile * ks + sp) * (size_t)(NA * TC_N * TC_M);
+#pragma unroll
+          for (int g = 0; g < NA; ++g)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[g][j] += __ldcg(&wp[(g * TC_N + half * 16 + j) * TC_M + row_l]);
+        }
+        if (tid == 0) a.counters[tile] = 0u;  // ready for the next call
+      }
+    }
+    if (!finish || row >= N) return;
+    if (a.y32 != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = half * 16 + j;
+        if (m < M) a.y32[(size_t)m * a.ldy + row] = acc[0][j];
+      }
+    } else if (SILU) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = half * 16 + j;
+        if (m < M) {
+          const float g = __half2float(__float2half_rn(acc[0][j]));
+          const float u = __half2float(__float2half_rn(acc[NA - 1][j]));
+          a.y[(size_t)m * a.ldy + row] = __float2half_rn(g / (1.0f + expf(-g)) * u);
         }
       }
-      // ---- B: 32 activation rows x 64 k (two 8-wide chunks per thread)
+    } else {
+      float bv = 0.f;
+      if (INT4) {
+        int r = row, si = 0;
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int c = tid + c2 * TC_THREADS;
-        const int m = c >> 3, w = c & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (m < M) v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + k0 + 8 * w);
-        if (INT4) v = permute_k8(v);
-        *reinterpret_cast<uint4*>(Bt + tc_off(m, w, TC_N * 32)) = v;
+        for (int k = 0; k < 2; ++k)
+          if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
+        if (a.seg[si].bias) bv = __half2float(a.seg[si].bias[r]);
       }
-      float sc_cur[NA];
 #pragma unroll
-      for (int g = 0; g < NA; ++g) sc_cur[g] = (INT4 && esrow[g]) ? __half2float(esrow[g][st >> 1]) : 1.0f;
-      // generic-proxy writes -> visible to the tensor core (async proxy)
+      for (int j = 0; j < 16; ++j) {
+        const int m = half * 16 + j;
+        if (m < M) {
+          float v = acc[0][j] + bv;
+          if (a.residual) v += __half2float(a.residual[(size_t)m * a.ldy + row]);
+          a.y[(size_t)m * a.ldy + row] = __float2half_rn(v);
+        }
+      }
+    }
+  };
+
+  int c_work = blockIdx.x, c_st = 0, c_end = 0, c_begin = 0;
+  auto c_item = [&]() {
+    const int split = c_work % ks;
+    c_begin = c_st = split * ps;
+    c_end = min(nst, c_begin + ps);
+  };
+  if (c_work < nwork) c_item();
+  // c: stages computed by this CTA.  Work items have an even number of
+  // stages and start at even c, so c & 1 tells a group's first (0) and
+  // second (1) stage, and a work item always ends on an odd c.
+  uint32_t c = 0, gc = 0, issued = 0;
+  bool run = c_work < nwork;
+  while (run) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      // (1) the MMAs of stage c-2 are done (A buffer u and ring slot
+      //     (c + TC_AHEAD) % TC_S are free); this thread's loads of stage c landed
+      if (c >= 2 && !tc_wait(&bars[u], ((c - 2) >> 1) & 1)) s_fail = 1;
+      cp_async_wait<TC_AHEAD - 1>();
       fence_proxy_async_smem();
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncthreads();
+      if (s_fail) {
+        run = false;
+        break;
+      }
+      // (2) scales parked; loads for stage c + TC_AHEAD
+      if (INT4 && u == 0 && half == 0) {
+        const int pi = (c >> 1) & 1;
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
+          s_scale[((c + 2) >> 1) & 3][g][row_l] = pend[pi][g];
+          if (l_work < nwork) pend[pi][g] = l_ok ? l_s[g][l_st >> 1] : __float2half(0.f);
+        }
+      }
+      const int ls = (int)((c + TC_AHEAD) % TC_S);
+      if (l_work < nwork) {
+        load_a(ls);
+        load_b(ls, l_st);
+      }
+      cp_async_commit();
+      l_next();
+      // (3) exact codes of stage c into A buffer u
+      unsigned char* slot = ring + (c % TC_S) * SH::SLOT;
+      if (INT4) {
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(slot + (g * TC_M + row_l) * 32 + half * 16);
+          unsigned char* A = afp + (u * NA + g) * TC_A_BYTES;
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(A + tc_off(row_l, 4 * half + i, TC_M * 32)) = codes_word(wv[i]);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncthreads();
+      // (4) MMAs (one thread), committed to the stage barrier and, at a
+      //     group's second stage, to the group barrier
       if (tid == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t gbase = tmem + (gc & 1) * (NA * TC_N);
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
+          const unsigned char* A = INT4 ? afp + (u * NA + g) * TC_A_BYTES : slot;
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
-            const uint64_t ad = tc_desc(smem_u32(A + g * TC_A_BYTES + kk * TC_M * 32));
-            const uint64_t bd = tc_desc(smem_u32(Bt + kk * TC_N * 32));
-            const uint32_t accum = (!group_first || kk > 0) ? 1u : 0u;
+            const uint64_t ad = tc_desc(smem_u32(A + kk * TC_M * 32));
+            const uint64_t bd = tc_desc(smem_u32(slot + SH::A_RAW + kk * TC_N * 32));
+            const uint32_t accum = (u == 1 || kk > 0) ? 1u : 0u;
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
@@ -323,104 +458,45 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
           }
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                         smem_u32(&bars[buf]))
+                         smem_u32(&bars[u]))
                      : "memory");
-        if (group_last)
+        if (u == 1)
           asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                            smem_u32(&gbars[gc & 1]))
                        : "memory");
       }
       ++issued;
-      if (group_first) {
-        // the previous group of this work item (if any) is read now, while
-        // the tensor core works on this group
-        if (st > s_begin && !read_group(gc - 1, sc_prev)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int g = 0; g < NA; ++g) sc_prev[g] = sc_cur[g];
+      // (5) the previous group of this item (its last MMAs were issued two
+      //     stages ago), while the tensor core works on this one
+      if (u == 1) {
+        if (c_st - 1 != c_begin) tm_read(gc - 1, (int)(((c - 3) >> 1) & 3));
+        ++gc;
       }
-      if (group_last) ++gc;
+      ++c;
+      if (u == 0) ++c_st;
     }
-    if (!ok) break;
-    // ---- the last group of this work item
-    const bool has_stages = s_end > s_begin;  // a split past the end of K contributes zeros
-    if (has_stages && !read_group(gc - 1, sc_prev)) {
-      ok = false;
-      break;
-    }
-    const int orow = erow;  // output row (feature n) of this thread
-
-    bool finish = true;
-    if (a.ksplit > 1) {
-      // split K: park the partial tile; the last split of the tile sums them
-      float* ws = a.ws + ((size_t)tile * a.ksplit + split) * (size_t)(NA * TC_N * TC_M);
+    if (!run) break;
+    // (6) end of the work item (always after a group's second stage): its
+    //     last group, then the epilogue
+    if (c_st == c_end - 1) {
+      tm_read(gc - 1, (int)(((c - 2) >> 1) & 3));
+      epilogue(c_work);
 #pragma unroll
       for (int g = 0; g < NA; ++g)
 #pragma unroll
-        for (int j = 0; j < TC_N; ++j) ws[(g * TC_N + j) * TC_M + warp * 32 + lane] = acc[g][j];
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(a.ksplit - 1));
-      __syncthreads();
-      finish = s_last;
-      if (finish) {
-        __threadfence();
-#pragma unroll
-        for (int g = 0; g < NA; ++g)
-#pragma unroll
-          for (int j = 0; j < TC_N; ++j) acc[g][j] = 0.f;
-        for (int sp = 0; sp < a.ksplit; ++sp) {
-          const float* wp = a.ws + ((size_t)tile * a.ksplit + sp) * (size_t)(NA * TC_N * TC_M);
-#pragma unroll
-          for (int g = 0; g < NA; ++g)
-#pragma unroll
-            for (int j = 0; j < TC_N; ++j) acc[g][j] += __ldcg(&wp[(g * TC_N + j) * TC_M + warp * 32 + lane]);
-        }
-        if (tid == 0) a.counters[tile] = 0u;  // ready for the next call
-      }
+        for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+      c_work += gridDim.x;
+      if (c_work >= nwork) break;
+      c_item();
+    } else {
+      ++c_st;
     }
-    if (finish && orow < N && a.y32 != nullptr) {
-#pragma unroll
-      for (int j = 0; j < TC_N; ++j)
-        if (j < M) a.y32[(size_t)j * a.ldy + orow] = acc[0][j];
-    } else if (finish && orow < N) {
-      if (SILU) {
-#pragma unroll
-        for (int j = 0; j < TC_N; ++j) {
-          if (j < M) {
-            const float g = __half2float(__float2half_rn(acc[0][j]));
-            const float u = __half2float(__float2half_rn(acc[NA - 1][j]));
-            a.y[(size_t)j * a.ldy + orow] = __float2half_rn(g / (1.0f + expf(-g)) * u);
-          }
-        }
-      } else {
-        float bv = 0.f;
-        if (INT4) {
-          int r = orow, si = 0;
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-          if (a.seg[si].bias) bv = __half2float(a.seg[si].bias[r]);
-        }
-#pragma unroll
-        for (int j = 0; j < TC_N; ++j) {
-          if (j < M) {
-            float v = acc[0][j] + bv;
-            if (a.residual) v += __half2float(a.residual[(size_t)j * a.ldy + orow]);
-            a.y[(size_t)j * a.ldy + orow] = __float2half_rn(v);
-          }
-        }
-      }
-    }
-    __syncthreads();  // accumulator reads done before the next work item's MMAs
   }
-  if (!ok && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
-  // before freeing tensor memory, no MMA of this CTA may still be in flight
-  if (!ok && tid == 0) {
-    for (uint32_t x = (issued >= 2 ? issued - 2 : 0); x < issued; ++x) (void)tc_wait(&bars[x & 1], (x >> 1) & 1);
-  }
+  cp_async_wait<0>();
+  if (s_fail && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
+  // before freeing tensor memory no MMA of this CTA may still be in flight:
+  // the last stage's commit covers all earlier ones
+  if (issued > 0 && tid == 0) (void)tc_wait(&bars[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
@@ -439,43 +515,75 @@ void tc_workspace_layout(TcArgs& a, void* ws) {
   a.ws = reinterpret_cast<float*>(static_cast<char*>(ws) + TC_TICKET_BYTES);
 }
 
-int tc_default_ksplit(int N, int K) {
-  const int ntiles = (N + TC_M - 1) / TC_M;
-  const int nst = K / TC_K;
-  int ks = 1;
-  if ((size_t)ntiles * 4 > TC_TICKET_BYTES) return 1;  // more tiles than tickets: no split
-  while (ntiles * ks * 2 <= num_sms() * 2 && nst / (ks * 2) >= 8) ks *= 2;
-  return ks;
+template <bool INT4, bool SILU>
+static int tc_ctas_per_sm() {
+  static int cached = 0;
+  if (cached == 0) {
+    auto kern = gemm_tc_kernel<INT4, SILU>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcShape<INT4, SILU>::SMEM);
+    int bps = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS, TcShape<INT4, SILU>::SMEM) !=
+            cudaSuccess ||
+        bps < 1)
+      bps = 1;
+    cached = std::min(bps, 4);  // tensor memory: at most 4 x 128 columns per SM
+  }
+  return cached;
 }
 
-int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s) {
+static int tc_slots(bool int4, bool silu) {
+  const int per = !int4 ? tc_ctas_per_sm<false, false>()
+                        : (silu ? tc_ctas_per_sm<true, true>() : tc_ctas_per_sm<true, false>());
+  return per * num_sms();
+}
+
+// Split of K: the split length (even number of stages, so splits start on a
+// scale group) that minimises waves x (stages per item + a per-item
+// overhead of ~4 stages) over the CTAs that fit on the GPU.
+void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split) {
+  const int ntiles = (N + TC_M - 1) / TC_M;
+  const int nst = K / TC_K;
+  const int slots = tc_slots(int4, silu);
+  int best_ps = nst, best_ks = 1;
+  long best = -1;
+  for (int p = nst; p >= 2; p -= 2) {
+    const int k = (nst + p - 1) / p;
+    if (k > 1 && (!allow_split || (size_t)ntiles * 4 > TC_TICKET_BYTES)) continue;
+    const long items = (long)ntiles * k;
+    const long waves = (items + slots - 1) / slots;
+    const long cost = waves * (p + 4);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_ps = p;
+      best_ks = k;
+    }
+  }
+  *ksplit = best_ks;
+  *per_split = best_ps;
+}
+
+int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
+  TcArgs a = a_in;
   if (a.M < 1 || a.M > TC_N) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, TC_N);
   // stages pair into 128-wide groups (the int4 scale group), dense weights too
   if (a.K % 128 != 0) return set_error(W4A16_ERR_SHAPE, "gemm_tc: K=%d not a multiple of 128", a.K);
   if (a.ksplit < 1) return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: ksplit < 1");
-  const int na = silu ? 2 : 1;
-  const size_t smem = (size_t)2 * na * TC_A_BYTES + (size_t)2 * TC_B_BYTES + 1024;
+  const int nst = a.K / TC_K;
+  if (a.per_split <= 0) a.per_split = (nst + a.ksplit - 1) / a.ksplit;
+  if (a.per_split % 2 != 0 || (long)a.per_split * (a.ksplit - 1) >= nst || (long)a.per_split * a.ksplit < nst)
+    return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: split of %d stages x %d does not tile %d stages", a.per_split,
+                     a.ksplit, nst);
   const int ntiles = (a.N + TC_M - 1) / TC_M;
   const int nwork = ntiles * a.ksplit;
-  static bool configured = false;  // all three instantiations share one function-pointer type
-  if (!configured) {
-    cudaFuncSetAttribute(gemm_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-    cudaFuncSetAttribute(gemm_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-    cudaFuncSetAttribute(gemm_tc_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-    configured = true;
-  }
-  auto pick = [&](auto kern) -> int {
-    int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS, smem) != cudaSuccess || bps < 1) bps = 1;
-    bps = std::min(bps, 4);  // tensor memory: <= 4 x 128 columns per SM of 512
-    const int blocks = std::max(1, std::min(nwork, bps * num_sms()));
+  auto go = [&](auto kern, size_t smem, int per_sm) -> int {
+    const int blocks = std::max(1, std::min(nwork, per_sm * num_sms()));
     cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(TC_THREADS), smem, s, a);
     if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemm_tc launch: %s", cudaGetErrorString(e));
     return W4A16_OK;
   };
-  if (!int4) return pick(gemm_tc_kernel<false, false>);
-  if (silu) return pick(gemm_tc_kernel<true, true>);
-  return pick(gemm_tc_kernel<true, false>);
+  if (!int4) return go(gemm_tc_kernel<false, false>, TcShape<false, false>::SMEM, tc_ctas_per_sm<false, false>());
+  if (silu) return go(gemm_tc_kernel<true, true>, TcShape<true, true>::SMEM, tc_ctas_per_sm<true, true>());
+  return go(gemm_tc_kernel<true, false>, TcShape<true, false>::SMEM, tc_ctas_per_sm<true, false>());
 }
 
 }  // namespace w4
@@ -529,12 +637,14 @@ using namespace w4;
 
 extern "C" size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu) {
   (void)M;
-  if (K < 64 || N < 1) return 0;
-  return tc_workspace_bytes(N, tc_default_ksplit(N, K), silu != 0);
+  if (K < 128 || N < 1) return 0;
+  int ks = 1, ps = 0;
+  tc_plan(N, K, true, silu != 0, true, &ks, &ps);
+  return tc_workspace_bytes(N, ks, silu != 0);
 }
 
 static int tc_common_checks(const uint16_t* x, int M, int K, int N, const uint16_t* y, const void* ws, size_t wsb,
-                            int N_silu, int* ksplit) {
+                            int N_silu, int* ksplit, int* per_split) {
   W4_CHECK_ARG(x && y, "w4a16_gemm: null x or y");
   W4_CHECK_ARG(M >= 1 && K >= 1 && N >= 1, "w4a16_gemm: sizes must be positive");
   W4_CHECK_SHAPE(M <= 32, "w4a16_gemm: M=%d > 32", M);
@@ -542,11 +652,9 @@ static int tc_common_checks(const uint16_t* x, int M, int K, int N, const uint16
   W4_CHECK_ALIGN(x, 128, "x");
   W4_CHECK_ALIGN(y, 128, "y");
   W4_CHECK_ALIGN(ws, 128, "workspace");
-  *ksplit = 1;
-  if (ws != nullptr) {
-    const int ks = tc_default_ksplit(N, K);
-    if (wsb >= tc_workspace_bytes(N, ks, N_silu != 0)) *ksplit = ks;
-  }
+  tc_plan(N, K, true, N_silu != 0, ws != nullptr, ksplit, per_split);
+  if (*ksplit > 1 && wsb < tc_workspace_bytes(N, *ksplit, N_silu != 0))
+    tc_plan(N, K, true, N_silu != 0, false, ksplit, per_split);
   return W4A16_OK;
 }
 
@@ -557,8 +665,8 @@ static void tc_ws(TcArgs& a, void* ws) {
 extern "C" int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweight, const uint16_t* scales, int N,
                           const uint16_t* bias, const uint16_t* residual, uint16_t* y, void* workspace,
                           size_t workspace_bytes, w4a16_stream_t stream) {
-  int ks = 1;
-  int rc = tc_common_checks(x, M, K, N, y, workspace, workspace_bytes, 0, &ks);
+  int ks = 1, ps = 0;
+  int rc = tc_common_checks(x, M, K, N, y, workspace, workspace_bytes, 0, &ks, &ps);
   if (rc) return rc;
   W4_CHECK_ARG(qweight && scales, "w4a16_gemm: null weights");
   W4_CHECK_ALIGN(qweight, 128, "qweight");
@@ -576,6 +684,7 @@ extern "C" int w4a16_gemm(const uint16_t* x, int M, int K, const uint32_t* qweig
   a.N = N;
   a.ldy = N;
   a.ksplit = ks;
+  a.per_split = ps;
   tc_ws(a, workspace);
   return launch_gemm_tc(a, true, false, (cudaStream_t)stream);
 }
@@ -584,8 +693,8 @@ extern "C" int w4a16_gemm_silu_mul(const uint16_t* x, int M, int K, const uint32
                                    const uint16_t* scales_gate, const uint32_t* qweight_up, const uint16_t* scales_up,
                                    int N, uint16_t* y, void* workspace, size_t workspace_bytes,
                                    w4a16_stream_t stream) {
-  int ks = 1;
-  int rc = tc_common_checks(x, M, K, N, y, workspace, workspace_bytes, 1, &ks);
+  int ks = 1, ps = 0;
+  int rc = tc_common_checks(x, M, K, N, y, workspace, workspace_bytes, 1, &ks, &ps);
   if (rc) return rc;
   W4_CHECK_ARG(qweight_gate && scales_gate && qweight_up && scales_up, "w4a16_gemm_silu_mul: null weights");
   W4_CHECK_ALIGN(qweight_gate, 128, "qweight_gate");
@@ -603,6 +712,7 @@ extern "C" int w4a16_gemm_silu_mul(const uint16_t* x, int M, int K, const uint32
   a.N = N;
   a.ldy = N;
   a.ksplit = ks;
+  a.per_split = ps;
   tc_ws(a, workspace);
   return launch_gemm_tc(a, true, true, (cudaStream_t)stream);
 }

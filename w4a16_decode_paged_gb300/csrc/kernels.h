@@ -44,6 +44,7 @@ struct TcArgs {
   unsigned int* counters;  // split-K tickets, one per 128-row tile (zero before first use)
   int32_t* err_flag;
   int M, K, N, ldy, ksplit, tag;
+  int per_split;           // stages (64 k) per split, even; 0: ceil(stages / ksplit)
 };
 int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
 
@@ -54,7 +55,8 @@ int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
 constexpr size_t TC_TICKET_BYTES = 8192;    // one ticket per 128-row tile: up to 2048 tiles
 constexpr size_t ATT_TICKET_BYTES = 16384;  // one ticket per (sequence, kv head): up to 4096
 size_t tc_workspace_bytes(int N, int ksplit, bool silu);
-int tc_default_ksplit(int N, int K);
+// split of K (ksplit splits of per_split stages) that fills whole waves of CTAs
+void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split);
 void tc_workspace_layout(TcArgs& a, void* ws);  // sets a.counters / a.ws (a.ksplit > 1)
 int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
                        int tag);

@@ -130,7 +130,9 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   const size_t o_l32 = off; off += max_batch > GEMV_MAX_BATCH ? up256((size_t)max_batch * c.vocab * 4) : 0;
   {
     auto need = [&](int N, int K, bool silu) {
-      m->tc_ws_bytes = std::max(m->tc_ws_bytes, tc_workspace_bytes(N, tc_default_ksplit(N, K), silu));
+      int ks = 1, ps = 0;
+      tc_plan(N, K, true, silu, true, &ks, &ps);
+      m->tc_ws_bytes = std::max(m->tc_ws_bytes, tc_workspace_bytes(N, ks, silu));
     };
     need((int)nqkv, c.hidden, false);
     need(c.hidden, c.n_q_heads * D, false);
@@ -247,8 +249,9 @@ static int project(w4a16_model* m, GemvArgs g, bool silu, cudaStream_t s, int* t
   t.K = g.K;
   t.N = g.N;
   t.ldy = g.N;
-  t.ksplit = tc_default_ksplit(g.N, g.K);
-  if (tc_workspace_bytes(g.N, t.ksplit, silu) > m->tc_ws_bytes) t.ksplit = 1;
+  tc_plan(g.N, g.K, true, silu, true, &t.ksplit, &t.per_split);
+  if (t.ksplit > 1 && tc_workspace_bytes(g.N, t.ksplit, silu) > m->tc_ws_bytes)
+    tc_plan(g.N, g.K, true, silu, false, &t.ksplit, &t.per_split);
   if (t.ksplit > 1) tc_workspace_layout(t, m->tc_ws);
   t.tag = (*tag)++;
   return launch_gemm_tc(t, true, silu, s);
