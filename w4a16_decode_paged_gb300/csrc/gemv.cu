@@ -9,22 +9,22 @@
 // and the products run as mixed-precision fp16 x fp16 -> fp32 FMAs, so every
 // product is exact and every sum is fp32.
 //
-// Dequant trick, per packed word w (nibbles u0..u7, u = q + 8).  Each pair of
-// nibbles (i, i + 4) is moved into the top four mantissa bits of the two
-// halves of a half2 and OR-ed with the exponent of 1.0:
-//   ((w << 6) & 0x03C003C0) | 0x3C003C00 = half2{1 + u0/16, 1 + u4/16}
-//   ((w << 2) & 0x03C003C0) | 0x3C003C00 = half2{1 + u1/16, 1 + u5/16}
-//   ((w >> 2) & 0x03C003C0) | 0x3C003C00 = half2{1 + u2/16, 1 + u6/16}
-//   ((w >> 6) & 0x03C003C0) | 0x3C003C00 = half2{1 + u3/16, 1 + u7/16}
-// The activations are staged once per CTA in shared memory in the matching
-// order, and mixed-precision fp16 x fp16 -> fp32 FMAs (exact products) give
-// S = sum_i (1 + u_i/16) x_i over a 32-weight chunk, so that
-//   sum_i q_i x_i = 16 S - 24 sum_i x_i,
-// with 24 sum x (one fp32 per chunk, shared by every row) staged beside x.
-// Because the implicit leading 1 is only ~16/15 of the code's range, the
-// subtraction costs about two bits of the fp32 sum (the 1024 + u magic would
-// cost about ten).  That is four shifts, four LOP3 and eight FMAs per 8
-// weights, with no fp16-pipe work.
+// Dequant trick, per packed word w (nibbles u0..u7, u = q + 8).  Nibbles i
+// and i + 4 sit 16 bits apart, so one LOP3 drops a pair into the two halves
+// of a half2 whose exponent field is that of 1024:
+//   (w        & 0x000F000F) | 0x64006400 = half2{1024 + u0,    1024 + u4}
+//   (w        & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u1, 1024 + 16 u5}
+//   ((w >> 8) & 0x000F000F) | 0x64006400 = half2{1024 + u2,    1024 + u6}
+//   ((w >> 8) & 0x00F000F0) | 0x64006400 = half2{1024 + 16 u3, 1024 + 16 u7}
+// all exact.  The activations are staged once per CTA in shared memory in the
+// matching order, and mixed-precision fp16 x fp16 -> fp32 FMAs (exact
+// products) give over a 32-weight chunk
+//   A = sum_{i even} x_i (1024 + u_i),  B = sum_{i odd} x_i (1024 + 16 u_i),
+//   sum_i q_i x_i = A + B/16 - (1032 sum_{i even} x_i + 72 sum_{i odd} x_i),
+// with the bracket (one fp32 per chunk, shared by every row) staged beside x.
+// The 1024 offset costs about ten bits of the fp32 sums, which leaves the
+// chunk sums some 100x more accurate than an fp16 output needs.  That is one
+// shift, four LOP3 and eight FMAs per eight weights, with no fp16-pipe work.
 //
 // Work split: LPR lanes cooperate on one weight row (LPR = 16 when K/32 is a
 // multiple of 16, else 8 or 4); a warp covers 32/LPR rows at a time; each
@@ -47,7 +47,7 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 
 // Stage x (optionally RMS-normalised, rounded to fp16) in shared memory in
 // nibble order: for 32-weight chunk j and word w of the chunk, one uint4 holds
-// {x0, x4}, {x1/16, x5/16}, {x2, x6}, {x3/16, x7/16} of k = 32 j + 8 w + i.
+// {x0, x4}, {x1, x5}, {x2, x6}, {x3, x7} of k = 32 j + 8 w + i.
 // Layout [MT][4][K/32] uint4, so consecutive chunks are consecutive 16 bytes.
 template <int MT>
 __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, float* cs, float (*red)[MT],
@@ -82,7 +82,7 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
   for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
     const int m = idx / NCH, j = idx - m * NCH;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
-    float csum = 0.f;
+    float csum_even = 0.f, csum_odd = 0.f;
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       uint4 raw = src[wi];
@@ -102,35 +102,47 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
       o.w = pack_h2(h[3], h[7]);
       xs[(size_t)(m * 4 + wi) * NCH + j] = o;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) csum += __half2float(h[i]);
+      for (int i = 0; i < 8; i += 2) {
+        csum_even += __half2float(h[i]);
+        csum_odd += __half2float(h[i + 1]);
+      }
     }
-    cs[(size_t)m * NCH + j] = 24.0f * csum;
+    cs[(size_t)m * NCH + j] = 1032.0f * csum_even + 72.0f * csum_odd;
   }
   __syncthreads();
 }
 
-constexpr uint32_t NIB_MASK = 0x03C003C0u;  // top four mantissa bits of both halves
-constexpr uint32_t ONE_H2 = 0x3C003C00u;    // half2{1, 1}
+constexpr uint32_t MAGIC_H2 = 0x64006400u;  // half2{1024, 1024}
 
-// S += sum over the 8 nibbles of word w of (1 + u/16) * x, x in staged order.
-// The shifts are written as integer multiplies (w << k == w * 2^k, and
-// w >> k == high word of w * 2^(32-k)) so they issue on the FMA pipe and
-// leave the half-rate ALU pipe to the four LOP3s.
-__device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t mul) {
+// w >> 8 as the high word of an integer multiply, so it issues on the FMA
+// pipe and leaves the half-rate ALU pipe to the LOP3s.
+__device__ __forceinline__ uint32_t shr8_fma(uint32_t w) {
   uint32_t d;
-  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(mul));
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(1u << 24));
   return d;
 }
-__device__ __forceinline__ uint32_t shr_fma(uint32_t w, uint32_t mul) {
-  uint32_t d;
-  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(mul));
-  return d;
+
+// Partial sums over the 8 nibbles of word w (nibble i = element i, offset
+// binary u = q + 8) against x in staged order {x0,x4},{x1,x5},{x2,x6},{x3,x7}:
+// a nibble ORed into the low mantissa bits of fp16 1024 is exactly 1024 + u,
+// one placed four bits higher 1024 + 16 u, so
+//   p[0] + p[1] = sum over i even of x_i (1024 + u_i),
+//   p[2] + p[3] = sum over i odd  of x_i (1024 + 16 u_i),
+// each product exact (fma.rn.f32.f16), and
+//   sum_i x_i q_i = p0 + p1 + (p2 + p3) / 16 - 1032 sum_even x - 72 sum_odd x.
+// One shift and four LOP3s per eight weights.
+__device__ __forceinline__ void word_dot(float (&p)[4], uint32_t w, const uint4 xv) {
+  const uint32_t w8 = shr8_fma(w);
+  fma2_f16_f32_split(p[0], p[1], and_or(w, 0x000F000Fu, MAGIC_H2), xv.x);
+  fma2_f16_f32_split(p[2], p[3], and_or(w, 0x00F000F0u, MAGIC_H2), xv.y);
+  fma2_f16_f32_split(p[0], p[1], and_or(w8, 0x000F000Fu, MAGIC_H2), xv.z);
+  fma2_f16_f32_split(p[2], p[3], and_or(w8, 0x00F000F0u, MAGIC_H2), xv.w);
 }
-__device__ __forceinline__ void word_dot(float& p0, float& p1, uint32_t w, const uint4 xv) {
-  fma2_f16_f32_split(p0, p1, and_or(shl_fma(w, 64u), NIB_MASK, ONE_H2), xv.x);          // w << 6
-  fma2_f16_f32_split(p0, p1, and_or(shl_fma(w, 4u), NIB_MASK, ONE_H2), xv.y);           // w << 2
-  fma2_f16_f32_split(p0, p1, and_or(shr_fma(w, 1u << 30), NIB_MASK, ONE_H2), xv.z);     // w >> 2
-  fma2_f16_f32_split(p0, p1, and_or(shr_fma(w, 1u << 26), NIB_MASK, ONE_H2), xv.w);     // w >> 6
+
+// sum over a 32-weight chunk of x q from its partial sums and the chunk's
+// activation constant c = 1032 sum_even x + 72 sum_odd x
+__device__ __forceinline__ float chunk_sum(const float (&p)[4], float c) {
+  return fmaf(0.0625f, p[2] + p[3], (p[0] + p[1]) - c);
 }
 
 template <int LPR, int MT, bool SILU>
@@ -243,10 +255,10 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               if (m < M) {
-                float p0 = 0.f, p1 = 0.f;
+                float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int wi = 0; wi < 4; ++wi) word_dot(p0, p1, wv[wi], xs[(size_t)(m * 4 + wi) * NCH + j]);
-                acc[m] = fmaf(fmaf(16.0f, p0 + p1, -cs[(size_t)m * NCH + j]), s, acc[m]);
+                for (int wi = 0; wi < 4; ++wi) word_dot(p, wv[wi], xs[(size_t)(m * 4 + wi) * NCH + j]);
+                acc[m] = fmaf(chunk_sum(p, cs[(size_t)m * NCH + j]), s, acc[m]);
               }
             }
           }
@@ -425,19 +437,19 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
         for (int m = 0; m < MT; ++m) {
           if (m < M) {
             const uint4* xc = xs + (size_t)(m * 4) * NCH + j;
-            float p[R][2];
+            float p[R][4];
 #pragma unroll
-            for (int r = 0; r < R; ++r) p[r][0] = p[r][1] = 0.f;
+            for (int r = 0; r < R; ++r) p[r][0] = p[r][1] = p[r][2] = p[r][3] = 0.f;
 #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
               const uint4 xv = xc[wi * NCH];
 #pragma unroll
-              for (int r = 0; r < R; ++r) word_dot(p[r][0], p[r][1], (&wv[r].x)[wi], xv);
+              for (int r = 0; r < R; ++r) word_dot(p[r], (&wv[r].x)[wi], xv);
             }
             const float c = cs[(size_t)m * NCH + j];
 #pragma unroll
             for (int r = 0; r < R; ++r)
-              acc[r][m] = fmaf(fmaf(16.0f, p[r][0] + p[r][1], -c), __half2float(sc[slot][r * U + u]), acc[r][m]);
+              acc[r][m] = fmaf(chunk_sum(p[r], c), __half2float(sc[slot][r * U + u]), acc[r][m]);
           }
         }
       }
