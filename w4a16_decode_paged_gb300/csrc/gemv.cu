@@ -337,15 +337,18 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   constexpr int NIT = NCH / LPR;                 // chunks per lane when one half-warp covers K
   constexpr int NIT_L = (NIT + KS - 1) / KS;     // this lane's share (upper bound)
   constexpr int NB = (NIT_L + U - 1) / U;        // batches per task
+  constexpr int NBT = (NB % 2 == 0) ? NB : 2 * NB;  // batches per unrolled round (even: ring slot = batch & 1)
+  constexpr int TPR = NBT / NB;                  // tasks per round
   constexpr int WROW = K / 8;
   constexpr int SROW = K / 128;
   constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
   constexpr int NT = GEMV_WPB * 32;
   static_assert(RU % R == 0, "R must divide RU");
   static_assert(!(SILU && KS == 2), "SiLU pairs gate and up across half-warps");
+  static_assert(NCH % LPR == 0, "every lane takes the same number of chunks");
   extern __shared__ uint4 smem[];
   uint4* xs = smem;                                          // [MT][4][NCH]
-  uint4* ring = smem + MT * 4 * NCH;                         // [2][RU][NT]
+  uint4* ring = smem + MT * 4 * NCH;                         // [2][RU][NT], each lane its own column
   float* cs = reinterpret_cast<float*>(ring + 2 * RU * NT);  // [MT][NCH]
   __shared__ float red[GEMV_WPB][MT];
   __shared__ float rscale[MT];
@@ -355,6 +358,10 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   const int M = a.M;
   const int ntask = (a.N + RPT - 1) / RPT;
   const int nwarps = gridDim.x * GEMV_WPB;
+  // chunk index of (batch b, word u) for this lane: j = jl + JSTEP * (b * U + u)
+  constexpr int JSTEP = LPR * KS;
+  const int jl = lr + (KS == 2 ? LPR * hw : 0);
+  auto it_ok = [&](int i) { return KS == 2 ? (2 * i + hw < NIT) : (i < NIT); };
   W4_TRACE_SCOPE(a.tag);
 
   // first output row of this lane's rows for task t, and the weight-row base
@@ -377,66 +384,74 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
       bp = a.seg[si].bias ? a.seg[si].bias + r : nullptr;
     }
   };
-  auto chunk_it = [&](int i) { return KS == 2 ? 2 * i + hw : i; };
 
-  // issue cursor (one batch ahead of the compute cursor)
-  int i_task = blockIdx.x * GEMV_WPB + warp, i_b = 0, i_out0;
-  const uint32_t* i_q;
-  const __half *i_s, *i_bias;
-  if (i_task < ntask) rows_of(i_task, i_out0, i_q, i_s, i_bias);
+  // issue side: the task whose batches are being loaded
+  int i_task = blockIdx.x * GEMV_WPB + warp, i_out0;
+  const uint32_t* i_q = nullptr;
+  const __half *i_s = nullptr, *i_bias;
+  if (i_task < ntask) {
+    rows_of(i_task, i_out0, i_q, i_s, i_bias);
+    i_q += 4 * jl;         // this lane's first 16-byte word
+    i_s += jl >> 2;
+  }
   __half sc[2][RU];
-  auto issue = [&](const int slot) {
+  // batch b of the issue task into ring slot `slot` (b, slot compile-time once unrolled)
+  auto issue = [&](const int slot, const int b) {
     if (i_task < ntask) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int it = chunk_it(i_b * U + u);
-        if (it < NIT) {
-          const int j = lr + LPR * it;
+        const int i = b * U + u;
+        if (i < NIT_L && it_ok(i)) {
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            cp_async16(&ring[(slot * RU + r * U + u) * NT + tid], i_q + r * WROW + 4 * j);
-            sc[slot][r * U + u] = i_s[r * SROW + (j >> 2)];
+            cp_async16(&ring[(slot * RU + r * U + u) * NT + tid], i_q + r * WROW + 4 * JSTEP * i);
+            sc[slot][r * U + u] = i_s[r * SROW + (JSTEP * i) / 4];
           }
         }
-      }
-      if (++i_b == NB) {
-        i_b = 0;
-        i_task += nwarps;
-        if (i_task < ntask) rows_of(i_task, i_out0, i_q, i_s, i_bias);
       }
     }
     cp_async_commit();
   };
+  auto next_issue_task = [&]() {
+    i_task += nwarps;
+    if (i_task < ntask) {
+      rows_of(i_task, i_out0, i_q, i_s, i_bias);
+      i_q += 4 * jl;
+      i_s += jl >> 2;
+    }
+  };
 
-  issue(0);  // weights do not depend on the previous kernel
+  issue(0, 0);  // weights do not depend on the previous kernel
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
   stage_activations<MT>(a, xs, cs, red, rscale);
 
-  // compute cursor
-  int c_task = blockIdx.x * GEMV_WPB + warp, c_b = 0, c_out0 = 0;
+  // compute side
+  int c_task = blockIdx.x * GEMV_WPB + warp, c_out0 = 0;
   const uint32_t* c_q;
   const __half *c_s, *c_bias = nullptr;
   if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
+  const uint4* xl = xs + jl;                               // this lane's chunk column of x
+  const float* csl = cs + jl;
   float acc[R][MT];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
 
-  auto compute = [&](const int slot) {
+  auto compute = [&](const int slot, const int b) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int it = chunk_it(c_b * U + u);
-      if (it < NIT) {
-        const int j = lr + LPR * it;
+      const int i = b * U + u;
+      if (i < NIT_L && it_ok(i)) {
+        const int jo = JSTEP * i;  // compile-time chunk offset
         uint4 wv[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) wv[r] = ring[(slot * RU + r * U + u) * NT + tid];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           if (m < M) {
-            const uint4* xc = xs + (size_t)(m * 4) * NCH + j;
+            const uint4* xc = xl + (size_t)(m * 4) * NCH + jo;
             float p[R][4];
 #pragma unroll
             for (int r = 0; r < R; ++r) p[r][0] = p[r][1] = p[r][2] = p[r][3] = 0.f;
@@ -446,7 +461,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
 #pragma unroll
               for (int r = 0; r < R; ++r) word_dot(p[r], (&wv[r].x)[wi], xv);
             }
-            const float c = cs[(size_t)m * NCH + j];
+            const float c = csl[(size_t)m * NCH + jo];
 #pragma unroll
             for (int r = 0; r < R; ++r)
               acc[r][m] = fmaf(chunk_sum(p[r], c), __half2float(sc[slot][r * U + u]), acc[r][m]);
@@ -454,8 +469,9 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
         }
       }
     }
-    if (++c_b < NB) return;
-    // task complete: reduce over the half-warp (and across half-warps for KS = 2), write
+  };
+  // task complete: reduce over the half-warp (and across half-warps for KS = 2), write
+  auto finish = [&]() {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -497,23 +513,27 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-    c_b = 0;
     c_task += nwarps;
     if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
   };
 
+  // rounds of NBT batches (TPR tasks); the issue side runs one batch ahead
   while (c_task < ntask) {
 #pragma unroll
-    for (int slot = 0; slot < 2; ++slot) {
-      issue(slot ^ 1);
-      cp_async_wait<1>();  // this lane's batch in `slot` has landed
-      compute(slot);
-      if (c_task >= ntask) break;
+    for (int qq = 0; qq < NBT; ++qq) {
+      const int b = qq % NB, bn = (qq + 1) % NB;
+      if (bn == 0) next_issue_task();
+      issue((qq + 1) & 1, bn);
+      cp_async_wait<1>();  // this lane's batch in slot qq & 1 has landed
+      compute(qq & 1, b);
+      if (b == NB - 1) {
+        finish();
+        if (c_task >= ntask) break;
+      }
     }
   }
   cp_async_wait<0>();
 }
-
 template <int NCH, int R, int KS, int MT, bool SILU, int RU>
 static int launch_fast(const GemvArgs& a, cudaStream_t s) {
   auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU>;
