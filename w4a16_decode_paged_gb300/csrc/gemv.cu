@@ -559,7 +559,7 @@ template <int MT, bool SILU>
 static int dispatch_fast(const GemvArgs& a, cudaStream_t s, bool* used) {
   *used = true;
   if (SILU) {
-    if (a.K == 3584) return launch_fast<112, 2, 1, MT, true, 8>(a, s);
+    if (a.K == 3584) return launch_fast<112, 2, 1, MT, true, 4>(a, s);
   } else {
     if (a.K == 3584) return launch_fast<112, 1, 1, MT, false, 8>(a, s);
     if (a.K == 18944) return launch_fast<592, 1, 2, MT, false, 4>(a, s);
