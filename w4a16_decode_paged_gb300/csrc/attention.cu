@@ -10,16 +10,22 @@
 // it is the unit of one 1-D bulk (TMA) copy into shared memory.
 //
 // One CTA handles (sequence b, kv head, partition p) for all G = Hq/Hkv query
-// heads that share the kv head (7:1 GQA in the article).  Its four warps take
+// heads that share the kv head (7:1 GQA in the article).  Its eight warps take
 // the partition's pages round-robin; each warp owns a private ring of
-// ATT_STAGES (K, V) page slots filled by 1-D bulk copies on an mbarrier, so
-// no warp waits on another inside the page loop.  Per page a warp computes
-// the 16 x G scores with packed fp32 FMAs (each K element is converted once
-// and used for all G heads), an fp32 online softmax (exp2 with the scale
-// folded into q), and the P.V update.  The warps' states are merged in shared
-// memory; with several partitions the merged (max, sum, weighted V) partials
-// go to the workspace and the last CTA of the (b, kv head) group to finish
-// (an atomic ticket, no spin) merges them and writes the output.
+// ATT_STAGES (K, V) page slots, filled row by row with 1-D bulk copies on an
+// mbarrier (the 32 lanes copy the 16 K and 16 V rows of a page at once), so no
+// warp waits on another inside the page loop.  Because the G query heads read
+// the same K and V, a page is a small dense contraction and runs on the tensor
+// cores with warp-level mma.sync (m16n8k16, fp16 in, fp32 accumulate): the
+// scores S[head][token] = Q K^T with the heads as the M rows (padded to 16),
+// an fp32 online softmax in registers (exp2, scale folded in), and O += P V
+// with the probabilities rounded to fp16 as the A operand (the score
+// accumulator layout is the A-fragment layout) and V read with ldmatrix.trans.
+// The warps' states are merged in shared memory; partitions are merged through
+// distributed shared memory when they fit one thread-block cluster, else their
+// (max, sum, weighted V) partials go to the workspace and the last CTA of the
+// (b, kv head) group to finish (an atomic ticket, no spin) merges them and
+// writes the output.
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -40,10 +46,15 @@ constexpr int ATT_PAGE = 16;
 constexpr int ATT_NW = 8;          // warps per CTA
 constexpr int ATT_MAX_CLUSTER = 8; // partitions merged through distributed shared memory
 constexpr int ATT_STAGES = 2;      // page slots per warp
-constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice
-constexpr uint32_t ATT_SLICE_BYTES = ATT_SLICE * 2;  // 4096
-constexpr size_t ATT_RING_BYTES = (size_t)ATT_NW * ATT_STAGES * 2 * ATT_SLICE_BYTES;
-constexpr size_t ATT_SMEM = ATT_RING_BYTES + ATT_NW * ATT_STAGES * 8 + ATT_NW * 8 * 16 * 4 + ATT_NW * 8 * 4;
+constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice in the pool
+constexpr uint32_t ATT_ROW_BYTES = ATT_D * 2;  // 256: one token's k (or v) of one kv head
+// In shared memory a slice's rows are 272 bytes apart (16 bytes of padding),
+// so the eight rows of an 8x8 ldmatrix tile fall on eight different bank
+// groups.
+constexpr int ATT_PITCH = ATT_D + 8;                   // halves per row in shared memory
+constexpr int ATT_SSLICE = ATT_PAGE * ATT_PITCH;       // halves per slice in shared memory
+constexpr size_t ATT_RING_BYTES = (size_t)ATT_NW * ATT_STAGES * 2 * ATT_SSLICE * 2;
+constexpr size_t ATT_SMEM = ATT_RING_BYTES + ATT_NW * ATT_STAGES * 8;
 constexpr unsigned long long ATT_TIMEOUT_NS = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -67,13 +78,21 @@ __device__ __forceinline__ float2 h2f2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
+// d += A (16 x 16, fp16, rows 8-15 zero) x B (16 x 8, fp16), fp32 accumulate.
+// a0: A[g][2t..2t+1], a2: A[g][8+2t..8+2t+1]; b0, b1: B[2t..2t+1][g], B[8+2t..][g].
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
 template <int G, bool FUSE>
 __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smraw[];
   __half* ring = reinterpret_cast<__half*>(smraw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + ATT_RING_BYTES);
-  float* sbuf = reinterpret_cast<float*>(bars + ATT_NW * ATT_STAGES);  // [NW][8][16]
-  float* corr = sbuf + ATT_NW * 8 * 16;                               // [NW][8]
   __shared__ __align__(16) float s_q[G][ATT_D];   // this group's q (rotated in the fused variant)
   __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
   __shared__ __align__(16) __half s_vnew[ATT_D];
@@ -107,7 +126,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   // this warp's pages: i = warp, warp + NW, ...
   const int my_pages = npages > warp ? (npages - warp + ATT_NW - 1) / ATT_NW : 0;
   uint64_t* mybar = bars + warp * ATT_STAGES;
-  __half* myring = ring + (size_t)warp * ATT_STAGES * 2 * ATT_SLICE;
+  __half* myring = ring + (size_t)warp * ATT_STAGES * 2 * ATT_SSLICE;
 
   auto page_load = [&](int li) -> int {  // li: index into this warp's page list
     const int gi = pg0 + warp + li * ATT_NW;
@@ -118,23 +137,25 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   // for all of them); page_of() broadcasts it.  Must be called warp-wide.
   const int pg_lane = lane < my_pages ? page_load(lane) : -1;
   auto page_of = [&](int li) -> int { return li < 32 ? __shfl_sync(0xffffffffu, pg_lane, li) : page_load(li); };
-  auto issue = [&](int li, int pg) {  // lane 0 only
+  // page li of this warp into its ring slot: lane 0 arms the mbarrier with
+  // the page's bytes, then lanes 0-15 copy K rows 0-15 and lanes 16-31 V rows
+  // 0-15 (256 bytes each) to the padded rows.  Must be called warp-wide.
+  auto issue = [&](int li, int pg) {
     uint64_t* bar = &mybar[li % ATT_STAGES];
-    __half* dst = myring + (size_t)(li % ATT_STAGES) * 2 * ATT_SLICE;
+    __half* dst = myring + (size_t)(li % ATT_STAGES) * 2 * ATT_SSLICE;
     if (pg >= 0) {
-      const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
-      mbar_arrive_expect_tx(bar, 2 * ATT_SLICE_BYTES);
-      bulk_g2s(dst, a.k_pool + off, ATT_SLICE_BYTES, bar);
-      bulk_g2s(dst + ATT_SLICE, a.v_pool + off, ATT_SLICE_BYTES, bar);
-    } else {
+      if (lane == 0) mbar_arrive_expect_tx(bar, 2 * ATT_PAGE * ATT_ROW_BYTES);
+      __syncwarp();
+      const int row = lane & (ATT_PAGE - 1);
+      const size_t off = (((size_t)pg * a.Hkv + kvh) * ATT_PAGE + row) * ATT_D;
+      const __half* src = (lane < ATT_PAGE ? a.k_pool : a.v_pool) + off;
+      bulk_g2s(dst + (lane >= ATT_PAGE ? ATT_SSLICE : 0) + row * ATT_PITCH, src, ATT_ROW_BYTES, bar);
+    } else if (lane == 0) {
       mbar_arrive(bar);  // nothing to copy; complete the phase
       if (a.err_flag) atomicOr(a.err_flag, 1);
     }
   };
-  for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) {
-    const int pg = page_of(li);
-    if (lane == 0) issue(li, pg);
-  }
+  for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) issue(li, page_of(li));
   if (FUSE) {
     pdl_wait_then_trigger();
     W4_TRACE_WAITED();
@@ -196,20 +217,34 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
 
   W4_TRACE_MARK(0);
-  // q for this lane's dims: lane = (tq, ds); dims [16 ds, 16 ds + 16)
-  const int tq = lane >> 3, ds = lane & 7;
-  float2 qr[G][8];
+  // ---- tensor-core fragments (mma.sync m16n8k16): lane = (g, t) ------------
+  // A rows are the query heads (rows >= G and the upper 8 rows are zero),
+  // B columns are tokens (scores) or dims (P.V).  This lane holds rows g of
+  // every accumulator, columns 2t, 2t+1.
+  const int g = lane >> 2, t4 = lane & 3;
+  const bool head_ok = g < G;
+  uint32_t qa[8][2];  // q of head g, dims 16s + 2t4 + {0,1} and 16s + 8 + 2t4 + {0,1}, fp16
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int st = 0; st < 8; ++st) {
+    if (head_ok) {
+      const float* qrow = s_q[head_ok ? g : 0] + 16 * st + 2 * t4;
+      const __half2 lo = __floats2half2_rn(qrow[0], qrow[1]);
+      const __half2 hi = __floats2half2_rn(qrow[8], qrow[9]);
+      qa[st][0] = *reinterpret_cast<const uint32_t*>(&lo);
+      qa[st][1] = *reinterpret_cast<const uint32_t*>(&hi);
+    } else {
+      qa[st][0] = qa[st][1] = 0u;
+    }
+  }
+  float m_run = -INFINITY, l_run = 0.f;  // head g's running max (log2 domain) and sum
+  float o[16][4];                        // P.V accumulators, n-block nb = dims 8nb..8nb+7
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      qr[h][j] = make_float2(s_q[h][16 * ds + 2 * j] * a.scale_log2, s_q[h][16 * ds + 2 * j + 1] * a.scale_log2);
-  float m_run = -INFINITY, l_run = 0.f;  // lane h < G holds head h's state
-  float2 o[G][2];                       // dims [4 lane, 4 lane + 4)
-#pragma unroll
-  for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = make_float2(0.f, 0.f);
-  float* ws = sbuf + warp * 8 * 16;
-  float* wcorr = corr + warp * 8;
+  for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  // ldmatrix row addresses (bytes within a slice): lane l feeds row l % 8 of
+  // tile l / 8
+  const int lt = lane >> 3, lr8 = lane & 7;
+  const uint32_t k_off = (uint32_t)((((lt >> 1) * 8 + lr8) * ATT_PITCH + (lt & 1) * 8) * 2);  // tokens x dims 16s+..
+  const uint32_t v_off = (uint32_t)((((lt & 1) * 8 + lr8) * ATT_PITCH + (lt >> 1) * 8) * 2);  // tokens x dims 8nb+..
 
   int consumed = 0;
   for (int li = 0; li < my_pages; ++li) {
@@ -220,8 +255,8 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       break;
     }
     consumed = li + 1;
-    __half* Ks = myring + (size_t)stage * 2 * ATT_SLICE;
-    __half* Vs = Ks + ATT_SLICE;
+    __half* Ks = myring + (size_t)stage * 2 * ATT_SSLICE;
+    __half* Vs = Ks + ATT_SSLICE;
     const int gi = warp + li * ATT_NW;  // page index within the partition
     const int tok0 = (pg0 + gi) * ATT_PAGE;
     const bool page_ok = page_of(li) >= 0;
@@ -229,111 +264,68 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     if (FUSE && page_ok && pos >= tok0 && pos < tok0 + ATT_PAGE) {
       // the page was fetched before the append: patch the new token's row
       const int slot = pos - tok0;
-      *reinterpret_cast<uint2*>(Ks + slot * ATT_D + 4 * lane) = *reinterpret_cast<const uint2*>(s_knew + 4 * lane);
-      *reinterpret_cast<uint2*>(Vs + slot * ATT_D + 4 * lane) = *reinterpret_cast<const uint2*>(s_vnew + 4 * lane);
+      *reinterpret_cast<uint2*>(Ks + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_knew + 4 * lane);
+      *reinterpret_cast<uint2*>(Vs + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_vnew + 4 * lane);
       __syncwarp();
     }
-
-    // ---- scores: 4 rounds of 4 tokens; lane (tq, ds) -------------------
+    if (nv > 0) {
+      // ---- scores S[head][token], tokens 0-7 (n-block 0) and 8-15 (1) -------
+      float sc[2][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int t = tq + 4 * r;
-      const uint4* krow = reinterpret_cast<const uint4*>(Ks + t * ATT_D + 16 * ds);
-      // bank-conflict-free order: upper half of the lanes reads its second 16 B first
-      const int first = (ds >> 2) & 1;
-      uint4 ka = krow[first], kb = krow[first ^ 1];
-      uint4 k0 = first ? kb : ka, k1 = first ? ka : kb;
-      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-      float2 kf[8];
+      for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+      const uint32_t kbase = smem_u32(Ks) + k_off;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) kf[j] = h2f2(kw[j]);
-      float v[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) v[h] = 0.f;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc = ffma2(qr[h][j], kf[j], acc);
-        v[h] = acc.x + acc.y;
+      for (int st = 0; st < 8; ++st) {
+        uint32_t b0, b1, b2, b3;  // (tokens 0-7: dims lo, hi), (tokens 8-15: dims lo, hi)
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                     : "r"(kbase + st * 32));
+        mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
+        mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
       }
-      // transpose-reduce over the 8 ds lanes: lane ds ends with head ds's sum
-      float v4[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool up = ds & 4;
-        float send = up ? v[j] : v[j + 4];
-        float keep = up ? v[j + 4] : v[j];
-        v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-      }
-      float v2[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const bool up = ds & 2;
-        float send = up ? v4[j] : v4[j + 2];
-        float keep = up ? v4[j + 2] : v4[j];
-        v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-      }
-      {
-        const bool up = ds & 1;
-        float send = up ? v2[0] : v2[1];
-        float keep = up ? v2[1] : v2[0];
-        float tot = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-        if (ds < G) ws[ds * 16 + t] = tot;
-      }
-    }
-    __syncwarp();
-
-    // ---- online softmax: lane h < G owns head h -----------------------
-    if (lane < G) {
-      float sv[16];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        sv[t] = (t < nv) ? ws[lane * 16 + t] : -INFINITY;
-        mx = fmaxf(mx, sv[t]);
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float c = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-      float sum = 0.f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float pv = (sv[t] == -INFINITY) ? 0.f : exp2f(sv[t] - m_new);
-        ws[lane * 16 + t] = pv;
-        sum += pv;
-      }
+      // ---- online softmax over this page (row g; four lanes share a row) ----
+      float s00 = sc[0][0] * a.scale_log2, s01 = sc[0][1] * a.scale_log2;
+      float s10 = sc[1][0] * a.scale_log2, s11 = sc[1][1] * a.scale_log2;
+      if (2 * t4 >= nv) s00 = -INFINITY;
+      if (2 * t4 + 1 >= nv) s01 = -INFINITY;
+      if (8 + 2 * t4 >= nv) s10 = -INFINITY;
+      if (8 + 2 * t4 + 1 >= nv) s11 = -INFINITY;
+      float mx = fmaxf(fmaxf(s00, s01), fmaxf(s10, s11));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);  // finite: token 0 of the page is valid
+      const float c = exp2f(m_run - m_new);  // 0 while m_run is -inf
+      const float p00 = exp2f(s00 - m_new), p01 = exp2f(s01 - m_new);
+      const float p10 = exp2f(s10 - m_new), p11 = exp2f(s11 - m_new);
+      float sum = (p00 + p01) + (p10 + p11);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       l_run = l_run * c + sum;
       m_run = m_new;
-      wcorr[lane] = c;
-    }
-    __syncwarp();
-
-    // ---- P.V: lane owns dims [4 lane, 4 lane + 4) ---------------------
+      const __half2 pa = __floats2half2_rn(p00, p01), pb = __floats2half2_rn(p10, p11);
+      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
+      // ---- O = O * c + P V ----------------------------------------------------
+      const uint32_t vbase = smem_u32(Vs) + v_off;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float c = wcorr[h];
-      o[h][0] = make_float2(o[h][0].x * c, o[h][0].y * c);
-      o[h][1] = make_float2(o[h][1].x * c, o[h][1].y * c);
-    }
-    for (int t = 0; t < nv; ++t) {
-      const uint2 vv = *reinterpret_cast<const uint2*>(Vs + t * ATT_D + 4 * lane);
-      const float2 v0 = h2f2(vv.x), v1 = h2f2(vv.y);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pv = ws[h * 16 + t];
-        const float2 p2 = make_float2(pv, pv);
-        o[h][0] = ffma2(p2, v0, o[h][0]);
-        o[h][1] = ffma2(p2, v1, o[h][1]);
+      for (int nb = 0; nb < 16; nb += 2) {
+        uint32_t b0, b1, b2, b3;  // (dims 8nb: tokens 0-7, 8-15), (dims 8nb+8: tokens 0-7, 8-15)
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                     : "r"(vbase + nb * 16));
+        o[nb][0] *= c;
+        o[nb][1] *= c;
+        o[nb + 1][0] *= c;
+        o[nb + 1][1] *= c;
+        mma_16816(o[nb], a0, a2, b0, b1);
+        mma_16816(o[nb + 1], a0, a2, b2, b3);
       }
     }
     __syncwarp();
     // refill this stage with the page ATT_STAGES ahead
     if (li + ATT_STAGES < my_pages) {
       const int pg = page_of(li + ATT_STAGES);
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(li + ATT_STAGES, pg);
-      }
+      fence_proxy_async_smem();
+      issue(li + ATT_STAGES, pg);
     }
   }
   // Every issued copy has been consumed unless a wait timed out; in that case
@@ -350,17 +342,14 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   // ---- merge the warps' states in shared memory (ring reused) ------------
   float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
   float* mml = mo + ATT_NW * 8 * ATT_D;                 // [NW][8][2]
+  if (head_ok) {
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float* dst = mo + (warp * 8 + h) * ATT_D + 4 * lane;
-    dst[0] = o[h][0].x;
-    dst[1] = o[h][0].y;
-    dst[2] = o[h][1].x;
-    dst[3] = o[h][1].y;
-  }
-  if (lane < G) {
-    mml[(warp * 8 + lane) * 2 + 0] = m_run;
-    mml[(warp * 8 + lane) * 2 + 1] = l_run;
+    for (int nb = 0; nb < 16; ++nb)
+      *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
+    if (t4 == 0) {
+      mml[(warp * 8 + g) * 2 + 0] = m_run;
+      mml[(warp * 8 + g) * 2 + 1] = l_run;
+    }
   }
   __syncthreads();
 
