@@ -12,9 +12,9 @@
 // One CTA handles (sequence b, kv head, partition p) for all G = Hq/Hkv query
 // heads that share the kv head (7:1 GQA in the article).  Its eight warps take
 // the partition's pages round-robin; each warp owns a private ring of
-// ATT_STAGES (K, V) page slots, filled row by row with 1-D bulk copies on an
-// mbarrier (the 32 lanes copy the 16 K and 16 V rows of a page at once), so no
-// warp waits on another inside the page loop.  Because the G query heads read
+// 2 or 3 (K, V) page slots, filled with 16-byte cp.async copies (the 32 lanes
+// move 512 contiguous bytes per instruction into padded rows), so no warp
+// waits on another inside the page loop.  Because the G query heads read
 // the same K and V, a page is a small dense contraction and runs on the tensor
 // cores with warp-level mma.sync (m16n8k16, fp16 in, fp32 accumulate): the
 // scores S[head][token] = Q K^T with the heads as the M rows (padded to 16),
@@ -43,9 +43,12 @@ __device__ unsigned int g_trace_n = 0;
 
 constexpr int ATT_D = 128;
 constexpr int ATT_PAGE = 16;
-constexpr int ATT_NW = 8;          // warps per CTA
+constexpr int ATT_NW = 8;          // warps per CTA (small grids); large grids use 4 so that
+                                   // three CTAs share an SM
 constexpr int ATT_MAX_CLUSTER = 8; // partitions merged through distributed shared memory
-constexpr int ATT_STAGES = 2;      // page slots per warp
+constexpr int ATT_STAGES = 2;      // page slots per warp (CTA per partition)
+constexpr int ATT_STAGES_WP = 3;   // page slots per warp (warp per partition: deeper, the
+                                   // warp streams a whole partition alone)
 constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice in the pool
 constexpr uint32_t ATT_ROW_BYTES = ATT_D * 2;  // 256: one token's k (or v) of one kv head
 // In shared memory a slice's rows are 272 bytes apart (16 bytes of padding),
@@ -53,8 +56,9 @@ constexpr uint32_t ATT_ROW_BYTES = ATT_D * 2;  // 256: one token's k (or v) of o
 // groups.
 constexpr int ATT_PITCH = ATT_D + 8;                   // halves per row in shared memory
 constexpr int ATT_SSLICE = ATT_PAGE * ATT_PITCH;       // halves per slice in shared memory
-constexpr size_t ATT_RING_BYTES = (size_t)ATT_NW * ATT_STAGES * 2 * ATT_SSLICE * 2;
-constexpr size_t ATT_SMEM = ATT_RING_BYTES + ATT_NW * ATT_STAGES * 8;
+constexpr int att_stages(bool wp) { return wp ? ATT_STAGES_WP : ATT_STAGES; }
+constexpr size_t att_ring_bytes(int nw, int st) { return (size_t)nw * st * 2 * ATT_SSLICE * 2; }
+constexpr size_t att_smem(int nw, int st) { return att_ring_bytes(nw, st); }
 constexpr unsigned long long ATT_TIMEOUT_NS = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -88,11 +92,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
-template <int G, bool FUSE>
-__global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
+template <int G, bool FUSE, int NW, bool WP>
+__global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int NPAR = NW * 32 / ATT_D;  // threads per output dim in the merges
+  constexpr int ST = att_stages(WP);      // page slots per warp
   extern __shared__ __align__(128) unsigned char smraw[];
   __half* ring = reinterpret_cast<__half*>(smraw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + ATT_RING_BYTES);
   __shared__ __align__(16) float s_q[G][ATT_D];   // this group's q (rotated in the fused variant)
   __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
   __shared__ __align__(16) __half s_vnew[ATT_D];
@@ -100,12 +105,12 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.z, kvh = blockIdx.y, p = blockIdx.x;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  // WP: each warp owns partition p (its pages, its own partial); else the
+  // CTA owns partition p and its warps share the pages round-robin
+  const int p = WP ? blockIdx.x * NW + warp : blockIdx.x;
   W4_TRACE_SCOPE(a.tag);
 
-  if (tid < ATT_NW * ATT_STAGES) mbar_init(&bars[tid], 1);
-  fence_mbar_init();
-  __syncthreads();
   // The fused variant writes the only KV slot that changes in this step
   // itself, and the lengths were written at the start of the step, so it
   // may fetch pages before its predecessor (the q|k|v GEMV) finishes.  The
@@ -115,21 +120,27 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     W4_TRACE_WAITED();
   }
 
+  // plain variant: this group's q (G x 128 fp16, one 16-byte word per
+  // thread) is requested first, so its latency overlaps the page-table reads
+  uint4 q_word = make_uint4(0u, 0u, 0u, 0u);
+  if (!FUSE && tid < G * ATT_D / 8)
+    q_word = __ldcg(reinterpret_cast<const uint4*>(a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D) + tid);
   const int L = __ldcg(&a.context_lens[b]);
   const int t_begin = p * a.part_tokens;
   const int t_end = min(L, t_begin + a.part_tokens);
   const int npages = t_end > t_begin ? (t_end - t_begin + ATT_PAGE - 1) / ATT_PAGE : 0;
   const int pg0 = t_begin / ATT_PAGE;
+  // tokens of this CTA (decides which CTA appends the new token)
+  const int cta_t0 = WP ? blockIdx.x * NW * a.part_tokens : t_begin;
+  const int cta_t1 = WP ? min(L, cta_t0 + NW * a.part_tokens) : t_end;
   const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
-  bool timed_out = false;
 
   // this warp's pages: i = warp, warp + NW, ...
-  const int my_pages = npages > warp ? (npages - warp + ATT_NW - 1) / ATT_NW : 0;
-  uint64_t* mybar = bars + warp * ATT_STAGES;
-  __half* myring = ring + (size_t)warp * ATT_STAGES * 2 * ATT_SSLICE;
+  const int my_pages = WP ? npages : (npages > warp ? (npages - warp + NW - 1) / NW : 0);
+  __half* myring = ring + (size_t)warp * ST * 2 * ATT_SSLICE;
 
   auto page_load = [&](int li) -> int {  // li: index into this warp's page list
-    const int gi = pg0 + warp + li * ATT_NW;
+    const int gi = pg0 + (WP ? li : warp + li * NW);
     const int pg = (gi < a.max_blocks) ? __ldcg(&bt[gi]) : -1;
     return (pg >= 0 && pg < a.num_pages) ? pg : -1;
   };
@@ -137,25 +148,27 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   // for all of them); page_of() broadcasts it.  Must be called warp-wide.
   const int pg_lane = lane < my_pages ? page_load(lane) : -1;
   auto page_of = [&](int li) -> int { return li < 32 ? __shfl_sync(0xffffffffu, pg_lane, li) : page_load(li); };
-  // page li of this warp into its ring slot: lane 0 arms the mbarrier with
-  // the page's bytes, then lanes 0-15 copy K rows 0-15 and lanes 16-31 V rows
-  // 0-15 (256 bytes each) to the padded rows.  Must be called warp-wide.
+  // page li of this warp into its ring slot with 16-byte cp.async copies:
+  // the 32 lanes move 512 contiguous bytes per instruction, 16 instructions
+  // per page (K rows 0-15, then V rows 0-15), into the padded rows.  One
+  // commit group per page (empty for a missing page).  Warp-wide.
   auto issue = [&](int li, int pg) {
-    uint64_t* bar = &mybar[li % ATT_STAGES];
-    __half* dst = myring + (size_t)(li % ATT_STAGES) * 2 * ATT_SSLICE;
+    __half* dst = myring + (size_t)(li % ST) * 2 * ATT_SSLICE;
     if (pg >= 0) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, 2 * ATT_PAGE * ATT_ROW_BYTES);
-      __syncwarp();
-      const int row = lane & (ATT_PAGE - 1);
-      const size_t off = (((size_t)pg * a.Hkv + kvh) * ATT_PAGE + row) * ATT_D;
-      const __half* src = (lane < ATT_PAGE ? a.k_pool : a.v_pool) + off;
-      bulk_g2s(dst + (lane >= ATT_PAGE ? ATT_SSLICE : 0) + row * ATT_PITCH, src, ATT_ROW_BYTES, bar);
-    } else if (lane == 0) {
-      mbar_arrive(bar);  // nothing to copy; complete the phase
-      if (a.err_flag) atomicOr(a.err_flag, 1);
+      const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = lane + 32 * i;  // 16-byte chunk of the page: [K|V][row][16]
+        const int which = c >> 8, row = (c >> 4) & 15, col = c & 15;
+        cp_async16(dst + which * ATT_SSLICE + row * ATT_PITCH + col * 8,
+                   (which ? a.v_pool : a.k_pool) + off + row * ATT_D + col * 8);
+      }
+    } else if (lane == 0 && li < my_pages && a.err_flag) {
+      atomicOr(a.err_flag, 1);
     }
+    cp_async_commit();
   };
-  for (int li = 0; li < ATT_STAGES && li < my_pages; ++li) issue(li, page_of(li));
+  for (int li = 0; li < ST; ++li) issue(li, li < my_pages ? page_of(li) : -1);
   if (FUSE) {
     pdl_wait_then_trigger();
     W4_TRACE_WAITED();
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
     }
     for (int d = tid; d < ATT_D; d += blockDim.x) s_vnew[d] = s_raw[(G + 1) * ATT_D + d];
     __syncthreads();
-    if (pos >= t_begin && pos < t_end) {  // this partition holds the new token: append it
+    if (pos >= cta_t0 && pos < cta_t1) {  // this CTA holds the new token: append it
       const int blk = pos / ATT_PAGE;
       const int pg = (blk < a.max_blocks) ? __ldcg(&bt[blk]) : -1;
       if (pg >= 0 && pg < a.num_pages) {
@@ -211,8 +224,12 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       }
     }
   } else {
-    for (int idx = tid; idx < G * ATT_D; idx += blockDim.x)
-      s_q[idx / ATT_D][idx % ATT_D] = __half2float(qb[(idx / ATT_D) * ATT_D + idx % ATT_D]);
+    static_assert(G * ATT_D / 8 <= 4 * 32, "one q word per thread of the smallest CTA");
+    if (tid < G * ATT_D / 8) {
+      const __half* hq = reinterpret_cast<const __half*>(&q_word);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s_q[(tid * 8 + i) / ATT_D][(tid * 8 + i) % ATT_D] = __half2float(hq[i]);
+    }
     __syncthreads();
   }
 
@@ -246,18 +263,13 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   const uint32_t k_off = (uint32_t)((((lt >> 1) * 8 + lr8) * ATT_PITCH + (lt & 1) * 8) * 2);  // tokens x dims 16s+..
   const uint32_t v_off = (uint32_t)((((lt & 1) * 8 + lr8) * ATT_PITCH + (lt >> 1) * 8) * 2);  // tokens x dims 8nb+..
 
-  int consumed = 0;
   for (int li = 0; li < my_pages; ++li) {
-    const int stage = li % ATT_STAGES;
-    const uint32_t parity = (li / ATT_STAGES) & 1;
-    if (!wait_phase(&mybar[stage], parity)) {
-      timed_out = true;
-      break;
-    }
-    consumed = li + 1;
+    const int stage = li % ST;
+    cp_async_wait<ST - 1>();  // this lane's copies of page li landed
+    __syncwarp();             // ... and every other lane's
     __half* Ks = myring + (size_t)stage * 2 * ATT_SSLICE;
     __half* Vs = Ks + ATT_SSLICE;
-    const int gi = warp + li * ATT_NW;  // page index within the partition
+    const int gi = WP ? li : warp + li * NW;  // page index within the partition
     const int tok0 = (pg0 + gi) * ATT_PAGE;
     const bool page_ok = page_of(li) >= 0;
     const int nv = page_ok ? min(ATT_PAGE, t_end - tok0) : 0;
@@ -321,129 +333,131 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
       }
     }
     __syncwarp();
-    // refill this stage with the page ATT_STAGES ahead
-    if (li + ATT_STAGES < my_pages) {
-      const int pg = page_of(li + ATT_STAGES);
-      fence_proxy_async_smem();
-      issue(li + ATT_STAGES, pg);
-    }
+    // refill this stage with the page ST ahead (an empty group past the end)
+    issue(li + ST, li + ST < my_pages ? page_of(li + ST) : -1);
   }
-  // Every issued copy has been consumed unless a wait timed out; in that case
-  // flag it and wait (bounded) for the copies still in flight before the
-  // ring memory is reused.
-  if (timed_out && lane == 0) {
-    if (a.err_flag) atomicOr(a.err_flag, 2);
-    for (int x = consumed; x < my_pages && x < consumed + ATT_STAGES; ++x)
-      (void)wait_phase(&mybar[x % ATT_STAGES], (x / ATT_STAGES) & 1);
-  }
+  cp_async_wait<0>();
   __syncthreads();  // all warps done with their rings
   W4_TRACE_MARK(1);
 
-  // ---- merge the warps' states in shared memory (ring reused) ------------
-  float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
-  float* mml = mo + ATT_NW * 8 * ATT_D;                 // [NW][8][2]
-  if (head_ok) {
-#pragma unroll
-    for (int nb = 0; nb < 16; ++nb)
-      *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
-    if (t4 == 0) {
-      mml[(warp * 8 + g) * 2 + 0] = m_run;
-      mml[(warp * 8 + g) * 2 + 1] = l_run;
-    }
-  }
-  __syncthreads();
-
-  const int d = tid & (ATT_D - 1);  // dim of this thread; two threads per dim split the heads
-  const int hpar = tid / ATT_D;     // 0 or 1
+  const int d = tid & (ATT_D - 1);  // dim of this thread; NPAR threads per dim split the heads
+  const int hpar = tid / ATT_D;     // 0 .. NPAR-1: heads h with h % NPAR == hpar
   const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
-  // this CTA's (partition's) merged state: cp_o[h][d] = sum e^(m - M) o,
-  // cp_ml[h] = (M, sum e^(m - M) l)
-  float* cp_o = mml + ATT_NW * 8 * 2;  // [G][128]
-  float* cp_ml = cp_o + G * ATT_D;     // [G][2]
+  if (WP) {
+    // this warp's partition state straight to the workspace (no merge)
+    if (head_ok && p < a.P && t_begin < L) {
+      float* dst = a.ws_o + ((qh0 + g) * a.P + p) * ATT_D + 2 * t4;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    if ((h & 1) != hpar) continue;
-    float M = -INFINITY;
-    for (int w = 0; w < ATT_NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < ATT_NW; ++w) {
-        const float mw = mml[(w * 8 + h) * 2];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        acc += mo[(w * 8 + h) * ATT_D + d] * f;
-        den += mml[(w * 8 + h) * 2 + 1] * f;
+      for (int nb = 0; nb < 16; ++nb) *reinterpret_cast<float2*>(dst + 8 * nb) = make_float2(o[nb][0], o[nb][1]);
+      if (t4 == 0) {
+        a.ws_ml[((qh0 + g) * a.P + p) * 2 + 0] = m_run;
+        a.ws_ml[((qh0 + g) * a.P + p) * 2 + 1] = l_run;
       }
     }
-    if (a.P == 1) {
-      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
-    } else {
-      cp_o[h * ATT_D + d] = acc;
-      if (d == 0) {
-        cp_ml[h * 2] = M;
-        cp_ml[h * 2 + 1] = den;
+  } else {
+    // ---- merge the warps' states in shared memory (ring reused) ------------
+    float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
+    float* mml = mo + NW * 8 * ATT_D;                     // [NW][8][2]
+    if (head_ok) {
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb)
+        *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
+      if (t4 == 0) {
+        mml[(warp * 8 + g) * 2 + 0] = m_run;
+        mml[(warp * 8 + g) * 2 + 1] = l_run;
       }
     }
-  }
-  if (a.P == 1) return;
-  W4_TRACE_MARK(2);
+    __syncthreads();
 
-  if (a.use_cluster) {
-    // All partitions of this (sequence, kv head) form one thread-block
-    // cluster: merge them through distributed shared memory.  CTA rank r
-    // produces the heads h with h % P == r.
-    cluster_sync();
-    const int P = a.P;
-    const unsigned int rank = cluster_ctarank();
-    for (int h = (int)rank + hpar * P; h < G; h += 2 * P) {
-      // all remote values first (independent loads), then the merge
-      float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
+    // this CTA's (partition's) merged state: cp_o[h][d] = sum e^(m - M) o,
+    // cp_ml[h] = (M, sum e^(m - M) l)
+    float* cp_o = mml + NW * 8 * 2;  // [G][128]
+    float* cp_ml = cp_o + G * ATT_D;     // [G][2]
 #pragma unroll
-      for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
-        if (j < P) {
-          mj[j] = ld_dsmem(&cp_ml[h * 2], j);
-          lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
-          oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
-        }
-      }
+    for (int h = 0; h < G; ++h) {
+      if (h % NPAR != hpar) continue;
       float M = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
-        if (j < P) M = fmaxf(M, mj[j]);
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
       float acc = 0.f, den = 0.f;
       if (M != -INFINITY) {
+        for (int w = 0; w < NW; ++w) {
+          const float mw = mml[(w * 8 + h) * 2];
+          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+          acc += mo[(w * 8 + h) * ATT_D + d] * f;
+          den += mml[(w * 8 + h) * 2 + 1] * f;
+        }
+      }
+      if (a.P == 1) {
+        a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+      } else {
+        cp_o[h * ATT_D + d] = acc;
+        if (d == 0) {
+          cp_ml[h * 2] = M;
+          cp_ml[h * 2 + 1] = den;
+        }
+      }
+    }
+    if (a.P == 1) return;
+    W4_TRACE_MARK(2);
+
+    if (a.use_cluster) {
+      // All partitions of this (sequence, kv head) form one thread-block
+      // cluster: merge them through distributed shared memory.  CTA rank r
+      // produces the heads h with h % P == r.
+      cluster_sync();
+      const int P = a.P;
+      const unsigned int rank = cluster_ctarank();
+      for (int h = (int)rank + hpar * P; h < G; h += NPAR * P) {
+        // all remote values first (independent loads), then the merge
+        float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
 #pragma unroll
         for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
           if (j < P) {
-            const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
-            acc += oj[j] * f;
-            den += lj[j] * f;
+            mj[j] = ld_dsmem(&cp_ml[h * 2], j);
+            lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
+            oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
           }
         }
+        float M = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
+          if (j < P) M = fmaxf(M, mj[j]);
+        float acc = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
+            if (j < P) {
+              const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+              acc += oj[j] * f;
+              den += lj[j] * f;
+            }
+          }
+        }
+        a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
       }
-      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+      cluster_sync();  // keep every CTA's shared memory alive until all reads are done
+      return;
     }
-    cluster_sync();  // keep every CTA's shared memory alive until all reads are done
-    return;
-  }
 
-  // several partitions without a cluster: this partition's partial goes to
-  // the workspace, then the ticket
-  __syncthreads();
-  if (t_begin < L) {
-    for (int idx = tid; idx < G * ATT_D; idx += blockDim.x) {
-      const int h = idx / ATT_D, dd = idx % ATT_D;
-      a.ws_o[((qh0 + h) * a.P + p) * ATT_D + dd] = cp_o[idx];
-    }
-    if (tid < G) {
-      a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 0] = cp_ml[tid * 2];
-      a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 1] = cp_ml[tid * 2 + 1];
+    // several partitions without a cluster: this partition's partial goes to
+    // the workspace, then the ticket
+    __syncthreads();
+    if (t_begin < L) {
+      for (int idx = tid; idx < G * ATT_D; idx += blockDim.x) {
+        const int h = idx / ATT_D, dd = idx % ATT_D;
+        a.ws_o[((qh0 + h) * a.P + p) * ATT_D + dd] = cp_o[idx];
+      }
+      if (tid < G) {
+        a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 0] = cp_ml[tid * 2];
+        a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 1] = cp_ml[tid * 2 + 1];
+      }
     }
   }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const unsigned int ticket = atomicAdd(&a.counters[(size_t)b * a.Hkv + kvh], 1u);
-    s_last = (ticket == (unsigned int)(a.P - 1));
+    s_last = (ticket == (unsigned int)(WP ? gridDim.x - 1 : a.P - 1));
   }
   __syncthreads();
   if (!s_last) return;
@@ -477,7 +491,7 @@ __global__ void __launch_bounds__(ATT_NW * 32) paged_attn_kernel(const __grid_co
   }
   __syncthreads();
 #pragma unroll 1
-  for (int h = hpar; h < G; h += 2) {
+  for (int h = hpar; h < G; h += NPAR) {
     const float* wts = cw + h * Pv;
     const float* src = a.ws_o + ((qh0 + h) * a.P) * ATT_D + d;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
@@ -508,21 +522,21 @@ void attention_workspace_layout(AttnArgs& a, void* ws, int B, int Hq, int P) {
   a.ws_ml = reinterpret_cast<float*>(w + ATT_TICKET_BYTES + up((size_t)B * Hq * P * ATT_D * 4));
 }
 
-template <int G>
-static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
+template <int G, int NW, bool WP>
+static int launch_attn_gw(const AttnArgs& a, cudaStream_t s) {
   static bool configured = false;
-  auto k0 = paged_attn_kernel<G, false>;
-  auto k1 = paged_attn_kernel<G, true>;
+  auto k0 = paged_attn_kernel<G, false, NW, WP>;
+  auto k1 = paged_attn_kernel<G, true, NW, WP>;
   if (!configured) {
-    cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
-    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM);
+    cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_smem(NW, att_stages(WP)));
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_smem(NW, att_stages(WP)));
     configured = true;
   }
-  dim3 grid(a.P, a.Hkv, a.B);
+  dim3 grid(WP ? (a.P + NW - 1) / NW : a.P, a.Hkv, a.B);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(ATT_NW * 32);
-  cfg.dynamicSmemBytes = ATT_SMEM;
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = att_smem(NW, att_stages(WP));
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -536,6 +550,17 @@ static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
   cudaError_t e = a.fuse_rope_append ? cudaLaunchKernelEx(&cfg, k1, a) : cudaLaunchKernelEx(&cfg, k0, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
+}
+
+// Many partitions (at least two per SM): every warp owns one partition and
+// writes its partial itself (4-warp CTAs, three per SM); the last CTA of a
+// (sequence, kv head) combines.  Fewer partitions: a CTA of 8 warps per
+// partition, merged in shared memory (and across a cluster).
+template <int G>
+static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
+  const long parts = (long)a.P * a.Hkv * a.B;
+  if (!a.use_cluster && parts >= 2L * num_sms()) return launch_attn_gw<G, 4, true>(a, s);
+  return launch_attn_gw<G, ATT_NW, false>(a, s);
 }
 
 int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
