@@ -340,137 +340,130 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   __syncthreads();  // all warps done with their rings
   W4_TRACE_MARK(1);
 
+  // ---- merge the warps' states in shared memory (ring reused).  In the
+  // warp-per-partition variant these are NW whole partitions, merged by the
+  // same online-softmax rule as any two partials. -----------------------------
   const int d = tid & (ATT_D - 1);  // dim of this thread; NPAR threads per dim split the heads
   const int hpar = tid / ATT_D;     // 0 .. NPAR-1: heads h with h % NPAR == hpar
   const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
-  if (WP) {
-    // this warp's partition state straight to the workspace (no merge)
-    if (head_ok && p < a.P && t_begin < L) {
-      float* dst = a.ws_o + ((qh0 + g) * a.P + p) * ATT_D + 2 * t4;
+  const int PC = gridDim.x;         // CTA partials per (sequence, kv head)
+  const int pc = blockIdx.x;
+  float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
+  float* mml = mo + NW * 8 * ATT_D;                     // [NW][8][2]
+  if (head_ok) {
 #pragma unroll
-      for (int nb = 0; nb < 16; ++nb) *reinterpret_cast<float2*>(dst + 8 * nb) = make_float2(o[nb][0], o[nb][1]);
-      if (t4 == 0) {
-        a.ws_ml[((qh0 + g) * a.P + p) * 2 + 0] = m_run;
-        a.ws_ml[((qh0 + g) * a.P + p) * 2 + 1] = l_run;
-      }
+    for (int nb = 0; nb < 16; ++nb)
+      *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
+    if (t4 == 0) {
+      mml[(warp * 8 + g) * 2 + 0] = m_run;
+      mml[(warp * 8 + g) * 2 + 1] = l_run;
     }
-  } else {
-    // ---- merge the warps' states in shared memory (ring reused) ------------
-    float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
-    float* mml = mo + NW * 8 * ATT_D;                     // [NW][8][2]
-    if (head_ok) {
-#pragma unroll
-      for (int nb = 0; nb < 16; ++nb)
-        *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
-      if (t4 == 0) {
-        mml[(warp * 8 + g) * 2 + 0] = m_run;
-        mml[(warp * 8 + g) * 2 + 1] = l_run;
-      }
-    }
-    __syncthreads();
+  }
+  __syncthreads();
 
-    // this CTA's (partition's) merged state: cp_o[h][d] = sum e^(m - M) o,
-    // cp_ml[h] = (M, sum e^(m - M) l)
-    float* cp_o = mml + NW * 8 * 2;  // [G][128]
-    float* cp_ml = cp_o + G * ATT_D;     // [G][2]
+  // this CTA's merged state: cp_o[h][d] = sum e^(m - M) o, cp_ml[h] = (M, sum e^(m - M) l)
+  float* cp_o = mml + NW * 8 * 2;  // [G][128]
+  float* cp_ml = cp_o + G * ATT_D; // [G][2]
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      if (h % NPAR != hpar) continue;
+  for (int h = 0; h < G; ++h) {
+    if (h % NPAR != hpar) continue;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < NW; ++w) {
+        const float mw = mml[(w * 8 + h) * 2];
+        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        acc += mo[(w * 8 + h) * ATT_D + d] * f;
+        den += mml[(w * 8 + h) * 2 + 1] * f;
+      }
+    }
+    if (PC == 1) {
+      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+    } else {
+      cp_o[h * ATT_D + d] = acc;
+      if (d == 0) {
+        cp_ml[h * 2] = M;
+        cp_ml[h * 2 + 1] = den;
+      }
+    }
+  }
+  if (PC == 1) return;
+  W4_TRACE_MARK(2);
+
+  if (!WP && a.use_cluster) {
+    // All partitions of this (sequence, kv head) form one thread-block
+    // cluster: merge them through distributed shared memory.  CTA rank r
+    // produces the heads h with h % P == r.
+    cluster_sync();
+    const int P = a.P;
+    const unsigned int rank = cluster_ctarank();
+    for (int h = (int)rank + hpar * P; h < G; h += NPAR * P) {
+      // all remote values first (independent loads), then the merge
+      float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
+#pragma unroll
+      for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
+        if (j < P) {
+          mj[j] = ld_dsmem(&cp_ml[h * 2], j);
+          lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
+          oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
+        }
+      }
       float M = -INFINITY;
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
+#pragma unroll
+      for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
+        if (j < P) M = fmaxf(M, mj[j]);
       float acc = 0.f, den = 0.f;
       if (M != -INFINITY) {
-        for (int w = 0; w < NW; ++w) {
-          const float mw = mml[(w * 8 + h) * 2];
-          const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-          acc += mo[(w * 8 + h) * ATT_D + d] * f;
-          den += mml[(w * 8 + h) * 2 + 1] * f;
-        }
-      }
-      if (a.P == 1) {
-        a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
-      } else {
-        cp_o[h * ATT_D + d] = acc;
-        if (d == 0) {
-          cp_ml[h * 2] = M;
-          cp_ml[h * 2 + 1] = den;
-        }
-      }
-    }
-    if (a.P == 1) return;
-    W4_TRACE_MARK(2);
-
-    if (a.use_cluster) {
-      // All partitions of this (sequence, kv head) form one thread-block
-      // cluster: merge them through distributed shared memory.  CTA rank r
-      // produces the heads h with h % P == r.
-      cluster_sync();
-      const int P = a.P;
-      const unsigned int rank = cluster_ctarank();
-      for (int h = (int)rank + hpar * P; h < G; h += NPAR * P) {
-        // all remote values first (independent loads), then the merge
-        float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
 #pragma unroll
         for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
           if (j < P) {
-            mj[j] = ld_dsmem(&cp_ml[h * 2], j);
-            lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
-            oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
+            const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+            acc += oj[j] * f;
+            den += lj[j] * f;
           }
         }
-        float M = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
-          if (j < P) M = fmaxf(M, mj[j]);
-        float acc = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
-            if (j < P) {
-              const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
-              acc += oj[j] * f;
-              den += lj[j] * f;
-            }
-          }
-        }
-        a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
       }
-      cluster_sync();  // keep every CTA's shared memory alive until all reads are done
-      return;
+      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
     }
+    cluster_sync();  // keep every CTA's shared memory alive until all reads are done
+    return;
+  }
 
-    // several partitions without a cluster: this partition's partial goes to
-    // the workspace, then the ticket
-    __syncthreads();
-    if (t_begin < L) {
-      for (int idx = tid; idx < G * ATT_D; idx += blockDim.x) {
-        const int h = idx / ATT_D, dd = idx % ATT_D;
-        a.ws_o[((qh0 + h) * a.P + p) * ATT_D + dd] = cp_o[idx];
-      }
-      if (tid < G) {
-        a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 0] = cp_ml[tid * 2];
-        a.ws_ml[((qh0 + tid) * a.P + p) * 2 + 1] = cp_ml[tid * 2 + 1];
-      }
+  // several CTA partials without a cluster: this CTA's partial goes to the
+  // workspace ([qh][PC][128]), then the ticket
+  const int cta_tokens = (WP ? NW : 1) * a.part_tokens;
+  __syncthreads();
+  if (pc * cta_tokens < L) {
+    for (int idx = tid; idx < G * ATT_D / 4; idx += blockDim.x) {
+      const int h = idx / (ATT_D / 4), d4 = idx % (ATT_D / 4);
+      *reinterpret_cast<float4*>(a.ws_o + ((qh0 + h) * PC + pc) * ATT_D + 4 * d4) =
+          *reinterpret_cast<const float4*>(cp_o + h * ATT_D + 4 * d4);
+    }
+    if (tid < G) {
+      a.ws_ml[((qh0 + tid) * PC + pc) * 2 + 0] = cp_ml[tid * 2];
+      a.ws_ml[((qh0 + tid) * PC + pc) * 2 + 1] = cp_ml[tid * 2 + 1];
     }
   }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const unsigned int ticket = atomicAdd(&a.counters[(size_t)b * a.Hkv + kvh], 1u);
-    s_last = (ticket == (unsigned int)(WP ? gridDim.x - 1 : a.P - 1));
+    s_last = (ticket == (unsigned int)(PC - 1));
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   // Combine, in parallel: (1) all (max, sum) pairs into shared memory,
-  // (2) one thread per head turns them into weights, (3) each thread (one
-  // output dim) sums the weighted partial outputs with independent loads.
-  const int Pv = L > 0 ? min(a.P, (L + a.part_tokens - 1) / a.part_tokens) : 0;
+  // (2) one thread per head turns them into weights, (3) the weighted
+  // partial outputs are summed four dims per thread (16-byte loads, all
+  // partials of a head in flight together).
+  const int Pv = L > 0 ? min(PC, (L + cta_tokens - 1) / cta_tokens) : 0;
   float* cw = reinterpret_cast<float*>(smraw);  // [G][Pv] maxima, then weights
   float* cl = cw + G * Pv;                      // [G][Pv] sums
   for (int idx = tid; idx < G * Pv; idx += blockDim.x) {
     const int h = idx / Pv, j = idx - h * Pv;
-    const size_t slot = (qh0 + h) * a.P + j;
+    const size_t slot = (qh0 + h) * PC + j;
     cw[idx] = __ldcg(&a.ws_ml[slot * 2]);
     cl[idx] = __ldcg(&a.ws_ml[slot * 2 + 1]);
   }
@@ -490,20 +483,24 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
     for (int j = 0; j < Pv; ++j) mw[j] *= inv;
   }
   __syncthreads();
-#pragma unroll 1
-  for (int h = hpar; h < G; h += NPAR) {
+  // G x 32 (head, 4-dim) outputs over the CTA's threads
+  for (int idx = tid; idx < G * (ATT_D / 4); idx += blockDim.x) {
+    const int h = idx / (ATT_D / 4), d4 = idx % (ATT_D / 4);
     const float* wts = cw + h * Pv;
-    const float* src = a.ws_o + ((qh0 + h) * a.P) * ATT_D + d;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int j = 0;
-    for (; j + 4 <= Pv; j += 4) {
-      acc0 += wts[j] * __ldcg(src + (size_t)j * ATT_D);
-      acc1 += wts[j + 1] * __ldcg(src + (size_t)(j + 1) * ATT_D);
-      acc2 += wts[j + 2] * __ldcg(src + (size_t)(j + 2) * ATT_D);
-      acc3 += wts[j + 3] * __ldcg(src + (size_t)(j + 3) * ATT_D);
+    const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((qh0 + h) * PC) * ATT_D) + d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int j = 0; j < Pv; ++j) {
+      const float4 v = __ldcg(src + (size_t)j * (ATT_D / 4));
+      const float w = wts[j];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
-    for (; j < Pv; ++j) acc0 += wts[j] * __ldcg(src + (size_t)j * ATT_D);
-    a.out[(qh0 + h) * ATT_D + d] = __float2half_rn((acc0 + acc1) + (acc2 + acc3));
+    __half2* dst = reinterpret_cast<__half2*>(a.out + (qh0 + h) * ATT_D + 4 * d4);
+    dst[0] = __floats2half2_rn(acc.x, acc.y);
+    dst[1] = __floats2half2_rn(acc.z, acc.w);
   }
   if (tid == 0) a.counters[(size_t)b * a.Hkv + kvh] = 0u;  // ready for the next call
 }
