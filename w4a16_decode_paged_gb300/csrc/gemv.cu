@@ -330,8 +330,8 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 // RU: chunks per lane per batch (R rows x U chunks).  K = 3584 uses 8 so a
 // whole row (7 chunks per lane) is in flight before the dependency wait;
 // the long-K down projection uses 4 to fit more CTAs per SM.
-template <int NCH, int R, int KS, int MT, bool SILU, int RU>
-__global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
+template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB>
+__global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
   constexpr int LPR = 16, U = RU / R;
   constexpr int K = NCH * 32;
   constexpr int NIT = NCH / LPR;                 // chunks per lane when one half-warp covers K
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   constexpr int WROW = K / 8;
   constexpr int SROW = K / 128;
   constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
-  constexpr int NT = GEMV_WPB * 32;
+  constexpr int NT = WPB * 32;
   static_assert(RU % R == 0, "R must divide RU");
   static_assert(!(SILU && KS == 2), "SiLU pairs gate and up across half-warps");
   static_assert(NCH % LPR == 0, "every lane takes the same number of chunks");
@@ -350,14 +350,14 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   uint4* xs = smem;                                          // [MT][4][NCH]
   uint4* ring = smem + MT * 4 * NCH;                         // [2][RU][NT], each lane its own column
   float* cs = reinterpret_cast<float*>(ring + 2 * RU * NT);  // [MT][NCH]
-  __shared__ float red[GEMV_WPB][MT];
+  __shared__ float red[WPB][MT];
   __shared__ float rscale[MT];
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int hw = lane >> 4, lr = lane & 15;
   const int M = a.M;
   const int ntask = (a.N + RPT - 1) / RPT;
-  const int nwarps = gridDim.x * GEMV_WPB;
+  const int nwarps = gridDim.x * WPB;
   // chunk index of (batch b, word u) for this lane: j = jl + JSTEP * (b * U + u)
   constexpr int JSTEP = LPR * KS;
   const int jl = lr + (KS == 2 ? LPR * hw : 0);
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   };
 
   // issue side: the task whose batches are being loaded
-  int i_task = blockIdx.x * GEMV_WPB + warp, i_out0;
+  int i_task = blockIdx.x * WPB + warp, i_out0;
   const uint32_t* i_q = nullptr;
   const __half *i_s = nullptr, *i_bias;
   if (i_task < ntask) {
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   stage_activations<MT>(a, xs, cs, red, rscale);
 
   // compute side
-  int c_task = blockIdx.x * GEMV_WPB + warp, c_out0 = 0;
+  int c_task = blockIdx.x * WPB + warp, c_out0 = 0;
   const uint32_t* c_q;
   const __half *c_s, *c_bias = nullptr;
   if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
@@ -534,23 +534,23 @@ __global__ void __launch_bounds__(GEMV_WPB * 32, 4) gemv_w4a16_fast(const __grid
   }
   cp_async_wait<0>();
 }
-template <int NCH, int R, int KS, int MT, bool SILU, int RU>
+template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB = GEMV_WPB>
 static int launch_fast(const GemvArgs& a, cudaStream_t s) {
-  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU>;
-  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * RU * GEMV_WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
+  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU, WPB>;
+  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * RU * WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     configured = true;
   }
   int bps = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, GEMV_WPB * 32, smem) != cudaSuccess || bps < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, WPB * 32, smem) != cudaSuccess || bps < 1)
     bps = 1;
   constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
   const int ntask = (a.N + RPT - 1) / RPT;
-  int blocks = std::min((ntask + GEMV_WPB - 1) / GEMV_WPB, bps * num_sms());
+  int blocks = std::min((ntask + WPB - 1) / WPB, bps * num_sms());
   blocks = std::max(blocks, 1);
-  cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(GEMV_WPB * 32), smem, s, a);
+  cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(WPB * 32), smem, s, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
