@@ -9,14 +9,16 @@
 // 128-row weight tile, its B operand the (up to) 32 activation rows, so
 // D[n][m] (128 lanes x 32 columns, fp32) lives in tensor memory.
 //
-// The weights are streamed once, so the kernel is a bandwidth pipe: a ring of
-// TC_S stages (64 k each) in shared memory, filled TC_AHEAD stages ahead with
-// cp.async (packed int4 rows and the activation tile, the latter directly in
-// the canonical no-swizzle K-major layout the MMA reads: core matrices of 8
-// rows x 16 bytes, K-adjacent core matrices 128 B apart, 8-row groups 256 B
-// apart).  Per stage each of 256 threads turns 32 codes of its weight row
-// into exact fp16 integers (q in [-8, 7]) in a double-buffered A tile, and
-// one thread issues four kind::f16 MMAs (K = 16) per weight matrix.
+// The weights are streamed once, so the kernel is a bandwidth pipe with
+// specialised warps that meet only at mbarriers: a producer warp fills a
+// ring of TC_S stages (64 k each) with cp.async (packed int4 rows, and the
+// activation tile directly in the canonical no-swizzle K-major layout the MMA
+// reads: core matrices of 8 rows x 16 bytes, K-adjacent core matrices 128 B
+// apart, 8-row groups 256 B apart); 256 reader threads turn the 32 codes per
+// stage of their weight row into exact fp16 integers (q in [-8, 7]) in a
+// double-buffered A tile; one thread issues four kind::f16 MMAs (K = 16) per
+// weight matrix and commits them to the barriers that free the A buffer, the
+// ring slot and, per group, the tensor-memory buffer.
 //
 // Precision: the MMAs see exact codes and exact fp16 activations (products
 // exact, fp32 sums).  Each 128-wide scale group accumulates into its own
@@ -41,7 +43,8 @@ namespace w4 {
 constexpr int TC_M = 128;      // weight rows per tile (MMA M)
 constexpr int TC_N = 32;       // batch columns (MMA N)
 constexpr int TC_K = 64;       // K per stage
-constexpr int TC_THREADS = 256;
+constexpr int TC_READERS = 256;                  // threads that expand codes and read tensor memory
+constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
 constexpr int TC_AHEAD = 6;    // stages loaded ahead of the one computed
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
@@ -130,30 +133,67 @@ __device__ __forceinline__ uint4 codes_word(uint32_t w) {
   return o;
 }
 
+// Bounded mbarrier wait that also gives up as soon as another role of the
+// CTA has given up (*fail set); a wait that runs out sets *fail.
+__device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = tc_now();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*fail) return false;
+    if (tc_now() - t0 > TC_TIMEOUT_NS) {
+      *fail = 1;
+      return false;
+    }
+  }
+}
+
+// The mbarrier gets one arrival once all of this thread's earlier cp.async
+// copies have landed (the arrival is counted in the barrier's init count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(TC_READERS) : "memory"); }
+
+// Warp roles: warp 0 copies (producer), warp 1 lane 0 issues the MMAs, warps
+// 2..9 (the readers, 256 threads) expand the int4 codes of their weight row
+// and, one stage behind the tensor core, read the group sums from tensor
+// memory and run the epilogue.  Stage s of this CTA's work uses ring slot
+// s % TC_S and A buffer s % 2; its group is s / 2 (work items have an even
+// number of stages).  The roles only meet at mbarriers:
+//   full[slot]   producer's copies of the slot landed          (32 arrivals)
+//   empty[slot]  readers done with the raw A, MMAs with the B  (256 + 1)
+//   afull[b]     readers wrote A buffer b                      (256)
+//   aempty[b]    MMAs that read A buffer b are done            (1, commit)
+//   gfull[b]     MMAs of the group in tensor-memory buffer b   (1, commit)
+//   gempty[b]    readers read tensor-memory buffer b           (256)
 template <bool INT4, bool SILU>
-__global__ void __launch_bounds__(TC_THREADS, SILU || !INT4 ? 1 : 2) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU>;
   constexpr int NA = SH::NA;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
   unsigned char* afp = smem + TC_S * SH::SLOT;   // [2][NA][TC_A_BYTES] exact codes (INT4)
-  __shared__ __align__(8) uint64_t bars[2];   // a stage's MMAs done: its A buffer and ring slot are free
-  __shared__ __align__(8) uint64_t gbars[2];  // a group's MMAs done (per tensor-memory buffer)
+  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[2], aempty[2], gfull[2], gempty[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_last;
+  __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int row_l = tid & (TC_M - 1);  // this thread's weight row within a tile
-  const int half = tid >> 7;           // k chunks 4h..4h+3 of a stage; batch columns 16h..16h+15
+  const int warp = tid >> 5, lane = tid & 31;
   const int K = a.K, M = a.M, N = a.N;
   const int nst = K / TC_K, ps = a.per_split, ks = a.ksplit;
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nwork = ntiles * ks;
   W4_TRACE_SCOPE(a.tag);
 
-  // tensor memory: two group buffers of NA accumulators of TC_N fp32 columns
   constexpr uint32_t TMEM_COLS = 2 * NA * TC_N;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -161,11 +201,17 @@ __global__ void __launch_bounds__(TC_THREADS, SILU || !INT4 ? 1 : 2) gemm_tc_ker
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    mbar_init(&gbars[0], 1);
-    mbar_init(&gbars[1], 1);
+  if (tid == 32) {
+    for (int i = 0; i < TC_S; ++i) {
+      mbar_init(&full[i], 32);
+      mbar_init(&empty[i], TC_READERS + 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&afull[i], TC_READERS);
+      mbar_init(&aempty[i], 1);
+      mbar_init(&gfull[i], 1);
+      mbar_init(&gempty[i], TC_READERS);
+    }
     s_fail = 0;
     fence_mbar_init();
   }
@@ -174,282 +220,161 @@ __global__ void __launch_bounds__(TC_THREADS, SILU || !INT4 ? 1 : 2) gemm_tc_ker
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
 
-  // ---- loader cursor: (work item, stage) of the next stage to load ----------
-  int l_work = blockIdx.x, l_st = 0, l_end = 0;
-  const uint32_t* l_q[NA];
-  const __half* l_s[NA];
-  const __half* l_w = nullptr;
-  bool l_ok = false;  // this thread's row exists
-  auto l_item = [&]() {
-    if (l_work >= nwork) return;
-    const int tile = l_work / ks, split = l_work % ks;
-    l_st = split * ps;
-    l_end = min(nst, l_st + ps);
+  // (work item, stage) cursor over this CTA's work, shared by all roles
+  struct Cursor {
+    int work, st, end, begin;
+  };
+  auto c_init = [&](Cursor& c) {
+    c.work = blockIdx.x;
+    if (c.work < nwork) {
+      c.begin = c.st = (c.work % ks) * ps;
+      c.end = min(nst, c.begin + ps);
+    }
+  };
+  auto c_next = [&](Cursor& c) {  // returns true when a new work item starts
+    if (++c.st < c.end) return false;
+    c.work += gridDim.x;
+    if (c.work < nwork) {
+      c.begin = c.st = (c.work % ks) * ps;
+      c.end = min(nst, c.begin + ps);
+    }
+    return true;
+  };
+  // A-operand row `row` of tile `tile` (weights): packed codes and scales
+  auto row_ptrs = [&](int tile, int row_l, const uint32_t* (&q)[NA], const __half* (&sp)[NA], bool& ok) {
     const int row = tile * TC_M + row_l;
-    l_ok = row < N;
-    const int rr = l_ok ? row : 0;
-    if (INT4) {
-      if (SILU) {
-#pragma unroll
-        for (int g = 0; g < NA; ++g) {
-          l_q[g] = a.seg[g].qw + (size_t)rr * (K / 8);
-          l_s[g] = a.seg[g].s + (size_t)rr * (K / 128);
-        }
-      } else {
-        int r = rr, si = 0;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-        l_q[0] = a.seg[si].qw + (size_t)r * (K / 8);
-        l_s[0] = a.seg[si].s + (size_t)r * (K / 128);
-      }
-    } else {
-      l_w = a.w16 + (size_t)rr * K;
-    }
-  };
-  auto l_next = [&]() {
-    if (l_work >= nwork) return;
-    if (++l_st >= l_end) {
-      l_work += gridDim.x;
-      l_item();
-    }
-  };
-  // weights of the loader's stage into ring slot `slot`
-  auto load_a = [&](int slot) {
-    if (l_work >= nwork) return;
-    unsigned char* sa = ring + slot * SH::SLOT;
-    const int k0 = l_st * TC_K;
-    if (INT4) {
-#pragma unroll
-      for (int g = 0; g < NA; ++g)
-        cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + half * 16, l_q[g] + k0 / 8 + 4 * half, l_ok);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int w = 4 * half + i;
-        cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), l_w + k0 + 8 * w, l_ok);
-      }
-    }
-  };
-  // activation tile of stage `st` into ring slot `slot` (canonical layout)
-  auto load_b = [&](int slot, int st) {
-    unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
-    const int m = tid >> 3, w = tid & 7;
-    const bool ok = m < M;
-    cp_async16_zfill(sb + tc_off(m, w, TC_N * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
-  };
-
-  // scales: the row's scale of a group is loaded (plain load, into a
-  // register) when the loader issues the group's first stage, parked in a
-  // shared ring four stages later, and used when the group's sums are read
-  // (the second stage of the next group, or the end of the work item)
-  __shared__ __half s_scale[4][NA][TC_M];
-  __half pend[2][NA];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int g = 0; g < NA; ++g) pend[i][g] = __float2half(0.f);
-
-  // prologue: weights (independent of the previous kernel) before the
-  // dependency wait, activations after it; one commit group per stage
-  l_item();
-  int pro_work[TC_AHEAD], pro_st[TC_AHEAD];
-#pragma unroll
-  for (int i = 0; i < TC_AHEAD; ++i) {
-    pro_work[i] = l_work;
-    pro_st[i] = l_st;
-    load_a(i);
-    if (INT4 && half == 0 && l_work < nwork && (l_st & 1) == 0) {
+    ok = row < N;
+    const int rr = ok ? row : 0;
+    if (SILU) {
 #pragma unroll
       for (int g = 0; g < NA; ++g) {
-        const __half v = l_ok ? l_s[g][l_st >> 1] : __float2half(0.f);
-        if (i == 0) s_scale[0][g][row_l] = v;
-        if (i == 2) pend[0][g] = v;
-        if (i == 4) pend[1][g] = v;
+        q[g] = a.seg[g].qw + (size_t)rr * (K / 8);
+        sp[g] = a.seg[g].s + (size_t)rr * (K / 128);
       }
+    } else {
+      int r = rr, si = 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
+      q[0] = a.seg[si].qw + (size_t)r * (K / 8);
+      sp[0] = a.seg[si].s + (size_t)r * (K / 128);
     }
-    l_next();
-  }
-  pdl_wait_then_trigger();
-  W4_TRACE_WAITED();
-#pragma unroll
-  for (int i = 0; i < TC_AHEAD; ++i) {
-    if (pro_work[i] < nwork) load_b(i, pro_st[i]);
-    cp_async_commit();
-  }
-
-  // ---- compute ---------------------------------------------------------------
-  float acc[NA][16];
-#pragma unroll
-  for (int g = 0; g < NA; ++g)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
-
-  // add tensor-memory group buffer `grp` (this thread's row, 16 columns) times the scales
-  auto tm_read = [&](uint32_t grp, int sslot) {
-    // tcgen05.ld is warp-collective: the warp goes on only if every lane saw the barrier
-    if (!__all_sync(0xffffffffu, tc_wait(&gbars[grp & 1], (grp >> 1) & 1))) {
-      s_fail = 1;
-      return;
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll
-    for (int g = 0; g < NA; ++g) {
-      uint32_t r[16];
-      const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * TC_N) +
-                             (uint32_t)(g * TC_N + half * 16);
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(taddr));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const float sc = INT4 ? __half2float(s_scale[sslot][g][row_l]) : 1.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[g][j] = fmaf(__uint_as_float(r[j]), sc, acc[g][j]);
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   };
 
-  // per-item epilogue: split-K partials and ticket, then the outputs
-  auto epilogue = [&](int work) {
-    const int tile = work / ks, split = work % ks;
-    const int row = tile * TC_M + row_l;
-    bool finish = true;
-    if (ks > 1) {
-      float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * TC_N * TC_M);
+  if (warp == 0) {
+    // =========================== producer ===================================
+    Cursor cur;
+    c_init(cur);
+    // this lane's four weight rows (lane + 32 j) of the current tile
+    const uint32_t* q[4][NA];
+    const __half* w16[4];
+    bool rok[4];
+    auto item_rows = [&]() {
+      const int tile = cur.work / ks;
 #pragma unroll
-      for (int g = 0; g < NA; ++g)
+      for (int j = 0; j < 4; ++j) {
+        if (INT4) {
+          const __half* sp[NA];
+          row_ptrs(tile, lane + 32 * j, q[j], sp, rok[j]);
+        } else {
+          const int row = tile * TC_M + lane + 32 * j;
+          rok[j] = row < N;
+          w16[j] = a.w16 + (size_t)(rok[j] ? row : 0) * K;
+        }
+      }
+    };
+    if (cur.work < nwork) item_rows();
+    auto load_a = [&](int slot) {
+      unsigned char* sa = ring + slot * SH::SLOT;
+      const int k0 = cur.st * TC_K;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) wsp[(g * TC_N + half * 16 + j) * TC_M + row_l] = acc[g][j];
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
-      __syncthreads();
-      finish = s_last;
-      if (finish) {
-        __threadfence();
-#pragma unroll
-        for (int g = 0; g < NA; ++g)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
-        for (int sp = 0; sp < ks; ++sp) {
-          const float* wp = a.ws + ((size_t)tile * ks + sp) * (size_t)(NA * TC_N * TC_M);
+      for (int j = 0; j < 4; ++j) {
+        const int row_l = lane + 32 * j;
+        if (INT4) {
 #pragma unroll
           for (int g = 0; g < NA; ++g)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[g][j] += __ldcg(&wp[(g * TC_N + half * 16 + j) * TC_M + row_l]);
+            for (int hh = 0; hh < 2; ++hh)
+              cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + hh * 16, q[j][g] + k0 / 8 + 4 * hh, rok[j]);
+        } else {
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), w16[j] + k0 + 8 * w, rok[j]);
         }
-        if (tid == 0) a.counters[tile] = 0u;  // ready for the next call
+      }
+    };
+    auto load_b = [&](int slot, int st) {
+      unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = lane + 32 * i;
+        const int m = c >> 3, w = c & 7;
+        const bool ok = m < M;
+        cp_async16_zfill(sb + tc_off(m, w, TC_N * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
+      }
+    };
+    // prologue: the weights of the first stages before the dependency wait
+    int pro_st[TC_S];
+    int npro = 0;
+    {
+      Cursor c2 = cur;
+      for (int i = 0; i < TC_S && c2.work < nwork; ++i) {
+        if (i > 0 && c2.st == c2.begin) {  // a new item inside the prologue: stop (its rows differ)
+          break;
+        }
+        pro_st[i] = c2.st;
+        cur = c2;
+        load_a(i);
+        ++npro;
+        c_next(c2);
       }
     }
-    if (!finish || row >= N) return;
-    if (a.y32 != nullptr) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = half * 16 + j;
-        if (m < M) a.y32[(size_t)m * a.ldy + row] = acc[0][j];
-      }
-    } else if (SILU) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = half * 16 + j;
-        if (m < M) {
-          const float g = __half2float(__float2half_rn(acc[0][j]));
-          const float u = __half2float(__float2half_rn(acc[NA - 1][j]));
-          a.y[(size_t)m * a.ldy + row] = __float2half_rn(g / (1.0f + expf(-g)) * u);
-        }
-      }
-    } else {
-      float bv = 0.f;
-      if (INT4) {
-        int r = row, si = 0;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-        if (a.seg[si].bias) bv = __half2float(a.seg[si].bias[r]);
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = half * 16 + j;
-        if (m < M) {
-          float v = acc[0][j] + bv;
-          if (a.residual) v += __half2float(a.residual[(size_t)m * a.ldy + row]);
-          a.y[(size_t)m * a.ldy + row] = __float2half_rn(v);
-        }
-      }
+    pdl_wait_then_trigger();
+    W4_TRACE_WAITED();
+    for (int i = 0; i < npro; ++i) {
+      load_b(i, pro_st[i]);
+      cp_async_mbar_arrive(&full[i]);
     }
-  };
-
-  int c_work = blockIdx.x, c_st = 0, c_end = 0, c_begin = 0;
-  auto c_item = [&]() {
-    const int split = c_work % ks;
-    c_begin = c_st = split * ps;
-    c_end = min(nst, c_begin + ps);
-  };
-  if (c_work < nwork) c_item();
-  // c: stages computed by this CTA.  Work items have an even number of
-  // stages and start at even c, so c & 1 tells a group's first (0) and
-  // second (1) stage, and a work item always ends on an odd c.
-  uint32_t c = 0, gc = 0, issued = 0;
-  bool run = c_work < nwork;
-  while (run) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      // (1) the MMAs of stage c-2 are done (A buffer u and ring slot
-      //     (c + TC_AHEAD) % TC_S are free); this thread's loads of stage c landed
-      if (c >= 2 && !tc_wait(&bars[u], ((c - 2) >> 1) & 1)) s_fail = 1;
-      cp_async_wait<TC_AHEAD - 1>();
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (s_fail) {
-        run = false;
-        break;
-      }
-      // (2) scales parked; loads for stage c + TC_AHEAD
-      if (INT4 && u == 0 && half == 0) {
-        const int pi = (c >> 1) & 1;
-#pragma unroll
-        for (int g = 0; g < NA; ++g) {
-          s_scale[((c + 2) >> 1) & 3][g][row_l] = pend[pi][g];
-          if (l_work < nwork) pend[pi][g] = l_ok ? l_s[g][l_st >> 1] : __float2half(0.f);
-        }
-      }
-      const int ls = (int)((c + TC_AHEAD) % TC_S);
-      if (l_work < nwork) {
-        load_a(ls);
-        load_b(ls, l_st);
-      }
-      cp_async_commit();
-      l_next();
-      // (3) exact codes of stage c into A buffer u
-      unsigned char* slot = ring + (c % TC_S) * SH::SLOT;
-      if (INT4) {
-#pragma unroll
-        for (int g = 0; g < NA; ++g) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(slot + (g * TC_M + row_l) * 32 + half * 16);
-          unsigned char* A = afp + (u * NA + g) * TC_A_BYTES;
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(A + tc_off(row_l, 4 * half + i, TC_M * 32)) = codes_word(wv[i]);
-        }
+    // restore the cursor to the stage after the prologue
+    c_init(cur);
+    if (cur.work < nwork) item_rows();
+    for (int i = 0; i < npro; ++i)
+      if (c_next(cur) && cur.work < nwork) item_rows();
+    for (uint32_t s = npro; cur.work < nwork; ++s) {
+      const int slot = s % TC_S;
+      if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail)) break;
+      load_a(slot);
+      load_b(slot, cur.st);
+      cp_async_mbar_arrive(&full[slot]);
+      if (c_next(cur) && cur.work < nwork) item_rows();
+    }
+    cp_async_wait<0>();
+  } else if (warp == 1) {
+    // =========================== MMA issuer =================================
+    pdl_wait_then_trigger();
+    if (lane == 0) {
+      Cursor cur;
+      c_init(cur);
+      uint32_t s = 0;
+      for (; cur.work < nwork; ++s) {
+        const int slot = s % TC_S, ab = s & 1;
+        const uint32_t grp = s >> 1;
+        const bool gfirst = (s & 1) == 0;
+        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail)) break;
+        if (INT4 && !tcw_wait(&afull[ab], (s >> 1) & 1, &s_fail)) break;
+        if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail)) break;
         fence_proxy_async_smem();
-      }
-      __syncthreads();
-      // (4) MMAs (one thread), committed to the stage barrier and, at a
-      //     group's second stage, to the group barrier
-      if (tid == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t gbase = tmem + (gc & 1) * (NA * TC_N);
+        unsigned char* sl = ring + slot * SH::SLOT;
+        const uint32_t gbase = tmem + (grp & 1) * (NA * TC_N);
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          const unsigned char* A = INT4 ? afp + (u * NA + g) * TC_A_BYTES : slot;
+          const unsigned char* A = INT4 ? afp + (ab * NA + g) * TC_A_BYTES : sl;
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
             const uint64_t ad = tc_desc(smem_u32(A + kk * TC_M * 32));
-            const uint64_t bd = tc_desc(smem_u32(slot + SH::A_RAW + kk * TC_N * 32));
-            const uint32_t accum = (u == 1 || kk > 0) ? 1u : 0u;
+            const uint64_t bd = tc_desc(smem_u32(sl + SH::A_RAW + kk * TC_N * 32));
+            const uint32_t accum = (!gfirst || kk > 0) ? 1u : 0u;
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
@@ -457,46 +382,190 @@ __global__ void __launch_bounds__(TC_THREADS, SILU || !INT4 ? 1 : 2) gemm_tc_ker
                 : "memory");
           }
         }
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                         smem_u32(&bars[u]))
-                     : "memory");
-        if (u == 1)
-          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                           smem_u32(&gbars[gc & 1]))
-                       : "memory");
+        if (INT4) tc_commit(&aempty[ab]);
+        tc_commit(&empty[slot]);
+        if (!gfirst) tc_commit(&gfull[grp & 1]);
+        c_next(cur);
       }
-      ++issued;
-      // (5) the previous group of this item (its last MMAs were issued two
-      //     stages ago), while the tensor core works on this one
-      if (u == 1) {
-        if (c_st - 1 != c_begin) tm_read(gc - 1, (int)(((c - 3) >> 1) & 3));
-        ++gc;
-      }
-      ++c;
-      if (u == 0) ++c_st;
+      // before tensor memory is freed no MMA may be in flight: the last
+      // commit (to empty[]) covers all earlier MMAs
+      if (s > 0) (void)tcw_wait(&empty[(s - 1) % TC_S], ((s - 1) / TC_S) & 1, &s_fail);
     }
-    if (!run) break;
-    // (6) end of the work item (always after a group's second stage): its
-    //     last group, then the epilogue
-    if (c_st == c_end - 1) {
-      tm_read(gc - 1, (int)(((c - 2) >> 1) & 3));
-      epilogue(c_work);
+  } else {
+    // =========================== readers ====================================
+    pdl_wait_then_trigger();
+    const int r = tid - 64;                       // 0..255
+    const int half = r >> 7;                      // k chunks 4h..4h+3; batch columns 16h..16h+15
+    const int row_l = 32 * (warp & 3) + lane;     // tensor-memory lanes of this warp's quadrant
+    Cursor cur;
+    c_init(cur);
+    const uint32_t* q[NA];
+    const __half* sp[NA];
+    bool rok = false;
+    if (INT4 && cur.work < nwork) row_ptrs(cur.work / ks, row_l, q, sp, rok);
+    __half sreg0[NA], sreg1[NA];  // scales of groups with even / odd index
 #pragma unroll
-      for (int g = 0; g < NA; ++g)
+    for (int g = 0; g < NA; ++g) sreg0[g] = sreg1[g] = __float2half(0.f);
+    float acc[NA][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
-      c_work += gridDim.x;
-      if (c_work >= nwork) break;
-      c_item();
-    } else {
-      ++c_st;
+    for (int g = 0; g < NA; ++g)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+
+    // add tensor-memory group `grp` (this row, 16 columns) times the scales
+    auto tm_read = [&](uint32_t grp) {
+      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail));
+      if (ok) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
+          uint32_t v[16];
+          const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * TC_N) +
+                                 (uint32_t)(g * TC_N + half * 16);
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+              : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                "=r"(v[15])
+              : "r"(taddr));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          const float sc = INT4 ? __half2float((grp & 1) ? sreg1[g] : sreg0[g]) : 1.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[g][j] = fmaf(__uint_as_float(v[j]), sc, acc[g][j]);
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      }
+      mbar_arrive(&gempty[grp & 1]);
+    };
+
+    auto epilogue = [&](int work) {
+      const int tile = work / ks, split = work % ks;
+      const int row = tile * TC_M + row_l;
+      bool finish = true;
+      if (ks > 1) {
+        float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * TC_N * TC_M);
+#pragma unroll
+        for (int g = 0; g < NA; ++g)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) wsp[(g * TC_N + half * 16 + j) * TC_M + row_l] = acc[g][j];
+        __threadfence();
+        readers_sync();
+        if (r == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
+        readers_sync();
+        finish = s_last;
+        if (finish) {
+          __threadfence();
+#pragma unroll
+          for (int g = 0; g < NA; ++g)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+          for (int spl = 0; spl < ks; ++spl) {
+            const float* wp = a.ws + ((size_t)tile * ks + spl) * (size_t)(NA * TC_N * TC_M);
+#pragma unroll
+            for (int g = 0; g < NA; ++g)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[g][j] += __ldcg(&wp[(g * TC_N + half * 16 + j) * TC_M + row_l]);
+          }
+          if (r == 0) a.counters[tile] = 0u;  // ready for the next call
+        }
+      }
+      if (!finish || row >= N) return;
+      if (a.y32 != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = half * 16 + j;
+          if (m < M) a.y32[(size_t)m * a.ldy + row] = acc[0][j];
+        }
+      } else if (SILU) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = half * 16 + j;
+          if (m < M) {
+            const float gv = __half2float(__float2half_rn(acc[0][j]));
+            const float u = __half2float(__float2half_rn(acc[NA - 1][j]));
+            a.y[(size_t)m * a.ldy + row] = __float2half_rn(gv / (1.0f + expf(-gv)) * u);
+          }
+        }
+      } else {
+        float bv = 0.f;
+        if (INT4) {
+          int rr = row, si = 0;
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            if (si < a.nseg - 1 && rr >= a.seg[si].rows) { rr -= a.seg[si].rows; ++si; }
+          if (a.seg[si].bias) bv = __half2float(a.seg[si].bias[rr]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = half * 16 + j;
+          if (m < M) {
+            float v = acc[0][j] + bv;
+            if (a.residual) v += __half2float(a.residual[(size_t)m * a.ldy + row]);
+            a.y[(size_t)m * a.ldy + row] = __float2half_rn(v);
+          }
+        }
+      }
+    };
+
+    for (uint32_t s = 0; cur.work < nwork; ++s) {
+      const int slot = s % TC_S, ab = s & 1;
+      const uint32_t grp = s >> 1;
+      const bool gfirst = (s & 1) == 0;
+      if (INT4) {
+        // (1) the A buffer's previous MMAs are done, the slot's copies landed
+        if (s >= 2) (void)tcw_wait(&aempty[ab], ((s - 2) >> 1) & 1, &s_fail);
+        (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail);
+        // (2) this group's scale (used when the group is read, three stages on)
+        // (loaded straight into the register that holds it until the read,
+        // so the load's latency is not waited for here)
+        if (gfirst && rok) {
+          if (grp & 1) {
+#pragma unroll
+            for (int g = 0; g < NA; ++g) sreg1[g] = sp[g][cur.st >> 1];
+          } else {
+#pragma unroll
+            for (int g = 0; g < NA; ++g) sreg0[g] = sp[g][cur.st >> 1];
+          }
+        }
+        // (3) exact codes into A buffer ab
+        const unsigned char* sl = ring + slot * SH::SLOT;
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + half * 16);
+          unsigned char* A = afp + (ab * NA + g) * TC_A_BYTES;
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(A + tc_off(row_l, 4 * half + i, TC_M * 32)) = codes_word(wv[i]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&afull[ab]);
+        mbar_arrive(&empty[slot]);
+      } else {
+        mbar_arrive(&empty[slot]);  // dense weights: nothing to expand; the MMA reads the slot
+      }
+      // (4) the previous group of this item, one group behind the tensor core
+      if (!gfirst && cur.st - 1 != cur.begin) tm_read(grp - 1);
+      // (5) end of the work item: its last group, the epilogue, the abort check
+      if (!gfirst && cur.st == cur.end - 1) {
+        tm_read(grp);
+        epilogue(cur.work);
+#pragma unroll
+        for (int g = 0; g < NA; ++g)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+        if (r == 0) s_rfail = s_fail;
+        readers_sync();
+        if (s_rfail) break;
+        c_next(cur);
+        if (INT4 && cur.work < nwork) row_ptrs(cur.work / ks, row_l, q, sp, rok);
+      } else {
+        c_next(cur);
+      }
     }
   }
-  cp_async_wait<0>();
+  __syncthreads();
   if (s_fail && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
-  // before freeing tensor memory no MMA of this CTA may still be in flight:
-  // the last stage's commit covers all earlier ones
-  if (issued > 0 && tid == 0) (void)tc_wait(&bars[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
@@ -522,7 +591,7 @@ static int tc_ctas_per_sm() {
     auto kern = gemm_tc_kernel<INT4, SILU>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcShape<INT4, SILU>::SMEM);
     int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS, TcShape<INT4, SILU>::SMEM) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, TcShape<INT4, SILU>::SMEM) !=
             cudaSuccess ||
         bps < 1)
       bps = 1;
@@ -577,7 +646,7 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   const int nwork = ntiles * a.ksplit;
   auto go = [&](auto kern, size_t smem, int per_sm) -> int {
     const int blocks = std::max(1, std::min(nwork, per_sm * num_sms()));
-    cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(TC_THREADS), smem, s, a);
+    cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(TC_THREADS_WS), smem, s, a);
     if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemm_tc launch: %s", cudaGetErrorString(e));
     return W4A16_OK;
   };

@@ -49,65 +49,158 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 // nibble order: for 32-weight chunk j and word w of the chunk, one uint4 holds
 // {x0, x4}, {x1, x5}, {x2, x6}, {x3, x7} of k = 32 j + 8 w + i.
 // Layout [MT][4][K/32] uint4, so consecutive chunks are consecutive 16 bytes.
+// Beside it, per chunk, cs = 1032 sum_{i even} x + 72 sum_{i odd} x.
+// Work unit: one 8-element group (16 bytes) per thread and step; the four
+// groups of a chunk sit on four neighbouring lanes, which add their parts of
+// cs with two shuffles.  With the RMSNorm the groups stay in registers
+// between the sum of squares and the scaling (x and gamma are read once).
+constexpr int STAGE_GMAX = 2;  // 8-element groups per thread held for the fused RMSNorm (K <= 4096 at 256 threads)
+
+__device__ __forceinline__ void stage_group(uint4* xs, float* cs, int NCH, int m, int g, const __half (&h)[8],
+                                            bool active) {
+  float part = 0.f;
+  if (active) {
+    uint4 o;
+    o.x = pack_h2(h[0], h[4]);
+    o.y = pack_h2(h[1], h[5]);
+    o.z = pack_h2(h[2], h[6]);
+    o.w = pack_h2(h[3], h[7]);
+    xs[(size_t)(m * 4 + (g & 3)) * NCH + (g >> 2)] = o;
+    const float se = (__half2float(h[0]) + __half2float(h[2])) + (__half2float(h[4]) + __half2float(h[6]));
+    const float so = (__half2float(h[1]) + __half2float(h[3])) + (__half2float(h[5]) + __half2float(h[7]));
+    part = 1032.0f * se + 72.0f * so;
+  }
+  part += __shfl_xor_sync(0xffffffffu, part, 1);
+  part += __shfl_xor_sync(0xffffffffu, part, 2);
+  if (active && (g & 3) == 0) cs[(size_t)m * NCH + (g >> 2)] = part;
+}
+
 template <int MT>
 __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, float* cs, float (*red)[MT],
                                                   float* rscale) {
-  const int K = a.K, M = a.M, NCH = K >> 5;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarp = blockDim.x >> 5;
-  if (a.gamma != nullptr) {
-    // one pass: partial sums of squares per warp, one barrier, every thread
-    // then adds the warps' partials itself
-    for (int m = 0; m < M; ++m) {
-      float ss = 0.f;
-      for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
-        uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + k);
-        const __half* h = reinterpret_cast<const __half*>(&raw);
+  const int K = a.K, M = a.M, NCH = K >> 5, NG = K >> 3;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarp = nthr >> 5;
+  if (a.gamma != nullptr && NG <= STAGE_GMAX * nthr) {
+    // one read of x and gamma into registers, sums of squares, one barrier
+    uint4 xr[MT][STAGE_GMAX], gr[STAGE_GMAX];
+    float ss[MT];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float v = __half2float(h[i]);
-          ss = fmaf(v, v, ss);
+    for (int m = 0; m < MT; ++m) ss[m] = 0.f;
+#pragma unroll
+    for (int i = 0; i < STAGE_GMAX; ++i) {
+      const int g = tid + i * nthr;
+      if (g < NG) {
+        gr[i] = *reinterpret_cast<const uint4*>(a.gamma + 8 * g);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < M) xr[m][i] = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 8 * g);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < STAGE_GMAX; ++i) {
+      if (tid + i * nthr < NG) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < M) {
+            const __half* h = reinterpret_cast<const __half*>(&xr[m][i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float v = __half2float(h[e]);
+              ss[m] = fmaf(v, v, ss[m]);
+            }
+          }
         }
       }
-      ss = warp_sum(ss);
-      if (lane == 0) red[warp][m] = ss;
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float t = warp_sum(ss[m]);
+      if (lane == 0) red[warp][m] = t;
     }
     __syncthreads();
-    for (int m = 0; m < M; ++m) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
       float t = 0.f;
       for (int w = 0; w < nwarp; ++w) t += red[w][m];
       rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);  // per-thread copy
     }
-  }
-  for (int idx = threadIdx.x; idx < M * NCH; idx += blockDim.x) {
-    const int m = idx / NCH, j = idx - m * NCH;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
-    float csum_even = 0.f, csum_odd = 0.f;
 #pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-      uint4 raw = src[wi];
-      __half h[8];
-      *reinterpret_cast<uint4*>(h) = raw;
-      if (a.gamma != nullptr) {
-        uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + 32 * j + 8 * wi);
-        const __half* g = reinterpret_cast<const __half*>(&graw);
-        const float r = rscale[m];
+    for (int i = 0; i < STAGE_GMAX; ++i) {
+      const int g = tid + i * nthr;
+      if (i * nthr + warp * 32 >= NG) break;  // warp-uniform: no group of this warp is left
+      const bool active = g < NG;
+      const __half* gh = reinterpret_cast<const __half*>(&gr[i]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
-      }
-      uint4 o;
-      o.x = pack_h2(h[0], h[4]);
-      o.y = pack_h2(h[1], h[5]);
-      o.z = pack_h2(h[2], h[6]);
-      o.w = pack_h2(h[3], h[7]);
-      xs[(size_t)(m * 4 + wi) * NCH + j] = o;
+      for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+          __half h[8];
+          if (active) {
+            const __half* xh = reinterpret_cast<const __half*>(&xr[m][i]);
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        csum_even += __half2float(h[i]);
-        csum_odd += __half2float(h[i + 1]);
+            for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(__half2float(xh[e]) * rscale[m] * __half2float(gh[e]));
+          }
+          stage_group(xs, cs, NCH, m, g, h, active);
+        }
       }
     }
-    cs[(size_t)m * NCH + j] = 1032.0f * csum_even + 72.0f * csum_odd;
+  } else {
+    // plain copy (or, past the register budget, RMSNorm in two reads): one
+    // 32-element chunk per thread and step, its four loads in flight together
+    if (a.gamma != nullptr) {
+      for (int m = 0; m < M; ++m) {
+        float ss = 0.f;
+        for (int g = tid; g < NG; g += nthr) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 8 * g);
+          const __half* h = reinterpret_cast<const __half*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float v = __half2float(h[e]);
+            ss = fmaf(v, v, ss);
+          }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp][m] = ss;
+      }
+      __syncthreads();
+      for (int m = 0; m < M; ++m) {
+        float t = 0.f;
+        for (int w = 0; w < nwarp; ++w) t += red[w][m];
+        rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);
+      }
+    }
+    for (int idx = tid; idx < M * NCH; idx += nthr) {
+      const int m = idx / NCH, j = idx - m * NCH;
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 32 * j);
+      uint4 raw[4];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) raw[wi] = src[wi];
+      float se = 0.f, so = 0.f;
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        __half h[8];
+        *reinterpret_cast<uint4*>(h) = raw[wi];
+        if (a.gamma != nullptr) {
+          const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + 32 * j + 8 * wi);
+          const __half* gh = reinterpret_cast<const __half*>(&graw);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(__half2float(h[e]) * rscale[m] * __half2float(gh[e]));
+        }
+        uint4 o;
+        o.x = pack_h2(h[0], h[4]);
+        o.y = pack_h2(h[1], h[5]);
+        o.z = pack_h2(h[2], h[6]);
+        o.w = pack_h2(h[3], h[7]);
+        xs[(size_t)(m * 4 + wi) * NCH + j] = o;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          se += __half2float(h[e]);
+          so += __half2float(h[e + 1]);
+        }
+      }
+      cs[(size_t)m * NCH + j] = 1032.0f * se + 72.0f * so;
+    }
   }
   __syncthreads();
 }
@@ -425,6 +518,7 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
   stage_activations<MT>(a, xs, cs, red, rscale);
+  W4_TRACE_MARK(0);
 
   // compute side
   int c_task = blockIdx.x * WPB + warp, c_out0 = 0;
@@ -527,6 +621,7 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
       cp_async_wait<1>();  // this lane's batch in slot qq & 1 has landed
       compute(qq & 1, b);
       if (b == NB - 1) {
+        W4_TRACE_MARK(1);
         finish();
         if (c_task >= ntask) break;
       }
