@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
   __shared__ __align__(16) __half s_vnew[ATT_D];
   __shared__ int s_last;
+  // cluster partial table (used in the leader CTA): [partition][head][128 + M, den, pad]
+  __shared__ __align__(16) float s_clu[WP ? 4 : ATT_MAX_CLUSTER * G * (ATT_D + 4)];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -169,6 +171,15 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
     cp_async_commit();
   };
   for (int li = 0; li < ST; ++li) issue(li, li < my_pages ? page_of(li) : -1);
+  const int pos = L - 1;
+  // fused: the 64 (cos, sin) pairs of this position, each computed once and
+  // before the dependency wait (the position comes from the lengths, which
+  // an older kernel of the step wrote)
+  __shared__ float s_cos[ATT_D / 2], s_sin[ATT_D / 2];
+  if (FUSE && tid < ATT_D / 2) {
+    const float ang = __fmul_rn((float)(pos > 0 ? pos : 0), a.inv_freq[tid]);  // the fp32 product
+    sincosf(ang, &s_sin[tid], &s_cos[tid]);
+  }
   if (FUSE) {
     pdl_wait_then_trigger();
     W4_TRACE_WAITED();
@@ -176,39 +187,45 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
 
   // ---- q (and, fused, RoPE of q and the new k; append of k and v) ----------
   const __half* qb = a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D;
-  const int pos = L - 1;
   if (FUSE) {
-    // raw q | k_new | v_new of this group into shared memory (16-byte loads),
-    // and the 64 (cos, sin) pairs of this position, each computed once
-    __shared__ __align__(16) __half s_raw[(G + 2) * ATT_D];
-    __shared__ float s_cos[ATT_D / 2], s_sin[ATT_D / 2];
+    // each thread rotates pairs (i, i + 64) of q heads / the new k straight
+    // from the q|k|v rows (the q|k|v GEMV's output, read through L2)
     const __half* kn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + kvh) * ATT_D;
     const __half* vn = a.q + (size_t)b * a.q_stride + (size_t)(a.Hq + a.Hkv + kvh) * ATT_D;
-    for (int c = tid; c < (G + 2) * (ATT_D / 8); c += blockDim.x) {
-      const int h = c / (ATT_D / 8), w = c % (ATT_D / 8);
-      const __half* src = h < G ? qb + h * ATT_D : (h == G ? kn : vn);
-      reinterpret_cast<uint4*>(s_raw)[c] = reinterpret_cast<const uint4*>(src)[w];
-    }
-    if (tid < ATT_D / 2) {
-      const float ang = __fmul_rn((float)(pos > 0 ? pos : 0), a.inv_freq[tid]);  // the fp32 product
-      sincosf(ang, &s_sin[tid], &s_cos[tid]);
-    }
-    __syncthreads();
-    for (int idx = tid; idx < (G + 1) * (ATT_D / 2); idx += blockDim.x) {
-      const int h = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
-      const float cs = s_cos[i], sn = s_sin[i];
-      const float x0 = __half2float(s_raw[h * ATT_D + i]), x1 = __half2float(s_raw[h * ATT_D + i + ATT_D / 2]);
-      const __half r0 = __float2half_rn(x0 * cs - x1 * sn);
-      const __half r1 = __float2half_rn(x1 * cs + x0 * sn);
-      if (h < G) {
-        s_q[h][i] = __half2float(r0);
-        s_q[h][i + ATT_D / 2] = __half2float(r1);
-      } else {
-        s_knew[i] = r0;
-        s_knew[i + ATT_D / 2] = r1;
+    constexpr int NPAIR = (G + 1) * (ATT_D / 2);
+    constexpr int PER = (NPAIR + NW * 32 - 1) / (NW * 32);
+    __half x0h[PER], x1h[PER], vh = __float2half(0.f);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = tid + u * NW * 32;
+      if (idx < NPAIR) {
+        const int h = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
+        const __half* src = h < G ? qb + h * ATT_D : kn;
+        x0h[u] = __ldcg(src + i);
+        x1h[u] = __ldcg(src + i + ATT_D / 2);
       }
     }
-    for (int d = tid; d < ATT_D; d += blockDim.x) s_vnew[d] = s_raw[(G + 1) * ATT_D + d];
+    if (tid < ATT_D) vh = __ldcg(vn + tid);
+    __syncthreads();  // s_cos / s_sin
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = tid + u * NW * 32;
+      if (idx < NPAIR) {
+        const int h = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
+        const float cs = s_cos[i], sn = s_sin[i];
+        const float x0 = __half2float(x0h[u]), x1 = __half2float(x1h[u]);
+        const __half r0 = __float2half_rn(x0 * cs - x1 * sn);
+        const __half r1 = __float2half_rn(x1 * cs + x0 * sn);
+        if (h < G) {
+          s_q[h][i] = __half2float(r0);
+          s_q[h][i + ATT_D / 2] = __half2float(r1);
+        } else {
+          s_knew[i] = r0;
+          s_knew[i + ATT_D / 2] = r1;
+        }
+      }
+    }
+    if (tid < ATT_D) s_vnew[tid] = vh;
     __syncthreads();
     if (pos >= cta_t0 && pos < cta_t1) {  // this CTA holds the new token: append it
       const int blk = pos / ATT_PAGE;
@@ -343,11 +360,10 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   // ---- merge the warps' states in shared memory (ring reused).  In the
   // warp-per-partition variant these are NW whole partitions, merged by the
   // same online-softmax rule as any two partials. -----------------------------
-  const int d = tid & (ATT_D - 1);  // dim of this thread; NPAR threads per dim split the heads
-  const int hpar = tid / ATT_D;     // 0 .. NPAR-1: heads h with h % NPAR == hpar
   const size_t qh0 = (size_t)b * a.Hq + (size_t)kvh * G;
   const int PC = gridDim.x;         // CTA partials per (sequence, kv head)
   const int pc = blockIdx.x;
+  const bool clu = !WP && a.use_cluster && PC > 1;
   float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
   float* mml = mo + NW * 8 * ATT_D;                     // [NW][8][2]
   if (head_ok) {
@@ -360,29 +376,43 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
     }
   }
   __syncthreads();
-
-  // this CTA's merged state: cp_o[h][d] = sum e^(m - M) o, cp_ml[h] = (M, sum e^(m - M) l)
-  float* cp_o = mml + NW * 8 * 2;  // [G][128]
+  // thread (h, 4 dims): this CTA's merged state; M = max m, den = sum e^(m-M) l,
+  // acc = sum e^(m-M) o.  It goes to the output (one partial), to the cluster
+  // leader's shared memory, or to the workspace.
+  float* cp_o = mml + NW * 8 * 2;  // [G][128] (workspace path)
   float* cp_ml = cp_o + G * ATT_D; // [G][2]
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    if (h % NPAR != hpar) continue;
+  for (int idx = tid; idx < G * (ATT_D / 4); idx += blockDim.x) {
+    const int h = idx / (ATT_D / 4), d4 = idx % (ATT_D / 4);
     float M = -INFINITY;
+#pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, mml[(w * 8 + h) * 2]);
-    float acc = 0.f, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
     if (M != -INFINITY) {
+#pragma unroll
       for (int w = 0; w < NW; ++w) {
         const float mw = mml[(w * 8 + h) * 2];
         const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        acc += mo[(w * 8 + h) * ATT_D + d] * f;
-        den += mml[(w * 8 + h) * 2 + 1] * f;
+        const float4 v = *reinterpret_cast<const float4*>(mo + (w * 8 + h) * ATT_D + 4 * d4);
+        acc.x = fmaf(v.x, f, acc.x);
+        acc.y = fmaf(v.y, f, acc.y);
+        acc.z = fmaf(v.z, f, acc.z);
+        acc.w = fmaf(v.w, f, acc.w);
+        den = fmaf(mml[(w * 8 + h) * 2 + 1], f, den);
       }
     }
     if (PC == 1) {
-      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      __half2* dst = reinterpret_cast<__half2*>(a.out + (qh0 + h) * ATT_D + 4 * d4);
+      dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    } else if (clu) {
+      // into slot `pc` of the leader's (rank 0's) partial table
+      st_dsmem4(&s_clu[(pc * G + h) * (ATT_D + 4) + 4 * d4], 0, acc);
+      if (d4 == 0) st_dsmem2(&s_clu[(pc * G + h) * (ATT_D + 4) + ATT_D], 0, make_float2(M, den));
     } else {
-      cp_o[h * ATT_D + d] = acc;
-      if (d == 0) {
+      *reinterpret_cast<float4*>(cp_o + h * ATT_D + 4 * d4) = acc;
+      if (d4 == 0) {
         cp_ml[h * 2] = M;
         cp_ml[h * 2 + 1] = den;
       }
@@ -391,42 +421,35 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   if (PC == 1) return;
   W4_TRACE_MARK(2);
 
-  if (!WP && a.use_cluster) {
-    // All partitions of this (sequence, kv head) form one thread-block
-    // cluster: merge them through distributed shared memory.  CTA rank r
-    // produces the heads h with h % P == r.
+  if (clu) {
+    // one cluster barrier: every CTA's partial has landed in the leader's
+    // table; the leader merges them (partitions with no tokens carry M = -inf)
     cluster_sync();
-    const int P = a.P;
-    const unsigned int rank = cluster_ctarank();
-    for (int h = (int)rank + hpar * P; h < G; h += NPAR * P) {
-      // all remote values first (independent loads), then the merge
-      float mj[ATT_MAX_CLUSTER], lj[ATT_MAX_CLUSTER], oj[ATT_MAX_CLUSTER];
-#pragma unroll
-      for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
-        if (j < P) {
-          mj[j] = ld_dsmem(&cp_ml[h * 2], j);
-          lj[j] = ld_dsmem(&cp_ml[h * 2 + 1], j);
-          oj[j] = ld_dsmem(&cp_o[h * ATT_D + d], j);
-        }
-      }
+    if (pc != 0) return;
+    for (int idx = tid; idx < G * (ATT_D / 4); idx += blockDim.x) {
+      const int h = idx / (ATT_D / 4), d4 = idx % (ATT_D / 4);
       float M = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < ATT_MAX_CLUSTER; ++j)
-        if (j < P) M = fmaxf(M, mj[j]);
-      float acc = 0.f, den = 0.f;
+      for (int j = 0; j < PC; ++j) M = fmaxf(M, s_clu[(j * G + h) * (ATT_D + 4) + ATT_D]);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
       if (M != -INFINITY) {
-#pragma unroll
-        for (int j = 0; j < ATT_MAX_CLUSTER; ++j) {
-          if (j < P) {
-            const float f = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
-            acc += oj[j] * f;
-            den += lj[j] * f;
-          }
+        for (int j = 0; j < PC; ++j) {
+          const float* e = &s_clu[(j * G + h) * (ATT_D + 4)];
+          const float mj = e[ATT_D];
+          const float f = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+          const float4 v = *reinterpret_cast<const float4*>(e + 4 * d4);
+          acc.x = fmaf(v.x, f, acc.x);
+          acc.y = fmaf(v.y, f, acc.y);
+          acc.z = fmaf(v.z, f, acc.z);
+          acc.w = fmaf(v.w, f, acc.w);
+          den = fmaf(e[ATT_D + 1], f, den);
         }
       }
-      a.out[(qh0 + h) * ATT_D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      __half2* dst = reinterpret_cast<__half2*>(a.out + (qh0 + h) * ATT_D + 4 * d4);
+      dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
     }
-    cluster_sync();  // keep every CTA's shared memory alive until all reads are done
     return;
   }
 

@@ -211,6 +211,20 @@ __device__ __forceinline__ unsigned int cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+// Store four floats at the same shared-memory offset in CTA `rank` of the
+// cluster (ordered before a later barrier.cluster.arrive.release).
+__device__ __forceinline__ void st_dsmem4(float* p, int rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_dsmem2(float* p, int rank, float2 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.x), "f"(v.y) : "memory");
+}
 // Load a float from the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float ld_dsmem(const float* p, int rank) {
   // Not volatile: the loads are ordered after the cluster barrier (which is
