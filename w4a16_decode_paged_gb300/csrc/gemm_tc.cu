@@ -47,6 +47,7 @@ constexpr int TC_READERS = 256;                  // threads that expand codes an
 constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
 constexpr int TC_AHEAD = 6;    // stages loaded ahead of the one computed
+constexpr int TC_NAB = 4;      // tensor-memory A buffers: how far code expansion runs ahead of the MMAs
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
 constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB activation tile per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
@@ -56,7 +57,10 @@ struct TcShape {
   static constexpr int NA = SILU ? 2 : 1;                                   // weight matrices per tile
   static constexpr uint32_t A_RAW = INT4 ? NA * TC_M * 32 : TC_A_BYTES;     // A bytes per ring slot
   static constexpr uint32_t SLOT = A_RAW + TC_B_BYTES;
-  static constexpr size_t SMEM = (size_t)TC_S * SLOT + (INT4 ? (size_t)2 * NA * TC_A_BYTES : 0) + 1024;
+  static constexpr size_t SMEM = (size_t)TC_S * SLOT + 1024;
+  // tensor memory: 2 group accumulators x NA x 32 columns, and (int4)
+  // TC_NAB A buffers x NA x 32 columns of exact codes (rounded up to a power of two)
+  static constexpr uint32_t TMEM_COLS = INT4 ? (NA == 2 ? 512 : 256) : 2 * NA * TC_N;
 };
 
 __device__ __forceinline__ unsigned long long tc_now() {
@@ -181,8 +185,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
-  unsigned char* afp = smem + TC_S * SH::SLOT;   // [2][NA][TC_A_BYTES] exact codes (INT4)
-  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[2], aempty[2], gfull[2], gempty[2];
+  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[TC_NAB], aempty[TC_NAB], gfull[2], gempty[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -194,7 +197,10 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
   const int nwork = ntiles * ks;
   W4_TRACE_SCOPE(a.tag);
 
-  constexpr uint32_t TMEM_COLS = 2 * NA * TC_N;
+  constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
+  // columns: [0, 2 NA 32) group accumulators; then (int4) A buffer ab, matrix g
+  // at 2 NA 32 + (ab NA + g) 32
+  constexpr uint32_t TM_A = 2 * NA * TC_N;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "r"(TMEM_COLS)
@@ -206,9 +212,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
       mbar_init(&full[i], 32);
       mbar_init(&empty[i], TC_READERS + 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < TC_NAB; ++i) {
       mbar_init(&afull[i], TC_READERS);
       mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&gfull[i], 1);
       mbar_init(&gempty[i], TC_READERS);
     }
@@ -265,21 +273,22 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
     // =========================== producer ===================================
     Cursor cur;
     c_init(cur);
-    // this lane's four weight rows (lane + 32 j) of the current tile
-    const uint32_t* q[4][NA];
-    const __half* w16[4];
-    bool rok[4];
+    // int4: lane pairs share a row (the two 16-byte halves of its 32 bytes per
+    // stage), so one copy instruction covers 16 rows with full sectors; this
+    // lane's rows are lane / 2 + 16 j.  Dense: eight lanes cover a row's 128
+    // bytes, rows lane / 8 + 4 j.
+    const uint32_t* q[8][NA];
+    bool rok[8];
+    const int hh = lane & 1;
+    int tile0 = 0;
     auto item_rows = [&]() {
       const int tile = cur.work / ks;
+      tile0 = tile * TC_M;
+      if (INT4) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (INT4) {
+        for (int j = 0; j < 8; ++j) {
           const __half* sp[NA];
-          row_ptrs(tile, lane + 32 * j, q[j], sp, rok[j]);
-        } else {
-          const int row = tile * TC_M + lane + 32 * j;
-          rok[j] = row < N;
-          w16[j] = a.w16 + (size_t)(rok[j] ? row : 0) * K;
+          row_ptrs(tile, (lane >> 1) + 16 * j, q[j], sp, rok[j]);
         }
       }
     };
@@ -287,19 +296,22 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
     auto load_a = [&](int slot) {
       unsigned char* sa = ring + slot * SH::SLOT;
       const int k0 = cur.st * TC_K;
+      if (INT4) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row_l = lane + 32 * j;
-        if (INT4) {
+        for (int j = 0; j < 8; ++j) {
+          const int row_l = (lane >> 1) + 16 * j;
 #pragma unroll
           for (int g = 0; g < NA; ++g)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + hh * 16, q[j][g] + k0 / 8 + 4 * hh, rok[j]);
-        } else {
-#pragma unroll
-          for (int w = 0; w < 8; ++w)
-            cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), w16[j] + k0 + 8 * w, rok[j]);
+            cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + hh * 16, q[j][g] + k0 / 8 + 4 * hh, rok[j]);
+        }
+      } else {
+        const int w = lane & 7;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+          const int row_l = (lane >> 3) + 4 * j;
+          const int row = tile0 + row_l;
+          const bool ok = row < N;
+          cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), a.w16 + (size_t)(ok ? row : 0) * K + k0 + 8 * w, ok);
         }
       }
     };
@@ -357,29 +369,39 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
       c_init(cur);
       uint32_t s = 0;
       for (; cur.work < nwork; ++s) {
-        const int slot = s % TC_S, ab = s & 1;
+        const int slot = s % TC_S, ab = s % TC_NAB;
         const uint32_t grp = s >> 1;
         const bool gfirst = (s & 1) == 0;
         if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail)) break;
-        if (INT4 && !tcw_wait(&afull[ab], (s >> 1) & 1, &s_fail)) break;
+        if (INT4 && !tcw_wait(&afull[ab], (s / TC_NAB) & 1, &s_fail)) break;
         if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail)) break;
         fence_proxy_async_smem();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         unsigned char* sl = ring + slot * SH::SLOT;
         const uint32_t gbase = tmem + (grp & 1) * (NA * TC_N);
+        const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          const unsigned char* A = INT4 ? afp + (ab * NA + g) * TC_A_BYTES : sl;
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
-            const uint64_t ad = tc_desc(smem_u32(A + kk * TC_M * 32));
-            const uint64_t bd = tc_desc(smem_u32(sl + SH::A_RAW + kk * TC_N * 32));
+            const uint64_t bd = bd0 + (uint64_t)((kk * TC_N * 32) >> 4);  // next 16-k slice of B
             const uint32_t accum = (!gfirst || kk > 0) ? 1u : 0u;
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
-                "l"(ad), "l"(bd), "r"(TC_IDESC), "r"(accum)
-                : "memory");
+            if (INT4) {
+              // A (128 x 16 exact codes) from tensor memory: 8 columns per 16 k
+              const uint32_t at = tmem + TM_A + (uint32_t)((ab * NA + g) * TC_N + kk * 8);
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
+                  "r"(at), "l"(bd), "r"(TC_IDESC), "r"(accum)
+                  : "memory");
+            } else {
+              const uint64_t ad = tc_desc(smem_u32(sl + kk * TC_M * 32));
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
+                  "l"(ad), "l"(bd), "r"(TC_IDESC), "r"(accum)
+                  : "memory");
+            }
           }
         }
         if (INT4) tc_commit(&aempty[ab]);
@@ -508,12 +530,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
     };
 
     for (uint32_t s = 0; cur.work < nwork; ++s) {
-      const int slot = s % TC_S, ab = s & 1;
+      const int slot = s % TC_S, ab = s % TC_NAB;
       const uint32_t grp = s >> 1;
       const bool gfirst = (s & 1) == 0;
       if (INT4) {
         // (1) the A buffer's previous MMAs are done, the slot's copies landed
-        if (s >= 2) (void)tcw_wait(&aempty[ab], ((s - 2) >> 1) & 1, &s_fail);
+        if (s >= TC_NAB) (void)tcw_wait(&aempty[ab], ((s - TC_NAB) / TC_NAB) & 1, &s_fail);
         (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail);
         // (2) this group's scale (used when the group is read, three stages on)
         // (loaded straight into the register that holds it until the read,
@@ -527,18 +549,23 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_
             for (int g = 0; g < NA; ++g) sreg0[g] = sp[g][cur.st >> 1];
           }
         }
-        // (3) exact codes into A buffer ab
+        // (3) exact codes of this row's 32 k (this half of the stage) into
+        //     tensor-memory A buffer ab: 16 columns of fp16 pairs in k order
         const unsigned char* sl = ring + slot * SH::SLOT;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
           const uint4 raw = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + half * 16);
-          unsigned char* A = afp + (ab * NA + g) * TC_A_BYTES;
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(A + tc_off(row_l, 4 * half + i, TC_M * 32)) = codes_word(wv[i]);
+          const uint4 c0 = codes_word(raw.x), c1 = codes_word(raw.y), c2 = codes_word(raw.z), c3 = codes_word(raw.w);
+          const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A + (uint32_t)((ab * NA + g) * TC_N + half * 16);
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
+              "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w), "r"(c2.x), "r"(c2.y),
+              "r"(c2.z), "r"(c2.w), "r"(c3.x), "r"(c3.y), "r"(c3.z), "r"(c3.w)
+              : "memory");
         }
-        fence_proxy_async_smem();
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         mbar_arrive(&afull[ab]);
         mbar_arrive(&empty[slot]);
       } else {
