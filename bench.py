@@ -395,6 +395,24 @@ def run_kernel(args):
     return 0
 
 
+def max_over_ranks(values, dev, world):
+    """Each timing, maximised over the ranks of the job (the slowest replica
+    sets the job's time).  dev: the device of the collective's tensor (cuda
+    for NCCL, cpu for gloo)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world, batch, steps, seconds):
+    """Tokens per second of the whole job: every rank decodes `batch`
+    sequences for `steps` steps (weak scaling), in `seconds` (max over ranks)."""
+    return world * batch * steps / seconds
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -497,17 +515,14 @@ def main():
             kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream, B)
 
     # max over ranks
-    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e_s = float(t[0]), float(t[1])
+    ms, e2e_s = max_over_ranks([ms, e2e_s], dev, world)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
     peak, peak_src = measured_peak()
-    value = world * B * K / (ms / 1e3)
+    value = job_throughput(world, B, K, ms / 1e3)
     mid_lens = inp["lens"] + 1 + K // 2
     sb = step_bytes(cfg, mid_lens)
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
