@@ -207,6 +207,9 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
 
 constexpr uint32_t MAGIC_H2 = 0x64006400u;  // half2{1024, 1024}
 
+constexpr int gcd_c(int x, int y) { return y == 0 ? x : gcd_c(y, x % y); }
+constexpr int lcm_c(int x, int y) { return x / gcd_c(x, y) * y; }
+
 // w >> 8 as the high word of an integer multiply, so it issues on the FMA
 // pipe and leaves the half-rate ALU pipe to the LOP3s.
 __device__ __forceinline__ uint32_t shr8_fma(uint32_t w) {
@@ -423,15 +426,16 @@ __global__ void __launch_bounds__(GEMV_WPB * 32) gemv_w4a16_kernel(const __grid_
 // RU: chunks per lane per batch (R rows x U chunks).  K = 3584 uses 8 so a
 // whole row (7 chunks per lane) is in flight before the dependency wait;
 // the long-K down projection uses 4 to fit more CTAs per SM.
-template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB>
+template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB, int NS>
 __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __grid_constant__ GemvArgs a) {
   constexpr int LPR = 16, U = RU / R;
   constexpr int K = NCH * 32;
   constexpr int NIT = NCH / LPR;                 // chunks per lane when one half-warp covers K
   constexpr int NIT_L = (NIT + KS - 1) / KS;     // this lane's share (upper bound)
   constexpr int NB = (NIT_L + U - 1) / U;        // batches per task
-  constexpr int NBT = (NB % 2 == 0) ? NB : 2 * NB;  // batches per unrolled round (even: ring slot = batch & 1)
-  constexpr int TPR = NBT / NB;                  // tasks per round
+  // batches per unrolled round: a multiple of NB and of the NS ring slots,
+  // so every slot index is a compile-time constant
+  constexpr int NBT = lcm_c(NB, NS);
   constexpr int WROW = K / 8;
   constexpr int SROW = K / 128;
   constexpr int RPT = SILU ? R : (KS == 2 ? R : 2 * R);
@@ -441,8 +445,8 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
   static_assert(NCH % LPR == 0, "every lane takes the same number of chunks");
   extern __shared__ uint4 smem[];
   uint4* xs = smem;                                          // [MT][4][NCH]
-  uint4* ring = smem + MT * 4 * NCH;                         // [2][RU][NT], each lane its own column
-  float* cs = reinterpret_cast<float*>(ring + 2 * RU * NT);  // [MT][NCH]
+  uint4* ring = smem + MT * 4 * NCH;                          // [NS][RU][NT], each lane its own column
+  float* cs = reinterpret_cast<float*>(ring + NS * RU * NT);  // [MT][NCH]
   __shared__ float red[WPB][MT];
   __shared__ float rscale[MT];
   const int tid = threadIdx.x;
@@ -487,7 +491,7 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
     i_q += 4 * jl;         // this lane's first 16-byte word
     i_s += jl >> 2;
   }
-  __half sc[2][RU];
+  __half sc[NS][RU];
   // batch b of the issue task into ring slot `slot` (b, slot compile-time once unrolled)
   auto issue = [&](const int slot, const int b) {
     if (i_task < ntask) {
@@ -514,7 +518,12 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
     }
   };
 
-  issue(0, 0);  // weights do not depend on the previous kernel
+  // the first NS - 1 batches: weights do not depend on the previous kernel
+#pragma unroll
+  for (int q0 = 0; q0 < NS - 1; ++q0) {
+    if (q0 > 0 && q0 % NB == 0) next_issue_task();
+    issue(q0, q0 % NB);
+  }
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
   stage_activations<MT>(a, xs, cs, red, rscale);
@@ -611,15 +620,15 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
     if (c_task < ntask) rows_of(c_task, c_out0, c_q, c_s, c_bias);
   };
 
-  // rounds of NBT batches (TPR tasks); the issue side runs one batch ahead
+  // rounds of NBT batches; the issue side runs NS - 1 batches ahead
   while (c_task < ntask) {
 #pragma unroll
     for (int qq = 0; qq < NBT; ++qq) {
-      const int b = qq % NB, bn = (qq + 1) % NB;
+      const int b = qq % NB, bn = (qq + NS - 1) % NB;  // computed batch; batch issued NS - 1 ahead
       if (bn == 0) next_issue_task();
-      issue((qq + 1) & 1, bn);
-      cp_async_wait<1>();  // this lane's batch in slot qq & 1 has landed
-      compute(qq & 1, b);
+      issue((qq + NS - 1) % NS, bn);
+      cp_async_wait<NS - 1>();  // this lane's batch in slot qq % NS has landed
+      compute(qq % NS, b);
       if (b == NB - 1) {
         W4_TRACE_MARK(1);
         finish();
@@ -629,10 +638,10 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) gemv_w4a16_fast(const __gr
   }
   cp_async_wait<0>();
 }
-template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB = GEMV_WPB>
+template <int NCH, int R, int KS, int MT, bool SILU, int RU, int WPB = GEMV_WPB, int NS = 2>
 static int launch_fast(const GemvArgs& a, cudaStream_t s) {
-  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU, WPB>;
-  const size_t smem = (size_t)MT * a.K * 2 + (size_t)2 * RU * WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
+  auto kern = gemv_w4a16_fast<NCH, R, KS, MT, SILU, RU, WPB, NS>;
+  const size_t smem = (size_t)MT * a.K * 2 + (size_t)NS * RU * WPB * 32 * 16 + (size_t)MT * (a.K / 32) * 4;
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
