@@ -50,7 +50,6 @@ constexpr int ATT_STAGES = 2;      // page slots per warp (CTA per partition)
 constexpr int ATT_STAGES_WP = 3;   // page slots per warp (warp per partition: deeper, the
                                    // warp streams a whole partition alone)
 constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice in the pool
-constexpr uint32_t ATT_ROW_BYTES = ATT_D * 2;  // 256: one token's k (or v) of one kv head
 // In shared memory a slice's rows are 272 bytes apart (16 bytes of padding),
 // so the eight rows of an 8x8 ldmatrix tile fall on eight different bank
 // groups.
@@ -94,7 +93,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 
 template <int G, bool FUSE, int NW, bool WP>
 __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
-  constexpr int NPAR = NW * 32 / ATT_D;  // threads per output dim in the merges
   constexpr int ST = att_stages(WP);      // page slots per warp
   extern __shared__ __align__(128) unsigned char smraw[];
   __half* ring = reinterpret_cast<__half*>(smraw);

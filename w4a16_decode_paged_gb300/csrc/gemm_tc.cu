@@ -15,17 +15,19 @@
 // activation tile directly in the canonical no-swizzle K-major layout the MMA
 // reads: core matrices of 8 rows x 16 bytes, K-adjacent core matrices 128 B
 // apart, 8-row groups 256 B apart); 256 reader threads turn the 32 codes per
-// stage of their weight row into exact fp16 integers (q in [-8, 7]) in a
-// double-buffered A tile; one thread issues four kind::f16 MMAs (K = 16) per
-// weight matrix and commits them to the barriers that free the A buffer, the
-// ring slot and, per group, the tensor-memory buffer.
+// stage of their weight row into exact fp16 integers (q in [-8, 7]) and store
+// them with tcgen05.st into one of TC_NAB tensor-memory A buffers (the MMA
+// reads A from tensor memory, so the expanded codes never touch shared
+// memory); one thread issues four kind::f16 MMAs (K = 16) per weight matrix
+// and commits them to the barriers that free the A buffer, the ring slot and,
+// per group, the accumulator buffer.
 //
 // Precision: the MMAs see exact codes and exact fp16 activations (products
 // exact, fp32 sums).  Each 128-wide scale group accumulates into its own
-// tensor-memory buffer (two alternate); the threads read a group's sums
-// with tcgen05.ld two stages after its last MMAs were issued (while the
-// tensor core works on the next group) and add them times the row's fp32
-// scale, so the only roundings are fp32 sums and the final fp16 store.
+// tensor-memory buffer (two alternate); the readers read a group's sums with
+// tcgen05.ld at the second stage of the next group (while the tensor core
+// works on that group) and add them times the row's fp32 scale, so the only
+// roundings are fp32 sums and the final fp16 store.
 //
 // Small-N projections split K across CTAs (split length chosen so the work
 // items fill whole waves of CTAs): each split parks its fp32 tile in the
@@ -46,7 +48,6 @@ constexpr int TC_K = 64;       // K per stage
 constexpr int TC_READERS = 256;                  // threads that expand codes and read tensor memory
 constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
-constexpr int TC_AHEAD = 6;    // stages loaded ahead of the one computed
 constexpr int TC_NAB = 4;      // tensor-memory A buffers: how far code expansion runs ahead of the MMAs
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
 constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB activation tile per stage
