@@ -48,7 +48,7 @@ constexpr int TC_K = 64;       // K per stage
 constexpr int TC_READERS = 256;                  // threads that expand codes and read tensor memory
 constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
-constexpr int TC_NAB = 4;      // tensor-memory A buffers: how far code expansion runs ahead of the MMAs
+constexpr int TC_NAB = 2;      // tensor-memory A buffers: how far code expansion runs ahead of the MMAs
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
 constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB activation tile per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
@@ -61,7 +61,7 @@ struct TcShape {
   static constexpr size_t SMEM = (size_t)TC_S * SLOT + 1024;
   // tensor memory: 2 group accumulators x NA x 32 columns, and (int4)
   // TC_NAB A buffers x NA x 32 columns of exact codes (rounded up to a power of two)
-  static constexpr uint32_t TMEM_COLS = INT4 ? (NA == 2 ? 512 : 256) : 2 * NA * TC_N;
+  static constexpr uint32_t TMEM_COLS = INT4 ? 2 * NA * TC_N + TC_NAB * NA * TC_N : 2 * NA * TC_N;
 };
 
 __device__ __forceinline__ unsigned long long tc_now() {
@@ -180,7 +180,7 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //   gfull[b]     MMAs of the group in tensor-memory buffer b   (1, commit)
 //   gempty[b]    readers read tensor-memory buffer b           (256)
 template <bool INT4, bool SILU>
-__global__ void __launch_bounds__(TC_THREADS_WS, 1) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU>;
   constexpr int NA = SH::NA;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
