@@ -99,7 +99,7 @@ def test_decode_step_matches_oracle_free_running(api):
     vps_o = [v.copy() for v in vps]
     t_oracle = toks.copy()
     n = lens.copy()
-    for step in range(4):
+    for step in range(16):
         m.decode_step(tok, tok, btd, ld, logits=logits, use_graph=True)
         n = n + 1
         t_next, lg_ref, _ = orc.decode_step(cfg, layers, kps_o, vps_o, embed, fnorm, lm, t_oracle, bt, n,
@@ -145,3 +145,45 @@ def test_model_err_flag_reports_bad_page(api):
     assert m.check_errors() == 0
     assert np.array_equal(to_host(dls[0]["v_pool"]), vps[0])   # the bad append wrote nothing
     m.close()
+
+
+def test_check_errors_refuses_while_capturing(api):
+    cfg, layers, kps, vps, embed, fnorm, lm, bt, lens, toks = _small_model(n_layers=1, vocab=300, seed=4400)
+    m, dls = _build(api, cfg, layers, kps, vps, embed, fnorm, lm, 1, 128)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+        status = m.check_errors(s)   # blocks and copies to the host: refused, nothing enqueued
+    assert status == 5               # W4A16_ERR_CAPTURE
+    assert m.check_errors() == 0
+    m.close()
+
+
+def test_decode_step_inside_a_caller_graph(api):
+    """decode_step on a stream the caller is capturing records its kernels into
+    the caller's graph; replaying that graph decodes like direct launches."""
+    cfg, layers, kps, vps, embed, fnorm, lm, bt, lens, toks = _small_model(n_layers=2, vocab=900, seed=4500)
+    outs = []
+    for mode in ("direct", "caller_graph"):
+        m, dls = _build(api, cfg, layers, kps, vps, embed, fnorm, lm, 1, 128)
+        tok = to_dev(toks, torch)
+        ld = to_dev(lens, torch)
+        btd = to_dev(bt, torch)
+        seq = []
+        if mode == "direct":
+            for _ in range(4):
+                m.decode_step(tok, tok, btd, ld, use_graph=False)
+                seq.append(int(to_host(tok)[0]))
+        else:
+            s = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                m.decode_step(tok, tok, btd, ld, use_graph=True, stream=s)
+            for _ in range(4):
+                g.replay()
+                torch.cuda.synchronize()
+                seq.append(int(to_host(tok)[0]))
+        outs.append((seq, int(to_host(ld)[0])))
+        m.close()
+    assert outs[0] == outs[1]
+    assert outs[0][1] == int(lens[0]) + 4
