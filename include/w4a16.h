@@ -92,8 +92,10 @@ W4A16_API int w4a16_version(void);
  *   bias     fp16 [N] or NULL
  *   residual fp16 [M][N] or NULL      added before the single fp16 rounding
  *   y        fp16 [M][N]              output (must not alias x)
- * Shapes: 1 <= M <= 32, K % 128 == 0, N >= 1.  M <= 4 with M*K <= 49152
- * runs on the CUDA cores; larger M on the tensor cores (see w4a16_gemm).
+ * Shapes: 1 <= M <= 32, K % 128 == 0, N >= 1.  M <= 4 runs on the CUDA
+ * cores (rows whose activations exceed 49152 elements together go in
+ * launches of floor(49152 / K) rows, each streaming the weights); larger M
+ * on the tensor cores (see w4a16_gemm).
  * ------------------------------------------------------------------------ */
 W4A16_API int w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qweight, const uint16_t* scales,
                int N, const uint16_t* bias, const uint16_t* residual, uint16_t* y,

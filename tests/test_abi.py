@@ -67,7 +67,7 @@ def test_gemv_rejects_bad_shapes_and_alignment(lib):
     rc = lib.w4a16_gemv(ALIGNED, 0, 128, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
     assert rc == 1
     rc = lib.w4a16_gemv(ALIGNED, 64, 4096, ALIGNED, ALIGNED, 8, None, None, ALIGNED, None)
-    assert rc == 3  # outside the CUDA-core path (M*K too large)
+    assert rc == 3  # M = 64: above the largest batch (32)
     with pytest.raises(_lib.W4A16Error):
         _lib.check(rc)
 
