@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -47,6 +48,8 @@ def parse():
                     choices=["gateup", "down", "qkv", "o", "attention", "lm_head"],
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
+    ap.add_argument("--clock-log", default=None,
+                    help="CSV of the nvidia-smi clock samples taken during the timed region (default: temp dir)")
     ap.add_argument("--workload", default="b1", choices=["b1", "b32"],
                     help="b1: 28-layer b=1 ctx-512 decode; b32: 28-layer batched decode, 32 sequences of "
                          "U[1,4096] tokens in a 16384-page pool")
@@ -118,10 +121,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id):
+    def __init__(self, gpu_id, path=None):
         self.gpu_id = gpu_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"w4a16_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -474,7 +477,7 @@ def main():
         barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(gpu_uuid(torch, dev)) as clk:
+        with ClockSampler(gpu_uuid(torch, dev), args.clock_log) as clk:
             e0.record(stream)
             for _ in range(K):
                 model.decode_step(tok, tok, bt, lens, use_graph=True)
