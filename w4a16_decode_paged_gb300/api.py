@@ -27,24 +27,75 @@ def _p(t):
     return None if t is None else t.data_ptr()
 
 
-def _need(t, dtypes, name):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _on_device(t) -> bool:
+    return t.is_cuda
+
+
+def _arg(t, dtypes, name, shape=None, optional=False):
+    """Check one tensor argument before its pointer goes to the library:
+    dtype, contiguity, shape (entries None match any extent) and device.
+    The library only sees pointers and sizes, so a wrong extent here would
+    become an out-of-bounds access on the GPU."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
     if t.dtype not in dtypes:
         raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(e is not None and t.shape[i] != e for i, e in enumerate(shape))):
+        want = tuple("*" if e is None else e for e in shape)
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {want}")
+    if not _on_device(t):
+        raise ValueError(f"{name} must be a CUDA tensor")
 
 
 _H = (torch.float16,)
 _W = (torch.int32, torch.uint32)
 _I = (torch.int32,)
+_F = (torch.float32,)
+_U8 = (torch.uint8,)
+
+
+def _xk(x):
+    """(M, K) of the activations x [M][K] (fp16)."""
+    _arg(x, _H, "x")
+    if x.dim() != 2:
+        raise ValueError(f"x: shape {tuple(x.shape)}, expected (M, K)")
+    return x.shape[0], x.shape[1]
+
+
+def _paging(k_pool, v_pool, block_table, context_lens):
+    """(pages, Hkv, D, B) of pools [pages][Hkv][16][D], a block table
+    [B][max_blocks] and context_lens [B]."""
+    _arg(k_pool, _H, "k_pool", (None, None, 16, None))
+    pages, Hkv, _, D = k_pool.shape
+    _arg(v_pool, _H, "v_pool", tuple(k_pool.shape))
+    _arg(block_table, _I, "block_table", (None, None))
+    B = block_table.shape[0]
+    _arg(context_lens, _I, "context_lens", (B,))
+    return pages, Hkv, D, B
+
+
+def _int4(qweight, scales, K, name="qweight", sname="scales"):
+    """N of a packed int4 matrix qweight [N][K/8] with scales [N][K/128]."""
+    _arg(qweight, _W, name)
+    if qweight.dim() != 2:
+        raise ValueError(f"{name}: shape {tuple(qweight.shape)}, expected (N, {K // 8})")
+    N = qweight.shape[0]
+    _arg(qweight, _W, name, (N, K // 8))
+    _arg(scales, _H, sname, (N, K // 128))
+    return N
 
 
 def w4a16_gemv(x, qweight, scales, bias=None, residual=None, out=None, stream=None):
-    _need(x, _H, "x"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
-    M, K = x.shape
-    N = qweight.shape[0]
+    M, K = _xk(x)
+    N = _int4(qweight, scales, K)
+    _arg(bias, _H, "bias", (N,), optional=True)
+    _arg(residual, _H, "residual", (M, N), optional=True)
+    _arg(out, _H, "out", (M, N), optional=True)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     check(load().w4a16_gemv(_p(x), M, K, _p(qweight), _p(scales), N, _p(bias), _p(residual), _p(out),
@@ -54,9 +105,12 @@ def w4a16_gemv(x, qweight, scales, bias=None, residual=None, out=None, stream=No
 
 def w4a16_gemm(x, qweight, scales, bias=None, residual=None, out=None, workspace=None, split=True, stream=None):
     """Tensor-core path for a decode batch (M <= 32)."""
-    _need(x, _H, "x"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
-    M, K = x.shape
-    N = qweight.shape[0]
+    M, K = _xk(x)
+    N = _int4(qweight, scales, K)
+    _arg(bias, _H, "bias", (N,), optional=True)
+    _arg(residual, _H, "residual", (M, N), optional=True)
+    _arg(out, _H, "out", (M, N), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
     lib = load()
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
@@ -70,9 +124,13 @@ def w4a16_gemm(x, qweight, scales, bias=None, residual=None, out=None, workspace
 
 def w4a16_gemm_silu_mul(x, qweight_gate, scales_gate, qweight_up, scales_up, out=None, workspace=None, split=True,
                         stream=None):
-    _need(x, _H, "x")
-    M, K = x.shape
-    N = qweight_gate.shape[0]
+    M, K = _xk(x)
+    N = _int4(qweight_gate, scales_gate, K, "qweight_gate", "scales_gate")
+    _int4(qweight_up, scales_up, K, "qweight_up", "scales_up")
+    if qweight_up.shape[0] != N:
+        raise ValueError(f"qweight_up: {qweight_up.shape[0]} rows, qweight_gate {N}")
+    _arg(out, _H, "out", (M, N), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
     lib = load()
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
@@ -86,8 +144,10 @@ def w4a16_gemm_silu_mul(x, qweight_gate, scales_gate, qweight_up, scales_up, out
 
 
 def lm_head_logits_batched(x, lm_head, out=None, stream=None):
-    B, H = x.shape
+    B, H = _xk(x)
+    _arg(lm_head, _H, "lm_head", (None, H))
     V = lm_head.shape[0]
+    _arg(out, _F, "out", (B, V), optional=True)
     if out is None:
         out = torch.empty((B, V), dtype=torch.float32, device=x.device)
     check(load().lm_head_logits_batched(_p(x), B, H, _p(lm_head), V, _p(out), stream_handle(stream)))
@@ -95,7 +155,10 @@ def lm_head_logits_batched(x, lm_head, out=None, stream=None):
 
 
 def argmax_rows(logits32, tokens_out=None, logits16=None, stream=None):
+    _arg(logits32, _F, "logits32", (None, None))
     B, V = logits32.shape
+    _arg(tokens_out, _I, "tokens_out", (B,), optional=True)
+    _arg(logits16, _H, "logits16", (B, V), optional=True)
     if tokens_out is None:
         tokens_out = torch.empty(B, dtype=torch.int32, device=logits32.device)
     check(load().argmax_rows(_p(logits32), B, V, _p(tokens_out), _p(logits16), stream_handle(stream)))
@@ -103,9 +166,11 @@ def argmax_rows(logits32, tokens_out=None, logits16=None, stream=None):
 
 
 def w4a16_gemv_rmsnorm(x, gamma, eps, qweight, scales, bias=None, out=None, stream=None):
-    _need(x, _H, "x"); _need(gamma, _H, "gamma"); _need(qweight, _W, "qweight"); _need(scales, _H, "scales")
-    M, K = x.shape
-    N = qweight.shape[0]
+    M, K = _xk(x)
+    _arg(gamma, _H, "gamma", (K,))
+    N = _int4(qweight, scales, K)
+    _arg(bias, _H, "bias", (N,), optional=True)
+    _arg(out, _H, "out", (M, N), optional=True)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     check(load().w4a16_gemv_rmsnorm(_p(x), _p(gamma), float(eps), M, K, _p(qweight), _p(scales), N, _p(bias),
@@ -114,9 +179,13 @@ def w4a16_gemv_rmsnorm(x, gamma, eps, qweight, scales, bias=None, out=None, stre
 
 
 def w4a16_gemv_silu_mul(x, gamma, eps, qweight_gate, scales_gate, qweight_up, scales_up, out=None, stream=None):
-    _need(x, _H, "x")
-    M, K = x.shape
-    N = qweight_gate.shape[0]
+    M, K = _xk(x)
+    _arg(gamma, _H, "gamma", (K,), optional=True)
+    N = _int4(qweight_gate, scales_gate, K, "qweight_gate", "scales_gate")
+    _int4(qweight_up, scales_up, K, "qweight_up", "scales_up")
+    if qweight_up.shape[0] != N:
+        raise ValueError(f"qweight_up: {qweight_up.shape[0]} rows, qweight_gate {N}")
+    _arg(out, _H, "out", (M, N), optional=True)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     check(load().w4a16_gemv_silu_mul(_p(x), _p(gamma), float(eps), M, K, _p(qweight_gate), _p(scales_gate),
@@ -125,8 +194,9 @@ def w4a16_gemv_silu_mul(x, gamma, eps, qweight_gate, scales_gate, qweight_up, sc
 
 
 def rmsnorm(x, gamma, eps, out=None, stream=None):
-    _need(x, _H, "x"); _need(gamma, _H, "gamma")
-    M, H = x.shape
+    M, H = _xk(x)
+    _arg(gamma, _H, "gamma", (H,))
+    _arg(out, _H, "out", (M, H), optional=True)
     if out is None:
         out = torch.empty_like(x)
     check(load().rmsnorm(_p(x), _p(gamma), _p(out), M, H, float(eps), stream_handle(stream)))
@@ -136,10 +206,8 @@ def rmsnorm(x, gamma, eps, out=None, stream=None):
 def kv_append_rope(q, k, v, k_pool, v_pool, block_table, context_lens, theta, row_stride=0, err_flag=None,
                    n_q_heads=None, n_kv_heads=None, stream=None):
     """q [B][Hq][D] (rotated in place), k/v [B][Hkv][D]; pools [pages][Hkv][16][D]."""
-    _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
-    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
-    pages, Hkv, _, D = k_pool.shape
-    B = block_table.shape[0]
+    pages, Hkv, D, B = _paging(k_pool, v_pool, block_table, context_lens)
+    _arg(err_flag, _I, "err_flag", optional=True)
     Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
     if n_kv_heads is not None:
         Hkv = n_kv_heads
@@ -164,11 +232,14 @@ def workspace_clear(ws, stream=None):
 def paged_gqa_decode(q, k_pool, v_pool, block_table, context_lens, max_context, sm_scale=None, partition_tokens=0,
                      workspace=None, out=None, err_flag=None, q_stride=0, n_q_heads=None, stream=None):
     """q [B][Hq][D] (or rows of pitch q_stride); returns out [B][Hq][D]."""
-    _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
-    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
-    pages, Hkv, _, D = k_pool.shape
-    B = block_table.shape[0]
+    pages, Hkv, D, B = _paging(k_pool, v_pool, block_table, context_lens)
+    _arg(q, _H, "q")
     Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
+    if q.numel() < (B - 1) * (q_stride or Hq * D) + Hq * D:
+        raise ValueError(f"q: {q.numel()} elements, too few for {B} rows of {Hq}x{D} at pitch {q_stride or Hq * D}")
+    _arg(out, _H, "out", (B, Hq, D), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
+    _arg(err_flag, _I, "err_flag", optional=True)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     lib = load()
@@ -189,11 +260,14 @@ def paged_gqa_decode_rope_append(qkv, k_pool, v_pool, block_table, context_lens,
                                  sm_scale=None, partition_tokens=0, workspace=None, out=None, err_flag=None,
                                  stream=None):
     """qkv rows [B][(Hq + 2 Hkv) D] (q | k_new | v_new); appends and attends."""
-    _need(qkv, _H, "qkv"); _need(k_pool, _H, "k_pool"); _need(v_pool, _H, "v_pool")
-    _need(block_table, _I, "block_table"); _need(context_lens, _I, "context_lens")
-    pages, Hkv, _, D = k_pool.shape
-    B = block_table.shape[0]
+    pages, Hkv, D, B = _paging(k_pool, v_pool, block_table, context_lens)
     Hq = n_q_heads
+    _arg(qkv, _H, "qkv", (B, None))
+    if qkv.shape[1] < (Hq + 2 * Hkv) * D:
+        raise ValueError(f"qkv: rows of {qkv.shape[1]}, need (Hq + 2 Hkv) D = {(Hq + 2 * Hkv) * D}")
+    _arg(out, _H, "out", (B, Hq, D), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
+    _arg(err_flag, _I, "err_flag", optional=True)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     lib = load()
@@ -212,8 +286,12 @@ def paged_gqa_decode_rope_append(qkv, k_pool, v_pool, block_table, context_lens,
 
 
 def embedding_gather(embed, tokens, out=None, err_flag=None, stream=None):
+    _arg(embed, _H, "embed", (None, None))
     vocab, H = embed.shape
+    _arg(tokens, _I, "tokens")
     B = tokens.numel()
+    _arg(out, _H, "out", (B, H), optional=True)
+    _arg(err_flag, _I, "err_flag", optional=True)
     if out is None:
         out = torch.empty((B, H), dtype=torch.float16, device=embed.device)
     check(load().embedding_gather(_p(embed), vocab, H, _p(tokens), B, _p(out), _p(err_flag),
@@ -222,8 +300,12 @@ def embedding_gather(embed, tokens, out=None, err_flag=None, stream=None):
 
 
 def lm_head_argmax(x, lm_head, logits=None, tokens_out=None, workspace=None, want_logits=False, stream=None):
-    B, H = x.shape
+    B, H = _xk(x)
+    _arg(lm_head, _H, "lm_head", (None, H))
     vocab = lm_head.shape[0]
+    _arg(logits, _H, "logits", (B, vocab), optional=True)
+    _arg(tokens_out, _I, "tokens_out", (B,), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
     lib = load()
     if workspace is None:
         workspace = torch.zeros(lib.lm_head_argmax_workspace_size(B, vocab), dtype=torch.uint8, device=x.device)
