@@ -158,3 +158,34 @@ def test_host_tensors_are_refused(monkeypatch):
     monkeypatch.setattr(api, "load", lambda: _Recorder())
     with pytest.raises(ValueError, match="CUDA"):
         api.w4a16_gemv(h(1, 128), i32(8, 16), h(8, 1))
+
+
+def _tiny_model(lib):
+    cfg = dict(hidden=128, n_q_heads=7, n_kv_heads=1, head_dim=128, inter=256, vocab=50, eps=1e-6, theta=1e6)
+    pool = h(8, 1, 16, 128)
+    layer = {k: h(1) for k in api.Model.LAYER_KEYS}
+    layer.update(k_pool=pool, v_pool=pool)
+    return api.Model(cfg, [layer], embed=h(50, 128), final_norm=h(128), lm_head=h(50, 128), max_batch=2,
+                     max_context=64, num_pages=8)
+
+
+def test_model_step_and_layer_arguments(lib):
+    m = _tiny_model(lib)
+    tok, bt, lens = i32(2), i32(2, 4), i32(2)
+    m.decode_step(tok, tok, bt, lens, logits=h(2, 50))
+    a = last(lib, "decode_step")
+    assert (a[4], a[6]) == (4, 2)                     # max_blocks, B
+    with pytest.raises(ValueError, match="logits"):
+        m.decode_step(tok, tok, bt, lens, logits=h(2, 49))
+    with pytest.raises(ValueError, match="context_lens"):
+        m.decode_step(tok, tok, bt, i32(1))
+    with pytest.raises(ValueError, match="block_table"):
+        m.decode_step(tok, tok, i32(1, 4), lens)
+    with pytest.raises(ValueError, match="tokens_out"):
+        m.decode_step(tok, i32(3), bt, lens)
+    with pytest.raises(ValueError, match="tokens_in"):
+        m.decode_step(torch.zeros(2, dtype=torch.int64), tok, bt, lens)
+    m.layer(0, h(2, 128), bt, lens)
+    with pytest.raises(ValueError, match="x"):
+        m.layer(0, h(2, 64), bt, lens)
+    m.close()

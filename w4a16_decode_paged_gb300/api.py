@@ -388,13 +388,24 @@ class Model:
         """Status code of the device error word (blocks; clears the word)."""
         return int(self._lib.w4a16_model_check_errors(self._h, stream_handle(stream)))
 
+    def _paging_args(self, B, block_table, context_lens):
+        _arg(block_table, _I, "block_table", (B, None))
+        _arg(context_lens, _I, "context_lens", (B,))
+
     def layer(self, i, x, block_table, context_lens, stream=None):
+        _arg(x, _H, "x", (None, self.cfg["hidden"]))
+        self._paging_args(x.shape[0], block_table, context_lens)
         check(self._lib.w4a16_model_layer(self._h, int(i), _p(x), _p(block_table), block_table.shape[1],
                                           _p(context_lens), x.shape[0], stream_handle(stream)))
         return x
 
     def decode_step(self, tokens_in, tokens_out, block_table, context_lens, logits=None, use_graph=True,
                     stream=None):
+        _arg(tokens_in, _I, "tokens_in")
+        B = tokens_in.numel()
+        _arg(tokens_out, _I, "tokens_out", tuple(tokens_in.shape))
+        self._paging_args(B, block_table, context_lens)
+        _arg(logits, _H, "logits", (B, self.cfg.get("vocab", 0)), optional=True)
         check(self._lib.decode_step(self._h, _p(tokens_in), _p(tokens_out), _p(block_table), block_table.shape[1],
                                     _p(context_lens), tokens_in.numel(), _p(logits), int(bool(use_graph)),
                                     stream_handle(stream)))
