@@ -116,3 +116,55 @@ def test_model_create_rejects_bad_config(lib):
     c = _lib.ModelConfig(896, 7, 1, 128, 2432, 1, 0, 1e-6, 1e6, 8, 0)
     assert lib.w4a16_model_create(ctypes.byref(c), ctypes.byref(w), 1, 64, ctypes.byref(h)) == 1
     assert not h.value
+
+
+def test_tensor_core_calls_reject(lib):
+    # w4a16_gemm(x, M, K, qweight, scales, N, bias, residual, y, workspace, bytes, stream)
+    good = [ALIGNED, 8, 256, ALIGNED, ALIGNED, 128, None, None, ALIGNED, None, 0, None]
+    for i, v, rc in ((1, 33, 3), (2, 200, 3), (0, None, 1), (3, None, 1), (0, MISALIGNED, 2),
+                     (8, MISALIGNED, 2), (9, MISALIGNED, 2), (7, MISALIGNED, 2), (1, 0, 1)):
+        a = list(good); a[i] = v
+        assert lib.w4a16_gemm(*a) == rc, (i, v)
+    # w4a16_gemm_silu_mul(x, M, K, qg, sg, qu, su, N, y, workspace, bytes, stream)
+    good = [ALIGNED, 8, 256, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 128, ALIGNED, None, 0, None]
+    for i, v, rc in ((5, None, 1), (6, MISALIGNED, 2), (1, 40, 3), (2, 130, 3)):
+        a = list(good); a[i] = v
+        assert lib.w4a16_gemm_silu_mul(*a) == rc, (i, v)
+    assert lib.w4a16_gemm_workspace_size(8, 64, 128, 0) == 0      # K below one scale group
+    assert lib.w4a16_gemm_workspace_size(32, 18944, 3584, 0) > 8192  # split K: tickets + partial tiles
+    # lm_head_logits_batched(x, B, H, lm_head, vocab, logits, stream)
+    assert lib.lm_head_logits_batched(ALIGNED, 33, 896, ALIGNED, 1000, ALIGNED, None) == 3
+    assert lib.lm_head_logits_batched(ALIGNED, 8, 900, ALIGNED, 1000, ALIGNED, None) == 3
+    assert lib.lm_head_logits_batched(ALIGNED, 8, 896, ALIGNED, 1000, MISALIGNED, None) == 2
+    assert lib.lm_head_logits_batched(ALIGNED, 8, 896, None, 1000, ALIGNED, None) == 1
+    # argmax_rows(logits, B, vocab, tokens, logits16, stream)
+    assert lib.argmax_rows(None, 2, 10, ALIGNED, None, None) == 1
+    assert lib.argmax_rows(ALIGNED, 0, 10, ALIGNED, None, None) == 1
+
+
+def test_fused_gemv_and_gather_calls_reject(lib):
+    # w4a16_gemv_rmsnorm(x, gamma, eps, M, K, qweight, scales, N, bias, y, stream)
+    good = [ALIGNED, ALIGNED, 1e-6, 1, 256, ALIGNED, ALIGNED, 64, None, ALIGNED, None]
+    for i, v, rc in ((1, None, 1), (2, -1.0, 1), (4, 200, 3), (1, MISALIGNED, 2), (9, MISALIGNED, 2)):
+        a = list(good); a[i] = v
+        assert lib.w4a16_gemv_rmsnorm(*a) == rc, (i, v)
+    # w4a16_gemv_silu_mul(x, gamma, eps, M, K, qg, sg, qu, su, N, y, stream)
+    good = [ALIGNED, None, 1e-6, 1, 256, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 64, ALIGNED, None]
+    for i, v, rc in ((7, None, 1), (2, -1.0, 1), (5, MISALIGNED, 2), (4, 100, 3)):
+        a = list(good); a[i] = v
+        assert lib.w4a16_gemv_silu_mul(*a) == rc, (i, v)
+    # embedding_gather(embed, vocab, H, tokens, B, x, err_flag, stream)
+    assert lib.embedding_gather(ALIGNED, 100, 12, ALIGNED, 1, ALIGNED, None, None) == 3
+    assert lib.embedding_gather(None, 100, 16, ALIGNED, 1, ALIGNED, None, None) == 1
+    assert lib.embedding_gather(ALIGNED, 100, 16, ALIGNED, 0, ALIGNED, None, None) == 1
+    assert lib.embedding_gather(MISALIGNED, 100, 16, ALIGNED, 1, ALIGNED, None, None) == 2
+
+
+def test_model_calls_reject_a_null_model(lib):
+    assert lib.decode_step(None, ALIGNED, ALIGNED, ALIGNED, 4, ALIGNED, 1, None, 1, None) == 1
+    assert lib.w4a16_model_layer(None, 0, ALIGNED, ALIGNED, 4, ALIGNED, 1, None) == 1
+    assert lib.w4a16_model_hidden(None, ALIGNED, 1, None) == 1
+    assert lib.w4a16_model_activation(None, 0, ALIGNED, 1, None) == 1
+    assert lib.w4a16_model_check_errors(None, None) == 1
+    assert lib.decode_step_kernel_count(None, 1) == 0
+    assert b"null" in lib.w4a16_last_error()
