@@ -398,3 +398,53 @@ def test_decode_step_zero_layers_is_norm_lm_head_argmax():
         ref = orc.fp16_gemv(orc.rmsnorm(embed[t], fn, cfg["eps"])[0], lm)
         assert out[b] == int(np.argmax(ref))
         assert np.array_equal(logits[b], ref.astype(np.float16))
+
+
+def test_decoder_layer_with_bias_and_two_sequences():
+    """The composition pin again with the q/k/v biases on and two sequences
+    whose new tokens land at a page's last slot (L = 16) and first slot
+    (L = 17), each sequence composed on its own."""
+    cfg = dict(synth.TINY_LAYER, bias=True, batch=2, pool_pages=8)
+    c = synth.layer_case(cfg, lens=[16, 17], seed=1010)
+    w = c["weights"]
+    assert w["bq"] is not None and np.any(w["bq"] != 0)
+    Hq, Hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    kp1, vp1 = c["k_pool"].copy(), c["v_pool"].copy()
+    out = orc.decoder_layer(cfg, w, c["x"], kp1, vp1, c["block_table"], c["context_lens"])
+    kp2, vp2 = c["k_pool"].copy(), c["v_pool"].copy()
+    for b in range(2):
+        L = int(c["context_lens"][b])
+        bt, lens = c["block_table"][b:b + 1], c["context_lens"][b:b + 1]
+        xn = orc.rmsnorm(c["x"][b:b + 1], w["ln1"], cfg["eps"])
+        q = orc.rope(orc.w4a16_gemv(xn, w["wq"], w["sq"], bias=w["bq"]).reshape(Hq, D), L - 1, cfg["theta"])
+        k = orc.rope(orc.w4a16_gemv(xn, w["wk"], w["sk"], bias=w["bk"]).reshape(Hkv, D), L - 1, cfg["theta"])
+        v = orc.w4a16_gemv(xn, w["wv"], w["sv"], bias=w["bv"]).reshape(Hkv, D)
+        orc.kv_append(k[None], v[None], kp2, vp2, bt, lens)
+        att = orc.paged_attention(q[None], kp2, vp2, bt, lens, 1 / math.sqrt(D))
+        h = orc.w4a16_gemv(att.reshape(1, Hq * D), w["wo"], w["so"], residual=c["x"][b:b + 1])
+        hn = orc.rmsnorm(h, w["ln2"], cfg["eps"])
+        m = orc.silu_mul(orc.w4a16_gemv(hn, w["wg"], w["sg"]), orc.w4a16_gemv(hn, w["wu"], w["su"]))
+        ref = orc.w4a16_gemv(m, w["wd"], w["sd"], residual=h)
+        assert np.array_equal(out[b], ref[0]), f"sequence {b}"
+    assert np.array_equal(kp1, kp2) and np.array_equal(vp1, vp2)
+    # the biases matter: without them the layer output differs
+    w0 = dict(w, bq=None, bk=None, bv=None)
+    out0 = orc.decoder_layer(cfg, w0, c["x"], c["k_pool"].copy(), c["v_pool"].copy(), c["block_table"],
+                             c["context_lens"])
+    assert not np.array_equal(out0, out)
+
+
+def test_decode_step_one_layer_is_embedding_layer_norm_lm_head_argmax():
+    cfg = dict(synth.TINY_LAYER, vocab=97, n_layers=1)
+    case = synth.model_case(cfg, lens=[20, 31], gen_tokens=2, pool_pages=8, seed=1020)
+    lens = case["lens"] + 1                                  # counts after this step's append
+    kp, vp = synth.host_pool(case, 0, "k"), synth.host_pool(case, 0, "v")
+    toks, logits, hidden = orc.decode_step(cfg, case["layers"], [kp.copy()], [vp.copy()], case["embed"],
+                                           case["fnorm"], case["lm"], case["tok"], case["bt"], lens,
+                                           want_logits=True)
+    x = orc.decoder_layer(cfg, case["layers"][0], case["embed"][case["tok"]], kp, vp, case["bt"], lens)
+    assert np.array_equal(hidden, x)
+    for b in range(2):
+        ref = orc.fp16_gemv(orc.rmsnorm(x[b], case["fnorm"], cfg["eps"])[0], case["lm"])
+        assert np.array_equal(logits[b], ref.astype(np.float16))
+        assert toks[b] == orc.argmax(ref)
