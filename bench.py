@@ -20,7 +20,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -49,7 +48,7 @@ def parse():
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
     ap.add_argument("--clock-log", default=None,
-                    help="CSV of the nvidia-smi clock samples taken during the timed region (default: temp dir)")
+                    help="write the raw nvidia-smi clock samples of the timed region to this CSV file")
     ap.add_argument("--workload", default="b1", choices=["b1", "b32"],
                     help="b1: 28-layer b=1 ctx-512 decode; b32: 28-layer batched decode, 32 sequences of "
                          "U[1,4096] tokens in a 16384-page pool")
@@ -117,44 +116,55 @@ def step_bytes(cfg, lens):
 # ---------------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock, power and throttle
+    reasons while the timed region runs, read from its stdout; `path`, if
+    given, receives a copy of the raw CSV lines."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_id, path=None):
+    def __init__(self, gpu_id, path=None, command=None):
         self.gpu_id = gpu_id
+        self.path = path
         self.proc = None
-        self.path = path or os.path.join(tempfile.gettempdir(), f"w4a16_clocks_{os.getpid()}.csv")
+        self.lines = []
+        cmd = command or ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if command is None and gpu_id is not None:
+            cmd += ["-i", str(gpu_id)]
+        self.cmd = cmd
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
-            if self.gpu_id is not None:
-                cmd += ["-i", str(self.gpu_id)]
-            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            time.sleep(0.25)
-            self.proc.terminate()
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = (out or "").splitlines()
+        if self.path:
             try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
+                with open(self.path, "w") as f:
+                    f.write("\n".join(self.lines) + "\n")
+            except OSError:
+                pass
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -163,7 +173,7 @@ class ClockSampler:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(self.REASONS, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,

@@ -115,3 +115,28 @@ def test_bench_bytes_equal_the_arrays_a_step_touches():
     assert bench.step_bytes(cfg, [L]) == 28 * (weights + act + att) + cfg["vocab"] * H * 2 + H * 2
     # the b=1 figure quoted with the roofline: about 4.49 GB per token
     assert abs(bench.step_bytes(cfg, [L]) / 1e9 - 4.49) < 0.01
+
+
+def test_clock_sampler_reads_samples_from_the_pipe():
+    """bench.ClockSampler against a stand-in for nvidia-smi that prints two
+    kinds of CSV samples: median SM clock, max clock and the active throttle
+    reasons, from the lines read off its stdout."""
+    import time
+
+    import bench
+    line_a = "0, 2070, 2070, 812.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active"
+    line_b = "0, 1980, 2070, 990.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+    script = f'while true; do echo "{line_a}"; echo "{line_b}"; echo "{line_a}"; sleep 0.05; done'
+    with bench.ClockSampler(0, command=["sh", "-c", script]) as clk:
+        time.sleep(0.3)
+    s = clk.summary()
+    assert s["samples"] >= 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert clk.lines[0] == line_a
+
+
+def test_clock_sampler_without_nvidia_smi():
+    import bench
+    with bench.ClockSampler(0, command=["/nonexistent/nvidia-smi"]) as clk:
+        pass
+    assert clk.summary()["reasons"] == ["unavailable"]
