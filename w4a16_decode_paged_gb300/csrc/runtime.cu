@@ -455,7 +455,7 @@ extern __device__ unsigned int g_trace_cap;
 extern __device__ unsigned int g_trace_n;
 }
 // Kernel timeline (trace builds only): start recording into a device buffer
-// of `cap` records of 32 bytes; w4a16_trace_count returns how many were
+// of `cap` records of 64 bytes; w4a16_trace_count returns how many were
 // written (synchronises the device).
 extern "C" W4A16_API int w4a16_trace_start(void* dev_buf, unsigned int cap) {
   unsigned int zero = 0;
