@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(LM_WPB * 32) lm_head_kernel(const __grid_const
 }
 
 size_t lm_head_workspace_bytes(int B, int vocab) {
+  (void)B;  // one fixed block: partial keys of up to LM_MAXB rows x LM_MAX_BLOCKS CTAs + counters
   (void)vocab;
   return (size_t)LM_MAXB * LM_MAX_BLOCKS * 8 + 256;
 }
