@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
                 "orc_half_to_double_array": (None, [_P, i64, _P]),
                 "orc_double_to_half_array": (None, [_P, i64, _P]),
                 "orc_num_threads": (i32, []),
+                "orc_set_num_threads": (None, [i32]),
                 "orc_unpack_code": (i32, [ctypes.c_uint32, i32]),
                 "orc_pack_int4": (None, [_P, i64, i64, _P]),
                 "orc_unpack_int4": (None, [_P, i64, i64, _P]),
@@ -83,6 +84,12 @@ def lib() -> ctypes.CDLL:
                 "orc_paged_attention": (None, [_P, _P, _P, _P, i32, _P, i32, i32, i32, i32, dbl, _P]),
                 "orc_attention_split_combine": (None, [_P, _P, _P, i32, i32, i32, i32, dbl, i32, i32, _P]),
                 "orc_silu_mul": (None, [_P, _P, i64, _P]),
+                "orc_e4m3_to_double": (dbl, [ctypes.c_uint8]),
+                "orc_float_to_e4m3": (ctypes.c_uint8, [ctypes.c_float]),
+                "orc_fp8_quantize_row": (None, [_P, i32, _P, _P]),
+                "orc_kv_append_fp8": (None, [_P, _P, _P, _P, _P, _P, _P, i32, _P, i32, i32, i32]),
+                "orc_paged_attention_fp8": (None, [_P, _P, _P, _P, _P, _P, i32, _P, i32, i32, i32, i32, dbl,
+                                                   _P]),
                 "orc_decoder_layer": (None, [ctypes.POINTER(Config), ctypes.POINTER(Layer), _P, _P, i32, _P, i32]),
                 "orc_decode_step": (None, [ctypes.POINTER(Config), ctypes.POINTER(Layer), i32, _P, _P, _P,
                                            _P, _P, i32, _P, i32, _P, _P, _P]),
@@ -109,6 +116,12 @@ def _ptr(a):
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (for timing it on
+    one core and on all host cores)."""
+    lib().orc_set_num_threads(int(n))
 
 
 def half_to_double(h: np.ndarray) -> np.ndarray:
@@ -268,6 +281,53 @@ def attention_split_combine(q, k, v, scale, h: int, part: int):
     L, Hkv, _ = k.shape
     out = np.empty(D, np.float64)
     lib().orc_attention_split_combine(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, D, L, scale, h, part, _ptr(out))
+    return out
+
+
+def e4m3_to_double(code: int) -> float:
+    """Value of one FP8 E4M3 code (NaN for S.1111.111)."""
+    return lib().orc_e4m3_to_double(int(code) & 0xFF)
+
+
+def float_to_e4m3(f: float) -> int:
+    """E4M3 code of an fp32 value: round to nearest even, saturating at 448."""
+    return int(lib().orc_float_to_e4m3(float(f)))
+
+
+def fp8_quantize_row(x):
+    """(codes uint8 [D], fp32 scale) of one fp16 row: the row's largest
+    magnitude maps to 448."""
+    x = _c(x, np.float16).ravel()
+    codes = np.empty(x.size, np.uint8)
+    sc = np.zeros(1, np.float32)
+    lib().orc_fp8_quantize_row(_ptr(x), x.size, _ptr(codes), _ptr(sc))
+    return codes, float(sc[0])
+
+
+def kv_append_fp8(k, v, k_pool, v_pool, k_scale, v_scale, block_table, context_lens):
+    """In place: quantise k[b], v[b] ([B][Hkv][D] fp16, k already rotated)
+    into slot context_lens[b]-1 of the FP8 pools ([pages][Hkv][16][D] uint8)
+    and their fp32 row scales ([pages][Hkv][16])."""
+    k, v = _c(k, np.float16), _c(v, np.float16)
+    for a, dt in ((k_pool, np.uint8), (v_pool, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    block_table, context_lens = _c(block_table, np.int32), _c(context_lens, np.int32)
+    B, Hkv, D = k.shape
+    lib().orc_kv_append_fp8(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                            _ptr(block_table), block_table.shape[1], _ptr(context_lens), B, Hkv, D)
+
+
+def paged_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, context_lens, scale):
+    q = _c(q, np.float16)
+    k_pool, v_pool = _c(k_pool, np.uint8), _c(v_pool, np.uint8)
+    k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    block_table, context_lens = _c(block_table, np.int32), _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    out = np.empty((B, Hq, D), np.float16)
+    lib().orc_paged_attention_fp8(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                  _ptr(block_table), block_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D,
+                                  scale, _ptr(out))
     return out
 
 

@@ -130,6 +130,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads later parallel loops use (timing on one core or on all of them). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* INT4 format ([RU] "symmetric group-wise INT4 (group 128)").              */
 /* ------------------------------------------------------------------------ */
@@ -398,6 +407,145 @@ void orc_paged_attention(const uint16_t* q, const uint16_t* k_pool, const uint16
                   out + (int64_t)b * Hq * D);
     free(kc);
     free(vc);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 KV pages.  [EN] "1. Weight Packing and FP8 Utilization" (twin: [ZH]   */
+/* "1. 权重打包（Weight Packing）与 FP8 利用"): FP8 values need scaling        */
+/* factors; E4M3 is one of the two FP8 formats it names.  Reading taken     */
+/* here (the page gives no granularity): one fp32 scale per (page, kv head, */
+/* token) row, chosen so the row's largest magnitude maps to 448 (the       */
+/* largest finite E4M3 value); the pools hold the codes, [pages][Hkv][16][D] */
+/* uint8, beside fp32 scales [pages][Hkv][16].                              */
+/*                                                                          */
+/* E4M3 ("fn" variant, no infinities): 1 sign bit, 4 exponent bits (bias   */
+/* 7), 3 fraction bits; exponent field 0 is subnormal, fraction * 2^-9;     */
+/* S.1111.111 is NaN; the largest finite value is 1.75 * 2^8 = 448.         */
+/* ------------------------------------------------------------------------ */
+
+double orc_e4m3_to_double(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int expo = (c >> 3) & 0xf;
+  int frac = c & 0x7;
+  double v;
+  if (expo == 15 && frac == 7) return NAN;
+  if (expo == 0) {
+    v = ldexp((double)frac, -9);
+  } else {
+    v = ldexp((double)(8 + frac), expo - 10);
+  }
+  return sign ? -v : v;
+}
+
+/* Round-to-nearest-even encoding of an fp32 value; magnitudes past 448
+ * saturate to 448 (no NaN for a finite input). */
+uint8_t orc_float_to_e4m3(float f) {
+  if (isnan(f)) return 0x7f;
+  uint8_t sign = signbit(f) ? 0x80 : 0;
+  double a = fabs((double)f);
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: integer multiple of 2^-9, ties to even; 8 is the
+     * smallest normal (exponent field 1, fraction 0) */
+    double q = nearbyint(ldexp(a, 9));
+    return sign | (uint8_t)q;
+  }
+  int e;
+  (void)frexp(a, &e);           /* a = f * 2^e, f in [0.5, 1) */
+  int E = e - 1;                /* a = m * 2^E, m in [1, 2) */
+  double m = nearbyint(ldexp(a, 3 - E)); /* in [8, 16] */
+  if (m == 16.0) {
+    m = 8.0;
+    E += 1;
+  }
+  if (E > 8 || (E == 8 && m > 14.0)) return sign | 0x7e; /* 448 */
+  return sign | (uint8_t)((E + 7) << 3) | (uint8_t)((int)m - 8);
+}
+
+/* Quantise one row of D fp16 values: amax = max |x|, inv = 448 / amax and
+ * scale = amax / 448 in fp32, code_i = E4M3(x_i * inv) with the product in
+ * fp32 (an all-zero row gets scale 0 and zero codes).  Dequantised value:
+ * code * scale. */
+void orc_fp8_quantize_row(const uint16_t* x, int D, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int d = 0; d < D; ++d) {
+    float a = (float)fabs(h2d(x[d]));
+    if (a > amax) amax = a;
+  }
+  float inv = amax > 0.0f ? 448.0f / amax : 0.0f;
+  for (int d = 0; d < D; ++d) {
+    float y = (float)h2d(x[d]) * inv;
+    codes[d] = orc_float_to_e4m3(y);
+  }
+  *scale = amax / 448.0f;
+}
+
+/* Append k[b][h][:] and v[b][h][:] (fp16, k already rotated) at position
+ * context_lens[b]-1 of FP8 pools. */
+void orc_kv_append_fp8(const uint16_t* k, const uint16_t* v, uint8_t* k_pool, uint8_t* v_pool,
+                       float* k_scale, float* v_scale, const int32_t* block_table, int max_blocks,
+                       const int32_t* context_lens, int B, int Hkv, int D) {
+  for (int b = 0; b < B; ++b) {
+    int pos = context_lens[b] - 1;
+    int32_t page = block_table[(int64_t)b * max_blocks + pos / ORC_PAGE_TOKENS];
+    int slot = pos % ORC_PAGE_TOKENS;
+    for (int h = 0; h < Hkv; ++h) {
+      int64_t row = ((int64_t)page * Hkv + h) * ORC_PAGE_TOKENS + slot;
+      orc_fp8_quantize_row(k + ((int64_t)b * Hkv + h) * D, D, k_pool + row * D, &k_scale[row]);
+      orc_fp8_quantize_row(v + ((int64_t)b * Hkv + h) * D, D, v_pool + row * D, &v_scale[row]);
+    }
+  }
+}
+
+/* Paged attention over FP8 pools: each gathered row dequantised (code *
+ * scale, in fp64), then the same softmax attention as orc_attention. */
+void orc_paged_attention_fp8(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                             const float* k_scale, const float* v_scale, const int32_t* block_table,
+                             int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                             double scale, uint16_t* out) {
+  int group = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic)
+  for (int b = 0; b < B; ++b) {
+    int L = context_lens[b];
+    size_t n = (size_t)(L > 0 ? L : 1) * Hkv * D;
+    double* kd = (double*)malloc(sizeof(double) * n);
+    double* vd = (double*)malloc(sizeof(double) * n);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    const int32_t* bt = block_table + (int64_t)b * max_blocks;
+    for (int t = 0; t < L; ++t) {
+      int32_t page = bt[t / ORC_PAGE_TOKENS];
+      for (int h = 0; h < Hkv; ++h) {
+        int64_t row = ((int64_t)page * Hkv + h) * ORC_PAGE_TOKENS + t % ORC_PAGE_TOKENS;
+        for (int d = 0; d < D; ++d) {
+          kd[((int64_t)t * Hkv + h) * D + d] = orc_e4m3_to_double(k_pool[row * D + d]) * (double)k_scale[row];
+          vd[((int64_t)t * Hkv + h) * D + d] = orc_e4m3_to_double(v_pool[row * D + d]) * (double)v_scale[row];
+        }
+      }
+    }
+    for (int h = 0; h < Hq; ++h) {
+      int kh = h / group;
+      const uint16_t* qh = q + ((int64_t)b * Hq + h) * D;
+      double mx = -INFINITY;
+      for (int t = 0; t < L; ++t) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += h2d(qh[d]) * kd[((int64_t)t * Hkv + kh) * D + d];
+        s[t] = dot * scale;
+        if (s[t] > mx) mx = s[t];
+      }
+      double den = 0.0;
+      for (int t = 0; t < L; ++t) {
+        s[t] = exp(s[t] - mx);
+        den += s[t];
+      }
+      for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t < L; ++t) acc += s[t] * vd[((int64_t)t * Hkv + kh) * D + d];
+        out[((int64_t)b * Hq + h) * D + d] = d2h(L > 0 ? acc / den : 0.0);
+      }
+    }
+    free(kd);
+    free(vd);
+    free(s);
   }
 }
 
