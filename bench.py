@@ -408,6 +408,129 @@ def run_kernel(args):
     return 0
 
 
+def time_attention_long(torch, api, dev, stream, reps=6):
+    """paged_gqa_decode on the long-context workload: 4 sequences of 32768
+    tokens (2048 pages each, scattered over a 16384-page pool), 28 query /
+    4 kv heads, 512-token partitions merged by the last partition.  Two pool
+    copies alternate so the 268 MB a launch reads does not stay in L2; a
+    CUDA graph of 8 launches, CUDA events on the launching stream."""
+    from w4a16_decode_paged_gb300 import synth
+    c = synth.QWEN_LONG
+    B, Hq, Hkv, D, L, pool, part = (c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["context"],
+                                    c["pool_pages"], c["partition_tokens"])
+    r = synth.rng(c["seed"] + 11)
+    lens = np.full(B, L, np.int32)
+    bt = torch.from_numpy(synth.block_table(r, lens, pool)).to(dev)
+    ld = torch.from_numpy(lens).to(dev)
+    pools = [(torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16),
+              torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16)) for _ in range(2)]
+    q = torch.randn((B, Hq, D), device=dev, dtype=torch.float16)
+    out = torch.empty_like(q)
+    ws = torch.zeros(api.paged_gqa_decode_workspace_size(B, Hq, Hkv, L, part), dtype=torch.uint8, device=dev)
+    fn = lambda i: api.paged_gqa_decode(q, pools[i % 2][0], pools[i % 2][1], bt, ld, max_context=L,
+                                        partition_tokens=part, workspace=ws, out=out)
+    nbytes = B * (2 * Hkv * L * D * 2 + 4 * ((L + 15) // 16) + 2 * Hq * D * 2)
+    per = _graph_time(torch, stream, fn, 8, reps)
+    del pools
+    return {"us_per_launch": per * 1e6, "bytes_per_launch": nbytes, "gbs": nbytes / per / 1e9,
+            "launches_timed": 8 * reps, "workload": f"b={B} x ctx {L}, {Hq}/{Hkv} heads, partitions of {part}"}
+
+
+def _graph_time(torch, stream, fn, per_graph, reps):
+    """Seconds per call of fn(i), i = 0..per_graph-1 captured in one CUDA
+    graph and replayed `reps` times (CUDA events on the launching stream)."""
+    for i in range(min(2, per_graph)):
+        fn(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for i in range(per_graph):
+            fn(i)
+    g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * per_graph)
+
+
+def time_b32_step(torch, api, cfg, dls, embed, fnorm, lm, dev, stream, steps=20, warmup=3):
+    """The batched decode workload on the same 28 layers' weights: 32
+    sequences whose lengths are uniform on [1, 4096] with 15/16/17 forced
+    into three slots, each layer with its own 16384-page K and V pools
+    (N(0,1)), random disjoint block tables; decode_step (tensor-core
+    projections, CUDA graph) timed over `steps` steps."""
+    from w4a16_decode_paged_gb300 import synth
+    c = synth.QWEN_BATCHED
+    B, pool = c["batch"], c["pool_pages"]
+    r = synth.rng(c["seed"])
+    post = synth.batched_lens(r, B, c["max_context"], c["forced_lens"])
+    lens0 = post - 1
+    gen = steps + warmup + 4
+    bt_np = synth.block_table(r, lens0 + gen, pool)
+    Hkv, D = cfg["n_kv_heads"], cfg["head_dim"]
+    layers = []
+    for w in dls:
+        layers.append({**w, "k_pool": torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16),
+                       "v_pool": torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16)})
+    model = api.Model(cfg, layers, embed=embed, final_norm=fnorm, lm_head=lm, max_batch=B,
+                      max_context=int(lens0.max()) + gen, num_pages=pool)
+    bt = torch.from_numpy(bt_np).to(dev)
+    lens = torch.from_numpy(lens0.astype(np.int32)).to(dev)
+    tok = torch.from_numpy(r.integers(0, cfg["vocab"], size=B).astype(np.int32)).to(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            model.decode_step(tok, tok, bt, lens, use_graph=True)
+        stream.synchronize()
+        assert model.check_errors(stream) == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            model.decode_step(tok, tok, bt, lens, use_graph=True)
+        e1.record(stream)
+        stream.synchronize()
+        assert model.check_errors(stream) == 0
+    ms = e0.elapsed_time(e1) / steps
+    mid = lens0 + 1 + warmup + steps // 2
+    sb = step_bytes(cfg, mid)
+    model.close()
+    del layers
+    return {"ms_per_step": ms, "tok_per_s": B / (ms / 1e3), "bytes_per_step": sb, "gbs": sb / (ms / 1e3) / 1e9,
+            "steps_timed": steps, "kernels_per_step": None,
+            "workload": "28 layers, batch 32, lengths U[1,4096] (15/16/17 forced), 16384-page pools, CUDA graph"}
+
+
+def time_prefill(torch, api, model, cfg, bt, dev, stream, T=512, reps=3):
+    """Time to first token of a T-token prompt on the model: w4a16_prefill
+    (every layer over the T rows, the prompt's KV pages written, the last
+    token's lm_head and argmax), CUDA events on the launching stream, each
+    rep from an empty cache; the prompt is seeded random tokens."""
+    r = np.random.default_rng(4242)
+    tokens = torch.from_numpy(r.integers(0, cfg["vocab"], size=T).astype(np.int32)).to(dev)
+    lens0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_tok = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(int(api.load().w4a16_prefill_workspace_size(model._h, T, bt.shape[1])), dtype=torch.uint8,
+                     device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 1):
+            lens0.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            model.prefill(tokens, bt[:1].contiguous(), lens0, token_out=out_tok, workspace=ws, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            if i > 0:
+                times.append(e0.elapsed_time(e1))
+        assert model.check_errors(stream) == 0
+    ms = statistics.median(times)
+    return {"ms": ms, "prompt_tokens": T, "tok_per_s": T / (ms / 1e3), "reps": reps,
+            "how": "w4a16_prefill: tensor-core GEMMs over row chunks of 32, causal paged attention, lm_head"}
+
+
 def max_over_ranks(values, dev, world):
     """Each timing, maximised over the ranks of the job (the slowest replica
     sets the job's time).  dev: the device of the collective's tensor (cuda
@@ -470,6 +593,7 @@ def main():
     lens = lens_init.clone()
     stream = torch.cuda.Stream(device=dev)
     kernels_per_step = model.kernel_count(B)
+    path = model.decode_path(B)
 
     def barrier():
         if world > 1:
@@ -522,10 +646,22 @@ def main():
         e2e_s = time.perf_counter() - t0
         barrier()
 
-        # ---- dominant projection kernel: gate|up + SiLU-mul, live ---------
+        # ---- time to first token: a 512-token prompt in one prefill -------
+        ttft = None
+        if args.workload == "b1" and not args.no_kernel_timing:
+            ttft = time_prefill(torch, api, model, cfg, bt, dev, stream, T=512)
+            lens.copy_(lens_init)
+
+        # ---- the projections alone, and the other workloads' kernels -------
         kern = None
         if not args.no_kernel_timing:
             kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream, B)
+            if args.workload == "b1":
+                kern["attention_b4_ctx32768"] = time_attention_long(torch, api, dev, stream)
+                kern["gateup_tc_m32"] = time_gemv_kernels(torch, api, cfg, dls, dev, stream, 32,
+                                                          only=("gateup",))["gateup"]
+                kern["b32_step"] = time_b32_step(torch, api, cfg, dls, embed, fnorm, lm, dev, stream)
+                torch.cuda.empty_cache()
 
     # max over ranks
     ms, e2e_s = max_over_ranks([ms, e2e_s], dev, world)
@@ -548,23 +684,44 @@ def main():
                       "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB read per step",
                       "parallelism": f"replicas x{world}"},
            "gpu_launches": kernels_per_step * K,
+           "decode_path": path,
            "e2e": {"value": world * B * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4 * B,
                    "d2h_bytes_per_step": 4 * B},
            "clocks": clk.summary()}
     out["step_roofline"] = {"bytes_per_step": sb, "achieved_gbs": sb / (ms / K / 1e3) / 1e9, "peak_gbs": peak,
                             "frac": sb / (ms / K / 1e3) / 1e9 / peak, "roofline_ms": sb / (peak * 1e9) * 1e3}
-    if kern is not None:
+    if path == "persistent":
+        # one kernel is the whole step: its bytes are the step's bytes
+        ach = sb / (ms / K / 1e3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "w4pg_decode_persistent (the whole b=1 step, one launch)",
+                           "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                           "peak_source": peak_src, "traffic": traffic_record("decode_persistent_b1")}
+    elif kern is not None:
         kname = ("w4a16_gemv_silu_mul (gate|up, 3584->2x18944)" if B <= 4 else
                  f"w4a16_gemm_silu_mul (tcgen05, M={B}, gate|up, 3584->2x18944)")
         out["roofline"] = {"bound": "hbm", "kernel": kname,
                            "achieved": kern["gateup"]["gbs"], "peak": peak, "unit": "GB/s",
                            "frac": kern["gateup"]["gbs"] / peak, "peak_source": peak_src,
                            "traffic": traffic_record("gemv_gateup" if B <= 4 else "gemm_tc_gateup_b32")}
+    if ttft is not None:
+        out["ttft"] = ttft
+    if kern is not None:
+        for k, v in kern.items():
+            if isinstance(v, dict) and "gbs" in v:
+                v["frac_of_peak"] = v["gbs"] / peak
         out["kernels"] = kern
     if not args.no_cpu_baseline:
+        import oracle as orc
         per_step, cores, sample, spent = oracle_token_time(cfg, inp)
         out["cpu_baseline"] = {"value": B / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": sample, "seconds_spent": round(spent, 2)}
+        orc.set_num_threads(1)
+        try:
+            per1, _, sample1, spent1 = oracle_token_time(cfg, inp, budget_s=12.0)
+        finally:
+            orc.set_num_threads(cores)
+        out["cpu_baseline"]["single_core"] = {"value": B / per1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                              "sample": sample1, "seconds_spent": round(spent1, 2)}
     out["setup_s"] = {"generate_inputs": round(t_gen, 1)}
     print(json.dumps(out))
     if world > 1:
@@ -572,55 +729,74 @@ def main():
     return 0
 
 
-def time_gemv_kernels(torch, api, cfg, dls, dev, stream, B=1, reps=3):
+def fused_qkv(torch, dls):
+    """Per layer, the q|k|v weights, scales and biases as one matrix (rows of
+    q, then k, then v): the single launch the decode step makes."""
+    out = []
+    for w in dls:
+        out.append({"w": torch.cat([w["wq"], w["wk"], w["wv"]], 0).contiguous(),
+                    "s": torch.cat([w["sq"], w["sk"], w["sv"]], 0).contiguous(),
+                    "b": torch.cat([w["bq"], w["bk"], w["bv"]], 0).contiguous() if w["bq"] is not None else None,
+                    "ln1": w["ln1"]})
+    return out
+
+
+def time_gemv_kernels(torch, api, cfg, dls, dev, stream, B=1, reps=3, only=None):
     """Average device time per launch of each projection kind as used in the
     step at batch B (CUDA-core GEMVs for B <= 4, tensor-core GEMMs with split
     K above), over all layers' weights (rotating, so nothing stays in L2),
     captured in a CUDA graph and timed with CUDA events on the launching
-    stream."""
+    stream.  The q|k|v projection is timed as the one fused launch of
+    (Hq + 2 Hkv) * D rows the step makes."""
     H, Hq, Hkv, D, I = cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"]
+    NQKV = (Hq + 2 * Hkv) * D
     x = torch.randn((B, H), device=dev).half()
     xi = torch.randn((B, I), device=dev).half()
     xa = torch.randn((B, Hq * D), device=dev).half()
     y_i = torch.empty((B, I), dtype=torch.float16, device=dev)
     y_h = torch.empty((B, H), dtype=torch.float16, device=dev)
-    y_q = torch.empty((B, Hq * D), dtype=torch.float16, device=dev)
+    y_q = torch.empty((B, NQKV), dtype=torch.float16, device=dev)
+    qkv = fused_qkv(torch, dls) if (only is None or "qkv" in only) else None
     if B <= 4:
         kinds = {
-            "gateup": (lambda w: api.w4a16_gemv_silu_mul(x, w["ln2"], 1e-6, w["wg"], w["sg"], w["wu"], w["su"],
-                                                         out=y_i),
+            "gateup": (lambda i: api.w4a16_gemv_silu_mul(x, dls[i]["ln2"], 1e-6, dls[i]["wg"], dls[i]["sg"],
+                                                         dls[i]["wu"], dls[i]["su"], out=y_i),
                        gemv_bytes(2 * I, H, B) - B * I * 2),
-            "down": (lambda w: api.w4a16_gemv(xi, w["wd"], w["sd"], residual=x, out=y_h),
+            "down": (lambda i: api.w4a16_gemv(xi, dls[i]["wd"], dls[i]["sd"], residual=x, out=y_h),
                      gemv_bytes(H, I, B, residual=True)),
-            "q": (lambda w: api.w4a16_gemv_rmsnorm(x, w["ln1"], 1e-6, w["wq"], w["sq"], bias=w["bq"], out=y_q),
-                  gemv_bytes(Hq * D, H, B, bias=True)),
-            "o": (lambda w: api.w4a16_gemv(xa, w["wo"], w["so"], residual=x, out=y_h),
+            "qkv": (lambda i: api.w4a16_gemv_rmsnorm(x, qkv[i]["ln1"], 1e-6, qkv[i]["w"], qkv[i]["s"],
+                                                     bias=qkv[i]["b"], out=y_q),
+                    gemv_bytes(NQKV, H, B, bias=True)),
+            "o": (lambda i: api.w4a16_gemv(xa, dls[i]["wo"], dls[i]["so"], residual=x, out=y_h),
                   gemv_bytes(H, Hq * D, B, residual=True)),
         }
     else:
         ws = torch.zeros(max(api.load().w4a16_gemm_workspace_size(B, K_, N_, s_) for N_, K_, s_ in
-                             ((I, H, 1), (H, I, 0), (Hq * D, H, 0), (H, Hq * D, 0))),
+                             ((I, H, 1), (H, I, 0), (NQKV, H, 0), (H, Hq * D, 0))),
                          dtype=torch.uint8, device=dev)
         kinds = {
-            "gateup": (lambda w: api.w4a16_gemm_silu_mul(x, w["wg"], w["sg"], w["wu"], w["su"], out=y_i,
-                                                         workspace=ws),
+            "gateup": (lambda i: api.w4a16_gemm_silu_mul(x, dls[i]["wg"], dls[i]["sg"], dls[i]["wu"], dls[i]["su"],
+                                                         out=y_i, workspace=ws),
                        gemv_bytes(2 * I, H, B) - B * I * 2),
-            "down": (lambda w: api.w4a16_gemm(xi, w["wd"], w["sd"], residual=x, out=y_h, workspace=ws),
+            "down": (lambda i: api.w4a16_gemm(xi, dls[i]["wd"], dls[i]["sd"], residual=x, out=y_h, workspace=ws),
                      gemv_bytes(H, I, B, residual=True)),
-            "q": (lambda w: api.w4a16_gemm(x, w["wq"], w["sq"], bias=w["bq"], out=y_q, workspace=ws),
-                  gemv_bytes(Hq * D, H, B, bias=True)),
-            "o": (lambda w: api.w4a16_gemm(xa, w["wo"], w["so"], residual=x, out=y_h, workspace=ws),
+            "qkv": (lambda i: api.w4a16_gemm(x, qkv[i]["w"], qkv[i]["s"], bias=qkv[i]["b"], out=y_q, workspace=ws),
+                    gemv_bytes(NQKV, H, B, bias=True)),
+            "o": (lambda i: api.w4a16_gemm(xa, dls[i]["wo"], dls[i]["so"], residual=x, out=y_h, workspace=ws),
                   gemv_bytes(H, Hq * D, B, residual=True)),
         }
+    if only is not None:
+        kinds = {k: v for k, v in kinds.items() if k in only}
     res = {}
+    n = len(dls)
     for name, (fn, nbytes) in kinds.items():
-        for w in dls[:2]:
-            fn(w)  # eager warm-up outside capture
+        for i in range(min(2, n)):
+            fn(i)  # eager warm-up outside capture
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            for w in dls:
-                fn(w)
+            for i in range(n):
+                fn(i)
         g.replay()
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

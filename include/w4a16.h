@@ -73,7 +73,8 @@ enum {
   W4A16_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
   W4A16_ERR_CAPTURE = 5,     /* call not allowed while the stream is capturing */
   W4A16_ERR_DEVICE_BOUNDS = 6, /* device reported an out-of-range index */
-  W4A16_ERR_TIMEOUT = 7      /* a bounded device wait gave up */
+  W4A16_ERR_TIMEOUT = 7,     /* a bounded device wait gave up */
+  W4A16_ERR_NO_PAGES = 8     /* the page allocator has fewer free pages than asked for */
 };
 
 /* Message of the last failed call on this thread ("" if none). */
@@ -126,6 +127,19 @@ W4A16_API int w4a16_gemm_silu_mul(const uint16_t* x, int M, int K, const uint32_
                                   const uint16_t* scales_up, int N, uint16_t* y, void* workspace,
                                   size_t workspace_bytes, w4a16_stream_t stream);
 W4A16_API size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu);
+
+/* Test hook for the failure path of the persistent decode kernel
+ * (W4A16_PATH_PERSISTENT below).  Its grid-barrier waits are bounded
+ * (default 2 s of the GPU's global timer); a wait that runs out sets bit 1
+ * of the model's error word and an abort flag, every CTA leaves at its next
+ * barrier once its own copies have landed, and w4a16_model_check_errors
+ * reports W4A16_ERR_TIMEOUT and resets the kernel's counters.  This sets the
+ * bound for launches enqueued from now on (a captured graph keeps the bound
+ * it was captured with) and returns the previous one; 0 makes the first
+ * barrier that is not already complete give up at once, which exercises
+ * that path without any stuck barrier.  The tensor-core GEMM's own mbarrier
+ * waits keep their fixed 2 s bound.  Not for production use. */
+W4A16_API unsigned long long w4a16_debug_set_wait_limit_ns(unsigned long long ns);
 
 /* Batched FP16 lm_head on the tensor cores: logits fp32 [B][vocab] = x . W^T,
  * B <= 32, H % 128 == 0; and the row-wise argmax (lowest index on ties) with
@@ -192,7 +206,9 @@ W4A16_API int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v, 
  * combine by the last partition to finish (no extra launch).
  *   q   fp16 [B][Hq][D] with row pitch q_stride elements (0 = Hq*D)
  *   out fp16 [B][Hq][D] (packed)
- *   max_context   upper bound on every context_lens[b] (sizes the grid)
+ *   max_context   upper bound on every context_lens[b] (sizes the grid); a
+ *                 longer context sets bit 0 of err_flag (its tokens past the
+ *                 grid's partitions are not attended to)
  *   workspace     device scratch of paged_gqa_decode_workspace_size() bytes;
  *                 its counter words must be zero before the first use and
  *                 every call leaves them zero again (w4a16_workspace_clear
@@ -230,6 +246,46 @@ W4A16_API int paged_gqa_decode_rope_append(const uint16_t* qkv, int qkv_stride, 
                                            int partition_tokens, void* workspace,
                                            size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
                                            w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) KV pages ([EN] "1. Weight Packing and FP8 Utilization": FP8
+ * halves the bytes of fp16 and needs scaling factors; E4M3 is the format it
+ * names).  A pool holds codes uint8 [num_pages][Hkv][16][D] (E4M3: sign, 4
+ * exponent bits with bias 7, 3 fraction bits, no infinities, largest 448)
+ * beside fp32 row scales [num_pages][Hkv][16]: value = code * scale.  A row
+ * is quantised when appended: amax = largest magnitude of its fp16 values
+ * (k after RoPE), inv = 448 / amax and scale = amax / 448 in fp32, code =
+ * E4M3(x * inv) with the product in fp32, round to nearest even (an all-zero
+ * row: scale 0, codes 0).  Per page and kv head: 2 x 2 KiB of codes and
+ * 2 x 64 B of scales instead of 2 x 4 KiB.
+ *   kv_append_rope_fp8     kv_append_rope into FP8 pools.
+ *   paged_gqa_decode_fp8   paged_gqa_decode over FP8 pools (q fp16; scores
+ *                          and P V in fp32 on the dequantised values).
+ *   paged_gqa_decode_rope_append_fp8  the fused form (qkv rows as for
+ *                          paged_gqa_decode_rope_append).
+ * Pools and scales must be 128-byte aligned; the other arguments, the
+ * workspace and the error flag are as for the fp16 calls.
+ * ------------------------------------------------------------------------ */
+W4A16_API int kv_append_rope_fp8(uint16_t* q, const uint16_t* k, const uint16_t* v, int row_stride,
+                                 uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
+                                 int num_pages, const int32_t* block_table, int max_blocks,
+                                 const int32_t* context_lens, int B, int Hq, int Hkv, int D, float theta,
+                                 int32_t* err_flag, w4a16_stream_t stream);
+W4A16_API int paged_gqa_decode_fp8(const uint16_t* q, int q_stride, const uint8_t* k_pool,
+                                   const uint8_t* v_pool, const float* k_scale, const float* v_scale,
+                                   int num_pages, const int32_t* block_table, int max_blocks,
+                                   const int32_t* context_lens, int max_context, int B, int Hq, int Hkv,
+                                   int D, float sm_scale, int partition_tokens, void* workspace,
+                                   size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
+                                   w4a16_stream_t stream);
+W4A16_API int paged_gqa_decode_rope_append_fp8(const uint16_t* qkv, int qkv_stride, uint8_t* k_pool,
+                                               uint8_t* v_pool, float* k_scale, float* v_scale,
+                                               int num_pages, const int32_t* block_table, int max_blocks,
+                                               const int32_t* context_lens, int max_context, int B,
+                                               int Hq, int Hkv, int D, float theta, float sm_scale,
+                                               int partition_tokens, void* workspace,
+                                               size_t workspace_bytes, uint16_t* out, int32_t* err_flag,
+                                               w4a16_stream_t stream);
 
 /* Bytes of workspace paged_gqa_decode needs for these sizes. */
 W4A16_API size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max_context,
@@ -324,7 +380,9 @@ typedef struct w4a16_model w4a16_model;
 /* Builds the model handle.  The only call that allocates: one device arena
  * for activations and workspaces sized for max_batch (1..32) sequences of up
  * to max_context tokens.  Weight and pool pointers are borrowed (caller keeps
- * them alive). */
+ * them alive).  A decode_step that takes a sequence past max_context tokens
+ * sets bit 0 of the model's error word (W4A16_ERR_DEVICE_BOUNDS from
+ * w4a16_model_check_errors). */
 W4A16_API int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
                        int max_context, w4a16_model** out);
 W4A16_API void w4a16_model_destroy(w4a16_model* m);
@@ -334,8 +392,10 @@ W4A16_API int32_t* w4a16_model_err_flag(w4a16_model* m);
 
 /* Synchronise `stream`, read and clear the model's device error word:
  * returns W4A16_ERR_DEVICE_BOUNDS if a kernel skipped an out-of-range page or
- * token, W4A16_ERR_TIMEOUT if a bounded wait gave up, else W4A16_OK.  This
- * call blocks and copies to the host, so it must not be used while the
+ * token, W4A16_ERR_TIMEOUT if a bounded wait gave up, else W4A16_OK.  After
+ * a timeout the step's outputs are not valid; the call also clears the
+ * split-K tickets of the model's workspaces, so the next step runs clean.
+ * This call blocks and copies to the host, so it must not be used while the
  * stream is capturing. */
 W4A16_API int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream);
 
@@ -393,6 +453,122 @@ W4A16_API int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tok
 
 /* Number of kernels one decode_step launches for B sequences (graph or not). */
 W4A16_API int decode_step_kernel_count(w4a16_model* m, int B);
+
+/* ------------------------------------------------------------------------
+ * w4a16_prefill -- the prompt of one sequence in one pass ([RU] "Ключевые
+ * метрики производительности": TTFT for a 512-token prompt).
+ *   tokens         int32 [T] device, the prompt (T >= 1)
+ *   block_table    int32 [1][max_blocks] device; pages for positions
+ *                  [context_lens[0], context_lens[0] + T) already assigned
+ *   context_lens   int32 [1] device: tokens cached before the prompt (0 for
+ *                  a new sequence); advanced by T on the device
+ *   token_out      int32 [1] device: greedy next token after the prompt
+ *   logits         fp16 [vocab] or NULL: the last prompt token's logits
+ *   workspace      w4a16_prefill_workspace_size(m, T, max_blocks) bytes,
+ *                  256-byte aligned (activations of the T rows)
+ * Per layer: RMSNorm, q|k|v (tensor-core GEMM over the T rows, bias), RoPE
+ * and the append of all T positions to the pages, causal paged attention
+ * (token t sees positions <= context_lens[0] + t), o + residual, RMSNorm,
+ * gate|up + SiLU-mul, down + residual; then final RMSNorm, lm_head and
+ * argmax for the last token.  Same arithmetic as T decode steps (fp16
+ * roundings at the same points; sums in other orders).  Enqueue only.
+ * ------------------------------------------------------------------------ */
+W4A16_API size_t w4a16_prefill_workspace_size(w4a16_model* m, int T, int max_blocks);
+W4A16_API int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const int32_t* block_table,
+                            int max_blocks, int32_t* context_lens, int32_t* token_out, uint16_t* logits,
+                            void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * How decode_step runs a step ([EN] "3. CUDA Graph Capture"; [RU]
+ * "Ключевые метрики производительности": the per-token cost that is not
+ * bandwidth is kernel launches).
+ *   W4A16_PATH_KERNELS     one kernel per operation (5 per layer for B <= 4),
+ *                          chained with programmatic dependent launch;
+ *   W4A16_PATH_PERSISTENT  one cooperative kernel for the whole step: every
+ *                          SM runs one CTA that walks all layers' phases with
+ *                          a grid-wide barrier between them, streaming the
+ *                          next phase's weights (and the attention's KV pages)
+ *                          into shared memory before each barrier.  It covers
+ *                          one sequence (B == 1) of a model with head_dim 128,
+ *                          Hq == 7 Hkv, inter <= 18944, an even vocabulary and
+ *                          max_context <= 4096; it needs all SMs (cooperative
+ *                          launch), and its barrier waits are bounded (a wait
+ *                          that runs out reports W4A16_ERR_TIMEOUT through
+ *                          w4a16_model_check_errors, which also resets it);
+ *   W4A16_PATH_AUTO        (default) the persistent kernel where it applies,
+ *                          else the kernels.
+ * Both paths compute the same step; sums are ordered differently, so
+ * outputs agree to fp16 rounding, not bit for bit.  Graphs captured by
+ * decode_step are keyed on the path.  set returns W4A16_ERR_SHAPE when the
+ * persistent path is asked for a model it does not cover;
+ * w4a16_model_decode_path reports the path decode_step takes for B
+ * sequences (W4A16_PATH_KERNELS or W4A16_PATH_PERSISTENT).
+ * ------------------------------------------------------------------------ */
+enum { W4A16_PATH_AUTO = 0, W4A16_PATH_KERNELS = 1, W4A16_PATH_PERSISTENT = 2 };
+W4A16_API int w4a16_model_set_decode_path(w4a16_model* m, int path);
+W4A16_API int w4a16_model_decode_path(w4a16_model* m, int B);
+
+/* ------------------------------------------------------------------------
+ * Host page allocator ([EN] "2. The KV Cache and PagedAttention": the KV
+ * cache managed like virtual memory, fixed-size pages handed out as
+ * sequences grow).  Host-side bookkeeping only, thread-safe; it never
+ * touches device memory.  Pages are the indices of a pool's first dimension.
+ *   create        pages [0, num_pages) all free; handed out lowest first.
+ *   alloc         n pages into pages[0..n): all or nothing (W4A16_ERR_NO_PAGES
+ *                 leaves the allocator unchanged).
+ *   free          returns pages; a page outside the pool, one not handed out,
+ *                 or one named twice returns W4A16_ERR_INVALID_ARG and frees
+ *                 nothing.
+ *   free_count    pages free now (-1 for a NULL allocator).
+ *   seq_reserve   makes a host block-table row cover len tokens: entries
+ *                 [0, ceil(len/16)) that are -1 get pages (all or nothing);
+ *                 W4A16_ERR_SHAPE if that exceeds max_blocks.
+ *   seq_release   frees every entry >= 0 of the row and sets it to -1.
+ * ------------------------------------------------------------------------ */
+typedef struct w4a16_page_allocator w4a16_page_allocator;
+W4A16_API int w4a16_page_allocator_create(int num_pages, w4a16_page_allocator** out);
+W4A16_API void w4a16_page_allocator_destroy(w4a16_page_allocator* a);
+W4A16_API int w4a16_page_alloc(w4a16_page_allocator* a, int n, int32_t* pages);
+W4A16_API int w4a16_page_free(w4a16_page_allocator* a, const int32_t* pages, int n);
+W4A16_API int w4a16_page_free_count(w4a16_page_allocator* a);
+W4A16_API int w4a16_seq_reserve(w4a16_page_allocator* a, int32_t* row, int max_blocks, int len);
+W4A16_API int w4a16_seq_release(w4a16_page_allocator* a, int32_t* row, int max_blocks);
+
+/* ------------------------------------------------------------------------
+ * Continuous batching over decode_step ([EN] "2. The KV Cache and
+ * PagedAttention", "Why Build from Scratch?" item 3: maximise batch sizes).
+ * The batcher owns a page allocator over the model's pools (num_pages must
+ * not exceed the model's), the host block tables and small device buffers
+ * (allocated at create; steps allocate nothing on the device).
+ *   submit   queues a sequence: its prompt (host int32, >= 1 token) is fed
+ *            one token per step, then up to max_new_tokens greedy tokens
+ *            are generated; prompt_len + max_new_tokens - 1 <= max_context,
+ *            and the sequence alone must fit the pool (else
+ *            W4A16_ERR_NO_PAGES).  Returns its id.
+ *   step     admits queued sequences into free slots (max_batch), gives
+ *            every active sequence the page of its next position (a page per
+ *            16 tokens; with the pool empty the most recently admitted
+ *            sequence is preempted -- pages freed, restarted from its prompt
+ *            later, same greedy result), uploads tokens, lengths and block
+ *            tables, runs decode_step for the B active sequences (one
+ *            captured graph per B), reads the new tokens back (synchronises
+ *            `stream`), and retires finished sequences, freeing their pages.
+ *            *n_active: sequences in the step (0: nothing to do).
+ *   poll     a sequence's generated tokens so far (up to cap copied),
+ *            their count and whether it finished.
+ *   stats    steps run, preemptions, queued and active sequences, free pages.
+ * ------------------------------------------------------------------------ */
+typedef struct w4a16_batcher w4a16_batcher;
+W4A16_API int w4a16_batcher_create(w4a16_model* model, int num_pages, int max_batch, int max_blocks,
+                                   int max_context, w4a16_batcher** out);
+W4A16_API void w4a16_batcher_destroy(w4a16_batcher* b);
+W4A16_API int w4a16_batcher_submit(w4a16_batcher* b, const int32_t* prompt, int prompt_len, int max_new_tokens,
+                                   int* seq_id);
+W4A16_API int w4a16_batcher_step(w4a16_batcher* b, w4a16_stream_t stream, int* n_active);
+W4A16_API int w4a16_batcher_poll(w4a16_batcher* b, int seq_id, int32_t* tokens, int cap, int* n_tokens,
+                                 int* done);
+W4A16_API int w4a16_batcher_stats(w4a16_batcher* b, long* steps, long* preemptions, int* waiting, int* active,
+                                  int* free_pages);
 
 #ifdef __cplusplus
 }

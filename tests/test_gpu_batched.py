@@ -118,3 +118,4 @@ def test_batched_tiny_layer_matches_oracle(api, B):
     cfg = dict(synth.TINY_LAYER, batch=B, pool_pages=16 * B + 16, bias=True)
     lens = synth.batched_lens(synth.rng(5300 + B), B, 200, forced=(15, 16, 17, 1))
     layer_parity(api, torch, orc, synth, cfg, lens=lens, seed=5400 + B)
+

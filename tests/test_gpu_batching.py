@@ -1,0 +1,96 @@
+"""Continuous batching (w4a16_batcher_*) over the decode step, against the
+CPU oracle's own greedy decode of each sequence.  GPU only (marked gpu).
+
+The pool is deliberately too small for every admitted sequence to reach its
+full length, so pages are reclaimed from finished sequences and handed to
+new ones, and sequences get preempted and restarted; batch sizes change from
+step to step (each size its own captured graph, size 1 the persistent
+kernel)."""
+import numpy as np
+import pytest
+
+import oracle as orc
+from gpu_util import to_dev
+from w4a16_decode_paged_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from w4a16_decode_paged_gb300 import api as _api
+    from w4a16_decode_paged_gb300 import build
+    build.build()
+    orc.build()
+    return _api
+
+
+def _oracle_greedy(cfg, layers, embed, fnorm, lm, prompt, n_new):
+    """Greedy continuation of `prompt` by the oracle, one decode step per
+    token (prompt tokens fed in turn), with each step's top-2 margin."""
+    Hkv, D = cfg["n_kv_heads"], cfg["head_dim"]
+    total = len(prompt) + n_new
+    pages = (total + 15) // 16
+    kps = [np.zeros((pages, Hkv, 16, D), np.float16) for _ in layers]
+    vps = [np.zeros((pages, Hkv, 16, D), np.float16) for _ in layers]
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    toks, margins = [], []
+    cur = int(prompt[0])
+    for i in range(total - 1):
+        t_next, lg, _ = orc.decode_step(cfg, layers, kps, vps, embed, fnorm, lm, np.array([cur], np.int32), bt,
+                                        np.array([i + 1], np.int32), want_logits=True)
+        if i + 1 < len(prompt):
+            cur = int(prompt[i + 1])
+            continue
+        srt = np.sort(lg[0].astype(np.float64))
+        toks.append(int(t_next[0]))
+        margins.append(float(srt[-1] - srt[-2]))
+        cur = int(t_next[0])
+    return toks, margins
+
+
+def test_continuous_batching_matches_oracle_with_page_reuse_and_preemption(api):
+    cfg = dict(synth.TINY_LAYER, n_layers=2, vocab=600, bias=True, codes="symmetric")
+    r = synth.rng(8100)
+    layers = [synth.layer_weights(r, cfg) for _ in range(2)]
+    embed = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]))
+    fnorm = synth.gamma(r, cfg["hidden"])
+    lm = synth.normal_fp16(r, (cfg["vocab"], cfg["hidden"]), std=0.02)
+    num_pages, max_blocks, max_context = 3, 4, 64
+    Hkv, D = cfg["n_kv_heads"], cfg["head_dim"]
+    pools = [(np.zeros((num_pages, Hkv, 16, D), np.float16), np.zeros((num_pages, Hkv, 16, D), np.float16))
+             for _ in layers]
+    dls = [api.device_layer(w, kp, vp) for w, (kp, vp) in zip(layers, pools)]
+    model = api.Model(cfg, dls, embed=to_dev(embed, torch), final_norm=to_dev(fnorm, torch),
+                      lm_head=to_dev(lm, torch), max_batch=4, max_context=max_context, num_pages=num_pages)
+    bat = api.Batcher(model, num_pages=num_pages, max_batch=4, max_blocks=max_blocks, max_context=max_context)
+    # every sequence fits the 3-page pool alone; four of them at once do not
+    plens = [1, 20, 25, 17, 30, 9, 22, 18]
+    news = [6, 10, 8, 12, 5, 14, 9, 11]
+    prompts = [r.integers(0, cfg["vocab"], size=n).astype(np.int32) for n in plens]
+    ids = [bat.submit(p, n) for p, n in zip(prompts, news)]
+    with pytest.raises(Exception):
+        bat.submit(prompts[0], 200)                     # beyond max_context
+    sizes = set()
+    for _ in range(2000):
+        n = bat.step()
+        if n == 0:
+            break
+        sizes.add(n)
+    st = bat.stats()
+    assert st["active"] == 0 and st["waiting"] == 0
+    assert st["free_pages"] == num_pages                # every page came back
+    assert st["preemptions"] > 0                        # the pool was too small for all at once
+    assert 1 in sizes and len(sizes) >= 2               # several graph buckets, incl. the persistent kernel
+    assert model.check_errors() == 0
+    for sid, p, n in zip(ids, prompts, news):
+        got, done = bat.poll(sid)
+        assert done and len(got) == n
+        ref, margins = _oracle_greedy(cfg, layers, embed, fnorm, lm, p, n)
+        for i, (g, t, mg) in enumerate(zip(got, ref, margins)):
+            if mg < 0.02:
+                break                                    # near-tie: the sequences may part here
+            assert int(g) == t, f"sequence {sid} token {i}: device {g} oracle {t}"
+    bat.close()
+    model.close()

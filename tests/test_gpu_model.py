@@ -147,6 +147,23 @@ def test_model_err_flag_reports_bad_page(api):
     m.close()
 
 
+def test_model_err_flag_reports_context_past_max_context(api):
+    """A step that takes a sequence past the model's max_context is
+    reported, not silently truncated (its pages exist, so the only fault is
+    the model's capacity)."""
+    cfg, layers, kps, vps, embed, fnorm, lm, bt, lens, toks = _small_model(n_layers=1, vocab=300, seed=4350)
+    m, dls = _build(api, cfg, layers, kps, vps, embed, fnorm, lm, 1, int(lens[0]) + 1)
+    tok = to_dev(toks, torch)
+    ld = to_dev(lens, torch)
+    btd = to_dev(bt, torch)
+    m.decode_step(tok, tok, btd, ld, use_graph=False)   # reaches max_context exactly: fine
+    assert m.check_errors() == 0
+    m.decode_step(tok, tok, btd, ld, use_graph=False)   # one token past it
+    assert m.check_errors() == 6          # W4A16_ERR_DEVICE_BOUNDS
+    assert int(to_host(ld)[0]) == int(lens[0]) + 2
+    m.close()
+
+
 def test_check_errors_refuses_while_capturing(api):
     cfg, layers, kps, vps, embed, fnorm, lm, bt, lens, toks = _small_model(n_layers=1, vocab=300, seed=4400)
     m, dls = _build(api, cfg, layers, kps, vps, embed, fnorm, lm, 1, 128)

@@ -22,7 +22,7 @@ F32 = ctypes.c_float
 SZ = ctypes.c_size_t
 
 ERR_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "SHAPE", 4: "CUDA", 5: "CAPTURE",
-             6: "DEVICE_BOUNDS", 7: "TIMEOUT"}
+             6: "DEVICE_BOUNDS", 7: "TIMEOUT", 8: "NO_PAGES"}
 
 
 class W4A16Error(RuntimeError):
@@ -54,6 +54,7 @@ SIGNATURES = {
     "w4a16_gemm": (I32, [P, I32, I32, P, P, I32, P, P, P, P, SZ, P]),
     "w4a16_gemm_silu_mul": (I32, [P, I32, I32, P, P, P, P, I32, P, P, SZ, P]),
     "w4a16_gemm_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "w4a16_debug_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "lm_head_logits_batched": (I32, [P, I32, I32, P, I32, P, P]),
     "argmax_rows": (I32, [P, I32, I32, P, P, P]),
     "w4a16_gemv_rmsnorm": (I32, [P, P, F32, I32, I32, P, P, I32, P, P, P]),
@@ -64,6 +65,11 @@ SIGNATURES = {
     "paged_gqa_decode_rope_append": (I32, [P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, F32, I32, P,
                                            SZ, P, P, P]),
     "paged_gqa_decode_noalloc": (I32, [P, I32, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, P]),
+    "paged_gqa_decode_fp8": (I32, [P, I32, P, P, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, SZ, P,
+                                   P, P]),
+    "paged_gqa_decode_rope_append_fp8": (I32, [P, I32, P, P, P, P, I32, P, I32, P, I32, I32, I32, I32, I32, F32, F32,
+                                               I32, P, SZ, P, P, P]),
+    "kv_append_rope_fp8": (I32, [P, P, P, I32, P, P, P, P, I32, P, I32, P, I32, I32, I32, I32, F32, P, P]),
     "paged_gqa_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
     "paged_gqa_decode_default_partition": (I32, [I32, I32, I32]),
     "w4a16_workspace_clear": (I32, [P, SZ, P]),
@@ -80,6 +86,24 @@ SIGNATURES = {
     "w4a16_model_layer": (I32, [P, I32, P, P, I32, P, I32, P]),
     "decode_step": (I32, [P, P, P, P, I32, P, I32, P, I32, P]),
     "decode_step_kernel_count": (I32, [P, I32]),
+    "w4a16_model_set_decode_path": (I32, [P, I32]),
+    "w4a16_prefill_workspace_size": (SZ, [P, I32, I32]),
+    "w4a16_prefill": (I32, [P, P, I32, P, I32, P, P, P, P, SZ, P]),
+    "w4a16_page_allocator_create": (I32, [I32, ctypes.POINTER(P)]),
+    "w4a16_page_allocator_destroy": (None, [P]),
+    "w4a16_page_alloc": (I32, [P, I32, P]),
+    "w4a16_page_free": (I32, [P, P, I32]),
+    "w4a16_page_free_count": (I32, [P]),
+    "w4a16_seq_reserve": (I32, [P, P, I32, I32]),
+    "w4a16_seq_release": (I32, [P, P, I32]),
+    "w4a16_batcher_create": (I32, [P, I32, I32, I32, I32, ctypes.POINTER(P)]),
+    "w4a16_batcher_destroy": (None, [P]),
+    "w4a16_batcher_submit": (I32, [P, P, I32, I32, ctypes.POINTER(I32)]),
+    "w4a16_batcher_step": (I32, [P, P, ctypes.POINTER(I32)]),
+    "w4a16_batcher_poll": (I32, [P, I32, P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]),
+    "w4a16_batcher_stats": (I32, [P, ctypes.POINTER(ctypes.c_long), ctypes.POINTER(ctypes.c_long),
+                                  ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32)]),
+    "w4a16_model_decode_path": (I32, [P, I32]),
 }
 
 

@@ -285,6 +285,74 @@ def paged_gqa_decode_rope_append(qkv, k_pool, v_pool, block_table, context_lens,
     return out
 
 
+def _paging_fp8(k_pool, v_pool, k_scale, v_scale, block_table, context_lens):
+    """(pages, Hkv, D, B) of FP8 pools: codes [pages][Hkv][16][D] uint8 and
+    fp32 row scales [pages][Hkv][16]."""
+    _arg(k_pool, _U8, "k_pool", (None, None, 16, None))
+    pages, Hkv, _, D = k_pool.shape
+    _arg(v_pool, _U8, "v_pool", tuple(k_pool.shape))
+    _arg(k_scale, _F, "k_scale", (pages, Hkv, 16))
+    _arg(v_scale, _F, "v_scale", (pages, Hkv, 16))
+    _arg(block_table, _I, "block_table", (None, None))
+    B = block_table.shape[0]
+    _arg(context_lens, _I, "context_lens", (B,))
+    return pages, Hkv, D, B
+
+
+def kv_append_rope_fp8(q, k, v, k_pool, v_pool, k_scale, v_scale, block_table, context_lens, theta, row_stride=0,
+                       err_flag=None, n_q_heads=None, n_kv_heads=None, stream=None):
+    """kv_append_rope into FP8 pools: q [B][Hq][D] rotated in place; the
+    rotated k row and the v row quantised (largest magnitude to 448) into
+    their slot's codes and row scale."""
+    pages, Hkv, D, B = _paging_fp8(k_pool, v_pool, k_scale, v_scale, block_table, context_lens)
+    _arg(err_flag, _I, "err_flag", optional=True)
+    Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
+    if n_kv_heads is not None:
+        Hkv = n_kv_heads
+    check(load().kv_append_rope_fp8(_p(q), _p(k), _p(v), int(row_stride), _p(k_pool), _p(v_pool), _p(k_scale),
+                                    _p(v_scale), pages, _p(block_table), block_table.shape[1], _p(context_lens), B,
+                                    Hq, Hkv, D, float(theta), _p(err_flag), stream_handle(stream)))
+    return q
+
+
+def paged_gqa_decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, context_lens, max_context, sm_scale=None,
+                         partition_tokens=0, workspace=None, out=None, err_flag=None, qkv_theta=None,
+                         n_q_heads=None, stream=None):
+    """paged_gqa_decode over FP8 pools.  With qkv_theta given, q holds q|k|v
+    rows (B, (Hq + 2 Hkv) D) and the call is the fused RoPE + FP8 append +
+    attention (paged_gqa_decode_rope_append_fp8)."""
+    pages, Hkv, D, B = _paging_fp8(k_pool, v_pool, k_scale, v_scale, block_table, context_lens)
+    _arg(q, _H, "q")
+    fuse = qkv_theta is not None
+    Hq = n_q_heads if n_q_heads is not None else q.shape[-2]
+    stride = q.shape[-1] if fuse else 0
+    if fuse and (q.dim() != 2 or q.shape[0] != B or q.shape[1] < (Hq + 2 * Hkv) * D):
+        raise ValueError(f"qkv: shape {tuple(q.shape)}, need ({B}, >= {(Hq + 2 * Hkv) * D})")
+    if not fuse:
+        _arg(q, _H, "q", (B, Hq, D))
+    _arg(out, _H, "out", (B, Hq, D), optional=True)
+    _arg(workspace, _U8, "workspace", optional=True)
+    _arg(err_flag, _I, "err_flag", optional=True)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    lib = load()
+    if workspace is None:
+        nbytes = lib.paged_gqa_decode_workspace_size(B, Hq, Hkv, max_context, partition_tokens, D)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=k_pool.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=k_pool.device)
+    common = (pages, _p(block_table), block_table.shape[1], _p(context_lens), int(max_context), B, Hq, Hkv, D)
+    tail = (int(partition_tokens), _p(workspace), workspace.numel() * workspace.element_size(), _p(out),
+            _p(err_flag), stream_handle(stream))
+    if fuse:
+        check(lib.paged_gqa_decode_rope_append_fp8(_p(q), int(stride), _p(k_pool), _p(v_pool), _p(k_scale),
+                                                   _p(v_scale), *common, float(qkv_theta), float(sm_scale), *tail))
+    else:
+        check(lib.paged_gqa_decode_fp8(_p(q), 0, _p(k_pool), _p(v_pool), _p(k_scale), _p(v_scale), *common,
+                                       float(sm_scale), *tail))
+    return out
+
+
 def embedding_gather(embed, tokens, out=None, err_flag=None, stream=None):
     _arg(embed, _H, "embed", (None, None))
     vocab, H = embed.shape
@@ -413,6 +481,95 @@ class Model:
 
     def kernel_count(self, B=1) -> int:
         return int(self._lib.decode_step_kernel_count(self._h, int(B)))
+
+    def prefill(self, tokens, block_table, context_lens, token_out=None, logits=None, workspace=None, stream=None):
+        """One sequence's prompt tokens [T] in one pass: writes their KV pages,
+        advances context_lens[0] by T, returns the greedy next token [1]."""
+        _arg(tokens, _I, "tokens")
+        T = tokens.numel()
+        _arg(block_table, _I, "block_table", (1, None))
+        _arg(context_lens, _I, "context_lens", (1,))
+        _arg(logits, _H, "logits", (1, self.cfg.get("vocab", 0)), optional=True)
+        lib = self._lib
+        need = int(lib.w4a16_prefill_workspace_size(self._h, T, block_table.shape[1]))
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=tokens.device)
+        _arg(workspace, _U8, "workspace")
+        if token_out is None:
+            token_out = torch.empty(1, dtype=torch.int32, device=tokens.device)
+        _arg(token_out, _I, "token_out", (1,))
+        check(lib.w4a16_prefill(self._h, _p(tokens), T, _p(block_table), block_table.shape[1], _p(context_lens),
+                                _p(token_out), _p(logits), _p(workspace), workspace.numel(), stream_handle(stream)))
+        return token_out
+
+    PATHS = {"auto": 0, "kernels": 1, "persistent": 2}
+
+    def set_decode_path(self, path: str) -> None:
+        """'auto' (persistent kernel where it applies), 'kernels' or
+        'persistent' (raises if the model is outside what it covers)."""
+        check(self._lib.w4a16_model_set_decode_path(self._h, self.PATHS[path]))
+
+    def decode_path(self, B=1) -> str:
+        """The path decode_step takes for B sequences."""
+        code = int(self._lib.w4a16_model_decode_path(self._h, int(B)))
+        return {1: "kernels", 2: "persistent"}[code]
+
+
+class Batcher:
+    """Continuous batching over a Model (w4a16_batcher_*): sequences are
+    queued with submit(), step() runs one decode step over the active ones
+    (admitting queued sequences as others finish, pages handed out and
+    reclaimed by the library's allocator), poll() reads a sequence's tokens."""
+
+    def __init__(self, model: "Model", num_pages: int, max_batch: int, max_blocks: int, max_context: int):
+        self._lib = load()
+        self.model = model
+        h = ctypes.c_void_p()
+        check(self._lib.w4a16_batcher_create(model._h, int(num_pages), int(max_batch), int(max_blocks),
+                                             int(max_context), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.w4a16_batcher_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def submit(self, prompt, max_new_tokens: int) -> int:
+        import numpy as np
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        sid = ctypes.c_int()
+        check(self._lib.w4a16_batcher_submit(self._h, p.ctypes.data, int(p.size), int(max_new_tokens),
+                                             ctypes.byref(sid)))
+        return sid.value
+
+    def step(self, stream=None) -> int:
+        n = ctypes.c_int()
+        check(self._lib.w4a16_batcher_step(self._h, stream_handle(stream), ctypes.byref(n)))
+        return n.value
+
+    def poll(self, seq_id: int):
+        """(generated tokens so far, finished?)"""
+        import numpy as np
+        n, done = ctypes.c_int(), ctypes.c_int()
+        check(self._lib.w4a16_batcher_poll(self._h, int(seq_id), None, 0, ctypes.byref(n), ctypes.byref(done)))
+        out = np.zeros(max(1, n.value), np.int32)
+        check(self._lib.w4a16_batcher_poll(self._h, int(seq_id), out.ctypes.data, n.value, ctypes.byref(n),
+                                           ctypes.byref(done)))
+        return out[:n.value], bool(done.value)
+
+    def stats(self) -> dict:
+        st, pre = ctypes.c_long(), ctypes.c_long()
+        wt, ac, fp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        check(self._lib.w4a16_batcher_stats(self._h, ctypes.byref(st), ctypes.byref(pre), ctypes.byref(wt),
+                                            ctypes.byref(ac), ctypes.byref(fp)))
+        return {"steps": st.value, "preemptions": pre.value, "waiting": wt.value, "active": ac.value,
+                "free_pages": fp.value}
 
 
 def device_pool(case: dict, layer: int, which: str, device="cuda"):

@@ -56,7 +56,9 @@ TRACE_LIB = os.path.join(TRACE_BUILD, "libw4a16_gb300_trace.so")
 def build_trace(force: bool = False) -> str:
     """Kernel-timeline build (-DW4A16_TRACE): a separate library that adds
     w4a16_trace_start / w4a16_trace_count; the product library is untouched."""
-    return build(force=force, extra_flags=["-DW4A16_TRACE", "-rdc=true"], out=TRACE_LIB)
+    # separately compiled device functions must fit the register budget of
+    # the kernels that call them (the persistent kernel runs 512 threads)
+    return build(force=force, extra_flags=["-DW4A16_TRACE", "-rdc=true", "-maxrregcount=128"], out=TRACE_LIB)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str = None) -> str:

@@ -7,7 +7,8 @@
 // block_table[b][t / 16].  The pool layout [page][kv_head][16][128] fp16 makes
 // each (page, kv head) slice one contiguous 4 KiB run, the unit the aikraft.ru
 // article ("Архитектурные решения и оптимизации") aligns to cache lines; here
-// it is the unit of one 1-D bulk (TMA) copy into shared memory.
+// one warp copies it into shared memory with 16-byte cp.async copies (512
+// contiguous bytes per instruction) into rows padded for ldmatrix.
 //
 // One CTA handles (sequence b, kv head, partition p) for all G = Hq/Hkv query
 // heads that share the kv head (7:1 GQA in the article).  Its eight warps take
@@ -30,6 +31,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "attn_core.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,64 +43,32 @@ __device__ unsigned int g_trace_cap = 0;
 __device__ unsigned int g_trace_n = 0;
 #endif
 
-constexpr int ATT_D = 128;
-constexpr int ATT_PAGE = 16;
 constexpr int ATT_NW = 8;          // warps per CTA (small grids); large grids use 4 so that
                                    // three CTAs share an SM
 constexpr int ATT_MAX_CLUSTER = 8; // partitions merged through distributed shared memory
 constexpr int ATT_STAGES = 2;      // page slots per warp (CTA per partition)
 constexpr int ATT_STAGES_WP = 3;   // page slots per warp (warp per partition: deeper, the
                                    // warp streams a whole partition alone)
-constexpr int ATT_SLICE = ATT_PAGE * ATT_D;  // halves per (page, kv head) slice in the pool
-// In shared memory a slice's rows are 272 bytes apart (16 bytes of padding),
-// so the eight rows of an 8x8 ldmatrix tile fall on eight different bank
-// groups.
-constexpr int ATT_PITCH = ATT_D + 8;                   // halves per row in shared memory
-constexpr int ATT_SSLICE = ATT_PAGE * ATT_PITCH;       // halves per slice in shared memory
 constexpr int att_stages(bool wp) { return wp ? ATT_STAGES_WP : ATT_STAGES; }
-constexpr size_t att_ring_bytes(int nw, int st) { return (size_t)nw * st * 2 * ATT_SSLICE * 2; }
-constexpr size_t att_smem(int nw, int st) { return att_ring_bytes(nw, st); }
-constexpr unsigned long long ATT_TIMEOUT_NS = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
+constexpr size_t att_slot_bytes(bool kv8) { return kv8 ? (size_t)ATT8_SLOT : (size_t)2 * ATT_SSLICE * 2; }
+constexpr size_t att_ring_bytes(int nw, int st, bool kv8) { return (size_t)nw * st * att_slot_bytes(kv8); }
+constexpr size_t att_smem(int nw, int st, bool kv8) {
+  // the ring is reused for the warps' merge ([NW][8][128 + 2] floats)
+  return att_ring_bytes(nw, st, kv8) > (size_t)nw * 8 * (ATT_D + 2) * 4 + 64 * 4 * 4
+             ? att_ring_bytes(nw, st, kv8)
+             : (size_t)nw * 8 * (ATT_D + 2) * 4 + 64 * 4 * 4;
 }
 
-// Bounded wait on an mbarrier phase (returns false on timeout).
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > ATT_TIMEOUT_NS) return false;
-  }
-}
-
-__device__ __forceinline__ float2 h2f2(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
-
-// d += A (16 x 16, fp16, rows 8-15 zero) x B (16 x 8, fp16), fp32 accumulate.
-// a0: A[g][2t..2t+1], a2: A[g][8+2t..8+2t+1]; b0, b1: B[2t..2t+1][g], B[8+2t..][g].
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-
-template <int G, bool FUSE, int NW, bool WP>
-__global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_constant__ AttnArgs a) {
+template <int G, bool FUSE, int NW, bool WP, bool KV8>
+__global__ void __launch_bounds__(NW * 32) w4pg_paged_attn(const __grid_constant__ AttnArgs a) {
   constexpr int ST = att_stages(WP);      // page slots per warp
+  constexpr int SLOT = (int)att_slot_bytes(KV8);
   extern __shared__ __align__(128) unsigned char smraw[];
-  __half* ring = reinterpret_cast<__half*>(smraw);
   __shared__ __align__(16) float s_q[G][ATT_D];   // this group's q (rotated in the fused variant)
   __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
   __shared__ __align__(16) __half s_vnew[ATT_D];
+  __shared__ __align__(16) unsigned char s_new8[2][ATT_D];  // fused, FP8 pages: codes of the new k, v
+  __shared__ float s_new8_scale[2];
   __shared__ int s_last;
   // cluster partial table (used in the leader CTA): [partition][head][128 + M, den, pad]
   __shared__ __align__(16) float s_clu[WP ? 4 : ATT_MAX_CLUSTER * G * (ATT_D + 4)];
@@ -126,6 +96,10 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   if (!FUSE && tid < G * ATT_D / 8)
     q_word = __ldcg(reinterpret_cast<const uint4*>(a.q + (size_t)b * a.q_stride + (size_t)kvh * G * ATT_D) + tid);
   const int L = __ldcg(&a.context_lens[b]);
+  // the grid covers P partitions: tokens past them would be dropped (and, in
+  // the fused variant, the new token never appended), so such a length is
+  // reported instead of silently truncated
+  if (L > a.P * a.part_tokens && blockIdx.x == 0 && tid == 0 && a.err_flag) atomicOr(a.err_flag, 1);
   const int t_begin = p * a.part_tokens;
   const int t_end = min(L, t_begin + a.part_tokens);
   const int npages = t_end > t_begin ? (t_end - t_begin + ATT_PAGE - 1) / ATT_PAGE : 0;
@@ -137,7 +111,7 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
 
   // this warp's pages: i = warp, warp + NW, ...
   const int my_pages = WP ? npages : (npages > warp ? (npages - warp + NW - 1) / NW : 0);
-  __half* myring = ring + (size_t)warp * ST * 2 * ATT_SSLICE;
+  unsigned char* myring = smraw + (size_t)warp * ST * SLOT;
 
   auto page_load = [&](int li) -> int {  // li: index into this warp's page list
     const int gi = pg0 + (WP ? li : warp + li * NW);
@@ -153,14 +127,29 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   // per page (K rows 0-15, then V rows 0-15), into the padded rows.  One
   // commit group per page (empty for a missing page).  Warp-wide.
   auto issue = [&](int li, int pg) {
-    __half* dst = myring + (size_t)(li % ST) * 2 * ATT_SSLICE;
-    if (pg >= 0) {
+    unsigned char* dst = myring + (size_t)(li % ST) * SLOT;
+    if (pg >= 0 && KV8) {
+      // FP8: 2 x 2 KiB of codes (8 x 16 bytes per row) and 2 x 64 bytes of row scales
+      const size_t row0 = ((size_t)pg * a.Hkv + kvh) * ATT_PAGE;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = lane + 32 * i;  // [K|V][row][8]
+        const int which = c >> 7, row = (c >> 3) & 15, col = c & 7;
+        cp_async16(dst + which * ATT8_CODES + row * ATT8_PITCH + col * 16,
+                   (which ? a.v8 : a.k8) + (row0 + row) * ATT_D + col * 16);
+      }
+      if (lane < 8) {
+        const int which = lane >> 2, part = lane & 3;
+        cp_async16(dst + 2 * ATT8_CODES + which * ATT_PAGE * 4 + part * 16, (which ? a.vs : a.ks) + row0 + 4 * part);
+      }
+    } else if (pg >= 0) {
       const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
+      __half* dh = reinterpret_cast<__half*>(dst);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = lane + 32 * i;  // 16-byte chunk of the page: [K|V][row][16]
         const int which = c >> 8, row = (c >> 4) & 15, col = c & 15;
-        cp_async16(dst + which * ATT_SSLICE + row * ATT_PITCH + col * 8,
+        cp_async16(dh + which * ATT_SSLICE + row * ATT_PITCH + col * 8,
                    (which ? a.v_pool : a.k_pool) + off + row * ATT_D + col * 8);
       }
     } else if (lane == 0 && li < my_pages && a.err_flag) {
@@ -225,14 +214,43 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
     }
     if (tid < ATT_D) s_vnew[tid] = vh;
     __syncthreads();
+    if (KV8 && warp < 2) {
+      // quantise the new k (warp 0) and v (warp 1) rows: the largest
+      // magnitude maps to 448, codes in fp32 round-to-nearest-even
+      const __half* src = warp == 0 ? s_knew : s_vnew;
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+      const __half* h4 = reinterpret_cast<const __half*>(&raw);
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(__half2float(h4[e])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+      const uint32_t c01 = f32x2_to_e4m3x2(__fmul_rn(__half2float(h4[0]), inv), __fmul_rn(__half2float(h4[1]), inv));
+      const uint32_t c23 = f32x2_to_e4m3x2(__fmul_rn(__half2float(h4[2]), inv), __fmul_rn(__half2float(h4[3]), inv));
+      *reinterpret_cast<uint32_t*>(&s_new8[warp][4 * lane]) = c01 | (c23 << 16);
+      if (lane == 0) s_new8_scale[warp] = __fdiv_rn(amax, 448.0f);
+    }
+    if (KV8) __syncthreads();
     if (pos >= cta_t0 && pos < cta_t1) {  // this CTA holds the new token: append it
       const int blk = pos / ATT_PAGE;
       const int pg = (blk < a.max_blocks) ? __ldcg(&bt[blk]) : -1;
       if (pg >= 0 && pg < a.num_pages) {
-        const size_t off = (((size_t)pg * a.Hkv + kvh) * ATT_PAGE + pos % ATT_PAGE) * ATT_D;
-        for (int d = tid; d < ATT_D; d += blockDim.x) {
-          a.k_pool[off + d] = s_knew[d];
-          a.v_pool[off + d] = s_vnew[d];
+        const size_t row = ((size_t)pg * a.Hkv + kvh) * ATT_PAGE + pos % ATT_PAGE;
+        if (KV8) {
+          for (int d = tid; d < ATT_D; d += blockDim.x) {
+            a.k8[row * ATT_D + d] = s_new8[0][d];
+            a.v8[row * ATT_D + d] = s_new8[1][d];
+          }
+          if (tid == 0) {
+            a.ks[row] = s_new8_scale[0];
+            a.vs[row] = s_new8_scale[1];
+          }
+        } else {
+          for (int d = tid; d < ATT_D; d += blockDim.x) {
+            a.k_pool[row * ATT_D + d] = s_knew[d];
+            a.v_pool[row * ATT_D + d] = s_vnew[d];
+          }
         }
       } else if (tid == 0 && a.err_flag) {
         atomicOr(a.err_flag, 1);
@@ -256,33 +274,19 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
   const int g = lane >> 2, t4 = lane & 3;
   const bool head_ok = g < G;
   uint32_t qa[8][2];  // q of head g, dims 16s + 2t4 + {0,1} and 16s + 8 + 2t4 + {0,1}, fp16
-#pragma unroll
-  for (int st = 0; st < 8; ++st) {
-    if (head_ok) {
-      const float* qrow = s_q[head_ok ? g : 0] + 16 * st + 2 * t4;
-      const __half2 lo = __floats2half2_rn(qrow[0], qrow[1]);
-      const __half2 hi = __floats2half2_rn(qrow[8], qrow[9]);
-      qa[st][0] = *reinterpret_cast<const uint32_t*>(&lo);
-      qa[st][1] = *reinterpret_cast<const uint32_t*>(&hi);
-    } else {
-      qa[st][0] = qa[st][1] = 0u;
-    }
-  }
+  attn_q_frags(s_q, G, g, t4, qa);
   float m_run = -INFINITY, l_run = 0.f;  // head g's running max (log2 domain) and sum
   float o[16][4];                        // P.V accumulators, n-block nb = dims 8nb..8nb+7
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
-  // ldmatrix row addresses (bytes within a slice): lane l feeds row l % 8 of
-  // tile l / 8
-  const int lt = lane >> 3, lr8 = lane & 7;
-  const uint32_t k_off = (uint32_t)((((lt >> 1) * 8 + lr8) * ATT_PITCH + (lt & 1) * 8) * 2);  // tokens x dims 16s+..
-  const uint32_t v_off = (uint32_t)((((lt & 1) * 8 + lr8) * ATT_PITCH + (lt >> 1) * 8) * 2);  // tokens x dims 8nb+..
+  const uint32_t k_off = attn_k_off(lane), v_off = attn_v_off(lane);
 
   for (int li = 0; li < my_pages; ++li) {
     const int stage = li % ST;
     cp_async_wait<ST - 1>();  // this lane's copies of page li landed
     __syncwarp();             // ... and every other lane's
-    __half* Ks = myring + (size_t)stage * 2 * ATT_SSLICE;
+    unsigned char* sl = myring + (size_t)stage * SLOT;
+    __half* Ks = reinterpret_cast<__half*>(sl);
     __half* Vs = Ks + ATT_SSLICE;
     const int gi = WP ? li : warp + li * NW;  // page index within the partition
     const int tok0 = (pg0 + gi) * ATT_PAGE;
@@ -291,61 +295,24 @@ __global__ void __launch_bounds__(NW * 32) paged_attn_kernel(const __grid_consta
     if (FUSE && page_ok && pos >= tok0 && pos < tok0 + ATT_PAGE) {
       // the page was fetched before the append: patch the new token's row
       const int slot = pos - tok0;
-      *reinterpret_cast<uint2*>(Ks + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_knew + 4 * lane);
-      *reinterpret_cast<uint2*>(Vs + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_vnew + 4 * lane);
+      if (KV8) {
+        *reinterpret_cast<uint32_t*>(sl + slot * ATT8_PITCH + 4 * lane) =
+            *reinterpret_cast<const uint32_t*>(&s_new8[0][4 * lane]);
+        *reinterpret_cast<uint32_t*>(sl + ATT8_CODES + slot * ATT8_PITCH + 4 * lane) =
+            *reinterpret_cast<const uint32_t*>(&s_new8[1][4 * lane]);
+        if (lane == 0) {
+          reinterpret_cast<float*>(sl + 2 * ATT8_CODES)[slot] = s_new8_scale[0];
+          reinterpret_cast<float*>(sl + 2 * ATT8_CODES)[ATT_PAGE + slot] = s_new8_scale[1];
+        }
+      } else {
+        *reinterpret_cast<uint2*>(Ks + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_knew + 4 * lane);
+        *reinterpret_cast<uint2*>(Vs + slot * ATT_PITCH + 4 * lane) = *reinterpret_cast<const uint2*>(s_vnew + 4 * lane);
+      }
       __syncwarp();
     }
     if (nv > 0) {
-      // ---- scores S[head][token], tokens 0-7 (n-block 0) and 8-15 (1) -------
-      float sc[2][4];
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
-      const uint32_t kbase = smem_u32(Ks) + k_off;
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        uint32_t b0, b1, b2, b3;  // (tokens 0-7: dims lo, hi), (tokens 8-15: dims lo, hi)
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                     : "r"(kbase + st * 32));
-        mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
-        mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
-      }
-      // ---- online softmax over this page (row g; four lanes share a row) ----
-      float s00 = sc[0][0] * a.scale_log2, s01 = sc[0][1] * a.scale_log2;
-      float s10 = sc[1][0] * a.scale_log2, s11 = sc[1][1] * a.scale_log2;
-      if (2 * t4 >= nv) s00 = -INFINITY;
-      if (2 * t4 + 1 >= nv) s01 = -INFINITY;
-      if (8 + 2 * t4 >= nv) s10 = -INFINITY;
-      if (8 + 2 * t4 + 1 >= nv) s11 = -INFINITY;
-      float mx = fmaxf(fmaxf(s00, s01), fmaxf(s10, s11));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);  // finite: token 0 of the page is valid
-      const float c = exp2f(m_run - m_new);  // 0 while m_run is -inf
-      const float p00 = exp2f(s00 - m_new), p01 = exp2f(s01 - m_new);
-      const float p10 = exp2f(s10 - m_new), p11 = exp2f(s11 - m_new);
-      float sum = (p00 + p01) + (p10 + p11);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      l_run = l_run * c + sum;
-      m_run = m_new;
-      const __half2 pa = __floats2half2_rn(p00, p01), pb = __floats2half2_rn(p10, p11);
-      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
-      // ---- O = O * c + P V ----------------------------------------------------
-      const uint32_t vbase = smem_u32(Vs) + v_off;
-#pragma unroll
-      for (int nb = 0; nb < 16; nb += 2) {
-        uint32_t b0, b1, b2, b3;  // (dims 8nb: tokens 0-7, 8-15), (dims 8nb+8: tokens 0-7, 8-15)
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                     : "r"(vbase + nb * 16));
-        o[nb][0] *= c;
-        o[nb][1] *= c;
-        o[nb + 1][0] *= c;
-        o[nb + 1][1] *= c;
-        mma_16816(o[nb], a0, a2, b0, b1);
-        mma_16816(o[nb + 1], a0, a2, b2, b3);
-      }
+      if (KV8) attn_page_fp8(sl, nv, qa, a.scale_log2, g, t4, m_run, l_run, o);
+      else attn_page(Ks, Vs, nv, qa, a.scale_log2, k_off, v_off, t4, m_run, l_run, o);
     }
     __syncwarp();
     // refill this stage with the page ST ahead (an empty group past the end)
@@ -540,21 +507,21 @@ void attention_workspace_layout(AttnArgs& a, void* ws, int B, int Hq, int P) {
   a.ws_ml = reinterpret_cast<float*>(w + ATT_TICKET_BYTES + up((size_t)B * Hq * P * ATT_D * 4));
 }
 
-template <int G, int NW, bool WP>
+template <int G, int NW, bool WP, bool KV8>
 static int launch_attn_gw(const AttnArgs& a, cudaStream_t s) {
-  static bool configured = false;
-  auto k0 = paged_attn_kernel<G, false, NW, WP>;
-  auto k1 = paged_attn_kernel<G, true, NW, WP>;
-  if (!configured) {
-    cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_smem(NW, att_stages(WP)));
-    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_smem(NW, att_stages(WP)));
-    configured = true;
-  }
+  static PerDeviceOnce once;
+  auto k0 = w4pg_paged_attn<G, false, NW, WP, KV8>;
+  auto k1 = w4pg_paged_attn<G, true, NW, WP, KV8>;
+  constexpr size_t smem = att_smem(NW, att_stages(WP), KV8);
+  once_per_device(once, [&] {
+    cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   dim3 grid(WP ? (a.P + NW - 1) / NW : a.P, a.Hkv, a.B);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NW * 32);
-  cfg.dynamicSmemBytes = att_smem(NW, att_stages(WP));
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -577,8 +544,9 @@ static int launch_attn_gw(const AttnArgs& a, cudaStream_t s) {
 template <int G>
 static int launch_attn_g(const AttnArgs& a, cudaStream_t s) {
   const long parts = (long)a.P * a.Hkv * a.B;
-  if (!a.use_cluster && parts >= 2L * num_sms()) return launch_attn_gw<G, 4, true>(a, s);
-  return launch_attn_gw<G, ATT_NW, false>(a, s);
+  const bool wp = !a.use_cluster && parts >= 2L * num_sms();
+  if (a.kv8) return wp ? launch_attn_gw<G, 4, true, true>(a, s) : launch_attn_gw<G, ATT_NW, false, true>(a, s);
+  return wp ? launch_attn_gw<G, 4, true, false>(a, s) : launch_attn_gw<G, ATT_NW, false, false>(a, s);
 }
 
 int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
@@ -605,7 +573,7 @@ int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 // RoPE + KV append: one CTA per sequence.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rope_append_kernel(const __grid_constant__ RopeArgs a) {
+__global__ void __launch_bounds__(256) w4pg_rope_append(const __grid_constant__ RopeArgs a) {
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
@@ -645,12 +613,69 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const __grid_constant_
   }
 }
 
+// RoPE + FP8 append: one CTA per sequence; q heads rotated in place, each kv
+// head's rotated k row and v row quantised by one warp (largest magnitude to
+// 448, fp32 round-to-nearest-even codes) into its slot.
+__global__ void __launch_bounds__(256) w4pg_rope_append_fp8(const __grid_constant__ RopeArgs a) {
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int pos = a.context_lens[b] - 1;
+  if (pos < 0) return;
+  const int blk = pos / ATT_PAGE, slot = pos % ATT_PAGE;
+  const int page = (blk < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + blk] : -1;
+  const bool ok = page >= 0 && page < a.num_pages;
+  if (!ok && threadIdx.x == 0 && a.err_flag) atomicOr(a.err_flag, 1);
+  const float fpos = (float)pos;
+  for (int idx = threadIdx.x; idx < a.Hq * (ATT_D / 2); idx += blockDim.x) {
+    const int head = idx / (ATT_D / 2), i = idx % (ATT_D / 2);
+    float sn, cs;
+    sincosf(__fmul_rn(fpos, a.inv_freq[i]), &sn, &cs);
+    __half* x = a.q + (size_t)b * a.stride_q + (size_t)head * ATT_D;
+    const float x0 = __half2float(x[i]), x1 = __half2float(x[i + ATT_D / 2]);
+    x[i] = __float2half_rn(x0 * cs - x1 * sn);
+    x[i + ATT_D / 2] = __float2half_rn(x1 * cs + x0 * sn);
+  }
+  if (!ok) return;
+  for (int kh = warp; kh < a.Hkv; kh += blockDim.x / 32) {
+    const __half* kx = a.k + (size_t)b * a.stride_kv + (size_t)kh * ATT_D;
+    const __half* vx = a.v + (size_t)b * a.stride_kv + (size_t)kh * ATT_D;
+    float kr[4], vr[4];  // dims lane, lane + 32, lane + 64, lane + 96
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = lane + 32 * e;
+      float sn, cs;
+      sincosf(__fmul_rn(fpos, a.inv_freq[i]), &sn, &cs);
+      const float x0 = __half2float(kx[i]), x1 = __half2float(kx[i + ATT_D / 2]);
+      kr[e] = __half2float(__float2half_rn(x0 * cs - x1 * sn));
+      kr[e + 2] = __half2float(__float2half_rn(x1 * cs + x0 * sn));
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) vr[e] = __half2float(vx[lane + 32 * e]);
+    const size_t row = ((size_t)page * a.Hkv + kh) * ATT_PAGE + slot;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float* r = which ? vr : kr;
+      float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+      uint8_t* dst = (which ? a.v8 : a.k8) + row * ATT_D;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = (uint8_t)(f32x2_to_e4m3x2(__fmul_rn(r[e], inv), 0.f) & 0xFFu);
+      if (lane == 0) (which ? a.vs : a.ks)[row] = __fdiv_rn(amax, 448.0f);
+    }
+  }
+}
+
 void rope_inv_freq_table(float theta, int D, float* out) {
   for (int i = 0; i < D / 2; ++i) out[i] = (float)std::pow((double)theta, -2.0 * (double)i / (double)D);
 }
 
 int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(rope_append_kernel, dim3(a.B), dim3(256), 0, s, a);
+  cudaError_t e = a.k8 ? launch_pdl(w4pg_rope_append_fp8, dim3(a.B), dim3(256), 0, s, a)
+                       : launch_pdl(w4pg_rope_append, dim3(a.B), dim3(256), 0, s, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "rope/append launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -831,6 +856,132 @@ extern "C" int kv_append_rope(uint16_t* q, const uint16_t* k, const uint16_t* v,
 }
 
 // ---------------------------------------------------------------------------
+// FP8 (E4M3) KV pages
+// ---------------------------------------------------------------------------
+static int check_fp8_pools(const uint8_t* k8, const uint8_t* v8, const float* ks, const float* vs, const char* who) {
+  W4_CHECK_ARG(k8 && v8 && ks && vs, "%s: null FP8 pool or scale pointer", who);
+  W4_CHECK_ALIGN(k8, 128, "k_pool");
+  W4_CHECK_ALIGN(v8, 128, "v_pool");
+  W4_CHECK_ALIGN(ks, 128, "k_scale");
+  W4_CHECK_ALIGN(vs, 128, "v_scale");
+  return W4A16_OK;
+}
+
+static int fp8_attention(const uint16_t* q, int q_stride, int fuse, uint8_t* k8, uint8_t* v8, float* ks, float* vs,
+                         int num_pages, const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                         int max_context, int B, int Hq, int Hkv, int D, float theta, float sm_scale,
+                         int partition_tokens, void* workspace, size_t workspace_bytes, uint16_t* out,
+                         int32_t* err_flag, cudaStream_t stream, const char* who) {
+  W4_CHECK_ARG(q && block_table && context_lens && out, "%s: null tensor pointer", who);
+  int rc = check_fp8_pools(k8, v8, ks, vs, who);
+  if (rc) return rc;
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1 && max_context >= 1,
+               "%s: sizes must be positive", who);
+  W4_CHECK_SHAPE(D == ATT_D, "%s: D=%d, only 128 is built", who, D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0 && Hq / Hkv <= 8, "%s: Hq=%d Hkv=%d", who, Hq, Hkv);
+  W4_CHECK_SHAPE(max_context <= max_blocks * ATT_PAGE, "%s: max_context > max_blocks*16", who);
+  if (fuse) W4_CHECK_ARG(theta > 0.f, "%s: theta must be positive", who);
+  if (partition_tokens <= 0) partition_tokens = default_partition(B, Hkv, max_context);
+  W4_CHECK_SHAPE(partition_tokens % ATT_PAGE == 0, "%s: partition_tokens %% 16 != 0", who);
+  const int min_stride = fuse ? (Hq + 2 * Hkv) * D : Hq * D;
+  if (q_stride == 0) q_stride = min_stride;
+  W4_CHECK_ARG(q_stride >= min_stride && (q_stride * 2) % 16 == 0, "%s: bad q_stride", who);
+  W4_CHECK_ALIGN(q, 128, "q");
+  W4_CHECK_ALIGN(out, 128, "out");
+  const int P = (max_context + partition_tokens - 1) / partition_tokens;
+  AttnArgs a = {};
+  if (P > 1) {
+    const size_t need = attention_workspace_bytes(B, Hq, Hkv, P);
+    W4_CHECK_ARG(workspace != nullptr && workspace_bytes >= need, "%s: workspace of %zu bytes needed", who, need);
+    W4_CHECK_ALIGN(workspace, 128, "workspace");
+    attention_workspace_layout(a, workspace, B, Hq, P);
+  }
+  a.q = reinterpret_cast<const __half*>(q);
+  a.kv8 = 1;
+  a.k8 = k8;
+  a.v8 = v8;
+  a.ks = ks;
+  a.vs = vs;
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  a.err_flag = err_flag;
+  a.q_stride = q_stride;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.P = P;
+  a.part_tokens = partition_tokens;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.fuse_rope_append = fuse;
+  if (fuse) rope_inv_freq_table(theta, D, a.inv_freq);
+  return launch_paged_attention(a, stream);
+}
+
+extern "C" int paged_gqa_decode_fp8(const uint16_t* q, int q_stride, const uint8_t* k_pool, const uint8_t* v_pool,
+                                    const float* k_scale, const float* v_scale, int num_pages,
+                                    const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                    int max_context, int B, int Hq, int Hkv, int D, float sm_scale,
+                                    int partition_tokens, void* workspace, size_t workspace_bytes, uint16_t* out,
+                                    int32_t* err_flag, w4a16_stream_t stream) {
+  return fp8_attention(q, q_stride, 0, const_cast<uint8_t*>(k_pool), const_cast<uint8_t*>(v_pool),
+                       const_cast<float*>(k_scale), const_cast<float*>(v_scale), num_pages, block_table, max_blocks,
+                       context_lens, max_context, B, Hq, Hkv, D, 0.f, sm_scale, partition_tokens, workspace,
+                       workspace_bytes, out, err_flag, (cudaStream_t)stream, "paged_gqa_decode_fp8");
+}
+
+extern "C" int paged_gqa_decode_rope_append_fp8(const uint16_t* qkv, int qkv_stride, uint8_t* k_pool,
+                                                uint8_t* v_pool, float* k_scale, float* v_scale, int num_pages,
+                                                const int32_t* block_table, int max_blocks,
+                                                const int32_t* context_lens, int max_context, int B, int Hq,
+                                                int Hkv, int D, float theta, float sm_scale, int partition_tokens,
+                                                void* workspace, size_t workspace_bytes, uint16_t* out,
+                                                int32_t* err_flag, w4a16_stream_t stream) {
+  return fp8_attention(qkv, qkv_stride, 1, k_pool, v_pool, k_scale, v_scale, num_pages, block_table, max_blocks,
+                       context_lens, max_context, B, Hq, Hkv, D, theta, sm_scale, partition_tokens, workspace,
+                       workspace_bytes, out, err_flag, (cudaStream_t)stream, "paged_gqa_decode_rope_append_fp8");
+}
+
+extern "C" int kv_append_rope_fp8(uint16_t* q, const uint16_t* k, const uint16_t* v, int row_stride,
+                                  uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale, int num_pages,
+                                  const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B,
+                                  int Hq, int Hkv, int D, float theta, int32_t* err_flag, w4a16_stream_t stream) {
+  W4_CHECK_ARG(q && k && v && block_table && context_lens, "kv_append_rope_fp8: null pointer");
+  int rc = check_fp8_pools(k_pool, v_pool, k_scale, v_scale, "kv_append_rope_fp8");
+  if (rc) return rc;
+  W4_CHECK_ARG(B >= 1 && Hq >= 1 && Hkv >= 1 && num_pages >= 1 && max_blocks >= 1, "kv_append_rope_fp8: sizes");
+  W4_CHECK_SHAPE(D == ATT_D, "kv_append_rope_fp8: D=%d, only 128 is built", D);
+  W4_CHECK_SHAPE(Hq % Hkv == 0, "kv_append_rope_fp8: Hq %% Hkv != 0");
+  W4_CHECK_ARG(theta > 0.f, "kv_append_rope_fp8: theta must be positive");
+  W4_CHECK_ARG(row_stride >= 0, "kv_append_rope_fp8: negative row_stride");
+  W4_CHECK_ALIGN(q, 128, "q");
+  W4_CHECK_ALIGN(k, 128, "k");
+  W4_CHECK_ALIGN(v, 128, "v");
+  RopeArgs a = {};
+  a.q = reinterpret_cast<__half*>(q);
+  a.k = reinterpret_cast<__half*>(const_cast<uint16_t*>(k));
+  a.v = reinterpret_cast<const __half*>(v);
+  a.k8 = k_pool;
+  a.v8 = v_pool;
+  a.ks = k_scale;
+  a.vs = v_scale;
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.err_flag = err_flag;
+  a.stride_q = row_stride ? row_stride : Hq * D;
+  a.stride_kv = row_stride ? row_stride : Hkv * D;
+  a.num_pages = num_pages;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  rope_inv_freq_table(theta, D, a.inv_freq);
+  return launch_rope_append(a, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
 // Allocation-free variant: the split-K scratch is a static device array.
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
 // memory, so its device address is looked up once per device and passed to
@@ -887,6 +1038,11 @@ extern "C" int paged_gqa_decode_noalloc(const uint16_t* q, int q_stride, const u
       return set_error(W4A16_ERR_SHAPE,
                        "paged_gqa_decode_noalloc: these sizes need %zu bytes of scratch; the static array holds %u",
                        need, (unsigned)W4A16_NOALLOC_SCRATCH_BYTES);
+    // the launcher repeats these checks; they come first here so that nothing
+    // is cleared for a call that is then refused
+    W4_CHECK_SHAPE(P <= ATT_MAX_PARTITIONS, "paged_gqa_decode_noalloc: %d partitions > %d", P, ATT_MAX_PARTITIONS);
+    W4_CHECK_SHAPE((size_t)B * Hkv * 4 <= ATT_TICKET_BYTES, "paged_gqa_decode_noalloc: B*Hkv=%d split-K tickets > %zu",
+                   B * Hkv, ATT_TICKET_BYTES / 4);
     void* base = nullptr;
     int rc = noalloc_scratch(&base);
     if (rc) return rc;

@@ -1,0 +1,276 @@
+// attn_core.cuh -- the per-page tensor-core step of the paged GQA decode
+// attention, shared by the stand-alone attention kernel and the persistent
+// decode kernel.
+//
+// Token t of a sequence lives in slot t % 16 of page block_table[t / 16]
+// ("Building a Custom LLM Inference Runtime on H100", explore.n1n.ai,
+// "2. The KV Cache and PagedAttention"); a (page, kv head) slice of the pool
+// is 16 rows of 128 fp16.  In shared memory the rows sit 272 bytes apart (16
+// bytes of padding), so the eight rows of an 8x8 ldmatrix tile fall on eight
+// different bank groups.  The G query heads that share a kv head are the M
+// rows (padded to 16) of warp-level mma.sync m16n8k16 products: the scores
+// S = Q K^T, an fp32 online softmax in registers (exp2, scale folded in), and
+// O += P V with the probabilities rounded to fp16 as the A operand.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+
+namespace w4 {
+
+constexpr int ATT_D = 128;
+constexpr int ATT_PAGE = 16;
+constexpr int ATT_SLICE = ATT_PAGE * ATT_D;        // halves per (page, kv head) slice in the pool
+constexpr int ATT_PITCH = ATT_D + 8;               // halves per row in shared memory
+constexpr int ATT_SSLICE = ATT_PAGE * ATT_PITCH;   // halves per slice in shared memory
+constexpr unsigned long long ATT_TIMEOUT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// d += A (16 x 16, fp16, rows 8-15 zero) x B (16 x 8, fp16), fp32 accumulate.
+// a0: A[g][2t..2t+1], a2: A[g][8+2t..8+2t+1]; b0, b1: B[2t..2t+1][g], B[8+2t..][g].
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// A fragments of the (rotated) query rows: lane (g = lane / 4, t4 = lane % 4)
+// holds head g, dims 16 s + 2 t4 + {0, 1} and 16 s + 8 + 2 t4 + {0, 1} for the
+// eight 16-dim k steps; heads g >= G are zero.
+__device__ __forceinline__ void attn_q_frags(const float (*s_q)[ATT_D], int G, int g, int t4, uint32_t (&qa)[8][2]) {
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    if (g < G) {
+      const float* qrow = s_q[g] + 16 * st + 2 * t4;
+      const __half2 lo = __floats2half2_rn(qrow[0], qrow[1]);
+      const __half2 hi = __floats2half2_rn(qrow[8], qrow[9]);
+      qa[st][0] = *reinterpret_cast<const uint32_t*>(&lo);
+      qa[st][1] = *reinterpret_cast<const uint32_t*>(&hi);
+    } else {
+      qa[st][0] = qa[st][1] = 0u;
+    }
+  }
+}
+
+// ldmatrix row addresses (bytes within a slice): lane l feeds row l % 8 of
+// tile l / 8; K tiles are tokens x dims, V tiles (read transposed) tokens x dims.
+__device__ __forceinline__ uint32_t attn_k_off(int lane) {
+  const int lt = lane >> 3, lr8 = lane & 7;
+  return (uint32_t)((((lt >> 1) * 8 + lr8) * ATT_PITCH + (lt & 1) * 8) * 2);
+}
+__device__ __forceinline__ uint32_t attn_v_off(int lane) {
+  const int lt = lane >> 3, lr8 = lane & 7;
+  return (uint32_t)((((lt & 1) * 8 + lr8) * ATT_PITCH + (lt >> 1) * 8) * 2);
+}
+
+// One page (nv >= 1 valid tokens, K rows at Ks and V rows at Vs in the padded
+// layout) against the warp's query fragments: scores, online-softmax update
+// of this lane's head (m_run in the log2 domain, l_run the running sum) and
+// O = O * c + P V.  Warp-wide.
+__device__ __forceinline__ void attn_page(const __half* Ks, const __half* Vs, int nv, const uint32_t (&qa)[8][2],
+                                          float scale_log2, uint32_t k_off, uint32_t v_off, int t4, float& m_run,
+                                          float& l_run, float (&o)[16][4]) {
+  // ---- scores S[head][token], tokens 0-7 (n-block 0) and 8-15 (1) -------
+  float sc[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  const uint32_t kbase = smem_u32(Ks) + k_off;
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    uint32_t b0, b1, b2, b3;  // (tokens 0-7: dims lo, hi), (tokens 8-15: dims lo, hi)
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(kbase + st * 32));
+    mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
+    mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
+  }
+  // ---- online softmax over this page (row g; four lanes share a row) ----
+  float s00 = sc[0][0] * scale_log2, s01 = sc[0][1] * scale_log2;
+  float s10 = sc[1][0] * scale_log2, s11 = sc[1][1] * scale_log2;
+  if (2 * t4 >= nv) s00 = -INFINITY;
+  if (2 * t4 + 1 >= nv) s01 = -INFINITY;
+  if (8 + 2 * t4 >= nv) s10 = -INFINITY;
+  if (8 + 2 * t4 + 1 >= nv) s11 = -INFINITY;
+  float mx = fmaxf(fmaxf(s00, s01), fmaxf(s10, s11));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float m_new = fmaxf(m_run, mx);  // finite: token 0 of the page is valid
+  const float c = exp2f(m_run - m_new);  // 0 while m_run is -inf
+  const float p00 = exp2f(s00 - m_new), p01 = exp2f(s01 - m_new);
+  const float p10 = exp2f(s10 - m_new), p11 = exp2f(s11 - m_new);
+  float sum = (p00 + p01) + (p10 + p11);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  l_run = l_run * c + sum;
+  m_run = m_new;
+  const __half2 pa = __floats2half2_rn(p00, p01), pb = __floats2half2_rn(p10, p11);
+  const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
+  // ---- O = O * c + P V ----------------------------------------------------
+  const uint32_t vbase = smem_u32(Vs) + v_off;
+#pragma unroll
+  for (int nb = 0; nb < 16; nb += 2) {
+    uint32_t b0, b1, b2, b3;  // (dims 8nb: tokens 0-7, 8-15), (dims 8nb+8: tokens 0-7, 8-15)
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(vbase + nb * 16));
+    o[nb][0] *= c;
+    o[nb][1] *= c;
+    o[nb + 1][0] *= c;
+    o[nb + 1][1] *= c;
+    mma_16816(o[nb], a0, a2, b0, b1);
+    mma_16816(o[nb + 1], a0, a2, b2, b3);
+  }
+}
+
+// The same page step for half of the head dimensions: P V only for dims
+// [64 dh, 64 dh + 64) (o holds those 8 n-blocks).  Two warps that share a page,
+// one per half, keep identical softmax states and half the accumulators each.
+__device__ __forceinline__ void attn_page_half(const __half* Ks, const __half* Vs, int nv, const uint32_t (&qa)[8][2],
+                                               float scale_log2, uint32_t k_off, uint32_t v_off, int t4, int dh,
+                                               float& m_run, float& l_run, float (&o)[8][4]) {
+  float sc[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  const uint32_t kbase = smem_u32(Ks) + k_off;
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    uint32_t b0, b1, b2, b3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(kbase + st * 32));
+    mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
+    mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
+  }
+  float s00 = sc[0][0] * scale_log2, s01 = sc[0][1] * scale_log2;
+  float s10 = sc[1][0] * scale_log2, s11 = sc[1][1] * scale_log2;
+  if (2 * t4 >= nv) s00 = -INFINITY;
+  if (2 * t4 + 1 >= nv) s01 = -INFINITY;
+  if (8 + 2 * t4 >= nv) s10 = -INFINITY;
+  if (8 + 2 * t4 + 1 >= nv) s11 = -INFINITY;
+  float mx = fmaxf(fmaxf(s00, s01), fmaxf(s10, s11));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  const float c = exp2f(m_run - m_new);
+  const float p00 = exp2f(s00 - m_new), p01 = exp2f(s01 - m_new);
+  const float p10 = exp2f(s10 - m_new), p11 = exp2f(s11 - m_new);
+  float sum = (p00 + p01) + (p10 + p11);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  l_run = l_run * c + sum;
+  m_run = m_new;
+  const __half2 pa = __floats2half2_rn(p00, p01), pb = __floats2half2_rn(p10, p11);
+  const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
+  const uint32_t vbase = smem_u32(Vs) + v_off + (uint32_t)(dh * 128);
+#pragma unroll
+  for (int nb = 0; nb < 8; nb += 2) {
+    uint32_t b0, b1, b2, b3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(vbase + nb * 16));
+    o[nb][0] *= c;
+    o[nb][1] *= c;
+    o[nb + 1][0] *= c;
+    o[nb + 1][1] *= c;
+    mma_16816(o[nb], a0, a2, b0, b1);
+    mma_16816(o[nb + 1], a0, a2, b2, b3);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) pages: a (page, kv head) slice holds 16 rows of 128 one-byte
+// codes per K and V plus one fp32 scale per row (value = code * scale).  In
+// shared memory the code rows sit 144 bytes apart (16 bytes of padding: the
+// 16-bit fragment loads of eight rows fall on eight bank groups), followed
+// by the 16 K and 16 V scales.
+// ---------------------------------------------------------------------------
+constexpr int ATT8_PITCH = ATT_D + 16;                         // bytes per code row in shared memory
+constexpr int ATT8_CODES = ATT_PAGE * ATT8_PITCH;              // bytes of one slice's K (or V) codes
+constexpr int ATT8_SLOT = 2 * ATT8_CODES + 2 * ATT_PAGE * 4;   // K codes | V codes | K scales | V scales
+static_assert(ATT8_SLOT % 16 == 0, "slots stay 16-byte aligned");
+
+// two E4M3 codes (low byte first) -> half2 (exact: every E4M3 value is an fp16)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(d) : "r"(two));
+  return d;
+}
+// E4M3 codes of two fp32 values, round to nearest even, saturating at 448:
+// lo in the low byte, hi in the high byte
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
+      : "=r"(d)
+      : "f"(hi), "f"(lo));
+  return d;
+}
+
+// One FP8 page against the warp's query fragments (the fp16 step above with
+// the codes converted while the fragments are built): scores scaled by the
+// K row scales, probabilities by the V row scales before P V (the softmax
+// sum keeps the unscaled probabilities).
+__device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv, const uint32_t (&qa)[8][2],
+                                              float scale_log2, int g, int t4, float& m_run, float& l_run,
+                                              float (&o)[16][4]) {
+  const unsigned char* Kc = slot;
+  const unsigned char* Vc = slot + ATT8_CODES;
+  const float* ks = reinterpret_cast<const float*>(slot + 2 * ATT8_CODES);
+  const float* vs = ks + ATT_PAGE;
+  float sc[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  const unsigned char* k0 = Kc + g * ATT8_PITCH + 2 * t4;        // token g
+  const unsigned char* k1 = k0 + 8 * ATT8_PITCH;                 // token 8 + g
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    const uint32_t b0 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k0 + 16 * st));
+    const uint32_t b1 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k0 + 16 * st + 8));
+    const uint32_t b2 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k1 + 16 * st));
+    const uint32_t b3 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k1 + 16 * st + 8));
+    mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
+    mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
+  }
+  float s00 = sc[0][0] * ks[2 * t4] * scale_log2, s01 = sc[0][1] * ks[2 * t4 + 1] * scale_log2;
+  float s10 = sc[1][0] * ks[8 + 2 * t4] * scale_log2, s11 = sc[1][1] * ks[9 + 2 * t4] * scale_log2;
+  if (2 * t4 >= nv) s00 = -INFINITY;
+  if (2 * t4 + 1 >= nv) s01 = -INFINITY;
+  if (8 + 2 * t4 >= nv) s10 = -INFINITY;
+  if (8 + 2 * t4 + 1 >= nv) s11 = -INFINITY;
+  float mx = fmaxf(fmaxf(s00, s01), fmaxf(s10, s11));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  const float c = exp2f(m_run - m_new);
+  const float p00 = exp2f(s00 - m_new), p01 = exp2f(s01 - m_new);
+  const float p10 = exp2f(s10 - m_new), p11 = exp2f(s11 - m_new);
+  float sum = (p00 + p01) + (p10 + p11);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  l_run = l_run * c + sum;
+  m_run = m_new;
+  const __half2 pa = __floats2half2_rn(p00 * vs[2 * t4], p01 * vs[2 * t4 + 1]);
+  const __half2 pb = __floats2half2_rn(p10 * vs[8 + 2 * t4], p11 * vs[9 + 2 * t4]);
+  const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
+  // V fragments: tokens (2 t4, 2 t4 + 1) and (8 + 2 t4, 9 + 2 t4) of dim 8 nb + g
+  const unsigned char* v0 = Vc + (2 * t4) * ATT8_PITCH + g;
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    const uint32_t lo0 = v0[8 * nb], hi0 = v0[ATT8_PITCH + 8 * nb];
+    const uint32_t lo1 = v0[8 * ATT8_PITCH + 8 * nb], hi1 = v0[9 * ATT8_PITCH + 8 * nb];
+    const uint32_t b0 = e4m3x2_to_h2(lo0 | (hi0 << 8));
+    const uint32_t b1 = e4m3x2_to_h2(lo1 | (hi1 << 8));
+    o[nb][0] *= c;
+    o[nb][1] *= c;
+    mma_16816(o[nb], a0, a2, b0, b1);
+  }
+}
+
+}  // namespace w4

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "w4a16.h"
 
 namespace w4 {
@@ -18,6 +20,23 @@ int check_launch(const char* what);
 bool aligned(const void* p, size_t a);
 int num_sms();
 int device_index();
+
+// One-time set-up per device (kernel attributes such as the dynamic shared
+// memory limit are per device): f() runs once for each device ordinal that
+// reaches it, under a lock, before any caller on that device proceeds.
+struct PerDeviceOnce {
+  std::mutex mu;
+  unsigned long long done = 0;  // bit d: device d is set up (ordinals < 64)
+};
+template <class F>
+inline void once_per_device(PerDeviceOnce& o, F f) {
+  const unsigned long long bit = 1ull << (device_index() & 63);
+  std::lock_guard<std::mutex> lk(o.mu);
+  if (!(o.done & bit)) {
+    f();
+    o.done |= bit;
+  }
+}
 
 #define W4_CHECK_ARG(cond, ...)                                   \
   do {                                                            \
@@ -96,6 +115,18 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                "l"(gmem_src)
                : "memory");
 }
+// 16-byte cp.async that writes zeros when `valid` is false (src not read).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+// 4-byte cp.async (through L1) that writes zeros when `valid` is false.
+__device__ __forceinline__ void cp_async4_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(valid ? 4 : 0)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -153,7 +184,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// mbarrier + 1-D bulk copy (TMA) helpers.  All waits are bounded: a wait
+// mbarrier helpers.  All waits are bounded: a wait
 // that runs out sets *timed_out and returns false instead of spinning.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -234,16 +265,6 @@ __device__ __forceinline__ float ld_dsmem(const float* p, int rank) {
   float v;
   asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
   return v;
-}
-
-// 1-D bulk async copy global -> shared, completion signalled on `bar`.
-// src, dst 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------

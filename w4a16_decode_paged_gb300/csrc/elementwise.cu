@@ -14,7 +14,7 @@ namespace w4 {
 // ---------------------------------------------------------------------------
 // RMSNorm: one CTA per row.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const __half* __restrict__ x, const __half* __restrict__ gamma,
+__global__ void __launch_bounds__(256) w4pg_rmsnorm(const __half* __restrict__ x, const __half* __restrict__ gamma,
                                                       __half* y, int H, float eps, int tag) {
   __shared__ float red[8];
   __shared__ float rs;
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __half* __restrict__
 
 int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s,
                    int tag) {
-  cudaError_t e = launch_pdl(rmsnorm_kernel, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps, tag);
+  cudaError_t e = launch_pdl(w4pg_rmsnorm, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "rmsnorm launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -64,9 +64,9 @@ int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H
 // ---------------------------------------------------------------------------
 // Embedding gather (+ optional device-side context length advance).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) embedding_kernel(const __half* __restrict__ embed, int vocab, int H,
+__global__ void __launch_bounds__(256) w4pg_embedding(const __half* __restrict__ embed, int vocab, int H,
                                                         const int32_t* tokens, __half* x, int32_t* err_flag,
-                                                        int32_t* lens, int tag) {
+                                                        int32_t* lens, int max_len, int tag) {
   W4_TRACE_SCOPE(tag);
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
@@ -77,14 +77,59 @@ __global__ void __launch_bounds__(256) embedding_kernel(const __half* __restrict
   const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)(ok ? tok : 0) * H);
   uint4* dst = reinterpret_cast<uint4*>(x + (size_t)b * H);
   for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
-  if (lens && threadIdx.x == 0) lens[b] += 1;
+  if (lens && threadIdx.x == 0) {
+    // the model's buffers and attention partitions cover max_len tokens: a
+    // longer context is reported, not silently truncated
+    const int n = lens[b] + 1;
+    if (n > max_len && err_flag) atomicOr(err_flag, 1);
+    lens[b] = n;
+  }
 }
 
 int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
-                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s, int tag) {
-  cudaError_t e = launch_pdl(embedding_kernel, dim3(B), dim3(256), 0, s, embed, vocab, H, tokens, x, err_flag,
-                             lens_to_advance, tag);
+                     int32_t* err_flag, int32_t* lens_to_advance, int max_len, cudaStream_t s, int tag) {
+  cudaError_t e = launch_pdl(w4pg_embedding, dim3(B), dim3(256), 0, s, embed, vocab, H, tokens, x, err_flag,
+                             lens_to_advance, max_len, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "embedding launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Prefill bookkeeping: the T prompt tokens of one sequence run as T rows
+// whose lengths are len0 + 1 .. len0 + T over copies of the sequence's
+// block-table row (token t attends to positions <= len0 + t); afterwards the
+// sequence's length advances by T.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) w4pg_prefill_rows(const int32_t* __restrict__ bt_row, int max_blocks,
+                                                         const int32_t* __restrict__ len0, int T,
+                                                         int32_t* __restrict__ bt_rep, int32_t* __restrict__ lens) {
+  pdl_wait_then_trigger();
+  const int l0 = *len0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * max_blocks; i += gridDim.x * blockDim.x) {
+    const int t = i / max_blocks, j = i - t * max_blocks;
+    bt_rep[i] = bt_row[j];
+    if (j == 0) lens[t] = l0 + t + 1;
+  }
+}
+__global__ void __launch_bounds__(32) w4pg_advance_len(int32_t* len, int T, int max_len, int32_t* err_flag) {
+  pdl_wait_then_trigger();
+  if (threadIdx.x == 0) {
+    const int n = *len + T;
+    if (n > max_len && err_flag) atomicOr(err_flag, 1);
+    *len = n;
+  }
+}
+int launch_prefill_rows(const int32_t* bt_row, int max_blocks, const int32_t* len0, int T, int32_t* bt_rep,
+                        int32_t* lens, cudaStream_t s) {
+  const int blocks = std::max(1, std::min(1024, (T * max_blocks + 255) / 256));
+  cudaError_t e = launch_pdl(w4pg_prefill_rows, dim3(blocks), dim3(256), 0, s, bt_row, max_blocks, len0, T, bt_rep,
+                             lens);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "prefill rows launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+int launch_advance_len(int32_t* len, int T, int max_len, int32_t* err_flag, cudaStream_t s) {
+  cudaError_t e = launch_pdl(w4pg_advance_len, dim3(1), dim3(32), 0, s, len, T, max_len, err_flag);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "advance length launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
 
@@ -105,7 +150,7 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
   return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
 
-__global__ void __launch_bounds__(LM_WPB * 32) lm_head_kernel(const __grid_constant__ LmHeadArgs a) {
+__global__ void __launch_bounds__(LM_WPB * 32) w4pg_lm_head_argmax(const __grid_constant__ LmHeadArgs a) {
   extern __shared__ uint4 xsm[];  // [B][H/8]
   __shared__ unsigned long long wbest[LM_WPB][LM_MAXB];
   __shared__ float red[LM_WPB];
@@ -251,18 +296,16 @@ size_t lm_head_workspace_bytes(int B, int vocab) {
 
 int launch_lm_head_argmax(const LmHeadArgs& a, cudaStream_t s) {
   const size_t smem = (size_t)a.B * a.H * 2;
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    configured = true;
-  }
+  static PerDeviceOnce once;
+  once_per_device(once,
+                  [] { cudaFuncSetAttribute(w4pg_lm_head_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024); });
   int bps = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, lm_head_kernel, LM_WPB * 32, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, w4pg_lm_head_argmax, LM_WPB * 32, smem) != cudaSuccess ||
       bps < 1)
     bps = 1;
   int blocks = std::min((a.vocab + 2 * LM_WPB - 1) / (2 * LM_WPB), bps * num_sms());
   blocks = std::max(1, std::min(blocks, LM_MAX_BLOCKS));
-  cudaError_t e = launch_pdl(lm_head_kernel, dim3(blocks), dim3(LM_WPB * 32), smem, s, a);
+  cudaError_t e = launch_pdl(w4pg_lm_head_argmax, dim3(blocks), dim3(LM_WPB * 32), smem, s, a);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "lm_head launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -292,7 +335,7 @@ extern "C" int embedding_gather(const uint16_t* embed, int vocab, int H, const i
   W4_CHECK_ALIGN(embed, 128, "embed");
   W4_CHECK_ALIGN(x, 128, "x");
   return launch_embedding(reinterpret_cast<const __half*>(embed), vocab, H, tokens, B, reinterpret_cast<__half*>(x),
-                          err_flag, nullptr, (cudaStream_t)stream);
+                          err_flag, nullptr, 0, (cudaStream_t)stream);
 }
 
 extern "C" size_t lm_head_argmax_workspace_size(int B, int vocab) { return lm_head_workspace_bytes(B, vocab); }

@@ -35,6 +35,7 @@
 // the epilogue.  Dense fp16 weights (the batched lm_head) are copied into the
 // ring in the canonical layout and used by the MMA as they are.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 
 #include "common.cuh"
@@ -80,12 +81,6 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// 16-byte cp.async that writes zeros when `valid` is false (src not read).
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
 
 // Shared-memory matrix descriptor: no swizzle, K-major, LBO = 128 B between
 // K-adjacent core matrices, SBO = 256 B between 8-row groups.
@@ -140,14 +135,15 @@ __device__ __forceinline__ uint4 codes_word(uint32_t w) {
 
 // Bounded mbarrier wait that also gives up as soon as another role of the
 // CTA has given up (*fail set); a wait that runs out sets *fail.
-__device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatile int* fail) {
+__device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatile int* fail,
+                                         unsigned long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = tc_now();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*fail) return false;
-    if (tc_now() - t0 > TC_TIMEOUT_NS) {
+    if (tc_now() - t0 > limit) {
       *fail = 1;
       return false;
     }
@@ -180,13 +176,13 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //   gfull[b]     MMAs of the group in tensor-memory buffer b   (1, commit)
 //   gempty[b]    readers read tensor-memory buffer b           (256)
 template <bool INT4, bool SILU>
-__global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU>;
   constexpr int NA = SH::NA;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
-  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[TC_NAB], aempty[TC_NAB], gfull[2], gempty[2];
+  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[TC_NAB], aempty[TC_NAB], gfull[2], gempty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -196,6 +192,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
   const int nst = K / TC_K, ps = a.per_split, ks = a.ksplit;
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nwork = ntiles * ks;
+  const unsigned long long wl = a.wait_limit_ns;
   W4_TRACE_SCOPE(a.tag);
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
@@ -221,6 +218,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
       mbar_init(&gfull[i], 1);
       mbar_init(&gempty[i], TC_READERS);
     }
+    mbar_init(&drain, 1);
     s_fail = 0;
     fence_mbar_init();
   }
@@ -355,7 +353,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
       if (c_next(cur) && cur.work < nwork) item_rows();
     for (uint32_t s = npro; cur.work < nwork; ++s) {
       const int slot = s % TC_S;
-      if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail)) break;
+      if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
       load_a(slot);
       load_b(slot, cur.st);
       cp_async_mbar_arrive(&full[slot]);
@@ -373,9 +371,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
         const int slot = s % TC_S, ab = s % TC_NAB;
         const uint32_t grp = s >> 1;
         const bool gfirst = (s & 1) == 0;
-        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail)) break;
-        if (INT4 && !tcw_wait(&afull[ab], (s / TC_NAB) & 1, &s_fail)) break;
-        if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail)) break;
+        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl)) break;
+        if (INT4 && !tcw_wait(&afull[ab], (s / TC_NAB) & 1, &s_fail, wl)) break;
+        if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl)) break;
         fence_proxy_async_smem();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         unsigned char* sl = ring + slot * SH::SLOT;
@@ -410,9 +408,14 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
         if (!gfirst) tc_commit(&gfull[grp & 1]);
         c_next(cur);
       }
-      // before tensor memory is freed no MMA may be in flight: the last
-      // commit (to empty[]) covers all earlier MMAs
-      if (s > 0) (void)tcw_wait(&empty[(s - 1) % TC_S], ((s - 1) / TC_S) & 1, &s_fail);
+      // before tensor memory is freed no MMA may be in flight: one more
+      // commit tracks every MMA this thread issued, and its wait ignores an
+      // abort elsewhere in the CTA (the MMAs finish on their own; the wait
+      // keeps the normal bound)
+      if (s > 0) {
+        tc_commit(&drain);
+        (void)tc_wait(&drain, 0);
+      }
     }
   } else {
     // =========================== readers ====================================
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
 
     // add tensor-memory group `grp` (this row, 16 columns) times the scales
     auto tm_read = [&](uint32_t grp) {
-      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail));
+      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail, wl));
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
@@ -536,8 +539,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) gemm_tc_kernel(const __grid_
       const bool gfirst = (s & 1) == 0;
       if (INT4) {
         // (1) the A buffer's previous MMAs are done, the slot's copies landed
-        if (s >= TC_NAB) (void)tcw_wait(&aempty[ab], ((s - TC_NAB) / TC_NAB) & 1, &s_fail);
-        (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail);
+        if (s >= TC_NAB) (void)tcw_wait(&aempty[ab], ((s - TC_NAB) / TC_NAB) & 1, &s_fail, wl);
+        (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl);
         // (2) this group's scale (used when the group is read, three stages on)
         // (loaded straight into the register that holds it until the read,
         // so the load's latency is not waited for here)
@@ -614,18 +617,19 @@ void tc_workspace_layout(TcArgs& a, void* ws) {
 
 template <bool INT4, bool SILU>
 static int tc_ctas_per_sm() {
-  static int cached = 0;
-  if (cached == 0) {
-    auto kern = gemm_tc_kernel<INT4, SILU>;
+  static PerDeviceOnce once;
+  static int cached[64] = {};
+  once_per_device(once, [] {
+    auto kern = w4pg_tc_batch<INT4, SILU>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcShape<INT4, SILU>::SMEM);
     int bps = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, TcShape<INT4, SILU>::SMEM) !=
             cudaSuccess ||
         bps < 1)
       bps = 1;
-    cached = std::min(bps, 4);  // tensor memory: at most 4 x 128 columns per SM
-  }
-  return cached;
+    cached[device_index() & 63] = std::min(bps, 4);  // tensor memory: at most 4 x 128 columns per SM
+  });
+  return cached[device_index() & 63];
 }
 
 static int tc_slots(bool int4, bool silu) {
@@ -659,8 +663,17 @@ void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, 
   *per_split = best_ps;
 }
 
+// Bound of the persistent decode kernel's grid-barrier waits (the test hook
+// below changes it).  The tensor-core GEMM always keeps its own 2 s bound:
+// when one of its roles gives up, the others still run to the end of their
+// work item against shared-memory and tensor-memory buffers the tensor core
+// may be using, so its abort is only a last resort, not something to trigger.
+static std::atomic<unsigned long long> g_wait_limit_ns{TC_TIMEOUT_NS};
+unsigned long long tc_wait_limit_ns() { return g_wait_limit_ns.load(); }
+
 int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   TcArgs a = a_in;
+  a.wait_limit_ns = TC_TIMEOUT_NS;
   if (a.M < 1 || a.M > TC_N) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, TC_N);
   // stages pair into 128-wide groups (the int4 scale group), dense weights too
   if (a.K % 128 != 0) return set_error(W4A16_ERR_SHAPE, "gemm_tc: K=%d not a multiple of 128", a.K);
@@ -678,9 +691,9 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
     if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemm_tc launch: %s", cudaGetErrorString(e));
     return W4A16_OK;
   };
-  if (!int4) return go(gemm_tc_kernel<false, false>, TcShape<false, false>::SMEM, tc_ctas_per_sm<false, false>());
-  if (silu) return go(gemm_tc_kernel<true, true>, TcShape<true, true>::SMEM, tc_ctas_per_sm<true, true>());
-  return go(gemm_tc_kernel<true, false>, TcShape<true, false>::SMEM, tc_ctas_per_sm<true, false>());
+  if (!int4) return go(w4pg_tc_batch<false, false>, TcShape<false, false>::SMEM, tc_ctas_per_sm<false, false>());
+  if (silu) return go(w4pg_tc_batch<true, true>, TcShape<true, true>::SMEM, tc_ctas_per_sm<true, true>());
+  return go(w4pg_tc_batch<true, false>, TcShape<true, false>::SMEM, tc_ctas_per_sm<true, false>());
 }
 
 }  // namespace w4
@@ -689,7 +702,7 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
 // argmax over fp32 logit rows (lowest index on ties), optional fp16 copy
 // ---------------------------------------------------------------------------
 namespace w4 {
-__global__ void __launch_bounds__(256) argmax_rows_kernel(const float* __restrict__ logits, int V, int32_t* tokens,
+__global__ void __launch_bounds__(256) w4pg_argmax_rows(const float* __restrict__ logits, int V, int32_t* tokens,
                                                           __half* logits16, int tag) {
   W4_TRACE_SCOPE(tag);
   pdl_wait_then_trigger();
@@ -721,7 +734,7 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(const float* __restric
 
 int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
                        int tag) {
-  cudaError_t e = launch_pdl(argmax_rows_kernel, dim3(B), dim3(256), 0, s, logits, V, tokens, logits16, tag);
+  cudaError_t e = launch_pdl(w4pg_argmax_rows, dim3(B), dim3(256), 0, s, logits, V, tokens, logits16, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "argmax launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -731,6 +744,10 @@ int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __hal
 // C ABI
 // ---------------------------------------------------------------------------
 using namespace w4;
+
+extern "C" unsigned long long w4a16_debug_set_wait_limit_ns(unsigned long long ns) {
+  return g_wait_limit_ns.exchange(ns);
+}
 
 extern "C" size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu) {
   (void)M;

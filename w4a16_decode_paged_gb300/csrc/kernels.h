@@ -45,7 +45,12 @@ struct TcArgs {
   int32_t* err_flag;
   int M, K, N, ldy, ksplit, tag;
   int per_split;           // stages (64 k) per split, even; 0: ceil(stages / ksplit)
+  unsigned long long wait_limit_ns;  // bound of every mbarrier wait (set by the launcher)
 };
+// Bound of the persistent decode kernel's grid-barrier waits, read at each
+// launch (w4a16_debug_set_wait_limit_ns changes it; 0 = give up at the first
+// barrier that is not already complete).
+unsigned long long tc_wait_limit_ns();
 int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
 
 // Split-K workspaces (tensor-core GEMM and attention) start with a fixed
@@ -79,6 +84,13 @@ struct AttnArgs {
   int use_cluster;          // set by the launcher: partitions merged in a thread-block cluster
   float inv_freq[64];       // RoPE inverse frequencies (fused variant)
   int tag;                  // launch index (kernel timeline builds only)
+  // FP8 (E4M3) pages instead of k_pool / v_pool: codes [pages][Hkv][16][D]
+  // and fp32 row scales [pages][Hkv][16] (value = code * scale)
+  int kv8;
+  uint8_t* k8;
+  uint8_t* v8;
+  float* ks;
+  float* vs;
 };
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
 constexpr int ATT_MAX_PARTITIONS = 1024;
@@ -97,14 +109,24 @@ struct RopeArgs {
   int32_t* err_flag;
   int stride_q, stride_kv, num_pages, max_blocks, B, Hq, Hkv;
   float inv_freq[64];       // fp32 inverse frequencies, D = 128
+  // FP8 pools (non-null k8 selects them): codes and fp32 row scales
+  uint8_t* k8;
+  uint8_t* v8;
+  float* ks;
+  float* vs;
 };
 int launch_rope_append(const RopeArgs& a, cudaStream_t s);
 void rope_inv_freq_table(float theta, int D, float* out);
 
 int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s,
                    int tag = 0);
+// lens_to_advance (nullable): context_lens[b] += 1; a length above max_len sets bit 0 of err_flag
 int launch_embedding(const __half* embed, int vocab, int H, const int32_t* tokens, int B, __half* x,
-                     int32_t* err_flag, int32_t* lens_to_advance, cudaStream_t s, int tag = 0);
+                     int32_t* err_flag, int32_t* lens_to_advance, int max_len, cudaStream_t s, int tag = 0);
+
+int launch_prefill_rows(const int32_t* bt_row, int max_blocks, const int32_t* len0, int T, int32_t* bt_rep,
+                        int32_t* lens, cudaStream_t s);
+int launch_advance_len(int32_t* len, int T, int max_len, int32_t* err_flag, cudaStream_t s);
 
 struct LmHeadArgs {
   const __half* x;      // [B][H]

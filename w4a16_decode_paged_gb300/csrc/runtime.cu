@@ -21,6 +21,8 @@
 // projection becomes [RMSNorm] + a tensor-core GEMM (exact int4 codes into
 // tcgen05 MMAs, K split across CTAs), and the lm_head a tensor-core GEMM to
 // fp32 logits followed by a row-wise argmax.
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -29,6 +31,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "persistent.h"
 
 namespace w4 {
 int default_partition(int B, int Hkv, int max_context);
@@ -37,11 +40,11 @@ int default_partition(int B, int Hkv, int max_context);
 using namespace w4;
 
 struct GraphKey {
-  int B, max_blocks;
+  int B, max_blocks, persistent;
   const void *tin, *tout, *bt, *lens, *logits;
   bool operator<(const GraphKey& o) const {
-    return std::tie(B, max_blocks, tin, tout, bt, lens, logits) <
-           std::tie(o.B, o.max_blocks, o.tin, o.tout, o.bt, o.lens, o.logits);
+    return std::tie(B, max_blocks, persistent, tin, tout, bt, lens, logits) <
+           std::tie(o.B, o.max_blocks, o.persistent, o.tin, o.tout, o.bt, o.lens, o.logits);
   }
 };
 
@@ -63,6 +66,18 @@ struct w4a16_model {
   size_t tc_ws_bytes = 0;
   int32_t* err_flag = nullptr;
   float inv_freq[64];
+  // persistent decode kernel (one sequence): layer table, attention partials
+  // and tickets, per-CTA argmax keys, control words (barrier counter, step
+  // counter, abort flag, lm_head ticket)
+  bool pk_ok = false;
+  int decode_path = W4A16_PATH_AUTO;
+  int pk_P = 0;
+  PkLayer* pk_layers = nullptr;
+  float* pk_att_part = nullptr;
+  unsigned* pk_att_tickets = nullptr;
+  unsigned long long* pk_lm_keys = nullptr;
+  unsigned* pk_ctl = nullptr;
+  size_t pk_att_tickets_bytes = 0;
   cudaStream_t cap_stream = nullptr;
   std::mutex mu;
   std::map<GraphKey, cudaGraphExec_t> graphs;
@@ -104,6 +119,21 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
       delete m;
       return set_error(W4A16_ERR_INVALID_ARG, "model_create: layer %d has a null weight", l);
     }
+    const void* ptrs[] = {L.ln1, L.ln2, L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.sq, L.sk, L.sv,
+                          L.so,  L.sg,  L.su, L.sd, L.bq, L.bk, L.bv, L.k_pool, L.v_pool};
+    for (const void* p : ptrs) {
+      if (p && !aligned(p, 128)) {
+        delete m;
+        return set_error(W4A16_ERR_ALIGNMENT, "model_create: layer %d has a weight not 128-byte aligned", l);
+      }
+    }
+  }
+  for (const void* p : {static_cast<const void*>(w->embed), static_cast<const void*>(w->final_norm),
+                        static_cast<const void*>(w->lm_head)}) {
+    if (p && !aligned(p, 128)) {
+      delete m;
+      return set_error(W4A16_ERR_ALIGNMENT, "model_create: embedding, final norm or lm_head not 128-byte aligned");
+    }
   }
   m->embed = reinterpret_cast<const __half*>(w->embed);
   m->final_norm = reinterpret_cast<const __half*>(w->final_norm);
@@ -141,6 +171,15 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   }
   const size_t o_tws = off; off += up256(m->tc_ws_bytes);
   const size_t o_err = off; off += 256;
+  // the persistent path: one sequence, the Qwen2-style 7:1 GQA shapes, contexts
+  // its attention merge covers
+  m->pk_ok = persistent_supported(c.hidden, c.n_q_heads, c.n_kv_heads, c.head_dim, c.inter, c.n_layers, max_context) &&
+             c.vocab >= 2 && c.vocab % 2 == 0;
+  size_t o_pk = off;
+  if (m->pk_ok) {
+    m->pk_P = (max_context + PK_PARTITION_TOKENS - 1) / PK_PARTITION_TOKENS;
+    off += up256(persistent_workspace_bytes(c.n_kv_heads, max_context, c.n_layers));
+  }
   m->arena_bytes = off;
   cudaError_t e = cudaMalloc(&m->arena, off);
   if (e != cudaSuccess) {
@@ -159,6 +198,33 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   m->logits32 = max_batch > GEMV_MAX_BATCH ? reinterpret_cast<float*>(m->arena + o_l32) : nullptr;
   m->tc_ws = m->arena + o_tws;
   m->err_flag = reinterpret_cast<int32_t*>(m->arena + o_err);
+  if (m->pk_ok) {
+    char* p = m->arena + o_pk;
+    m->pk_layers = reinterpret_cast<PkLayer*>(p);
+    p += up256((size_t)c.n_layers * sizeof(PkLayer));
+    m->pk_att_part = reinterpret_cast<float*>(p);
+    p += up256((size_t)c.n_kv_heads * m->pk_P * 7 * (c.head_dim + 4) * 4);  // 16-byte aligned records
+    m->pk_att_tickets = reinterpret_cast<unsigned*>(p);
+    m->pk_att_tickets_bytes = up256((size_t)c.n_kv_heads * 4);
+    p += m->pk_att_tickets_bytes;
+    m->pk_lm_keys = reinterpret_cast<unsigned long long*>(p);
+    p += up256((size_t)1024 * 8);
+    m->pk_ctl = reinterpret_cast<unsigned*>(p);
+    std::vector<PkLayer> tab(c.n_layers);
+    auto hp = [](const uint16_t* q) { return reinterpret_cast<const __half*>(q); };
+    for (int l = 0; l < c.n_layers; ++l) {
+      const w4a16_layer_weights& L = m->layers[l];
+      tab[l] = PkLayer{L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, hp(L.sq), hp(L.sk), hp(L.sv), hp(L.so), hp(L.sg),
+                       hp(L.su), hp(L.sd), hp(L.bq), hp(L.bk), hp(L.bv), hp(L.ln1), hp(L.ln2),
+                       reinterpret_cast<__half*>(L.k_pool), reinterpret_cast<__half*>(L.v_pool)};
+    }
+    e = cudaMemcpy(m->pk_layers, tab.data(), tab.size() * sizeof(PkLayer), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      cudaFree(m->arena);
+      delete m;
+      return set_error(W4A16_ERR_CUDA, "model_create: layer table: %s", cudaGetErrorString(e));
+    }
+  }
   e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -219,7 +285,19 @@ extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err_flag, 0, sizeof(int32_t), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "model_check_errors: %s", cudaGetErrorString(e));
-  if (host & 2) return set_error(W4A16_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", host);
+  if (host & 2) {
+    // a CTA that gave up left its split-K tiles unfinished: their tickets
+    // may be part-counted, so every ticket block is cleared before the next step
+    e = cudaMemsetAsync(m->tc_ws, 0, std::min(m->tc_ws_bytes, TC_TICKET_BYTES), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->attn_ws, 0, std::min(m->attn_ws_bytes, ATT_TICKET_BYTES), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->lm_ws, 0, m->lm_ws_bytes, s);
+    // the persistent kernel's barrier and step counters restart together
+    if (e == cudaSuccess && m->pk_ok) e = cudaMemsetAsync(m->pk_ctl, 0, PK_CTL_WORDS * 4, s);
+    if (e == cudaSuccess && m->pk_ok) e = cudaMemsetAsync(m->pk_att_tickets, 0, m->pk_att_tickets_bytes, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "model_check_errors: %s", cudaGetErrorString(e));
+    return set_error(W4A16_ERR_TIMEOUT, "a bounded device wait gave up (flag 0x%x)", host);
+  }
   if (host & 1) return set_error(W4A16_ERR_DEVICE_BOUNDS, "a kernel skipped an out-of-range index (flag 0x%x)", host);
   return W4A16_OK;
 }
@@ -342,6 +420,170 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   return project(m, dn, false, s, &tag);
 }
 
+// ---------------------------------------------------------------------------
+// Prefill: the T prompt tokens of one sequence in one pass (the "TTFT (512
+// tokens)" row of the aikraft.ru article's "Ключевые метрики
+// производительности").  Each projection is a tensor-core GEMM over the T
+// rows (row chunks of 32); RoPE + append write all T positions into the
+// sequence's pages; the attention runs the T tokens as T rows of lengths
+// len0 + 1 .. len0 + T over copies of the block-table row, which is causal
+// attention over the prompt (and any tokens cached before it).
+// ---------------------------------------------------------------------------
+struct PrefillWs {
+  __half *x, *xn, *qkv, *att, *h, *mlp;
+  int32_t *bt_rep, *lens;
+};
+
+static size_t prefill_layout(const w4a16_model* m, int T, int max_blocks, char* base, PrefillWs* w) {
+  const w4a16_model_config& c = m->cfg;
+  const size_t D = c.head_dim, nqkv = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * D;
+  const size_t maxK = std::max(std::max((size_t)c.hidden, (size_t)c.inter), (size_t)c.n_q_heads * D);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += up256(bytes);
+    return base ? base + o : nullptr;
+  };
+  char* px = take((size_t)T * c.hidden * 2);
+  char* pxn = take((size_t)T * maxK * 2);
+  char* pqkv = take((size_t)T * nqkv * 2);
+  char* patt = take((size_t)T * c.n_q_heads * D * 2);
+  char* ph = take((size_t)T * c.hidden * 2);
+  char* pmlp = take((size_t)T * c.inter * 2);
+  char* pbt = take((size_t)T * max_blocks * 4);
+  char* pl = take((size_t)T * 4);
+  if (w) {
+    w->x = reinterpret_cast<__half*>(px);
+    w->xn = reinterpret_cast<__half*>(pxn);
+    w->qkv = reinterpret_cast<__half*>(pqkv);
+    w->att = reinterpret_cast<__half*>(patt);
+    w->h = reinterpret_cast<__half*>(ph);
+    w->mlp = reinterpret_cast<__half*>(pmlp);
+    w->bt_rep = reinterpret_cast<int32_t*>(pbt);
+    w->lens = reinterpret_cast<int32_t*>(pl);
+  }
+  return off;
+}
+
+extern "C" size_t w4a16_prefill_workspace_size(w4a16_model* m, int T, int max_blocks) {
+  if (!m || T < 1 || max_blocks < 1) return 0;
+  return prefill_layout(m, T, max_blocks, nullptr, nullptr);
+}
+
+// y[T][N] = x[T][K] . W^T (+bias, +residual; SiLU-mul for gate|up) in row
+// chunks of at most 32 on the tensor cores
+static int gemm_rows(w4a16_model* m, const __half* x, int T, int K, const GemvSeg* segs, int nseg, int N,
+                     const __half* residual, __half* y, bool silu, cudaStream_t s) {
+  for (int r0 = 0; r0 < T; r0 += 32) {
+    TcArgs t = {};
+    t.x = x + (size_t)r0 * K;
+    t.residual = residual ? residual + (size_t)r0 * N : nullptr;
+    t.y = y + (size_t)r0 * N;
+    for (int i = 0; i < nseg; ++i) t.seg[i] = segs[i];
+    t.nseg = nseg;
+    t.err_flag = m->err_flag;
+    t.M = std::min(32, T - r0);
+    t.K = K;
+    t.N = N;
+    t.ldy = N;
+    tc_plan(N, K, true, silu, true, &t.ksplit, &t.per_split);
+    if (t.ksplit > 1 && tc_workspace_bytes(N, t.ksplit, silu) > m->tc_ws_bytes)
+      tc_plan(N, K, true, silu, false, &t.ksplit, &t.per_split);
+    if (t.ksplit > 1) tc_workspace_layout(t, m->tc_ws);
+    const int rc = launch_gemm_tc(t, true, silu, s);
+    if (rc) return rc;
+  }
+  return W4A16_OK;
+}
+
+extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const int32_t* block_table,
+                             int max_blocks, int32_t* context_lens, int32_t* token_out, uint16_t* logits,
+                             void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  W4_CHECK_ARG(m && tokens && block_table && context_lens && token_out && workspace, "prefill: null argument");
+  W4_CHECK_ARG(m->embed && m->final_norm && m->lm_head && m->cfg.vocab > 0, "prefill: model has no lm_head");
+  W4_CHECK_ARG(T >= 1 && max_blocks >= 1, "prefill: T=%d max_blocks=%d", T, max_blocks);
+  W4_CHECK_SHAPE(T <= m->max_context, "prefill: %d tokens > max_context %d", T, m->max_context);
+  W4_CHECK_ALIGN(workspace, 256, "workspace");
+  W4_CHECK_ALIGN(logits, 128, "logits");
+  const size_t need = prefill_layout(m, T, max_blocks, nullptr, nullptr);
+  W4_CHECK_ARG(workspace_bytes >= need, "prefill: workspace of %zu bytes needed", need);
+  const w4a16_model_config& c = m->cfg;
+  const int D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, H = c.hidden, I = c.inter;
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  cudaStream_t s = (cudaStream_t)stream;
+  PrefillWs w;
+  prefill_layout(m, T, max_blocks, static_cast<char*>(workspace), &w);
+  auto hp = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
+  int rc;
+  if ((rc = launch_embedding(m->embed, c.vocab, H, tokens, T, w.x, m->err_flag, nullptr, 0, s))) return rc;
+  if ((rc = launch_prefill_rows(block_table, max_blocks, context_lens, T, w.bt_rep, w.lens, s))) return rc;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const w4a16_layer_weights& L = m->layers[l];
+    if ((rc = launch_rmsnorm(w.x, hp(L.ln1), w.xn, T, H, c.eps, s))) return rc;
+    const GemvSeg qkv[3] = {{L.wq, hp(L.sq), hp(L.bq), Hq * D}, {L.wk, hp(L.sk), hp(L.bk), Hkv * D},
+                            {L.wv, hp(L.sv), hp(L.bv), Hkv * D}};
+    if ((rc = gemm_rows(m, w.xn, T, H, qkv, 3, nqkv, nullptr, w.qkv, false, s))) return rc;
+    RopeArgs ra = {};
+    ra.q = w.qkv;
+    ra.k = w.qkv + (size_t)Hq * D;
+    ra.v = w.qkv + (size_t)(Hq + Hkv) * D;
+    ra.k_pool = reinterpret_cast<__half*>(L.k_pool);
+    ra.v_pool = reinterpret_cast<__half*>(L.v_pool);
+    ra.block_table = w.bt_rep;
+    ra.context_lens = w.lens;
+    ra.err_flag = m->err_flag;
+    ra.stride_q = nqkv;
+    ra.stride_kv = nqkv;
+    ra.num_pages = c.num_pages;
+    ra.max_blocks = max_blocks;
+    ra.B = T;
+    ra.Hq = Hq;
+    ra.Hkv = Hkv;
+    std::memcpy(ra.inv_freq, m->inv_freq, sizeof(ra.inv_freq));
+    if ((rc = launch_rope_append(ra, s))) return rc;
+    AttnArgs a = {};
+    a.q = w.qkv;
+    a.q_stride = nqkv;
+    a.k_pool = ra.k_pool;
+    a.v_pool = ra.v_pool;
+    a.block_table = w.bt_rep;
+    a.context_lens = w.lens;
+    a.out = w.att;
+    a.err_flag = m->err_flag;
+    a.num_pages = c.num_pages;
+    a.max_blocks = max_blocks;
+    a.B = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.P = 1;  // one partition per row: no split-K workspace
+    a.part_tokens = (m->max_context + 15) / 16 * 16;
+    a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    if ((rc = launch_paged_attention(a, s))) return rc;
+    const GemvSeg o[1] = {{L.wo, hp(L.so), nullptr, H}};
+    if ((rc = gemm_rows(m, w.att, T, Hq * D, o, 1, H, w.x, w.h, false, s))) return rc;
+    if ((rc = launch_rmsnorm(w.h, hp(L.ln2), w.xn, T, H, c.eps, s))) return rc;
+    const GemvSeg gu[2] = {{L.wg, hp(L.sg), nullptr, I}, {L.wu, hp(L.su), nullptr, I}};
+    if ((rc = gemm_rows(m, w.xn, T, H, gu, 2, I, nullptr, w.mlp, true, s))) return rc;
+    const GemvSeg dn[1] = {{L.wd, hp(L.sd), nullptr, H}};
+    if ((rc = gemm_rows(m, w.mlp, T, I, dn, 1, H, w.h, w.x, false, s))) return rc;
+  }
+  // the last prompt token's logits and greedy next token
+  LmHeadArgs la = {};
+  la.x = w.x + (size_t)(T - 1) * H;
+  la.w = m->lm_head;
+  la.gamma = m->final_norm;
+  la.eps = c.eps;
+  la.logits = reinterpret_cast<__half*>(logits);
+  la.tokens_out = token_out;
+  la.partial = reinterpret_cast<unsigned long long*>(m->lm_ws);
+  la.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(m->lm_ws) + (size_t)4 * 4096 * 8);
+  la.B = 1;
+  la.H = H;
+  la.vocab = c.vocab;
+  if ((rc = launch_lm_head_argmax(la, s))) return rc;
+  return launch_advance_len(context_lens, T, m->max_context, m->err_flag, s);
+}
+
 // kernels one layer launches at batch B
 static int layer_kernel_count(const w4a16_model* m, int B) { return batched_path(m, B) ? 7 : 5; }
 
@@ -358,7 +600,7 @@ extern "C" int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const i
 static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const int32_t* bt, int max_blocks,
                         int32_t* lens, int B, uint16_t* logits, cudaStream_t s) {
   const w4a16_model_config& c = m->cfg;
-  int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, s, 0);
+  int rc = launch_embedding(m->embed, c.vocab, c.hidden, tin, B, m->x, m->err_flag, lens, m->max_context, s, 0);
   if (rc) return rc;
   const int per_layer = layer_kernel_count(m, B);
   for (int l = 0; l < c.n_layers; ++l)
@@ -397,9 +639,72 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
   return launch_lm_head_argmax(a, s);
 }
 
+// decode_step takes the persistent kernel for this batch size
+static bool use_persistent(const w4a16_model* m, int B) {
+  return m->pk_ok && B == 1 && m->decode_path != W4A16_PATH_KERNELS;
+}
+
+static int enqueue_persistent(w4a16_model* m, const int32_t* tin, int32_t* tout, const int32_t* bt, int max_blocks,
+                              int32_t* lens, uint16_t* logits, cudaStream_t s) {
+  const w4a16_model_config& c = m->cfg;
+  PkArgs a = {};
+  a.layers = m->pk_layers;
+  a.n_layers = c.n_layers;
+  a.embed = m->embed;
+  a.final_norm = m->final_norm;
+  a.lm_head = m->lm_head;
+  a.tokens_in = tin;
+  a.tokens_out = tout;
+  a.block_table = bt;
+  a.max_blocks = max_blocks;
+  a.context_lens = lens;
+  a.logits = reinterpret_cast<__half*>(logits);
+  a.x = m->x;
+  a.qkv = m->qkv;
+  a.att = m->att;
+  a.h = m->h;
+  a.mlp = m->mlp;
+  a.att_part = m->pk_att_part;
+  a.att_tickets = m->pk_att_tickets;
+  a.lm_keys = m->pk_lm_keys;
+  a.ctl = m->pk_ctl;
+  a.err_flag = m->err_flag;
+  a.H = c.hidden;
+  a.Hq = c.n_q_heads;
+  a.Hkv = c.n_kv_heads;
+  a.I = c.inter;
+  a.vocab = c.vocab;
+  a.num_pages = c.num_pages;
+  a.max_context = m->max_context;
+  a.P = m->pk_P;
+  a.eps = c.eps;
+  a.scale_log2 = (1.0f / sqrtf((float)c.head_dim)) * 1.4426950408889634f;
+  a.wait_limit_ns = tc_wait_limit_ns();
+  std::memcpy(a.inv_freq, m->inv_freq, sizeof(a.inv_freq));
+  return launch_persistent(a, s);
+}
+
 extern "C" int decode_step_kernel_count(w4a16_model* m, int B) {
   if (!m) return 0;
+  if (use_persistent(m, B)) return 1;
   return 1 + layer_kernel_count(m, B) * m->cfg.n_layers + (batched_path(m, B) ? 3 : 1);
+}
+
+extern "C" int w4a16_model_set_decode_path(w4a16_model* m, int path) {
+  W4_CHECK_ARG(m, "model_set_decode_path: null model");
+  W4_CHECK_ARG(path == W4A16_PATH_AUTO || path == W4A16_PATH_KERNELS || path == W4A16_PATH_PERSISTENT,
+               "model_set_decode_path: unknown path %d", path);
+  if (path == W4A16_PATH_PERSISTENT && !m->pk_ok)
+    return set_error(W4A16_ERR_SHAPE, "model_set_decode_path: the persistent kernel does not cover this model "
+                                      "(one sequence, head_dim 128, Hq = 7 Hkv, max_context <= %d)", PK_MAX_CONTEXT);
+  std::lock_guard<std::mutex> lk(m->mu);
+  m->decode_path = path;
+  return W4A16_OK;
+}
+
+extern "C" int w4a16_model_decode_path(w4a16_model* m, int B) {
+  if (!m) return -1;
+  return use_persistent(m, B) ? W4A16_PATH_PERSISTENT : W4A16_PATH_KERNELS;
 }
 
 extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* tokens_out, const int32_t* block_table,
@@ -410,14 +715,19 @@ extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* to
   W4_CHECK_ARG(B >= 1 && B <= m->max_batch && max_blocks >= 1, "decode_step: B=%d (max %d)", B, m->max_batch);
   W4_CHECK_ALIGN(logits, 128, "logits");
   cudaStream_t s = (cudaStream_t)stream;
-  if (!use_graph) return enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, s);
+  const bool pk = use_persistent(m, B);
+  auto enqueue = [&](cudaStream_t st) {
+    return pk ? enqueue_persistent(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, logits, st)
+              : enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, st);
+  };
+  if (!use_graph) return enqueue(s);
 
   cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
   if (s != nullptr && cudaStreamIsCapturing(s, &cst) == cudaSuccess && cst == cudaStreamCaptureStatusActive) {
     // The caller is capturing already: record the kernels into their graph.
-    return enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, s);
+    return enqueue(s);
   }
-  GraphKey key{B, max_blocks, tokens_in, tokens_out, block_table, context_lens, logits};
+  GraphKey key{B, max_blocks, pk ? 1 : 0, tokens_in, tokens_out, block_table, context_lens, logits};
   cudaGraphExec_t exec = nullptr;
   {
     std::lock_guard<std::mutex> lk(m->mu);
@@ -429,7 +739,7 @@ extern "C" int decode_step(w4a16_model* m, const int32_t* tokens_in, int32_t* to
     // capture); nothing but kernel launches is recorded.
     cudaError_t e = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed);
     if (e != cudaSuccess) return set_error(W4A16_ERR_CAPTURE, "decode_step: begin capture: %s", cudaGetErrorString(e));
-    int rc = enqueue_step(m, tokens_in, tokens_out, block_table, max_blocks, context_lens, B, logits, m->cap_stream);
+    int rc = enqueue(m->cap_stream);
     cudaGraph_t graph = nullptr;
     e = cudaStreamEndCapture(m->cap_stream, &graph);
     if (rc != W4A16_OK) {
