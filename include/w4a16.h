@@ -495,8 +495,9 @@ W4A16_API int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const 
  *                          launch), and its barrier waits are bounded (a wait
  *                          that runs out reports W4A16_ERR_TIMEOUT through
  *                          w4a16_model_check_errors, which also resets it);
- *   W4A16_PATH_AUTO        (default) the persistent kernel where it applies,
- *                          else the kernels.
+ *   W4A16_PATH_AUTO        (default) the path measured faster on GB300 for
+ *                          the shapes the persistent kernel covers (see
+ *                          w4a16_model_decode_path); else the kernels.
  * Both paths compute the same step; sums are ordered differently, so
  * outputs agree to fp16 rounding, not bit for bit.  Graphs captured by
  * decode_step are keyed on the path.  set returns W4A16_ERR_SHAPE when the

@@ -4,8 +4,7 @@ CPU oracle's own greedy decode of each sequence.  GPU only (marked gpu).
 The pool is deliberately too small for every admitted sequence to reach its
 full length, so pages are reclaimed from finished sequences and handed to
 new ones, and sequences get preempted and restarted; batch sizes change from
-step to step (each size its own captured graph, size 1 the persistent
-kernel)."""
+step to step (each size its own captured graph)."""
 import numpy as np
 import pytest
 
@@ -82,7 +81,7 @@ def test_continuous_batching_matches_oracle_with_page_reuse_and_preemption(api):
     assert st["active"] == 0 and st["waiting"] == 0
     assert st["free_pages"] == num_pages                # every page came back
     assert st["preemptions"] > 0                        # the pool was too small for all at once
-    assert 1 in sizes and len(sizes) >= 2               # several graph buckets, incl. the persistent kernel
+    assert 1 in sizes and len(sizes) >= 2               # several graph buckets
     assert model.check_errors() == 0
     for sid, p, n in zip(ids, prompts, news):
         got, done = bat.poll(sid)

@@ -228,8 +228,11 @@ def test_decode_path_selection(api):
     case = _tiny(1, 7800, vocab=500)
     m, _ = _model(api, case, 128, path="kernels")
     assert m.decode_path(1) == "kernels" and m.kernel_count(1) == 1 + 5 + 1
-    m.set_decode_path("auto")
+    m.set_decode_path("persistent")
     assert m.decode_path(1) == "persistent" and m.kernel_count(1) == 1
+    m.set_decode_path("auto")
+    assert m.decode_path(1) in ("kernels", "persistent")
+    assert m.decode_path(2) == "kernels"
     m.close()
     # a model the persistent kernel does not cover (context beyond its merge)
     m, _ = _model(api, case, 8192, path="auto")

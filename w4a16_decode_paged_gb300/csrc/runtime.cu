@@ -639,9 +639,12 @@ static int enqueue_step(w4a16_model* m, const int32_t* tin, int32_t* tout, const
   return launch_lm_head_argmax(a, s);
 }
 
-// decode_step takes the persistent kernel for this batch size
+// decode_step takes the persistent kernel for this batch size: when asked
+// for, or by default where it is the faster path (see PK_IS_DEFAULT)
+static constexpr bool PK_IS_DEFAULT = false;
 static bool use_persistent(const w4a16_model* m, int B) {
-  return m->pk_ok && B == 1 && m->decode_path != W4A16_PATH_KERNELS;
+  if (!m->pk_ok || B != 1) return false;
+  return m->decode_path == W4A16_PATH_PERSISTENT || (m->decode_path == W4A16_PATH_AUTO && PK_IS_DEFAULT);
 }
 
 static int enqueue_persistent(w4a16_model* m, const int32_t* tin, int32_t* tout, const int32_t* bt, int max_blocks,
