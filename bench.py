@@ -44,11 +44,14 @@ def parse():
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--kernel", default=None,
-                    choices=["gateup", "down", "qkv", "o", "attention", "lm_head"],
+                    choices=["gateup", "down", "qkv", "o", "attention", "lm_head", "attention_long",
+                             "attention_fp8"],
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
     ap.add_argument("--clock-log", default=None,
                     help="write the raw nvidia-smi clock samples of the timed region to this CSV file")
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "kernels", "persistent"],
+                    help="how decode_step runs a b=1 step (auto: the library's default)")
     ap.add_argument("--workload", default="b1", choices=["b1", "b32"],
                     help="b1: 28-layer b=1 ctx-512 decode; b32: 28-layer batched decode, 32 sequences of "
                          "U[1,4096] tokens in a 16384-page pool")
@@ -78,7 +81,7 @@ def workload(args):
                  f"(CUDA graph, tcgen05 projections)")
         return cfg, post - 1, cfg["pool_pages"], label
     cfg = model_cfg(args.layers)
-    label = f"qwen2.5-7b-{cfg['n_layers']}L-b1-ctx{args.context} greedy decode (CUDA graph)"
+    label = f"qwen2.5-7b-{cfg['n_layers']}L-b1-ctx{args.context} greedy decode (CUDA graph of decode_step)"
     return cfg, np.array([args.context], np.int32), 256, label
 
 
@@ -320,6 +323,14 @@ def run_kernel(args):
     r = synth.rng(args.seed)
     tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int32) if a.dtype == np.uint32 else a)).to(dev)
     name = args.kernel
+    if name in ("attention_long", "attention_fp8"):
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            res = time_attention_long(torch, api, dev, stream, reps=max(1, args.steps), fp8=name == "attention_fp8")
+        peak, src = measured_peak()
+        res.update({"kernel": name, "frac_of_peak": res["gbs"] / peak, "peak_gbs": peak, "peak_source": src})
+        print(json.dumps(res))
+        return 0
     if name == "attention":
         lens = np.full(B, L, np.int32)
         pages = B * ((L + 15) // 16) + 8
@@ -408,12 +419,14 @@ def run_kernel(args):
     return 0
 
 
-def time_attention_long(torch, api, dev, stream, reps=6):
+def time_attention_long(torch, api, dev, stream, reps=6, fp8=False):
     """paged_gqa_decode on the long-context workload: 4 sequences of 32768
     tokens (2048 pages each, scattered over a 16384-page pool), 28 query /
     4 kv heads, 512-token partitions merged by the last partition.  Two pool
     copies alternate so the 268 MB a launch reads does not stay in L2; a
-    CUDA graph of 8 launches, CUDA events on the launching stream."""
+    CUDA graph of 8 launches, CUDA events on the launching stream.  fp8:
+    the same over FP8 (E4M3) pools with fp32 row scales (134 MB of codes +
+    4 MB of scales per launch)."""
     from w4a16_decode_paged_gb300 import synth
     c = synth.QWEN_LONG
     B, Hq, Hkv, D, L, pool, part = (c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["context"],
@@ -422,18 +435,27 @@ def time_attention_long(torch, api, dev, stream, reps=6):
     lens = np.full(B, L, np.int32)
     bt = torch.from_numpy(synth.block_table(r, lens, pool)).to(dev)
     ld = torch.from_numpy(lens).to(dev)
-    pools = [(torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16),
-              torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16)) for _ in range(2)]
     q = torch.randn((B, Hq, D), device=dev, dtype=torch.float16)
     out = torch.empty_like(q)
     ws = torch.zeros(api.paged_gqa_decode_workspace_size(B, Hq, Hkv, L, part), dtype=torch.uint8, device=dev)
-    fn = lambda i: api.paged_gqa_decode(q, pools[i % 2][0], pools[i % 2][1], bt, ld, max_context=L,
-                                        partition_tokens=part, workspace=ws, out=out)
-    nbytes = B * (2 * Hkv * L * D * 2 + 4 * ((L + 15) // 16) + 2 * Hq * D * 2)
+    if fp8:
+        codes = lambda: torch.randint(0, 0x7E, (pool, Hkv, 16, D), device=dev, dtype=torch.uint8)
+        scales = lambda: torch.rand((pool, Hkv, 16), device=dev, dtype=torch.float32) * 0.01 + 0.001
+        pools = [(codes(), codes(), scales(), scales()) for _ in range(2)]
+        fn = lambda i: api.paged_gqa_decode_fp8(q, *pools[i % 2], bt, ld, max_context=L, partition_tokens=part,
+                                                workspace=ws, out=out)
+        nbytes = B * (2 * Hkv * L * (D + 4) + 4 * ((L + 15) // 16) + 2 * Hq * D * 2)
+    else:
+        pools = [(torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16),
+                  torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16)) for _ in range(2)]
+        fn = lambda i: api.paged_gqa_decode(q, pools[i % 2][0], pools[i % 2][1], bt, ld, max_context=L,
+                                            partition_tokens=part, workspace=ws, out=out)
+        nbytes = B * (2 * Hkv * L * D * 2 + 4 * ((L + 15) // 16) + 2 * Hq * D * 2)
     per = _graph_time(torch, stream, fn, 8, reps)
     del pools
     return {"us_per_launch": per * 1e6, "bytes_per_launch": nbytes, "gbs": nbytes / per / 1e9,
-            "launches_timed": 8 * reps, "workload": f"b={B} x ctx {L}, {Hq}/{Hkv} heads, partitions of {part}"}
+            "launches_timed": 8 * reps, "workload": f"b={B} x ctx {L}, {Hq}/{Hkv} heads, partitions of {part}"
+                                                    + (", FP8 E4M3 pages" if fp8 else "")}
 
 
 def _graph_time(torch, stream, fn, per_graph, reps):
@@ -592,6 +614,7 @@ def main():
     lens_init = tdev(inp["lens"])
     lens = lens_init.clone()
     stream = torch.cuda.Stream(device=dev)
+    model.set_decode_path(args.decode_path)
     kernels_per_step = model.kernel_count(B)
     path = model.decode_path(B)
 
@@ -646,6 +669,30 @@ def main():
         e2e_s = time.perf_counter() - t0
         barrier()
 
+        # ---- the other decode path on the same model (b=1): its step time --
+        other = None
+        if args.workload == "b1" and not args.no_kernel_timing:
+            alt = "persistent" if path == "kernels" else "kernels"
+            model.set_decode_path(alt)
+            if model.decode_path(B) == alt:
+                lens.copy_(lens_init)
+                for _ in range(3):
+                    model.decode_step(tok, tok, bt, lens, use_graph=True)
+                stream.synchronize()
+                assert model.check_errors(stream) == 0
+                lens.copy_(lens_init)
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(K):
+                    model.decode_step(tok, tok, bt, lens, use_graph=True)
+                a1.record(stream)
+                stream.synchronize()
+                assert model.check_errors(stream) == 0
+                other = {"decode_path": alt, "ms_per_step": a0.elapsed_time(a1) / K,
+                         "tok_per_s": B * K / (a0.elapsed_time(a1) / 1e3), "kernels_per_step": model.kernel_count(B)}
+            model.set_decode_path(args.decode_path)
+            lens.copy_(lens_init)
+
         # ---- time to first token: a 512-token prompt in one prefill -------
         ttft = None
         if args.workload == "b1" and not args.no_kernel_timing:
@@ -658,6 +705,7 @@ def main():
             kern = time_gemv_kernels(torch, api, cfg, dls, dev, stream, B)
             if args.workload == "b1":
                 kern["attention_b4_ctx32768"] = time_attention_long(torch, api, dev, stream)
+                kern["attention_fp8_b4_ctx32768"] = time_attention_long(torch, api, dev, stream, fp8=True)
                 kern["gateup_tc_m32"] = time_gemv_kernels(torch, api, cfg, dls, dev, stream, 32,
                                                           only=("gateup",))["gateup"]
                 kern["b32_step"] = time_b32_step(torch, api, cfg, dls, embed, fnorm, lm, dev, stream)
@@ -705,6 +753,9 @@ def main():
                            "traffic": traffic_record("gemv_gateup" if B <= 4 else "gemm_tc_gateup_b32")}
     if ttft is not None:
         out["ttft"] = ttft
+    if other is not None:
+        other["bytes_roofline_frac"] = sb / (other["ms_per_step"] / 1e3) / 1e9 / peak
+        out["other_decode_path"] = other
     if kern is not None:
         for k, v in kern.items():
             if isinstance(v, dict) and "gbs" in v:

@@ -443,26 +443,30 @@ struct PkShared {
 };
 
 // ---------------------------------------------------------------------------
-// Epilogue of one finished pair (v: the sums of its weight rows).
+// Epilogue of one finished pair (v: the sums of its weight rows; add: the
+// bias (q|k|v) or residual (o, down) of its two output rows, loaded when the
+// pair was started so the load's latency is hidden by the pair's work).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void pk_epilogue(const PkArgs& a, const PkLayer* L, int ph, int pair, const float (&v)[4],
-                                            unsigned long long& key) {
+__device__ __forceinline__ float pk_epi_operand(const PkArgs& a, const PkLayer* L, int ph, int row) {
   if (ph == PH_QKV) {
     const int nq = a.Hq * ATT_D, nk = a.Hkv * ATT_D;
+    const __half* b = row < nq ? L->bq : (row < nq + nk ? L->bk : L->bv);
+    const int br = row < nq ? row : (row < nq + nk ? row - nq : row - nq - nk);
+    return b ? __half2float(__ldg(b + br)) : 0.f;
+  }
+  if (ph == PH_O) return __half2float(__ldcg(a.x + row));
+  if (ph == PH_D) return __half2float(__ldcg(a.h + row));
+  return 0.f;
+}
+
+__device__ __forceinline__ void pk_epilogue(const PkArgs& a, int ph, int pair, const float (&v)[4],
+                                            const float (&add)[2], unsigned long long& key) {
+  if (ph == PH_QKV) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = 2 * pair + r;
-      const __half* b = row < nq ? L->bq : (row < nq + nk ? L->bk : L->bv);
-      const int br = row < nq ? row : (row < nq + nk ? row - nq : row - nq - nk);
-      const float bv = b ? __half2float(b[br]) : 0.f;
-      a.qkv[row] = __float2half_rn(v[r] + bv);
-    }
+    for (int r = 0; r < 2; ++r) a.qkv[2 * pair + r] = __float2half_rn(v[r] + add[r]);
   } else if (ph == PH_O) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = 2 * pair + r;
-      a.h[row] = __float2half_rn(v[r] + __half2float(__ldcg(a.x + row)));
-    }
+    for (int r = 0; r < 2; ++r) a.h[2 * pair + r] = __float2half_rn(v[r] + add[r]);
   } else if (ph == PH_GU) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -472,10 +476,7 @@ __device__ __forceinline__ void pk_epilogue(const PkArgs& a, const PkLayer* L, i
     }
   } else if (ph == PH_D) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = 2 * pair + r;
-      a.x[row] = __float2half_rn(v[r] + __half2float(__ldcg(a.h + row)));
-    }
+    for (int r = 0; r < 2; ++r) a.x[2 * pair + r] = __float2half_rn(v[r] + add[r]);
   } else {  // lm_head: logits and the running argmax (lowest index on ties)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -505,6 +506,12 @@ __device__ __forceinline__ void pk_gemv_phase(const PkArgs& a, int ph, int layer
   int pair = g.p0 + (g.it1 > g.it0 ? g.it0 / g.ipp : 0);
   int cb = g.it1 > g.it0 ? g.it0 % g.ipp : 0;
   bool whole = cb == 0;  // this half-warp holds the pair's first item
+  const bool has_add = ph == PH_QKV || ph == PH_O || ph == PH_D;
+  float add[2] = {0.f, 0.f};
+  if (has_add && lr == 0 && g.it1 > g.it0) {
+    add[0] = pk_epi_operand(a, L, ph, 2 * pair);
+    add[1] = pk_epi_operand(a, L, ph, 2 * pair + 1);
+  }
   for (int it = g.it0; it < g.it1; ++it) {
     for (int r = 0; r < nr; ++r) is.issue_one(a, ring, sfifo, tid, hw_id, lr);
     cp_async_wait<PK_AHEAD>();
@@ -557,7 +564,7 @@ __device__ __forceinline__ void pk_gemv_phase(const PkArgs& a, int ph, int layer
       }
       if (lr == 0) {
         if (pair_done && whole) {
-          pk_epilogue(a, L, ph, pair, acc, key);
+          pk_epilogue(a, ph, pair, acc, add, key);
         } else {
           // cut pair: the first pair of this range if it ends here (we hold
           // its last item), else the last pair of this range
@@ -572,6 +579,10 @@ __device__ __forceinline__ void pk_gemv_phase(const PkArgs& a, int ph, int layer
         cb = 0;
         ++pair;
         whole = true;
+        if (has_add && lr == 0 && it + 1 < g.it1) {
+          add[0] = pk_epi_operand(a, L, ph, 2 * pair);
+          add[1] = pk_epi_operand(a, L, ph, 2 * pair + 1);
+        }
       }
     }
   }
@@ -596,7 +607,10 @@ __device__ __forceinline__ void pk_gemv_phase(const PkArgs& a, int ph, int layer
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) v[r] += sh.rec[h][0][r];
-        pk_epilogue(a, L, ph, gh.p0 + lp, v, key);
+        const int pr = gh.p0 + lp;
+        const float ad[2] = {has_add ? pk_epi_operand(a, L, ph, 2 * pr) : 0.f,
+                             has_add ? pk_epi_operand(a, L, ph, 2 * pr + 1) : 0.f};
+        pk_epilogue(a, ph, pr, v, ad, key);
       }
     }
   }
@@ -814,20 +828,30 @@ __device__ __noinline__ bool pk_attention_unit(const PkArgs& a, const PkLayer& L
   if (!*s_last) return ok;
   __threadfence();
   const int Pv = min(a.P, (L + PK_PART - 1) / PK_PART);  // partitions with tokens
-  float* cw = mo;                  // [G][Pv] weights
+  float* cw = mo;                  // [G][Pv] maxima, then weights
+  float* cl = cw + G * Pv;         // [G][Pv] sums
   const float* base = a.att_part + (size_t)kvh * a.P * G * PK_PREC;
+  // every (max, sum) pair in flight at once, then one thread per head
+  for (int idx = tid; idx < G * Pv; idx += PK_THREADS) {
+    const int h = idx / Pv, j = idx - h * Pv;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + ((size_t)j * G + h) * PK_PREC + ATT_D));
+    cw[idx] = ml.x;
+    cl[idx] = ml.y;
+  }
+  __syncthreads();
   if (tid < G) {
+    float* mw = cw + tid * Pv;
+    const float* lw = cl + tid * Pv;
     float M = -INFINITY;
-    for (int j = 0; j < Pv; ++j) M = fmaxf(M, __ldcg(base + ((size_t)j * G + tid) * PK_PREC + ATT_D));
+    for (int j = 0; j < Pv; ++j) M = fmaxf(M, mw[j]);
     float den = 0.f;
     for (int j = 0; j < Pv; ++j) {
-      const float mj = __ldcg(base + ((size_t)j * G + tid) * PK_PREC + ATT_D);
-      const float f = (M == -INFINITY || mj == -INFINITY) ? 0.f : exp2f(mj - M);
-      cw[tid * Pv + j] = f;
-      den += __ldcg(base + ((size_t)j * G + tid) * PK_PREC + ATT_D + 1) * f;
+      const float f = (M == -INFINITY || mw[j] == -INFINITY) ? 0.f : exp2f(mw[j] - M);
+      mw[j] = f;
+      den += lw[j] * f;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int j = 0; j < Pv; ++j) cw[tid * Pv + j] *= inv;
+    for (int j = 0; j < Pv; ++j) mw[j] *= inv;
   }
   __syncthreads();
   for (int idx = tid; idx < G * (ATT_D / 4); idx += PK_THREADS) {
