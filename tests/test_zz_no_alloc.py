@@ -11,6 +11,7 @@ import math
 import numpy as np
 import pytest
 
+import oracle as orc
 from gpu_util import assert_close, to_dev, to_host
 from w4a16_decode_paged_gb300 import synth
 
@@ -22,17 +23,22 @@ pytestmark = pytest.mark.gpu
 def lib():
     from w4a16_decode_paged_gb300 import _lib, build
     build.build()
+    orc.build()
     return _lib.load()
 
 
-def _case(seed, lens, Hq=28, Hkv=4, D=128):
+def _host_case(seed, lens, Hq=28, Hkv=4, D=128):
     r = np.random.default_rng(seed)
     pages = int(sum((L + 15) // 16 for L in lens)) + 9
     kp = synth.kv_pool(r, pages, Hkv, D)
     vp = synth.kv_pool(r, pages, Hkv, D)
     bt = synth.block_table(r, lens, pages)
     q = synth.normal_fp16(r, (len(lens), Hq, D), std=2.0)
-    return [to_dev(a, torch) for a in (q, kp, vp, bt, np.asarray(lens, np.int32))]
+    return q, kp, vp, bt, np.asarray(lens, np.int32)
+
+
+def _case(seed, lens, Hq=28, Hkv=4, D=128):
+    return [to_dev(a, torch) for a in _host_case(seed, lens, Hq, Hkv, D)]
 
 
 def _run(lib, fn, q, kp, vp, bt, ln, max_context, part, ws=None):
@@ -63,6 +69,20 @@ def test_noalloc_matches_workspace_version_two_calls_in_a_row(lib):
         got = _run(lib, "paged_gqa_decode_noalloc", q, kp, vp, bt, ln, max_context, part)
         torch.cuda.synchronize()
         assert_close(to_host(got), to_host(ref), what=f"noalloc call {seed}")
+
+
+def test_noalloc_matches_oracle_across_partitions(lib):
+    """The static-scratch path against the CPU oracle directly: lengths on
+    both sides of a page and of a 64-token partition, so the partials of
+    several partitions meet in the static array's merge."""
+    lens = [1, 15, 16, 17, 63, 64, 65, 700]
+    part, max_context = 64, 700
+    hq, hkp, hvp, hbt, hln = _host_case(11, lens)
+    q, kp, vp, bt, ln = (to_dev(a, torch) for a in (hq, hkp, hvp, hbt, hln))
+    got = _run(lib, "paged_gqa_decode_noalloc", q, kp, vp, bt, ln, max_context, part)
+    torch.cuda.synchronize()
+    ref = orc.paged_attention(hq, hkp, hvp, hbt, hln, 1.0 / math.sqrt(hq.shape[2]))
+    assert_close(to_host(got), ref, what="noalloc vs oracle")
 
 
 def test_noalloc_rejects_sizes_beyond_the_static_scratch(lib):
