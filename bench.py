@@ -550,7 +550,8 @@ def time_prefill(torch, api, model, cfg, bt, dev, stream, T=512, reps=3):
         assert model.check_errors(stream) == 0
     ms = statistics.median(times)
     return {"ms": ms, "prompt_tokens": T, "tok_per_s": T / (ms / 1e3), "reps": reps,
-            "how": "w4a16_prefill: tensor-core GEMMs over row chunks of 32, causal paged attention, lm_head"}
+            "how": "w4a16_prefill: tensor-core GEMMs over row blocks of 128 (gate|up 64), causal paged attention, "
+                   "lm_head"}
 
 
 def max_over_ranks(values, dev, world):

@@ -103,8 +103,11 @@ W4A16_API int w4a16_gemv(const uint16_t* x, int M, int K, const uint32_t* qweigh
                w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * w4a16_gemm -- the same product for a decode batch (1 <= M <= 32) on the
- * tensor cores (tcgen05 MMAs, fp32 accumulation in tensor memory).  The
+ * w4a16_gemm -- the same product for a batch of rows on the tensor cores
+ * (tcgen05 MMAs, fp32 accumulation in tensor memory): a decode batch
+ * (1 <= M <= 32), or the wider row block of a prompt (M <= 128;
+ * w4a16_gemm_silu_mul M <= 64), where every 128-row weight tile is read
+ * once for all M rows.  The
  * MMAs take the exact integer codes q; each 128-wide scale group is summed
  * in tensor memory and multiplied by its fp32 scale on the way out, so the
  * only roundings are fp32 accumulation and the final fp16 store.

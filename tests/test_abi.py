@@ -121,17 +121,18 @@ def test_model_create_rejects_bad_config(lib):
 def test_tensor_core_calls_reject(lib):
     # w4a16_gemm(x, M, K, qweight, scales, N, bias, residual, y, workspace, bytes, stream)
     good = [ALIGNED, 8, 256, ALIGNED, ALIGNED, 128, None, None, ALIGNED, None, 0, None]
-    for i, v, rc in ((1, 33, 3), (2, 200, 3), (0, None, 1), (3, None, 1), (0, MISALIGNED, 2),
+    for i, v, rc in ((1, 129, 3), (2, 200, 3), (0, None, 1), (3, None, 1), (0, MISALIGNED, 2),
                      (8, MISALIGNED, 2), (9, MISALIGNED, 2), (7, MISALIGNED, 2), (1, 0, 1)):
         a = list(good); a[i] = v
         assert lib.w4a16_gemm(*a) == rc, (i, v)
     # w4a16_gemm_silu_mul(x, M, K, qg, sg, qu, su, N, y, workspace, bytes, stream)
     good = [ALIGNED, 8, 256, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 128, ALIGNED, None, 0, None]
-    for i, v, rc in ((5, None, 1), (6, MISALIGNED, 2), (1, 40, 3), (2, 130, 3)):
+    for i, v, rc in ((5, None, 1), (6, MISALIGNED, 2), (1, 65, 3), (2, 130, 3)):
         a = list(good); a[i] = v
         assert lib.w4a16_gemm_silu_mul(*a) == rc, (i, v)
     assert lib.w4a16_gemm_workspace_size(8, 64, 128, 0) == 0      # K below one scale group
     assert lib.w4a16_gemm_workspace_size(32, 18944, 3584, 0) > 8192  # split K: tickets + partial tiles
+    assert lib.w4a16_gemm_workspace_size(128, 18944, 3584, 0) > 8192  # a prompt's row block: wider tiles
     # lm_head_logits_batched(x, B, H, lm_head, vocab, logits, stream)
     assert lib.lm_head_logits_batched(ALIGNED, 33, 896, ALIGNED, 1000, ALIGNED, None) == 3
     assert lib.lm_head_logits_batched(ALIGNED, 8, 900, ALIGNED, 1000, ALIGNED, None) == 3

@@ -36,6 +36,47 @@ def test_w4a16_gemm_matches_oracle(api, K, N, M, split):
     assert_close(to_host(y), ref, what=f"gemm K={K} N={N} M={M} split={split}")
 
 
+@pytest.mark.parametrize("K,N,M", [(256, 200, 33), (3584, 512, 64), (3584, 512, 128), (896, 130, 100),
+                                   (18944, 384, 97)])
+@pytest.mark.parametrize("split", [False, True])
+def test_w4a16_gemm_wide_row_blocks_match_oracle(api, K, N, M, split):
+    """Row blocks wider than a decode batch (a prompt's rows): 64 and 128
+    batch columns per weight tile, ragged M and N, K split or not."""
+    r = np.random.default_rng(K + 7 * N + 31 * M + split)
+    qw, s = synth.int4_weight(r, N, K)
+    x = synth.normal_fp16(r, (M, K))
+    bias = synth.normal_fp16(r, (N,), 0.1)
+    res = synth.normal_fp16(r, (M, N)) if split else None
+    ref = orc.w4a16_gemv(x, qw, s, bias=bias, residual=res)
+    y = api.w4a16_gemm(to_dev(x, torch), to_dev(qw, torch), to_dev(s, torch), bias=to_dev(bias, torch),
+                       residual=None if res is None else to_dev(res, torch), split=split)
+    torch.cuda.synchronize()
+    assert_close(to_host(y), ref, what=f"wide gemm K={K} N={N} M={M} split={split}")
+
+
+@pytest.mark.parametrize("K,N,M", [(896, 2432, 64), (3584, 1024, 45)])
+def test_w4a16_gemm_silu_mul_wide_row_blocks(api, K, N, M):
+    r = np.random.default_rng(K + N + 3 * M)
+    qg, sg = synth.int4_weight(r, N, K)
+    qu, su = synth.int4_weight(r, N, K)
+    x = synth.normal_fp16(r, (M, K))
+    ref = orc.silu_mul(orc.w4a16_gemv(x, qg, sg), orc.w4a16_gemv(x, qu, su))
+    y = api.w4a16_gemm_silu_mul(to_dev(x, torch), to_dev(qg, torch), to_dev(sg, torch), to_dev(qu, torch),
+                                to_dev(su, torch))
+    torch.cuda.synchronize()
+    assert_close(to_host(y), ref, what=f"wide gemm silu K={K} N={N} M={M}")
+
+
+def test_w4a16_gemm_rejects_rows_beyond_the_widest_block(api):
+    r = np.random.default_rng(4)
+    qw, s = synth.int4_weight(r, 128, 256)
+    with pytest.raises(Exception):
+        api.w4a16_gemm(to_dev(synth.normal_fp16(r, (129, 256)), torch), to_dev(qw, torch), to_dev(s, torch))
+    with pytest.raises(Exception):
+        api.w4a16_gemm_silu_mul(to_dev(synth.normal_fp16(r, (65, 256)), torch), to_dev(qw, torch), to_dev(s, torch),
+                                to_dev(qw, torch), to_dev(s, torch))
+
+
 def test_w4a16_gemm_repeat_calls_leave_counters_zero(api):
     r = np.random.default_rng(3)
     qw, s = synth.int4_weight(r, 3584, 18944)

@@ -104,7 +104,8 @@ def w4a16_gemv(x, qweight, scales, bias=None, residual=None, out=None, stream=No
 
 
 def w4a16_gemm(x, qweight, scales, bias=None, residual=None, out=None, workspace=None, split=True, stream=None):
-    """Tensor-core path for a decode batch (M <= 32)."""
+    """Tensor-core path for a batch of rows: decode batches (M <= 32) and the
+    wider row blocks of a prompt (M <= 128)."""
     M, K = _xk(x)
     N = _int4(qweight, scales, K)
     _arg(bias, _H, "bias", (N,), optional=True)

@@ -273,10 +273,11 @@ __global__ void __launch_bounds__(NW * 32) w4pg_paged_attn(const __grid_constant
   // every accumulator, columns 2t, 2t+1.
   const int g = lane >> 2, t4 = lane & 3;
   const bool head_ok = g < G;
-  uint32_t qa[8][2];  // q of head g, dims 16s + 2t4 + {0,1} and 16s + 8 + 2t4 + {0,1}, fp16
-  attn_q_frags(s_q, G, g, t4, qa);
+  uint32_t qa[8][2];  // q of head g, dims 16s + 2t4 + {0,1} and 16s + 8 + 2t4 + {0,1}, fp16 (FP8: attn8_qdim)
+  if (KV8) attn_q_frags_fp8(s_q, G, g, t4, qa);
+  else attn_q_frags(s_q, G, g, t4, qa);
   float m_run = -INFINITY, l_run = 0.f;  // head g's running max (log2 domain) and sum
-  float o[16][4];                        // P.V accumulators, n-block nb = dims 8nb..8nb+7
+  float o[16][4];                        // P.V accumulators, n-block nb = dims 8nb..8nb+7 (FP8: attn8_odim)
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
   const uint32_t k_off = attn_k_off(lane), v_off = attn_v_off(lane);
@@ -332,9 +333,17 @@ __global__ void __launch_bounds__(NW * 32) w4pg_paged_attn(const __grid_constant
   float* mo = reinterpret_cast<float*>(smraw);          // [NW][8][128]
   float* mml = mo + NW * 8 * ATT_D;                     // [NW][8][2]
   if (head_ok) {
+    if (KV8) {
 #pragma unroll
-    for (int nb = 0; nb < 16; ++nb)
-      *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
+      for (int nb = 0; nb < 16; ++nb) {
+        mo[(warp * 8 + g) * ATT_D + attn8_odim(nb, t4, 0)] = o[nb][0];
+        mo[(warp * 8 + g) * ATT_D + attn8_odim(nb, t4, 1)] = o[nb][1];
+      }
+    } else {
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb)
+        *reinterpret_cast<float2*>(mo + (warp * 8 + g) * ATT_D + 8 * nb + 2 * t4) = make_float2(o[nb][0], o[nb][1]);
+    }
     if (t4 == 0) {
       mml[(warp * 8 + g) * 2 + 0] = m_run;
       mml[(warp * 8 + g) * 2 + 1] = l_run;

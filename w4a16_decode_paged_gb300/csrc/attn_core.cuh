@@ -213,10 +213,47 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return d;
 }
 
-// One FP8 page against the warp's query fragments (the fp16 step above with
-// the codes converted while the fragments are built): scores scaled by the
-// K row scales, probabilities by the V row scales before P V (the softmax
-// sum keeps the unscaled probabilities).
+// Four E4M3 codes (bytes 0..3 of w) -> half2 of bytes (0, 1) and of (2, 3).
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// FP8 pages are read with 16-byte loads by permuting the two contractions'
+// index order (a sum does not depend on the order of its terms):
+//  * Q K^T: the MMA step st, lane quad t4 multiplies (logical k) pairs
+//    2 t4 + {0,1} and 8 + 2 t4 + {0,1}; they are taken as the physical dims
+//    p0 + {0,1} and p0 + {2,3} with p0 = 64 (st / 4) + 16 t4 + 4 (st % 4), so
+//    a lane's K codes for steps 0-3 (4-7) are the 16 bytes at 16 t4 (64 +
+//    16 t4) of the token's row.  The query fragments use the same order.
+//  * P V: n-block nb, column n is output dim 16 n + nb (not 8 nb + n), so the
+//    16 V codes a lane needs from a token row are the 16 bytes at 16 g.  The
+//    accumulator column 2 t4 + e of n-block nb is then dim 32 t4 + 16 e + nb.
+__device__ __forceinline__ int attn8_qdim(int st, int t4) { return 64 * (st >> 2) + 16 * t4 + 4 * (st & 3); }
+__device__ __forceinline__ int attn8_odim(int nb, int t4, int e) { return 32 * t4 + 16 * e + nb; }
+
+// Query fragments in the FP8 pages' dim order (see above); heads g >= G are zero.
+__device__ __forceinline__ void attn_q_frags_fp8(const float (*s_q)[ATT_D], int G, int g, int t4,
+                                                 uint32_t (&qa)[8][2]) {
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    if (g < G) {
+      const float4 q4 = *reinterpret_cast<const float4*>(s_q[g] + attn8_qdim(st, t4));
+      const __half2 lo = __floats2half2_rn(q4.x, q4.y);
+      const __half2 hi = __floats2half2_rn(q4.z, q4.w);
+      qa[st][0] = *reinterpret_cast<const uint32_t*>(&lo);
+      qa[st][1] = *reinterpret_cast<const uint32_t*>(&hi);
+    } else {
+      qa[st][0] = qa[st][1] = 0u;
+    }
+  }
+}
+
+// One FP8 page against the warp's query fragments (built by attn_q_frags_fp8):
+// scores scaled by the K row scales, probabilities by the V row scales before
+// P V (the softmax sum keeps the unscaled probabilities); o in the FP8 output
+// dim order (attn8_odim).
 __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv, const uint32_t (&qa)[8][2],
                                               float scale_log2, int g, int t4, float& m_run, float& l_run,
                                               float (&o)[16][4]) {
@@ -227,14 +264,18 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
   float sc[2][4];
 #pragma unroll
   for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
-  const unsigned char* k0 = Kc + g * ATT8_PITCH + 2 * t4;        // token g
-  const unsigned char* k1 = k0 + 8 * ATT8_PITCH;                 // token 8 + g
+  // K codes: tokens g (n-block 0) and 8 + g (n-block 1), dims [16 t4, +16) and [64 + 16 t4, +16)
+  uint4 kw[2][2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      kw[r][h] = *reinterpret_cast<const uint4*>(Kc + (g + 8 * r) * ATT8_PITCH + 64 * h + 16 * t4);
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
-    const uint32_t b0 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k0 + 16 * st));
-    const uint32_t b1 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k0 + 16 * st + 8));
-    const uint32_t b2 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k1 + 16 * st));
-    const uint32_t b3 = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(k1 + 16 * st + 8));
+    uint32_t b0, b1, b2, b3;
+    e4m3x4_to_h2x2((&kw[0][st >> 2].x)[st & 3], b0, b1);
+    e4m3x4_to_h2x2((&kw[1][st >> 2].x)[st & 3], b2, b3);
     mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
     mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
   }
@@ -259,14 +300,19 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
   const __half2 pa = __floats2half2_rn(p00 * vs[2 * t4], p01 * vs[2 * t4 + 1]);
   const __half2 pb = __floats2half2_rn(p10 * vs[8 + 2 * t4], p11 * vs[9 + 2 * t4]);
   const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
-  // V fragments: tokens (2 t4, 2 t4 + 1) and (8 + 2 t4, 9 + 2 t4) of dim 8 nb + g
-  const unsigned char* v0 = Vc + (2 * t4) * ATT8_PITCH + g;
+  // V codes: tokens 2 t4, 2 t4 + 1, 8 + 2 t4, 9 + 2 t4, dims [16 g, +16) (dim 16 g + nb of n-block nb)
+  uint4 vw[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    vw[r] = *reinterpret_cast<const uint4*>(Vc + (2 * t4 + (r & 1) + 8 * (r >> 1)) * ATT8_PITCH + 16 * g);
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) {
-    const uint32_t lo0 = v0[8 * nb], hi0 = v0[ATT8_PITCH + 8 * nb];
-    const uint32_t lo1 = v0[8 * ATT8_PITCH + 8 * nb], hi1 = v0[9 * ATT8_PITCH + 8 * nb];
-    const uint32_t b0 = e4m3x2_to_h2(lo0 | (hi0 << 8));
-    const uint32_t b1 = e4m3x2_to_h2(lo1 | (hi1 << 8));
+    const uint32_t sel = (uint32_t)(nb & 3) | ((uint32_t)(4 + (nb & 3)) << 4);
+    uint32_t pair0, pair1;  // (token 2 t4, 2 t4 + 1) and (8 + 2 t4, 9 + 2 t4) of dim 16 g + nb
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(pair0) : "r"((&vw[0].x)[nb >> 2]), "r"((&vw[1].x)[nb >> 2]), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(pair1) : "r"((&vw[2].x)[nb >> 2]), "r"((&vw[3].x)[nb >> 2]), "r"(sel));
+    const uint32_t b0 = e4m3x2_to_h2(pair0);
+    const uint32_t b1 = e4m3x2_to_h2(pair1);
     o[nb][0] *= c;
     o[nb][1] *= c;
     mma_16816(o[nb], a0, a2, b0, b1);

@@ -16,7 +16,7 @@
 // reads: core matrices of 8 rows x 16 bytes, K-adjacent core matrices 128 B
 // apart, 8-row groups 256 B apart); 256 reader threads turn the 32 codes per
 // stage of their weight row into exact fp16 integers (q in [-8, 7]) and store
-// them with tcgen05.st into one of TC_NAB tensor-memory A buffers (the MMA
+// them with tcgen05.st into one of NAB tensor-memory A buffers (the MMA
 // reads A from tensor memory, so the expanded codes never touch shared
 // memory); one thread issues four kind::f16 MMAs (K = 16) per weight matrix
 // and commits them to the barriers that free the A buffer, the ring slot and,
@@ -44,25 +44,44 @@
 namespace w4 {
 
 constexpr int TC_M = 128;      // weight rows per tile (MMA M)
-constexpr int TC_N = 32;       // batch columns (MMA N)
+constexpr int TC_N = 32;       // batch columns (MMA N) of the decode-batch shape
 constexpr int TC_K = 64;       // K per stage
+constexpr int TC_ACOLS = 32;   // tensor-memory columns of one A buffer (128 rows x 64 k fp16)
 constexpr int TC_READERS = 256;                  // threads that expand codes and read tensor memory
 constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
-constexpr int TC_NAB = 2;      // tensor-memory A buffers: how far code expansion runs ahead of the MMAs
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
-constexpr int TC_B_BYTES = TC_N * TC_K * 2;  // 4 KB activation tile per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
 
-template <bool INT4, bool SILU>
+constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// NC: batch columns per tile (the MMA's N).  32 for decode batches; 128
+// (one weight matrix) or 64 (gate and up together) for the wide row blocks
+// of a prompt, where each weight tile is then read once per NC rows.
+template <bool INT4, bool SILU, int NC>
 struct TcShape {
   static constexpr int NA = SILU ? 2 : 1;                                   // weight matrices per tile
   static constexpr uint32_t A_RAW = INT4 ? NA * TC_M * 32 : TC_A_BYTES;     // A bytes per ring slot
-  static constexpr uint32_t SLOT = A_RAW + TC_B_BYTES;
+  static constexpr uint32_t B_BYTES = NC * TC_K * 2;                        // activation tile per stage
+  static constexpr uint32_t SLOT = A_RAW + B_BYTES;
   static constexpr size_t SMEM = (size_t)TC_S * SLOT + 1024;
-  // tensor memory: 2 group accumulators x NA x 32 columns, and (int4)
-  // TC_NAB A buffers x NA x 32 columns of exact codes (rounded up to a power of two)
-  static constexpr uint32_t TMEM_COLS = INT4 ? 2 * NA * TC_N + TC_NAB * NA * TC_N : 2 * NA * TC_N;
+  static constexpr int CPT = NC / 2;                                        // columns per reader thread
+  // A buffers in tensor memory (int4): how far code expansion runs ahead of
+  // the MMAs.  As many as fit (2 to 4) beside the 2 group accumulators without
+  // costing a CTA per SM: 256 columns for the two-CTA decode shape, else 512.
+  static constexpr int TM_BUDGET = NC == 32 ? 256 : 512;
+  static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
+  static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
+  // tensor memory: 2 group accumulators x NA x NC columns, and (int4) NAB A
+  // buffers x NA x 32 columns of exact codes, rounded up to a power of two
+  static constexpr uint32_t TMEM_COLS =
+      pow2_at_least(INT4 ? 2 * NA * NC + NAB * NA * TC_ACOLS : 2 * NA * NC);
+  static_assert(NC % 32 == 0 && NC <= 128, "NC: 32, 64 or 128 columns");
+  static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
 
 __device__ __forceinline__ unsigned long long tc_now() {
@@ -90,9 +109,11 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor: kind::f16, fp32 accumulate, fp16 A and B, both
-// K-major, N = 32, M = 128.
-constexpr uint32_t TC_IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TC_N >> 3) << 17) |
-                              ((uint32_t)(TC_M >> 4) << 24);
+// K-major, N = NC, M = 128.
+template <int NC>
+constexpr uint32_t tc_idesc() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NC >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
 
 // byte offset of (row, 8-wide k group w) of a 64-wide stage in the canonical layout
 __device__ __forceinline__ uint32_t tc_off(int row, int w, int slice_bytes) {
@@ -175,14 +196,16 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //   aempty[b]    MMAs that read A buffer b are done            (1, commit)
 //   gfull[b]     MMAs of the group in tensor-memory buffer b   (1, commit)
 //   gempty[b]    readers read tensor-memory buffer b           (256)
-template <bool INT4, bool SILU>
-__global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_constant__ TcArgs a) {
-  using SH = TcShape<INT4, SILU>;
+template <bool INT4, bool SILU, int NC>
+__global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_batch(const __grid_constant__ TcArgs a) {
+  using SH = TcShape<INT4, SILU, NC>;
   constexpr int NA = SH::NA;
+  constexpr int CPT = SH::CPT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
-  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[TC_NAB], aempty[TC_NAB], gfull[2], gempty[2], drain;
+  constexpr int NAB = SH::NAB;
+  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[NAB], aempty[NAB], gfull[2], gempty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -196,9 +219,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
   W4_TRACE_SCOPE(a.tag);
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
-  // columns: [0, 2 NA 32) group accumulators; then (int4) A buffer ab, matrix g
-  // at 2 NA 32 + (ab NA + g) 32
-  constexpr uint32_t TM_A = 2 * NA * TC_N;
+  // columns: [0, 2 NA NC) group accumulators; then (int4) A buffer ab, matrix g
+  // at 2 NA NC + (ab NA + g) 32
+  constexpr uint32_t TM_A = 2 * NA * NC;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "r"(TMEM_COLS)
@@ -210,7 +233,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
       mbar_init(&full[i], 32);
       mbar_init(&empty[i], TC_READERS + 1);
     }
-    for (int i = 0; i < TC_NAB; ++i) {
+    for (int i = 0; i < NAB; ++i) {
       mbar_init(&afull[i], TC_READERS);
       mbar_init(&aempty[i], 1);
     }
@@ -316,12 +339,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
     };
     auto load_b = [&](int slot, int st) {
       unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
+#pragma unroll 8
+      for (int i = 0; i < NC / 4; ++i) {
         const int c = lane + 32 * i;
         const int m = c >> 3, w = c & 7;
         const bool ok = m < M;
-        cp_async16_zfill(sb + tc_off(m, w, TC_N * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
+        cp_async16_zfill(sb + tc_off(m, w, NC * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
       }
     };
     // prologue: the weights of the first stages before the dependency wait
@@ -368,37 +391,37 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
       c_init(cur);
       uint32_t s = 0;
       for (; cur.work < nwork; ++s) {
-        const int slot = s % TC_S, ab = s % TC_NAB;
+        const int slot = s % TC_S, ab = s % NAB;
         const uint32_t grp = s >> 1;
         const bool gfirst = (s & 1) == 0;
         if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl)) break;
-        if (INT4 && !tcw_wait(&afull[ab], (s / TC_NAB) & 1, &s_fail, wl)) break;
+        if (INT4 && !tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl)) break;
         if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl)) break;
         fence_proxy_async_smem();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         unsigned char* sl = ring + slot * SH::SLOT;
-        const uint32_t gbase = tmem + (grp & 1) * (NA * TC_N);
+        const uint32_t gbase = tmem + (grp & 1) * (NA * NC);
         const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
-            const uint64_t bd = bd0 + (uint64_t)((kk * TC_N * 32) >> 4);  // next 16-k slice of B
+            const uint64_t bd = bd0 + (uint64_t)((kk * NC * 32) >> 4);  // next 16-k slice of B
             const uint32_t accum = (!gfirst || kk > 0) ? 1u : 0u;
             if (INT4) {
               // A (128 x 16 exact codes) from tensor memory: 8 columns per 16 k
-              const uint32_t at = tmem + TM_A + (uint32_t)((ab * NA + g) * TC_N + kk * 8);
+              const uint32_t at = tmem + TM_A + (uint32_t)((ab * NA + g) * TC_ACOLS + kk * 8);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
-                  "r"(at), "l"(bd), "r"(TC_IDESC), "r"(accum)
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * NC)),
+                  "r"(at), "l"(bd), "r"(tc_idesc<NC>()), "r"(accum)
                   : "memory");
             } else {
               const uint64_t ad = tc_desc(smem_u32(sl + kk * TC_M * 32));
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * TC_N)),
-                  "l"(ad), "l"(bd), "r"(TC_IDESC), "r"(accum)
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * NC)),
+                  "l"(ad), "l"(bd), "r"(tc_idesc<NC>()), "r"(accum)
                   : "memory");
             }
           }
@@ -421,7 +444,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
     // =========================== readers ====================================
     pdl_wait_then_trigger();
     const int r = tid - 64;                       // 0..255
-    const int half = r >> 7;                      // k chunks 4h..4h+3; batch columns 16h..16h+15
+    const int half = r >> 7;                      // k chunks 4h..4h+3; batch columns CPT h .. CPT h + CPT - 1
     const int row_l = 32 * (warp & 3) + lane;     // tensor-memory lanes of this warp's quadrant
     Cursor cur;
     c_init(cur);
@@ -432,32 +455,35 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
     __half sreg0[NA], sreg1[NA];  // scales of groups with even / odd index
 #pragma unroll
     for (int g = 0; g < NA; ++g) sreg0[g] = sreg1[g] = __float2half(0.f);
-    float acc[NA][16];
+    float acc[NA][CPT];
 #pragma unroll
     for (int g = 0; g < NA; ++g)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+      for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
 
-    // add tensor-memory group `grp` (this row, 16 columns) times the scales
+    // add tensor-memory group `grp` (this row, CPT columns) times the scales
     auto tm_read = [&](uint32_t grp) {
       const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail, wl));
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          uint32_t v[16];
-          const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * TC_N) +
-                                 (uint32_t)(g * TC_N + half * 16);
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-              : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                "=r"(v[15])
-              : "r"(taddr));
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           const float sc = INT4 ? __half2float((grp & 1) ? sreg1[g] : sreg0[g]) : 1.0f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[g][j] = fmaf(__uint_as_float(v[j]), sc, acc[g][j]);
+          for (int c0 = 0; c0 < CPT; c0 += 16) {
+            uint32_t v[16];
+            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * NC) +
+                                   (uint32_t)(g * NC + half * CPT + c0);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                  "=r"(v[15])
+                : "r"(taddr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[g][c0 + j] = fmaf(__uint_as_float(v[j]), sc, acc[g][c0 + j]);
+          }
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       }
@@ -469,11 +495,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
       const int row = tile * TC_M + row_l;
       bool finish = true;
       if (ks > 1) {
-        float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * TC_N * TC_M);
+        float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * NC * TC_M);
 #pragma unroll
         for (int g = 0; g < NA; ++g)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) wsp[(g * TC_N + half * 16 + j) * TC_M + row_l] = acc[g][j];
+          for (int j = 0; j < CPT; ++j) wsp[(g * NC + half * CPT + j) * TC_M + row_l] = acc[g][j];
         __threadfence();
         readers_sync();
         if (r == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
@@ -484,13 +510,13 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
 #pragma unroll
           for (int g = 0; g < NA; ++g)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+            for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
           for (int spl = 0; spl < ks; ++spl) {
-            const float* wp = a.ws + ((size_t)tile * ks + spl) * (size_t)(NA * TC_N * TC_M);
+            const float* wp = a.ws + ((size_t)tile * ks + spl) * (size_t)(NA * NC * TC_M);
 #pragma unroll
             for (int g = 0; g < NA; ++g)
 #pragma unroll
-              for (int j = 0; j < 16; ++j) acc[g][j] += __ldcg(&wp[(g * TC_N + half * 16 + j) * TC_M + row_l]);
+              for (int j = 0; j < CPT; ++j) acc[g][j] += __ldcg(&wp[(g * NC + half * CPT + j) * TC_M + row_l]);
           }
           if (r == 0) a.counters[tile] = 0u;  // ready for the next call
         }
@@ -498,14 +524,14 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
       if (!finish || row >= N) return;
       if (a.y32 != nullptr) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = half * 16 + j;
+        for (int j = 0; j < CPT; ++j) {
+          const int m = half * CPT + j;
           if (m < M) a.y32[(size_t)m * a.ldy + row] = acc[0][j];
         }
       } else if (SILU) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = half * 16 + j;
+        for (int j = 0; j < CPT; ++j) {
+          const int m = half * CPT + j;
           if (m < M) {
             const float gv = __half2float(__float2half_rn(acc[0][j]));
             const float u = __half2float(__float2half_rn(acc[NA - 1][j]));
@@ -522,8 +548,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
           if (a.seg[si].bias) bv = __half2float(a.seg[si].bias[rr]);
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = half * 16 + j;
+        for (int j = 0; j < CPT; ++j) {
+          const int m = half * CPT + j;
           if (m < M) {
             float v = acc[0][j] + bv;
             if (a.residual) v += __half2float(a.residual[(size_t)m * a.ldy + row]);
@@ -534,12 +560,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
     };
 
     for (uint32_t s = 0; cur.work < nwork; ++s) {
-      const int slot = s % TC_S, ab = s % TC_NAB;
+      const int slot = s % TC_S, ab = s % NAB;
       const uint32_t grp = s >> 1;
       const bool gfirst = (s & 1) == 0;
       if (INT4) {
         // (1) the A buffer's previous MMAs are done, the slot's copies landed
-        if (s >= TC_NAB) (void)tcw_wait(&aempty[ab], ((s - TC_NAB) / TC_NAB) & 1, &s_fail, wl);
+        if (s >= NAB) (void)tcw_wait(&aempty[ab], ((s - NAB) / NAB) & 1, &s_fail, wl);
         (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl);
         // (2) this group's scale (used when the group is read, three stages on)
         // (loaded straight into the register that holds it until the read,
@@ -561,7 +587,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
         for (int g = 0; g < NA; ++g) {
           const uint4 raw = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + half * 16);
           const uint4 c0 = codes_word(raw.x), c1 = codes_word(raw.y), c2 = codes_word(raw.z), c3 = codes_word(raw.w);
-          const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A + (uint32_t)((ab * NA + g) * TC_N + half * 16);
+          const uint32_t ta =
+              tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A + (uint32_t)((ab * NA + g) * TC_ACOLS + half * 16);
           asm volatile(
               "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
               "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w), "r"(c2.x), "r"(c2.y),
@@ -584,7 +611,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
 #pragma unroll
         for (int g = 0; g < NA; ++g)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+          for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
         if (r == 0) s_rfail = s_fail;
         readers_sync();
         if (s_rfail) break;
@@ -603,11 +630,18 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 2) w4pg_tc_batch(const __grid_c
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
 }
 
-size_t tc_workspace_bytes(int N, int ksplit, bool silu) {
+int tc_cols(int M, bool int4, bool silu) {
+  if (M <= TC_N || !int4) return TC_N;
+  return silu ? 64 : 128;
+}
+
+int tc_max_rows(bool int4, bool silu) { return int4 ? (silu ? 64 : 128) : TC_N; }
+
+size_t tc_workspace_bytes(int N, int ksplit, bool silu, int nc) {
   const int ntiles = (N + TC_M - 1) / TC_M;
   const size_t na = silu ? 2 : 1;
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  return TC_TICKET_BYTES + up((size_t)ntiles * ksplit * na * TC_N * TC_M * 4);
+  return TC_TICKET_BYTES + up((size_t)ntiles * ksplit * na * nc * TC_M * 4);
 }
 
 void tc_workspace_layout(TcArgs& a, void* ws) {
@@ -615,36 +649,38 @@ void tc_workspace_layout(TcArgs& a, void* ws) {
   a.ws = reinterpret_cast<float*>(static_cast<char*>(ws) + TC_TICKET_BYTES);
 }
 
-template <bool INT4, bool SILU>
+template <bool INT4, bool SILU, int NC>
 static int tc_ctas_per_sm() {
+  using SH = TcShape<INT4, SILU, NC>;
   static PerDeviceOnce once;
   static int cached[64] = {};
   once_per_device(once, [] {
-    auto kern = w4pg_tc_batch<INT4, SILU>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcShape<INT4, SILU>::SMEM);
+    auto kern = w4pg_tc_batch<INT4, SILU, NC>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM);
     int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, TcShape<INT4, SILU>::SMEM) !=
-            cudaSuccess ||
-        bps < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, SH::SMEM) != cudaSuccess || bps < 1)
       bps = 1;
-    cached[device_index() & 63] = std::min(bps, 4);  // tensor memory: at most 4 x 128 columns per SM
+    // tensor memory: 512 columns per SM
+    cached[device_index() & 63] = std::max(1, std::min(bps, (int)(512 / SH::TMEM_COLS)));
   });
   return cached[device_index() & 63];
 }
 
-static int tc_slots(bool int4, bool silu) {
-  const int per = !int4 ? tc_ctas_per_sm<false, false>()
-                        : (silu ? tc_ctas_per_sm<true, true>() : tc_ctas_per_sm<true, false>());
+static int tc_slots(bool int4, bool silu, int nc) {
+  int per;
+  if (!int4) per = tc_ctas_per_sm<false, false, TC_N>();
+  else if (nc == TC_N) per = silu ? tc_ctas_per_sm<true, true, TC_N>() : tc_ctas_per_sm<true, false, TC_N>();
+  else per = silu ? tc_ctas_per_sm<true, true, 64>() : tc_ctas_per_sm<true, false, 128>();
   return per * num_sms();
 }
 
 // Split of K: the split length (even number of stages, so splits start on a
 // scale group) that minimises waves x (stages per item + a per-item
 // overhead of ~4 stages) over the CTAs that fit on the GPU.
-void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split) {
+void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split, int nc) {
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nst = K / TC_K;
-  const int slots = tc_slots(int4, silu);
+  const int slots = tc_slots(int4, silu, nc);
   int best_ps = nst, best_ks = 1;
   long best = -1;
   for (int p = nst; p >= 2; p -= 2) {
@@ -674,7 +710,9 @@ unsigned long long tc_wait_limit_ns() { return g_wait_limit_ns.load(); }
 int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   TcArgs a = a_in;
   a.wait_limit_ns = TC_TIMEOUT_NS;
-  if (a.M < 1 || a.M > TC_N) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, TC_N);
+  const int maxm = tc_max_rows(int4, silu);
+  if (a.M < 1 || a.M > maxm) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, maxm);
+  const int nc = tc_cols(a.M, int4, silu);
   // stages pair into 128-wide groups (the int4 scale group), dense weights too
   if (a.K % 128 != 0) return set_error(W4A16_ERR_SHAPE, "gemm_tc: K=%d not a multiple of 128", a.K);
   if (a.ksplit < 1) return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: ksplit < 1");
@@ -691,9 +729,14 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
     if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemm_tc launch: %s", cudaGetErrorString(e));
     return W4A16_OK;
   };
-  if (!int4) return go(w4pg_tc_batch<false, false>, TcShape<false, false>::SMEM, tc_ctas_per_sm<false, false>());
-  if (silu) return go(w4pg_tc_batch<true, true>, TcShape<true, true>::SMEM, tc_ctas_per_sm<true, true>());
-  return go(w4pg_tc_batch<true, false>, TcShape<true, false>::SMEM, tc_ctas_per_sm<true, false>());
+  if (!int4) return go(w4pg_tc_batch<false, false, TC_N>, TcShape<false, false, TC_N>::SMEM,
+                       tc_ctas_per_sm<false, false, TC_N>());
+  if (nc == TC_N) {
+    if (silu) return go(w4pg_tc_batch<true, true, TC_N>, TcShape<true, true, TC_N>::SMEM, tc_ctas_per_sm<true, true, TC_N>());
+    return go(w4pg_tc_batch<true, false, TC_N>, TcShape<true, false, TC_N>::SMEM, tc_ctas_per_sm<true, false, TC_N>());
+  }
+  if (silu) return go(w4pg_tc_batch<true, true, 64>, TcShape<true, true, 64>::SMEM, tc_ctas_per_sm<true, true, 64>());
+  return go(w4pg_tc_batch<true, false, 128>, TcShape<true, false, 128>::SMEM, tc_ctas_per_sm<true, false, 128>());
 }
 
 }  // namespace w4
@@ -750,25 +793,27 @@ extern "C" unsigned long long w4a16_debug_set_wait_limit_ns(unsigned long long n
 }
 
 extern "C" size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu) {
-  (void)M;
-  if (K < 128 || N < 1) return 0;
+  if (K < 128 || N < 1 || M < 1) return 0;
+  const int nc = tc_cols(M, true, silu != 0);
   int ks = 1, ps = 0;
-  tc_plan(N, K, true, silu != 0, true, &ks, &ps);
-  return tc_workspace_bytes(N, ks, silu != 0);
+  tc_plan(N, K, true, silu != 0, true, &ks, &ps, nc);
+  return tc_workspace_bytes(N, ks, silu != 0, nc);
 }
 
 static int tc_common_checks(const uint16_t* x, int M, int K, int N, const uint16_t* y, const void* ws, size_t wsb,
                             int N_silu, int* ksplit, int* per_split) {
   W4_CHECK_ARG(x && y, "w4a16_gemm: null x or y");
   W4_CHECK_ARG(M >= 1 && K >= 1 && N >= 1, "w4a16_gemm: sizes must be positive");
-  W4_CHECK_SHAPE(M <= 32, "w4a16_gemm: M=%d > 32", M);
+  const int maxm = tc_max_rows(true, N_silu != 0);
+  W4_CHECK_SHAPE(M <= maxm, "w4a16_gemm: M=%d > %d", M, maxm);
   W4_CHECK_SHAPE(K % 128 == 0, "w4a16_gemm: K=%d must be a multiple of 128", K);
   W4_CHECK_ALIGN(x, 128, "x");
   W4_CHECK_ALIGN(y, 128, "y");
   W4_CHECK_ALIGN(ws, 128, "workspace");
-  tc_plan(N, K, true, N_silu != 0, ws != nullptr, ksplit, per_split);
-  if (*ksplit > 1 && wsb < tc_workspace_bytes(N, *ksplit, N_silu != 0))
-    tc_plan(N, K, true, N_silu != 0, false, ksplit, per_split);
+  const int nc = tc_cols(M, true, N_silu != 0);
+  tc_plan(N, K, true, N_silu != 0, ws != nullptr, ksplit, per_split, nc);
+  if (*ksplit > 1 && wsb < tc_workspace_bytes(N, *ksplit, N_silu != 0, nc))
+    tc_plan(N, K, true, N_silu != 0, false, ksplit, per_split, nc);
   return W4A16_OK;
 }
 

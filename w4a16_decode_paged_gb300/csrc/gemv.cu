@@ -42,9 +42,11 @@ namespace w4 {
 constexpr int GEMV_WPB = 8;  // warps per block
 constexpr int GEMV_U = 8;    // 16-byte weight loads in flight per lane
 
+// gpre: gamma's groups already in registers (loaded before the dependency
+// wait by the caller), or null to load them here.
 template <int MT>
 __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, float* cs, float (*red)[MT],
-                                                  float* rscale) {
+                                                  float* rscale, const uint4* gpre = nullptr) {
   const int K = a.K, M = a.M, NCH = K >> 5, NG = K >> 3;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -59,7 +61,7 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
     for (int i = 0; i < STAGE_GMAX; ++i) {
       const int g = tid + i * nthr;
       if (g < NG) {
-        gr[i] = *reinterpret_cast<const uint4*>(a.gamma + 8 * g);
+        gr[i] = gpre ? gpre[i] : *reinterpret_cast<const uint4*>(a.gamma + 8 * g);
 #pragma unroll
         for (int m = 0; m < MT; ++m)
           if (m < M) xr[m][i] = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + 8 * g);
@@ -449,6 +451,17 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) w4pg_matvec_int4_ring(cons
     }
   };
 
+  // RMSNorm weight first: like the weights it does not depend on the
+  // previous kernel, and it is rarely still in L2 when its layer comes round
+  uint4 gpre[STAGE_GMAX];
+  const bool gp = a.gamma != nullptr && (K >> 3) <= STAGE_GMAX * NT;
+  if (gp) {
+#pragma unroll
+    for (int i = 0; i < STAGE_GMAX; ++i) {
+      const int g = tid + i * NT;
+      if (g < (K >> 3)) gpre[i] = *reinterpret_cast<const uint4*>(a.gamma + 8 * g);
+    }
+  }
   // the first NS - 1 batches: weights do not depend on the previous kernel
 #pragma unroll
   for (int q0 = 0; q0 < NS - 1; ++q0) {
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(WPB * 32, 32 / WPB) w4pg_matvec_int4_ring(cons
   }
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
-  stage_activations<MT>(a, xs, cs, red, rscale);
+  stage_activations<MT>(a, xs, cs, red, rscale, gp ? gpre : nullptr);
   W4_TRACE_MARK(0);
 
   // compute side

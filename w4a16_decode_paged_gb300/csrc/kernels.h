@@ -31,7 +31,8 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, bool silu, cudaStream_t s);
 int gemv_cuda_core_supported(int M, int K);
 
-// Tensor-core (tcgen05) GEMM for decode batches of up to 32 sequences.
+// Tensor-core (tcgen05) GEMM: decode batches of up to 32 sequences, and the
+// wider row blocks of a prompt (up to tc_max_rows rows per call).
 struct TcArgs {
   const __half* x;         // [M][K] activations
   const __half* residual;  // [M][ldy] or null
@@ -59,9 +60,12 @@ int launch_gemm_tc(const TcArgs& a, bool int4, bool silu, cudaStream_t s);
 // workspace can serve calls of different shapes in turn.
 constexpr size_t TC_TICKET_BYTES = 8192;    // one ticket per 128-row tile: up to 2048 tiles
 constexpr size_t ATT_TICKET_BYTES = 16384;  // one ticket per (sequence, kv head): up to 4096
-size_t tc_workspace_bytes(int N, int ksplit, bool silu);
+// batch columns per tile for M rows (32, or 64 / 128 for wider int4 blocks)
+int tc_cols(int M, bool int4, bool silu);
+int tc_max_rows(bool int4, bool silu);  // 128 int4, 64 int4 gate|up, 32 dense
+size_t tc_workspace_bytes(int N, int ksplit, bool silu, int nc = 32);
 // split of K (ksplit splits of per_split stages) that fills whole waves of CTAs
-void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split);
+void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split, int nc = 32);
 void tc_workspace_layout(TcArgs& a, void* ws);  // sets a.counters / a.ws (a.ksplit > 1)
 int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
                        int tag);

@@ -432,7 +432,27 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
 struct PrefillWs {
   __half *x, *xn, *qkv, *att, *h, *mlp;
   int32_t *bt_rep, *lens;
+  void* tc;         // split-K workspace of the tensor-core GEMMs (tickets first)
+  size_t tc_bytes;
 };
+
+// rows per tensor-core GEMM launch of the prompt, and that launch's split-K
+// workspace need (the largest over the layer's projections)
+static size_t prefill_tc_bytes(const w4a16_model_config& c, int T) {
+  const int D = c.head_dim;
+  const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * D;
+  const struct { int N, K; bool silu; } proj[4] = {
+      {nqkv, c.hidden, false}, {c.hidden, c.n_q_heads * D, false}, {c.inter, c.hidden, true}, {c.hidden, c.inter, false}};
+  size_t need = TC_TICKET_BYTES;
+  for (const auto& p : proj) {
+    const int rows = std::min(T, tc_max_rows(true, p.silu));
+    const int nc = tc_cols(rows, true, p.silu);
+    int ks = 1, ps = 0;
+    tc_plan(p.N, p.K, true, p.silu, true, &ks, &ps, nc);
+    if (ks > 1) need = std::max(need, tc_workspace_bytes(p.N, ks, p.silu, nc));
+  }
+  return need;
+}
 
 static size_t prefill_layout(const w4a16_model* m, int T, int max_blocks, char* base, PrefillWs* w) {
   const w4a16_model_config& c = m->cfg;
@@ -452,6 +472,8 @@ static size_t prefill_layout(const w4a16_model* m, int T, int max_blocks, char* 
   char* pmlp = take((size_t)T * c.inter * 2);
   char* pbt = take((size_t)T * max_blocks * 4);
   char* pl = take((size_t)T * 4);
+  const size_t tcb = prefill_tc_bytes(c, T);
+  char* ptc = take(tcb);
   if (w) {
     w->x = reinterpret_cast<__half*>(px);
     w->xn = reinterpret_cast<__half*>(pxn);
@@ -461,6 +483,8 @@ static size_t prefill_layout(const w4a16_model* m, int T, int max_blocks, char* 
     w->mlp = reinterpret_cast<__half*>(pmlp);
     w->bt_rep = reinterpret_cast<int32_t*>(pbt);
     w->lens = reinterpret_cast<int32_t*>(pl);
+    w->tc = ptc;
+    w->tc_bytes = tcb;
   }
   return off;
 }
@@ -470,11 +494,14 @@ extern "C" size_t w4a16_prefill_workspace_size(w4a16_model* m, int T, int max_bl
   return prefill_layout(m, T, max_blocks, nullptr, nullptr);
 }
 
-// y[T][N] = x[T][K] . W^T (+bias, +residual; SiLU-mul for gate|up) in row
-// chunks of at most 32 on the tensor cores
-static int gemm_rows(w4a16_model* m, const __half* x, int T, int K, const GemvSeg* segs, int nseg, int N,
-                     const __half* residual, __half* y, bool silu, cudaStream_t s) {
-  for (int r0 = 0; r0 < T; r0 += 32) {
+// y[T][N] = x[T][K] . W^T (+bias, +residual; SiLU-mul for gate|up) on the
+// tensor cores in row blocks of up to 128 (64 for gate|up, whose two weight
+// matrices share the tile's tensor memory), so each weight tile is read once
+// per block
+static int gemm_rows(w4a16_model* m, const PrefillWs& w, const __half* x, int T, int K, const GemvSeg* segs, int nseg,
+                     int N, const __half* residual, __half* y, bool silu, cudaStream_t s) {
+  const int rows = tc_max_rows(true, silu);
+  for (int r0 = 0; r0 < T; r0 += rows) {
     TcArgs t = {};
     t.x = x + (size_t)r0 * K;
     t.residual = residual ? residual + (size_t)r0 * N : nullptr;
@@ -482,14 +509,15 @@ static int gemm_rows(w4a16_model* m, const __half* x, int T, int K, const GemvSe
     for (int i = 0; i < nseg; ++i) t.seg[i] = segs[i];
     t.nseg = nseg;
     t.err_flag = m->err_flag;
-    t.M = std::min(32, T - r0);
+    t.M = std::min(rows, T - r0);
     t.K = K;
     t.N = N;
     t.ldy = N;
-    tc_plan(N, K, true, silu, true, &t.ksplit, &t.per_split);
-    if (t.ksplit > 1 && tc_workspace_bytes(N, t.ksplit, silu) > m->tc_ws_bytes)
-      tc_plan(N, K, true, silu, false, &t.ksplit, &t.per_split);
-    if (t.ksplit > 1) tc_workspace_layout(t, m->tc_ws);
+    const int nc = tc_cols(t.M, true, silu);
+    tc_plan(N, K, true, silu, true, &t.ksplit, &t.per_split, nc);
+    if (t.ksplit > 1 && tc_workspace_bytes(N, t.ksplit, silu, nc) > w.tc_bytes)
+      tc_plan(N, K, true, silu, false, &t.ksplit, &t.per_split, nc);
+    if (t.ksplit > 1) tc_workspace_layout(t, w.tc);
     const int rc = launch_gemm_tc(t, true, silu, s);
     if (rc) return rc;
   }
@@ -515,6 +543,9 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
   prefill_layout(m, T, max_blocks, static_cast<char*>(workspace), &w);
   auto hp = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
   int rc;
+  // split-K tickets of the GEMMs start at zero (each call leaves them zero)
+  if (cudaMemsetAsync(w.tc, 0, TC_TICKET_BYTES, s) != cudaSuccess)
+    return set_error(W4A16_ERR_CUDA, "prefill: workspace memset failed");
   if ((rc = launch_embedding(m->embed, c.vocab, H, tokens, T, w.x, m->err_flag, nullptr, 0, s))) return rc;
   if ((rc = launch_prefill_rows(block_table, max_blocks, context_lens, T, w.bt_rep, w.lens, s))) return rc;
   for (int l = 0; l < c.n_layers; ++l) {
@@ -522,7 +553,7 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
     if ((rc = launch_rmsnorm(w.x, hp(L.ln1), w.xn, T, H, c.eps, s))) return rc;
     const GemvSeg qkv[3] = {{L.wq, hp(L.sq), hp(L.bq), Hq * D}, {L.wk, hp(L.sk), hp(L.bk), Hkv * D},
                             {L.wv, hp(L.sv), hp(L.bv), Hkv * D}};
-    if ((rc = gemm_rows(m, w.xn, T, H, qkv, 3, nqkv, nullptr, w.qkv, false, s))) return rc;
+    if ((rc = gemm_rows(m, w, w.xn, T, H, qkv, 3, nqkv, nullptr, w.qkv, false, s))) return rc;
     RopeArgs ra = {};
     ra.q = w.qkv;
     ra.k = w.qkv + (size_t)Hq * D;
@@ -560,12 +591,12 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
     a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
     if ((rc = launch_paged_attention(a, s))) return rc;
     const GemvSeg o[1] = {{L.wo, hp(L.so), nullptr, H}};
-    if ((rc = gemm_rows(m, w.att, T, Hq * D, o, 1, H, w.x, w.h, false, s))) return rc;
+    if ((rc = gemm_rows(m, w, w.att, T, Hq * D, o, 1, H, w.x, w.h, false, s))) return rc;
     if ((rc = launch_rmsnorm(w.h, hp(L.ln2), w.xn, T, H, c.eps, s))) return rc;
     const GemvSeg gu[2] = {{L.wg, hp(L.sg), nullptr, I}, {L.wu, hp(L.su), nullptr, I}};
-    if ((rc = gemm_rows(m, w.xn, T, H, gu, 2, I, nullptr, w.mlp, true, s))) return rc;
+    if ((rc = gemm_rows(m, w, w.xn, T, H, gu, 2, I, nullptr, w.mlp, true, s))) return rc;
     const GemvSeg dn[1] = {{L.wd, hp(L.sd), nullptr, H}};
-    if ((rc = gemm_rows(m, w.mlp, T, I, dn, 1, H, w.h, w.x, false, s))) return rc;
+    if ((rc = gemm_rows(m, w, w.mlp, T, I, dn, 1, H, w.h, w.x, false, s))) return rc;
   }
   // the last prompt token's logits and greedy next token
   LmHeadArgs la = {};
