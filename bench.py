@@ -670,6 +670,26 @@ def main():
         e2e_s = time.perf_counter() - t0
         barrier()
 
+        # ---- the same steps without the CUDA graph (direct launches) ------
+        eager = None
+        if not args.no_kernel_timing:
+            ke = min(K, 20)
+            lens.copy_(lens_init)
+            for _ in range(2):
+                model.decode_step(tok, tok, bt, lens, use_graph=False)
+            stream.synchronize()
+            lens.copy_(lens_init)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(ke):
+                model.decode_step(tok, tok, bt, lens, use_graph=False)
+            g1.record(stream)
+            stream.synchronize()
+            assert model.check_errors(stream) == 0
+            eager = {"ms_per_step": g0.elapsed_time(g1) / ke, "steps": ke,
+                     "how": "decode_step with use_graph=0: the same kernels launched from the host each step"}
+            lens.copy_(lens_init)
+
         # ---- the other decode path on the same model (b=1): its step time --
         other = None
         if args.workload == "b1" and not args.no_kernel_timing:
@@ -752,6 +772,9 @@ def main():
                            "achieved": kern["gateup"]["gbs"], "peak": peak, "unit": "GB/s",
                            "frac": kern["gateup"]["gbs"] / peak, "peak_source": peak_src,
                            "traffic": traffic_record("gemv_gateup" if B <= 4 else "gemm_tc_gateup_b32")}
+    if eager is not None:
+        eager["graph_speedup"] = eager["ms_per_step"] / (ms / K)
+        out["eager"] = eager
     if ttft is not None:
         out["ttft"] = ttft
     if other is not None:

@@ -580,6 +580,140 @@ int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
+// Causal attention of a prompt (prefill): row i of q (i < T) is the token at
+// position context_lens[i] - 1 of ONE sequence, whose pages are row 0 of the
+// block table, and attends to the keys at positions 0 .. its own.  A CTA
+// takes 16 consecutive rows and one kv head; every K/V page of its range is
+// copied once into a ring shared by the CTA's 8 warps, and warp w works on
+// rows 2w and 2w + 1 together (the MMA's rows 0-7 and 8-15), so each page
+// feeds 16 query tokens x G heads.
+// ---------------------------------------------------------------------------
+constexpr int PF_ROWS = 16;    // query rows per CTA
+constexpr int PF_WARPS = 8;
+constexpr int PF_STAGES = 3;   // page slots of the CTA's ring
+
+template <int G>
+__global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_constant__ AttnArgs a) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kvh = blockIdx.y;
+  const int row0 = blockIdx.x * PF_ROWS;
+  const int g = lane >> 2, t4 = lane & 3;
+  W4_TRACE_SCOPE(a.tag);
+  pdl_wait_then_trigger();
+  W4_TRACE_WAITED();
+  // this warp's two rows and their positions (-1: no such row)
+  const int rA = row0 + 2 * warp, rB = rA + 1;
+  const int posA = rA < a.B ? __ldcg(&a.context_lens[rA]) - 1 : -1;
+  const int posB = rB < a.B ? __ldcg(&a.context_lens[rB]) - 1 : -1;
+  // the CTA's key range: up to its last row's position
+  const int rl = min(a.B, row0 + PF_ROWS) - 1;
+  const int L = __ldcg(&a.context_lens[rl]);
+  const int npages = (L + ATT_PAGE - 1) / ATT_PAGE;
+  if (L > a.max_blocks * ATT_PAGE && tid == 0 && a.err_flag) atomicOr(a.err_flag, 1);
+  // query fragments: rows g (token A) and 8 + g (token B), head kvh G + g
+  uint32_t qa[8][4];
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = r ? rB : rA;
+      uint32_t lo = 0u, hi = 0u;
+      if (g < G && row < a.B) {
+        const __half* qrow = a.q + (size_t)row * a.q_stride + (size_t)(kvh * G + g) * ATT_D + 16 * st + 2 * t4;
+        lo = __ldcg(reinterpret_cast<const unsigned int*>(qrow));
+        hi = __ldcg(reinterpret_cast<const unsigned int*>(qrow + 8));
+      }
+      qa[st][r] = lo;
+      qa[st][2 + r] = hi;
+    }
+  }
+  constexpr int SLOT = 2 * ATT_SSLICE * 2;  // K and V slices, padded rows
+  auto page_id = [&](int li) -> int {
+    const int pg = li < a.max_blocks ? __ldcg(&a.block_table[li]) : -1;
+    return (pg >= 0 && pg < a.num_pages) ? pg : -1;
+  };
+  // page li into slot li % PF_STAGES: 2 x 16 rows of 256 bytes, 512 16-byte
+  // copies over the CTA's 256 threads; one commit group per page
+  auto issue = [&](int li) {
+    if (li < npages) {
+      const int pg = page_id(li);
+      if (pg >= 0) {
+        unsigned char* dst = smraw + (size_t)(li % PF_STAGES) * SLOT;
+        const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = tid + 256 * i;  // [K|V][row][16 chunks]
+          const int which = c >> 8, row = (c >> 4) & 15, col = c & 15;
+          cp_async16(dst + (size_t)which * ATT_SSLICE * 2 + row * ATT_PITCH * 2 + col * 16,
+                     (which ? a.v_pool : a.k_pool) + off + (size_t)row * ATT_D + col * 8);
+        }
+      } else if (tid == 0 && a.err_flag) {
+        atomicOr(a.err_flag, 1);
+      }
+    }
+    cp_async_commit();
+  };
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[16][4];
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  const uint32_t k_off = attn_k_off(lane), v_off = attn_v_off(lane);
+#pragma unroll
+  for (int i = 0; i < PF_STAGES - 1; ++i) issue(i);
+  for (int li = 0; li < npages; ++li) {
+    cp_async_wait<PF_STAGES - 2>();  // this thread's copies of page li landed
+    __syncthreads();                 // everyone's; and every warp is done with page li - 1
+    issue(li + PF_STAGES - 1);       // into the slot page li - 1 used
+    const int tok0 = li * ATT_PAGE;
+    // rows whose position is before this page see nothing in it (posB is -1
+    // when the warp has only row A)
+    if (max(posA, posB) >= tok0 && page_id(li) >= 0) {
+      const __half* Ks = reinterpret_cast<const __half*>(smraw + (size_t)(li % PF_STAGES) * SLOT);
+      attn_page_pair(Ks, Ks + ATT_SSLICE, tok0, posA, posB, qa, a.scale_log2, k_off, v_off, t4, m_run, l_run, o);
+    }
+  }
+  cp_async_wait<0>();
+  // normalise and write: row g -> token A, head kvh G + g; row 8 + g -> token B
+  if (g < G) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = r ? rB : rA;
+      if (row >= a.B) continue;
+      const float inv = l_run[r] > 0.f ? 1.0f / l_run[r] : 0.f;
+      __half* out = a.out + (size_t)row * a.Hq * ATT_D + (size_t)(kvh * G + g) * ATT_D + 2 * t4;
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb)
+        *reinterpret_cast<__half2*>(out + 8 * nb) = __floats2half2_rn(o[nb][2 * r] * inv, o[nb][2 * r + 1] * inv);
+    }
+  }
+}
+
+template <int G>
+static int launch_prefill_attn_g(const AttnArgs& a, cudaStream_t s) {
+  constexpr size_t smem = (size_t)PF_STAGES * 2 * ATT_SSLICE * 2;
+  auto kern = w4pg_prefill_attn<G>;
+  static PerDeviceOnce once;
+  once_per_device(once, [&] { cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); });
+  const dim3 grid((a.B + PF_ROWS - 1) / PF_ROWS, a.Hkv);
+  cudaError_t e = launch_pdl(kern, grid, dim3(PF_WARPS * 32), smem, s, a);
+  if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "prefill attention launch: %s", cudaGetErrorString(e));
+  return W4A16_OK;
+}
+
+int launch_prefill_attention(const AttnArgs& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_prefill_attn_g<1>(a, s);
+    case 2: return launch_prefill_attn_g<2>(a, s);
+    case 4: return launch_prefill_attn_g<4>(a, s);
+    case 7: return launch_prefill_attn_g<7>(a, s);
+    case 8: return launch_prefill_attn_g<8>(a, s);
+    default:
+      return set_error(W4A16_ERR_SHAPE, "prefill attention: Hq/Hkv=%d not built (1, 2, 4, 7, 8)", a.Hq / a.Hkv);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // RoPE + KV append: one CTA per sequence.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) w4pg_rope_append(const __grid_constant__ RopeArgs a) {

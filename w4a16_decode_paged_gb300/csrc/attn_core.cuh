@@ -185,6 +185,93 @@ __device__ __forceinline__ void attn_page_half(const __half* Ks, const __half* V
   }
 }
 
+// d += A (16 x 16, fp16, all rows) x B (16 x 8, fp16), fp32 accumulate.
+// a0: A[g][2t..], a1: A[8+g][2t..], a2: A[g][8+2t..], a3: A[8+g][8+2t..].
+__device__ __forceinline__ void mma_16816_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One page against two query tokens at once (causal prompt attention): the
+// MMA's rows 0-7 are the heads of token A, rows 8-15 those of token B
+// (qa[st][0..3] = a0..a3 of k step st).  Keys at positions past a row's own
+// position (page tokens tok0 + n > pos) are masked.  Per lane: the states of
+// row g (token A) and row 8 + g (token B); o[nb][0..1] row g, o[nb][2..3]
+// row 8 + g.  Warp-wide.
+__device__ __forceinline__ void attn_page_pair(const __half* Ks, const __half* Vs, int tok0, int posA, int posB,
+                                               const uint32_t (&qa)[8][4], float scale_log2, uint32_t k_off,
+                                               uint32_t v_off, int t4, float (&m_run)[2], float (&l_run)[2],
+                                               float (&o)[16][4]) {
+  float sc[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  const uint32_t kbase = smem_u32(Ks) + k_off;
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    uint32_t b0, b1, b2, b3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(kbase + st * 32));
+    mma_16816_full(sc[0], qa[st][0], qa[st][1], qa[st][2], qa[st][3], b0, b1);
+    mma_16816_full(sc[1], qa[st][0], qa[st][1], qa[st][2], qa[st][3], b2, b3);
+  }
+  // s[r][j]: row r (0: token A, 1: token B), page token n = 8 (j >> 1) + 2 t4 + (j & 1)
+  float s[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int pos = r ? posB : posA;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = 8 * (j >> 1) + 2 * t4 + (j & 1);
+      const float v = sc[j >> 1][2 * r + (j & 1)] * scale_log2;
+      s[r][j] = (tok0 + n <= pos) ? v : -INFINITY;
+    }
+  }
+  float c[2], p[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float mx = fmaxf(fmaxf(s[r][0], s[r][1]), fmaxf(s[r][2], s[r][3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run[r], mx);
+    // a row with no valid key yet keeps m = -inf: nothing to rescale, no weight
+    const bool none = m_new == -INFINITY;
+    c[r] = none ? 1.f : exp2f(m_run[r] - m_new);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[r][j] = none ? 0.f : exp2f(s[r][j] - m_new);
+    float sum = (p[r][0] + p[r][1]) + (p[r][2] + p[r][3]);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    l_run[r] = l_run[r] * c[r] + sum;
+    m_run[r] = m_new;
+  }
+  const __half2 h0 = __floats2half2_rn(p[0][0], p[0][1]), h1 = __floats2half2_rn(p[1][0], p[1][1]);
+  const __half2 h2 = __floats2half2_rn(p[0][2], p[0][3]), h3 = __floats2half2_rn(p[1][2], p[1][3]);
+  const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&h0), a1 = *reinterpret_cast<const uint32_t*>(&h1);
+  const uint32_t a2 = *reinterpret_cast<const uint32_t*>(&h2), a3 = *reinterpret_cast<const uint32_t*>(&h3);
+  const uint32_t vbase = smem_u32(Vs) + v_off;
+#pragma unroll
+  for (int nb = 0; nb < 16; nb += 2) {
+    uint32_t b0, b1, b2, b3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                 : "r"(vbase + nb * 16));
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      o[nb + e][0] *= c[0];
+      o[nb + e][1] *= c[0];
+      o[nb + e][2] *= c[1];
+      o[nb + e][3] *= c[1];
+    }
+    mma_16816_full(o[nb], a0, a1, a2, a3, b0, b1);
+    mma_16816_full(o[nb + 1], a0, a1, a2, a3, b2, b3);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // FP8 (E4M3) pages: a (page, kv head) slice holds 16 rows of 128 one-byte
 // codes per K and V plus one fp32 scale per row (value = code * scale).  In

@@ -292,6 +292,7 @@ struct TraceScope {
   __device__ TraceScope(unsigned int tg) : t0(trace_now()), tw(0), m{0, 0, 0}, tag(tg) {}
   __device__ void waited() { tw = trace_now(); }
   __device__ void mark(int k) { m[k] = trace_now(); }
+  __device__ void set_mark(int k, unsigned long long v) { m[k] = v; }
   __device__ ~TraceScope() {
     if (threadIdx.x == 0 && g_trace_buf != nullptr) {
       const unsigned int i = atomicAdd(&g_trace_n, 1u);
@@ -306,6 +307,7 @@ struct TraceScope {
 #define W4_TRACE_SCOPE(tag) ::w4::TraceScope w4_trace_scope_(tag)
 #define W4_TRACE_WAITED() w4_trace_scope_.waited()
 #define W4_TRACE_MARK(k) w4_trace_scope_.mark(k)
+#define W4_TRACE_SET_MARK(k, v) w4_trace_scope_.set_mark(k, v)
 #else
 #define W4_TRACE_SCOPE(tag) \
   do {                     \
@@ -315,6 +317,9 @@ struct TraceScope {
   } while (0)
 #define W4_TRACE_MARK(k) \
   do {                   \
+  } while (0)
+#define W4_TRACE_SET_MARK(k, v) \
+  do {                          \
   } while (0)
 #endif
 

@@ -47,8 +47,9 @@ constexpr int TC_M = 128;      // weight rows per tile (MMA M)
 constexpr int TC_N = 32;       // batch columns (MMA N) of the decode-batch shape
 constexpr int TC_K = 64;       // K per stage
 constexpr int TC_ACOLS = 32;   // tensor-memory columns of one A buffer (128 rows x 64 k fp16)
-constexpr int TC_READERS = 256;                  // threads that expand codes and read tensor memory
-constexpr int TC_THREADS_WS = 64 + TC_READERS;   // + producer warp + MMA warp
+constexpr int TC_EXP_WARPS = 4;                  // warps that expand int4 codes into tensor memory
+constexpr int TC_READERS = 256;                  // threads that read the group sums and run the epilogue
+constexpr int TC_THREADS_WS = 64 + 32 * TC_EXP_WARPS + TC_READERS;  // + producer warp + MMA warp
 constexpr int TC_S = 8;        // ring stages
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
@@ -101,11 +102,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
 }
 
 
-// Shared-memory matrix descriptor: no swizzle, K-major, LBO = 128 B between
-// K-adjacent core matrices, SBO = 256 B between 8-row groups.
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: a
+// stage's rows of 64 fp16 are 128 bytes each, 8-row atoms of 1024 bytes apart
+// (SBO); 16-byte chunk c of row r sits at chunk c ^ (r % 8) of the row, so
+// the eight rows of a core matrix fall on different banks.  The 16-k slice kk
+// of the stage starts 32 kk bytes into the atom (the swizzle applies to the
+// absolute address; every stage tile is 1024-byte aligned).
 __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) |
-         (1ull << 46);
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 
 // Instruction descriptor: kind::f16, fp32 accumulate, fp16 A and B, both
@@ -115,10 +120,8 @@ constexpr uint32_t tc_idesc() {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NC >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
 
-// byte offset of (row, 8-wide k group w) of a 64-wide stage in the canonical layout
-__device__ __forceinline__ uint32_t tc_off(int row, int w, int slice_bytes) {
-  return (uint32_t)((w >> 1) * slice_bytes + (row >> 3) * 256 + (w & 1) * 128 + (row & 7) * 16);
-}
+// byte offset of (row, 8-wide k group w) of a 64-wide stage in the swizzled layout
+__device__ __forceinline__ uint32_t tc_off(int row, int w) { return (uint32_t)(row * 128 + ((w ^ (row & 7)) << 4)); }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -184,18 +187,22 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(TC_READERS) : "memory"); }
 
-// Warp roles: warp 0 copies (producer), warp 1 lane 0 issues the MMAs, warps
-// 2..9 (the readers, 256 threads) expand the int4 codes of their weight row
-// and, one stage behind the tensor core, read the group sums from tensor
-// memory and run the epilogue.  Stage s of this CTA's work uses ring slot
-// s % TC_S and A buffer s % 2; its group is s / 2 (work items have an even
-// number of stages).  The roles only meet at mbarriers:
-//   full[slot]   producer's copies of the slot landed          (32 arrivals)
-//   empty[slot]  readers done with the raw A, MMAs with the B  (256 + 1)
-//   afull[b]     readers wrote A buffer b                      (256)
-//   aempty[b]    MMAs that read A buffer b are done            (1, commit)
-//   gfull[b]     MMAs of the group in tensor-memory buffer b   (1, commit)
-//   gempty[b]    readers read tensor-memory buffer b           (256)
+// Warp roles: warp 0 copies (producer), warp 1 lane 0 issues the MMAs,
+// warps 2..5 (the expanders, 128 threads, one weight row each) expand the
+// int4 codes of their row into tensor-memory A buffers, up to NAB stages
+// ahead of the tensor core, and warps 6..13 (the readers, 256 threads: a row
+// and half of the batch columns each) read each group's sums from tensor
+// memory as soon as the tensor core has finished the group and run the
+// epilogue.  Stage s of this CTA's work uses ring slot s % TC_S and A buffer
+// s % NAB; its group is s / 2 (work items have an even number of stages).
+// The roles only meet at mbarriers:
+//   full[slot]   producer's copies of the slot landed           (32 arrivals)
+//   empty[slot]  expanders done with the raw A, MMAs with the B  (128 + 1; dense: 1);
+//                its phase for stage s also tells the expanders that A
+//                buffer s % NAB is free again at stage s + NAB
+//   afull[b]     expanders wrote A buffer b                     (128)
+//   gfull[b]     MMAs of the group in tensor-memory buffer b    (1, commit)
+//   gempty[b]    readers read tensor-memory buffer b            (256)
 template <bool INT4, bool SILU, int NC>
 __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_batch(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU, NC>;
@@ -205,7 +212,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
   constexpr int NAB = SH::NAB;
-  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[NAB], aempty[NAB], gfull[2], gempty[2], drain;
+  static_assert(NAB < TC_S, "an A buffer is reused before its ring slot");
+  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[NAB], gfull[2], gempty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -217,6 +225,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
   const int nwork = ntiles * ks;
   const unsigned long long wl = a.wait_limit_ns;
   W4_TRACE_SCOPE(a.tag);
+#ifdef W4A16_TRACE
+  // trace builds: total time spent waiting by the producer (lane 0), an
+  // expander (warp 2, lane 0) and a reader (the first)
+  __shared__ unsigned long long s_tmark[3];
+  if (tid == 0) s_tmark[0] = s_tmark[1] = s_tmark[2] = 0ull;
+#endif
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
   // columns: [0, 2 NA NC) group accumulators; then (int4) A buffer ab, matrix g
@@ -231,11 +245,10 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
   if (tid == 32) {
     for (int i = 0; i < TC_S; ++i) {
       mbar_init(&full[i], 32);
-      mbar_init(&empty[i], TC_READERS + 1);
+      mbar_init(&empty[i], (INT4 ? 32 * TC_EXP_WARPS : 0) + 1);
     }
     for (int i = 0; i < NAB; ++i) {
-      mbar_init(&afull[i], TC_READERS);
-      mbar_init(&aempty[i], 1);
+      mbar_init(&afull[i], 32 * TC_EXP_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&gfull[i], 1);
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
           const int row_l = (lane >> 3) + 4 * j;
           const int row = tile0 + row_l;
           const bool ok = row < N;
-          cp_async16_zfill(sa + tc_off(row_l, w, TC_M * 32), a.w16 + (size_t)(ok ? row : 0) * K + k0 + 8 * w, ok);
+          cp_async16_zfill(sa + tc_off(row_l, w), a.w16 + (size_t)(ok ? row : 0) * K + k0 + 8 * w, ok);
         }
       }
     };
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
         const int c = lane + 32 * i;
         const int m = c >> 3, w = c & 7;
         const bool ok = m < M;
-        cp_async16_zfill(sb + tc_off(m, w, NC * 32), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
+        cp_async16_zfill(sb + tc_off(m, w), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
       }
     };
     // prologue: the weights of the first stages before the dependency wait
@@ -376,7 +389,13 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
       if (c_next(cur) && cur.work < nwork) item_rows();
     for (uint32_t s = npro; cur.work < nwork; ++s) {
       const int slot = s % TC_S;
+#ifdef W4A16_TRACE
+      const unsigned long long tw0 = tc_now();
+#endif
       if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
+#ifdef W4A16_TRACE
+      if (lane == 0) s_tmark[0] += tc_now() - tw0;
+#endif
       load_a(slot);
       load_b(slot, cur.st);
       cp_async_mbar_arrive(&full[slot]);
@@ -385,28 +404,31 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
     cp_async_wait<0>();
   } else if (warp == 1) {
     // =========================== MMA issuer =================================
+    // The whole warp runs the loop (waits, descriptors: warp-uniform values);
+    // lane 0 issues the MMAs and the commits.
     pdl_wait_then_trigger();
-    if (lane == 0) {
-      Cursor cur;
-      c_init(cur);
-      uint32_t s = 0;
-      for (; cur.work < nwork; ++s) {
-        const int slot = s % TC_S, ab = s % NAB;
-        const uint32_t grp = s >> 1;
-        const bool gfirst = (s & 1) == 0;
-        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl)) break;
-        if (INT4 && !tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl)) break;
-        if (gfirst && grp >= 2 && !tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl)) break;
-        fence_proxy_async_smem();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        unsigned char* sl = ring + slot * SH::SLOT;
-        const uint32_t gbase = tmem + (grp & 1) * (NA * NC);
-        const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
+    Cursor cur;
+    c_init(cur);
+    uint32_t s = 0;
+    for (; cur.work < nwork; ++s) {
+      const int slot = s % TC_S, ab = s % NAB;
+      const uint32_t grp = s >> 1;
+      const bool gfirst = (s & 1) == 0;
+      bool ok = tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl);
+      if (INT4 && ok) ok = tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl);
+      if (gfirst && grp >= 2 && ok) ok = tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      fence_proxy_async_smem();
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      unsigned char* sl = ring + slot * SH::SLOT;
+      const uint32_t gbase = tmem + (grp & 1) * (NA * NC);
+      const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
+      if (lane == 0) {
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
-            const uint64_t bd = bd0 + (uint64_t)((kk * NC * 32) >> 4);  // next 16-k slice of B
+            const uint64_t bd = bd0 + (uint64_t)((kk * 32) >> 4);  // next 16-k slice of B
             const uint32_t accum = (!gfirst || kk > 0) ? 1u : 0u;
             if (INT4) {
               // A (128 x 16 exact codes) from tensor memory: 8 columns per 16 k
@@ -417,7 +439,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
                   "r"(at), "l"(bd), "r"(tc_idesc<NC>()), "r"(accum)
                   : "memory");
             } else {
-              const uint64_t ad = tc_desc(smem_u32(sl + kk * TC_M * 32));
+              const uint64_t ad = tc_desc(smem_u32(sl)) + (uint64_t)((kk * 32) >> 4);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                   "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * NC)),
@@ -426,35 +448,87 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
             }
           }
         }
-        if (INT4) tc_commit(&aempty[ab]);
+        // one commit frees the ring slot (producer) and, through it, the A
+        // buffer (expanders wait on the slot of the stage NAB back)
         tc_commit(&empty[slot]);
         if (!gfirst) tc_commit(&gfull[grp & 1]);
-        c_next(cur);
       }
-      // before tensor memory is freed no MMA may be in flight: one more
-      // commit tracks every MMA this thread issued, and its wait ignores an
-      // abort elsewhere in the CTA (the MMAs finish on their own; the wait
-      // keeps the normal bound)
-      if (s > 0) {
-        tc_commit(&drain);
-        (void)tc_wait(&drain, 0);
+      __syncwarp();
+      c_next(cur);
+    }
+    // before tensor memory is freed no MMA may be in flight: one more
+    // commit tracks every MMA this thread issued, and its wait ignores an
+    // abort elsewhere in the CTA (the MMAs finish on their own; the wait
+    // keeps the normal bound)
+    if (s > 0) {
+      if (lane == 0) tc_commit(&drain);
+      __syncwarp();
+      (void)tc_wait(&drain, 0);
+    }
+  } else if (warp < 2 + TC_EXP_WARPS) {
+    // =========================== expanders ==================================
+    // Each thread expands its weight row's 64 codes per stage (per matrix)
+    // into A buffer s % NAB, up to NAB stages ahead of the tensor core.
+    pdl_wait_then_trigger();
+    if (INT4) {
+      const int row_l = 32 * (warp & 3) + lane;  // tensor-memory lanes of this warp's quadrant
+      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A;
+      Cursor cur;
+      c_init(cur);
+      for (uint32_t s = 0; cur.work < nwork; ++s) {
+        const int slot = s % TC_S, ab = s % NAB;
+        // the A buffer's previous MMAs are done, the slot's copies landed
+        // (the MMA's commit to that stage's ring slot also covers A buffer ab)
+#ifdef W4A16_TRACE
+        const unsigned long long tw0 = tc_now();
+#endif
+        if (s >= NAB && !tcw_wait(&empty[(s - NAB) % TC_S], ((s - NAB) / TC_S) & 1, &s_fail, wl)) break;
+        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl)) break;
+#ifdef W4A16_TRACE
+        if (warp == 2 && lane == 0) s_tmark[1] += tc_now() - tw0;
+#endif
+        const unsigned char* sl = ring + slot * SH::SLOT;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
+          // exact codes of this row's 64 k: 32 columns of fp16 pairs in k order
+          const uint4 r0 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + 16);
+          const uint4 c0 = codes_word(r0.x), c1 = codes_word(r0.y), c2 = codes_word(r0.z), c3 = codes_word(r0.w);
+          const uint4 c4 = codes_word(r1.x), c5 = codes_word(r1.y), c6 = codes_word(r1.z), c7 = codes_word(r1.w);
+          const uint32_t ta = lane_base + (uint32_t)((ab * NA + g) * TC_ACOLS);
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+              "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+              "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w), "r"(c2.x), "r"(c2.y),
+              "r"(c2.z), "r"(c2.w), "r"(c3.x), "r"(c3.y), "r"(c3.z), "r"(c3.w), "r"(c4.x), "r"(c4.y), "r"(c4.z),
+              "r"(c4.w), "r"(c5.x), "r"(c5.y), "r"(c5.z), "r"(c5.w), "r"(c6.x), "r"(c6.y), "r"(c6.z), "r"(c6.w),
+              "r"(c7.x), "r"(c7.y), "r"(c7.z), "r"(c7.w)
+              : "memory");
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(&afull[ab]);
+        mbar_arrive(&empty[slot]);
+        c_next(cur);
       }
     }
   } else {
-    // =========================== readers ====================================
+    // =========================== accumulators ===============================
+    // Group by group (two stages each, in the order the tensor core finishes
+    // them): tcgen05.ld of this row's CPT columns of the group's buffer, times
+    // the group's scale into fp32 registers; at the end of a work item the
+    // epilogue.  They run up to one group behind the tensor core.
     pdl_wait_then_trigger();
-    const int r = tid - 64;                       // 0..255
-    const int half = r >> 7;                      // k chunks 4h..4h+3; batch columns CPT h .. CPT h + CPT - 1
+    const int r = tid - 64 - 32 * TC_EXP_WARPS;   // 0..255
+    const int half = r >> 7;                      // batch columns CPT h .. CPT h + CPT - 1
     const int row_l = 32 * (warp & 3) + lane;     // tensor-memory lanes of this warp's quadrant
     Cursor cur;
     c_init(cur);
     const uint32_t* q[NA];
     const __half* sp[NA];
     bool rok = false;
-    if (INT4 && cur.work < nwork) row_ptrs(cur.work / ks, row_l, q, sp, rok);
-    __half sreg0[NA], sreg1[NA];  // scales of groups with even / odd index
-#pragma unroll
-    for (int g = 0; g < NA; ++g) sreg0[g] = sreg1[g] = __float2half(0.f);
+    __half sreg[NA];  // the scales of the group being read
     float acc[NA][CPT];
 #pragma unroll
     for (int g = 0; g < NA; ++g)
@@ -463,12 +537,18 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
 
     // add tensor-memory group `grp` (this row, CPT columns) times the scales
     auto tm_read = [&](uint32_t grp) {
+#ifdef W4A16_TRACE
+      const unsigned long long tw0 = tc_now();
+#endif
       const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail, wl));
+#ifdef W4A16_TRACE
+      if (r == 0) s_tmark[2] += tc_now() - tw0;
+#endif
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          const float sc = INT4 ? __half2float((grp & 1) ? sreg1[g] : sreg0[g]) : 1.0f;
+          const float sc = INT4 ? __half2float(sreg[g]) : 1.0f;
 #pragma unroll
           for (int c0 = 0; c0 < CPT; c0 += 16) {
             uint32_t v[16];
@@ -559,70 +639,45 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
       }
     };
 
-    for (uint32_t s = 0; cur.work < nwork; ++s) {
-      const int slot = s % TC_S, ab = s % NAB;
-      const uint32_t grp = s >> 1;
-      const bool gfirst = (s & 1) == 0;
-      if (INT4) {
-        // (1) the A buffer's previous MMAs are done, the slot's copies landed
-        if (s >= NAB) (void)tcw_wait(&aempty[ab], ((s - NAB) / NAB) & 1, &s_fail, wl);
-        (void)tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl);
-        // (2) this group's scale (used when the group is read, three stages on)
-        // (loaded straight into the register that holds it until the read,
-        // so the load's latency is not waited for here)
-        if (gfirst && rok) {
-          if (grp & 1) {
+    uint32_t grp = 0;  // groups read so far (all items): buffer grp & 1
+    while (cur.work < nwork) {
+      if (INT4) row_ptrs(cur.work / ks, row_l, q, sp, rok);
+      const int g0 = cur.begin >> 1, ng = (cur.end - cur.begin) >> 1;
+      __half snext[NA];
 #pragma unroll
-            for (int g = 0; g < NA; ++g) sreg1[g] = sp[g][cur.st >> 1];
-          } else {
-#pragma unroll
-            for (int g = 0; g < NA; ++g) sreg0[g] = sp[g][cur.st >> 1];
-          }
-        }
-        // (3) exact codes of this row's 32 k (this half of the stage) into
-        //     tensor-memory A buffer ab: 16 columns of fp16 pairs in k order
-        const unsigned char* sl = ring + slot * SH::SLOT;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      for (int g = 0; g < NA; ++g) snext[g] = (INT4 && rok) ? sp[g][g0] : __float2half(0.f);
+      for (int gi = 0; gi < ng; ++gi, ++grp) {
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + half * 16);
-          const uint4 c0 = codes_word(raw.x), c1 = codes_word(raw.y), c2 = codes_word(raw.z), c3 = codes_word(raw.w);
-          const uint32_t ta =
-              tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A + (uint32_t)((ab * NA + g) * TC_ACOLS + half * 16);
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
-              "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w), "r"(c2.x), "r"(c2.y),
-              "r"(c2.z), "r"(c2.w), "r"(c3.x), "r"(c3.y), "r"(c3.z), "r"(c3.w)
-              : "memory");
+          sreg[g] = snext[g];
+          // the next group's scale is requested now; used one group later
+          if (INT4 && rok && gi + 1 < ng) snext[g] = sp[g][g0 + gi + 1];
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        mbar_arrive(&afull[ab]);
-        mbar_arrive(&empty[slot]);
-      } else {
-        mbar_arrive(&empty[slot]);  // dense weights: nothing to expand; the MMA reads the slot
-      }
-      // (4) the previous group of this item, one group behind the tensor core
-      if (!gfirst && cur.st - 1 != cur.begin) tm_read(grp - 1);
-      // (5) end of the work item: its last group, the epilogue, the abort check
-      if (!gfirst && cur.st == cur.end - 1) {
         tm_read(grp);
-        epilogue(cur.work);
+      }
+      epilogue(cur.work);
 #pragma unroll
-        for (int g = 0; g < NA; ++g)
+      for (int g = 0; g < NA; ++g)
 #pragma unroll
-          for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
-        if (r == 0) s_rfail = s_fail;
-        readers_sync();
-        if (s_rfail) break;
-        c_next(cur);
-        if (INT4 && cur.work < nwork) row_ptrs(cur.work / ks, row_l, q, sp, rok);
-      } else {
-        c_next(cur);
+        for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
+      if (r == 0) s_rfail = s_fail;
+      readers_sync();
+      if (s_rfail) break;
+      cur.work += gridDim.x;
+      if (cur.work < nwork) {
+        cur.begin = cur.st = (cur.work % ks) * ps;
+        cur.end = min(nst, cur.begin + ps);
       }
     }
   }
   __syncthreads();
+#ifdef W4A16_TRACE
+  if (tid == 0) {
+    W4_TRACE_SET_MARK(0, s_tmark[0]);
+    W4_TRACE_SET_MARK(1, s_tmark[1]);
+    W4_TRACE_SET_MARK(2, s_tmark[2]);
+  }
+#endif
   if (s_fail && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();

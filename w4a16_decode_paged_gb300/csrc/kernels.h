@@ -97,6 +97,9 @@ struct AttnArgs {
   float* vs;
 };
 int launch_paged_attention(const AttnArgs& a, cudaStream_t s);
+// Causal prompt attention: rows 0..B-1 of q are tokens of one sequence at
+// positions context_lens[i] - 1, its pages in row 0 of block_table; out [B][Hq][D].
+int launch_prefill_attention(const AttnArgs& a, cudaStream_t s);
 constexpr int ATT_MAX_PARTITIONS = 1024;
 size_t attention_workspace_bytes(int B, int Hq, int Hkv, int P);
 void attention_workspace_layout(AttnArgs& a, void* ws, int B, int Hq, int P);  // sets ws_o, ws_ml, counters

@@ -424,10 +424,10 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
 // Prefill: the T prompt tokens of one sequence in one pass (the "TTFT (512
 // tokens)" row of the aikraft.ru article's "Ключевые метрики
 // производительности").  Each projection is a tensor-core GEMM over the T
-// rows (row chunks of 32); RoPE + append write all T positions into the
-// sequence's pages; the attention runs the T tokens as T rows of lengths
-// len0 + 1 .. len0 + T over copies of the block-table row, which is causal
-// attention over the prompt (and any tokens cached before it).
+// rows (row blocks of up to 128); RoPE + append write all T positions into
+// the sequence's pages; the attention gives row i the keys at positions
+// 0 .. len0 + i (causal attention over the prompt and any tokens cached
+// before it), 16 rows per CTA sharing every page they read.
 // ---------------------------------------------------------------------------
 struct PrefillWs {
   __half *x, *xn, *qkv, *att, *h, *mlp;
@@ -586,10 +586,8 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
     a.B = T;
     a.Hq = Hq;
     a.Hkv = Hkv;
-    a.P = 1;  // one partition per row: no split-K workspace
-    a.part_tokens = (m->max_context + 15) / 16 * 16;
     a.scale_log2 = (1.0f / sqrtf((float)D)) * 1.4426950408889634f;
-    if ((rc = launch_paged_attention(a, s))) return rc;
+    if ((rc = launch_prefill_attention(a, s))) return rc;
     const GemvSeg o[1] = {{L.wo, hp(L.so), nullptr, H}};
     if ((rc = gemm_rows(m, w, w.att, T, Hq * D, o, 1, H, w.x, w.h, false, s))) return rc;
     if ((rc = launch_rmsnorm(w.h, hp(L.ln2), w.xn, T, H, c.eps, s))) return rc;
