@@ -34,9 +34,12 @@
 // workspace and the last split of a tile (atomic ticket) sums them and runs
 // the epilogue.  Dense fp16 weights (the batched lm_head) are copied into the
 // ring in the canonical layout and used by the MMA as they are.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -174,6 +177,16 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// One 2-D bulk-tensor (TMA) copy of the box at (c0 innermost, c1) of `map`
+// into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The mbarrier gets one arrival once all of this thread's earlier cp.async
 // copies have landed (the arrival is counted in the barrier's init count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
   }
   if (tid == 32) {
     for (int i = 0; i < TC_S; ++i) {
-      mbar_init(&full[i], 32);
+      mbar_init(&full[i], a.tma ? 1 : 32);
       mbar_init(&empty[i], (INT4 ? 32 * TC_EXP_WARPS : 0) + 1);
     }
     for (int i = 0; i < NAB; ++i) {
@@ -360,6 +373,75 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
         cp_async16_zfill(sb + tc_off(m, w), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
       }
     };
+    // TMA: lane 0 copies a stage's weight tiles and activation tile with one
+    // bulk-tensor copy each; the slot's barrier expects their bytes
+    constexpr uint32_t B_TX = SH::B_BYTES;
+    constexpr uint32_t A_TX = INT4 ? (uint32_t)(TC_M * 32) : (uint32_t)TC_A_BYTES;  // per matrix
+    int tm_map[NA], tm_row = 0;  // the item's weight map per matrix and its first row in it
+    auto item_tma = [&]() {
+      const int r0 = (cur.work / ks) * TC_M;
+      tm_row = r0;
+      if (SILU || !INT4) {
+#pragma unroll
+        for (int g = 0; g < NA; ++g) tm_map[g] = g;
+      } else {
+        int si = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (si < a.nseg - 1 && tm_row >= a.seg[si].rows) { tm_row -= a.seg[si].rows; ++si; }
+        tm_map[0] = si;
+      }
+    };
+    auto tma_a = [&](int slot, int st) {
+      unsigned char* sa = ring + slot * SH::SLOT;
+#pragma unroll
+      for (int g = 0; g < NA; ++g)
+        tma_load_2d(sa + g * (int)A_TX, &a.tm_w[tm_map[g]], INT4 ? st * (TC_K / 8) : st * TC_K, tm_row, &full[slot]);
+    };
+    auto tma_b = [&](int slot, int st) {
+      tma_load_2d(ring + slot * SH::SLOT + SH::A_RAW, &a.tm_x, st * TC_K, 0, &full[slot]);
+    };
+    if (a.tma) {
+      if (cur.work < nwork) item_tma();
+      int pro_st[TC_S];
+      int npro = 0;
+      {
+        Cursor c2 = cur;
+        for (int i = 0; i < TC_S && c2.work < nwork; ++i) {
+          if (i > 0 && c2.st == c2.begin) break;  // a new item inside the prologue: stop
+          pro_st[i] = c2.st;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[i], NA * A_TX + B_TX);
+            tma_a(i, c2.st);
+          }
+          ++npro;
+          c_next(c2);
+        }
+      }
+      pdl_wait_then_trigger();
+      W4_TRACE_WAITED();
+      if (lane == 0)
+        for (int i = 0; i < npro; ++i) tma_b(i, pro_st[i]);
+      for (int i = 0; i < npro; ++i)
+        if (c_next(cur) && cur.work < nwork) item_tma();
+      for (uint32_t s = npro; cur.work < nwork; ++s) {
+        const int slot = s % TC_S;
+#ifdef W4A16_TRACE
+        const unsigned long long tw0 = tc_now();
+#endif
+        if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
+#ifdef W4A16_TRACE
+        if (lane == 0) s_tmark[0] += tc_now() - tw0;
+#endif
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], NA * A_TX + B_TX);
+          tma_a(slot, cur.st);
+          tma_b(slot, cur.st);
+        }
+        __syncwarp();
+        if (c_next(cur) && cur.work < nwork) item_tma();
+      }
+    } else {
     // prologue: the weights of the first stages before the dependency wait
     int pro_st[TC_S];
     int npro = 0;
@@ -402,6 +484,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
       if (c_next(cur) && cur.work < nwork) item_rows();
     }
     cp_async_wait<0>();
+    }
   } else if (warp == 1) {
     // =========================== MMA issuer =================================
     // The whole warp runs the loop (waits, descriptors: warp-uniform values);
@@ -762,12 +845,61 @@ void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, 
 static std::atomic<unsigned long long> g_wait_limit_ns{TC_TIMEOUT_NS};
 unsigned long long tc_wait_limit_ns() { return g_wait_limit_ns.load(); }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null if the driver does not provide it.
+static PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over rows of `inner` elements, `row_bytes` apart; boxes of
+// box_inner x box_rows (rows past the end read as zeros)
+static bool tma_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto enc = tma_encoder();
+  if (enc == nullptr || base == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps for the launch (a.tma = 1), or a.tma = 0 when some operand
+// does not fit them (a 128-row weight tile across two segments).
+static void tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
+  a.tma = 0;
+  bool ok = tma_map_2d(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
+                       (uint64_t)a.K * 2, TC_K, (uint32_t)nc, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (int4) {
+    const int nm = silu ? 2 : a.nseg;
+    for (int i = 0; i + 1 < nm && !silu; ++i) ok = ok && a.seg[i].rows % TC_M == 0;
+    for (int i = 0; i < nm && ok; ++i)
+      ok = tma_map_2d(&a.tm_w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.seg[i].qw, (uint64_t)a.K / 8,
+                      (uint64_t)a.seg[i].rows, (uint64_t)a.K / 2, TC_K / 8, TC_M, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    ok = ok && tma_map_2d(&a.tm_w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.w16, (uint64_t)a.K, (uint64_t)a.N,
+                          (uint64_t)a.K * 2, TC_K, TC_M, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  a.tma = ok ? 1 : 0;
+}
+
 int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   TcArgs a = a_in;
   a.wait_limit_ns = TC_TIMEOUT_NS;
   const int maxm = tc_max_rows(int4, silu);
   if (a.M < 1 || a.M > maxm) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, maxm);
   const int nc = tc_cols(a.M, int4, silu);
+  tc_tensor_maps(a, int4, silu, nc);
   // stages pair into 128-wide groups (the int4 scale group), dense weights too
   if (a.K % 128 != 0) return set_error(W4A16_ERR_SHAPE, "gemm_tc: K=%d not a multiple of 128", a.K);
   if (a.ksplit < 1) return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: ksplit < 1");

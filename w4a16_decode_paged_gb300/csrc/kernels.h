@@ -2,6 +2,7 @@
 // model runtime (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's driver entry point)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -47,6 +48,13 @@ struct TcArgs {
   int M, K, N, ldy, ksplit, tag;
   int per_split;           // stages (64 k) per split, even; 0: ceil(stages / ksplit)
   unsigned long long wait_limit_ns;  // bound of every mbarrier wait (set by the launcher)
+  // Bulk-tensor (TMA) copies, set by the launcher: tm_w[i] the weights of
+  // segment i (int4: u32 [rows][K/8], 8 x 128 boxes; dense fp16: [N][K],
+  // 64 x 128 boxes, 128-byte swizzle), tm_x the activations [M][K] (64 x NC
+  // boxes, 128-byte swizzle).  tma = 0: per-lane 16-byte copies instead.
+  int tma;
+  CUtensorMap tm_w[3];
+  CUtensorMap tm_x;
 };
 // Bound of the persistent decode kernel's grid-barrier waits, read at each
 // launch (w4a16_debug_set_wait_limit_ns changes it; 0 = give up at the first
