@@ -75,9 +75,8 @@ struct TcShape {
   static constexpr size_t SMEM = (size_t)TC_S * SLOT + 1024;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
-  // the MMAs.  As many as fit (2 to 4) beside the 2 group accumulators without
-  // costing a CTA per SM: 256 columns for the two-CTA decode shape, else 512.
-  static constexpr int TM_BUDGET = NC == 32 ? 256 : 512;
+  // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators.
+  static constexpr int TM_BUDGET = 512;
   static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
   static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
   // tensor memory: 2 group accumulators x NA x NC columns, and (int4) NAB A
@@ -177,6 +176,22 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+#ifdef W4A16_TRACE
+// Trace builds: per-stage event times of CTA 0 of the last launch
+// (w4a16_trace_tc_timeline): 0 producer issued, 1 expander starts, 2 expander
+// released, 3 MMA operands ready, 4 MMA issued, 5 reader saw the group done.
+constexpr int TC_TL_EVENTS = 6, TC_TL_STAGES = 512;
+__device__ unsigned long long g_tc_timeline[TC_TL_EVENTS][TC_TL_STAGES];
+#define TC_TL(ev, s)                                                        \
+  do {                                                                       \
+    if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = tc_now(); \
+  } while (0)
+#else
+#define TC_TL(ev, s) \
+  do {               \
+  } while (0)
+#endif
+
 // One 2-D bulk-tensor (TMA) copy of the box at (c0 innermost, c1) of `map`
 // into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
@@ -217,7 +232,8 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //   gfull[b]     MMAs of the group in tensor-memory buffer b    (1, commit)
 //   gempty[b]    readers read tensor-memory buffer b            (256)
 template <bool INT4, bool SILU, int NC>
-__global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_batch(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_COLS <= 256 ? 2 : 1)
+    w4pg_tc_batch(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU, NC>;
   constexpr int NA = SH::NA;
   constexpr int CPT = SH::CPT;
@@ -239,8 +255,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
   const unsigned long long wl = a.wait_limit_ns;
   W4_TRACE_SCOPE(a.tag);
 #ifdef W4A16_TRACE
-  // trace builds: total time spent waiting by the producer (lane 0), an
-  // expander (warp 2, lane 0) and a reader (the first)
+  // trace builds: total time the producer spends issuing its bulk-tensor
+  // copies, and the time an expander (warp 2, lane 0) and a reader (the
+  // first) spend waiting
   __shared__ unsigned long long s_tmark[3];
   if (tid == 0) s_tmark[0] = s_tmark[1] = s_tmark[2] = 0ull;
 #endif
@@ -426,17 +443,18 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
         if (c_next(cur) && cur.work < nwork) item_tma();
       for (uint32_t s = npro; cur.work < nwork; ++s) {
         const int slot = s % TC_S;
-#ifdef W4A16_TRACE
-        const unsigned long long tw0 = tc_now();
-#endif
         if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
-#ifdef W4A16_TRACE
-        if (lane == 0) s_tmark[0] += tc_now() - tw0;
-#endif
         if (lane == 0) {
+#ifdef W4A16_TRACE
+          const unsigned long long tw0 = tc_now();
+#endif
           mbar_arrive_expect_tx(&full[slot], NA * A_TX + B_TX);
           tma_a(slot, cur.st);
           tma_b(slot, cur.st);
+#ifdef W4A16_TRACE
+          s_tmark[0] += tc_now() - tw0;
+#endif
+          TC_TL(0, s);
         }
         __syncwarp();
         if (c_next(cur) && cur.work < nwork) item_tma();
@@ -501,6 +519,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
       if (INT4 && ok) ok = tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl);
       if (gfirst && grp >= 2 && ok) ok = tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane == 0) TC_TL(3, s);
       fence_proxy_async_smem();
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       unsigned char* sl = ring + slot * SH::SLOT;
@@ -535,6 +554,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
         // buffer (expanders wait on the slot of the stage NAB back)
         tc_commit(&empty[slot]);
         if (!gfirst) tc_commit(&gfull[grp & 1]);
+        TC_TL(4, s);
       }
       __syncwarp();
       c_next(cur);
@@ -556,9 +576,20 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
     if (INT4) {
       const int row_l = 32 * (warp & 3) + lane;  // tensor-memory lanes of this warp's quadrant
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A;
+      // The tensor-memory stores of a stage complete while the next stage is
+      // expanded: its buffer and ring slot are released one iteration later.
+      auto release = [&](uint32_t ps) {
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(&afull[ps % NAB]);
+        mbar_arrive(&empty[ps % TC_S]);
+        if (warp == 2 && lane == 0) TC_TL(2, ps);
+      };
       Cursor cur;
       c_init(cur);
-      for (uint32_t s = 0; cur.work < nwork; ++s) {
+      bool pend = false;
+      uint32_t s = 0;
+      for (; cur.work < nwork; ++s) {
         const int slot = s % TC_S, ab = s % NAB;
         // the A buffer's previous MMAs are done, the slot's copies landed
         // (the MMA's commit to that stage's ring slot also covers A buffer ab)
@@ -570,31 +601,43 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
 #ifdef W4A16_TRACE
         if (warp == 2 && lane == 0) s_tmark[1] += tc_now() - tw0;
 #endif
+        if (warp == 2 && lane == 0) TC_TL(1, s);
         const unsigned char* sl = ring + slot * SH::SLOT;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // exact codes of this row's 64 k per matrix: 32 columns of fp16 pairs in k order
+        uint4 c[NA][8];
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          // exact codes of this row's 64 k: 32 columns of fp16 pairs in k order
           const uint4 r0 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32);
           const uint4 r1 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + 16);
-          const uint4 c0 = codes_word(r0.x), c1 = codes_word(r0.y), c2 = codes_word(r0.z), c3 = codes_word(r0.w);
-          const uint4 c4 = codes_word(r1.x), c5 = codes_word(r1.y), c6 = codes_word(r1.z), c7 = codes_word(r1.w);
+          c[g][0] = codes_word(r0.x);
+          c[g][1] = codes_word(r0.y);
+          c[g][2] = codes_word(r0.z);
+          c[g][3] = codes_word(r0.w);
+          c[g][4] = codes_word(r1.x);
+          c[g][5] = codes_word(r1.y);
+          c[g][6] = codes_word(r1.z);
+          c[g][7] = codes_word(r1.w);
+        }
+        if (pend) release(s - 1);
+#pragma unroll
+        for (int g = 0; g < NA; ++g) {
           const uint32_t ta = lane_base + (uint32_t)((ab * NA + g) * TC_ACOLS);
           asm volatile(
               "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
               "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
-              "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w), "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w), "r"(c2.x), "r"(c2.y),
-              "r"(c2.z), "r"(c2.w), "r"(c3.x), "r"(c3.y), "r"(c3.z), "r"(c3.w), "r"(c4.x), "r"(c4.y), "r"(c4.z),
-              "r"(c4.w), "r"(c5.x), "r"(c5.y), "r"(c5.z), "r"(c5.w), "r"(c6.x), "r"(c6.y), "r"(c6.z), "r"(c6.w),
-              "r"(c7.x), "r"(c7.y), "r"(c7.z), "r"(c7.w)
+              "r"(c[g][0].x), "r"(c[g][0].y), "r"(c[g][0].z), "r"(c[g][0].w), "r"(c[g][1].x), "r"(c[g][1].y),
+              "r"(c[g][1].z), "r"(c[g][1].w), "r"(c[g][2].x), "r"(c[g][2].y), "r"(c[g][2].z), "r"(c[g][2].w),
+              "r"(c[g][3].x), "r"(c[g][3].y), "r"(c[g][3].z), "r"(c[g][3].w), "r"(c[g][4].x), "r"(c[g][4].y),
+              "r"(c[g][4].z), "r"(c[g][4].w), "r"(c[g][5].x), "r"(c[g][5].y), "r"(c[g][5].z), "r"(c[g][5].w),
+              "r"(c[g][6].x), "r"(c[g][6].y), "r"(c[g][6].z), "r"(c[g][6].w), "r"(c[g][7].x), "r"(c[g][7].y),
+              "r"(c[g][7].z), "r"(c[g][7].w)
               : "memory");
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        mbar_arrive(&afull[ab]);
-        mbar_arrive(&empty[slot]);
+        pend = true;
         c_next(cur);
       }
+      if (pend && cur.work >= nwork) release(s - 1);
     }
   } else {
     // =========================== accumulators ===============================
@@ -627,6 +670,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
 #ifdef W4A16_TRACE
       if (r == 0) s_tmark[2] += tc_now() - tw0;
 #endif
+      if (r == 0) TC_TL(5, grp);
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
@@ -726,15 +770,19 @@ __global__ void __launch_bounds__(TC_THREADS_WS, NC == TC_N ? 2 : 1) w4pg_tc_bat
     while (cur.work < nwork) {
       if (INT4) row_ptrs(cur.work / ks, row_l, q, sp, rok);
       const int g0 = cur.begin >> 1, ng = (cur.end - cur.begin) >> 1;
-      __half snext[NA];
+      // scales of the next two groups in flight (requested two groups ahead)
+      __half snext[NA], snext2[NA];
 #pragma unroll
-      for (int g = 0; g < NA; ++g) snext[g] = (INT4 && rok) ? sp[g][g0] : __float2half(0.f);
+      for (int g = 0; g < NA; ++g) {
+        snext[g] = (INT4 && rok) ? sp[g][g0] : __float2half(0.f);
+        snext2[g] = (INT4 && rok && ng > 1) ? sp[g][g0 + 1] : __float2half(0.f);
+      }
       for (int gi = 0; gi < ng; ++gi, ++grp) {
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
           sreg[g] = snext[g];
-          // the next group's scale is requested now; used one group later
-          if (INT4 && rok && gi + 1 < ng) snext[g] = sp[g][g0 + gi + 1];
+          snext[g] = snext2[g];
+          if (INT4 && rok && gi + 2 < ng) snext2[g] = sp[g][g0 + gi + 2];
         }
         tm_read(grp);
       }
@@ -892,6 +940,14 @@ static void tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
   }
   a.tma = ok ? 1 : 0;
 }
+
+#ifdef W4A16_TRACE
+// trace builds: copy CTA 0's per-stage event times of the last GEMM launch
+extern "C" W4A16_API int w4a16_trace_tc_timeline(unsigned long long* host_out, int n) {
+  const size_t bytes = std::min((size_t)n, (size_t)TC_TL_EVENTS * TC_TL_STAGES) * sizeof(unsigned long long);
+  return cudaMemcpyFromSymbol(host_out, g_tc_timeline, bytes) == cudaSuccess ? 0 : 4;
+}
+#endif
 
 int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   TcArgs a = a_in;
