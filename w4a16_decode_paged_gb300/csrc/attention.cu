@@ -63,7 +63,7 @@ template <int G, bool FUSE, int NW, bool WP, bool KV8>
 __global__ void __launch_bounds__(NW * 32) w4pg_paged_attn(const __grid_constant__ AttnArgs a) {
   constexpr int ST = att_stages(WP);      // page slots per warp
   constexpr int SLOT = (int)att_slot_bytes(KV8);
-  extern __shared__ __align__(128) unsigned char smraw[];
+  extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ __align__(16) float s_q[G][ATT_D];   // this group's q (rotated in the fused variant)
   __shared__ __align__(16) __half s_knew[ATT_D];  // fused: rotated new k and new v (read as uint2)
   __shared__ __align__(16) __half s_vnew[ATT_D];
@@ -594,7 +594,7 @@ constexpr int PF_STAGES = 3;   // page slots of the CTA's ring
 
 template <int G>
 __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_constant__ AttnArgs a) {
-  extern __shared__ __align__(128) unsigned char smraw[];
+  extern __shared__ __align__(16) unsigned char smraw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y;
   const int row0 = blockIdx.x * PF_ROWS;

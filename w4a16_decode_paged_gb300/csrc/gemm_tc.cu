@@ -11,7 +11,7 @@
 //
 // The weights are streamed once, so the kernel is a bandwidth pipe with
 // specialised warps that meet only at mbarriers: a producer warp fills a
-// ring of TC_S stages (64 k each) with cp.async (packed int4 rows, and the
+// ring of stages (64 k each) with cp.async (packed int4 rows, and the
 // activation tile directly in the canonical no-swizzle K-major layout the MMA
 // reads: core matrices of 8 rows x 16 bytes, K-adjacent core matrices 128 B
 // apart, 8-row groups 256 B apart); 256 reader threads turn the 32 codes per
@@ -53,7 +53,6 @@ constexpr int TC_ACOLS = 32;   // tensor-memory columns of one A buffer (128 row
 constexpr int TC_EXP_WARPS = 4;                  // warps that expand int4 codes into tensor memory
 constexpr int TC_READERS = 256;                  // threads that read the group sums and run the epilogue
 constexpr int TC_THREADS_WS = 64 + 32 * TC_EXP_WARPS + TC_READERS;  // + producer warp + MMA warp
-constexpr int TC_S = 8;        // ring stages
 constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
 
@@ -72,7 +71,6 @@ struct TcShape {
   static constexpr uint32_t A_RAW = INT4 ? NA * TC_M * 32 : TC_A_BYTES;     // A bytes per ring slot
   static constexpr uint32_t B_BYTES = NC * TC_K * 2;                        // activation tile per stage
   static constexpr uint32_t SLOT = A_RAW + B_BYTES;
-  static constexpr size_t SMEM = (size_t)TC_S * SLOT + 1024;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
   // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators.
@@ -83,6 +81,11 @@ struct TcShape {
   // buffers x NA x 32 columns of exact codes, rounded up to a power of two
   static constexpr uint32_t TMEM_COLS =
       pow2_at_least(INT4 ? 2 * NA * NC + NAB * NA * TC_ACOLS : 2 * NA * NC);
+  // ring stages: as many as the shared memory holds (4 to 24), the weights of
+  // that many stages in flight per CTA hide the memory latency
+  static constexpr int SMEM_BUDGET = TMEM_COLS <= 256 ? 110 * 1024 : 200 * 1024;
+  static constexpr int S = (int)(SMEM_BUDGET / SLOT) < 4 ? 4 : ((int)(SMEM_BUDGET / SLOT) > 24 ? 24 : (int)(SMEM_BUDGET / SLOT));
+  static constexpr size_t SMEM = (size_t)S * SLOT + 1024;
   static_assert(NC % 32 == 0 && NC <= 128, "NC: 32, 64 or 128 columns");
   static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
@@ -221,7 +224,7 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 // ahead of the tensor core, and warps 6..13 (the readers, 256 threads: a row
 // and half of the batch columns each) read each group's sums from tensor
 // memory as soon as the tensor core has finished the group and run the
-// epilogue.  Stage s of this CTA's work uses ring slot s % TC_S and A buffer
+// epilogue.  Stage s of this CTA's work uses ring slot s % TS and A buffer
 // s % NAB; its group is s / 2 (work items have an even number of stages).
 // The roles only meet at mbarriers:
 //   full[slot]   producer's copies of the slot landed           (32 arrivals)
@@ -237,12 +240,18 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   using SH = TcShape<INT4, SILU, NC>;
   constexpr int NA = SH::NA;
   constexpr int CPT = SH::CPT;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* ring = smem;                    // [TC_S][A raw | B tile]
+  // The array is declared with the alignment every build guarantees (16
+  // bytes): the 1024-byte alignment of the ring (needed by the 128-byte
+  // swizzle) is made at run time, as an offset into the array so that the
+  // compiler keeps shared-memory loads for it.  (Declaring 1024 here lets
+  // the compiler take the offset to be 0, which relocatable builds do not
+  // honour.)
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // [TS][A raw | B tile]
   constexpr int NAB = SH::NAB;
-  static_assert(NAB < TC_S, "an A buffer is reused before its ring slot");
-  __shared__ __align__(8) uint64_t full[TC_S], empty[TC_S], afull[NAB], gfull[2], gempty[2], drain;
+  constexpr int TS = SH::S;  // ring stages
+  static_assert(NAB < TS, "an A buffer is reused before its ring slot");
+  __shared__ __align__(8) uint64_t full[TS], empty[TS], afull[NAB], gfull[2], gempty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -273,7 +282,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 32) {
-    for (int i = 0; i < TC_S; ++i) {
+    for (int i = 0; i < TS; ++i) {
       mbar_init(&full[i], a.tma ? 1 : 32);
       mbar_init(&empty[i], (INT4 ? 32 * TC_EXP_WARPS : 0) + 1);
     }
@@ -420,11 +429,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     };
     if (a.tma) {
       if (cur.work < nwork) item_tma();
-      int pro_st[TC_S];
+      int pro_st[TS];
       int npro = 0;
       {
         Cursor c2 = cur;
-        for (int i = 0; i < TC_S && c2.work < nwork; ++i) {
+        for (int i = 0; i < TS && c2.work < nwork; ++i) {
           if (i > 0 && c2.st == c2.begin) break;  // a new item inside the prologue: stop
           pro_st[i] = c2.st;
           if (lane == 0) {
@@ -442,8 +451,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       for (int i = 0; i < npro; ++i)
         if (c_next(cur) && cur.work < nwork) item_tma();
       for (uint32_t s = npro; cur.work < nwork; ++s) {
-        const int slot = s % TC_S;
-        if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
+        const int slot = s % TS;
+        if (s >= TS && !tcw_wait(&empty[slot], ((s / TS) - 1) & 1, &s_fail, wl)) break;
         if (lane == 0) {
 #ifdef W4A16_TRACE
           const unsigned long long tw0 = tc_now();
@@ -461,11 +470,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       }
     } else {
     // prologue: the weights of the first stages before the dependency wait
-    int pro_st[TC_S];
+    int pro_st[TS];
     int npro = 0;
     {
       Cursor c2 = cur;
-      for (int i = 0; i < TC_S && c2.work < nwork; ++i) {
+      for (int i = 0; i < TS && c2.work < nwork; ++i) {
         if (i > 0 && c2.st == c2.begin) {  // a new item inside the prologue: stop (its rows differ)
           break;
         }
@@ -488,11 +497,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     for (int i = 0; i < npro; ++i)
       if (c_next(cur) && cur.work < nwork) item_rows();
     for (uint32_t s = npro; cur.work < nwork; ++s) {
-      const int slot = s % TC_S;
+      const int slot = s % TS;
 #ifdef W4A16_TRACE
       const unsigned long long tw0 = tc_now();
 #endif
-      if (s >= TC_S && !tcw_wait(&empty[slot], ((s / TC_S) - 1) & 1, &s_fail, wl)) break;
+      if (s >= TS && !tcw_wait(&empty[slot], ((s / TS) - 1) & 1, &s_fail, wl)) break;
 #ifdef W4A16_TRACE
       if (lane == 0) s_tmark[0] += tc_now() - tw0;
 #endif
@@ -512,10 +521,10 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     c_init(cur);
     uint32_t s = 0;
     for (; cur.work < nwork; ++s) {
-      const int slot = s % TC_S, ab = s % NAB;
+      const int slot = s % TS, ab = s % NAB;
       const uint32_t grp = s >> 1;
       const bool gfirst = (s & 1) == 0;
-      bool ok = tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl);
+      bool ok = tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl);
       if (INT4 && ok) ok = tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl);
       if (gfirst && grp >= 2 && ok) ok = tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -582,7 +591,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         mbar_arrive(&afull[ps % NAB]);
-        mbar_arrive(&empty[ps % TC_S]);
+        mbar_arrive(&empty[ps % TS]);
         if (warp == 2 && lane == 0) TC_TL(2, ps);
       };
       Cursor cur;
@@ -590,14 +599,14 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       bool pend = false;
       uint32_t s = 0;
       for (; cur.work < nwork; ++s) {
-        const int slot = s % TC_S, ab = s % NAB;
+        const int slot = s % TS, ab = s % NAB;
         // the A buffer's previous MMAs are done, the slot's copies landed
         // (the MMA's commit to that stage's ring slot also covers A buffer ab)
 #ifdef W4A16_TRACE
         const unsigned long long tw0 = tc_now();
 #endif
-        if (s >= NAB && !tcw_wait(&empty[(s - NAB) % TC_S], ((s - NAB) / TC_S) & 1, &s_fail, wl)) break;
-        if (!tcw_wait(&full[slot], (s / TC_S) & 1, &s_fail, wl)) break;
+        if (s >= NAB && !tcw_wait(&empty[(s - NAB) % TS], ((s - NAB) / TS) & 1, &s_fail, wl)) break;
+        if (!tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl)) break;
 #ifdef W4A16_TRACE
         if (warp == 2 && lane == 0) s_tmark[1] += tc_now() - tw0;
 #endif

@@ -905,7 +905,7 @@ __device__ __forceinline__ void pk_trace(unsigned tag, unsigned long long t0, un
 // ---------------------------------------------------------------------------
 template <int G>
 __global__ void __launch_bounds__(PK_THREADS, 1) w4pg_decode_persistent(const __grid_constant__ PkArgs a) {
-  extern __shared__ __align__(1024) unsigned char pk_smem[];
+  extern __shared__ __align__(16) unsigned char pk_smem[];
   uint4* ring = reinterpret_cast<uint4*>(pk_smem);
   uint32_t* sfifo = reinterpret_cast<uint32_t*>(pk_smem + PK_RING_BYTES);
   unsigned char* area = pk_smem + PK_RING_BYTES + PK_SFIFO_BYTES;  // staging / attention pages / merges
