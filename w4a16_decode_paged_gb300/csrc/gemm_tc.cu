@@ -73,7 +73,8 @@ struct TcShape {
   static constexpr uint32_t SLOT = A_RAW + B_BYTES;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
-  // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators.
+  // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators (8
+  // measured no faster than 4).
   static constexpr int TM_BUDGET = 512;
   static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
   static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
@@ -182,16 +183,25 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
 #ifdef W4A16_TRACE
 // Trace builds: per-stage event times of CTA 0 of the last launch
 // (w4a16_trace_tc_timeline): 0 producer issued, 1 expander starts, 2 expander
-// released, 3 MMA operands ready, 4 MMA issued, 5 reader saw the group done.
-constexpr int TC_TL_EVENTS = 6, TC_TL_STAGES = 512;
+// released, 3 MMA operands ready, 4 MMA issued, 5 reader saw the group done
+// (global timer, ns); 6..9 the MMA warp in SM clock cycles: operands ready,
+// fence done, MMAs issued, commits issued.
+constexpr int TC_TL_EVENTS = 10, TC_TL_STAGES = 512;
 __device__ unsigned long long g_tc_timeline[TC_TL_EVENTS][TC_TL_STAGES];
 #define TC_TL(ev, s)                                                        \
   do {                                                                       \
     if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = tc_now(); \
   } while (0)
+#define TC_TLC(ev, s)                                                              \
+  do {                                                                             \
+    if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = clock64();   \
+  } while (0)
 #else
 #define TC_TL(ev, s) \
   do {               \
+  } while (0)
+#define TC_TLC(ev, s) \
+  do {                \
   } while (0)
 #endif
 
@@ -524,13 +534,18 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       const int slot = s % TS, ab = s % NAB;
       const uint32_t grp = s >> 1;
       const bool gfirst = (s & 1) == 0;
-      bool ok = tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl);
-      if (INT4 && ok) ok = tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl);
+      // int4: the expanders saw the slot's copies land before they filled A
+      // buffer ab, so its barrier (acquired here) covers the B tile too
+      bool ok = INT4 ? tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl) : tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl);
       if (gfirst && grp >= 2 && ok) ok = tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl);
+      if (lane == 0) TC_TLC(6, s);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (lane == 0) TC_TL(3, s);
-      fence_proxy_async_smem();
+      // per-lane copies write the ring through the generic proxy, which the
+      // MMA reads through the async proxy; bulk-tensor copies need no fence
+      if (!a.tma) fence_proxy_async_smem();
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (lane == 0) TC_TLC(7, s);
       unsigned char* sl = ring + slot * SH::SLOT;
       const uint32_t gbase = tmem + (grp & 1) * (NA * NC);
       const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
@@ -559,10 +574,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
             }
           }
         }
+        TC_TLC(8, s);
         // one commit frees the ring slot (producer) and, through it, the A
         // buffer (expanders wait on the slot of the stage NAB back)
         tc_commit(&empty[slot]);
         if (!gfirst) tc_commit(&gfull[grp & 1]);
+        TC_TLC(9, s);
         TC_TL(4, s);
       }
       __syncwarp();
