@@ -49,7 +49,8 @@ _P = ctypes.c_void_p
 class Layer(ctypes.Structure):
     _fields_ = [(n, _P) for n in (
         "ln1", "ln2", "wq", "wk", "wv", "wo", "wg", "wu", "wd",
-        "sq", "sk", "sv", "so", "sg", "su", "sd", "bq", "bk", "bv", "k_pool", "v_pool")]
+        "sq", "sk", "sv", "so", "sg", "su", "sd", "bq", "bk", "bv", "k_pool", "v_pool",
+        "k8", "v8", "k_scale", "v_scale")]
 
 
 def lib() -> ctypes.CDLL:
@@ -348,7 +349,9 @@ def make_config(cfg: dict) -> Config:
                   cfg["n_layers"], cfg.get("vocab", 0), cfg["eps"], cfg["theta"])
 
 
-def make_layer(w: dict, k_pool: np.ndarray, v_pool: np.ndarray, keep: list) -> Layer:
+def make_layer(w: dict, k_pool, v_pool, keep: list) -> Layer:
+    """k_pool / v_pool: fp16 pools, or FP8 pools as (codes uint8, scales fp32)
+    pairs (updated in place by the layer's append)."""
     lay = Layer()
     for name in ("ln1", "ln2", "sq", "sk", "sv", "so", "sg", "su", "sd"):
         a = _c(w[name], np.float16)
@@ -363,6 +366,12 @@ def make_layer(w: dict, k_pool: np.ndarray, v_pool: np.ndarray, keep: list) -> L
             a = _c(w[name], np.float16)
             keep.append(a)
             setattr(lay, name, a.ctypes.data)
+    if isinstance(k_pool, tuple):
+        (k8, ks), (v8, vs) = k_pool, v_pool
+        for a, dt in ((k8, np.uint8), (v8, np.uint8), (ks, np.float32), (vs, np.float32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        lay.k8, lay.v8, lay.k_scale, lay.v_scale = k8.ctypes.data, v8.ctypes.data, ks.ctypes.data, vs.ctypes.data
+        return lay
     assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
     assert k_pool.dtype == np.float16 and v_pool.dtype == np.float16
     lay.k_pool = k_pool.ctypes.data

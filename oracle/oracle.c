@@ -622,6 +622,10 @@ typedef struct {
   const uint16_t *sq, *sk, *sv, *so, *sg, *su, *sd;    /* group scales */
   const uint16_t *bq, *bk, *bv;                        /* nullable */
   uint16_t *k_pool, *v_pool;                           /* [pages][Hkv][16][D] */
+  /* FP8 (E4M3) pools instead of k_pool / v_pool when k8 is set: codes
+   * [pages][Hkv][16][D] and fp32 row scales [pages][Hkv][16] */
+  uint8_t *k8, *v8;
+  float *k_scale, *v_scale;
 } orc_layer;
 
 /* x [B][H] is replaced by the layer output.  context_lens are post-append. */
@@ -650,9 +654,18 @@ void orc_decoder_layer(const orc_config* c, const orc_layer* w, uint16_t* x,
     orc_rope(q + (size_t)b * Hq * D, Hq, D, pos, c->theta);
     orc_rope(k + (size_t)b * Hkv * D, Hkv, D, pos, c->theta);
   }
-  orc_kv_append(k, v, w->k_pool, w->v_pool, block_table, max_blocks, context_lens, B, Hkv, D);
-  orc_paged_attention(q, w->k_pool, w->v_pool, block_table, max_blocks, context_lens, B, Hq, Hkv,
-                      D, 1.0 / sqrt((double)D), att);
+  if (w->k8) {
+    /* the KV cache in FP8 pages: the new rows quantised, every row read back
+     * as code * scale ([EN] "1. Weight Packing and FP8 Utilization") */
+    orc_kv_append_fp8(k, v, w->k8, w->v8, w->k_scale, w->v_scale, block_table, max_blocks, context_lens, B,
+                      Hkv, D);
+    orc_paged_attention_fp8(q, w->k8, w->v8, w->k_scale, w->v_scale, block_table, max_blocks, context_lens,
+                            B, Hq, Hkv, D, 1.0 / sqrt((double)D), att);
+  } else {
+    orc_kv_append(k, v, w->k_pool, w->v_pool, block_table, max_blocks, context_lens, B, Hkv, D);
+    orc_paged_attention(q, w->k_pool, w->v_pool, block_table, max_blocks, context_lens, B, Hq, Hkv,
+                        D, 1.0 / sqrt((double)D), att);
+  }
   orc_w4a16_gemv(att, B, Hq * D, w->wo, w->so, H, NULL, x, h);
   orc_rmsnorm(h, w->ln2, B, H, c->eps, xn);
   orc_w4a16_gemv(xn, B, H, w->wg, w->sg, I, NULL, NULL, gt);

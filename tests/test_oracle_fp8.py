@@ -136,3 +136,55 @@ def test_fp8_paged_attention_equals_fp16_attention_on_exact_pools():
     got = orc.paged_attention_fp8(q, kc, vc, ks, vs, bt, lens, 1.0 / np.sqrt(D))
     ref = orc.paged_attention(q, k16, v16, bt, lens, 1.0 / np.sqrt(D))
     assert np.array_equal(got, ref)
+
+
+def _fp8_pools(pool):
+    """Quantise every row of an fp16 pool [pages][Hkv][16][D] with the
+    (pinned) row quantiser: (codes uint8, scales fp32 [pages][Hkv][16])."""
+    P, Hkv, T, D = pool.shape
+    codes = np.zeros((P, Hkv, T, D), np.uint8)
+    scales = np.zeros((P, Hkv, T), np.float32)
+    for p in range(P):
+        for h in range(Hkv):
+            for t in range(T):
+                codes[p, h, t], scales[p, h, t] = orc.fp8_quantize_row(pool[p, h, t])
+    return codes, scales
+
+
+def test_decoder_layer_over_fp8_pools_is_composition_of_pinned_parts():
+    """A layer whose KV cache is FP8 pages: the same composition as the fp16
+    layer with the FP8 append and the FP8 paged attention in place of the
+    fp16 ones (each pinned above); only the appended rows of the pools
+    change."""
+    import math
+    cfg = dict(synth.TINY_LAYER, bias=True)
+    c = synth.layer_case(cfg, seed=1200)
+    w = c["weights"]
+    Hq, Hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    L = int(c["context_lens"][0])
+    k8, ks = _fp8_pools(c["k_pool"])
+    v8, vs = _fp8_pools(c["v_pool"])
+    k1, ks1, v1, vs1 = k8.copy(), ks.copy(), v8.copy(), vs.copy()
+    out = orc.decoder_layer(cfg, w, c["x"], (k1, ks1), (v1, vs1), c["block_table"], c["context_lens"])
+
+    k2, ks2, v2, vs2 = k8.copy(), ks.copy(), v8.copy(), vs.copy()
+    xn = orc.rmsnorm(c["x"], w["ln1"], cfg["eps"])
+    q = orc.rope(orc.w4a16_gemv(xn, w["wq"], w["sq"], bias=w["bq"]).reshape(Hq, D), L - 1, cfg["theta"])
+    k = orc.rope(orc.w4a16_gemv(xn, w["wk"], w["sk"], bias=w["bk"]).reshape(Hkv, D), L - 1, cfg["theta"])
+    v = orc.w4a16_gemv(xn, w["wv"], w["sv"], bias=w["bv"]).reshape(Hkv, D)
+    orc.kv_append_fp8(k[None], v[None], k2, v2, ks2, vs2, c["block_table"], c["context_lens"])
+    att = orc.paged_attention_fp8(q[None], k2, v2, ks2, vs2, c["block_table"], c["context_lens"], 1 / math.sqrt(D))
+    h = orc.w4a16_gemv(att.reshape(1, Hq * D), w["wo"], w["so"], residual=c["x"])
+    hn = orc.rmsnorm(h, w["ln2"], cfg["eps"])
+    m = orc.silu_mul(orc.w4a16_gemv(hn, w["wg"], w["sg"]), orc.w4a16_gemv(hn, w["wu"], w["su"]))
+    ref = orc.w4a16_gemv(m, w["wd"], w["sd"], residual=h)
+    assert np.array_equal(out, ref)
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    assert np.array_equal(ks1, ks2) and np.array_equal(vs1, vs2)
+    page, slot = int(c["block_table"][0, (L - 1) // 16]), (L - 1) % 16
+    changed = {tuple(p) for p in np.argwhere(np.any(k1 != k8, axis=-1))}
+    assert changed <= {(page, h, slot) for h in range(Hkv)}
+    # the same layer over the fp16 pools differs (the cache really is FP8)
+    out16 = orc.decoder_layer(cfg, w, c["x"], c["k_pool"].copy(), c["v_pool"].copy(), c["block_table"],
+                              c["context_lens"])
+    assert not np.array_equal(out, out16)
