@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--kernel", default=None,
                     choices=["gateup", "down", "qkv", "o", "attention", "lm_head", "attention_long",
-                             "attention_fp8"],
+                             "attention_fp8", "prefill"],
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
     ap.add_argument("--clock-log", default=None,
@@ -323,6 +323,22 @@ def run_kernel(args):
     r = synth.rng(args.seed)
     tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int32) if a.dtype == np.uint32 else a)).to(dev)
     name = args.kernel
+    if name == "prefill":
+        # the 28-layer model (the b=1 workload's weights), a 512-token prompt
+        # prefilled args.steps times from an empty cache
+        from w4a16_decode_paged_gb300 import synth as _s  # noqa: F401
+        cfg, lens0, pool_pages, _ = workload(args)
+        inp = make_inputs(cfg, args.seed, lens0, 64, pool_pages)
+        dls = [api.device_layer(w, api.device_pool(inp, l, "k", dev), api.device_pool(inp, l, "v", dev), device=dev)
+               for l, w in enumerate(inp["layers"])]
+        model = api.Model(cfg, dls, embed=tdev(inp["embed"]), final_norm=tdev(inp["fnorm"]), lm_head=tdev(inp["lm"]),
+                          max_batch=1, max_context=600, num_pages=inp["pool_pages"])
+        stream = torch.cuda.Stream(device=dev)
+        res = time_prefill(torch, api, model, cfg, tdev(inp["bt"]), dev, stream, T=512, reps=max(1, args.steps))
+        res.update({"kernel": "prefill", "workload": "28 layers, 512-token prompt, empty cache"})
+        print(json.dumps(res))
+        model.close()
+        return 0
     if name in ("attention_long", "attention_fp8"):
         stream = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(stream):

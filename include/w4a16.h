@@ -369,6 +369,13 @@ typedef struct {
   const uint16_t *sq, *sk, *sv, *so, *sg, *su, *sd;   /* fp16 group scales */
   const uint16_t *bq, *bk, *bv;                       /* fp16 biases or NULL */
   uint16_t *k_pool, *v_pool;                          /* this layer's pools */
+  /* FP8 (E4M3) KV pages instead of k_pool / v_pool (every layer or none;
+   * k_pool / v_pool then NULL): codes uint8 [num_pages][Hkv][16][D] and fp32
+   * row scales [num_pages][Hkv][16], as paged_gqa_decode_fp8 takes them.
+   * The decode step then appends quantised rows and attends over the codes;
+   * the persistent decode path and w4a16_prefill are not built for them. */
+  uint8_t *k8, *v8;
+  float *k_scale, *v_scale;
 } w4a16_layer_weights;
 
 typedef struct {

@@ -159,3 +159,96 @@ def test_fp8_fused_rope_append_attention(api, lens, part):
     rows = {(int(bt[b, (L - 1) // 16]), (L - 1) % 16) for b, L in enumerate(lens)}
     changed = np.argwhere(np.any(gkc != kc, axis=-1))
     assert {(int(p), int(s)) for p, _, s in changed} <= rows
+
+
+def _fp8_of_pool(pool):
+    """The oracle's row quantiser over a whole fp16 pool [pages][Hkv][16][D]."""
+    codes = np.zeros(pool.shape, np.uint8)
+    scales = np.zeros(pool.shape[:3], np.float32)
+    for idx in np.ndindex(pool.shape[:3]):
+        if np.any(pool[idx] != 0):
+            codes[idx], scales[idx] = orc.fp8_quantize_row(pool[idx])
+    return codes, scales
+
+
+def _fp8_model(api, case, max_context):
+    cfg = case["cfg"]
+    host, dls = [], []
+    for l, w in enumerate(case["layers"]):
+        k8, ks = _fp8_of_pool(synth.host_pool(case, l, "k"))
+        v8, vs = _fp8_of_pool(synth.host_pool(case, l, "v"))
+        host.append(((k8, ks), (v8, vs)))
+        dls.append(api.device_layer(w, (k8, ks), (v8, vs)))
+    m = api.Model(cfg, dls, embed=to_dev(case["embed"], torch), final_norm=to_dev(case["fnorm"], torch),
+                  lm_head=to_dev(case["lm"], torch), max_batch=case["tok"].size, max_context=max_context,
+                  num_pages=case["pool_pages"])
+    return m, dls, host
+
+
+def test_fp8_model_decode_free_running_matches_oracle(api):
+    """A 3-layer model whose KV cache is FP8 pages: 10 free-running greedy
+    steps of decode_step against the oracle's decode over FP8 pools (the same
+    codes and scales to start with; each side appends its own quantised rows)."""
+    cfg = dict(synth.TINY_LAYER, n_layers=3, vocab=900, bias=True, codes="symmetric")
+    case = synth.model_case(cfg, lens=[37], gen_tokens=16, pool_pages=32, seed=9900)
+    m, dls, host = _fp8_model(api, case, 128)
+    assert m.decode_path(1) == "kernels"   # the persistent kernel is not built for FP8 pools
+    tok = to_dev(case["tok"], torch)
+    ld = to_dev(case["lens"], torch)
+    btd = to_dev(case["bt"], torch)
+    logits = torch.empty((1, cfg["vocab"]), dtype=torch.float16, device="cuda")
+    kps = [h[0] for h in host]
+    vps = [h[1] for h in host]
+    t_or, n = case["tok"].copy(), case["lens"].copy()
+    for step in range(10):
+        fed = to_host(tok).astype(np.int32).copy()
+        m.decode_step(tok, tok, btd, ld, logits=logits, use_graph=True)
+        n = n + 1
+        t_next, lg, _ = orc.decode_step(cfg, case["layers"], kps, vps, case["embed"], case["fnorm"], case["lm"],
+                                        fed, case["bt"], n, want_logits=True)
+        got, ref = to_host(logits)[0].astype(np.float64), lg[0].astype(np.float64)
+        rel = np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2))
+        assert rel < 0.03, f"step {step}: logits differ by {rel:.3g} of their RMS"
+        srt = np.sort(ref)
+        if srt[-1] - srt[-2] > 4 * float(np.max(np.abs(got - ref))) + 2e-3:
+            assert int(to_host(tok)[0]) == int(t_next[0]), f"step {step}"
+    assert m.check_errors() == 0
+    # the appended rows are FP8: every new position's scale is set, codes decode near the oracle's rows
+    pos = np.arange(int(case["lens"][0]), int(n[0]))
+    pages, slots = case["bt"][0, pos // 16], pos % 16
+    for l in range(cfg["n_layers"]):
+        vs_dev = to_host(dls[l]["v_scale"])[pages, :, slots]
+        assert np.all(vs_dev > 0)
+        v_dev = np.vectorize(orc.e4m3_to_double)(to_host(dls[l]["v8"])[pages, :, slots]) * vs_dev[..., None]
+        v_ref = np.vectorize(orc.e4m3_to_double)(vps[l][0][pages, :, slots]) * vps[l][1][pages, :, slots][..., None]
+        rel = np.sqrt(np.mean((v_dev - v_ref) ** 2) / np.mean(v_ref ** 2))
+        assert rel < 0.05, f"layer {l}: appended v rows differ by {rel:.3g} of their RMS"
+    m.close()
+
+
+def test_fp8_model_batched_step_and_prefill_refusal(api):
+    """Four sequences on FP8 pools (the CUDA-core batch path) for two steps
+    against the oracle, and w4a16_prefill refusing FP8 pools."""
+    cfg = dict(synth.TINY_LAYER, n_layers=2, vocab=700, bias=True, codes="symmetric")
+    case = synth.model_case(cfg, lens=[1, 16, 17, 40], gen_tokens=4, pool_pages=32, seed=9910)
+    m, dls, host = _fp8_model(api, case, 64)
+    tok = to_dev(case["tok"], torch)
+    ld = to_dev(case["lens"], torch)
+    logits = torch.empty((4, cfg["vocab"]), dtype=torch.float16, device="cuda")
+    kps = [h[0] for h in host]
+    vps = [h[1] for h in host]
+    n = case["lens"].copy()
+    for step in range(2):
+        fed = to_host(tok).astype(np.int32).copy()
+        m.decode_step(tok, tok, to_dev(case["bt"], torch), ld, logits=logits, use_graph=False)
+        n = n + 1
+        _, lg, _ = orc.decode_step(cfg, case["layers"], kps, vps, case["embed"], case["fnorm"], case["lm"],
+                                   fed, case["bt"], n, want_logits=True)
+        got, ref = to_host(logits).astype(np.float64), lg.astype(np.float64)
+        rel = np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2))
+        assert rel < 0.03, f"step {step}: logits differ by {rel:.3g} of their RMS"
+    assert m.check_errors() == 0
+    with pytest.raises(Exception):
+        m.prefill(to_dev(np.arange(8, dtype=np.int32), torch), to_dev(case["bt"][:1], torch),
+                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+    m.close()

@@ -39,7 +39,8 @@ class ModelConfig(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, P) for n in ("ln1", "ln2", "wq", "wk", "wv", "wo", "wg", "wu", "wd", "sq", "sk", "sv", "so",
-                                 "sg", "su", "sd", "bq", "bk", "bv", "k_pool", "v_pool")]
+                                 "sg", "su", "sd", "bq", "bk", "bv", "k_pool", "v_pool",
+                                 "k8", "v8", "k_scale", "v_scale")]
 
 
 class ModelWeights(ctypes.Structure):

@@ -392,7 +392,7 @@ class Model:
     (torch tensors kept alive here), the library owns its activation arena."""
 
     LAYER_KEYS = ("ln1", "ln2", "wq", "wk", "wv", "wo", "wg", "wu", "wd", "sq", "sk", "sv", "so", "sg", "su",
-                  "sd", "bq", "bk", "bv", "k_pool", "v_pool")
+                  "sd", "bq", "bk", "bv", "k_pool", "v_pool", "k8", "v8", "k_scale", "v_scale")
 
     def __init__(self, cfg: dict, layers: list, embed=None, final_norm=None, lm_head=None, max_batch=1,
                  max_context=4096, num_pages=None, partition_tokens=0):
@@ -402,7 +402,7 @@ class Model:
         c = ModelConfig(cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["inter"],
                         len(layers), cfg.get("vocab", 0) if lm_head is not None else 0, float(cfg["eps"]),
                         float(cfg["theta"]), int(num_pages if num_pages is not None else
-                                                 layers[0]["k_pool"].shape[0]), int(partition_tokens))
+                                                 _layer_pool(layers[0]).shape[0]), int(partition_tokens))
         arr = (LayerWeights * max(1, len(layers)))()
         for i, lw in enumerate(layers):
             for key in self.LAYER_KEYS:
@@ -584,9 +584,15 @@ def device_pool(case: dict, layer: int, which: str, device="cuda"):
     return p
 
 
+def _layer_pool(layer: dict):
+    return layer["k_pool"] if layer.get("k_pool") is not None else layer["k8"]
+
+
 def device_layer(w: dict, k_pool, v_pool, device="cuda") -> dict:
     """Move one layer's numpy weights (as drawn by ``synth``) and its pools to
-    the device as torch tensors (uint32 words travel as int32)."""
+    the device as torch tensors (uint32 words travel as int32).  A pool given
+    as a (codes uint8, scales fp32) pair makes the layer's KV cache FP8
+    (E4M3) pages."""
     import numpy as np
 
     out = {}
@@ -598,6 +604,16 @@ def device_layer(w: dict, k_pool, v_pool, device="cuda") -> dict:
         if a.dtype == np.uint32:
             a = a.view(np.int32)
         out[key] = torch.from_numpy(a).to(device)
+    dev = lambda a: a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    if isinstance(k_pool, tuple):
+        (k8, ks), (v8, vs) = k_pool, v_pool
+        out["k_pool"] = out["v_pool"] = None
+        out["k8"], out["k_scale"], out["v8"], out["v_scale"] = dev(k8), dev(ks), dev(v8), dev(vs)
+        for key, dt in (("k8", torch.uint8), ("v8", torch.uint8), ("k_scale", torch.float32),
+                        ("v_scale", torch.float32)):
+            if out[key].dtype != dt or not out[key].is_contiguous():
+                raise ValueError(f"{key}: {dt} contiguous expected")
+        return out
     for key, a in (("k_pool", k_pool), ("v_pool", v_pool)):
-        out[key] = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        out[key] = dev(a)
     return out

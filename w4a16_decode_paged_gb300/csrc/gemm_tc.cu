@@ -1,39 +1,41 @@
-// gemm_tc.cu -- batched-decode W4A16 GEMM (M <= 32 sequences) on the
-// 5th-generation tensor cores (tcgen05, accumulator in tensor memory).
+// gemm_tc.cu -- W4A16 GEMM for a batch of rows (decode batches of up to 32
+// sequences; the wider row blocks of a prompt) on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory).
 //
 // With a decode batch of 32 the q/k/v, o, gate/up and down projections
 // become real dense contractions, y[m][n] = sum_k x[m][k] * w[n][k]
 // ("Архитектурные решения и оптимизации" of the aikraft.ru article fixes the
 // symmetric group-wise INT4 weights with group 128; the pages' "maximize
 // batch sizes" motivates the batched form).  Swap-AB: the MMA's A operand is a
-// 128-row weight tile, its B operand the (up to) 32 activation rows, so
-// D[n][m] (128 lanes x 32 columns, fp32) lives in tensor memory.
+// 128-row weight tile, its B operand the NC activation rows (32, or 64 / 128
+// for a prompt), so D[n][m] (128 lanes x NC columns, fp32) lives in tensor
+// memory.
 //
 // The weights are streamed once, so the kernel is a bandwidth pipe with
 // specialised warps that meet only at mbarriers: a producer warp fills a
-// ring of stages (64 k each) with cp.async (packed int4 rows, and the
-// activation tile directly in the canonical no-swizzle K-major layout the MMA
-// reads: core matrices of 8 rows x 16 bytes, K-adjacent core matrices 128 B
-// apart, 8-row groups 256 B apart); 256 reader threads turn the 32 codes per
-// stage of their weight row into exact fp16 integers (q in [-8, 7]) and store
-// them with tcgen05.st into one of NAB tensor-memory A buffers (the MMA
-// reads A from tensor memory, so the expanded codes never touch shared
-// memory); one thread issues four kind::f16 MMAs (K = 16) per weight matrix
-// and commits them to the barriers that free the A buffer, the ring slot and,
-// per group, the accumulator buffer.
+// ring of 64-k stages with one bulk-tensor (TMA) copy per operand (the packed
+// int4 rows; the activation tile with the 128-byte swizzle the MMA's
+// shared-memory descriptor reads), or per-lane 16-byte copies where a weight
+// tile would straddle two segments; expander warps turn each row's codes into
+// exact fp16 integers (q in [-8, 7]) and store them with tcgen05.st into one
+// of NAB tensor-memory A buffers (the MMA reads A from tensor memory, so the
+// expanded codes never touch shared memory); one warp issues four kind::f16
+// MMAs (K = 16) per weight matrix and stage and commits them to the barriers
+// that free the ring slot (and with it the A buffer) and, per group, the
+// accumulator buffer; reader warps take the group sums out.
 //
 // Precision: the MMAs see exact codes and exact fp16 activations (products
 // exact, fp32 sums).  Each 128-wide scale group accumulates into its own
 // tensor-memory buffer (two alternate); the readers read a group's sums with
-// tcgen05.ld at the second stage of the next group (while the tensor core
-// works on that group) and add them times the row's fp32 scale, so the only
-// roundings are fp32 sums and the final fp16 store.
+// tcgen05.ld as soon as the tensor core has finished the group and add them
+// times the row's fp32 scale, so the only roundings are fp32 sums and the
+// final fp16 store.
 //
 // Small-N projections split K across CTAs (split length chosen so the work
 // items fill whole waves of CTAs): each split parks its fp32 tile in the
 // workspace and the last split of a tile (atomic ticket) sums them and runs
 // the epilogue.  Dense fp16 weights (the batched lm_head) are copied into the
-// ring in the canonical layout and used by the MMA as they are.
+// ring in the swizzled layout and used by the MMA as they are.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

@@ -53,6 +53,7 @@ struct w4a16_model {
   std::vector<w4a16_layer_weights> layers;
   const __half *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
   int max_batch = 0, max_context = 0, part_tokens = 0, P = 0;
+  bool kv8 = false;  // the layers' KV pools are FP8 (E4M3) codes + row scales
   char* arena = nullptr;
   size_t arena_bytes = 0;
   __half *x = nullptr, *qkv = nullptr, *att = nullptr, *h = nullptr, *mlp = nullptr;
@@ -112,15 +113,18 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   w4a16_model* m = new w4a16_model();
   m->cfg = c;
   m->layers.assign(w->layers, w->layers + c.n_layers);
+  m->kv8 = c.n_layers > 0 && m->layers[0].k8 != nullptr;
   for (int l = 0; l < c.n_layers; ++l) {
     const w4a16_layer_weights& L = m->layers[l];
+    const bool pools = m->kv8 ? (L.k8 && L.v8 && L.k_scale && L.v_scale) : (L.k_pool && L.v_pool && !L.k8);
     if (!(L.ln1 && L.ln2 && L.wq && L.wk && L.wv && L.wo && L.wg && L.wu && L.wd && L.sq && L.sk && L.sv && L.so &&
-          L.sg && L.su && L.sd && L.k_pool && L.v_pool)) {
+          L.sg && L.su && L.sd && pools)) {
       delete m;
-      return set_error(W4A16_ERR_INVALID_ARG, "model_create: layer %d has a null weight", l);
+      return set_error(W4A16_ERR_INVALID_ARG,
+                       "model_create: layer %d has a null weight or pool (FP8 pools: every layer or none)", l);
     }
-    const void* ptrs[] = {L.ln1, L.ln2, L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.sq, L.sk, L.sv,
-                          L.so,  L.sg,  L.su, L.sd, L.bq, L.bk, L.bv, L.k_pool, L.v_pool};
+    const void* ptrs[] = {L.ln1, L.ln2, L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.sq, L.sk, L.sv, L.so, L.sg,
+                          L.su,  L.sd,  L.bq, L.bk, L.bv, L.k_pool, L.v_pool, L.k8, L.v8, L.k_scale, L.v_scale};
     for (const void* p : ptrs) {
       if (p && !aligned(p, 128)) {
         delete m;
@@ -174,7 +178,7 @@ extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_mod
   // the persistent path: one sequence, the Qwen2-style 7:1 GQA shapes, contexts
   // its attention merge covers
   m->pk_ok = persistent_supported(c.hidden, c.n_q_heads, c.n_kv_heads, c.head_dim, c.inter, c.n_layers, max_context) &&
-             c.vocab >= 2 && c.vocab % 2 == 0;
+             c.vocab >= 2 && c.vocab % 2 == 0 && !m->kv8;
   size_t o_pk = off;
   if (m->pk_ok) {
     m->pk_P = (max_context + PK_PARTITION_TOKENS - 1) / PK_PARTITION_TOKENS;
@@ -366,6 +370,13 @@ static int run_layer(w4a16_model* m, int l, __half* x, const int32_t* bt, int ma
   a.q_stride = nqkv;
   a.k_pool = reinterpret_cast<__half*>(L.k_pool);
   a.v_pool = reinterpret_cast<__half*>(L.v_pool);
+  if (m->kv8) {
+    a.kv8 = 1;
+    a.k8 = L.k8;
+    a.v8 = L.v8;
+    a.ks = L.k_scale;
+    a.vs = L.v_scale;
+  }
   a.block_table = bt;
   a.context_lens = lens;
   a.out = m->att;
@@ -529,6 +540,7 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
                              void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
   W4_CHECK_ARG(m && tokens && block_table && context_lens && token_out && workspace, "prefill: null argument");
   W4_CHECK_ARG(m->embed && m->final_norm && m->lm_head && m->cfg.vocab > 0, "prefill: model has no lm_head");
+  W4_CHECK_SHAPE(!m->kv8, "prefill: not built for FP8 KV pools (decode them in, one token per step)");
   W4_CHECK_ARG(T >= 1 && max_blocks >= 1, "prefill: T=%d max_blocks=%d", T, max_blocks);
   W4_CHECK_SHAPE(T <= m->max_context, "prefill: %d tokens > max_context %d", T, m->max_context);
   W4_CHECK_ALIGN(workspace, 256, "workspace");
@@ -728,7 +740,8 @@ extern "C" int w4a16_model_set_decode_path(w4a16_model* m, int path) {
                "model_set_decode_path: unknown path %d", path);
   if (path == W4A16_PATH_PERSISTENT && !m->pk_ok)
     return set_error(W4A16_ERR_SHAPE, "model_set_decode_path: the persistent kernel does not cover this model "
-                                      "(one sequence, head_dim 128, Hq = 7 Hkv, max_context <= %d)", PK_MAX_CONTEXT);
+                                      "(one sequence, head_dim 128, Hq = 7 Hkv, max_context <= %d, fp16 KV pools)",
+                     PK_MAX_CONTEXT);
   std::lock_guard<std::mutex> lk(m->mu);
   m->decode_path = path;
   return W4A16_OK;
