@@ -372,8 +372,8 @@ typedef struct {
   /* FP8 (E4M3) KV pages instead of k_pool / v_pool (every layer or none;
    * k_pool / v_pool then NULL): codes uint8 [num_pages][Hkv][16][D] and fp32
    * row scales [num_pages][Hkv][16], as paged_gqa_decode_fp8 takes them.
-   * The decode step then appends quantised rows and attends over the codes;
-   * the persistent decode path and w4a16_prefill are not built for them. */
+   * The decode step and w4a16_prefill then append quantised rows and attend
+   * over the codes; the persistent decode path is not built for them. */
   uint8_t *k8, *v8;
   float *k_scale, *v_scale;
 } w4a16_layer_weights;

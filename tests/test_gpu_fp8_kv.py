@@ -226,9 +226,9 @@ def test_fp8_model_decode_free_running_matches_oracle(api):
     m.close()
 
 
-def test_fp8_model_batched_step_and_prefill_refusal(api):
+def test_fp8_model_batched_step(api):
     """Four sequences on FP8 pools (the CUDA-core batch path) for two steps
-    against the oracle, and w4a16_prefill refusing FP8 pools."""
+    against the oracle."""
     cfg = dict(synth.TINY_LAYER, n_layers=2, vocab=700, bias=True, codes="symmetric")
     case = synth.model_case(cfg, lens=[1, 16, 17, 40], gen_tokens=4, pool_pages=32, seed=9910)
     m, dls, host = _fp8_model(api, case, 64)
@@ -248,7 +248,47 @@ def test_fp8_model_batched_step_and_prefill_refusal(api):
         rel = np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2))
         assert rel < 0.03, f"step {step}: logits differ by {rel:.3g} of their RMS"
     assert m.check_errors() == 0
-    with pytest.raises(Exception):
-        m.prefill(to_dev(np.arange(8, dtype=np.int32), torch), to_dev(case["bt"][:1], torch),
-                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+    m.close()
+
+
+@pytest.mark.parametrize("cached,T", [(0, 37), (21, 16)])
+def test_fp8_prefill_matches_oracle_token_by_token(api, cached, T):
+    """w4a16_prefill over FP8 pools (quantised append of every prompt row,
+    the causal prompt attention over the codes) against the oracle feeding
+    the prompt one token per decode step over the same FP8 pools: last-token
+    logits, and the appended rows (scales set, values close)."""
+    cfg = dict(synth.TINY_LAYER, n_layers=2, vocab=800, bias=True, codes="symmetric")
+    case = synth.model_case(cfg, lens=[cached], gen_tokens=T + 2, pool_pages=(cached + T) // 16 + 8,
+                            seed=9920 + cached)
+    prompt = synth.rng(9921 + cached).integers(0, cfg["vocab"], size=T).astype(np.int32)
+    m, dls, host = _fp8_model(api, case, cached + T + 16)
+    ld = to_dev(case["lens"], torch)
+    logits = torch.empty((1, cfg["vocab"]), dtype=torch.float16, device="cuda")
+    tok = m.prefill(to_dev(prompt, torch), to_dev(case["bt"], torch), ld, logits=logits)
+    torch.cuda.synchronize()
+    assert m.check_errors() == 0
+    assert int(to_host(ld)[0]) == cached + T
+    kps = [h[0] for h in host]
+    vps = [h[1] for h in host]
+    for i, tk in enumerate(prompt):
+        t_next, lg, _ = orc.decode_step(cfg, case["layers"], kps, vps, case["embed"], case["fnorm"], case["lm"],
+                                        np.array([tk], np.int32), case["bt"], np.array([cached + i + 1], np.int32),
+                                        want_logits=True)
+    got, ref = to_host(logits)[0].astype(np.float64), lg[0].astype(np.float64)
+    rel = np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2))
+    assert rel < 0.03, f"logits differ by {rel:.3g} of their RMS"
+    srt = np.sort(ref)
+    if srt[-1] - srt[-2] > 4 * float(np.max(np.abs(got - ref))) + 2e-3:
+        assert int(to_host(tok)[0]) == int(t_next[0])
+    pos = np.arange(cached, cached + T)
+    pages, slots = case["bt"][0, pos // 16], pos % 16
+    dec = np.vectorize(orc.e4m3_to_double)
+    for l in range(cfg["n_layers"]):
+        for name, (codes, scales) in (("k", kps[l]), ("v", vps[l])):
+            sd = to_host(dls[l][name + "_scale"])[pages, :, slots]
+            assert np.all(sd > 0), (l, name)
+            got_rows = dec(to_host(dls[l][name + "8"])[pages, :, slots]) * sd[..., None]
+            ref_rows = dec(codes[pages, :, slots]) * scales[pages, :, slots][..., None]
+            rel = np.sqrt(np.mean((got_rows - ref_rows) ** 2) / np.mean(ref_rows ** 2))
+            assert rel < 0.05, f"layer {l} {name}: prompt rows differ by {rel:.3g} of their RMS"
     m.close()

@@ -586,13 +586,15 @@ int launch_paged_attention(const AttnArgs& a_in, cudaStream_t s) {
 // takes 16 consecutive rows and one kv head; every K/V page of its range is
 // copied once into a ring shared by the CTA's 8 warps, and warp w works on
 // rows 2w and 2w + 1 together (the MMA's rows 0-7 and 8-15), so each page
-// feeds 16 query tokens x G heads.
+// feeds 16 query tokens x G heads.  KV8: FP8 (E4M3) pages, codes and row
+// scales, in the dim orders of the FP8 decode step (attn8_qdim, attn8_odim).
 // ---------------------------------------------------------------------------
 constexpr int PF_ROWS = 16;    // query rows per CTA
 constexpr int PF_WARPS = 8;
 constexpr int PF_STAGES = 3;   // page slots of the CTA's ring
+constexpr size_t pf_slot_bytes(bool kv8) { return kv8 ? (size_t)ATT8_SLOT : (size_t)2 * ATT_SSLICE * 2; }
 
-template <int G>
+template <int G, bool KV8>
 __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -620,15 +622,22 @@ __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_
       const int row = r ? rB : rA;
       uint32_t lo = 0u, hi = 0u;
       if (g < G && row < a.B) {
-        const __half* qrow = a.q + (size_t)row * a.q_stride + (size_t)(kvh * G + g) * ATT_D + 16 * st + 2 * t4;
-        lo = __ldcg(reinterpret_cast<const unsigned int*>(qrow));
-        hi = __ldcg(reinterpret_cast<const unsigned int*>(qrow + 8));
+        const __half* qh = a.q + (size_t)row * a.q_stride + (size_t)(kvh * G + g) * ATT_D;
+        if (KV8) {
+          // physical dims p0 .. p0 + 3 (see attn8_qdim)
+          const uint2 q4 = __ldcg(reinterpret_cast<const uint2*>(qh + attn8_qdim(st, t4)));
+          lo = q4.x;
+          hi = q4.y;
+        } else {
+          lo = __ldcg(reinterpret_cast<const unsigned int*>(qh + 16 * st + 2 * t4));
+          hi = __ldcg(reinterpret_cast<const unsigned int*>(qh + 16 * st + 8 + 2 * t4));
+        }
       }
       qa[st][r] = lo;
       qa[st][2 + r] = hi;
     }
   }
-  constexpr int SLOT = 2 * ATT_SSLICE * 2;  // K and V slices, padded rows
+  constexpr int SLOT = (int)pf_slot_bytes(KV8);  // K and V slices, padded rows (+ FP8 row scales)
   auto page_id = [&](int li) -> int {
     const int pg = li < a.max_blocks ? __ldcg(&a.block_table[li]) : -1;
     return (pg >= 0 && pg < a.num_pages) ? pg : -1;
@@ -638,7 +647,18 @@ __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_
   auto issue = [&](int li) {
     if (li < npages) {
       const int pg = page_id(li);
-      if (pg >= 0) {
+      if (pg >= 0 && KV8) {
+        // 2 x 16 rows of 128 code bytes (256 16-byte copies) and the 2 x 16 row scales
+        unsigned char* dst = smraw + (size_t)(li % PF_STAGES) * SLOT;
+        const size_t row0 = ((size_t)pg * a.Hkv + kvh) * ATT_PAGE;
+        const int which = tid >> 7, row = (tid >> 3) & 15, col = tid & 7;  // [K|V][row][8 chunks]
+        cp_async16(dst + which * ATT8_CODES + row * ATT8_PITCH + col * 16,
+                   (which ? a.v8 : a.k8) + (row0 + row) * ATT_D + col * 16);
+        if (tid < 8) {
+          const int w = tid >> 2, part = tid & 3;
+          cp_async16(dst + 2 * ATT8_CODES + w * ATT_PAGE * 4 + part * 16, (w ? a.vs : a.ks) + row0 + 4 * part);
+        }
+      } else if (pg >= 0) {
         unsigned char* dst = smraw + (size_t)(li % PF_STAGES) * SLOT;
         const size_t off = ((size_t)pg * a.Hkv + kvh) * ATT_SLICE;
 #pragma unroll
@@ -669,8 +689,13 @@ __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_
     // rows whose position is before this page see nothing in it (posB is -1
     // when the warp has only row A)
     if (max(posA, posB) >= tok0 && page_id(li) >= 0) {
-      const __half* Ks = reinterpret_cast<const __half*>(smraw + (size_t)(li % PF_STAGES) * SLOT);
-      attn_page_pair(Ks, Ks + ATT_SSLICE, tok0, posA, posB, qa, a.scale_log2, k_off, v_off, t4, m_run, l_run, o);
+      const unsigned char* sl = smraw + (size_t)(li % PF_STAGES) * SLOT;
+      if (KV8) {
+        attn_page_pair_fp8(sl, tok0, posA, posB, qa, a.scale_log2, g, t4, m_run, l_run, o);
+      } else {
+        const __half* Ks = reinterpret_cast<const __half*>(sl);
+        attn_page_pair(Ks, Ks + ATT_SSLICE, tok0, posA, posB, qa, a.scale_log2, k_off, v_off, t4, m_run, l_run, o);
+      }
     }
   }
   cp_async_wait<0>();
@@ -681,18 +706,27 @@ __global__ void __launch_bounds__(PF_WARPS * 32) w4pg_prefill_attn(const __grid_
       const int row = r ? rB : rA;
       if (row >= a.B) continue;
       const float inv = l_run[r] > 0.f ? 1.0f / l_run[r] : 0.f;
-      __half* out = a.out + (size_t)row * a.Hq * ATT_D + (size_t)(kvh * G + g) * ATT_D + 2 * t4;
+      __half* outh = a.out + (size_t)row * a.Hq * ATT_D + (size_t)(kvh * G + g) * ATT_D;
+      if (KV8) {
 #pragma unroll
-      for (int nb = 0; nb < 16; ++nb)
-        *reinterpret_cast<__half2*>(out + 8 * nb) = __floats2half2_rn(o[nb][2 * r] * inv, o[nb][2 * r + 1] * inv);
+        for (int nb = 0; nb < 16; ++nb) {
+          outh[attn8_odim(nb, t4, 0)] = __float2half_rn(o[nb][2 * r] * inv);
+          outh[attn8_odim(nb, t4, 1)] = __float2half_rn(o[nb][2 * r + 1] * inv);
+        }
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb)
+          *reinterpret_cast<__half2*>(outh + 8 * nb + 2 * t4) =
+              __floats2half2_rn(o[nb][2 * r] * inv, o[nb][2 * r + 1] * inv);
+      }
     }
   }
 }
 
-template <int G>
+template <int G, bool KV8>
 static int launch_prefill_attn_g(const AttnArgs& a, cudaStream_t s) {
-  constexpr size_t smem = (size_t)PF_STAGES * 2 * ATT_SSLICE * 2;
-  auto kern = w4pg_prefill_attn<G>;
+  constexpr size_t smem = (size_t)PF_STAGES * pf_slot_bytes(KV8);
+  auto kern = w4pg_prefill_attn<G, KV8>;
   static PerDeviceOnce once;
   once_per_device(once, [&] { cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); });
   const dim3 grid((a.B + PF_ROWS - 1) / PF_ROWS, a.Hkv);
@@ -703,11 +737,11 @@ static int launch_prefill_attn_g(const AttnArgs& a, cudaStream_t s) {
 
 int launch_prefill_attention(const AttnArgs& a, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_prefill_attn_g<1>(a, s);
-    case 2: return launch_prefill_attn_g<2>(a, s);
-    case 4: return launch_prefill_attn_g<4>(a, s);
-    case 7: return launch_prefill_attn_g<7>(a, s);
-    case 8: return launch_prefill_attn_g<8>(a, s);
+    case 1: return a.kv8 ? launch_prefill_attn_g<1, true>(a, s) : launch_prefill_attn_g<1, false>(a, s);
+    case 2: return a.kv8 ? launch_prefill_attn_g<2, true>(a, s) : launch_prefill_attn_g<2, false>(a, s);
+    case 4: return a.kv8 ? launch_prefill_attn_g<4, true>(a, s) : launch_prefill_attn_g<4, false>(a, s);
+    case 7: return a.kv8 ? launch_prefill_attn_g<7, true>(a, s) : launch_prefill_attn_g<7, false>(a, s);
+    case 8: return a.kv8 ? launch_prefill_attn_g<8, true>(a, s) : launch_prefill_attn_g<8, false>(a, s);
     default:
       return set_error(W4A16_ERR_SHAPE, "prefill attention: Hq/Hkv=%d not built (1, 2, 4, 7, 8)", a.Hq / a.Hkv);
   }

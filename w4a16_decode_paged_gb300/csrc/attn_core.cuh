@@ -406,4 +406,83 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
   }
 }
 
+// attn_page_pair over an FP8 page (codes and row scales as attn_page_fp8
+// reads them): two query tokens at once, query fragments qa[st][0..3] in the
+// FP8 dim order (attn8_qdim), o in the FP8 output dim order (attn8_odim).
+__device__ __forceinline__ void attn_page_pair_fp8(const unsigned char* slot, int tok0, int posA, int posB,
+                                                   const uint32_t (&qa)[8][4], float scale_log2, int g, int t4,
+                                                   float (&m_run)[2], float (&l_run)[2], float (&o)[16][4]) {
+  const unsigned char* Kc = slot;
+  const unsigned char* Vc = slot + ATT8_CODES;
+  const float* ks = reinterpret_cast<const float*>(slot + 2 * ATT8_CODES);
+  const float* vs = ks + ATT_PAGE;
+  float sc[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  uint4 kw[2][2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      kw[r][h] = *reinterpret_cast<const uint4*>(Kc + (g + 8 * r) * ATT8_PITCH + 64 * h + 16 * t4);
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    uint32_t b0, b1, b2, b3;
+    e4m3x4_to_h2x2((&kw[0][st >> 2].x)[st & 3], b0, b1);
+    e4m3x4_to_h2x2((&kw[1][st >> 2].x)[st & 3], b2, b3);
+    mma_16816_full(sc[0], qa[st][0], qa[st][1], qa[st][2], qa[st][3], b0, b1);
+    mma_16816_full(sc[1], qa[st][0], qa[st][1], qa[st][2], qa[st][3], b2, b3);
+  }
+  float s[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int pos = r ? posB : posA;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = 8 * (j >> 1) + 2 * t4 + (j & 1);
+      const float v = sc[j >> 1][2 * r + (j & 1)] * ks[n] * scale_log2;
+      s[r][j] = (tok0 + n <= pos) ? v : -INFINITY;
+    }
+  }
+  float c[2], p[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float mx = fmaxf(fmaxf(s[r][0], s[r][1]), fmaxf(s[r][2], s[r][3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run[r], mx);
+    const bool none = m_new == -INFINITY;
+    c[r] = none ? 1.f : exp2f(m_run[r] - m_new);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[r][j] = none ? 0.f : exp2f(s[r][j] - m_new);
+    float sum = (p[r][0] + p[r][1]) + (p[r][2] + p[r][3]);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    l_run[r] = l_run[r] * c[r] + sum;
+    m_run[r] = m_new;
+  }
+  // P times the V row scales (token n = 8 (j >> 1) + 2 t4 + (j & 1)) as the A operand
+  const float v0 = vs[2 * t4], v1 = vs[2 * t4 + 1], v8 = vs[8 + 2 * t4], v9 = vs[9 + 2 * t4];
+  const __half2 h0 = __floats2half2_rn(p[0][0] * v0, p[0][1] * v1), h1 = __floats2half2_rn(p[1][0] * v0, p[1][1] * v1);
+  const __half2 h2 = __floats2half2_rn(p[0][2] * v8, p[0][3] * v9), h3 = __floats2half2_rn(p[1][2] * v8, p[1][3] * v9);
+  const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&h0), a1 = *reinterpret_cast<const uint32_t*>(&h1);
+  const uint32_t a2 = *reinterpret_cast<const uint32_t*>(&h2), a3 = *reinterpret_cast<const uint32_t*>(&h3);
+  uint4 vw[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    vw[r] = *reinterpret_cast<const uint4*>(Vc + (2 * t4 + (r & 1) + 8 * (r >> 1)) * ATT8_PITCH + 16 * g);
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    const uint32_t sel = (uint32_t)(nb & 3) | ((uint32_t)(4 + (nb & 3)) << 4);
+    uint32_t pair0, pair1;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(pair0) : "r"((&vw[0].x)[nb >> 2]), "r"((&vw[1].x)[nb >> 2]), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(pair1) : "r"((&vw[2].x)[nb >> 2]), "r"((&vw[3].x)[nb >> 2]), "r"(sel));
+    o[nb][0] *= c[0];
+    o[nb][1] *= c[0];
+    o[nb][2] *= c[1];
+    o[nb][3] *= c[1];
+    mma_16816_full(o[nb], a0, a1, a2, a3, e4m3x2_to_h2(pair0), e4m3x2_to_h2(pair1));
+  }
+}
+
 }  // namespace w4

@@ -540,7 +540,6 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
                              void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
   W4_CHECK_ARG(m && tokens && block_table && context_lens && token_out && workspace, "prefill: null argument");
   W4_CHECK_ARG(m->embed && m->final_norm && m->lm_head && m->cfg.vocab > 0, "prefill: model has no lm_head");
-  W4_CHECK_SHAPE(!m->kv8, "prefill: not built for FP8 KV pools (decode them in, one token per step)");
   W4_CHECK_ARG(T >= 1 && max_blocks >= 1, "prefill: T=%d max_blocks=%d", T, max_blocks);
   W4_CHECK_SHAPE(T <= m->max_context, "prefill: %d tokens > max_context %d", T, m->max_context);
   W4_CHECK_ALIGN(workspace, 256, "workspace");
@@ -572,6 +571,12 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
     ra.v = w.qkv + (size_t)(Hq + Hkv) * D;
     ra.k_pool = reinterpret_cast<__half*>(L.k_pool);
     ra.v_pool = reinterpret_cast<__half*>(L.v_pool);
+    if (m->kv8) {  // FP8 pages: quantised rows appended
+      ra.k8 = L.k8;
+      ra.v8 = L.v8;
+      ra.ks = L.k_scale;
+      ra.vs = L.v_scale;
+    }
     ra.block_table = w.bt_rep;
     ra.context_lens = w.lens;
     ra.err_flag = m->err_flag;
@@ -589,6 +594,13 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
     a.q_stride = nqkv;
     a.k_pool = ra.k_pool;
     a.v_pool = ra.v_pool;
+    if (m->kv8) {
+      a.kv8 = 1;
+      a.k8 = L.k8;
+      a.v8 = L.v8;
+      a.ks = L.k_scale;
+      a.vs = L.v_scale;
+    }
     a.block_table = w.bt_rep;
     a.context_lens = w.lens;
     a.out = w.att;
