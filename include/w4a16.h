@@ -145,8 +145,9 @@ W4A16_API size_t w4a16_gemm_workspace_size(int M, int K, int N, int silu);
 W4A16_API unsigned long long w4a16_debug_set_wait_limit_ns(unsigned long long ns);
 
 /* Batched FP16 lm_head on the tensor cores: logits fp32 [B][vocab] = x . W^T,
- * B <= 32, H % 128 == 0; and the row-wise argmax (lowest index on ties) with
- * an optional fp16 copy of the logits. */
+ * B <= 32, H % 128 == 0; and the row-wise argmax (lowest index on ties, NaN
+ * skipped, -1 for a row of NaN) with an optional fp16 copy of the logits,
+ * B <= 65535. */
 W4A16_API int lm_head_logits_batched(const uint16_t* x, int B, int H, const uint16_t* lm_head,
                                      int vocab, float* logits, w4a16_stream_t stream);
 W4A16_API int argmax_rows(const float* logits, int B, int vocab, int32_t* tokens_out,
@@ -295,7 +296,8 @@ W4A16_API size_t paged_gqa_decode_workspace_size(int B, int Hq, int Hkv, int max
                                        int partition_tokens, int D);
 
 /* Partition size the library picks when partition_tokens == 0 is passed to
- * paged_gqa_decode (a multiple of 16; depends on the SM count). */
+ * paged_gqa_decode (a multiple of 16): 128 up to 1024 tokens of context,
+ * else 256 when B * Hkv >= 64, else 512. */
 W4A16_API int paged_gqa_decode_default_partition(int B, int Hkv, int max_context);
 
 /* ------------------------------------------------------------------------

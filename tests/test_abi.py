@@ -169,3 +169,12 @@ def test_model_calls_reject_a_null_model(lib):
     assert lib.w4a16_model_check_errors(None, None) == 1
     assert lib.decode_step_kernel_count(None, 1) == 0
     assert b"null" in lib.w4a16_last_error()
+
+
+def test_default_partition_rule(lib):
+    """Host-side choice of the attention partition (no GPU call)."""
+    f = lib.paged_gqa_decode_default_partition
+    assert f(1, 4, 512) == 128 and f(32, 4, 1024) == 128      # one cluster of 128-token partitions
+    assert f(4, 4, 32768) == 512 and f(1, 4, 2000) == 512      # few (sequence, kv head) pairs
+    assert f(32, 4, 4096) == 256 and f(16, 4, 1025) == 256     # many pairs: a warp per 256 tokens
+    assert f(0, 4, 512) == 64                                  # invalid sizes: a fallback value

@@ -168,3 +168,32 @@ def test_argmax_rows_ties_lowest_index(api):
     toks = api.argmax_rows(lg)
     torch.cuda.synchronize()
     assert to_host(toks).tolist() == [17, 0]
+
+
+@pytest.mark.parametrize("B,V", [(33, 152064), (3, 1001), (2, 7), (1, 8)])
+def test_argmax_rows_slices_ties_nan(api, B, V):
+    """Row argmax over slices of the row: random rows, a tie planted across
+    two slices (the lower index wins), a row with NaN entries (skipped), a
+    row of NaN only (-1), negative rows; fp16 copy of the logits."""
+    r = np.random.default_rng(7000 + V)
+    lg = r.standard_normal((B, V)).astype(np.float32)
+    if V >= 16:
+        i0, i1 = V // 8 + 1, V - 2              # different slices of eight
+        lg[0, i1] = lg[0, i0] = lg[0].max() + 1.0
+    if B >= 3:
+        lg[1, ::3] = np.nan
+        lg[2, :] = -np.abs(lg[2, :]) - 1.0
+    if B >= 2 and V < 16:
+        lg[1, :] = np.nan
+    d = to_dev(lg, torch)
+    l16 = torch.empty((B, V), dtype=torch.float16, device="cuda")
+    toks = to_host(api.argmax_rows(d, logits16=l16)).tolist()
+    torch.cuda.synchronize()
+    for b in range(B):
+        row = lg[b]
+        want = -1 if np.all(np.isnan(row)) else int(np.nanargmax(row))
+        assert toks[b] == want, (b, toks[b], want)
+    got16 = to_host(l16)
+    assert np.array_equal(np.isnan(got16), np.isnan(lg))
+    m = ~np.isnan(lg)
+    assert np.array_equal(got16[m], lg[m].astype(np.float16))

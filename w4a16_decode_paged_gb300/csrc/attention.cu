@@ -859,12 +859,13 @@ int launch_rope_append(const RopeArgs& a, cudaStream_t s) {
 
 // Partition size: up to 1024 tokens, 128-token partitions (one page per warp,
 // every page fetched before the CTA's dependency wait) merged within one
-// cluster; longer contexts use 512-token partitions.
+// cluster.  Longer contexts: with many (sequence, kv head) pairs, 256-token
+// partitions, one warp each (the 28-layer batch-32 step with lengths up to
+// 4096 measured 5.00 ms against 6.03 with 512 and 5.09 with 128); with few,
+// 512-token partitions.
 int default_partition(int B, int Hkv, int max_context) {
-  (void)B;
-  (void)Hkv;
   if (max_context <= ATT_MAX_CLUSTER * 128) return 128;  // one page per warp, one cluster
-  if (max_context <= ATT_MAX_CLUSTER * 512) return 512;
+  if ((long)B * Hkv >= 64) return 256;
   return 512;
 }
 

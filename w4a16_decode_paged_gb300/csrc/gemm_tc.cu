@@ -1016,23 +1016,47 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
 // argmax over fp32 logit rows (lowest index on ties), optional fp16 copy
 // ---------------------------------------------------------------------------
 namespace w4 {
-__global__ void __launch_bounds__(256) w4pg_argmax_rows(const float* __restrict__ logits, int V, int32_t* tokens,
-                                                          __half* logits16, int tag) {
+// One cluster of AM_CL CTAs per row: each CTA takes a contiguous slice of
+// the row (eight loads in flight per thread), the slice maxima meet in the
+// shared memory of CTA 0 of the cluster.  Keys order by value, then by the
+// lower index.
+constexpr int AM_CL = 8;
+constexpr int AM_U = 8;
+__device__ __forceinline__ void st_dsmem_u64(unsigned long long* p, int rank, unsigned long long v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+__global__ void __cluster_dims__(AM_CL, 1, 1) __launch_bounds__(256)
+    w4pg_argmax_rows(const float* __restrict__ logits, int V, int32_t* tokens, __half* logits16, int tag) {
   W4_TRACE_SCOPE(tag);
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
   __shared__ unsigned long long best[8];
-  const int b = blockIdx.x;
+  __shared__ unsigned long long cl_best[AM_CL];
+  const int b = blockIdx.y, rank = blockIdx.x;
+  const int per = (V + AM_CL - 1) / AM_CL;
+  const int lo = rank * per, hi = min(V, lo + per);
   const float* row = logits + (size_t)b * V;
   unsigned long long k = 0;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float v = row[i];
-    if (logits16) logits16[(size_t)b * V + i] = __float2half_rn(v);
-    if (v == v) {  // skip NaN
-      uint32_t bits = __float_as_uint(v);
-      uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
-      const unsigned long long key = ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)i);
-      k = max(k, key);
+  for (int i0 = lo + threadIdx.x; i0 < hi; i0 += 256 * AM_U) {
+    float v[AM_U];
+#pragma unroll
+    for (int u = 0; u < AM_U; ++u) {
+      const int i = i0 + u * 256;
+      v[u] = i < hi ? row[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < AM_U; ++u) {
+      const int i = i0 + u * 256;
+      if (i < hi) {
+        if (logits16) logits16[(size_t)b * V + i] = __float2half_rn(v[u]);
+        if (v[u] == v[u]) {  // skip NaN
+          const uint32_t bits = __float_as_uint(v[u]);
+          const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+          k = max(k, ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)i));
+        }
+      }
     }
   }
 #pragma unroll
@@ -1042,13 +1066,19 @@ __global__ void __launch_bounds__(256) w4pg_argmax_rows(const float* __restrict_
   if (threadIdx.x == 0) {
     unsigned long long m = 0;
     for (int w = 0; w < 8; ++w) m = max(m, best[w]);
+    st_dsmem_u64(&cl_best[rank], 0, m);
+  }
+  cluster_sync();  // every slice maximum is in CTA 0's shared memory
+  if (rank == 0 && threadIdx.x == 0) {
+    unsigned long long m = 0;
+    for (int r = 0; r < AM_CL; ++r) m = max(m, cl_best[r]);
     tokens[b] = m ? (int32_t)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull)) : -1;
   }
 }
 
 int launch_argmax_rows(const float* logits, int B, int V, int32_t* tokens, __half* logits16, cudaStream_t s,
                        int tag) {
-  cudaError_t e = launch_pdl(w4pg_argmax_rows, dim3(B), dim3(256), 0, s, logits, V, tokens, logits16, tag);
+  cudaError_t e = launch_pdl(w4pg_argmax_rows, dim3(AM_CL, B), dim3(256), 0, s, logits, V, tokens, logits16, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "argmax launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
@@ -1173,6 +1203,7 @@ extern "C" int argmax_rows(const float* logits, int B, int vocab, int32_t* token
                            w4a16_stream_t stream) {
   W4_CHECK_ARG(logits && tokens_out, "argmax_rows: null pointer");
   W4_CHECK_ARG(B >= 1 && vocab >= 1, "argmax_rows: sizes must be positive");
+  W4_CHECK_SHAPE(B <= 65535, "argmax_rows: B=%d > 65535", B);
   return launch_argmax_rows(logits, B, vocab, tokens_out, reinterpret_cast<__half*>(logits16), (cudaStream_t)stream,
                             0);
 }
