@@ -50,12 +50,13 @@ namespace w4 {
 
 constexpr int TC_M = 128;      // weight rows per tile (MMA M)
 constexpr int TC_N = 32;       // batch columns (MMA N) of the decode-batch shape
-constexpr int TC_K = 64;       // K per stage
-constexpr int TC_ACOLS = 32;   // tensor-memory columns of one A buffer (128 rows x 64 k fp16)
+constexpr int TC_K = 128;      // K per stage: one scale group
+constexpr int TC_KH = 64;      // K of one 128-byte swizzled half of a stage's fp16 tiles
+constexpr int TC_ACOLS = 64;   // tensor-memory columns of one A buffer (128 rows x 128 k fp16)
 constexpr int TC_EXP_WARPS = 4;                  // warps that expand int4 codes into tensor memory
 constexpr int TC_READERS = 256;                  // threads that read the group sums and run the epilogue
 constexpr int TC_THREADS_WS = 64 + 32 * TC_EXP_WARPS + TC_READERS;  // + producer warp + MMA warp
-constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 16 KB fp16 A tile per matrix per stage
+constexpr int TC_A_BYTES = TC_M * TC_K * 2;  // 32 KB fp16 A tile per matrix per stage (two halves)
 constexpr unsigned long long TC_TIMEOUT_NS = 2000000000ull;
 
 constexpr uint32_t pow2_at_least(uint32_t v) {
@@ -70,24 +71,29 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
 template <bool INT4, bool SILU, int NC>
 struct TcShape {
   static constexpr int NA = SILU ? 2 : 1;                                   // weight matrices per tile
-  static constexpr uint32_t A_RAW = INT4 ? NA * TC_M * 32 : TC_A_BYTES;     // A bytes per ring slot
+  static constexpr uint32_t A_TX = INT4 ? TC_M * (TC_K / 2) : TC_A_BYTES;   // A bytes per matrix per stage
+  static constexpr uint32_t A_RAW = NA * A_TX;                              // A bytes per ring slot
+  static constexpr uint32_t B_HALF = NC * TC_KH * 2;                        // one swizzled half of B
   static constexpr uint32_t B_BYTES = NC * TC_K * 2;                        // activation tile per stage
   static constexpr uint32_t SLOT = A_RAW + B_BYTES;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
   // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators (8
-  // measured no faster than 4).
-  static constexpr int TM_BUDGET = 512;
+  // measured no faster than 4); within 256 columns where two fit, so that
+  // two CTAs can share an SM.
+  static constexpr int NAB_256 = (256 - 2 * NA * NC) / (NA * TC_ACOLS);
+  static constexpr int TM_BUDGET = NAB_256 >= 2 ? 256 : 512;
   static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
   static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
   // tensor memory: 2 group accumulators x NA x NC columns, and (int4) NAB A
   // buffers x NA x 32 columns of exact codes, rounded up to a power of two
   static constexpr uint32_t TMEM_COLS =
       pow2_at_least(INT4 ? 2 * NA * NC + NAB * NA * TC_ACOLS : 2 * NA * NC);
-  // ring stages: as many as the shared memory holds (4 to 24), the weights of
+  // ring stages: as many as the shared memory holds (4 to 12), the weights of
   // that many stages in flight per CTA hide the memory latency
   static constexpr int SMEM_BUDGET = TMEM_COLS <= 256 ? 110 * 1024 : 200 * 1024;
-  static constexpr int S = (int)(SMEM_BUDGET / SLOT) < 4 ? 4 : ((int)(SMEM_BUDGET / SLOT) > 24 ? 24 : (int)(SMEM_BUDGET / SLOT));
+  static constexpr int S = (int)(SMEM_BUDGET / SLOT) < 4 ? 4 : ((int)(SMEM_BUDGET / SLOT) > 12 ? 12 : (int)(SMEM_BUDGET / SLOT));
+  static_assert(A_RAW % 1024 == 0 && B_HALF % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
   static constexpr size_t SMEM = (size_t)S * SLOT + 1024;
   static_assert(NC % 32 == 0 && NC <= 128, "NC: 32, 64 or 128 columns");
   static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
@@ -183,27 +189,24 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
 }
 
 #ifdef W4A16_TRACE
-// Trace builds: per-stage event times of CTA 0 of the last launch
-// (w4a16_trace_tc_timeline): 0 producer issued, 1 expander starts, 2 expander
-// released, 3 MMA operands ready, 4 MMA issued, 5 reader saw the group done
-// (global timer, ns); 6..9 the MMA warp in SM clock cycles: operands ready,
-// fence done, MMAs issued, commits issued.
-constexpr int TC_TL_EVENTS = 10, TC_TL_STAGES = 512;
+// Trace builds: per-stage event times of CTA 0 of the last launch, in SM
+// clock cycles (one SM, so the roles' clocks agree; w4a16_trace_tc_timeline):
+//   0 producer issued the stage's copies      5 MMA warp at the loop top
+//   1 expander: A buffer free                 6 MMA: operands ready
+//   2 expander: the stage's copies landed     7 MMA: accumulator buffer free
+//   3 expander: codes stored                  8 MMA: fence done
+//   4 expander: stage released                9 MMA: MMAs issued
+//  10 MMA: commits issued, 11 reader: before the group wait, 12 group done
+//  seen, 13 buffer read and released
+constexpr int TC_TL_EVENTS = 14, TC_TL_STAGES = 512;
 __device__ unsigned long long g_tc_timeline[TC_TL_EVENTS][TC_TL_STAGES];
-#define TC_TL(ev, s)                                                        \
-  do {                                                                       \
-    if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = tc_now(); \
-  } while (0)
-#define TC_TLC(ev, s)                                                              \
+#define TC_TL(ev, s)                                                              \
   do {                                                                             \
     if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = clock64();   \
   } while (0)
 #else
 #define TC_TL(ev, s) \
   do {               \
-  } while (0)
-#define TC_TLC(ev, s) \
-  do {                \
   } while (0)
 #endif
 
@@ -217,12 +220,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// The mbarrier gets one arrival once all of this thread's earlier cp.async
-// copies have landed (the arrival is counted in the barrier's init count).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -230,22 +227,24 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(TC_READERS) : "memory"); }
 
-// Warp roles: warp 0 copies (producer), warp 1 lane 0 issues the MMAs,
-// warps 2..5 (the expanders, 128 threads, one weight row each) expand the
-// int4 codes of their row into tensor-memory A buffers, up to NAB stages
-// ahead of the tensor core, and warps 6..13 (the readers, 256 threads: a row
-// and half of the batch columns each) read each group's sums from tensor
-// memory as soon as the tensor core has finished the group and run the
-// epilogue.  Stage s of this CTA's work uses ring slot s % TS and A buffer
-// s % NAB; its group is s / 2 (work items have an even number of stages).
-// The roles only meet at mbarriers:
-//   full[slot]   producer's copies of the slot landed           (32 arrivals)
+// Warp roles: warp 0 lane 0 issues the bulk-tensor copies (producer), warp
+// 1 lane 0 issues the MMAs, warps 2..5 (the expanders, 128 threads, one
+// weight row each) expand the int4 codes of their row into tensor-memory A
+// buffers, up to NAB stages ahead of the tensor core, and warps 6..13 (the
+// readers, 256 threads: a row and half of the batch columns each) read each
+// stage's sums from tensor memory as soon as the tensor core has finished
+// the stage and run the epilogue.  A stage is 128 k, one scale group: eight
+// MMAs per weight matrix between one barrier wait, one fence and two
+// commits of the MMA warp, whose loop is what bounds the kernel at small N.
+// Stage s of this CTA's work uses ring slot s % TS, A buffer s % NAB and
+// accumulator buffer s % 2.  The roles only meet at mbarriers:
+//   full[slot]   the slot's bulk-tensor copies landed            (1 + tx bytes)
 //   empty[slot]  expanders done with the raw A, MMAs with the B  (128 + 1; dense: 1);
 //                its phase for stage s also tells the expanders that A
 //                buffer s % NAB is free again at stage s + NAB
 //   afull[b]     expanders wrote A buffer b                     (128)
-//   gfull[b]     MMAs of the group in tensor-memory buffer b    (1, commit)
-//   gempty[b]    readers read tensor-memory buffer b            (256)
+//   gfull[b]     MMAs of the stage in accumulator buffer b      (1, commit)
+//   gempty[b]    readers read accumulator buffer b              (256)
 template <bool INT4, bool SILU, int NC>
 __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_COLS <= 256 ? 2 : 1)
     w4pg_tc_batch(const __grid_constant__ TcArgs a) {
@@ -269,23 +268,16 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   __shared__ volatile int s_fail;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int K = a.K, M = a.M, N = a.N;
+  const int K = a.K, N = a.N;
   const int nst = K / TC_K, ps = a.per_split, ks = a.ksplit;
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nwork = ntiles * ks;
   const unsigned long long wl = a.wait_limit_ns;
   W4_TRACE_SCOPE(a.tag);
-#ifdef W4A16_TRACE
-  // trace builds: total time the producer spends issuing its bulk-tensor
-  // copies, and the time an expander (warp 2, lane 0) and a reader (the
-  // first) spend waiting
-  __shared__ unsigned long long s_tmark[3];
-  if (tid == 0) s_tmark[0] = s_tmark[1] = s_tmark[2] = 0ull;
-#endif
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
-  // columns: [0, 2 NA NC) group accumulators; then (int4) A buffer ab, matrix g
-  // at 2 NA NC + (ab NA + g) 32
+  // columns: [0, 2 NA NC) accumulators; then (int4) A buffer ab, matrix g at
+  // 2 NA NC + (ab NA + g) TC_ACOLS
   constexpr uint32_t TM_A = 2 * NA * NC;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -295,12 +287,10 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   }
   if (tid == 32) {
     for (int i = 0; i < TS; ++i) {
-      mbar_init(&full[i], a.tma ? 1 : 32);
-      mbar_init(&empty[i], (INT4 ? 32 * TC_EXP_WARPS : 0) + 1);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], (INT4 ? 128 : 0) + 1);
     }
-    for (int i = 0; i < NAB; ++i) {
-      mbar_init(&afull[i], 32 * TC_EXP_WARPS);
-    }
+    for (int i = 0; i < NAB; ++i) mbar_init(&afull[i], 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&gfull[i], 1);
       mbar_init(&gempty[i], TC_READERS);
@@ -334,87 +324,14 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     }
     return true;
   };
-  // A-operand row `row` of tile `tile` (weights): packed codes and scales
-  auto row_ptrs = [&](int tile, int row_l, const uint32_t* (&q)[NA], const __half* (&sp)[NA], bool& ok) {
-    const int row = tile * TC_M + row_l;
-    ok = row < N;
-    const int rr = ok ? row : 0;
-    if (SILU) {
-#pragma unroll
-      for (int g = 0; g < NA; ++g) {
-        q[g] = a.seg[g].qw + (size_t)rr * (K / 8);
-        sp[g] = a.seg[g].s + (size_t)rr * (K / 128);
-      }
-    } else {
-      int r = rr, si = 0;
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (si < a.nseg - 1 && r >= a.seg[si].rows) { r -= a.seg[si].rows; ++si; }
-      q[0] = a.seg[si].qw + (size_t)r * (K / 8);
-      sp[0] = a.seg[si].s + (size_t)r * (K / 128);
-    }
-  };
 
   if (warp == 0) {
     // =========================== producer ===================================
+    // Lane 0 copies a stage's weight tiles (int4: 128 rows x 64 bytes of
+    // codes; dense: two swizzled 64-k halves) and its activation tile (two
+    // swizzled halves); the slot's barrier expects their bytes.
     Cursor cur;
     c_init(cur);
-    // int4: lane pairs share a row (the two 16-byte halves of its 32 bytes per
-    // stage), so one copy instruction covers 16 rows with full sectors; this
-    // lane's rows are lane / 2 + 16 j.  Dense: eight lanes cover a row's 128
-    // bytes, rows lane / 8 + 4 j.
-    const uint32_t* q[8][NA];
-    bool rok[8];
-    const int hh = lane & 1;
-    int tile0 = 0;
-    auto item_rows = [&]() {
-      const int tile = cur.work / ks;
-      tile0 = tile * TC_M;
-      if (INT4) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const __half* sp[NA];
-          row_ptrs(tile, (lane >> 1) + 16 * j, q[j], sp, rok[j]);
-        }
-      }
-    };
-    if (cur.work < nwork) item_rows();
-    auto load_a = [&](int slot) {
-      unsigned char* sa = ring + slot * SH::SLOT;
-      const int k0 = cur.st * TC_K;
-      if (INT4) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int row_l = (lane >> 1) + 16 * j;
-#pragma unroll
-          for (int g = 0; g < NA; ++g)
-            cp_async16_zfill(sa + (g * TC_M + row_l) * 32 + hh * 16, q[j][g] + k0 / 8 + 4 * hh, rok[j]);
-        }
-      } else {
-        const int w = lane & 7;
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-          const int row_l = (lane >> 3) + 4 * j;
-          const int row = tile0 + row_l;
-          const bool ok = row < N;
-          cp_async16_zfill(sa + tc_off(row_l, w), a.w16 + (size_t)(ok ? row : 0) * K + k0 + 8 * w, ok);
-        }
-      }
-    };
-    auto load_b = [&](int slot, int st) {
-      unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
-#pragma unroll 8
-      for (int i = 0; i < NC / 4; ++i) {
-        const int c = lane + 32 * i;
-        const int m = c >> 3, w = c & 7;
-        const bool ok = m < M;
-        cp_async16_zfill(sb + tc_off(m, w), a.x + (size_t)(ok ? m : 0) * K + st * TC_K + 8 * w, ok);
-      }
-    };
-    // TMA: lane 0 copies a stage's weight tiles and activation tile with one
-    // bulk-tensor copy each; the slot's barrier expects their bytes
-    constexpr uint32_t B_TX = SH::B_BYTES;
-    constexpr uint32_t A_TX = INT4 ? (uint32_t)(TC_M * 32) : (uint32_t)TC_A_BYTES;  // per matrix
     int tm_map[NA], tm_row = 0;  // the item's weight map per matrix and its first row in it
     auto item_tma = [&]() {
       const int r0 = (cur.work / ks) * TC_M;
@@ -433,156 +350,113 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     auto tma_a = [&](int slot, int st) {
       unsigned char* sa = ring + slot * SH::SLOT;
 #pragma unroll
-      for (int g = 0; g < NA; ++g)
-        tma_load_2d(sa + g * (int)A_TX, &a.tm_w[tm_map[g]], INT4 ? st * (TC_K / 8) : st * TC_K, tm_row, &full[slot]);
+      for (int g = 0; g < NA; ++g) {
+        if (INT4) {
+          tma_load_2d(sa + g * SH::A_TX, &a.tm_w[tm_map[g]], st * (TC_K / 8), tm_row, &full[slot]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sa + h * (TC_A_BYTES / 2), &a.tm_w[tm_map[g]], st * TC_K + h * TC_KH, tm_row, &full[slot]);
+        }
+      }
     };
     auto tma_b = [&](int slot, int st) {
-      tma_load_2d(ring + slot * SH::SLOT + SH::A_RAW, &a.tm_x, st * TC_K, 0, &full[slot]);
+      unsigned char* sb = ring + slot * SH::SLOT + SH::A_RAW;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) tma_load_2d(sb + h * SH::B_HALF, &a.tm_x, st * TC_K + h * TC_KH, 0, &full[slot]);
     };
-    if (a.tma) {
-      if (cur.work < nwork) item_tma();
-      int pro_st[TS];
-      int npro = 0;
-      {
-        Cursor c2 = cur;
-        for (int i = 0; i < TS && c2.work < nwork; ++i) {
-          if (i > 0 && c2.st == c2.begin) break;  // a new item inside the prologue: stop
-          pro_st[i] = c2.st;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full[i], NA * A_TX + B_TX);
-            tma_a(i, c2.st);
-          }
-          ++npro;
-          c_next(c2);
-        }
-      }
-      pdl_wait_then_trigger();
-      W4_TRACE_WAITED();
-      if (lane == 0)
-        for (int i = 0; i < npro; ++i) tma_b(i, pro_st[i]);
-      for (int i = 0; i < npro; ++i)
-        if (c_next(cur) && cur.work < nwork) item_tma();
-      for (uint32_t s = npro; cur.work < nwork; ++s) {
-        const int slot = s % TS;
-        if (s >= TS && !tcw_wait(&empty[slot], ((s / TS) - 1) & 1, &s_fail, wl)) break;
-        if (lane == 0) {
-#ifdef W4A16_TRACE
-          const unsigned long long tw0 = tc_now();
-#endif
-          mbar_arrive_expect_tx(&full[slot], NA * A_TX + B_TX);
-          tma_a(slot, cur.st);
-          tma_b(slot, cur.st);
-#ifdef W4A16_TRACE
-          s_tmark[0] += tc_now() - tw0;
-#endif
-          TC_TL(0, s);
-        }
-        __syncwarp();
-        if (c_next(cur) && cur.work < nwork) item_tma();
-      }
-    } else {
+    if (cur.work < nwork) item_tma();
     // prologue: the weights of the first stages before the dependency wait
     int pro_st[TS];
     int npro = 0;
     {
       Cursor c2 = cur;
       for (int i = 0; i < TS && c2.work < nwork; ++i) {
-        if (i > 0 && c2.st == c2.begin) {  // a new item inside the prologue: stop (its rows differ)
-          break;
-        }
+        if (i > 0 && c2.st == c2.begin) break;  // a new item inside the prologue: stop (its rows differ)
         pro_st[i] = c2.st;
-        cur = c2;
-        load_a(i);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[i], SH::A_RAW + SH::B_BYTES);
+          tma_a(i, c2.st);
+        }
         ++npro;
         c_next(c2);
       }
     }
     pdl_wait_then_trigger();
     W4_TRACE_WAITED();
-    for (int i = 0; i < npro; ++i) {
-      load_b(i, pro_st[i]);
-      cp_async_mbar_arrive(&full[i]);
-    }
-    // restore the cursor to the stage after the prologue
-    c_init(cur);
-    if (cur.work < nwork) item_rows();
+    if (lane == 0)
+      for (int i = 0; i < npro; ++i) tma_b(i, pro_st[i]);
     for (int i = 0; i < npro; ++i)
-      if (c_next(cur) && cur.work < nwork) item_rows();
+      if (c_next(cur) && cur.work < nwork) item_tma();
     for (uint32_t s = npro; cur.work < nwork; ++s) {
       const int slot = s % TS;
-#ifdef W4A16_TRACE
-      const unsigned long long tw0 = tc_now();
-#endif
       if (s >= TS && !tcw_wait(&empty[slot], ((s / TS) - 1) & 1, &s_fail, wl)) break;
-#ifdef W4A16_TRACE
-      if (lane == 0) s_tmark[0] += tc_now() - tw0;
-#endif
-      load_a(slot);
-      load_b(slot, cur.st);
-      cp_async_mbar_arrive(&full[slot]);
-      if (c_next(cur) && cur.work < nwork) item_rows();
-    }
-    cp_async_wait<0>();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[slot], SH::A_RAW + SH::B_BYTES);
+        tma_a(slot, cur.st);
+        tma_b(slot, cur.st);
+        TC_TL(0, s);
+      }
+      __syncwarp();
+      if (c_next(cur) && cur.work < nwork) item_tma();
     }
   } else if (warp == 1) {
     // =========================== MMA issuer =================================
-    // The whole warp runs the loop (waits, descriptors: warp-uniform values);
-    // lane 0 issues the MMAs and the commits.
+    // The whole warp runs the loop (waits: warp-uniform values); lane 0
+    // issues the MMAs and the commits.
     pdl_wait_then_trigger();
     Cursor cur;
     c_init(cur);
     uint32_t s = 0;
     for (; cur.work < nwork; ++s) {
-      const int slot = s % TS, ab = s % NAB;
-      const uint32_t grp = s >> 1;
-      const bool gfirst = (s & 1) == 0;
+      const int slot = s % TS, ab = s % NAB, gb = s & 1;
+      if (lane == 0) TC_TL(5, s);
       // int4: the expanders saw the slot's copies land before they filled A
       // buffer ab, so its barrier (acquired here) covers the B tile too
       bool ok = INT4 ? tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl) : tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl);
-      if (gfirst && grp >= 2 && ok) ok = tcw_wait(&gempty[grp & 1], ((grp - 2) >> 1) & 1, &s_fail, wl);
-      if (lane == 0) TC_TLC(6, s);
+      if (lane == 0) TC_TL(6, s);
+      if (s >= 2 && ok) ok = tcw_wait(&gempty[gb], ((s - 2) >> 1) & 1, &s_fail, wl);
+      if (lane == 0) TC_TL(7, s);
       if (!__all_sync(0xffffffffu, ok)) break;
-      if (lane == 0) TC_TL(3, s);
-      // per-lane copies write the ring through the generic proxy, which the
-      // MMA reads through the async proxy; bulk-tensor copies need no fence
-      if (!a.tma) fence_proxy_async_smem();
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (lane == 0) TC_TLC(7, s);
+      if (lane == 0) TC_TL(8, s);
       unsigned char* sl = ring + slot * SH::SLOT;
-      const uint32_t gbase = tmem + (grp & 1) * (NA * NC);
-      const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
+      const uint32_t dbase = tmem + gb * (NA * NC);
       if (lane == 0) {
+        const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
+        const uint64_t bd1 = tc_desc(smem_u32(sl + SH::A_RAW + SH::B_HALF));
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
-            const uint64_t bd = bd0 + (uint64_t)((kk * 32) >> 4);  // next 16-k slice of B
-            const uint32_t accum = (!gfirst || kk > 0) ? 1u : 0u;
+            // 16-k slice kk: half kk / 4 of the swizzled B tile, 32 bytes per slice
+            const uint64_t bd = (kk < 4 ? bd0 : bd1) + (uint64_t)(((kk & 3) * 32) >> 4);
+            const uint32_t accum = kk > 0 ? 1u : 0u;
             if (INT4) {
               // A (128 x 16 exact codes) from tensor memory: 8 columns per 16 k
               const uint32_t at = tmem + TM_A + (uint32_t)((ab * NA + g) * TC_ACOLS + kk * 8);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * NC)),
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dbase + (uint32_t)(g * NC)),
                   "r"(at), "l"(bd), "r"(tc_idesc<NC>()), "r"(accum)
                   : "memory");
             } else {
-              const uint64_t ad = tc_desc(smem_u32(sl)) + (uint64_t)((kk * 32) >> 4);
+              const uint64_t ad =
+                  tc_desc(smem_u32(sl + (kk < 4 ? 0 : TC_A_BYTES / 2))) + (uint64_t)(((kk & 3) * 32) >> 4);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(gbase + (uint32_t)(g * NC)),
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dbase + (uint32_t)(g * NC)),
                   "l"(ad), "l"(bd), "r"(tc_idesc<NC>()), "r"(accum)
                   : "memory");
             }
           }
         }
-        TC_TLC(8, s);
-        // one commit frees the ring slot (producer) and, through it, the A
-        // buffer (expanders wait on the slot of the stage NAB back)
+        TC_TL(9, s);
+        // the ring slot (producer) and, through it, A buffer ab (expanders
+        // wait on the slot of the stage NAB back); the stage's sums (readers)
         tc_commit(&empty[slot]);
-        if (!gfirst) tc_commit(&gfull[grp & 1]);
-        TC_TLC(9, s);
-        TC_TL(4, s);
+        tc_commit(&gfull[gb]);
+        TC_TL(10, s);
       }
       __syncwarp();
       c_next(cur);
@@ -598,20 +472,23 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     }
   } else if (warp < 2 + TC_EXP_WARPS) {
     // =========================== expanders ==================================
-    // Each thread expands its weight row's 64 codes per stage (per matrix)
+    // Each thread expands its weight row's 128 codes per stage (per matrix)
     // into A buffer s % NAB, up to NAB stages ahead of the tensor core.
     pdl_wait_then_trigger();
     if (INT4) {
       const int row_l = 32 * (warp & 3) + lane;  // tensor-memory lanes of this warp's quadrant
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A;
-      // The tensor-memory stores of a stage complete while the next stage is
-      // expanded: its buffer and ring slot are released one iteration later.
-      auto release = [&](uint32_t ps) {
+      // With more than two A buffers the tensor-memory stores of a stage
+      // complete while the expanders wait for the next stage, and the stage
+      // is released one iteration later; with two, that wait is on the MMAs
+      // of the stage before, so the stage is released at once.
+      constexpr bool LAZY = NAB > 2;
+      auto release = [&](uint32_t ps_) {
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        mbar_arrive(&afull[ps % NAB]);
-        mbar_arrive(&empty[ps % TS]);
-        if (warp == 2 && lane == 0) TC_TL(2, ps);
+        mbar_arrive(&afull[ps_ % NAB]);
+        mbar_arrive(&empty[ps_ % TS]);
+        if (warp == 2 && lane == 0) TC_TL(4, ps_);
       };
       Cursor cur;
       c_init(cur);
@@ -621,65 +498,62 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         const int slot = s % TS, ab = s % NAB;
         // the A buffer's previous MMAs are done, the slot's copies landed
         // (the MMA's commit to that stage's ring slot also covers A buffer ab)
-#ifdef W4A16_TRACE
-        const unsigned long long tw0 = tc_now();
-#endif
         if (s >= NAB && !tcw_wait(&empty[(s - NAB) % TS], ((s - NAB) / TS) & 1, &s_fail, wl)) break;
-        if (!tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl)) break;
-#ifdef W4A16_TRACE
-        if (warp == 2 && lane == 0) s_tmark[1] += tc_now() - tw0;
-#endif
         if (warp == 2 && lane == 0) TC_TL(1, s);
+        if (!tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl)) break;
+        if (warp == 2 && lane == 0) TC_TL(2, s);
         const unsigned char* sl = ring + slot * SH::SLOT;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // exact codes of this row's 64 k per matrix: 32 columns of fp16 pairs in k order
-        uint4 c[NA][8];
+        if (LAZY && pend) release(s - 1);
+        // exact codes of this row's 128 k per matrix, 64 k (32 columns of
+        // fp16 pairs in k order) at a time
 #pragma unroll
         for (int g = 0; g < NA; ++g) {
-          const uint4 r0 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32);
-          const uint4 r1 = *reinterpret_cast<const uint4*>(sl + (g * TC_M + row_l) * 32 + 16);
-          c[g][0] = codes_word(r0.x);
-          c[g][1] = codes_word(r0.y);
-          c[g][2] = codes_word(r0.z);
-          c[g][3] = codes_word(r0.w);
-          c[g][4] = codes_word(r1.x);
-          c[g][5] = codes_word(r1.y);
-          c[g][6] = codes_word(r1.z);
-          c[g][7] = codes_word(r1.w);
-        }
-        if (pend) release(s - 1);
 #pragma unroll
-        for (int g = 0; g < NA; ++g) {
-          const uint32_t ta = lane_base + (uint32_t)((ab * NA + g) * TC_ACOLS);
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-              "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
-              "r"(c[g][0].x), "r"(c[g][0].y), "r"(c[g][0].z), "r"(c[g][0].w), "r"(c[g][1].x), "r"(c[g][1].y),
-              "r"(c[g][1].z), "r"(c[g][1].w), "r"(c[g][2].x), "r"(c[g][2].y), "r"(c[g][2].z), "r"(c[g][2].w),
-              "r"(c[g][3].x), "r"(c[g][3].y), "r"(c[g][3].z), "r"(c[g][3].w), "r"(c[g][4].x), "r"(c[g][4].y),
-              "r"(c[g][4].z), "r"(c[g][4].w), "r"(c[g][5].x), "r"(c[g][5].y), "r"(c[g][5].z), "r"(c[g][5].w),
-              "r"(c[g][6].x), "r"(c[g][6].y), "r"(c[g][6].z), "r"(c[g][6].w), "r"(c[g][7].x), "r"(c[g][7].y),
-              "r"(c[g][7].z), "r"(c[g][7].w)
-              : "memory");
+          for (int h = 0; h < 2; ++h) {
+            const unsigned char* src = sl + (g * TC_M + row_l) * (TC_K / 2) + h * 32;
+            const uint4 r0 = *reinterpret_cast<const uint4*>(src);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(src + 16);
+            uint4 c[8];
+            c[0] = codes_word(r0.x);
+            c[1] = codes_word(r0.y);
+            c[2] = codes_word(r0.z);
+            c[3] = codes_word(r0.w);
+            c[4] = codes_word(r1.x);
+            c[5] = codes_word(r1.y);
+            c[6] = codes_word(r1.z);
+            c[7] = codes_word(r1.w);
+            const uint32_t ta = lane_base + (uint32_t)((ab * NA + g) * TC_ACOLS + h * 32);
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+                "r"(c[0].x), "r"(c[0].y), "r"(c[0].z), "r"(c[0].w), "r"(c[1].x), "r"(c[1].y), "r"(c[1].z), "r"(c[1].w),
+                "r"(c[2].x), "r"(c[2].y), "r"(c[2].z), "r"(c[2].w), "r"(c[3].x), "r"(c[3].y), "r"(c[3].z), "r"(c[3].w),
+                "r"(c[4].x), "r"(c[4].y), "r"(c[4].z), "r"(c[4].w), "r"(c[5].x), "r"(c[5].y), "r"(c[5].z), "r"(c[5].w),
+                "r"(c[6].x), "r"(c[6].y), "r"(c[6].z), "r"(c[6].w), "r"(c[7].x), "r"(c[7].y), "r"(c[7].z), "r"(c[7].w)
+                : "memory");
+          }
         }
+        if (warp == 2 && lane == 0) TC_TL(3, s);
+        if (!LAZY) release(s);
         pend = true;
         c_next(cur);
       }
-      if (pend && cur.work >= nwork) release(s - 1);
+      if (LAZY && pend && cur.work >= nwork) release(s - 1);
     }
   } else {
     // =========================== accumulators ===============================
-    // Group by group (two stages each, in the order the tensor core finishes
-    // them): tcgen05.ld of this row's CPT columns of the group's buffer, times
-    // the group's scale into fp32 registers; at the end of a work item the
-    // epilogue.  They run up to one group behind the tensor core.
+    // Stage by stage (one scale group each, in the order the tensor core
+    // finishes them): tcgen05.ld of this row's CPT columns of the stage's
+    // buffer, times the group's scale into fp32 registers; at the end of a
+    // work item the epilogue.  They run up to one stage behind the tensor core.
     pdl_wait_then_trigger();
     const int r = tid - 64 - 32 * TC_EXP_WARPS;   // 0..255
     const int half = r >> 7;                      // batch columns CPT h .. CPT h + CPT - 1
     const int row_l = 32 * (warp & 3) + lane;     // tensor-memory lanes of this warp's quadrant
+    const int M = a.M;
     Cursor cur;
     c_init(cur);
-    const uint32_t* q[NA];
     const __half* sp[NA];
     bool rok = false;
     __half sreg[NA];  // the scales of the group being read
@@ -689,16 +563,28 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
 
-    // add tensor-memory group `grp` (this row, CPT columns) times the scales
-    auto tm_read = [&](uint32_t grp) {
-#ifdef W4A16_TRACE
-      const unsigned long long tw0 = tc_now();
-#endif
-      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[grp & 1], (grp >> 1) & 1, &s_fail, wl));
-#ifdef W4A16_TRACE
-      if (r == 0) s_tmark[2] += tc_now() - tw0;
-#endif
-      if (r == 0) TC_TL(5, grp);
+    // the scales of tile `tile`, row row_l
+    auto scale_rows = [&](int tile) {
+      const int row = tile * TC_M + row_l;
+      rok = row < N;
+      const int rr = rok ? row : 0;
+      if (SILU) {
+#pragma unroll
+        for (int g = 0; g < NA; ++g) sp[g] = a.seg[g].s + (size_t)rr * (K / 128);
+      } else if (INT4) {
+        int q = rr, si = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (si < a.nseg - 1 && q >= a.seg[si].rows) { q -= a.seg[si].rows; ++si; }
+        sp[0] = a.seg[si].s + (size_t)q * (K / 128);
+      }
+    };
+
+    // add tensor-memory stage `st_i` (this row, CPT columns) times the scales
+    auto tm_read = [&](uint32_t st_i) {
+      if (r == 0) TC_TL(11, st_i);
+      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[st_i & 1], (st_i >> 1) & 1, &s_fail, wl));
+      if (r == 0) TC_TL(12, st_i);
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
@@ -707,7 +593,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
 #pragma unroll
           for (int c0 = 0; c0 < CPT; c0 += 16) {
             uint32_t v[16];
-            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (grp & 1) * (NA * NC) +
+            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (st_i & 1) * (NA * NC) +
                                    (uint32_t)(g * NC + half * CPT + c0);
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -722,7 +608,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       }
-      mbar_arrive(&gempty[grp & 1]);
+      mbar_arrive(&gempty[st_i & 1]);
+      if (r == 0) TC_TL(13, st_i);
     };
 
     auto epilogue = [&](int work) {
@@ -794,10 +681,10 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       }
     };
 
-    uint32_t grp = 0;  // groups read so far (all items): buffer grp & 1
+    uint32_t grp = 0;  // stages read so far (all items): buffer grp & 1
     while (cur.work < nwork) {
-      if (INT4) row_ptrs(cur.work / ks, row_l, q, sp, rok);
-      const int g0 = cur.begin >> 1, ng = (cur.end - cur.begin) >> 1;
+      if (INT4) scale_rows(cur.work / ks);
+      const int g0 = cur.begin, ng = cur.end - cur.begin;  // one scale group per stage
       // scales of the next two groups in flight (requested two groups ahead)
       __half snext[NA], snext2[NA];
 #pragma unroll
@@ -830,13 +717,6 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     }
   }
   __syncthreads();
-#ifdef W4A16_TRACE
-  if (tid == 0) {
-    W4_TRACE_SET_MARK(0, s_tmark[0]);
-    W4_TRACE_SET_MARK(1, s_tmark[1]);
-    W4_TRACE_SET_MARK(2, s_tmark[2]);
-  }
-#endif
   if (s_fail && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -888,21 +768,21 @@ static int tc_slots(bool int4, bool silu, int nc) {
   return per * num_sms();
 }
 
-// Split of K: the split length (even number of stages, so splits start on a
-// scale group) that minimises waves x (stages per item + a per-item
-// overhead of ~4 stages) over the CTAs that fit on the GPU.
+// Split of K: the split length (in stages, each a scale group) that
+// minimises waves x (stages per item + a per-item overhead of ~2 stages)
+// over the CTAs that fit on the GPU.
 void tc_plan(int N, int K, bool int4, bool silu, bool allow_split, int* ksplit, int* per_split, int nc) {
   const int ntiles = (N + TC_M - 1) / TC_M;
   const int nst = K / TC_K;
   const int slots = tc_slots(int4, silu, nc);
   int best_ps = nst, best_ks = 1;
   long best = -1;
-  for (int p = nst; p >= 2; p -= 2) {
+  for (int p = nst; p >= 1; --p) {
     const int k = (nst + p - 1) / p;
     if (k > 1 && (!allow_split || (size_t)ntiles * 4 > TC_TICKET_BYTES)) continue;
     const long items = (long)ntiles * k;
     const long waves = (items + slots - 1) / slots;
-    const long cost = waves * (p + 4);
+    const long cost = waves * (p + 2);
     if (best < 0 || cost < best) {
       best = cost;
       best_ps = p;
@@ -950,12 +830,13 @@ static bool tma_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps for the launch (a.tma = 1), or a.tma = 0 when some operand
-// does not fit them (a 128-row weight tile across two segments).
-static void tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
-  a.tma = 0;
+// Tensor maps of the launch's operands: activations and dense weights in
+// swizzled 64-k halves, int4 codes in 128-row x 64-byte boxes.  False when
+// the driver gives no encoder or an operand does not fit the boxes (a
+// 128-row weight tile across two segments).
+static bool tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
   bool ok = tma_map_2d(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
-                       (uint64_t)a.K * 2, TC_K, (uint32_t)nc, CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)a.K * 2, TC_KH, (uint32_t)nc, CU_TENSOR_MAP_SWIZZLE_128B);
   if (int4) {
     const int nm = silu ? 2 : a.nseg;
     for (int i = 0; i + 1 < nm && !silu; ++i) ok = ok && a.seg[i].rows % TC_M == 0;
@@ -964,9 +845,9 @@ static void tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
                       (uint64_t)a.seg[i].rows, (uint64_t)a.K / 2, TC_K / 8, TC_M, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     ok = ok && tma_map_2d(&a.tm_w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.w16, (uint64_t)a.K, (uint64_t)a.N,
-                          (uint64_t)a.K * 2, TC_K, TC_M, CU_TENSOR_MAP_SWIZZLE_128B);
+                          (uint64_t)a.K * 2, TC_KH, TC_M, CU_TENSOR_MAP_SWIZZLE_128B);
   }
-  a.tma = ok ? 1 : 0;
+  return ok;
 }
 
 #ifdef W4A16_TRACE
@@ -983,13 +864,15 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
   const int maxm = tc_max_rows(int4, silu);
   if (a.M < 1 || a.M > maxm) return set_error(W4A16_ERR_SHAPE, "gemm_tc: M=%d outside 1..%d", a.M, maxm);
   const int nc = tc_cols(a.M, int4, silu);
-  tc_tensor_maps(a, int4, silu, nc);
-  // stages pair into 128-wide groups (the int4 scale group), dense weights too
+  // a stage is one 128-wide group (the int4 scale group), dense weights too
   if (a.K % 128 != 0) return set_error(W4A16_ERR_SHAPE, "gemm_tc: K=%d not a multiple of 128", a.K);
+  if (!tc_tensor_maps(a, int4, silu, nc))
+    return set_error(W4A16_ERR_SHAPE, "gemm_tc: no tensor maps for the operands (weight segments must be "
+                     "multiples of 128 rows, rows 16-byte aligned)");
   if (a.ksplit < 1) return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: ksplit < 1");
   const int nst = a.K / TC_K;
   if (a.per_split <= 0) a.per_split = (nst + a.ksplit - 1) / a.ksplit;
-  if (a.per_split % 2 != 0 || (long)a.per_split * (a.ksplit - 1) >= nst || (long)a.per_split * a.ksplit < nst)
+  if ((long)a.per_split * (a.ksplit - 1) >= nst || (long)a.per_split * a.ksplit < nst)
     return set_error(W4A16_ERR_INVALID_ARG, "gemm_tc: split of %d stages x %d does not tile %d stages", a.per_split,
                      a.ksplit, nst);
   const int ntiles = (a.N + TC_M - 1) / TC_M;

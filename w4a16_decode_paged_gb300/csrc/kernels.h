@@ -46,13 +46,12 @@ struct TcArgs {
   unsigned int* counters;  // split-K tickets, one per 128-row tile (zero before first use)
   int32_t* err_flag;
   int M, K, N, ldy, ksplit, tag;
-  int per_split;           // stages (64 k) per split, even; 0: ceil(stages / ksplit)
+  int per_split;           // stages (128 k, one scale group) per split; 0: ceil(stages / ksplit)
   unsigned long long wait_limit_ns;  // bound of every mbarrier wait (set by the launcher)
   // Bulk-tensor (TMA) copies, set by the launcher: tm_w[i] the weights of
-  // segment i (int4: u32 [rows][K/8], 8 x 128 boxes; dense fp16: [N][K],
+  // segment i (int4: u32 [rows][K/8], 16 x 128 boxes; dense fp16: [N][K],
   // 64 x 128 boxes, 128-byte swizzle), tm_x the activations [M][K] (64 x NC
-  // boxes, 128-byte swizzle).  tma = 0: per-lane 16-byte copies instead.
-  int tma;
+  // boxes, 128-byte swizzle).
   CUtensorMap tm_w[3];
   CUtensorMap tm_x;
 };
