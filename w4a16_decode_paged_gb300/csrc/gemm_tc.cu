@@ -197,16 +197,23 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
 //   3 expander: codes stored                  8 MMA: fence done
 //   4 expander: stage released                9 MMA: MMAs issued
 //  10 MMA: commits issued, 11 reader: before the group wait, 12 group done
-//  seen, 13 buffer read and released
-constexpr int TC_TL_EVENTS = 14, TC_TL_STAGES = 512;
+//  seen, 13 buffer read and released; row 14 by event, once per launch:
+//  0 entry, 1 set up, 2 producer past the dependency wait, 3 MMA warp past
+//  it, 4 readers' epilogue start, 5 partial stored and ticket taken, 6 split
+//  sums added, 7 epilogue end, 8 exit
+constexpr int TC_TL_EVENTS = 15, TC_TL_STAGES = 512;
 __device__ unsigned long long g_tc_timeline[TC_TL_EVENTS][TC_TL_STAGES];
 #define TC_TL(ev, s)                                                              \
   do {                                                                             \
     if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = clock64();   \
   } while (0)
+#define TC_CE(e) TC_TL(14, e)
 #else
 #define TC_TL(ev, s) \
   do {               \
+  } while (0)
+#define TC_CE(e) \
+  do {           \
   } while (0)
 #endif
 
@@ -234,17 +241,19 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 // readers, 256 threads: a row and half of the batch columns each) read each
 // stage's sums from tensor memory as soon as the tensor core has finished
 // the stage and run the epilogue.  A stage is 128 k, one scale group: eight
-// MMAs per weight matrix between one barrier wait, one fence and two
-// commits of the MMA warp, whose loop is what bounds the kernel at small N.
-// Stage s of this CTA's work uses ring slot s % TS, A buffer s % NAB and
-// accumulator buffer s % 2.  The roles only meet at mbarriers:
+// MMAs per weight matrix between one barrier wait, one fence and one commit
+// of the MMA warp, whose loop is what bounds the kernel at small N.  Stage s
+// of this CTA's work uses ring slot s % TS, A buffer s % NAB and accumulator
+// buffer s % 2.  The roles only meet at mbarriers:
 //   full[slot]   the slot's bulk-tensor copies landed            (1 + tx bytes)
-//   empty[slot]  expanders done with the raw A, MMAs with the B  (128 + 1; dense: 1);
+//   empty[slot]  expanders done with the raw A, MMAs done        (128 + 1; dense: 1);
 //                its phase for stage s also tells the expanders that A
-//                buffer s % NAB is free again at stage s + NAB
-//   afull[b]     expanders wrote A buffer b                     (128)
-//   gfull[b]     MMAs of the stage in accumulator buffer b      (1, commit)
-//   gempty[b]    readers read accumulator buffer b              (256)
+//                buffer s % NAB is free again at stage s + NAB, and the
+//                readers that the stage's sums are in tensor memory
+//   afull[b]     stage s = b (mod NAB) may start: expanders wrote A buffer b,
+//                and readers read accumulator buffer s % 2 of stage s - 2
+//                (for s < 2 they arrive at the start)          (128 + 256)
+//   gempty[b]    dense only: readers read accumulator buffer b  (256)
 template <bool INT4, bool SILU, int NC>
 __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_COLS <= 256 ? 2 : 1)
     w4pg_tc_batch(const __grid_constant__ TcArgs a) {
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   constexpr int NAB = SH::NAB;
   constexpr int TS = SH::S;  // ring stages
   static_assert(NAB < TS, "an A buffer is reused before its ring slot");
-  __shared__ __align__(8) uint64_t full[TS], empty[TS], afull[NAB], gfull[2], gempty[2], drain;
+  __shared__ __align__(8) uint64_t full[TS], empty[TS], afull[NAB], gempty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_last, s_rfail;
   __shared__ volatile int s_fail;
@@ -274,6 +283,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   const int nwork = ntiles * ks;
   const unsigned long long wl = a.wait_limit_ns;
   W4_TRACE_SCOPE(a.tag);
+  if (tid == 0) TC_CE(0);
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
   // columns: [0, 2 NA NC) accumulators; then (int4) A buffer ab, matrix g at
@@ -290,11 +300,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], (INT4 ? 128 : 0) + 1);
     }
-    for (int i = 0; i < NAB; ++i) mbar_init(&afull[i], 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&gfull[i], 1);
-      mbar_init(&gempty[i], TC_READERS);
-    }
+    for (int i = 0; i < NAB; ++i) mbar_init(&afull[i], 128 + TC_READERS);
+    for (int i = 0; i < 2; ++i) mbar_init(&gempty[i], TC_READERS);
     mbar_init(&drain, 1);
     s_fail = 0;
     fence_mbar_init();
@@ -303,6 +310,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
+  if (tid == 0) TC_CE(1);
 
   // (work item, stage) cursor over this CTA's work, shared by all roles
   struct Cursor {
@@ -384,6 +392,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     }
     pdl_wait_then_trigger();
     W4_TRACE_WAITED();
+    if (lane == 0) TC_CE(2);
     if (lane == 0)
       for (int i = 0; i < npro; ++i) tma_b(i, pro_st[i]);
     for (int i = 0; i < npro; ++i)
@@ -405,6 +414,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     // The whole warp runs the loop (waits: warp-uniform values); lane 0
     // issues the MMAs and the commits.
     pdl_wait_then_trigger();
+    if (lane == 0) TC_CE(3);
     Cursor cur;
     c_init(cur);
     uint32_t s = 0;
@@ -412,10 +422,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       const int slot = s % TS, ab = s % NAB, gb = s & 1;
       if (lane == 0) TC_TL(5, s);
       // int4: the expanders saw the slot's copies land before they filled A
-      // buffer ab, so its barrier (acquired here) covers the B tile too
+      // buffer ab, so its barrier (acquired here) covers the B tile too, and
+      // the readers' arrivals on it free the accumulator buffer
       bool ok = INT4 ? tcw_wait(&afull[ab], (s / NAB) & 1, &s_fail, wl) : tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl);
       if (lane == 0) TC_TL(6, s);
-      if (s >= 2 && ok) ok = tcw_wait(&gempty[gb], ((s - 2) >> 1) & 1, &s_fail, wl);
+      if (!INT4 && s >= 2 && ok) ok = tcw_wait(&gempty[gb], ((s - 2) >> 1) & 1, &s_fail, wl);
       if (lane == 0) TC_TL(7, s);
       if (!__all_sync(0xffffffffu, ok)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -452,10 +463,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
           }
         }
         TC_TL(9, s);
-        // the ring slot (producer) and, through it, A buffer ab (expanders
-        // wait on the slot of the stage NAB back); the stage's sums (readers)
+        // the ring slot (producer), through it A buffer ab (expanders wait on
+        // the slot of the stage NAB back) and the stage's sums (readers)
         tc_commit(&empty[slot]);
-        tc_commit(&gfull[gb]);
         TC_TL(10, s);
       }
       __syncwarp();
@@ -554,6 +564,14 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     const int M = a.M;
     Cursor cur;
     c_init(cur);
+    // stages of this CTA's work: the readers free the accumulator buffer of
+    // stage s + 2 after reading stage s, and those of stages 0 and 1 now
+    uint32_t nstages = 0;
+    for (int w = blockIdx.x; w < nwork; w += gridDim.x) nstages += (uint32_t)(min(nst, (w % ks) * ps + ps) - (w % ks) * ps);
+    if (INT4) {
+      if (nstages > 0) mbar_arrive(&afull[0]);
+      if (nstages > 1) mbar_arrive(&afull[1 % NAB]);
+    }
     const __half* sp[NA];
     bool rok = false;
     __half sreg[NA];  // the scales of the group being read
@@ -583,7 +601,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     // add tensor-memory stage `st_i` (this row, CPT columns) times the scales
     auto tm_read = [&](uint32_t st_i) {
       if (r == 0) TC_TL(11, st_i);
-      const bool ok = __all_sync(0xffffffffu, tcw_wait(&gfull[st_i & 1], (st_i >> 1) & 1, &s_fail, wl));
+      const bool ok = __all_sync(0xffffffffu, tcw_wait(&empty[st_i % TS], (st_i / TS) & 1, &s_fail, wl));
       if (r == 0) TC_TL(12, st_i);
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -608,7 +626,8 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       }
-      mbar_arrive(&gempty[st_i & 1]);
+      if (!INT4) mbar_arrive(&gempty[st_i & 1]);
+      else if (st_i + 2 < nstages) mbar_arrive(&afull[(st_i + 2) % NAB]);
       if (r == 0) TC_TL(13, st_i);
     };
 
@@ -616,6 +635,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
       const int tile = work / ks, split = work % ks;
       const int row = tile * TC_M + row_l;
       bool finish = true;
+      if (r == 0) TC_CE(4);
       if (ks > 1) {
         float* wsp = a.ws + ((size_t)tile * ks + split) * (size_t)(NA * NC * TC_M);
 #pragma unroll
@@ -626,6 +646,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         readers_sync();
         if (r == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
         readers_sync();
+        if (r == 0) TC_CE(5);
         finish = s_last;
         if (finish) {
           __threadfence();
@@ -641,6 +662,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
               for (int j = 0; j < CPT; ++j) acc[g][j] += __ldcg(&wp[(g * NC + half * CPT + j) * TC_M + row_l]);
           }
           if (r == 0) a.counters[tile] = 0u;  // ready for the next call
+          if (r == 0) TC_CE(6);
         }
       }
       if (!finish || row >= N) return;
@@ -702,6 +724,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
         tm_read(grp);
       }
       epilogue(cur.work);
+      if (r == 0) TC_CE(7);
 #pragma unroll
       for (int g = 0; g < NA; ++g)
 #pragma unroll
@@ -717,6 +740,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_C
     }
   }
   __syncthreads();
+  if (tid == 0) TC_CE(8);
   if (s_fail && tid == 0 && a.err_flag) atomicOr(a.err_flag, 2);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
