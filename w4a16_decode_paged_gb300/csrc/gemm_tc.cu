@@ -78,11 +78,11 @@ struct TcShape {
   static constexpr uint32_t SLOT = A_RAW + B_BYTES;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
-  // the MMAs, as many as fit (2 to 4) beside the 2 group accumulators (8
-  // measured no faster than 4); within 256 columns where two fit, so that
-  // two CTAs can share an SM.
-  static constexpr int NAB_256 = (256 - 2 * NA * NC) / (NA * TC_ACOLS);
-  static constexpr int TM_BUDGET = NAB_256 >= 2 ? 256 : 512;
+  // the MMAs, as many as fit (2 to 4) beside the 2 accumulators (8 measured
+  // no faster than 4).  The occupancy calculator allows one CTA of this
+  // kernel per SM whatever its registers and shared memory, so the CTA may
+  // take all 512 columns.
+  static constexpr int TM_BUDGET = 512;
   static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
   static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
   // tensor memory: 2 group accumulators x NA x NC columns, and (int4) NAB A
@@ -91,7 +91,7 @@ struct TcShape {
       pow2_at_least(INT4 ? 2 * NA * NC + NAB * NA * TC_ACOLS : 2 * NA * NC);
   // ring stages: as many as the shared memory holds (4 to 12), the weights of
   // that many stages in flight per CTA hide the memory latency
-  static constexpr int SMEM_BUDGET = TMEM_COLS <= 256 ? 110 * 1024 : 200 * 1024;
+  static constexpr int SMEM_BUDGET = 200 * 1024;
   static constexpr int S = (int)(SMEM_BUDGET / SLOT) < 4 ? 4 : ((int)(SMEM_BUDGET / SLOT) > 12 ? 12 : (int)(SMEM_BUDGET / SLOT));
   static_assert(A_RAW % 1024 == 0 && B_HALF % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
   static constexpr size_t SMEM = (size_t)S * SLOT + 1024;
@@ -255,7 +255,7 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //                (for s < 2 they arrive at the start)          (128 + 256)
 //   gempty[b]    dense only: readers read accumulator buffer b  (256)
 template <bool INT4, bool SILU, int NC>
-__global__ void __launch_bounds__(TC_THREADS_WS, TcShape<INT4, SILU, NC>::TMEM_COLS <= 256 ? 2 : 1)
+__global__ void __launch_bounds__(TC_THREADS_WS, 1)
     w4pg_tc_batch(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU, NC>;
   constexpr int NA = SH::NA;
@@ -875,6 +875,55 @@ static bool tc_tensor_maps(TcArgs& a, bool int4, bool silu, int nc) {
 }
 
 #ifdef W4A16_TRACE
+// trace builds: occupancy of each GEMM shape, 16 ints per shape (raw CTAs per
+// SM from the occupancy calculator, its error code, tensor-memory columns,
+// dynamic shared memory bytes, registers per thread, static shared memory,
+// CTAs per SM without dynamic shared memory, shared memory per SM, registers
+// and threads per SM, the kernel's thread limit, CTAs per SM at 320 and 224
+// threads, local memory) for <int4,silu,nc> = <1,0,32>, <1,1,32>,
+// <1,0,128>, <1,1,64>, <0,0,32>
+template <bool INT4, bool SILU, int NC>
+static void tc_occ(int* o) {
+  using SH = TcShape<INT4, SILU, NC>;
+  auto kern = w4pg_tc_batch<INT4, SILU, NC>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM);
+  int bps = -1;
+  o[1] = (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, SH::SMEM);
+  o[0] = bps;
+  o[2] = (int)SH::TMEM_COLS;
+  o[3] = (int)SH::SMEM;
+  cudaFuncAttributes fa = {};
+  cudaFuncGetAttributes(&fa, kern);
+  o[4] = fa.numRegs;
+  o[5] = (int)fa.sharedSizeBytes;
+  int b0 = -1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, kern, TC_THREADS_WS, 0);
+  o[6] = b0;
+  int smpm = 0;
+  cudaDeviceGetAttribute(&smpm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, 0);
+  o[7] = smpm;
+  int v = 0;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxRegistersPerMultiprocessor, 0);
+  o[8] = v;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxThreadsPerMultiProcessor, 0);
+  o[9] = v;
+  o[10] = fa.maxThreadsPerBlock;
+  int b1 = -1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, kern, 320, 0);
+  o[11] = b1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, kern, 224, 0);
+  o[12] = b1;
+  o[13] = (int)fa.localSizeBytes;
+}
+extern "C" W4A16_API int w4a16_trace_tc_occupancy(int* out) {
+  tc_occ<true, false, 32>(out);
+  tc_occ<true, true, 32>(out + 16);
+  tc_occ<true, false, 128>(out + 32);
+  tc_occ<true, true, 64>(out + 48);
+  tc_occ<false, false, 32>(out + 64);
+  return 0;
+}
+
 // trace builds: copy CTA 0's per-stage event times of the last GEMM launch
 extern "C" W4A16_API int w4a16_trace_tc_timeline(unsigned long long* host_out, int n) {
   const size_t bytes = std::min((size_t)n, (size_t)TC_TL_EVENTS * TC_TL_STAGES) * sizeof(unsigned long long);
