@@ -68,33 +68,47 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
 // NC: batch columns per tile (the MMA's N).  32 for decode batches; 128
 // (one weight matrix) or 64 (gate and up together) for the wide row blocks
 // of a prompt, where each weight tile is then read once per NC rows.
+// PIPES: pipelines per CTA.  The occupancy calculator allows one CTA of this
+// kernel per SM whatever its registers and shared memory, and at NC = 32 one
+// MMA warp's issue loop bounds the kernel, so the int4 NC = 32 shapes run two
+// complete pipelines (producer, MMA warp, expanders, readers, ring, half the
+// tensor memory) per CTA: gate|up with pipeline p on matrix p of every tile
+// (COOP, the readers meet in shared memory for SiLU(gate) x up), the other
+// projections with the pipelines on alternate work items (IND).
 template <bool INT4, bool SILU, int NC>
 struct TcShape {
   static constexpr int NA = SILU ? 2 : 1;                                   // weight matrices per tile
+  static constexpr int PIPES = (INT4 && NC == 32) ? 2 : 1;
+  static constexpr bool COOP = SILU && PIPES == 2;
+  static constexpr bool IND = !SILU && PIPES == 2;
+  static constexpr int NAP = PIPES == 2 ? 1 : NA;                           // matrices per pipeline
+  static constexpr int THREADS = PIPES * TC_THREADS_WS;
   static constexpr uint32_t A_TX = INT4 ? TC_M * (TC_K / 2) : TC_A_BYTES;   // A bytes per matrix per stage
-  static constexpr uint32_t A_RAW = NA * A_TX;                              // A bytes per ring slot
+  static constexpr uint32_t A_RAW = NAP * A_TX;                             // A bytes per ring slot
   static constexpr uint32_t B_HALF = NC * TC_KH * 2;                        // one swizzled half of B
   static constexpr uint32_t B_BYTES = NC * TC_K * 2;                        // activation tile per stage
   static constexpr uint32_t SLOT = A_RAW + B_BYTES;
   static constexpr int CPT = NC / 2;                                        // columns per reader thread
   // A buffers in tensor memory (int4): how far code expansion runs ahead of
-  // the MMAs, as many as fit (2 to 4) beside the 2 accumulators (8 measured
-  // no faster than 4).  The occupancy calculator allows one CTA of this
-  // kernel per SM whatever its registers and shared memory, so the CTA may
-  // take all 512 columns.
-  static constexpr int TM_BUDGET = 512;
-  static constexpr int NAB_FIT = (TM_BUDGET - 2 * NA * NC) / (NA * TC_ACOLS);
+  // the MMAs, as many as fit (2 to 4) beside a pipeline's 2 accumulators (8
+  // measured no faster than 4); each pipeline has 512 / PIPES columns.
+  static constexpr int TM_BUDGET = 512 / PIPES;
+  static constexpr int NAB_FIT = (TM_BUDGET - 2 * NAP * NC) / (NAP * TC_ACOLS);
   static constexpr int NAB = NAB_FIT < 2 ? 2 : (NAB_FIT > 4 ? 4 : NAB_FIT);
-  // tensor memory: 2 group accumulators x NA x NC columns, and (int4) NAB A
-  // buffers x NA x 32 columns of exact codes, rounded up to a power of two
-  static constexpr uint32_t TMEM_COLS =
-      pow2_at_least(INT4 ? 2 * NA * NC + NAB * NA * TC_ACOLS : 2 * NA * NC);
-  // ring stages: as many as the shared memory holds (4 to 12), the weights of
-  // that many stages in flight per CTA hide the memory latency
+  // tensor memory of a pipeline: 2 accumulators x NAP x NC columns, and
+  // (int4) NAB A buffers x NAP x 64 columns of exact codes, rounded up to a
+  // power of two
+  static constexpr uint32_t TM_P = pow2_at_least(INT4 ? 2 * NAP * NC + NAB * NAP * TC_ACOLS : 2 * NAP * NC);
+  static constexpr uint32_t TMEM_COLS = PIPES * TM_P;
+  // ring stages per pipeline: as many as the shared memory holds (4 to 12),
+  // the weights of that many stages in flight per CTA hide the memory latency
   static constexpr int SMEM_BUDGET = 200 * 1024;
-  static constexpr int S = (int)(SMEM_BUDGET / SLOT) < 4 ? 4 : ((int)(SMEM_BUDGET / SLOT) > 12 ? 12 : (int)(SMEM_BUDGET / SLOT));
+  static constexpr int S_FIT = (int)(SMEM_BUDGET / (PIPES * SLOT));
+  static constexpr int S = S_FIT < 4 ? 4 : (S_FIT > 12 ? 12 : S_FIT);
   static_assert(A_RAW % 1024 == 0 && B_HALF % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
-  static constexpr size_t SMEM = (size_t)S * SLOT + 1024;
+  // COOP: the up sums of a tile, fp32 [NC][128], from pipeline 1's readers
+  static constexpr uint32_t XCH = COOP ? (uint32_t)NC * TC_M * 4 : 0u;
+  static constexpr size_t SMEM = (size_t)PIPES * S * SLOT + XCH + 1024;
   static_assert(NC % 32 == 0 && NC <= 128, "NC: 32, 64 or 128 columns");
   static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
@@ -189,8 +203,9 @@ __device__ __forceinline__ bool tcw_wait(uint64_t* bar, uint32_t parity, volatil
 }
 
 #ifdef W4A16_TRACE
-// Trace builds: per-stage event times of CTA 0 of the last launch, in SM
-// clock cycles (one SM, so the roles' clocks agree; w4a16_trace_tc_timeline):
+// Trace builds: per-stage event times of CTA 0 (pipeline 0) of the last
+// launch, in SM clock cycles (one SM, so the roles' clocks agree;
+// w4a16_trace_tc_timeline):
 //   0 producer issued the stage's copies      5 MMA warp at the loop top
 //   1 expander: A buffer free                 6 MMA: operands ready
 //   2 expander: the stage's copies landed     7 MMA: accumulator buffer free
@@ -205,7 +220,7 @@ constexpr int TC_TL_EVENTS = 15, TC_TL_STAGES = 512;
 __device__ unsigned long long g_tc_timeline[TC_TL_EVENTS][TC_TL_STAGES];
 #define TC_TL(ev, s)                                                              \
   do {                                                                             \
-    if (blockIdx.x == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = clock64();   \
+    if (blockIdx.x == 0 && pipe == 0 && (s) < TC_TL_STAGES) g_tc_timeline[ev][s] = clock64(); \
   } while (0)
 #define TC_CE(e) TC_TL(14, e)
 #else
@@ -232,9 +247,8 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(TC_READERS) : "memory"); }
-
-// Warp roles: warp 0 lane 0 issues the bulk-tensor copies (producer), warp
+// Warp roles within a pipeline (14 warps; pipeline p is warps 14p ..
+// 14p + 13): warp 0 lane 0 issues the bulk-tensor copies (producer), warp
 // 1 lane 0 issues the MMAs, warps 2..5 (the expanders, 128 threads, one
 // weight row each) expand the int4 codes of their row into tensor-memory A
 // buffers, up to NAB stages ahead of the tensor core, and warps 6..13 (the
@@ -243,8 +257,8 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 // the stage and run the epilogue.  A stage is 128 k, one scale group: eight
 // MMAs per weight matrix between one barrier wait, one fence and one commit
 // of the MMA warp, whose loop is what bounds the kernel at small N.  Stage s
-// of this CTA's work uses ring slot s % TS, A buffer s % NAB and accumulator
-// buffer s % 2.  The roles only meet at mbarriers:
+// of a pipeline's work uses its ring slot s % TS, A buffer s % NAB and
+// accumulator buffer s % 2.  The roles only meet at the pipeline's mbarriers:
 //   full[slot]   the slot's bulk-tensor copies landed            (1 + tx bytes)
 //   empty[slot]  expanders done with the raw A, MMAs done        (128 + 1; dense: 1);
 //                its phase for stage s also tells the expanders that A
@@ -255,10 +269,14 @@ __device__ __forceinline__ void readers_sync() { asm volatile("bar.sync 1, %0;" 
 //                (for s < 2 they arrive at the start)          (128 + 256)
 //   gempty[b]    dense only: readers read accumulator buffer b  (256)
 template <bool INT4, bool SILU, int NC>
-__global__ void __launch_bounds__(TC_THREADS_WS, 1)
+__global__ void __launch_bounds__(TcShape<INT4, SILU, NC>::THREADS, 1)
     w4pg_tc_batch(const __grid_constant__ TcArgs a) {
   using SH = TcShape<INT4, SILU, NC>;
   constexpr int NA = SH::NA;
+  constexpr int NAP = SH::NAP;
+  constexpr int PIPES = SH::PIPES;
+  constexpr bool COOP = SH::COOP;
+  constexpr bool IND = SH::IND;
   constexpr int CPT = SH::CPT;
   // The array is declared with the alignment every build guarantees (16
   // bytes): the 1024-byte alignment of the ring (needed by the 128-byte
@@ -267,16 +285,28 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
   // the compiler take the offset to be 0, which relocatable builds do not
   // honour.)
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned char* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // [TS][A raw | B tile]
+  unsigned char* ring0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // [PIPES][TS][A raw | B]
   constexpr int NAB = SH::NAB;
-  constexpr int TS = SH::S;  // ring stages
+  constexpr int TS = SH::S;  // ring stages per pipeline
   static_assert(NAB < TS, "an A buffer is reused before its ring slot");
-  __shared__ __align__(8) uint64_t full[TS], empty[TS], afull[NAB], gempty[2], drain;
+  __shared__ __align__(8) uint64_t full_[PIPES][TS], empty_[PIPES][TS], afull_[PIPES][NAB], gempty_[PIPES][2],
+      drain_[PIPES];
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_last, s_rfail;
+  __shared__ int s_last_[PIPES], s_rfail_[PIPES];
   __shared__ volatile int s_fail;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int pipe = PIPES == 2 ? warp / 14 : 0;
+  const int lw = warp - 14 * pipe;  // warp within the pipeline
+  unsigned char* ring = ring0 + pipe * TS * SH::SLOT;
+  float* xch = reinterpret_cast<float*>(ring0 + PIPES * TS * SH::SLOT);  // COOP exchange [NC][128]
+  uint64_t* const full = full_[pipe];
+  uint64_t* const empty = empty_[pipe];
+  uint64_t* const afull = afull_[pipe];
+  uint64_t* const gempty = gempty_[pipe];
+  uint64_t* const drainp = &drain_[pipe];
+  int& s_last = s_last_[pipe];
+  int& s_rfail = s_rfail_[pipe];
   const int K = a.K, N = a.N;
   const int nst = K / TC_K, ps = a.per_split, ks = a.ksplit;
   const int ntiles = (N + TC_M - 1) / TC_M;
@@ -286,9 +316,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
   if (tid == 0) TC_CE(0);
 
   constexpr uint32_t TMEM_COLS = SH::TMEM_COLS;
-  // columns: [0, 2 NA NC) accumulators; then (int4) A buffer ab, matrix g at
-  // 2 NA NC + (ab NA + g) TC_ACOLS
-  constexpr uint32_t TM_A = 2 * NA * NC;
+  // a pipeline's columns, from its base: [0, 2 NAP NC) accumulators; then
+  // (int4) A buffer ab, matrix g at 2 NAP NC + (ab NAP + g) TC_ACOLS
+  constexpr uint32_t TM_A = 2 * NAP * NC;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "r"(TMEM_COLS)
@@ -296,28 +326,33 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 32) {
-    for (int i = 0; i < TS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], (INT4 ? 128 : 0) + 1);
+    for (int p = 0; p < PIPES; ++p) {
+      for (int i = 0; i < TS; ++i) {
+        mbar_init(&full_[p][i], 1);
+        mbar_init(&empty_[p][i], (INT4 ? 128 : 0) + 1);
+      }
+      for (int i = 0; i < NAB; ++i) mbar_init(&afull_[p][i], 128 + TC_READERS);
+      for (int i = 0; i < 2; ++i) mbar_init(&gempty_[p][i], TC_READERS);
+      mbar_init(&drain_[p], 1);
     }
-    for (int i = 0; i < NAB; ++i) mbar_init(&afull[i], 128 + TC_READERS);
-    for (int i = 0; i < 2; ++i) mbar_init(&gempty[i], TC_READERS);
-    mbar_init(&drain, 1);
     s_fail = 0;
     fence_mbar_init();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = tmem_slot;
+  const uint32_t tmem = tmem_slot + (uint32_t)pipe * SH::TM_P;  // this pipeline's columns
   if (tid == 0) TC_CE(1);
 
   // (work item, stage) cursor over this CTA's work, shared by all roles
   struct Cursor {
     int work, st, end, begin;
   };
+  // IND: the pipelines take alternate work items
+  const int wstep = IND ? 2 * (int)gridDim.x : (int)gridDim.x;
+  const int wfirst = IND ? 2 * (int)blockIdx.x + pipe : (int)blockIdx.x;
   auto c_init = [&](Cursor& c) {
-    c.work = blockIdx.x;
+    c.work = wfirst;
     if (c.work < nwork) {
       c.begin = c.st = (c.work % ks) * ps;
       c.end = min(nst, c.begin + ps);
@@ -325,7 +360,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
   };
   auto c_next = [&](Cursor& c) {  // returns true when a new work item starts
     if (++c.st < c.end) return false;
-    c.work += gridDim.x;
+    c.work += wstep;
     if (c.work < nwork) {
       c.begin = c.st = (c.work % ks) * ps;
       c.end = min(nst, c.begin + ps);
@@ -333,20 +368,20 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     return true;
   };
 
-  if (warp == 0) {
+  if (lw == 0) {
     // =========================== producer ===================================
     // Lane 0 copies a stage's weight tiles (int4: 128 rows x 64 bytes of
     // codes; dense: two swizzled 64-k halves) and its activation tile (two
     // swizzled halves); the slot's barrier expects their bytes.
     Cursor cur;
     c_init(cur);
-    int tm_map[NA], tm_row = 0;  // the item's weight map per matrix and its first row in it
+    int tm_map[NAP], tm_row = 0;  // the item's weight map per matrix and its first row in it
     auto item_tma = [&]() {
       const int r0 = (cur.work / ks) * TC_M;
       tm_row = r0;
       if (SILU || !INT4) {
 #pragma unroll
-        for (int g = 0; g < NA; ++g) tm_map[g] = g;
+        for (int g = 0; g < NAP; ++g) tm_map[g] = COOP ? pipe : g;
       } else {
         int si = 0;
 #pragma unroll
@@ -358,7 +393,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     auto tma_a = [&](int slot, int st) {
       unsigned char* sa = ring + slot * SH::SLOT;
 #pragma unroll
-      for (int g = 0; g < NA; ++g) {
+      for (int g = 0; g < NAP; ++g) {
         if (INT4) {
           tma_load_2d(sa + g * SH::A_TX, &a.tm_w[tm_map[g]], st * (TC_K / 8), tm_row, &full[slot]);
         } else {
@@ -409,7 +444,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
       __syncwarp();
       if (c_next(cur) && cur.work < nwork) item_tma();
     }
-  } else if (warp == 1) {
+  } else if (lw == 1) {
     // =========================== MMA issuer =================================
     // The whole warp runs the loop (waits: warp-uniform values); lane 0
     // issues the MMAs and the commits.
@@ -432,12 +467,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (lane == 0) TC_TL(8, s);
       unsigned char* sl = ring + slot * SH::SLOT;
-      const uint32_t dbase = tmem + gb * (NA * NC);
+      const uint32_t dbase = tmem + gb * (NAP * NC);
       if (lane == 0) {
         const uint64_t bd0 = tc_desc(smem_u32(sl + SH::A_RAW));
         const uint64_t bd1 = tc_desc(smem_u32(sl + SH::A_RAW + SH::B_HALF));
 #pragma unroll
-        for (int g = 0; g < NA; ++g) {
+        for (int g = 0; g < NAP; ++g) {
 #pragma unroll
           for (int kk = 0; kk < TC_K / 16; ++kk) {
             // 16-k slice kk: half kk / 4 of the swizzled B tile, 32 bytes per slice
@@ -445,7 +480,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
             const uint32_t accum = kk > 0 ? 1u : 0u;
             if (INT4) {
               // A (128 x 16 exact codes) from tensor memory: 8 columns per 16 k
-              const uint32_t at = tmem + TM_A + (uint32_t)((ab * NA + g) * TC_ACOLS + kk * 8);
+              const uint32_t at = tmem + TM_A + (uint32_t)((ab * NAP + g) * TC_ACOLS + kk * 8);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                   "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dbase + (uint32_t)(g * NC)),
@@ -476,11 +511,11 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     // abort elsewhere in the CTA (the MMAs finish on their own; the wait
     // keeps the normal bound)
     if (s > 0) {
-      if (lane == 0) tc_commit(&drain);
+      if (lane == 0) tc_commit(drainp);
       __syncwarp();
-      (void)tc_wait(&drain, 0);
+      (void)tc_wait(drainp, 0);
     }
-  } else if (warp < 2 + TC_EXP_WARPS) {
+  } else if (lw < 2 + TC_EXP_WARPS) {
     // =========================== expanders ==================================
     // Each thread expands its weight row's 128 codes per stage (per matrix)
     // into A buffer s % NAB, up to NAB stages ahead of the tensor core.
@@ -498,7 +533,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         mbar_arrive(&afull[ps_ % NAB]);
         mbar_arrive(&empty[ps_ % TS]);
-        if (warp == 2 && lane == 0) TC_TL(4, ps_);
+        if (lw == 2 && lane == 0) TC_TL(4, ps_);
       };
       Cursor cur;
       c_init(cur);
@@ -509,16 +544,16 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
         // the A buffer's previous MMAs are done, the slot's copies landed
         // (the MMA's commit to that stage's ring slot also covers A buffer ab)
         if (s >= NAB && !tcw_wait(&empty[(s - NAB) % TS], ((s - NAB) / TS) & 1, &s_fail, wl)) break;
-        if (warp == 2 && lane == 0) TC_TL(1, s);
+        if (lw == 2 && lane == 0) TC_TL(1, s);
         if (!tcw_wait(&full[slot], (s / TS) & 1, &s_fail, wl)) break;
-        if (warp == 2 && lane == 0) TC_TL(2, s);
+        if (lw == 2 && lane == 0) TC_TL(2, s);
         const unsigned char* sl = ring + slot * SH::SLOT;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (LAZY && pend) release(s - 1);
         // exact codes of this row's 128 k per matrix, 64 k (32 columns of
         // fp16 pairs in k order) at a time
 #pragma unroll
-        for (int g = 0; g < NA; ++g) {
+        for (int g = 0; g < NAP; ++g) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const unsigned char* src = sl + (g * TC_M + row_l) * (TC_K / 2) + h * 32;
@@ -533,7 +568,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
             c[5] = codes_word(r1.y);
             c[6] = codes_word(r1.z);
             c[7] = codes_word(r1.w);
-            const uint32_t ta = lane_base + (uint32_t)((ab * NA + g) * TC_ACOLS + h * 32);
+            const uint32_t ta = lane_base + (uint32_t)((ab * NAP + g) * TC_ACOLS + h * 32);
             asm volatile(
                 "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
@@ -544,7 +579,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
                 : "memory");
           }
         }
-        if (warp == 2 && lane == 0) TC_TL(3, s);
+        if (lw == 2 && lane == 0) TC_TL(3, s);
         if (!LAZY) release(s);
         pend = true;
         c_next(cur);
@@ -558,7 +593,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     // buffer, times the group's scale into fp32 registers; at the end of a
     // work item the epilogue.  They run up to one stage behind the tensor core.
     pdl_wait_then_trigger();
-    const int r = tid - 64 - 32 * TC_EXP_WARPS;   // 0..255
+    const int r = tid - TC_THREADS_WS * pipe - 64 - 32 * TC_EXP_WARPS;   // 0..255
     const int half = r >> 7;                      // batch columns CPT h .. CPT h + CPT - 1
     const int row_l = 32 * (warp & 3) + lane;     // tensor-memory lanes of this warp's quadrant
     const int M = a.M;
@@ -567,14 +602,16 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
     // stages of this CTA's work: the readers free the accumulator buffer of
     // stage s + 2 after reading stage s, and those of stages 0 and 1 now
     uint32_t nstages = 0;
-    for (int w = blockIdx.x; w < nwork; w += gridDim.x) nstages += (uint32_t)(min(nst, (w % ks) * ps + ps) - (w % ks) * ps);
+    for (int w = wfirst; w < nwork; w += wstep) nstages += (uint32_t)(min(nst, (w % ks) * ps + ps) - (w % ks) * ps);
+    // the readers' own barrier (one per pipeline; 3 joins both pipelines' readers)
+    auto rsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + pipe), "n"(TC_READERS) : "memory"); };
     if (INT4) {
       if (nstages > 0) mbar_arrive(&afull[0]);
       if (nstages > 1) mbar_arrive(&afull[1 % NAB]);
     }
-    const __half* sp[NA];
+    const __half* sp[NAP];
     bool rok = false;
-    __half sreg[NA];  // the scales of the group being read
+    __half sreg[NAP];  // the scales of the group being read
     float acc[NA][CPT];
 #pragma unroll
     for (int g = 0; g < NA; ++g)
@@ -588,7 +625,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
       const int rr = rok ? row : 0;
       if (SILU) {
 #pragma unroll
-        for (int g = 0; g < NA; ++g) sp[g] = a.seg[g].s + (size_t)rr * (K / 128);
+        for (int g = 0; g < NAP; ++g) sp[g] = a.seg[COOP ? pipe : g].s + (size_t)rr * (K / 128);
       } else if (INT4) {
         int q = rr, si = 0;
 #pragma unroll
@@ -606,12 +643,12 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
       if (ok) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-        for (int g = 0; g < NA; ++g) {
+        for (int g = 0; g < NAP; ++g) {
           const float sc = INT4 ? __half2float(sreg[g]) : 1.0f;
 #pragma unroll
           for (int c0 = 0; c0 < CPT; c0 += 16) {
             uint32_t v[16];
-            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (st_i & 1) * (NA * NC) +
+            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (st_i & 1) * (NAP * NC) +
                                    (uint32_t)(g * NC + half * CPT + c0);
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -643,9 +680,9 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
 #pragma unroll
           for (int j = 0; j < CPT; ++j) wsp[(g * NC + half * CPT + j) * TC_M + row_l] = acc[g][j];
         __threadfence();
-        readers_sync();
+        rsync();
         if (r == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned int)(ks - 1));
-        readers_sync();
+        rsync();
         if (r == 0) TC_CE(5);
         finish = s_last;
         if (finish) {
@@ -708,31 +745,46 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
       if (INT4) scale_rows(cur.work / ks);
       const int g0 = cur.begin, ng = cur.end - cur.begin;  // one scale group per stage
       // scales of the next two groups in flight (requested two groups ahead)
-      __half snext[NA], snext2[NA];
+      __half snext[NAP], snext2[NAP];
 #pragma unroll
-      for (int g = 0; g < NA; ++g) {
+      for (int g = 0; g < NAP; ++g) {
         snext[g] = (INT4 && rok) ? sp[g][g0] : __float2half(0.f);
         snext2[g] = (INT4 && rok && ng > 1) ? sp[g][g0 + 1] : __float2half(0.f);
       }
       for (int gi = 0; gi < ng; ++gi, ++grp) {
 #pragma unroll
-        for (int g = 0; g < NA; ++g) {
+        for (int g = 0; g < NAP; ++g) {
           sreg[g] = snext[g];
           snext[g] = snext2[g];
           if (INT4 && rok && gi + 2 < ng) snext2[g] = sp[g][g0 + gi + 2];
         }
         tm_read(grp);
       }
-      epilogue(cur.work);
+      if (COOP) {
+        // pipeline 1's up sums to pipeline 0's readers, which run the epilogue
+        if (pipe == 1) {
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) xch[(half * CPT + j) * TC_M + row_l] = acc[0][j];
+        }
+        asm volatile("bar.sync 3, %0;" ::"n"(2 * TC_READERS) : "memory");
+        if (pipe == 0) {
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) acc[NA - 1][j] = xch[(half * CPT + j) * TC_M + row_l];
+        }
+        asm volatile("bar.sync 3, %0;" ::"n"(2 * TC_READERS) : "memory");
+      }
+      if (!COOP || pipe == 0) epilogue(cur.work);
       if (r == 0) TC_CE(7);
 #pragma unroll
       for (int g = 0; g < NA; ++g)
 #pragma unroll
         for (int j = 0; j < CPT; ++j) acc[g][j] = 0.f;
       if (r == 0) s_rfail = s_fail;
-      readers_sync();
-      if (s_rfail) break;
-      cur.work += gridDim.x;
+      rsync();
+      // both COOP pipelines run every item (their exchange barriers must meet);
+      // after a failure their waits give up at once
+      if (s_rfail && !COOP) break;
+      cur.work += wstep;
       if (cur.work < nwork) {
         cur.begin = cur.st = (cur.work % ks) * ps;
         cur.end = min(nst, cur.begin + ps);
@@ -745,7 +797,7 @@ __global__ void __launch_bounds__(TC_THREADS_WS, 1)
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_slot), "r"(TMEM_COLS) : "memory");
 }
 
 int tc_cols(int M, bool int4, bool silu) {
@@ -776,7 +828,7 @@ static int tc_ctas_per_sm() {
     auto kern = w4pg_tc_batch<INT4, SILU, NC>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM);
     int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, SH::SMEM) != cudaSuccess || bps < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, SH::THREADS, SH::SMEM) != cudaSuccess || bps < 1)
       bps = 1;
     // tensor memory: 512 columns per SM
     cached[device_index() & 63] = std::max(1, std::min(bps, (int)(512 / SH::TMEM_COLS)));
@@ -787,9 +839,9 @@ static int tc_ctas_per_sm() {
 static int tc_slots(bool int4, bool silu, int nc) {
   int per;
   if (!int4) per = tc_ctas_per_sm<false, false, TC_N>();
-  else if (nc == TC_N) per = silu ? tc_ctas_per_sm<true, true, TC_N>() : tc_ctas_per_sm<true, false, TC_N>();
+  else if (nc == TC_N) per = silu ? tc_ctas_per_sm<true, true, TC_N>() : tc_ctas_per_sm<true, false, TC_N>() * 2;
   else per = silu ? tc_ctas_per_sm<true, true, 64>() : tc_ctas_per_sm<true, false, 128>();
-  return per * num_sms();
+  return per * num_sms();  // work items in flight (the two pipelines of an IND CTA take one each)
 }
 
 // Split of K: the split length (in stages, each a scale group) that
@@ -888,7 +940,7 @@ static void tc_occ(int* o) {
   auto kern = w4pg_tc_batch<INT4, SILU, NC>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM);
   int bps = -1;
-  o[1] = (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, TC_THREADS_WS, SH::SMEM);
+  o[1] = (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, SH::THREADS, SH::SMEM);
   o[0] = bps;
   o[2] = (int)SH::TMEM_COLS;
   o[3] = (int)SH::SMEM;
@@ -897,7 +949,7 @@ static void tc_occ(int* o) {
   o[4] = fa.numRegs;
   o[5] = (int)fa.sharedSizeBytes;
   int b0 = -1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, kern, TC_THREADS_WS, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, kern, SH::THREADS, 0);
   o[6] = b0;
   int smpm = 0;
   cudaDeviceGetAttribute(&smpm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, 0);
@@ -950,20 +1002,22 @@ int launch_gemm_tc(const TcArgs& a_in, bool int4, bool silu, cudaStream_t s) {
                      a.ksplit, nst);
   const int ntiles = (a.N + TC_M - 1) / TC_M;
   const int nwork = ntiles * a.ksplit;
-  auto go = [&](auto kern, size_t smem, int per_sm) -> int {
-    const int blocks = std::max(1, std::min(nwork, per_sm * num_sms()));
-    cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(TC_THREADS_WS), smem, s, a);
+  auto go = [&](auto kern, auto shape, int per_sm) -> int {
+    using SH = decltype(shape);
+    const int items_per_cta = SH::IND ? 2 : 1;
+    const int blocks = std::max(1, std::min((nwork + items_per_cta - 1) / items_per_cta, per_sm * num_sms()));
+    cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(SH::THREADS), SH::SMEM, s, a);
     if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "gemm_tc launch: %s", cudaGetErrorString(e));
     return W4A16_OK;
   };
-  if (!int4) return go(w4pg_tc_batch<false, false, TC_N>, TcShape<false, false, TC_N>::SMEM,
+  if (!int4) return go(w4pg_tc_batch<false, false, TC_N>, TcShape<false, false, TC_N>{},
                        tc_ctas_per_sm<false, false, TC_N>());
   if (nc == TC_N) {
-    if (silu) return go(w4pg_tc_batch<true, true, TC_N>, TcShape<true, true, TC_N>::SMEM, tc_ctas_per_sm<true, true, TC_N>());
-    return go(w4pg_tc_batch<true, false, TC_N>, TcShape<true, false, TC_N>::SMEM, tc_ctas_per_sm<true, false, TC_N>());
+    if (silu) return go(w4pg_tc_batch<true, true, TC_N>, TcShape<true, true, TC_N>{}, tc_ctas_per_sm<true, true, TC_N>());
+    return go(w4pg_tc_batch<true, false, TC_N>, TcShape<true, false, TC_N>{}, tc_ctas_per_sm<true, false, TC_N>());
   }
-  if (silu) return go(w4pg_tc_batch<true, true, 64>, TcShape<true, true, 64>::SMEM, tc_ctas_per_sm<true, true, 64>());
-  return go(w4pg_tc_batch<true, false, 128>, TcShape<true, false, 128>::SMEM, tc_ctas_per_sm<true, false, 128>());
+  if (silu) return go(w4pg_tc_batch<true, true, 64>, TcShape<true, true, 64>{}, tc_ctas_per_sm<true, true, 64>());
+  return go(w4pg_tc_batch<true, false, 128>, TcShape<true, false, 128>{}, tc_ctas_per_sm<true, false, 128>());
 }
 
 }  // namespace w4
