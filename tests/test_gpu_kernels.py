@@ -379,3 +379,24 @@ def test_fused_rope_append_attention_matches_oracle(api, Hq, Hkv, part):
     assert np.array_equal(kg[~mask], kp[~mask])        # nothing else moved
     assert_close(kg[mask], kp_ref[mask], what="appended k")
     assert np.array_equal(to_host(qkvd), qkv)         # q|k|v rows are read only
+
+
+def test_paged_gqa_decode_batch32_mixed_lengths(api):
+    """32 sequences with lengths U[1, 4096] (15/16/17 among them) and the
+    library's partition choice (a warp per 256-token partition, CTAs handed
+    out longest sequence first): every output against the oracle."""
+    c = synth.QWEN_BATCHED
+    r = synth.rng(4242)
+    lens = synth.batched_lens(r, 32, 4096, c["forced_lens"]).astype(np.int32)
+    Hq, Hkv, D = 28, 4, 128
+    pages = int(sum((L + 15) // 16 for L in lens)) + 5
+    kp = synth.kv_pool(r, pages, Hkv, D)
+    vp = synth.kv_pool(r, pages, Hkv, D)
+    bt = synth.block_table(r, lens, pages)
+    q = synth.normal_fp16(r, (32, Hq, D), std=2.0)
+    assert api.load().paged_gqa_decode_default_partition(32, Hkv, int(lens.max())) == 256
+    out = api.paged_gqa_decode(to_dev(q, torch), to_dev(kp, torch), to_dev(vp, torch), to_dev(bt, torch),
+                               to_dev(lens, torch), max_context=int(lens.max()))
+    torch.cuda.synchronize()
+    ref = orc.paged_attention(q, kp, vp, bt, lens, 1 / math.sqrt(D))
+    assert_close(to_host(out), ref, what="attention b32 mixed lengths")
