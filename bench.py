@@ -474,6 +474,39 @@ def time_attention_long(torch, api, dev, stream, reps=6, fp8=False):
                                                     + (", FP8 E4M3 pages" if fp8 else "")}
 
 
+def time_layer_long(torch, api, dls, dev, stream, reps=6):
+    """One whole decoder layer (RMSNorm, q|k|v, RoPE + append + attention,
+    o + residual, RMSNorm, gate|up + SiLU-mul, down + residual) on the
+    long-context workload: 4 sequences of 32768 tokens in a 16384-page pool,
+    512-token partitions, the b=1 workload's layer-0 weights (CUDA-core
+    GEMVs at M = 4).  The 268 MB of KV a call reads pushes the layer's
+    120 MB of weights out of L2 between calls; a CUDA graph of 4 calls, CUDA
+    events on the launching stream.  The appended token's slot is the same
+    every call (the lengths are not advanced)."""
+    from w4a16_decode_paged_gb300 import synth
+    c = synth.QWEN_LONG
+    B, Hkv, D, L, pool, part = (c["batch"], c["n_kv_heads"], c["head_dim"], c["context"], c["pool_pages"],
+                                c["partition_tokens"])
+    r = synth.rng(c["seed"] + 13)
+    lens = np.full(B, L, np.int32)
+    bt = torch.from_numpy(synth.block_table(r, lens, pool)).to(dev)
+    ld = torch.from_numpy(lens).to(dev)
+    layer = {**dls[0], "k_pool": torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16),
+             "v_pool": torch.randn((pool, Hkv, 16, D), device=dev, dtype=torch.float16)}
+    model = api.Model(dict(c, vocab=0), [layer], max_batch=B, max_context=L, num_pages=pool, partition_tokens=part)
+    x = (torch.randn((B, c["hidden"]), device=dev) * 0.5).half()
+    fn = lambda i: model.layer(0, x, bt, ld, stream=stream)
+    per = _graph_time(torch, stream, fn, 4, reps)
+    assert model.check_errors(stream) == 0
+    g, att = layer_bytes(c, lens)
+    model.close()
+    del layer
+    return {"us_per_launch": per * 1e6, "bytes_per_launch": g + att, "gbs": (g + att) / per / 1e9,
+            "launches_timed": 4 * reps,
+            "workload": f"one decoder layer, b={B} x ctx {L}, partitions of {part} (weights {g / 1e6:.1f} MB, "
+                        f"KV {att / 1e6:.1f} MB)"}
+
+
 def _graph_time(torch, stream, fn, per_graph, reps):
     """Seconds per call of fn(i), i = 0..per_graph-1 captured in one CUDA
     graph and replayed `reps` times (CUDA events on the launching stream)."""
@@ -743,6 +776,7 @@ def main():
             if args.workload == "b1":
                 kern["attention_b4_ctx32768"] = time_attention_long(torch, api, dev, stream)
                 kern["attention_fp8_b4_ctx32768"] = time_attention_long(torch, api, dev, stream, fp8=True)
+                kern["layer_b4_ctx32768"] = time_layer_long(torch, api, dls, dev, stream)
                 kern["gateup_tc_m32"] = time_gemv_kernels(torch, api, cfg, dls, dev, stream, 32,
                                                           only=("gateup",))["gateup"]
                 kern["b32_step"] = time_b32_step(torch, api, cfg, dls, embed, fnorm, lm, dev, stream)
