@@ -446,7 +446,9 @@ W4A16_API int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const in
  *   attention -> o GEMV + residual -> RMSNorm -> gate/up GEMV + SiLU-mul ->
  *   down GEMV + residual), final RMSNorm, lm_head, argmax -> tokens_out.
  *   B <= 4 runs the CUDA-core GEMVs with the RMSNorms fused in front and
- *   the lm_head GEMV with a fused argmax; 4 < B <= max_batch runs each
+ *   the lm_head GEMV with a fused argmax (at B = 3, 4 gate/up, and down
+ *   at K = 18944, take the tensor-core GEMM, gate/up after its own
+ *   RMSNorm); 4 < B <= max_batch runs each
  *   RMSNorm on its own, the projections and the lm_head as tensor-core
  *   GEMMs (fp32 logits in the model's arena) and a row-wise argmax.
  *   tokens_in, tokens_out  int32 [B] device (may be the same buffer)

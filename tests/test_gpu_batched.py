@@ -109,6 +109,7 @@ def test_batched_kernel_count(api):
     case = _tiny_case(8, n_layers=3, seed=5200)
     m, _ = _device_model(api, case, 8, 160)
     assert m.kernel_count(2) == 1 + 5 * 3 + 1   # CUDA-core path: fused norms, fused lm_head + argmax
+    assert m.kernel_count(4) == 1 + 6 * 3 + 1   # gate|up on the tensor cores after its own RMSNorm
     assert m.kernel_count(8) == 1 + 7 * 3 + 3   # + separate RMSNorms, lm_head GEMM, argmax
     m.close()
 

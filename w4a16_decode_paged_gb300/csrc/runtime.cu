@@ -92,6 +92,11 @@ static constexpr int GEMV_MAX_BATCH = 4;
 static bool batched_path(const w4a16_model* m, int B) {
   return B > GEMV_MAX_BATCH || !gemv_cuda_core_supported(B, m->cfg.hidden);
 }
+// From 3 rows on, gate|up (the largest projection) takes the tensor-core GEMM
+// after an RMSNorm of its own: at M = 3 / 4 the CUDA-core GEMV does 3-4 FMAs
+// per weight (39.7 / 45.9 us for 2 x 18944 rows at K = 3584, against 26.7 us
+// for the GEMM).  q|k|v and o stay on the GEMV (13 us against 14).
+static constexpr int SILU_TC_MIN_ROWS = 3;
 
 extern "C" int w4a16_model_create(const w4a16_model_config* cfg, const w4a16_model_weights* w, int max_batch,
                                   int max_context, w4a16_model** out) {
@@ -311,7 +316,8 @@ extern "C" int w4a16_model_check_errors(w4a16_model* m, w4a16_stream_t stream) {
 // tensor-core GEMM follows with K split across CTAs.  Returns the number of
 // tags used through *tag.
 static int project(w4a16_model* m, GemvArgs g, bool silu, cudaStream_t s, int* tag) {
-  if (gemv_cuda_core_supported(g.M, g.K) && !(g.gamma && batched_path(m, g.M))) {
+  if (gemv_cuda_core_supported(g.M, g.K) && !(g.gamma && batched_path(m, g.M)) &&
+      !(silu && g.M >= SILU_TC_MIN_ROWS)) {
     g.tag = (*tag)++;
     return launch_gemv(g, silu, s);
   }
@@ -638,7 +644,9 @@ extern "C" int w4a16_prefill(w4a16_model* m, const int32_t* tokens, int T, const
 }
 
 // kernels one layer launches at batch B
-static int layer_kernel_count(const w4a16_model* m, int B) { return batched_path(m, B) ? 7 : 5; }
+static int layer_kernel_count(const w4a16_model* m, int B) {
+  return batched_path(m, B) ? 7 : (B >= SILU_TC_MIN_ROWS ? 6 : 5);
+}
 
 extern "C" int w4a16_model_layer(w4a16_model* m, int layer, uint16_t* x, const int32_t* block_table, int max_blocks,
                                  const int32_t* context_lens, int B, w4a16_stream_t stream) {
