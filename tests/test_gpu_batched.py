@@ -24,7 +24,7 @@ def _tiny_case(B, n_layers=2, vocab=3000, max_len=100, seed=5000):
     cfg = dict(synth.TINY_LAYER, n_layers=n_layers, vocab=vocab, bias=True, batch=B, seed=seed,
                codes="symmetric")
     r = synth.rng(seed + 1)
-    post = synth.batched_lens(r, B, max_len, forced=(15, 16, 17, 1))  # lengths after this step's append
+    post = synth.batched_lens(r, B, max_len, forced=(15, 16, 17, 1)[:B])  # lengths after this step's append
     return synth.model_case(cfg, lens=post - 1, gen_tokens=4, pool_pages=16 * B + 64)
 
 
@@ -76,8 +76,11 @@ def _free_running(api, case, B, steps, rows=None):
     m.close()
 
 
-@pytest.mark.parametrize("B", [5, 8, 32])
+@pytest.mark.parametrize("B", [3, 4, 5, 8, 32])
 def test_batched_decode_matches_oracle(api, B):
+    """B = 3, 4: q|k|v and o on the CUDA-core GEMVs, gate|up on the
+    tensor-core GEMM after its own RMSNorm, the fused lm_head; B > 4: the
+    batched path throughout."""
     case = _tiny_case(B, seed=5000 + B)
     _free_running(api, case, B, steps=3)
 
