@@ -348,9 +348,6 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
   const unsigned char* Vc = slot + ATT8_CODES;
   const float* ks = reinterpret_cast<const float*>(slot + 2 * ATT8_CODES);
   const float* vs = ks + ATT_PAGE;
-  float sc[2][4];
-#pragma unroll
-  for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
   // K codes: tokens g (n-block 0) and 8 + g (n-block 1), dims [16 t4, +16) and [64 + 16 t4, +16)
   uint4 kw[2][2];
 #pragma unroll
@@ -358,14 +355,31 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       kw[r][h] = *reinterpret_cast<const uint4*>(Kc + (g + 8 * r) * ATT8_PITCH + 64 * h + 16 * t4);
+  // V codes (used after the softmax, loaded now): tokens 2 t4, 2 t4 + 1, 8 + 2 t4, 9 + 2 t4,
+  // dims [16 g, +16) (dim 16 g + nb of n-block nb)
+  uint4 vw[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    vw[r] = *reinterpret_cast<const uint4*>(Vc + (2 * t4 + (r & 1) + 8 * (r >> 1)) * ATT8_PITCH + 16 * g);
+  // the 8 k steps of each n-block alternate between two accumulators
+  float sc[2][4], sd[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[nb][e] = sd[nb][e] = 0.f;
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
     uint32_t b0, b1, b2, b3;
     e4m3x4_to_h2x2((&kw[0][st >> 2].x)[st & 3], b0, b1);
     e4m3x4_to_h2x2((&kw[1][st >> 2].x)[st & 3], b2, b3);
-    mma_16816(sc[0], qa[st][0], qa[st][1], b0, b1);
-    mma_16816(sc[1], qa[st][0], qa[st][1], b2, b3);
+    float (&acc)[2][4] = (st & 1) ? sd : sc;
+    mma_16816(acc[0], qa[st][0], qa[st][1], b0, b1);
+    mma_16816(acc[1], qa[st][0], qa[st][1], b2, b3);
   }
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[nb][e] += sd[nb][e];
   float s00 = sc[0][0] * ks[2 * t4] * scale_log2, s01 = sc[0][1] * ks[2 * t4 + 1] * scale_log2;
   float s10 = sc[1][0] * ks[8 + 2 * t4] * scale_log2, s11 = sc[1][1] * ks[9 + 2 * t4] * scale_log2;
   if (2 * t4 >= nv) s00 = -INFINITY;
@@ -387,11 +401,6 @@ __device__ __forceinline__ void attn_page_fp8(const unsigned char* slot, int nv,
   const __half2 pa = __floats2half2_rn(p00 * vs[2 * t4], p01 * vs[2 * t4 + 1]);
   const __half2 pb = __floats2half2_rn(p10 * vs[8 + 2 * t4], p11 * vs[9 + 2 * t4]);
   const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&pa), a2 = *reinterpret_cast<const uint32_t*>(&pb);
-  // V codes: tokens 2 t4, 2 t4 + 1, 8 + 2 t4, 9 + 2 t4, dims [16 g, +16) (dim 16 g + nb of n-block nb)
-  uint4 vw[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-    vw[r] = *reinterpret_cast<const uint4*>(Vc + (2 * t4 + (r & 1) + 8 * (r >> 1)) * ATT8_PITCH + 16 * g);
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) {
     const uint32_t sel = (uint32_t)(nb & 3) | ((uint32_t)(4 + (nb & 3)) << 4);
