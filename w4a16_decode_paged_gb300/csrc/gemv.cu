@@ -89,11 +89,12 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, uint4* xs, 
       if (lane == 0) red[warp][m] = t;
     }
     __syncthreads();
+    // every warp adds the warps' sums in the same shuffle tree (one shared
+    // load per lane instead of nwarp dependent ones per thread)
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      float t = 0.f;
-      for (int w = 0; w < nwarp; ++w) t += red[w][m];
-      rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);  // per-thread copy
+      const float t = warp_sum(lane < nwarp ? red[lane][m] : 0.f);
+      rscale[m] = 1.0f / sqrtf(t / (float)K + a.eps);  // the same value from every thread
     }
 #pragma unroll
     for (int i = 0; i < STAGE_GMAX; ++i) {
