@@ -114,3 +114,54 @@ def test_sequence_rows_grow_one_page_per_16_tokens(lib):
     assert lib.w4a16_seq_reserve(a, other.ctypes.data, 4, 48) == 0
     assert len(set(other[:3].tolist())) == 3
     lib.w4a16_page_allocator_destroy(a)
+
+
+def test_concurrent_alloc_and_free_from_several_threads(lib):
+    """The allocator serialises its calls (one mutex per pool): threads that
+    allocate and free at the same time never receive a page another thread
+    still holds, and every page comes back at the end.  ctypes releases the
+    GIL around each call, so the calls do overlap."""
+    import threading
+
+    n_pages, n_threads, rounds = 64, 4, 400
+    a = _new(lib, n_pages)
+    held, guard, errors = set(), threading.Lock(), []
+
+    def worker(seed):
+        rng = np.random.default_rng(seed)
+        mine = []
+        for _ in range(rounds):
+            if mine and (rng.random() < 0.5 or len(mine) > 24):
+                k = int(rng.integers(1, len(mine) + 1))
+                give, mine = mine[:k], mine[k:]
+                with guard:
+                    held.difference_update(give)
+                if _free(lib, a, give) != 0:
+                    errors.append("free refused")
+            else:
+                rc, got = _alloc(lib, a, int(rng.integers(1, 6)))
+                if rc == 0:
+                    with guard:
+                        dup = held.intersection(got.tolist())
+                        if dup or len(set(got.tolist())) != got.size:
+                            errors.append(f"page handed out twice: {sorted(dup)}")
+                        held.update(got.tolist())
+                    mine += got.tolist()
+                elif rc != 8:  # W4A16_ERR_NO_PAGES is the only expected refusal
+                    errors.append(f"alloc rc {rc}")
+        with guard:
+            held.difference_update(mine)
+        if mine and _free(lib, a, mine) != 0:
+            errors.append("final free refused")
+
+    ts = [threading.Thread(target=worker, args=(100 + i,)) for i in range(n_threads)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors[:3]
+    assert not held
+    assert lib.w4a16_page_free_count(a) == n_pages
+    rc, pages = _alloc(lib, a, n_pages)
+    assert rc == 0 and sorted(pages.tolist()) == list(range(n_pages))
+    lib.w4a16_page_allocator_destroy(a)
