@@ -178,3 +178,20 @@ def test_default_partition_rule(lib):
     assert f(4, 4, 32768) == 512 and f(1, 4, 2000) == 512      # few (sequence, kv head) pairs
     assert f(32, 4, 4096) == 256 and f(16, 4, 1025) == 256     # many pairs: a warp per 256 tokens
     assert f(0, 4, 512) == 64                                  # invalid sizes: a fallback value
+
+
+def test_attention_workspace_holds_every_partial(lib):
+    """Host-side workspace size (no GPU call): room for each (sequence, q head,
+    partition) partial -- 128 fp32 output dims plus its running max and sum --
+    and it grows with the batch, the context and finer partitions."""
+    f = lib.paged_gqa_decode_workspace_size
+    for B, Hq, Hkv, L, part in ((1, 28, 4, 512, 128), (4, 28, 4, 32768, 512), (32, 28, 4, 4096, 256),
+                                (3, 8, 8, 1000, 64), (2, 28, 4, 17, 16)):
+        P = -(-L // part)
+        ws = f(B, Hq, Hkv, L, part, 128)
+        assert ws >= B * Hq * P * (128 + 2) * 4, (B, L, part)
+        assert ws % 128 == 0
+        assert f(B + 1, Hq, Hkv, L, part, 128) >= ws
+        assert f(B, Hq, Hkv, 2 * L, part, 128) >= ws
+        if part >= 32:
+            assert f(B, Hq, Hkv, L, part // 2, 128) >= ws
