@@ -383,8 +383,9 @@ def test_fused_rope_append_attention_matches_oracle(api, Hq, Hkv, part):
 
 def test_paged_gqa_decode_batch32_mixed_lengths(api):
     """32 sequences with lengths U[1, 4096] (15/16/17 among them) and the
-    library's partition choice (a warp per 256-token partition, CTAs handed
-    out longest sequence first): every output against the oracle."""
+    library's partition choice (a warp per 256-token partition, partials
+    combined by the last CTA of each sequence and kv head): every output
+    against the oracle."""
     c = synth.QWEN_BATCHED
     r = synth.rng(4242)
     lens = synth.batched_lens(r, 32, 4096, c["forced_lens"]).astype(np.int32)
