@@ -12,51 +12,90 @@
 namespace w4 {
 
 // ---------------------------------------------------------------------------
-// RMSNorm: one CTA per row.
+// RMSNorm: one CTA per row.  Rows of up to RN_THREADS * RN_HELD * 8 values
+// (8192 for the model's 3584) stay in registers between the sum of squares
+// and the scaling, so x is read once, and gamma, which does not depend on the
+// previous kernel, is loaded before the dependency wait.  Longer rows are
+// read twice.  Either way each thread sums its words in the same order.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) w4pg_rmsnorm(const __half* __restrict__ x, const __half* __restrict__ gamma,
-                                                      __half* y, int H, float eps, int tag) {
-  __shared__ float red[8];
+constexpr int RN_THREADS = 256;
+constexpr int RN_HELD = 4;  // 16-byte words of the row each thread holds
+
+__global__ void __launch_bounds__(RN_THREADS) w4pg_rmsnorm(const __half* __restrict__ x,
+                                                             const __half* __restrict__ gamma, __half* y, int H,
+                                                             float eps, int tag) {
+  __shared__ float red[RN_THREADS / 32];
   __shared__ float rs;
   W4_TRACE_SCOPE(tag);
+  const int m = blockIdx.x;
+  const int nw = H / 8;  // 16-byte words per row
+  const bool held = nw <= RN_THREADS * RN_HELD;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)m * H);
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)m * H);
+  uint4 xv[RN_HELD], gv[RN_HELD];
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < RN_HELD; ++i) {
+      const int w = threadIdx.x + i * RN_THREADS;
+      if (w < nw) gv[i] = gr[w];
+    }
+  }
   pdl_wait_then_trigger();
   W4_TRACE_WAITED();
-  const int m = blockIdx.x;
-  const __half* xr = x + (size_t)m * H;
-  float ss = 0.f;
-  for (int k = threadIdx.x * 8; k < H; k += blockDim.x * 8) {
-    uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
+  auto sumsq = [](const uint4& raw, float ss) {
     const __half* h = reinterpret_cast<const __half*>(&raw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float v = __half2float(h[i]);
       ss = fmaf(v, v, ss);
     }
+    return ss;
+  };
+  auto scaled = [](uint4 raw, const uint4& graw, float r) {
+    __half* h = reinterpret_cast<__half*>(&raw);
+    const __half* g = reinterpret_cast<const __half*>(&graw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
+    return raw;
+  };
+  float ss = 0.f;
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < RN_HELD; ++i) {
+      const int w = threadIdx.x + i * RN_THREADS;
+      if (w < nw) xv[i] = xr[w];
+    }
+#pragma unroll
+    for (int i = 0; i < RN_HELD; ++i)
+      if (threadIdx.x + i * RN_THREADS < nw) ss = sumsq(xv[i], ss);
+  } else {
+    for (int w = threadIdx.x; w < nw; w += RN_THREADS) ss = sumsq(xr[w], ss);
   }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    for (int w = 0; w < RN_THREADS / 32; ++w) t += red[w];
     rs = 1.0f / sqrtf(t / (float)H + eps);
   }
   __syncthreads();
   const float r = rs;
-  for (int k = threadIdx.x * 8; k < H; k += blockDim.x * 8) {
-    uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
-    uint4 graw = *reinterpret_cast<const uint4*>(gamma + k);
-    __half* h = reinterpret_cast<__half*>(&raw);
-    const __half* g = reinterpret_cast<const __half*>(&graw);
+  if (held) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(__half2float(h[i]) * r * __half2float(g[i]));
-    *reinterpret_cast<uint4*>(y + (size_t)m * H + k) = raw;
+    for (int i = 0; i < RN_HELD; ++i) {
+      const int w = threadIdx.x + i * RN_THREADS;
+      if (w < nw) yr[w] = scaled(xv[i], gv[i], r);
+    }
+  } else {
+    for (int w = threadIdx.x; w < nw; w += RN_THREADS) yr[w] = scaled(xr[w], gr[w], r);
   }
 }
 
 int launch_rmsnorm(const __half* x, const __half* gamma, __half* y, int M, int H, float eps, cudaStream_t s,
                    int tag) {
-  cudaError_t e = launch_pdl(w4pg_rmsnorm, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps, tag);
+  cudaError_t e = launch_pdl(w4pg_rmsnorm, dim3(M), dim3(RN_THREADS), 0, s, x, gamma, y, H, eps, tag);
   if (e != cudaSuccess) return set_error(W4A16_ERR_CUDA, "rmsnorm launch: %s", cudaGetErrorString(e));
   return W4A16_OK;
 }
