@@ -70,3 +70,33 @@ def test_index_lists_every_summary():
     index = open(os.path.join(PROF, "README.md")).read()
     for f in _summaries():
         assert f"`{f}`" in index, f
+
+
+def test_traffic_of_the_bench_line_kernels_is_current():
+    """The bench line reports `roofline.traffic` only for kernel source the
+    DRAM counters were taken on.  The committed records of the kernels the
+    line names are current, and a record whose source changed reads as None."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    for key in ("gemv_gateup", "gemm_tc_gateup_b32", "decode_persistent_b1"):
+        assert bench.traffic_record(key) is not None, key
+    assert bench.traffic_record("no_such_kernel") is None
+
+
+def test_stale_traffic_record_reads_as_none(tmp_path, monkeypatch):
+    import shutil
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    rec = json.load(open(os.path.join(PROF, "traffic.json")))["gemv_gateup"]
+    src = tmp_path / rec["source"]
+    src.parent.mkdir(parents=True)
+    shutil.copy(os.path.join(ROOT, rec["source"]), src)
+    json.dump({"gemv_gateup": rec}, open(tmp_path / "profiles" / "traffic.json", "w"))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("gemv_gateup") == rec["dram_bytes_per_launch"]
+    with open(src, "a") as f:
+        f.write("\n// edited\n")
+    assert bench.traffic_record("gemv_gateup") is None
