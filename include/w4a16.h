@@ -23,6 +23,14 @@
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *    enqueue work: none allocates, synchronises or copies through the host, so
  *    all of them may be recorded into a CUDA graph ([EN] "Bug 3").
+ *  - Kernels are launched with programmatic dependent launch.  A kernel of
+ *    this library may start while the previous kernel of this library on the
+ *    same stream is still running.  It may read its weights (packed weights,
+ *    scales, biases, RMSNorm gamma, lm_head rows) before waiting for that
+ *    kernel, and waits before it reads activations, KV pools, block tables or
+ *    lengths.  So weights must not be produced by the call of this library
+ *    immediately before on the same stream; a copy, another library's kernel
+ *    or an earlier call in between orders them as usual.
  *  - Return value: W4A16_OK or an error code; w4a16_last_error() gives the
  *    message of the last failure on the calling thread.  Shape and pointer
  *    checks happen on the host before anything is enqueued.  Conditions only
