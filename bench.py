@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--kernel", default=None,
                     choices=["gateup", "down", "qkv", "o", "attention", "lm_head", "attention_long",
-                             "attention_fp8", "prefill"],
+                             "attention_fp8", "prefill", "batching"],
                     help="time one kernel of the workload alone (per-launch JSON line)")
     ap.add_argument("--batch", type=int, default=1, help="sequences (kernel mode)")
     ap.add_argument("--clock-log", default=None,
@@ -339,6 +339,20 @@ def run_kernel(args):
         print(json.dumps(res))
         model.close()
         return 0
+    if name == "batching":
+        # the 28-layer model (the b=1 workload's weights) under continuous
+        # batching: 64 sequences through 32 batch slots
+        cfg, lens0, pool_pages, _ = workload(args)
+        inp = make_inputs(cfg, args.seed, lens0, 64, pool_pages)
+        Hkv, D = cfg["n_kv_heads"], cfg["head_dim"]
+        zeros = lambda n: (torch.zeros((n, Hkv, 16, D), dtype=torch.float16, device=dev),
+                           torch.zeros((n, Hkv, 16, D), dtype=torch.float16, device=dev))
+        res = time_batching(api, cfg, inp["layers"], tdev(inp["embed"]), tdev(inp["fnorm"]), tdev(inp["lm"]),
+                            zeros, lambda: torch.cuda.synchronize(dev), time.perf_counter)
+        res.update({"kernel": "batching", "workload": "28 layers, 64 sequences, prompts U[16,128], 64 new tokens "
+                                                      "each, 32 batch slots"})
+        print(json.dumps(res))
+        return 0
     if name in ("attention_long", "attention_fp8"):
         stream = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(stream):
@@ -601,6 +615,64 @@ def time_prefill(torch, api, model, cfg, bt, dev, stream, T=512, reps=3):
     return {"ms": ms, "prompt_tokens": T, "tok_per_s": T / (ms / 1e3), "reps": reps,
             "how": "w4a16_prefill: tensor-core GEMMs over row blocks of 128 (gate|up 64), causal paged attention, "
                    "lm_head"}
+
+
+def batching_prompts(seed, n_seq, lo=16, hi=128):
+    """Seeded prompt lengths of the continuous-batching run: uniform on [lo, hi]."""
+    r = np.random.default_rng(seed)
+    return [int(n) for n in r.integers(lo, hi + 1, size=n_seq)]
+
+
+def time_batching(api, cfg, dls, embed, fnorm, lm, new_pools, sync, clock, n_seq=64, max_batch=32,
+                  new_tokens=64, seed=4343):
+    """Continuous batching through the library's scheduler and page allocator
+    (w4a16_batcher_*): n_seq sequences with prompts of 16..128 seeded random
+    tokens and new_tokens generated tokens each, through max_batch slots.  A
+    prompt is fed one token per step, so a sequence with a p-token prompt
+    occupies its slot for p + new_tokens - 1 steps.  The pool gives every
+    slot room for its longest sequence (no preemption).  The same submissions
+    run twice; the first pass captures the step's graph for every batch size
+    it meets and is not timed.  Time is host wall clock around the step loop
+    (scheduling, uploads and the decode steps), the device synchronised on
+    both sides."""
+    plens = batching_prompts(seed, n_seq)
+    max_context = max(plens) + new_tokens
+    max_blocks = (max_context + 15) // 16
+    num_pages = max_batch * max_blocks
+    layers = [api.device_layer(w, *new_pools(num_pages)) for w in dls]
+    model = api.Model(cfg, layers, embed=embed, final_norm=fnorm, lm_head=lm, max_batch=max_batch,
+                      max_context=max_context, num_pages=num_pages)
+    bat = api.Batcher(model, num_pages=num_pages, max_batch=max_batch, max_blocks=max_blocks,
+                      max_context=max_context)
+    r = np.random.default_rng(seed + 1)
+    prompts = [r.integers(0, cfg["vocab"], size=p).astype(np.int32) for p in plens]
+    res = None
+    for timed in (False, True):
+        ids = [bat.submit(p, new_tokens) for p in prompts]
+        steps = token_steps = 0
+        sync()
+        t0 = clock()
+        while True:
+            n = bat.step()
+            if n == 0:
+                break
+            steps += 1
+            token_steps += n
+        sync()
+        sec = clock() - t0
+        gen = sum(len(bat.poll(i)[0]) for i in ids)
+        if timed:
+            st = bat.stats()
+            res = {"sequences": n_seq, "max_batch": max_batch, "new_tokens_each": new_tokens,
+                   "prompt_tokens": int(sum(plens)), "generated_tokens": gen, "steps": steps,
+                   "token_steps": token_steps, "mean_batch": token_steps / max(steps, 1), "seconds": sec,
+                   "generated_tok_per_s": gen / sec, "token_steps_per_s": token_steps / sec,
+                   "ms_per_step": sec / max(steps, 1) * 1e3, "preemptions": st["preemptions"],
+                   "free_pages_after": st["free_pages"], "num_pages": num_pages,
+                   "how": "w4a16_batcher_step loop, host wall clock, prompts fed one token per step"}
+    bat.close()
+    model.close()
+    return res
 
 
 def max_over_ranks(values, dev, world):
