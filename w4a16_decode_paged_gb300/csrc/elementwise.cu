@@ -12,9 +12,9 @@
 namespace w4 {
 
 // ---------------------------------------------------------------------------
-// RMSNorm: one CTA per row.  Rows of up to RN_THREADS * RN_HELD * 8 values
-// (8192 for the model's 3584) stay in registers between the sum of squares
-// and the scaling, so x is read once, and gamma, which does not depend on the
+// RMSNorm: one CTA per row.  Rows of up to RN_THREADS * RN_HELD * 8 = 8192
+// values (the model's hidden size is 3584) stay in registers between the sum
+// of squares and the scaling, so x is read once, and gamma, which does not depend on the
 // previous kernel, is loaded before the dependency wait.  Longer rows are
 // read twice.  Either way each thread sums its words in the same order.
 // ---------------------------------------------------------------------------
